@@ -1,0 +1,212 @@
+"""compressed_sparse_attention_kv_gb300: DeepSeek-V4-style compressed-KV decode attention on GB300.
+
+Thin Python binding over libcskv.so (include/cskv.h).  Every function here only
+marshals arguments: torch tensors provide device memory and the current CUDA
+stream; all arithmetic of the decode path runs in the library's sm_103a
+kernels.  There is no CPU fallback: calling into the library without it being
+built raises.
+
+Calls (same names as the C ABI, without the ``cskv_`` prefix):
+
+    compress(...)            gated per-channel pooling compressor -> cache rows
+    index_topk(...)          lightning-indexer scores + top-k selection
+    sparse_decode_attn(...)  shared-KV attention over window + compressed entries
+    encode_rows(...)         code rows of values into a cache format
+"""
+
+import math
+
+import numpy as np
+
+from . import _lib
+
+FMT_BF16 = 0
+FMT_FP8 = 1
+FMT_FP4 = 2
+FMT_FP8_PAGESPLIT = 3
+PAGE_ROWS = 64
+WINDOW = 128
+
+_STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error", 4: "device timeout",
+           5: "device bounds"}
+
+
+class CskvError(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        super().__init__("%s failed: %s (status %d)" % (what, _STATUS.get(status, "?"), status))
+
+
+def _check(status, what):
+    if status != 0:
+        raise CskvError(status, what)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _need(t, dtype, name, device=True):
+    import torch
+    if t is None:
+        return
+    if device and not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def row_bytes(fmt, dim):
+    return int(_lib.lib().cskv_row_bytes(fmt, dim))
+
+
+def version():
+    return int(_lib.lib().cskv_version())
+
+
+def device_status(stream=None):
+    """Synchronise the stream and return (and clear) the library's sticky device status."""
+    return int(_lib.lib().cskv_device_status(_stream(stream)))
+
+
+def set_spin_limit(cycles):
+    _lib.lib().cskv_set_spin_limit(int(cycles))
+
+
+class PagedCache:
+    """A paged cache: `pool` uint8 [num_pages, page_bytes] on the GPU and an int32
+    block table [batch, max_pages] (or None for a flat array of rows)."""
+
+    def __init__(self, pool, block_table, fmt, dim):
+        import torch
+        _need(pool, torch.uint8, "pool")
+        _need(block_table, torch.int32, "block_table")
+        self.pool = pool
+        self.block_table = block_table
+        self.fmt = int(fmt)
+        self.dim = int(dim)
+
+    @classmethod
+    def allocate(cls, num_pages, fmt, dim, block_table=None, device="cuda"):
+        import torch
+        rb = row_bytes(fmt, dim)
+        page = PAGE_ROWS * rb
+        page = (page + 15) // 16 * 16
+        pool = torch.zeros((num_pages, page), dtype=torch.uint8, device=device)
+        return cls(pool, block_table, fmt, dim)
+
+    def desc(self):
+        return _lib.Paged(self.pool.data_ptr(),
+                          None if self.block_table is None else self.block_table.data_ptr(),
+                          self.pool.shape[1], self.pool.shape[0],
+                          0 if self.block_table is None else self.block_table.shape[1],
+                          self.fmt, self.dim)
+
+
+def rope_table(positions, theta=160000.0, rope_dim=64):
+    """Host helper: float32 [n, 32, 2] (cos, sin) of positions * theta^(-2k/64), computed in fp64."""
+    pos = np.asarray(positions, dtype=np.float64)
+    k = np.arange(rope_dim // 2, dtype=np.float64)
+    ang = pos[..., None] * (theta ** (-2.0 * k / rope_dim))
+    return np.stack([np.cos(ang), np.sin(ang)], axis=-1).astype(np.float32)
+
+
+def encode_rows(src, dst, req=None, row=None, stream=None):
+    """Code rows of src (fp32 or bf16 [n, dim]) into the cache dst (rows row[i] of request req[i])."""
+    import torch
+    if src.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("src must be float32 or bfloat16")
+    _need(src, None, "src")
+    _need(req, torch.int32, "req")
+    _need(row, torch.int32, "row")
+    n, dim = src.shape
+    st = _lib.lib().cskv_encode_rows(src.data_ptr(), int(src.dtype == torch.bfloat16), n, dim,
+                                     _ptr(req), _ptr(row), dst.desc(), _stream(stream))
+    _check(st, "cskv_encode_rows")
+
+
+def compress(kv, gate, ape, ratio, overlap, out, req, first_entry, prev_kv=None, prev_gate=None,
+             norm_w=None, eps=1e-6, rope_cs=None, stream=None):
+    """Gated per-channel pooling of S sequences of T tokens (kv, gate: bf16 [S, T, coff, dim])."""
+    import torch
+    for t, n in ((kv, "kv"), (gate, "gate"), (prev_kv, "prev_kv"), (prev_gate, "prev_gate")):
+        _need(t, torch.bfloat16, n)
+    for t, n in ((ape, "ape"), (norm_w, "norm_w"), (rope_cs, "rope_cs")):
+        _need(t, torch.float32, n)
+    _need(req, torch.int32, "req")
+    _need(first_entry, torch.int32, "first_entry")
+    S, T, coff, dim = kv.shape
+    st = _lib.lib().cskv_compress(kv.data_ptr(), gate.data_ptr(), _ptr(prev_kv), _ptr(prev_gate),
+                                  ape.data_ptr(), _ptr(norm_w), float(eps), _ptr(rope_cs),
+                                  S, T, int(ratio), int(bool(overlap)), dim, req.data_ptr(),
+                                  first_entry.data_ptr(), out.desc(), _stream(stream))
+    _check(st, "cskv_compress")
+
+
+def index_topk_workspace_size(B, max_ctx_len, ratio, Hi, k):
+    return int(_lib.lib().cskv_index_topk_workspace_size(B, max_ctx_len, ratio, Hi, k))
+
+
+def index_topk(q_idx, w, keys, ctx_len, ratio, k, max_ctx_len, topk_idx=None, topk_score=None,
+               workspace=None, want_scores=True, stream=None):
+    """Lightning-indexer top-k; returns (topk_idx int32 [B, k], topk_score fp32 [B, k] or None)."""
+    import torch
+    _need(q_idx, torch.bfloat16, "q_idx")
+    _need(w, torch.float32, "w")
+    _need(ctx_len, torch.int32, "ctx_len")
+    B, Hi, _ = q_idx.shape
+    dev = q_idx.device
+    if topk_idx is None:
+        topk_idx = torch.empty((B, k), dtype=torch.int32, device=dev)
+    if topk_score is None and want_scores:
+        topk_score = torch.empty((B, k), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(index_topk_workspace_size(B, max_ctx_len, ratio, Hi, k),
+                                dtype=torch.uint8, device=dev)
+    st = _lib.lib().cskv_index_topk(q_idx.data_ptr(), w.data_ptr(), keys.desc(), ctx_len.data_ptr(),
+                                    B, Hi, int(ratio), int(k), int(max_ctx_len), topk_idx.data_ptr(),
+                                    _ptr(topk_score), workspace.data_ptr(), workspace.numel(),
+                                    _stream(stream))
+    _check(st, "cskv_index_topk")
+    return topk_idx, topk_score
+
+
+def sparse_decode_attn_workspace_size(B, H, max_ctx_len, ratio, k):
+    return int(_lib.lib().cskv_sparse_decode_attn_workspace_size(B, H, max_ctx_len, ratio, k))
+
+
+def sparse_decode_attn(q, main_kv, swa, swa_fmt, ctx_len, topk_idx, k, ratio, max_ctx_len, sink,
+                       softmax_scale, q_rope_cs, out=None, workspace=None, stream=None):
+    """Shared-KV decode attention; returns out bf16 [B, H, 512]."""
+    import torch
+    _need(q, torch.bfloat16, "q")
+    _need(swa, torch.uint8, "swa")
+    _need(ctx_len, torch.int32, "ctx_len")
+    _need(topk_idx, torch.int32, "topk_idx")
+    _need(sink, torch.float32, "sink")
+    _need(q_rope_cs, torch.float32, "q_rope_cs")
+    B, H, _ = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    kk = int(k) if topk_idx is not None else 0
+    if workspace is None:
+        workspace = torch.empty(sparse_decode_attn_workspace_size(B, H, max_ctx_len, ratio, kk),
+                                dtype=torch.uint8, device=q.device)
+    st = _lib.lib().cskv_sparse_decode_attn(q.data_ptr(), main_kv.desc(), swa.data_ptr(), int(swa_fmt),
+                                            ctx_len.data_ptr(), _ptr(topk_idx), kk, int(ratio),
+                                            int(max_ctx_len), _ptr(sink), float(softmax_scale),
+                                            q_rope_cs.data_ptr(), B, H, out.data_ptr(),
+                                            workspace.data_ptr(), workspace.numel(), _stream(stream))
+    _check(st, "cskv_sparse_decode_attn")
+    return out
+
+
+DEFAULT_SCALE = 1.0 / math.sqrt(512.0)

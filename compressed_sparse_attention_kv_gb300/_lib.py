@@ -1,0 +1,68 @@
+"""ctypes view of libcskv.so (the C ABI declared in include/cskv.h)."""
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libcskv.so")
+
+c_int32 = ctypes.c_int32
+c_int64 = ctypes.c_int64
+c_size_t = ctypes.c_size_t
+c_void_p = ctypes.c_void_p
+c_float = ctypes.c_float
+
+
+class Paged(ctypes.Structure):
+    """struct cskv_paged."""
+    _fields_ = [
+        ("pool", c_void_p),
+        ("block_table", c_void_p),
+        ("page_bytes", c_int64),
+        ("num_pages", c_int32),
+        ("max_pages", c_int32),
+        ("fmt", c_int32),
+        ("dim", c_int32),
+    ]
+
+
+# name -> (restype, argtypes); every symbol include/cskv.h declares
+SIGNATURES = {
+    "cskv_row_bytes": (c_size_t, [c_int32, c_int32]),
+    "cskv_status_string": (ctypes.c_char_p, [c_int32]),
+    "cskv_version": (c_int32, []),
+    "cskv_device_status": (c_int32, [c_void_p]),
+    "cskv_set_spin_limit": (None, [ctypes.c_uint64]),
+    "cskv_encode_rows": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, Paged,
+                                   c_void_p]),
+    "cskv_compress": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_float,
+                                c_void_p, c_int32, c_int32, c_int32, c_int32, c_int32, c_void_p,
+                                c_void_p, Paged, c_void_p]),
+    "cskv_index_topk_workspace_size": (c_size_t, [c_int32, c_int32, c_int32, c_int32, c_int32]),
+    "cskv_index_topk": (c_int32, [c_void_p, c_void_p, Paged, c_void_p, c_int32, c_int32, c_int32,
+                                  c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "cskv_sparse_decode_attn_workspace_size": (c_size_t, [c_int32, c_int32, c_int32, c_int32, c_int32]),
+    "cskv_sparse_decode_attn": (c_int32, [c_void_p, Paged, c_void_p, c_int32, c_void_p, c_void_p,
+                                          c_int32, c_int32, c_int32, c_void_p, c_float, c_void_p,
+                                          c_int32, c_int32, c_void_p, c_void_p, c_size_t, c_void_p]),
+}
+
+_lib = None
+
+
+def lib():
+    """The loaded library; raises if libcskv.so has not been built (no fallback exists)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                "libcskv.so is missing at %s: build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'` "
+                "(there is no CPU fallback for the decode path)" % LIB_PATH)
+        h = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(h, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = h
+    return _lib

@@ -1,0 +1,460 @@
+// Shared-KV sparse decode attention (cskv_sparse_decode_attn).
+//
+// "DeepSeek-V4 deep dive": section 3.1 (one 512-d entry is key and value of
+// every head), section 3.3 (query rotated by its position, output rotated back),
+// section 3.4 Eq. 27 (one softmax over window + compressed keys with a per-head
+// sink in the denominator), section 5.3 (index list = window slots, then the
+// selected entries; -1 skipped; duplicates kept) and section 6.1 (HCA reads
+// every visible entry).
+//
+// GB300 design.  A request's key list is cut into 128-key tiles: tile 0 is the
+// 128-slot window ring, tiles 1.. are 128 consecutive list entries.  One block
+// handles one (request, tile, head group of <= 64 heads):
+//   * 8 warps gather the tile's rows (528 B FP8, 288 B FP4 or 1 KiB bf16; the
+//     row addresses come from the block table), dequantise them exactly into
+//     bf16 and store a 128 x 512 K-major tile with 128-byte swizzle;
+//   * the query is rotated (fp32) and stored as bf16 in the same layout;
+//   * one thread issues tcgen05 MMAs S^T = K Q^T (M = 128 keys, N = heads,
+//     K = 512) into TMEM - keys are the MMA rows, so 16..64 heads need no padding;
+//   * softmax statistics per head (max, sum of exp2) over the tile, P^T stored
+//     as the bf16 MN-major B operand;
+//   * O^T = V^T P^T (M = 128 dims x 4 blocks, N = heads, K = 128 keys): the same
+//     smem tile is read a second time as the MN-major A operand (K = V);
+//   * the partial (m, l, O) goes to the workspace.
+// attn_combine_kernel merges the partials of a request in a fixed order with
+// the sink, applies the inverse rotation and writes bf16.
+#include "codec.cuh"
+#include "internal.h"
+
+namespace cskv {
+
+namespace {
+
+constexpr int kD = 512;
+constexpr int kKeys = 128;
+constexpr int kAttnThreads = 256;
+constexpr int kMaxHeadsPerBlock = 64;
+constexpr int kZStride = kKeys + 1;   // fp32 logits, transposed [head][key], padded
+
+__host__ __device__ inline size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct AttnLayout {
+  size_t opart, ml, total;
+  int max_tiles;
+};
+
+__host__ __device__ inline AttnLayout attn_layout(int B, int H, int max_ctx, int ratio, int k) {
+  AttnLayout L;
+  const int comp = k > 0 ? k : (ratio > 0 ? max_ctx / ratio : 0);
+  L.max_tiles = 1 + (comp + kKeys - 1) / kKeys;
+  size_t o = 0;
+  L.opart = o; o = a256(o + size_t(B) * L.max_tiles * H * kD * 4);
+  L.ml = o;    o = a256(o + size_t(B) * L.max_tiles * H * 2 * 4);
+  L.total = o;
+  return L;
+}
+
+struct AttnArgs {
+  const uint8_t* q;
+  cskv_paged kv;
+  int kv_row_bytes;
+  const uint8_t* swa;
+  int swa_fmt, swa_row_bytes;
+  const int32_t* ctx_len;
+  const int32_t* topk;
+  int k, ratio, max_ctx;
+  const float* sink;
+  float scale_log2;       // softmax_scale * log2(e)
+  const float* q_rope;
+  int B, H;
+  uint8_t* out;
+  float* opart;
+  float* ml;
+  int max_tiles;
+};
+
+__device__ __forceinline__ int query_len(const AttnArgs& a, int b) {
+  int c = a.ctx_len[b];
+  if (c < 1 || c > a.max_ctx) {
+    set_err(CSKV_ERR_BOUNDS);
+    c = max(1, min(c, a.max_ctx));
+  }
+  return c;
+}
+
+// number of compressed keys in the list of request b
+__device__ __forceinline__ int comp_keys(const AttnArgs& a, int ctx) {
+  return a.topk ? a.k : ctx / a.ratio;
+}
+
+// 16 dequantised values -> 32 bytes of bf16 at dst (two 16-byte chunks)
+__device__ __forceinline__ void put16(uint8_t* tile, int row, int l, const float (&v)[16]) {
+  // dims 16l .. 16l+15 -> chunk l/4 of the K tile, 16-byte chunks 2(l%4), 2(l%4)+1
+  uint8_t* base = tile + (l >> 2) * (kKeys * 128);
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    w[i] = *reinterpret_cast<uint32_t*>(&h);
+  }
+  const int c0 = (l & 3) * 2;
+  *reinterpret_cast<uint4*>(base + sw128_offset(row, c0)) = make_uint4(w[0], w[1], w[2], w[3]);
+  *reinterpret_cast<uint4*>(base + sw128_offset(row, c0 + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+__device__ __forceinline__ void dequant16(int fmt, const uint8_t* row, int l, float (&v)[16]) {
+  if (fmt == CSKV_FMT_FP8_E4M3_E8M0_B32) {
+    const uint4 c = *reinterpret_cast<const uint4*>(row + 16 * l);
+    const float s = exp2i(static_cast<int>(row[kD + (l >> 1)]) - 127);
+    const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t h0, h1;
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h0) : "h"(static_cast<uint16_t>(cw[i] & 0xFFFF)));
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h1) : "h"(static_cast<uint16_t>(cw[i] >> 16)));
+      v[4 * i + 0] = __fmul_rn(__half2float(__ushort_as_half(h0 & 0xFFFF)), s);
+      v[4 * i + 1] = __fmul_rn(__half2float(__ushort_as_half(h0 >> 16)), s);
+      v[4 * i + 2] = __fmul_rn(__half2float(__ushort_as_half(h1 & 0xFFFF)), s);
+      v[4 * i + 3] = __fmul_rn(__half2float(__ushort_as_half(h1 >> 16)), s);
+    }
+  } else if (fmt == CSKV_FMT_FP4_E2M1_E4M3_B16) {
+    const uint2 c = *reinterpret_cast<const uint2*>(row + 8 * l);
+    const float s = e4m3_to_f32(row[kD / 2 + l]);
+    const uint32_t cw[2] = {c.x, c.y};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t h;
+        asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+            : "=r"(h)
+            : "r"((cw[i] >> (8 * j)) & 0xFF));
+        v[8 * i + 2 * j + 0] = __fmul_rn(__half2float(__ushort_as_half(h & 0xFFFF)), s);
+        v[8 * i + 2 * j + 1] = __fmul_rn(__half2float(__ushort_as_half(h >> 16)), s);
+      }
+    }
+  } else {
+    const uint4 c0 = *reinterpret_cast<const uint4*>(row + 32 * l);
+    const uint4 c1 = *reinterpret_cast<const uint4*>(row + 32 * l + 16);
+    const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[2 * i] = bf16lo(cw[i]);
+      v[2 * i + 1] = bf16hi(cw[i]);
+    }
+  }
+}
+
+struct AttnSmem {
+  uint64_t bar_s, bar_o;
+  uint32_t tmem_base;
+  float m[kMaxHeadsPerBlock];
+  float l[kMaxHeadsPerBlock];
+  int valid[kKeys];
+};
+
+__global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ktile = base;                                   // 8 chunks x 128 rows x 128 B = 128 KiB
+  uint8_t* qtile = ktile + 8 * kKeys * 128;                // 8 chunks x Nq rows x 128 B <= 64 KiB
+  float* zt = reinterpret_cast<float*>(qtile);             // reused after S: [Nq][kZStride]
+  uint8_t* ptile = qtile + 40960;                          // reused after S: 128 keys x 128 B (1024-aligned)
+  AttnSmem* sm = reinterpret_cast<AttnSmem*>(qtile + 8 * kMaxHeadsPerBlock * 128);
+
+  const int b = blockIdx.y;
+  const int tile = blockIdx.x;
+  const int h0 = blockIdx.z * kMaxHeadsPerBlock;
+  const int Hb = min(kMaxHeadsPerBlock, a.H - h0);
+  const int Nq = (Hb + 15) / 16 * 16;
+  const int ctx = query_len(a, b);
+  const int t = ctx - 1;
+  const int ncomp = comp_keys(a, ctx);
+  const int ntiles = 1 + (ncomp + kKeys - 1) / kKeys;
+  if (tile >= ntiles) return;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(&sm->bar_s, 1);
+    mbar_init(&sm->bar_o, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(&sm->tmem_base, 512);
+
+  // ---- rows of this tile: validity and address
+  for (int r = threadIdx.x; r < kKeys; r += blockDim.x) {
+    int v = 0;
+    if (tile == 0) {
+      v = (t >= kKeys - 1) || (r <= t);
+    } else {
+      const int li = (tile - 1) * kKeys + r;
+      if (li < ncomp) {
+        int e = a.topk ? a.topk[size_t(b) * a.k + li] : li;
+        if (e >= 0) {
+          if (e < ctx / a.ratio) v = 1;
+          else set_err(CSKV_ERR_BOUNDS);
+        }
+      }
+    }
+    sm->valid[r] = v;
+  }
+
+  // ---- query: rotate the last 64 dims by the query position, store bf16 (K-major, swizzled)
+  {
+    const float* cs = a.q_rope + size_t(b) * 64;
+    for (int idx = threadIdx.x; idx < Nq * 64; idx += blockDim.x) {
+      const int h = idx >> 6, g8 = idx & 63;          // 8 consecutive dims per item
+      const int d0 = g8 * 8;
+      uint4 outw = make_uint4(0u, 0u, 0u, 0u);
+      if (h < Hb) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(a.q + ((size_t(b) * a.H + h0 + h) * kD + d0) * 2);
+        float v[8] = {bf16lo(raw.x), bf16hi(raw.x), bf16lo(raw.y), bf16hi(raw.y),
+                      bf16lo(raw.z), bf16hi(raw.z), bf16lo(raw.w), bf16hi(raw.w)};
+        if (d0 >= kD - 64) {
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {
+            const int kk = (d0 - (kD - 64)) / 2 + p;
+            const float c = cs[2 * kk], s = cs[2 * kk + 1];
+            const float y0 = v[2 * p], y1 = v[2 * p + 1];
+            v[2 * p] = y0 * c - y1 * s;
+            v[2 * p + 1] = y0 * s + y1 * c;
+          }
+        }
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          __nv_bfloat162 hh = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+          w[i] = *reinterpret_cast<uint32_t*>(&hh);
+        }
+        outw = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      // dims d0..d0+7 -> chunk d0/64, 16-byte chunk (d0%64)/8
+      *reinterpret_cast<uint4*>(qtile + (d0 >> 6) * (Nq * 128) + sw128_offset(h, (d0 & 63) >> 3)) = outw;
+    }
+  }
+  __syncthreads();
+
+  // ---- gather + dequantise the 128 key rows (warp per row, lane = 16 dims)
+  {
+    const int fmt_c = a.kv.fmt;
+    for (int r = warp; r < kKeys; r += kAttnThreads / 32) {
+      float v[16];
+      const uint8_t* row = nullptr;
+      int fmt = fmt_c;
+      if (sm->valid[r]) {
+        if (tile == 0) {
+          row = a.swa + (size_t(b) * kWindow + r) * a.swa_row_bytes;
+          fmt = a.swa_fmt;
+        } else {
+          const int li = (tile - 1) * kKeys + r;
+          const int e = a.topk ? a.topk[size_t(b) * a.k + li] : li;
+          const RowPtr rp = paged_row(a.kv, b, e, a.kv_row_bytes);
+          row = rp.data;
+        }
+      }
+      if (row != nullptr) {
+        dequant16(fmt, row, lane, v);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = 0.f;
+        if (lane == 0 && sm->valid[r]) sm->valid[r] = 0;
+      }
+      put16(ktile, r, lane, v);
+    }
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm->tmem_base;
+
+  // ---- S^T = K Q^T : M = 128 keys, N = Nq, K = 512
+  if (threadIdx.x == 0) {
+    const uint32_t id = make_idesc(1, 1, 0, 0, 128, 0) | (static_cast<uint32_t>(Nq >> 3) << 17);
+    const uint32_t ka = smem_u32(ktile), qa = smem_u32(qtile);
+#pragma unroll
+    for (int kk = 0; kk < 32; ++kk) {
+      const int c = kk >> 2, o = (kk & 3) * 32;
+      mma_f16(tmem, smem_desc_sw128(ka + c * (kKeys * 128) + o, 16, 1024),
+              smem_desc_sw128(qa + c * (Nq * 128) + o, 16, 1024), id, kk > 0);
+    }
+    mma_commit(&sm->bar_s);
+  }
+  mbar_wait(&sm->bar_s, 0, kDefaultSpinLimit);
+  tc_fence_after();
+
+  // ---- logits to smem, transposed [head][key]
+  if (warp < 4) {
+    const int r = warp * 32 + lane;
+    const bool ok = sm->valid[r] != 0;
+    for (int c0 = 0; c0 < Nq; c0 += 16) {
+      float s[16];
+      tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0, s);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 16; ++i) zt[(c0 + i) * kZStride + r] = ok ? s[i] * a.scale_log2 : -INFINITY;
+    }
+  }
+  __syncthreads();
+
+  // ---- per head: max, exp2, sum; P^T stored as the MN-major B operand [key][head]
+  for (int h = warp; h < Nq; h += kAttnThreads / 32) {
+    float z[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) z[i] = zt[h * kZStride + lane + 32 * i];
+    float m = fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    float p[4], l = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      p[i] = (m == -INFINITY || h >= Hb) ? 0.f : exp2f(z[i] - m);
+      l += p[i];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, o);
+    if (lane == 0) { sm->m[h] = m; sm->l[h] = l; }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int key = lane + 32 * i;
+      const __nv_bfloat16 pb = __float2bfloat16_rn(p[i]);
+      *reinterpret_cast<__nv_bfloat16*>(ptile + sw128_offset(key, h >> 3) + (h & 7) * 2) = pb;
+    }
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  // ---- O^T = V^T P^T : 4 blocks of 128 dims, N = Nq, K = 128 keys; both operands MN-major
+  if (threadIdx.x == 0) {
+    const uint32_t id = make_idesc(1, 1, 1, 1, 128, 0) | (static_cast<uint32_t>(Nq >> 3) << 17);
+    const uint32_t ka = smem_u32(ktile), pa = smem_u32(ptile);
+#pragma unroll
+    for (int mb = 0; mb < 4; ++mb) {
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        mma_f16(tmem + 128 + mb * Nq,
+                smem_desc_sw128(ka + 2 * mb * (kKeys * 128) + ks * 2048, kKeys * 128, 1024),
+                smem_desc_sw128(pa + ks * 2048, kKeys * 128, 1024), id, ks > 0);
+      }
+    }
+    mma_commit(&sm->bar_o);
+  }
+  mbar_wait(&sm->bar_o, 0, kDefaultSpinLimit);
+  tc_fence_after();
+
+  // ---- partial out: O^T lanes = dims; warps 0-3 blocks 0,1; warps 4-7 blocks 2,3
+  {
+    const size_t slot = (size_t(b) * a.max_tiles + tile) * a.H + h0;
+    const int sub = warp & 3;
+    for (int mb = (warp >> 2) * 2; mb < (warp >> 2) * 2 + 2; ++mb) {
+      const int d = mb * 128 + sub * 32 + lane;
+      for (int c0 = 0; c0 < Nq; c0 += 16) {
+        float o[16];
+        tmem_ld16(tmem + (static_cast<uint32_t>(sub * 32) << 16) + 128 + mb * Nq + c0, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          if (c0 + i < Hb) a.opart[(slot + c0 + i) * kD + d] = o[i];
+        }
+      }
+    }
+    if (threadIdx.x < Hb) {
+      a.ml[(slot + threadIdx.x) * 2 + 0] = sm->m[threadIdx.x];
+      a.ml[(slot + threadIdx.x) * 2 + 1] = sm->l[threadIdx.x];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// merge the tiles of (request, head) in tile order, sink, inverse RoPE, bf16
+__global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
+  const int b = blockIdx.x, h = blockIdx.y;
+  const int ctx = query_len(a, b);
+  const int ncomp = comp_keys(a, ctx);
+  const int ntiles = 1 + (ncomp + kKeys - 1) / kKeys;
+  const size_t slot0 = size_t(b) * a.max_tiles * a.H + h;
+  float M = a.sink ? a.sink[h] * 1.4426950408889634f : -INFINITY;
+  for (int s = 0; s < ntiles; ++s) M = fmaxf(M, a.ml[(slot0 + size_t(s) * a.H) * 2]);
+  float L = (a.sink && M != -INFINITY) ? exp2f(a.sink[h] * 1.4426950408889634f - M) : 0.f;
+  const int d = 2 * threadIdx.x;
+  float o0 = 0.f, o1 = 0.f;
+  for (int s = 0; s < ntiles; ++s) {
+    const size_t sl = slot0 + size_t(s) * a.H;
+    const float m = a.ml[sl * 2];
+    if (m == -INFINITY) continue;
+    const float f = exp2f(m - M);
+    L += f * a.ml[sl * 2 + 1];
+    const float2 v = *reinterpret_cast<const float2*>(a.opart + sl * kD + d);
+    o0 += f * v.x;
+    o1 += f * v.y;
+  }
+  const float inv = L > 0.f ? 1.0f / L : 0.f;
+  o0 *= inv;
+  o1 *= inv;
+  if (d >= kD - 64) {
+    const int kk = (d - (kD - 64)) / 2;
+    const float c = a.q_rope[size_t(b) * 64 + 2 * kk], s = a.q_rope[size_t(b) * 64 + 2 * kk + 1];
+    const float y0 = o0, y1 = o1;
+    o0 = y0 * c + y1 * s;
+    o1 = -y0 * s + y1 * c;
+  }
+  __nv_bfloat162 r = __floats2bfloat162_rn(o0, o1);
+  *reinterpret_cast<__nv_bfloat162*>(a.out + ((size_t(b) * a.H + h) * kD + d) * 2) = r;
+}
+
+// 16 KiB of slack keeps every descriptor-addressed read inside the allocation
+size_t attn_smem_bytes() { return 1024 + 8 * kKeys * 128 + 8 * kMaxHeadsPerBlock * 128 + sizeof(AttnSmem) + 16384; }
+
+}  // namespace
+
+size_t attn_workspace_bytes(int B, int H, int max_ctx, int ratio, int k) {
+  return attn_layout(B, H, max_ctx, ratio, k).total;
+}
+
+cudaError_t launch_sparse_decode_attn(const void* q, const cskv_paged& kv, const void* swa, int swa_fmt,
+                                      const int32_t* ctx_len, const int32_t* topk, int k, int ratio,
+                                      int max_ctx, const float* sink, float softmax_scale,
+                                      const float* q_rope, int B, int H, void* out, void* workspace,
+                                      cudaStream_t stream) {
+  const AttnLayout L = attn_layout(B, H, max_ctx, ratio, topk ? k : 0);
+  AttnArgs a;
+  a.q = static_cast<const uint8_t*>(q);
+  a.kv = kv;
+  a.kv_row_bytes = static_cast<int>(cskv_row_bytes(kv.fmt, kv.dim));
+  a.swa = static_cast<const uint8_t*>(swa);
+  a.swa_fmt = swa_fmt;
+  a.swa_row_bytes = static_cast<int>(cskv_row_bytes(swa_fmt, kD));
+  a.ctx_len = ctx_len;
+  a.topk = topk;
+  a.k = k;
+  a.ratio = ratio;
+  a.max_ctx = max_ctx;
+  a.sink = sink;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  a.q_rope = q_rope;
+  a.B = B;
+  a.H = H;
+  a.out = static_cast<uint8_t*>(out);
+  a.opart = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + L.opart);
+  a.ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + L.ml);
+  a.max_tiles = L.max_tiles;
+  const size_t smem = attn_smem_bytes();
+  cudaFuncSetAttribute(attn_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  dim3 grid(L.max_tiles, B, (H + kMaxHeadsPerBlock - 1) / kMaxHeadsPerBlock);
+  attn_tile_kernel<<<grid, kAttnThreads, smem, stream>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  attn_combine_kernel<<<dim3(B, H), 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+unsigned int take_err_attention() { return take_dev_err(); }
+
+}  // namespace cskv

@@ -1,0 +1,113 @@
+// Device codecs of the cache formats and the row writer shared by the
+// compressor and cskv_encode_rows.
+//
+// FP8 rows ("DeepSeek-V4-Flash" model record, engine kernel constraint (2)):
+// e4m3 codes over all dims, one e8m0 scale per 32 values.  FP4 rows
+// ("DeepSeek-V4.1-Flash" diagram, "The four compression axes"): e2m1 codes, one
+// e4m3 scale per 16 channels.  Block rules (fixed here, as the pages give none):
+//  - e8m0: the smallest 2^e with amax <= 448 * 2^e, e in [-127, 127]; an
+//    all-zero block stores 127; values are RNE(x * 2^-e) saturated to +-448;
+//  - FP4: s = RNE_e4m3(amax / 6); s == 0 zeroes the block; nibbles are
+//    RNE_e2m1(x / s) saturated to +-6; channel 2i in the low nibble.
+// The sign of an input that rounds to zero is kept (IEEE conversion rule).
+#pragma once
+
+#include "common.cuh"
+
+namespace cskv {
+
+// Smallest e with amax <= 448 * 2^e, from the bits of amax (amax >= 0, finite).
+__device__ __forceinline__ int e8m0_exponent(float amax) {
+  if (amax == 0.f) return 0;
+  const uint32_t bits = __float_as_uint(amax);
+  const int biased = static_cast<int>(bits >> 23);
+  const uint32_t mant = bits & 0x7FFFFFu;
+  // amax = 1.mant * 2^(biased-127) and 448 = 1.75 * 2^8; 1.75 is mantissa 0x600000
+  int e = (mant <= 0x600000u) ? biased - 135 : biased - 134;
+  if (biased == 0) e = -127;
+  return max(-127, min(127, e));
+}
+
+// 2^e as fp32 for e in [-149, 127] (exact; subnormal below -126).
+__device__ __forceinline__ float exp2i(int e) {
+  return e >= -126 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23)
+                   : __uint_as_float(1u << (e + 149));
+}
+
+// Two fp32 -> two e4m3 codes, RNE with saturation; `lo` lands in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two fp32 -> two e2m1 nibbles, RNE with saturation; `lo` lands in the low nibble.
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+  uint16_t r;
+  asm("{\n\t.reg .b8 t;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+      "cvt.u16.u8 %0, t;\n\t}"
+      : "=h"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+
+// e4m3 code -> fp32 (exact, through the f16x2 conversion).
+__device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(code & 0xFF)));
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFF)));
+}
+
+// Writes one row whose values are spread over the threads of a group: thread
+// `lt` holds channels 4*lt .. 4*lt+3 in y.  The groups of 8 (FP8) or 4 (FP4)
+// threads that share a scale block must be consecutive lanes of one warp and
+// every thread of the group must call this (it shuffles).  `valid` false
+// skips the stores (the shuffles still run).
+__device__ __forceinline__ void store_row_values(const float4& y, int lt, int fmt, int dim,
+                                                 RowPtr dst, bool valid) {
+  const unsigned full = 0xFFFFFFFFu;
+  if (fmt == CSKV_FMT_BF16) {
+    if (valid) {
+      __nv_bfloat162 a = __floats2bfloat162_rn(y.x, y.y);
+      __nv_bfloat162 b = __floats2bfloat162_rn(y.z, y.w);
+      uint2 u;
+      u.x = *reinterpret_cast<uint32_t*>(&a);
+      u.y = *reinterpret_cast<uint32_t*>(&b);
+      *reinterpret_cast<uint2*>(dst.data + 8 * lt) = u;
+    }
+    return;
+  }
+  float amax = fmaxf(fmaxf(fabsf(y.x), fabsf(y.y)), fmaxf(fabsf(y.z), fabsf(y.w)));
+  if (fmt == CSKV_FMT_FP4_E2M1_E4M3_B16) {
+    amax = fmaxf(amax, __shfl_xor_sync(full, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(full, amax, 2));
+    const uint32_t scode = e4m3x2(__fdiv_rn(amax, 6.0f), 0.f) & 0xFF;
+    const float s = e4m3_to_f32(scode);
+    uint32_t packed = 0;
+    if (s > 0.f) {
+      packed = e2m1x2(__fdiv_rn(y.x, s), __fdiv_rn(y.y, s)) |
+               (e2m1x2(__fdiv_rn(y.z, s), __fdiv_rn(y.w, s)) << 8);
+    }
+    if (valid) {
+      *reinterpret_cast<uint16_t*>(dst.data + 2 * lt) = static_cast<uint16_t>(packed);
+      if ((lt & 3) == 0) dst.scale[lt >> 2] = static_cast<uint8_t>(scode);
+    }
+    return;
+  }
+  // FP8 (inline or page-split): blocks of 32 channels = 8 threads
+  amax = fmaxf(amax, __shfl_xor_sync(full, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(full, amax, 2));
+  amax = fmaxf(amax, __shfl_xor_sync(full, amax, 4));
+  const int e = e8m0_exponent(amax);
+  const float inv = exp2i(-e);
+  const uint32_t codes = e4m3x2(__fmul_rn(y.x, inv), __fmul_rn(y.y, inv)) |
+                         (e4m3x2(__fmul_rn(y.z, inv), __fmul_rn(y.w, inv)) << 16);
+  if (valid) {
+    *reinterpret_cast<uint32_t*>(dst.data + 4 * lt) = codes;
+    if ((lt & 7) == 0) dst.scale[lt >> 3] = static_cast<uint8_t>(e + 127);
+  }
+  (void)dim;
+}
+
+}  // namespace cskv

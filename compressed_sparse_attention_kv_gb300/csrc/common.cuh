@@ -1,0 +1,243 @@
+// Shared device helpers of libcskv: the per-translation-unit error word, bf16
+// loads, and thin inline-PTX wrappers for mbarriers, bulk/TMA copies and the
+// tcgen05 tensor-core instructions of sm_103a.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "../../include/cskv.h"
+
+namespace cskv {
+
+// ---------------------------------------------------------------------------
+// sticky device error word (one per translation unit; cskv_device_status ORs them)
+// ---------------------------------------------------------------------------
+static __device__ unsigned int g_dev_err;
+
+__device__ __forceinline__ void set_err(int status) { atomicOr(&g_dev_err, 1u << status); }
+
+// Host side: read and clear this translation unit's word (synchronous).
+static inline unsigned int take_dev_err() {
+  unsigned int v = 0, z = 0;
+  cudaMemcpyFromSymbol(&v, g_dev_err, sizeof(v));
+  cudaMemcpyToSymbol(g_dev_err, &z, sizeof(z));
+  return v;
+}
+
+constexpr int kPageRows = 64;
+constexpr int kWindow = 128;
+
+// ---------------------------------------------------------------------------
+// small numeric helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// Four bf16 values (8 bytes) -> four floats (exact).
+__device__ __forceinline__ float4 load_bf16x4(const void* p) {
+  uint2 u = *reinterpret_cast<const uint2*>(p);
+  return make_float4(bf16lo(u.x), bf16hi(u.x), bf16lo(u.y), bf16hi(u.y));
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------------------
+// paged row addressing
+// ---------------------------------------------------------------------------
+struct RowPtr {
+  uint8_t* data;   // first byte of the row's values (nullptr: out of bounds)
+  uint8_t* scale;  // first scale byte of the row (formats with scales)
+};
+
+// Address of row `row` of request `req` in a paged cache; nullptr (and a sticky
+// error) when the row is outside the request's table or the page outside the pool.
+__device__ __forceinline__ RowPtr paged_row(const cskv_paged& c, int req, long long row,
+                                            int row_bytes) {
+  RowPtr r{nullptr, nullptr};
+  long long lp = row / kPageRows;
+  int slot = static_cast<int>(row % kPageRows);
+  long long pp = lp;
+  if (c.block_table != nullptr) {
+    if (lp >= c.max_pages || row < 0) { set_err(CSKV_ERR_BOUNDS); return r; }
+    pp = c.block_table[static_cast<long long>(req) * c.max_pages + lp];
+  }
+  if (pp < 0 || pp >= c.num_pages) { set_err(CSKV_ERR_BOUNDS); return r; }
+  uint8_t* page = static_cast<uint8_t*>(c.pool) + pp * c.page_bytes;
+  if (c.fmt == CSKV_FMT_FP8_E4M3_E8M0_B32_PAGESPLIT) {
+    r.data = page + static_cast<long long>(slot) * c.dim;
+    r.scale = page + static_cast<long long>(kPageRows) * c.dim + slot * (c.dim / 32);
+  } else {
+    r.data = page + static_cast<long long>(slot) * row_bytes;
+    r.scale = r.data + (c.fmt == CSKV_FMT_FP8_E4M3_E8M0_B32 ? c.dim
+                        : c.fmt == CSKV_FMT_FP4_E2M1_E4M3_B16 ? c.dim / 2 : 0);
+  }
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier (shared::cta) with bounded waits
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Waits for the phase with the given parity to complete, at most `limit` clock
+// cycles.  Returns false (and sets CSKV_ERR_TIMEOUT) if the limit ran out.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned long long limit) {
+  if (mbar_try_wait(bar, parity)) return true;
+  unsigned long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > limit) { set_err(CSKV_ERR_TIMEOUT); return false; }
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------------------
+// bulk and tensor copies global -> shared (complete_tx on an mbarrier)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int c0, int c1, int c2,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_tmap(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05: tensor memory, MMA, commit, loads
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16/f16 inputs, fp32 accumulate)
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// kind::f8f6f4 (e4m3/e5m2/... inputs, fp32 accumulate)
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on `bar` once all previously issued MMAs of this thread have completed.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// 32 lanes x 32 bit, 16 consecutive columns: thread i of the warp gets lane
+// (warp's sub-partition base + i), columns col .. col+15.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
+      "[%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor (tcgen05), swizzle-128B layouts.
+//   start address >> 4 in bits 0-13, leading byte offset >> 4 in 16-29,
+//   stride byte offset >> 4 in 32-45, descriptor version 1 in bits 46-47,
+//   layout type in bits 61-63 (2 = 128-byte swizzle).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFF);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFF) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFF) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// Instruction descriptor, dense MMA with fp32 accumulator.
+//   bits 4-5 accumulator format (1 = f32), 7-9 A type, 10-12 B type,
+//   15 A major (0 K-major, 1 MN-major), 16 B major, 17-22 N>>3, 24-28 M>>4.
+// Types: kind::f16 -> 0 f16, 1 bf16; kind::f8f6f4 -> 0 e4m3.
+__host__ __device__ constexpr uint32_t make_idesc(int a_type, int b_type, int a_mn_major,
+                                                  int b_mn_major, int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(a_type) << 7) | (static_cast<uint32_t>(b_type) << 10) |
+         (static_cast<uint32_t>(a_mn_major) << 15) | (static_cast<uint32_t>(b_mn_major) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Byte offset of the 16-byte chunk `chunk` (0..7) of row `row` in a 128-byte
+// swizzled tile whose rows are 128 bytes apart (8-row atoms of 1024 bytes).
+__device__ __forceinline__ uint32_t sw128_offset(int row, int chunk) {
+  return static_cast<uint32_t>(row) * 128u + static_cast<uint32_t>((chunk ^ (row & 7)) << 4);
+}
+
+}  // namespace cskv

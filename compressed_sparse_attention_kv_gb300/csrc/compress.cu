@@ -1,0 +1,276 @@
+// The KV compressor (cskv_compress) and the row coder (cskv_encode_rows).
+//
+// "DeepSeek-V4 deep dive", section 4.1: entry i pools, channel by channel, the
+// softmax over its slots of (gate + slot bias) times the projected values;
+// section 4.2: ratio 4 reads the previous block through channel half 0 and its
+// own block through half 1 (8 slots, bias added before the transform, the first
+// entry's missing half has value 0 and score -inf); ratio 128 pools its own 128
+// tokens; then RMSNorm over the channels and RoPE on the last 64 dims at the
+// position of the entry's first token.
+//
+// Design: a bandwidth kernel.  Threads own 4 consecutive channels (8-byte bf16
+// loads, coalesced across the group); an entry of D channels is a group of D/4
+// threads (one warp at D = 128, the whole 128-thread block at D = 512).  The
+// arithmetic is the bit-exact fp32 contract: separately rounded __f*_rn
+// operations (never contracted to FMA), exp_own below, a pairwise sum of squares
+// that follows the channel order (in-thread pairs, then warp xor-shuffles, then
+// the warps of the block), and the coding of codec.cuh.
+#include "codec.cuh"
+#include "internal.h"
+
+namespace cskv {
+
+// ---------------------------------------------------------------------------
+// exp_own: e^x in a fixed fp32 operation order (Cody & Waite range reduction,
+// degree-7 Taylor polynomial).  Constants derived from ln 2: LN2_HI is ln 2 to
+// 16 significant bits (so n * LN2_HI is exact), LN2_LO the fp32 remainder,
+// C_k = fp32(1/k!).  Returns 0 below 2^-126 and for -inf.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float exp_own(float x) {
+  // every constant is the fp32 rounding of a double-precision expression
+  constexpr double kLn2 = 0.69314718055994530942;
+  const float kLog2e = static_cast<float>(1.0 / kLn2);
+  const float kLn2Hi = 0.693145751953125f;                       // 45426 / 65536
+  const float kLn2Lo = static_cast<float>(kLn2 - 0.693145751953125);
+  const float t = __fmul_rn(x, kLog2e);
+  if (!(t >= -126.0f)) return 0.0f;
+  const float n = rintf(t);
+  const float r = __fsub_rn(__fsub_rn(x, __fmul_rn(n, kLn2Hi)), __fmul_rn(n, kLn2Lo));
+  float p = static_cast<float>(1.0 / 5040.0);
+  p = __fadd_rn(__fmul_rn(p, r), static_cast<float>(1.0 / 720.0));
+  p = __fadd_rn(__fmul_rn(p, r), static_cast<float>(1.0 / 120.0));
+  p = __fadd_rn(__fmul_rn(p, r), static_cast<float>(1.0 / 24.0));
+  p = __fadd_rn(__fmul_rn(p, r), static_cast<float>(1.0 / 6.0));
+  p = __fadd_rn(__fmul_rn(p, r), 0.5f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+  return __fmul_rn(p, exp2i(static_cast<int>(n)));
+}
+
+struct CompressArgs {
+  const uint8_t* kv;
+  const uint8_t* gate;
+  const uint8_t* prev_kv;
+  const uint8_t* prev_gate;
+  const float* ape;
+  const float* norm_w;
+  const float* rope_cs;
+  const int32_t* req;
+  const int32_t* first_entry;
+  float eps;
+  int S, T, ratio, overlap, n;  // n = T / ratio entries per sequence
+  cskv_paged out;
+  int out_row_bytes;
+};
+
+// bf16 row pointer of token `tok` (channel half `half`) of sequence s.
+__device__ __forceinline__ const uint8_t* tok_ptr(const uint8_t* base, long long s, long long T,
+                                                  long long tok, int coff, int half, int D) {
+  return base + (((s * T + tok) * coff + half) * D) * 2;
+}
+
+template <int D>
+__device__ __forceinline__ float block_sum_pairwise(float v, int lt) {
+  // channel groups of 4 are already reduced in-thread; now threads in channel
+  // order: xor 1, 2, 4, 8, 16 inside a warp ...
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  if constexpr (D == 512) {
+    // ... then the four warps of the block: (w0 + w1) + (w2 + w3)
+    __shared__ float part[4];
+    if ((lt & 31) == 0) part[lt >> 5] = v;
+    __syncthreads();
+    v = __fadd_rn(__fadd_rn(part[0], part[1]), __fadd_rn(part[2], part[3]));
+  }
+  return v;
+}
+
+template <int D>
+__global__ void __launch_bounds__(128) compress_kernel(const CompressArgs a) {
+  constexpr int TPE = D / 4;        // threads per entry
+  constexpr int EPB = 128 / TPE;    // entries per block
+  const int lt = threadIdx.x % TPE;
+  const long long gentry = static_cast<long long>(blockIdx.x) * EPB + threadIdx.x / TPE;
+  const long long total = static_cast<long long>(a.S) * a.n;
+  const bool live = gentry < total;
+  // D == 512: one entry per block, the whole block stays for the block-wide sum.
+  if (!live && D != 512) return;
+  const long long s = live ? gentry / a.n : 0;
+  const int i = live ? static_cast<int>(gentry % a.n) : 0;
+  const int c0 = 4 * lt;
+  const int r = a.ratio;
+  const int coff = a.overlap ? 2 : 1;
+  const int slots = a.overlap ? 2 * r : r;
+
+  // slot j -> (value row, score row, bias row); nullptr value = the empty half
+  auto slot_src = [&](int j, const uint8_t*& vp, const uint8_t*& gp, const float*& ap) {
+    if (a.overlap && j < r) {
+      ap = a.ape + static_cast<long long>(j) * coff * D + c0;   // half 0 bias
+      if (i > 0) {
+        const long long tok = static_cast<long long>(i - 1) * r + j;
+        vp = tok_ptr(a.kv, s, a.T, tok, coff, 0, D) + 2 * c0;
+        gp = tok_ptr(a.gate, s, a.T, tok, coff, 0, D) + 2 * c0;
+      } else if (a.prev_kv != nullptr) {
+        vp = tok_ptr(a.prev_kv, s, r, j, 2, 0, D) + 2 * c0;
+        gp = tok_ptr(a.prev_gate, s, r, j, 2, 0, D) + 2 * c0;
+      } else {
+        vp = nullptr;
+        gp = nullptr;
+      }
+    } else {
+      const int jj = a.overlap ? j - r : j;
+      const int half = a.overlap ? 1 : 0;
+      const long long tok = static_cast<long long>(i) * r + jj;
+      ap = a.ape + static_cast<long long>(jj) * coff * D + half * D + c0;
+      vp = tok_ptr(a.kv, s, a.T, tok, coff, half, D) + 2 * c0;
+      gp = tok_ptr(a.gate, s, a.T, tok, coff, half, D) + 2 * c0;
+    }
+  };
+  auto score = [&](const uint8_t* gp, const float* ap) -> float4 {
+    if (gp == nullptr) return make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    const float4 g = load_bf16x4(gp);
+    const float4 b = *reinterpret_cast<const float4*>(ap);
+    return make_float4(__fadd_rn(g.x, b.x), __fadd_rn(g.y, b.y), __fadd_rn(g.z, b.z),
+                       __fadd_rn(g.w, b.w));
+  };
+
+  float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 den = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (live) {
+    // pass 1: m = max over slots of the biased scores
+    float4 m = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    for (int j = 0; j < slots; ++j) {
+      const uint8_t *vp, *gp;
+      const float* ap;
+      slot_src(j, vp, gp, ap);
+      const float4 sc = score(gp, ap);
+      m.x = fmaxf(m.x, sc.x); m.y = fmaxf(m.y, sc.y); m.z = fmaxf(m.z, sc.z); m.w = fmaxf(m.w, sc.w);
+    }
+    // pass 2: weights and slot-ordered sums (the scores are recomputed bit for bit)
+    for (int j = 0; j < slots; ++j) {
+      const uint8_t *vp, *gp;
+      const float* ap;
+      slot_src(j, vp, gp, ap);
+      const float4 sc = score(gp, ap);
+      const float4 v = vp ? load_bf16x4(vp) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float e0 = exp_own(__fsub_rn(sc.x, m.x)), e1 = exp_own(__fsub_rn(sc.y, m.y));
+      const float e2 = exp_own(__fsub_rn(sc.z, m.z)), e3 = exp_own(__fsub_rn(sc.w, m.w));
+      num.x = __fadd_rn(num.x, __fmul_rn(e0, v.x)); den.x = __fadd_rn(den.x, e0);
+      num.y = __fadd_rn(num.y, __fmul_rn(e1, v.y)); den.y = __fadd_rn(den.y, e1);
+      num.z = __fadd_rn(num.z, __fmul_rn(e2, v.z)); den.z = __fadd_rn(den.z, e2);
+      num.w = __fadd_rn(num.w, __fmul_rn(e3, v.w)); den.w = __fadd_rn(den.w, e3);
+    }
+  }
+  float4 y = live ? make_float4(__fdiv_rn(num.x, den.x), __fdiv_rn(num.y, den.y),
+                                __fdiv_rn(num.z, den.z), __fdiv_rn(num.w, den.w))
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+
+  if (a.norm_w != nullptr) {
+    const float local = __fadd_rn(__fadd_rn(__fmul_rn(y.x, y.x), __fmul_rn(y.y, y.y)),
+                                  __fadd_rn(__fmul_rn(y.z, y.z), __fmul_rn(y.w, y.w)));
+    const float ss = block_sum_pairwise<D>(local, threadIdx.x % 128);
+    const float rr = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(D)), a.eps)));
+    const float4 w = *reinterpret_cast<const float4*>(a.norm_w + c0);
+    y.x = __fmul_rn(__fmul_rn(y.x, rr), w.x);
+    y.y = __fmul_rn(__fmul_rn(y.y, rr), w.y);
+    y.z = __fmul_rn(__fmul_rn(y.z, rr), w.z);
+    y.w = __fmul_rn(__fmul_rn(y.w, rr), w.w);
+  }
+  if (a.rope_cs != nullptr && live && c0 >= D - 64) {
+    const int k = (c0 - (D - 64)) / 2;   // pairs k and k+1
+    const float4 cs = *reinterpret_cast<const float4*>(a.rope_cs + ((s * a.n + i) * 32 + k) * 2);
+    const float y0 = y.x, y1 = y.y, y2 = y.z, y3 = y.w;
+    y.x = __fsub_rn(__fmul_rn(y0, cs.x), __fmul_rn(y1, cs.y));
+    y.y = __fadd_rn(__fmul_rn(y0, cs.y), __fmul_rn(y1, cs.x));
+    y.z = __fsub_rn(__fmul_rn(y2, cs.z), __fmul_rn(y3, cs.w));
+    y.w = __fadd_rn(__fmul_rn(y2, cs.w), __fmul_rn(y3, cs.z));
+  }
+  RowPtr dst{nullptr, nullptr};
+  if (live) {
+    const long long row = static_cast<long long>(a.first_entry[s]) + i;
+    dst = paged_row(a.out, a.req[s], row, a.out_row_bytes);
+  }
+  store_row_values(y, lt, a.out.fmt, D, dst, live && dst.data != nullptr);
+}
+
+struct EncodeArgs {
+  const uint8_t* src;
+  int src_bf16;
+  int n;
+  const int32_t* req;
+  const int32_t* row;
+  cskv_paged out;
+  int out_row_bytes;
+};
+
+template <int D>
+__global__ void __launch_bounds__(128) encode_rows_kernel(const EncodeArgs a) {
+  constexpr int TPE = D / 4;
+  constexpr int EPB = 128 / TPE;
+  const int lt = threadIdx.x % TPE;
+  const long long i = static_cast<long long>(blockIdx.x) * EPB + threadIdx.x / TPE;
+  if (i >= a.n) return;   // whole groups leave together
+  float4 y;
+  if (a.src_bf16) {
+    y = load_bf16x4(a.src + (i * D + 4 * lt) * 2);
+  } else {
+    y = *reinterpret_cast<const float4*>(a.src + (i * D + 4 * lt) * 4);
+  }
+  const int req = a.req ? a.req[i] : 0;
+  const long long row = a.row ? a.row[i] : i;
+  const RowPtr dst = paged_row(a.out, req, row, a.out_row_bytes);
+  store_row_values(y, lt, a.out.fmt, D, dst, dst.data != nullptr);
+}
+
+// ---------------------------------------------------------------------------
+// launchers
+// ---------------------------------------------------------------------------
+cudaError_t launch_compress(const void* kv, const void* gate, const void* prev_kv,
+                            const void* prev_gate, const float* ape, const float* norm_w, float eps,
+                            const float* rope_cs, int S, int T, int ratio, int overlap, int dim,
+                            const int32_t* req, const int32_t* first_entry, const cskv_paged& out,
+                            int out_row_bytes, cudaStream_t stream) {
+  CompressArgs a;
+  a.kv = static_cast<const uint8_t*>(kv);
+  a.gate = static_cast<const uint8_t*>(gate);
+  a.prev_kv = static_cast<const uint8_t*>(prev_kv);
+  a.prev_gate = static_cast<const uint8_t*>(prev_gate);
+  a.ape = ape;
+  a.norm_w = norm_w;
+  a.rope_cs = rope_cs;
+  a.req = req;
+  a.first_entry = first_entry;
+  a.eps = eps;
+  a.S = S;
+  a.T = T;
+  a.ratio = ratio;
+  a.overlap = overlap;
+  a.n = T / ratio;
+  a.out = out;
+  a.out_row_bytes = out_row_bytes;
+  const long long total = static_cast<long long>(S) * a.n;
+  if (total == 0) return cudaSuccess;
+  if (dim == 512) {
+    compress_kernel<512><<<static_cast<unsigned>(total), 128, 0, stream>>>(a);
+  } else {
+    compress_kernel<128><<<static_cast<unsigned>((total + 3) / 4), 128, 0, stream>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_encode_rows(const void* src, int src_bf16, int n, int dim, const int32_t* req,
+                               const int32_t* row, const cskv_paged& out, int out_row_bytes,
+                               cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  EncodeArgs a{static_cast<const uint8_t*>(src), src_bf16, n, req, row, out, out_row_bytes};
+  if (dim == 512) {
+    encode_rows_kernel<512><<<static_cast<unsigned>(n), 128, 0, stream>>>(a);
+  } else {
+    encode_rows_kernel<128><<<static_cast<unsigned>((n + 3) / 4), 128, 0, stream>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+unsigned int take_err_compress() { return take_dev_err(); }
+
+}  // namespace cskv

@@ -1,0 +1,169 @@
+// C-ABI front end of libcskv: synchronous argument checks, then launches.
+// Nothing here allocates device memory or synchronises (cskv_device_status
+// excepted).
+#include <atomic>
+#include <cstdint>
+
+#include "internal.h"
+
+namespace cskv {
+
+static std::atomic<unsigned long long> g_spin_limit{kDefaultSpinLimit};
+unsigned long long spin_limit() { return g_spin_limit.load(std::memory_order_relaxed); }
+
+static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+static int32_t cuda_status(cudaError_t e) { return e == cudaSuccess ? CSKV_OK : CSKV_ERR_CUDA; }
+
+// Checks a paged-cache descriptor for a lane of dimension `dim`; `formats` is a
+// bit mask of the accepted cskv_format values.
+static bool paged_ok(const cskv_paged& c, int dim, unsigned formats) {
+  if (c.pool == nullptr || !aligned(c.pool, 16)) return false;
+  if (c.fmt < 0 || c.fmt > 3 || !((formats >> c.fmt) & 1u)) return false;
+  if (c.dim != dim) return false;
+  const size_t rb = cskv_row_bytes(c.fmt, c.dim);
+  if (rb == 0) return false;
+  if (c.page_bytes < static_cast<int64_t>(64 * rb) || c.page_bytes % 16 != 0) return false;
+  if (c.num_pages <= 0) return false;
+  if (c.block_table != nullptr && (c.max_pages <= 0 || !aligned(c.block_table, 4))) return false;
+  return true;
+}
+
+}  // namespace cskv
+
+using namespace cskv;
+
+extern "C" {
+
+size_t cskv_row_bytes(int32_t fmt, int32_t dim) {
+  if (dim != 128 && dim != 512) return 0;
+  switch (fmt) {
+    case CSKV_FMT_BF16: return 2u * dim;
+    case CSKV_FMT_FP8_E4M3_E8M0_B32:
+    case CSKV_FMT_FP8_E4M3_E8M0_B32_PAGESPLIT: return dim + dim / 32;
+    case CSKV_FMT_FP4_E2M1_E4M3_B16: return dim / 2 + dim / 16;
+    default: return 0;
+  }
+}
+
+const char* cskv_status_string(int32_t s) {
+  switch (s) {
+    case CSKV_OK: return "ok";
+    case CSKV_ERR_INVALID: return "invalid argument (nothing launched)";
+    case CSKV_ERR_UNSUPPORTED: return "unsupported configuration";
+    case CSKV_ERR_CUDA: return "CUDA error";
+    case CSKV_ERR_TIMEOUT: return "device wait timed out";
+    case CSKV_ERR_BOUNDS: return "device index outside its table or pool";
+    default: return "unknown status";
+  }
+}
+
+int32_t cskv_version(void) { return 100; }
+
+void cskv_set_spin_limit(uint64_t cycles) {
+  g_spin_limit.store(cycles == 0 ? kDefaultSpinLimit : cycles, std::memory_order_relaxed);
+}
+
+int32_t cskv_device_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return CSKV_ERR_CUDA;
+  const unsigned int bits = take_err_compress() | take_err_index() | take_err_attention();
+  if (bits & (1u << CSKV_ERR_TIMEOUT)) return CSKV_ERR_TIMEOUT;
+  if (bits & (1u << CSKV_ERR_BOUNDS)) return CSKV_ERR_BOUNDS;
+  if (bits) return CSKV_ERR_CUDA;
+  return CSKV_OK;
+}
+
+int32_t cskv_encode_rows(const void* src, int32_t src_is_bf16, int32_t n, int32_t dim,
+                         const int32_t* dst_req, const int32_t* dst_row, cskv_paged dst,
+                         void* stream) {
+  if (n < 0 || (dim != 128 && dim != 512)) return CSKV_ERR_INVALID;
+  if (n > 0 && (src == nullptr || !aligned(src, 16))) return CSKV_ERR_INVALID;
+  if (!paged_ok(dst, dim, 0xFu)) return CSKV_ERR_INVALID;
+  if (dst.fmt == CSKV_FMT_FP8_E4M3_E8M0_B32_PAGESPLIT && dim != 128) return CSKV_ERR_INVALID;
+  return cuda_status(launch_encode_rows(src, src_is_bf16 != 0, n, dim, dst_req, dst_row, dst,
+                                        static_cast<int>(cskv_row_bytes(dst.fmt, dim)),
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+int32_t cskv_compress(const void* kv, const void* gate, const void* prev_kv, const void* prev_gate,
+                      const float* ape, const float* norm_w, float eps, const float* rope_cs,
+                      int32_t S, int32_t T, int32_t ratio, int32_t overlap, int32_t dim,
+                      const int32_t* req, const int32_t* first_entry, cskv_paged out,
+                      void* stream) {
+  if (kv == nullptr || gate == nullptr || ape == nullptr || req == nullptr || first_entry == nullptr)
+    return CSKV_ERR_INVALID;
+  if (dim != 128 && dim != 512) return CSKV_ERR_INVALID;
+  if (S < 0 || T < 0 || ratio < 1 || ratio > 1024 || T % ratio != 0) return CSKV_ERR_INVALID;
+  if (overlap != 0 && overlap != 1) return CSKV_ERR_INVALID;
+  if (overlap && ratio > 8) return CSKV_ERR_INVALID;
+  if ((prev_kv == nullptr) != (prev_gate == nullptr)) return CSKV_ERR_INVALID;
+  if (!(eps >= 0.0f)) return CSKV_ERR_INVALID;
+  if (!aligned(kv, 8) || !aligned(gate, 8) || !aligned(ape, 16)) return CSKV_ERR_INVALID;
+  if (prev_kv && (!aligned(prev_kv, 8) || !aligned(prev_gate, 8))) return CSKV_ERR_INVALID;
+  if ((norm_w && !aligned(norm_w, 16)) || (rope_cs && !aligned(rope_cs, 16))) return CSKV_ERR_INVALID;
+  if (!paged_ok(out, dim, 0xFu)) return CSKV_ERR_INVALID;
+  if (out.fmt == CSKV_FMT_FP8_E4M3_E8M0_B32_PAGESPLIT && dim != 128) return CSKV_ERR_INVALID;
+  return cuda_status(launch_compress(kv, gate, prev_kv, prev_gate, ape, norm_w, eps, rope_cs, S, T,
+                                     ratio, overlap, dim, req, first_entry, out,
+                                     static_cast<int>(cskv_row_bytes(out.fmt, dim)),
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+size_t cskv_index_topk_workspace_size(int32_t B, int32_t max_ctx_len, int32_t ratio, int32_t Hi,
+                                      int32_t k) {
+  if (B <= 0 || max_ctx_len < 0 || ratio < 1 || Hi < 1 || k < 1) return 0;
+  return index_workspace_bytes(B, max_ctx_len / ratio, Hi, k);
+}
+
+int32_t cskv_index_topk(const void* q_idx, const float* w, cskv_paged keys, const int32_t* ctx_len,
+                        int32_t B, int32_t Hi, int32_t ratio, int32_t k, int32_t max_ctx_len,
+                        int32_t* topk_idx, float* topk_score, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  if (q_idx == nullptr || w == nullptr || ctx_len == nullptr || topk_idx == nullptr)
+    return CSKV_ERR_INVALID;
+  if (B < 1 || Hi < 1 || ratio < 1 || k < 1 || k > 2048 || max_ctx_len < 0) return CSKV_ERR_INVALID;
+  if (Hi > 64) return CSKV_ERR_UNSUPPORTED;
+  if (!aligned(q_idx, 16) || !aligned(w, 4)) return CSKV_ERR_INVALID;
+  if (!paged_ok(keys, 128, (1u << CSKV_FMT_BF16) | (1u << CSKV_FMT_FP8_E4M3_E8M0_B32_PAGESPLIT)))
+    return CSKV_ERR_INVALID;
+  if (keys.block_table == nullptr) return CSKV_ERR_INVALID;
+  const size_t need = index_workspace_bytes(B, max_ctx_len / ratio, Hi, k);
+  if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < need)
+    return CSKV_ERR_INVALID;
+  return cuda_status(launch_index_topk(q_idx, w, keys, ctx_len, B, Hi, ratio, k, max_ctx_len,
+                                       topk_idx, topk_score, workspace,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+size_t cskv_sparse_decode_attn_workspace_size(int32_t B, int32_t H, int32_t max_ctx_len,
+                                              int32_t ratio, int32_t k) {
+  if (B <= 0 || H <= 0 || max_ctx_len < 0 || ratio < 1) return 0;
+  return attn_workspace_bytes(B, H, max_ctx_len, ratio, k);
+}
+
+int32_t cskv_sparse_decode_attn(const void* q, cskv_paged main_kv, const void* swa, int32_t swa_fmt,
+                                const int32_t* ctx_len, const int32_t* topk_idx, int32_t k,
+                                int32_t ratio, int32_t max_ctx_len, const float* sink,
+                                float softmax_scale, const float* q_rope_cs, int32_t B, int32_t H,
+                                void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  if (q == nullptr || swa == nullptr || ctx_len == nullptr || q_rope_cs == nullptr || out == nullptr)
+    return CSKV_ERR_INVALID;
+  if (B < 1 || H < 1 || H > 128 || ratio < 1 || max_ctx_len < 0) return CSKV_ERR_INVALID;
+  if (topk_idx != nullptr && (k < 1 || k > 2048)) return CSKV_ERR_INVALID;
+  if (swa_fmt != CSKV_FMT_BF16 && swa_fmt != CSKV_FMT_FP8_E4M3_E8M0_B32) return CSKV_ERR_INVALID;
+  if (!aligned(q, 16) || !aligned(swa, 16) || !aligned(q_rope_cs, 16) || !aligned(out, 16))
+    return CSKV_ERR_INVALID;
+  if (!(softmax_scale > 0.0f)) return CSKV_ERR_INVALID;
+  if (!paged_ok(main_kv, 512, (1u << CSKV_FMT_BF16) | (1u << CSKV_FMT_FP8_E4M3_E8M0_B32) |
+                                  (1u << CSKV_FMT_FP4_E2M1_E4M3_B16)))
+    return CSKV_ERR_INVALID;
+  const size_t need = attn_workspace_bytes(B, H, max_ctx_len, ratio, topk_idx ? k : 0);
+  if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < need)
+    return CSKV_ERR_INVALID;
+  return cuda_status(launch_sparse_decode_attn(q, main_kv, swa, swa_fmt, ctx_len, topk_idx,
+                                               topk_idx ? k : 0, ratio, max_ctx_len, sink,
+                                               softmax_scale, q_rope_cs, B, H, out, workspace,
+                                               static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

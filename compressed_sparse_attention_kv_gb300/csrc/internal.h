@@ -1,0 +1,44 @@
+// Launchers and per-translation-unit error readers shared between the C-ABI
+// front end (cskv_api.cu) and the kernel files.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/cskv.h"
+
+namespace cskv {
+
+// default bound of every mbarrier spin-wait, in SM cycles (about 1 s at 2 GHz)
+constexpr unsigned long long kDefaultSpinLimit = 1ull << 31;
+unsigned long long spin_limit();
+
+cudaError_t launch_compress(const void* kv, const void* gate, const void* prev_kv,
+                            const void* prev_gate, const float* ape, const float* norm_w, float eps,
+                            const float* rope_cs, int S, int T, int ratio, int overlap, int dim,
+                            const int32_t* req, const int32_t* first_entry, const cskv_paged& out,
+                            int out_row_bytes, cudaStream_t stream);
+
+cudaError_t launch_encode_rows(const void* src, int src_bf16, int n, int dim, const int32_t* req,
+                               const int32_t* row, const cskv_paged& out, int out_row_bytes,
+                               cudaStream_t stream);
+
+size_t index_workspace_bytes(int B, int n_max, int Hi, int k);
+cudaError_t launch_index_topk(const void* q_idx, const float* w, const cskv_paged& keys,
+                              const int32_t* ctx_len, int B, int Hi, int ratio, int k,
+                              int max_ctx_len, int32_t* topk_idx, float* topk_score,
+                              void* workspace, cudaStream_t stream);
+
+size_t attn_workspace_bytes(int B, int H, int max_ctx, int ratio, int k);
+cudaError_t launch_sparse_decode_attn(const void* q, const cskv_paged& kv, const void* swa, int swa_fmt,
+                                      const int32_t* ctx_len, const int32_t* topk, int k, int ratio,
+                                      int max_ctx, const float* sink, float softmax_scale,
+                                      const float* q_rope, int B, int H, void* out, void* workspace,
+                                      cudaStream_t stream);
+
+unsigned int take_err_compress();
+unsigned int take_err_index();
+unsigned int take_err_attention();
+
+}  // namespace cskv

@@ -1,0 +1,222 @@
+/*
+ * cskv - compressed sparse attention KV: DeepSeek-V4-style compressed-KV decode
+ * attention for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI of libcskv.so.  Every pointer argument named "device" is CUDA device
+ * memory owned by the caller; the library never allocates, frees or keeps a
+ * pointer past the call.  Every call is asynchronous on the given stream
+ * (a cudaStream_t passed as void*, NULL = legacy default stream) and never
+ * synchronises, except cskv_device_status().
+ *
+ * Errors: arguments are checked on the host before anything is launched; a
+ * failed check returns CSKV_ERR_INVALID (or CSKV_ERR_UNSUPPORTED) and launches
+ * nothing.  A failed launch returns CSKV_ERR_CUDA.  Problems that only the
+ * device can see (a block-table entry outside the pool, a context longer than
+ * the table, a bounded wait that ran out) never fault: the kernel skips the
+ * offending access and sets a sticky error word, which cskv_device_status()
+ * reports and clears.
+ *
+ * Layout conventions (all row-major):
+ *  - a cache "row" is one 512-d compressed entry / window token (main lane) or
+ *    one 128-d index key, stored in a cskv_format;
+ *  - caches are paged: 64 rows per page, a per-request block table maps a
+ *    request's logical page p (rows 64p .. 64p+63) to a physical page of a
+ *    shared pool;
+ *  - the sliding-window ring of request b is 128 rows, row (b*128 + pos % 128).
+ *
+ * The operations follow "DeepSeek-V4 deep dive" (gangliao.me): section 4 for
+ * the compressor, section 5.2 for the indexer, sections 3.3-3.4 and 5.3 for the
+ * attention; the cache formats follow the "DeepSeek-V4-Flash" model record
+ * (528 B FP8 rows) and the "DeepSeek-V4.1-Flash" KV-compression diagram
+ * (MXFP4 with an E4M3 scale per 16 channels).
+ */
+#ifndef CSKV_H
+#define CSKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define CSKV_API __attribute__((visibility("default")))
+#else
+#define CSKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CSKV_OK = 0,
+  CSKV_ERR_INVALID = 1,     /* bad argument; nothing launched */
+  CSKV_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. > 64 indexer heads) */
+  CSKV_ERR_CUDA = 3,        /* a CUDA call failed */
+  CSKV_ERR_TIMEOUT = 4,     /* device: a bounded wait gave up (see cskv_set_spin_limit) */
+  CSKV_ERR_BOUNDS = 5       /* device: an index outside its table or pool was skipped */
+} cskv_status;
+
+typedef enum {
+  /* dim bf16 values: 2*dim bytes (1024 B at 512). */
+  CSKV_FMT_BF16 = 0,
+  /* dim float8_e4m3 codes, then dim/32 float8_e8m0 scale bytes (scale j covers
+   * channels 32j..32j+31): dim + dim/32 bytes, 528 B at 512, inline per row.
+   * "DeepSeek-V4-Flash" model record, engine kernel constraint (2). */
+  CSKV_FMT_FP8_E4M3_E8M0_B32 = 1,
+  /* dim/2 bytes of packed float4_e2m1 (channel 2i in the low nibble of byte i),
+   * then dim/16 float8_e4m3 scale codes (scale j covers channels 16j..16j+15):
+   * 288 B at 512, inline per row.  "DeepSeek-V4.1-Flash" diagram, MXFP4. */
+  CSKV_FMT_FP4_E2M1_E4M3_B16 = 2,
+  /* the FP8 codes of format 1, but each 64-row page stores its 64 data rows
+   * (dim bytes each) first and then its 64 scale rows (dim/32 bytes each):
+   * 132 B per 128-d index key, 8,448 B per page.  Index keys only. */
+  CSKV_FMT_FP8_E4M3_E8M0_B32_PAGESPLIT = 3
+} cskv_format;
+
+/* A paged cache (or, with block_table == NULL, a flat array of rows in which
+ * row r lives in page r/64 at slot r%64). */
+typedef struct cskv_paged {
+  void* pool;                 /* device, 16-byte aligned: num_pages pages, page_bytes apart */
+  const int32_t* block_table; /* device [batch, max_pages] logical page -> physical page, or NULL */
+  int64_t page_bytes;         /* bytes from one page to the next: >= 64*row_bytes, multiple of 16 */
+  int32_t num_pages;          /* pages in the pool; table entries outside [0, num_pages) are errors */
+  int32_t max_pages;          /* row stride of block_table = most pages one request may own */
+  int32_t fmt;                /* cskv_format */
+  int32_t dim;                /* 512 (main entries and window) or 128 (index keys) */
+} cskv_paged;
+
+/* Bytes of one row of format fmt at dimension dim (528, 288, 1024, 132 ...);
+ * 0 for an invalid pair. */
+CSKV_API size_t cskv_row_bytes(int32_t fmt, int32_t dim);
+
+/* Static description of a status code. */
+CSKV_API const char* cskv_status_string(int32_t status);
+
+/* Library version (major*10000 + minor*100 + patch). */
+CSKV_API int32_t cskv_version(void);
+
+/* Synchronises `stream`, then returns and clears the sticky device error word
+ * (CSKV_OK if no kernel reported a problem since the last call).  The only call
+ * that blocks. */
+CSKV_API int32_t cskv_device_status(void* stream);
+
+/* Upper bound, in SM clock cycles, of every spin-wait on an mbarrier inside the
+ * library's kernels (default 2^31, about one second).  A wait that runs out sets
+ * CSKV_ERR_TIMEOUT, drains the copies its block has in flight and returns.
+ * 0 restores the default.  Applies to launches made after the call. */
+CSKV_API void cskv_set_spin_limit(uint64_t cycles);
+
+/* ------------------------------------------------------------------------
+ * cskv_encode_rows: code rows of values into a cache.
+ * Row i of src (fp32 or bf16, [n, dim] row-major) is coded in dst.fmt and
+ * written as row dst_row[i] (or i if dst_row is NULL) of request dst_req[i]
+ * (or 0 if dst_req is NULL) of the paged cache dst.  Codes follow the block
+ * rules of cskv_compress (same bits for the same fp32 values).
+ * src: device, 16-byte aligned; n >= 0; dim in {128, 512}.
+ * ------------------------------------------------------------------------ */
+CSKV_API int32_t cskv_encode_rows(const void* src, int32_t src_is_bf16, int32_t n, int32_t dim,
+                         const int32_t* dst_req, const int32_t* dst_row,
+                         cskv_paged dst, void* stream);
+
+/* ------------------------------------------------------------------------
+ * cskv_compress: the KV compressor ("DeepSeek-V4 deep dive", section 4.1
+ * "Idea: average, but let the model choose the weights per channel" and
+ * section 4.2 "Ratio 4 (CSA) overlaps; ratio 128 (HCA) does not").
+ *
+ * S independent sequences, each a chunk of T tokens (T a multiple of ratio)
+ * of projected values kv and gate scores gate, both bf16 [S, T, coff, dim]
+ * (coff = 2 with overlap, 1 without).  Entry i of sequence s pools, for every
+ * channel c, the softmax over its slots of (gate + ape[slot position]) times kv:
+ *   - no overlap: slots = tokens ratio*i .. ratio*i + ratio-1, channel half 0;
+ *   - overlap (ratio <= 8): 2*ratio slots; the first ratio are the previous
+ *     block's tokens through channel half 0 with ape[:, :dim], the last ratio
+ *     the entry's own tokens through half 1 with ape[:, dim:].  The block before
+ *     a chunk's first block comes from prev_kv / prev_gate ([S, ratio, 2, dim]
+ *     bf16); NULL means the chunk starts the sequence (value 0, score -inf).
+ * then RMSNorm over dim with weight norm_w ([dim] fp32; NULL = no norm) and
+ * eps, then RoPE on the last 64 dims with the table rope_cs ([S, T/ratio, 32, 2]
+ * fp32 (cos, sin) per entry, pair k = dims (dim-64+2k, dim-64+2k+1); NULL = no
+ * RoPE), then coding in out.fmt.  Entry i of sequence s is written as row
+ * first_entry[s] + i of request req[s] of `out`.
+ *
+ * Arithmetic: bit-exact fp32 in a fixed order (no fused multiply-add): slot
+ * scores s = gate + ape; m = max; e = exp_own(s - m) (Cody-Waite reduction and a
+ * degree-7 Taylor polynomial); numerator and denominator summed in slot order;
+ * division; RMSNorm with a pairwise (recursive halves) sum of squares,
+ * 1/sqrt(ss/dim + eps); rotation y0*c - y1*s, y0*s + y1*c.
+ * ape: [ratio, coff*dim] fp32.  req, first_entry: device int32 [S].
+ * Alignment: kv, gate, prev_* 8 bytes; ape, norm_w, rope_cs 16 bytes.
+ * ------------------------------------------------------------------------ */
+CSKV_API int32_t cskv_compress(const void* kv, const void* gate,
+                      const void* prev_kv, const void* prev_gate,
+                      const float* ape, const float* norm_w, float eps,
+                      const float* rope_cs,
+                      int32_t S, int32_t T, int32_t ratio, int32_t overlap, int32_t dim,
+                      const int32_t* req, const int32_t* first_entry,
+                      cskv_paged out, void* stream);
+
+/* ------------------------------------------------------------------------
+ * cskv_index_topk: the lightning indexer and top-k ("DeepSeek-V4 deep dive",
+ * section 5.2 "What is different from V3.2's indexer"):
+ *   I_{b,j} = sum_h w[b,h] * ReLU(q[b,h,:] . k_{b,j})   for j < n_b,
+ *   n_b = floor(ctx_len[b] / ratio) visible entries (the query sits at
+ *   position ctx_len[b]-1),
+ * and topk_idx[b, :] = the min(k, n_b) entries with the largest I (ties: the
+ * smaller entry index), in ascending entry order, -1 after them.
+ * q_idx: bf16 [B, Hi, 128] device (post-RoPE).  w: fp32 [B, Hi] device (final
+ * head weights, any scale included).  keys: 128-d index keys, format
+ * FP8_..._PAGESPLIT (queries are then coded e4m3 with one e8m0 scale per head
+ * and the products run on the FP8 tensor cores) or BF16.  ctx_len: int32 [B]
+ * device, each <= max_ctx_len.  Hi in [1, 64]; k in [1, 2048].
+ * topk_score: optional fp32 [B, k] (NULL to skip): the kernel's fp32 score of
+ * each selected entry (-inf after the selection).
+ * workspace: device, >= cskv_index_topk_workspace_size(...) bytes, 256-byte
+ * aligned; its contents need no initialisation and are garbage afterwards.
+ * ------------------------------------------------------------------------ */
+CSKV_API size_t cskv_index_topk_workspace_size(int32_t B, int32_t max_ctx_len, int32_t ratio,
+                                      int32_t Hi, int32_t k);
+CSKV_API int32_t cskv_index_topk(const void* q_idx, const float* w, cskv_paged keys,
+                        const int32_t* ctx_len, int32_t B, int32_t Hi, int32_t ratio,
+                        int32_t k, int32_t max_ctx_len,
+                        int32_t* topk_idx, float* topk_score,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * cskv_sparse_decode_attn: shared-KV decode attention over the sliding window
+ * and the compressed entries in one softmax with a sink ("DeepSeek-V4 deep
+ * dive", section 3.1 "K = V, one head", section 3.3 partial RoPE with the
+ * inverse rotation, section 3.4 Eq. 27, section 5.3 index list; section 6.1
+ * for HCA).
+ * For request b with query position t = ctx_len[b] - 1 and every head h:
+ *   q' = q[b,h] with its last 64 dims rotated by angle(t) (q_rope_cs[b]),
+ *   keys = window rows of positions max(0, t-127) .. t (ring slot pos % 128 of
+ *          `swa`), then the compressed entries topk_idx[b, 0..k) (-1 skipped,
+ *          duplicates kept) or, if topk_idx is NULL, every visible entry
+ *          j < floor(ctx_len[b] / ratio) (HCA),
+ *   z_j = (q' . c_j) * softmax_scale,
+ *   o   = sum_j exp(z_j) c_j / (sum_j exp(z_j) + exp(sink[h])),
+ *   out[b,h] = o with its last 64 dims rotated back by -angle(t).
+ * q: bf16 [B, H, 512] device (pre-RoPE).  main_kv: 512-d entries, format FP8,
+ * FP4 or BF16.  swa: device [B, 128, row_bytes(swa_fmt, 512)], swa_fmt FP8 or
+ * BF16.  sink: fp32 [H] or NULL (no sink).  q_rope_cs: fp32 [B, 32, 2] (cos,
+ * sin) of each query position.  out: bf16 [B, H, 512] device.  H in [1, 128].
+ * Dequantised keys and values are exact in bf16; products run as tcgen05
+ * bf16 MMAs with fp32 accumulation; the query is rounded to bf16 after RoPE.
+ * workspace: >= cskv_sparse_decode_attn_workspace_size(...) bytes, 256-byte
+ * aligned, no initialisation needed.
+ * ------------------------------------------------------------------------ */
+CSKV_API size_t cskv_sparse_decode_attn_workspace_size(int32_t B, int32_t H, int32_t max_ctx_len,
+                                              int32_t ratio, int32_t k);
+CSKV_API int32_t cskv_sparse_decode_attn(const void* q, cskv_paged main_kv,
+                                const void* swa, int32_t swa_fmt,
+                                const int32_t* ctx_len, const int32_t* topk_idx, int32_t k,
+                                int32_t ratio, int32_t max_ctx_len,
+                                const float* sink, float softmax_scale,
+                                const float* q_rope_cs, int32_t B, int32_t H,
+                                void* out, void* workspace, size_t workspace_bytes,
+                                void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSKV_H */

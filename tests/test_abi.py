@@ -1,0 +1,98 @@
+"""The C-ABI library: it builds, loads without a GPU, exports every symbol include/cskv.h
+declares, and rejects bad arguments on the host before any launch (CPU only)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from compressed_sparse_attention_kv_gb300 import build, _lib
+    build.build()
+    return _lib.lib()
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "cskv.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"CSKV_API\s+[\w\s\*]+?\b(cskv_\w+)\s*\(", text)))
+
+
+def test_header_and_binding_agree():
+    from compressed_sparse_attention_kv_gb300 import _lib
+    names = _declared()
+    assert len(names) == 11
+    assert sorted(_lib.SIGNATURES) == names
+
+
+def test_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+    out = os.popen("nm -D --defined-only %s" % os.path.join(ROOT, "compressed_sparse_attention_kv_gb300",
+                                                             "libcskv.so")).read()
+    exported = set(re.findall(r"\bT (cskv_\w+)", out))
+    assert exported == set(_declared())
+
+
+def test_row_bytes_and_status(lib):
+    assert lib.cskv_row_bytes(1, 512) == 528
+    assert lib.cskv_row_bytes(2, 512) == 288
+    assert lib.cskv_row_bytes(0, 512) == 1024
+    assert lib.cskv_row_bytes(3, 128) == 132
+    assert lib.cskv_row_bytes(1, 100) == 0
+    assert lib.cskv_status_string(0) == b"ok"
+    assert lib.cskv_version() >= 100
+
+
+def test_workspace_sizes(lib):
+    small = lib.cskv_index_topk_workspace_size(1, 4096, 4, 4, 512)
+    big = lib.cskv_index_topk_workspace_size(8, 1 << 20, 4, 64, 512)
+    assert 0 < small < big
+    # scores + candidates dominate: 12 bytes per visible entry
+    assert big >= 8 * (1 << 18) * 12
+    assert lib.cskv_sparse_decode_attn_workspace_size(8, 64, 1 << 20, 4, 512) >= 8 * 5 * 64 * 512 * 4
+    assert lib.cskv_index_topk_workspace_size(0, 10, 4, 4, 4) == 0
+
+
+def test_invalid_arguments_launch_nothing(lib):
+    from compressed_sparse_attention_kv_gb300._lib import Paged
+    bad = Paged(None, None, 0, 0, 0, 1, 512)
+    # null required pointers / bad sizes -> CSKV_ERR_INVALID (1), checked before any CUDA call
+    assert lib.cskv_compress(None, None, None, None, None, None, 1e-6, None, 1, 4, 4, 1, 512,
+                             None, None, bad, None) == 1
+    fake = ctypes.c_void_p(4096)
+    good = Paged(4096, None, 64 * 528, 4, 0, 1, 512)
+    assert lib.cskv_compress(fake, fake, None, None, fake, None, 1e-6, None, 1, 6, 4, 1, 512,
+                             fake, fake, good, None) == 1                      # T % ratio != 0
+    assert lib.cskv_compress(fake, fake, None, None, fake, None, 1e-6, None, 1, 128, 128, 1, 512,
+                             fake, fake, good, None) == 1                      # overlap needs ratio <= 8
+    assert lib.cskv_compress(fake, fake, None, None, fake, None, -1.0, None, 1, 8, 4, 1, 512,
+                             fake, fake, good, None) == 1                      # eps < 0
+    keys = Paged(4096, 4096, 64 * 132, 4, 4, 3, 128)
+    assert lib.cskv_index_topk(fake, fake, keys, fake, 1, 65, 4, 512, 4096, fake, None, fake, 1 << 30,
+                               None) == 2                                       # > 64 heads
+    assert lib.cskv_index_topk(fake, fake, keys, fake, 1, 4, 4, 4096, 4096, fake, None, fake, 1 << 30,
+                               None) == 1                                       # k > 2048
+    assert lib.cskv_index_topk(fake, fake, keys, fake, 1, 4, 4, 512, 4096, fake, None, fake, 16,
+                               None) == 1                                       # workspace too small
+    main = Paged(4096, 4096, 64 * 528, 4, 4, 3, 512)                           # page-split is not a main format
+    assert lib.cskv_sparse_decode_attn(fake, main, fake, 1, fake, None, 0, 128, 4096, None, 0.04, fake,
+                                       1, 64, fake, fake, 1 << 30, None) == 1
+    main = Paged(4096, 4096, 64 * 528, 4, 4, 1, 512)
+    assert lib.cskv_sparse_decode_attn(fake, main, fake, 2, fake, None, 0, 128, 4096, None, 0.04, fake,
+                                       1, 64, fake, fake, 1 << 30, None) == 1    # FP4 window not allowed
+    assert lib.cskv_sparse_decode_attn(fake, main, fake, 1, fake, None, 0, 128, 4096, None, 0.04, fake,
+                                       1, 129, fake, fake, 1 << 30, None) == 1   # H > 128
+
+
+def test_binding_refuses_without_library(tmp_path, monkeypatch):
+    from compressed_sparse_attention_kv_gb300 import _lib
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(_lib, "_lib", None)
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        _lib.lib()

@@ -1,0 +1,125 @@
+"""GPU parity: lightning indexer + top-k against the oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import compressed_sparse_attention_kv_gb300 as cskv
+from compressed_sparse_attention_kv_gb300 import synth
+from oracle import codecs, indexer
+
+from cases import HostPaged, bf16_values, check_topk, cuda
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(q_t, w, cache, ctx, ratio, k, max_ctx):
+    dev = cache.to_device()
+    idx, sc = cskv.index_topk(q_t.cuda(), cuda(w), dev, cuda(np.asarray(ctx, np.int32)), ratio, k, max_ctx)
+    assert cskv.device_status() == 0
+    return idx.cpu().numpy(), sc.cpu().numpy()
+
+
+def test_integer_inputs_exact_with_ties():
+    """Integer-valued q, k, w: every fp32 partial sum is exact, so the selected sets
+    (with their tie-breaks to the smaller index) must equal the oracle's exactly."""
+    ratio, k, Hi = 4, 512, 64
+    ctx = [4 * 1000 + 3, 4 * 5000, 4 * 300 + 1, 4 * 777 + 2]
+    n = [c // ratio for c in ctx]
+    q, _, w = synth.integer_index_inputs(11, len(ctx), Hi, 1)
+    cache = HostPaged(codecs.FMT_FP8_PAGESPLIT, 128, n, seed=5)
+    keys = []
+    for b, nb in enumerate(n):
+        _, kk, _ = synth.integer_index_inputs(100 + b, 1, 1, nb)
+        cache.fill(b, kk)
+        keys.append(cache.decoded[b])
+    q_t, q_v = bf16_values(q)
+    idx, sc = _run(q_t, w, cache, ctx, ratio, k, max(ctx))
+    for b, nb in enumerate(n):
+        q_hat = indexer.quantize_queries(q_v[b])
+        I = indexer.scores_fp64(q_hat, w[b], keys[b])
+        ref = indexer.select_topk(I, k)
+        assert np.array_equal(idx[b], ref), b
+        m = min(k, nb)
+        assert np.array_equal(sc[b, :m].astype(np.float64), I[ref[:m]])
+        assert np.all(np.isneginf(sc[b, m:]))
+
+
+@pytest.mark.parametrize("Hi", [64, 16, 4])
+def test_random_fp8_keys(Hi):
+    ratio, k = 4, 512
+    ctx = [4 * 7000 + 1, 4 * 513, 4 * 512, 4 * 129 + 3, 4 * 20001]
+    n = [c // ratio for c in ctx]
+    rs = np.random.default_rng(Hi)
+    q = rs.standard_normal((len(ctx), Hi, 128)).astype(np.float32)
+    w = rs.uniform(0, 1, (len(ctx), Hi)).astype(np.float32)
+    cache = HostPaged(codecs.FMT_FP8_PAGESPLIT, 128, n, seed=6)
+    for b, nb in enumerate(n):
+        cache.fill(b, rs.standard_normal((nb, 128)).astype(np.float32))
+    q_t, q_v = bf16_values(q)
+    idx, sc = _run(q_t, w, cache, ctx, ratio, k, max(ctx))
+    swaps = 0
+    for b, nb in enumerate(n):
+        swaps += check_topk(idx[b], sc[b], indexer.quantize_queries(q_v[b]), w[b], cache.decoded[b], nb, k)
+    assert swaps <= 1
+
+
+def test_bf16_keys_and_negative_weights():
+    ratio, k, Hi = 4, 64, 8
+    ctx = [4 * 1024, 4 * 50 + 2, 4 * 3000 + 1]
+    n = [c // ratio for c in ctx]
+    rs = np.random.default_rng(3)
+    q = rs.standard_normal((len(ctx), Hi, 128)).astype(np.float32)
+    w = rs.uniform(-1, 1, (len(ctx), Hi)).astype(np.float32)
+    cache = HostPaged(codecs.FMT_BF16, 128, n, seed=7)
+    for b, nb in enumerate(n):
+        cache.fill(b, rs.standard_normal((nb, 128)).astype(np.float32))
+    q_t, q_v = bf16_values(q)
+    idx, sc = _run(q_t, w, cache, ctx, ratio, k, max(ctx))
+    for b, nb in enumerate(n):
+        check_topk(idx[b], sc[b], q_v[b].astype(np.float64), w[b], cache.decoded[b], nb, k)
+
+
+def test_empty_and_tiny_contexts():
+    ratio, k, Hi = 4, 16, 4
+    ctx = [0, 3, 4, 4 * 16, 4 * 17]
+    n = [c // ratio for c in ctx]
+    rs = np.random.default_rng(4)
+    q = rs.standard_normal((len(ctx), Hi, 128)).astype(np.float32)
+    w = rs.uniform(0, 1, (len(ctx), Hi)).astype(np.float32)
+    cache = HostPaged(codecs.FMT_FP8_PAGESPLIT, 128, [max(1, x) for x in n], seed=8)
+    for b, nb in enumerate(n):
+        cache.fill(b, rs.standard_normal((max(1, nb), 128)).astype(np.float32))
+    q_t, q_v = bf16_values(q)
+    idx, sc = _run(q_t, w, cache, ctx, ratio, k, max(ctx))
+    assert np.all(idx[0] == -1) and np.all(idx[1] == -1)
+    assert idx[2, 0] == 0 and np.all(idx[2, 1:] == -1)
+    assert np.array_equal(idx[3], np.arange(16))
+    check_topk(idx[4], sc[4], indexer.quantize_queries(q_v[4]), w[4], cache.decoded[4], n[4], k)
+
+
+def test_csa_1m_full_size_sampled():
+    """The 1M-context workload (batch 8, 262,144 FP8 keys per request, 64 heads,
+    top-512) in the bench's launch configuration; two requests checked in full."""
+    wl = synth.workload("csa_1m")
+    n = int(wl.n_entries[0])
+    bt, num_pages = synth.page_tables(wl, "index")
+    pb = 64 * 132
+    pool = torch.zeros((num_pages, pb), dtype=torch.uint8, device="cuda")
+    dev = cskv.PagedCache(pool, cuda(bt), codecs.FMT_FP8_PAGESPLIT, 128)
+    ppr = int(wl.pages_per_req()[0])
+    for b in range(wl.B):
+        vals = synth.request_values(wl, b, "index")
+        rows = np.arange(ppr * 64, dtype=np.int32)
+        cskv.encode_rows(cuda(vals), dev, req=cuda(np.full(rows.shape, b, np.int32)), row=cuda(rows))
+    _, q_idx, w, _ = synth.queries(wl)
+    q_t, q_v = bf16_values(q_idx)
+    ctx = wl.ctx_len.astype(np.int32)
+    idx, sc = cskv.index_topk(q_t.cuda(), cuda(w), dev, cuda(ctx), wl.ratio, wl.k, wl.max_ctx)
+    assert cskv.device_status() == 0
+    idx = idx.cpu().numpy()
+    sc = sc.cpu().numpy()
+    for b in (0, 5):
+        vals = synth.request_values(wl, b, "index")
+        k_hat = codecs.decode_pagesplit(codecs.encode_pagesplit(vals), 128)
+        check_topk(idx[b], sc[b], indexer.quantize_queries(q_v[b]), w[b], k_hat, n, wl.k)
