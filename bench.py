@@ -1,0 +1,500 @@
+#!/usr/bin/env python
+"""Decode-attention benchmark: queries/s per layer at 1M context on one GB300.
+
+One step = one decode token through one CSA layer for a batch of 8 requests at
+1,048,576 tokens (262,144 compressed entries each), i.e. every row of the hot path:
+  1. compress the block that the new token completes (main 512-d entry -> FP8-528,
+     index 128-d key -> FP8-132),
+  2. index_topk: score all 262,144 FP8 keys per request with 64 indexer heads, keep 512,
+  3. sparse_decode_attn: 64 heads over 128 window rows + 512 selected FP8 entries,
+     one softmax with the sink, inverse RoPE.
+Caches are resident in HBM before timing; the L2 is flushed (512 MB write) between
+timed steps, outside the timed region.  Inputs are seeded synthetic data.
+
+  python bench.py [--steps K] [--warmup W] [--gpus N] [--impl cskv|reference]
+
+--impl reference times the CPU oracle (the test oracle, not tuned) on the same workload,
+one query per step.  Under torchrun each rank runs an independent replica (the path
+shards by request; no collective); rank 0 prints one JSON line.
+"""
+
+import argparse
+import concurrent.futures
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from compressed_sparse_attention_kv_gb300 import synth  # noqa: E402
+
+METRIC = "decode attn queries/s per layer at 1M ctx; KV-read GB/s and % of HBM/FP8 roofline"
+WORKLOAD = "csa_1m"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def workload_desc(wl):
+    return ("CSA decode at 1M context: batch %d, %d tokens -> %d entries at ratio %d, indexer %d heads "
+            "x 128 FP8 keys (132 B) w~U(0,1), top-%d, %d query heads x 512 over FP8-528 entries "
+            "+ FP8 window 128, sink; per step: compress the completed block (main + index key), "
+            "index_topk, sparse_decode_attn" % (wl.B, int(wl.ctx_len[0]), int(wl.n_entries[0]), wl.ratio,
+                                               wl.Hi, wl.k, wl.H))
+
+
+def step_inputs(wl):
+    """Per-step inputs (host arrays): queries and the completed block for both compressors."""
+    q, q_idx, w, sink = synth.queries(wl)
+    kv, gate, pkv, pgate, ikv, igate, ipkv, ipgate = ([] for _ in range(8))
+    for b in range(wl.B):
+        a, g = synth.compressor_tokens(wl.seed, wl.ratio, wl.ratio, True, 512, seq=b)
+        pa, pg = synth.compressor_prev(wl.seed, wl.ratio, 512, seq=b)
+        ia, ig = synth.compressor_tokens(wl.seed, wl.ratio, wl.ratio, True, 128, index_lane=True, seq=b)
+        ipa, ipg = synth.compressor_prev(wl.seed, wl.ratio, 128, index_lane=True, seq=b)
+        kv.append(a); gate.append(g); pkv.append(pa); pgate.append(pg)
+        ikv.append(ia); igate.append(ig); ipkv.append(ipa); ipgate.append(ipg)
+    ape, nw = synth.compressor_params(wl.seed, wl.ratio, True, 512)
+    iape, inw = synth.compressor_params(wl.seed, wl.ratio, True, 128, index_lane=True)
+    st = lambda x: np.ascontiguousarray(np.stack(x))  # noqa: E731
+    return dict(q=q, q_idx=q_idx, w=w, sink=sink, kv=st(kv), gate=st(gate), pkv=st(pkv), pgate=st(pgate),
+                ikv=st(ikv), igate=st(igate), ipkv=st(ipkv), ipgate=st(ipgate), ape=ape, nw=nw, iape=iape,
+                inw=inw)
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.proc = None
+        self.gpu_id = gpu_id
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_id), "--query-gpu=" + self.FIELDS, "--format=csv,noheader",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 8]
+        sm = [float(r[1].split()[0]) for r in rows if r[1].split()[0].replace(".", "").isdigit()]
+        mx = [float(r[2].split()[0]) for r in rows if r[2].split()[0].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip().lower() == "active"})
+        loaded = [s for s in sm if mx and s >= 0.3 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def live_events(torch):
+    """Two timing events whose CUDA handles exist (torch creates them on first record)."""
+    evs = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    for e in evs:
+        e.record()
+    torch.cuda.synchronize()
+    return evs
+
+
+def gen_parallel(fn, items, threads=16):
+    with concurrent.futures.ThreadPoolExecutor(max_workers=threads) as ex:
+        return list(ex.map(fn, items))
+
+
+def build_caches(wl, torch, cskv):
+    """Resident caches: index keys (FP8 page-split), main entries (FP8-528), window ring (FP8-528)."""
+    dev = "cuda"
+    bt_i, np_i = synth.page_tables(wl, "index")
+    bt_m, np_m = synth.page_tables(wl, "main")
+    keys = cskv.PagedCache(torch.zeros((np_i, 64 * 132), dtype=torch.uint8, device=dev),
+                           torch.from_numpy(bt_i).to(dev), cskv.FMT_FP8_PAGESPLIT, 128)
+    main = cskv.PagedCache(torch.zeros((np_m, 64 * 528), dtype=torch.uint8, device=dev),
+                           torch.from_numpy(bt_m).to(dev), cskv.FMT_FP8, 512)
+    ppr = int(wl.pages_per_req()[0])
+    rows = torch.arange(ppr * 64, dtype=torch.int32, device=dev)
+    for lane, cache, dim in (("index", keys, 128), ("main", main, 512)):
+        f = synth.index_page_values if lane == "index" else synth.main_page_values
+        for b in range(wl.B):
+            pages = gen_parallel(lambda p: f(wl, b, p), range(ppr))
+            vals = torch.from_numpy(np.concatenate(pages)).to(dev)
+            cskv.encode_rows(vals, cache, req=torch.full_like(rows, b), row=rows)
+            del vals
+    swa_vals = torch.from_numpy(np.stack([synth.swa_values(wl, b) for b in range(wl.B)])).to(dev)
+    swa = torch.zeros((wl.B, 128, 528), dtype=torch.uint8, device=dev)
+    swa_c = cskv.PagedCache(swa.view(wl.B * 2, 64 * 528), None, cskv.FMT_FP8, 512)
+    cskv.encode_rows(swa_vals.reshape(-1, 512), swa_c)
+    torch.cuda.synchronize()
+    return keys, main, swa
+
+
+def run_gpu(args, rank, world):
+    import torch
+    import compressed_sparse_attention_kv_gb300 as cskv
+    from compressed_sparse_attention_kv_gb300 import _lib
+
+    _lib.lib()
+    dev = "cuda"
+    wl = synth.workload(WORKLOAD)
+    B, H, Hi, k, r = wl.B, wl.H, wl.Hi, wl.k, wl.ratio
+    L = int(wl.ctx_len[0])
+    n = L // r
+    t_setup = time.time()
+    keys, main, swa = build_caches(wl, torch, cskv)
+    inp = step_inputs(wl)
+
+    # ---- static device buffers (graph-capture safe) and pinned host copies of the step inputs
+    bf = torch.bfloat16
+    host = {
+        "q": torch.from_numpy(inp["q"]).to(bf), "q_idx": torch.from_numpy(inp["q_idx"]).to(bf),
+        "w": torch.from_numpy(inp["w"]), "kv": torch.from_numpy(inp["kv"]).to(bf),
+        "gate": torch.from_numpy(inp["gate"]).to(bf), "pkv": torch.from_numpy(inp["pkv"]).to(bf),
+        "pgate": torch.from_numpy(inp["pgate"]).to(bf), "ikv": torch.from_numpy(inp["ikv"]).to(bf),
+        "igate": torch.from_numpy(inp["igate"]).to(bf), "ipkv": torch.from_numpy(inp["ipkv"]).to(bf),
+        "ipgate": torch.from_numpy(inp["ipgate"]).to(bf),
+        "ecs": torch.from_numpy(cskv.rope_table(np.full((B, 1), (n - 1) * r))),
+        "qcs": torch.from_numpy(cskv.rope_table(wl.ctx_len - 1)),
+        "ctx": torch.from_numpy(wl.ctx_len.astype(np.int32)),
+        "first": torch.full((B,), n - 1, dtype=torch.int32),
+    }
+    host = {kk: v.contiguous().pin_memory() for kk, v in host.items()}
+    d = {kk: v.to(dev) for kk, v in host.items()}
+    req = torch.arange(B, dtype=torch.int32, device=dev)
+    ape, nw = torch.from_numpy(inp["ape"]).to(dev), torch.from_numpy(inp["nw"]).to(dev)
+    iape, inw = torch.from_numpy(inp["iape"]).to(dev), torch.from_numpy(inp["inw"]).to(dev)
+    sink = torch.from_numpy(inp["sink"]).to(dev)
+    topk = torch.empty((B, k), dtype=torch.int32, device=dev)
+    out = torch.empty((B, H, 512), dtype=bf, device=dev)
+    ws_i = torch.empty(cskv.index_topk_workspace_size(B, L, r, Hi, k), dtype=torch.uint8, device=dev)
+    ws_a = torch.empty(cskv.sparse_decode_attn_workspace_size(B, H, L, r, k), dtype=torch.uint8, device=dev)
+    out_host = torch.empty_like(out, device="cpu").pin_memory()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        cskv.compress(d["kv"], d["gate"], ape, r, True, main, req, d["first"], prev_kv=d["pkv"],
+                      prev_gate=d["pgate"], norm_w=nw, rope_cs=d["ecs"])
+        cskv.compress(d["ikv"], d["igate"], iape, r, True, keys, req, d["first"], prev_kv=d["ipkv"],
+                      prev_gate=d["ipgate"], norm_w=inw, rope_cs=d["ecs"])
+        cskv.index_topk(d["q_idx"], d["w"], keys, d["ctx"], r, k, L, topk_idx=topk, workspace=ws_i,
+                        want_scores=False)
+        cskv.sparse_decode_attn(d["q"], main, swa, cskv.FMT_FP8, d["ctx"], topk, k, r, L, sink,
+                                cskv.DEFAULT_SCALE, d["qcs"], out=out, workspace=ws_a)
+
+    launches_per_step = 2 + 4 + 2
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    status = cskv.device_status()
+    if status != 0:
+        raise RuntimeError("device status %d after warm-up" % status)
+
+    graph = None
+    if not args.no_graph:
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            step()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        ev_sb, ev_se = live_events(torch)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            cskv.set_timing_events(ev_sb, ev_se)
+            step()
+            cskv.set_timing_events(None, None)
+    setup_s = time.time() - t_setup
+
+    def run_once():
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        run_once()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K steps, L2 flushed before each (outside the events)
+    clk = ClockSampler(os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0])
+    clk.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    score_ms = []
+    if graph is None:
+        ev_sb, ev_se = live_events(torch)
+        cskv.set_timing_events(ev_sb, ev_se)
+    wall0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        evs[i][0].record()
+        run_once()
+        evs[i][1].record()
+        evs[i][1].synchronize()
+        score_ms.append(ev_sb.elapsed_time(ev_se))
+    torch.cuda.synchronize()
+    wall = time.time() - wall0
+    if world > 1:
+        torch.distributed.barrier()
+    cskv.set_timing_events(None, None)
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    clocks = clk.stop()
+    status = cskv.device_status()
+    if status != 0:
+        raise RuntimeError("device status %d after timing" % status)
+
+    # ---- end to end through the public API: host inputs -> device, step, result -> host
+    e2e_ms = []
+    names = [kk for kk in host if kk not in ("ctx", "first")] + ["ctx", "first"]
+    h2d = sum(host[kk].numel() * host[kk].element_size() for kk in names)
+    d2h = out.numel() * out.element_size()
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for kk in names:
+            d[kk].copy_(host[kk], non_blocking=True)
+        run_once()
+        out_host.copy_(out, non_blocking=True)
+        e1.record()
+        e1.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(e0.elapsed_time(e1))
+
+    mean_ms = statistics.mean(step_ms)
+    if world > 1:
+        t = torch.tensor([mean_ms, statistics.mean(e2e_ms)], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        mean_ms, e2e_mean = float(t[0]), float(t[1])
+    else:
+        e2e_mean = statistics.mean(e2e_ms)
+
+    # ---- roofline of the dominant kernel (the indexer score pass): bytes it must read
+    algo_bytes = 132 * int(wl.n_entries.sum())
+    score_mean = statistics.mean(score_ms)
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except OSError:
+        pass
+    peak = peaks.get("hbm_gbs", 6800.0)
+    achieved = algo_bytes / (score_mean * 1e-3) / 1e9
+    traffic = profiled_traffic()
+    path_bytes = algo_bytes + B * (640 * 528 + 2 * 64 * 512 + 64 * 128 * 2)
+
+    res = {
+        "metric": METRIC,
+        "value": world * B / (mean_ms * 1e-3),
+        "unit": "queries/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": mean_ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3 (indexer MMA) + bf16 (attention MMA), fp32 accumulate",
+        "data": "synthetic (seeded N(0,1) caches and queries, U(0,1) head weights)",
+        "config": {"workload": workload_desc(wl), "batch_per_gpu": B, "context": L,
+                   "l2": "flushed before every timed step (512 MB write, outside the timed region); "
+                         "inputs (277 MB of index keys) also exceed L2",
+                   "timing": "CUDA events per step around a CUDA-graph replay" if graph else "CUDA events per step",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"kernel": "index_score_kernel (FP8 keys, tcgen05 e4m3 MMA)", "bound": "hbm",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": "measured" if "hbm_gbs" in peaks else "fallback",
+                     "algorithmic_bytes_per_launch": algo_bytes, "ms_per_launch": score_mean,
+                     "traffic": traffic},
+        "kv_read_gbs": path_bytes / (mean_ms * 1e-3) / 1e9,
+        "step_frac_of_hbm_roofline": (path_bytes / (peak * 1e9)) / (mean_ms * 1e-3),
+        "e2e": {"value": world * B / (e2e_mean * 1e-3), "unit": "queries/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "wall_s_timed": wall,
+        "setup_s": setup_s,
+    }
+    return res
+
+
+def profiled_traffic():
+    """DRAM bytes per score-kernel launch from the committed ncu summary, if the kernel
+    source is unchanged since that capture (else None)."""
+    src = os.path.join(ROOT, "compressed_sparse_attention_kv_gb300", "csrc", "index_topk.cu")
+    summ = os.path.join(ROOT, "profiles", "index_score_csa_1m.json")
+    try:
+        with open(src, "rb") as f:
+            h = hashlib.sha256(f.read()).hexdigest()[:16]
+        with open(summ) as f:
+            p = json.load(f)
+    except OSError:
+        return None
+    if p.get("source_sha256_16") != h:
+        return None
+    return p.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------- oracle arm
+
+class OracleRunner:
+    """The CPU oracle on the same workload: one query (one request) per step, from the coded bytes."""
+
+    def __init__(self, wl, requests):
+        from oracle import codecs
+        self.wl = wl
+        self.inp = step_inputs(wl)
+        self.req = list(requests)
+        self.keys, self.main_pages, self.swa = {}, {}, {}
+        for b in self.req:
+            vals = synth.request_values(wl, b, "index")
+            self.keys[b] = codecs.encode_pagesplit(vals)
+            self.swa[b] = codecs.encode_rows(synth.swa_values(wl, b), codecs.FMT_FP8)
+            # the main pages this request's selection will read, coded ahead (cache preparation)
+            top = self._select(b)
+            pages = sorted(set(int(j) // 64 for j in top if j >= 0) | {(int(wl.n_entries[b]) - 1) // 64})
+            self.main_pages[b] = {p: codecs.encode_rows(synth.main_page_values(wl, b, p), codecs.FMT_FP8)
+                                  for p in pages}
+
+    def _select(self, b):
+        from oracle import codecs, indexer
+        k_hat = codecs.decode_pagesplit(self.keys[b], 128)
+        top, _ = indexer.index_topk(self.inp["q_idx"][b], self.inp["w"][b], k_hat, int(self.wl.ctx_len[b]),
+                                    self.wl.ratio, self.wl.k, True)
+        return top
+
+    def query(self, b):
+        """compress (main + index key of the completed block), index_topk, attention for request b."""
+        from oracle import attention, codecs, compress, indexer, rope
+        wl, inp = self.wl, self.inp
+        r = wl.ratio
+        n = int(wl.n_entries[b])
+        bf = lambda x: codecs.bf16_decode(codecs.bf16_encode(x)).astype(np.float32)  # noqa: E731
+        cs = rope.table(np.array([(n - 1) * r]))
+        ent = compress.compress_contract(bf(inp["kv"][b]), bf(inp["gate"][b]), inp["ape"], r, True,
+                                         prev_kv=bf(inp["pkv"][b]), prev_gate=bf(inp["pgate"][b]),
+                                         norm_w=inp["nw"], rope_cs=cs)
+        ik = compress.compress_contract(bf(inp["ikv"][b]), bf(inp["igate"][b]), inp["iape"], r, True,
+                                        prev_kv=bf(inp["ipkv"][b]), prev_gate=bf(inp["ipgate"][b]),
+                                        norm_w=inp["inw"], rope_cs=cs)
+        k_hat = codecs.decode_pagesplit(self.keys[b], 128)
+        k_hat[n - 1] = codecs.fp8_decode(*codecs.fp8_encode(ik))[0]
+        top, _ = indexer.index_topk(bf(inp["q_idx"][b]), inp["w"][b], k_hat, int(wl.ctx_len[b]), r, wl.k, True)
+        pages = self.main_pages[b]
+
+        def rows(ids):
+            out = np.empty((len(ids), 512))
+            for i, j in enumerate(ids):
+                j = int(j)
+                if j == n - 1:
+                    out[i] = codecs.decode_rows(codecs.encode_rows(ent, codecs.FMT_FP8), codecs.FMT_FP8, 512)[0]
+                else:
+                    out[i] = codecs.decode_rows(pages[j // 64][j % 64:j % 64 + 1], codecs.FMT_FP8, 512)[0]
+            return out
+
+        swa_dec = codecs.decode_rows(self.swa[b], codecs.FMT_FP8, 512)
+        return attention.request_attention(bf(inp["q"][b]), int(wl.ctx_len[b]), r, swa_dec, rows, top,
+                                           inp["sink"], 512 ** -0.5)
+
+
+def cores_used():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args):
+    wl = synth.workload(WORKLOAD)
+    nreq = min(wl.B, max(1, args.steps))
+    runner = OracleRunner(wl, range(nreq))
+    for i in range(args.warmup):
+        runner.query(i % nreq)
+    times = []
+    for i in range(args.steps):
+        t0 = time.perf_counter()
+        runner.query(i % nreq)
+        times.append(time.perf_counter() - t0)
+    per = statistics.mean(times)
+    value = 1.0 / per
+    sample = "one 1M-context query (one request of the batch) per step, %d distinct requests" % nreq
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "queries/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (f32 for the compressor contract)",
+        "data": "synthetic", "config": {"workload": workload_desc(wl)},
+        "cpu_baseline": {"value": value, "unit": "queries/s", "cores": cores_used(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def cpu_baseline_sample():
+    """The oracle timed on a bounded sample (2 queries) of the benchmark workload."""
+    wl = synth.workload(WORKLOAD)
+    runner = OracleRunner(wl, [0, 1])
+    t0 = time.perf_counter()
+    for b in (0, 1):
+        runner.query(b)
+    dt = time.perf_counter() - t0
+    return {"value": 2.0 / dt, "unit": "queries/s", "cores": cores_used(), "kind": "oracle",
+            "sample": "2 of the 8 queries of one batch (requests 0 and 1), full 1M context each; "
+                      "numpy, BLAS threads for the score product"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["cskv", "reference"], default="cskv")
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)))
+        return
+
+    import torch
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    res = run_gpu(args, rank, world)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline_sample()
+        print(json.dumps(res))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -81,6 +81,14 @@ def set_spin_limit(cycles):
     _lib.lib().cskv_set_spin_limit(int(cycles))
 
 
+def set_timing_events(begin, end):
+    """Record torch.cuda.Event `begin`/`end` around every later indexer score kernel (None, None: off)."""
+    if begin is None or end is None:
+        _lib.lib().cskv_set_timing_events(None, None)
+    else:
+        _lib.lib().cskv_set_timing_events(begin.cuda_event, end.cuda_event)
+
+
 class PagedCache:
     """A paged cache: `pool` uint8 [num_pages, page_bytes] on the GPU and an int32
     block table [batch, max_pages] (or None for a flat array of rows)."""

@@ -33,6 +33,7 @@ SIGNATURES = {
     "cskv_version": (c_int32, []),
     "cskv_device_status": (c_int32, [c_void_p]),
     "cskv_set_spin_limit": (None, [ctypes.c_uint64]),
+    "cskv_set_timing_events": (None, [c_void_p, c_void_p]),
     "cskv_encode_rows": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, Paged,
                                    c_void_p]),
     "cskv_compress": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_float,

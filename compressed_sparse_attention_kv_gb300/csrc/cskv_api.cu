@@ -11,6 +11,19 @@ namespace cskv {
 static std::atomic<unsigned long long> g_spin_limit{kDefaultSpinLimit};
 unsigned long long spin_limit() { return g_spin_limit.load(std::memory_order_relaxed); }
 
+static std::atomic<void*> g_ev_begin{nullptr}, g_ev_end{nullptr};
+void timing_events(cudaEvent_t* begin, cudaEvent_t* end) {
+  *begin = static_cast<cudaEvent_t>(g_ev_begin.load(std::memory_order_relaxed));
+  *end = static_cast<cudaEvent_t>(g_ev_end.load(std::memory_order_relaxed));
+}
+void record_timing_event(cudaEvent_t ev, cudaStream_t stream) {
+  if (ev == nullptr) return;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaStreamIsCapturing(stream, &cs);
+  cudaEventRecordWithFlags(ev, stream,
+                           cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault);
+}
+
 static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 static int32_t cuda_status(cudaError_t e) { return e == cudaSuccess ? CSKV_OK : CSKV_ERR_CUDA; }
@@ -62,6 +75,12 @@ int32_t cskv_version(void) { return 100; }
 
 void cskv_set_spin_limit(uint64_t cycles) {
   g_spin_limit.store(cycles == 0 ? kDefaultSpinLimit : cycles, std::memory_order_relaxed);
+}
+
+void cskv_set_timing_events(void* begin, void* end) {
+  const bool on = begin != nullptr && end != nullptr;
+  g_ev_begin.store(on ? begin : nullptr, std::memory_order_relaxed);
+  g_ev_end.store(on ? end : nullptr, std::memory_order_relaxed);
 }
 
 int32_t cskv_device_status(void* stream) {

@@ -742,6 +742,9 @@ cudaError_t launch_index_topk(const void* q_idx, const float* w, const cskv_page
   if (e != cudaSuccess) return e;
 
   const int grid = sm_count();
+  cudaEvent_t ev_begin, ev_end;
+  timing_events(&ev_begin, &ev_end);
+  record_timing_event(ev_begin, stream);
   if (a.fp8) {
     const size_t smem = score_smem_bytes<1>();
     cudaFuncSetAttribute(index_score_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
@@ -752,6 +755,7 @@ cudaError_t launch_index_topk(const void* q_idx, const float* w, const cskv_page
     index_score_kernel<0><<<grid, kScoreThreads, smem, stream>>>(tmap, a);
   }
   e = cudaGetLastError();
+  record_timing_event(ev_end, stream);
   if (e != cudaSuccess) return e;
 
   dim3 g1((a.L.n_pad + kSelChunk - 1) / kSelChunk, B);

@@ -13,6 +13,9 @@ namespace cskv {
 // default bound of every mbarrier spin-wait, in SM cycles (about 1 s at 2 GHz)
 constexpr unsigned long long kDefaultSpinLimit = 1ull << 31;
 unsigned long long spin_limit();
+// measurement hook around the indexer score kernel (may be null)
+void timing_events(cudaEvent_t* begin, cudaEvent_t* end);
+void record_timing_event(cudaEvent_t ev, cudaStream_t stream);
 
 cudaError_t launch_compress(const void* kv, const void* gate, const void* prev_kv,
                             const void* prev_gate, const float* ape, const float* norm_w, float eps,

@@ -105,6 +105,14 @@ CSKV_API int32_t cskv_device_status(void* stream);
  * 0 restores the default.  Applies to launches made after the call. */
 CSKV_API void cskv_set_spin_limit(uint64_t cycles);
 
+/* Measurement hook.  With both non-NULL (cudaEvent_t handles passed as void*),
+ * every later cskv_index_topk call records `begin` right before and `end` right
+ * after its score kernel - the pass that streams the index keys - on the call's
+ * stream; inside a stream capture they become external event-record nodes, so a
+ * replayed CUDA graph records them on every replay.  NULL, NULL turns it off.
+ * Process-wide; meant for benchmarks, not for concurrent use. */
+CSKV_API void cskv_set_timing_events(void* begin, void* end);
+
 /* ------------------------------------------------------------------------
  * cskv_encode_rows: code rows of values into a cache.
  * Row i of src (fp32 or bf16, [n, dim] row-major) is coded in dst.fmt and
