@@ -372,26 +372,24 @@ class OracleRunner:
             vals = synth.request_values(wl, b, "index")
             self.keys[b] = codecs.encode_pagesplit(vals)
             self.swa[b] = codecs.encode_rows(synth.swa_values(wl, b), codecs.FMT_FP8)
-            # the main pages this request's selection will read, coded ahead (cache preparation)
-            top = self._select(b)
-            pages = sorted(set(int(j) // 64 for j in top if j >= 0) | {(int(wl.n_entries[b]) - 1) // 64})
+            # cache preparation (untimed): code the main pages this request's selection reads
+            ent, ik = self._compress(b)
+            top = self._topk(b, ik)
+            pages = sorted(set(int(j) // 64 for j in top if j >= 0))
             self.main_pages[b] = {p: codecs.encode_rows(synth.main_page_values(wl, b, p), codecs.FMT_FP8)
                                   for p in pages}
 
-    def _select(self, b):
-        from oracle import codecs, indexer
-        k_hat = codecs.decode_pagesplit(self.keys[b], 128)
-        top, _ = indexer.index_topk(self.inp["q_idx"][b], self.inp["w"][b], k_hat, int(self.wl.ctx_len[b]),
-                                    self.wl.ratio, self.wl.k, True)
-        return top
+    @staticmethod
+    def _bf(x):
+        from oracle import codecs
+        return codecs.bf16_decode(codecs.bf16_encode(x)).astype(np.float32)
 
-    def query(self, b):
-        """compress (main + index key of the completed block), index_topk, attention for request b."""
-        from oracle import attention, codecs, compress, indexer, rope
-        wl, inp = self.wl, self.inp
+    def _compress(self, b):
+        """The completed block's main entry and index key (fp32 contract)."""
+        from oracle import compress, rope
+        wl, inp, bf = self.wl, self.inp, self._bf
         r = wl.ratio
         n = int(wl.n_entries[b])
-        bf = lambda x: codecs.bf16_decode(codecs.bf16_encode(x)).astype(np.float32)  # noqa: E731
         cs = rope.table(np.array([(n - 1) * r]))
         ent = compress.compress_contract(bf(inp["kv"][b]), bf(inp["gate"][b]), inp["ape"], r, True,
                                          prev_kv=bf(inp["pkv"][b]), prev_gate=bf(inp["pgate"][b]),
@@ -399,24 +397,41 @@ class OracleRunner:
         ik = compress.compress_contract(bf(inp["ikv"][b]), bf(inp["igate"][b]), inp["iape"], r, True,
                                         prev_kv=bf(inp["ipkv"][b]), prev_gate=bf(inp["ipgate"][b]),
                                         norm_w=inp["inw"], rope_cs=cs)
+        return ent, ik
+
+    def _topk(self, b, ik):
+        from oracle import codecs, indexer
+        wl, inp = self.wl, self.inp
+        n = int(wl.n_entries[b])
         k_hat = codecs.decode_pagesplit(self.keys[b], 128)
         k_hat[n - 1] = codecs.fp8_decode(*codecs.fp8_encode(ik))[0]
-        top, _ = indexer.index_topk(bf(inp["q_idx"][b]), inp["w"][b], k_hat, int(wl.ctx_len[b]), r, wl.k, True)
+        top, _ = indexer.index_topk(self._bf(inp["q_idx"][b]), inp["w"][b], k_hat, int(wl.ctx_len[b]),
+                                    wl.ratio, wl.k, True)
+        return top
+
+    def query(self, b):
+        """compress (main + index key of the completed block), index_topk, attention for request b."""
+        from oracle import attention, codecs
+        wl, inp = self.wl, self.inp
+        n = int(wl.n_entries[b])
+        ent, ik = self._compress(b)
+        top = self._topk(b, ik)
         pages = self.main_pages[b]
+        ent_row = codecs.decode_rows(codecs.encode_rows(ent, codecs.FMT_FP8), codecs.FMT_FP8, 512)[0]
 
         def rows(ids):
             out = np.empty((len(ids), 512))
             for i, j in enumerate(ids):
                 j = int(j)
                 if j == n - 1:
-                    out[i] = codecs.decode_rows(codecs.encode_rows(ent, codecs.FMT_FP8), codecs.FMT_FP8, 512)[0]
+                    out[i] = ent_row
                 else:
                     out[i] = codecs.decode_rows(pages[j // 64][j % 64:j % 64 + 1], codecs.FMT_FP8, 512)[0]
             return out
 
         swa_dec = codecs.decode_rows(self.swa[b], codecs.FMT_FP8, 512)
-        return attention.request_attention(bf(inp["q"][b]), int(wl.ctx_len[b]), r, swa_dec, rows, top,
-                                           inp["sink"], 512 ** -0.5)
+        return attention.request_attention(self._bf(inp["q"][b]), int(wl.ctx_len[b]), wl.ratio, swa_dec, rows,
+                                           top, inp["sink"], 512 ** -0.5)
 
 
 def cores_used():
@@ -490,7 +505,10 @@ def main():
     res = run_gpu(args, rank, world)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
-            res["cpu_baseline"] = cpu_baseline_sample()
+            try:
+                res["cpu_baseline"] = cpu_baseline_sample()
+            except Exception as e:  # report the GPU line even if the CPU leg fails
+                res["cpu_baseline"] = {"value": None, "error": repr(e)[:200]}
         print(json.dumps(res))
     if world > 1:
         torch.distributed.destroy_process_group()
