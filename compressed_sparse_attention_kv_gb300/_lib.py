@@ -42,6 +42,8 @@ SIGNATURES = {
     "cskv_index_topk_workspace_size": (c_size_t, [c_int32, c_int32, c_int32, c_int32, c_int32]),
     "cskv_index_topk": (c_int32, [c_void_p, c_void_p, Paged, c_void_p, c_int32, c_int32, c_int32,
                                   c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "cskv_index_topk_noalloc": (c_int32, [c_void_p, c_void_p, Paged, c_void_p, c_int32, c_int32, c_int32,
+                                          c_int32, c_int32, c_void_p, c_void_p, c_void_p]),
     "cskv_sparse_decode_attn_workspace_size": (c_size_t, [c_int32, c_int32, c_int32, c_int32, c_int32]),
     "cskv_sparse_decode_attn": (c_int32, [c_void_p, Paged, c_void_p, c_int32, c_void_p, c_void_p,
                                           c_int32, c_int32, c_int32, c_void_p, c_float, c_void_p,

@@ -154,6 +154,25 @@ int32_t cskv_index_topk(const void* q_idx, const float* w, cskv_paged keys, cons
                                        static_cast<cudaStream_t>(stream)));
 }
 
+int32_t cskv_index_topk_noalloc(const void* q_idx, const float* w, cskv_paged keys,
+                                const int32_t* ctx_len, int32_t B, int32_t Hi, int32_t ratio,
+                                int32_t k, int32_t max_ctx_len, int32_t* topk_idx, float* topk_score,
+                                void* stream) {
+  if (q_idx == nullptr || w == nullptr || ctx_len == nullptr || topk_idx == nullptr)
+    return CSKV_ERR_INVALID;
+  if (B < 1 || Hi < 1 || ratio < 1 || k < 1 || k > 2048 || max_ctx_len < 0) return CSKV_ERR_INVALID;
+  if (Hi > 64) return CSKV_ERR_UNSUPPORTED;
+  if (!aligned(q_idx, 16) || !aligned(w, 4)) return CSKV_ERR_INVALID;
+  if (!paged_ok(keys, 128, (1u << CSKV_FMT_BF16) | (1u << CSKV_FMT_FP8_E4M3_E8M0_B32_PAGESPLIT)))
+    return CSKV_ERR_INVALID;
+  if (keys.block_table == nullptr) return CSKV_ERR_INVALID;
+  // the whole workspace must fit in the library's fixed scratch array
+  if (index_workspace_bytes(B, max_ctx_len / ratio, Hi, k) > CSKV_NOALLOC_SCRATCH_BYTES)
+    return CSKV_ERR_INVALID;
+  return cuda_status(launch_index_topk_noalloc(q_idx, w, keys, ctx_len, B, Hi, ratio, k, max_ctx_len,
+                                               topk_idx, topk_score, static_cast<cudaStream_t>(stream)));
+}
+
 size_t cskv_sparse_decode_attn_workspace_size(int32_t B, int32_t H, int32_t max_ctx_len,
                                               int32_t ratio, int32_t k) {
   if (B <= 0 || H <= 0 || max_ctx_len < 0 || ratio < 1) return 0;

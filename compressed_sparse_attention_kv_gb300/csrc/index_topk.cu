@@ -26,6 +26,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <mutex>
+
 #include "codec.cuh"
 #include "internal.h"
 
@@ -768,5 +770,46 @@ cudaError_t launch_index_topk(const void* q_idx, const float* w, const cskv_page
 }
 
 unsigned int take_err_index() { return take_dev_err(); }
+
+// ---------------------------------------------------------------------------
+// Scratch for cskv_index_topk_noalloc: callers that cannot allocate device
+// memory get the indexer's workspace from this fixed array instead.  It lives
+// in every GPU context that loads the library, for the life of the process.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) uint8_t g_noalloc_scratch[CSKV_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch on the current device.  Host code must not
+// use the symbol itself (it is a host-side stand-in, not a device address); the
+// address is looked up once per device, with that device current, and cached.
+static void* noalloc_scratch_address(cudaError_t* err) {
+  static std::mutex mu;
+  static void* addr[256] = {};
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= 256) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (*err != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+cudaError_t launch_index_topk_noalloc(const void* q_idx, const float* w, const cskv_paged& keys,
+                                      const int32_t* ctx_len, int B, int Hi, int ratio, int k,
+                                      int max_ctx_len, int32_t* topk_idx, float* topk_score,
+                                      cudaStream_t stream) {
+  cudaError_t err = cudaSuccess;
+  void* scratch = noalloc_scratch_address(&err);
+  if (scratch == nullptr) return err;
+  return launch_index_topk(q_idx, w, keys, ctx_len, B, Hi, ratio, k, max_ctx_len, topk_idx, topk_score,
+                           scratch, stream);
+}
 
 }  // namespace cskv

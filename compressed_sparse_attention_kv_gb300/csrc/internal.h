@@ -33,6 +33,11 @@ cudaError_t launch_index_topk(const void* q_idx, const float* w, const cskv_page
                               int max_ctx_len, int32_t* topk_idx, float* topk_score,
                               void* workspace, cudaStream_t stream);
 
+cudaError_t launch_index_topk_noalloc(const void* q_idx, const float* w, const cskv_paged& keys,
+                                      const int32_t* ctx_len, int B, int Hi, int ratio, int k,
+                                      int max_ctx_len, int32_t* topk_idx, float* topk_score,
+                                      cudaStream_t stream);
+
 size_t attn_workspace_bytes(int B, int H, int max_ctx, int ratio, int k);
 cudaError_t launch_sparse_decode_attn(const void* q, const cskv_paged& kv, const void* swa, int swa_fmt,
                                       const int32_t* ctx_len, const int32_t* topk, int k, int ratio,

@@ -189,6 +189,34 @@ CSKV_API int32_t cskv_index_topk(const void* q_idx, const float* w, cskv_paged k
                         void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * cskv_index_topk_noalloc: cskv_index_topk for callers that cannot allocate
+ * device memory.  The paper has no counterpart: this is a deployment variant.
+ * Same arguments, results and bits as cskv_index_topk, minus the workspace.
+ * Some callers cannot call cudaMalloc: code that runs while a stream is being
+ * captured into a CUDA graph (allocation is not a stream operation and may
+ * synchronise the device), plugins inside hosts that own every byte of device
+ * memory and expose no allocator, and latency-critical threads that must never
+ * block on the driver.  They get the workspace from a fixed array inside the
+ * library instead: CSKV_NOALLOC_SCRATCH_BYTES (32 MiB) of device memory that
+ * every GPU which loads the library holds until the process exits.  Sizes
+ * whose workspace (cskv_index_topk_workspace_size) would exceed it are
+ * rejected with CSKV_ERR_INVALID before anything is launched - about 2.6
+ * million visible entries in total over the batch, e.g. 8 requests at 1M tokens.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Every call uses the same array and leaves its last contents
+ * behind; each call clears what must start at zero itself, but calls whose
+ * kernels overlap on the GPU (different streams, or graphs replayed
+ * concurrently) race on the array and give wrong results.  The call allocates
+ * nothing: no cudaMalloc, no cudaFree.
+ * ------------------------------------------------------------------------ */
+#define CSKV_NOALLOC_SCRATCH_BYTES (32u << 20)
+CSKV_API int32_t cskv_index_topk_noalloc(const void* q_idx, const float* w, cskv_paged keys,
+                                         const int32_t* ctx_len, int32_t B, int32_t Hi,
+                                         int32_t ratio, int32_t k, int32_t max_ctx_len,
+                                         int32_t* topk_idx, float* topk_score, void* stream);
+
+/* ------------------------------------------------------------------------
  * cskv_sparse_decode_attn: shared-KV decode attention over the sliding window
  * and the compressed entries in one softmax with a sink ("DeepSeek-V4 deep
  * dive", section 3.1 "K = V, one head", section 3.3 partial RoPE with the
