@@ -199,7 +199,7 @@ def run_gpu(args, rank, world):
         cskv.sparse_decode_attn(d["q"], main, swa, cskv.FMT_FP8, d["ctx"], topk, k, r, L, sink,
                                 cskv.DEFAULT_SCALE, d["qcs"], out=out, workspace=ws_a)
 
-    launches_per_step = 2 + 4 + 2
+    launches_per_step = 2 + 2 + 2   # compressor x2, indexer prep + fused score/select, attention tiles + combine
     for _ in range(max(1, args.warmup)):
         step()
     torch.cuda.synchronize()

@@ -95,7 +95,21 @@ __device__ __forceinline__ void store_row_values(const float4& y, int lt, int fm
     }
     return;
   }
-  // FP8 (inline or page-split): blocks of 32 channels = 8 threads
+  if (fmt == CSKV_FMT_FP8_E4M3_ROWSCALE_PAGESPLIT) {
+    // index key: one power-of-two scale for the whole row (the group is one warp at dim 128)
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(full, amax, o));
+    const int e = e8m0_exponent(amax);
+    const float inv = exp2i(-e);
+    const uint32_t codes = e4m3x2(__fmul_rn(y.x, inv), __fmul_rn(y.y, inv)) |
+                           (e4m3x2(__fmul_rn(y.z, inv), __fmul_rn(y.w, inv)) << 16);
+    if (valid) {
+      *reinterpret_cast<uint32_t*>(dst.data + 4 * lt) = codes;
+      if (lt == 0) *reinterpret_cast<float*>(dst.scale) = exp2i(e);
+    }
+    return;
+  }
+  // FP8 inline rows: blocks of 32 channels = 8 threads
   amax = fmaxf(amax, __shfl_xor_sync(full, amax, 1));
   amax = fmaxf(amax, __shfl_xor_sync(full, amax, 2));
   amax = fmaxf(amax, __shfl_xor_sync(full, amax, 4));

@@ -52,8 +52,8 @@ size_t cskv_row_bytes(int32_t fmt, int32_t dim) {
   if (dim != 128 && dim != 512) return 0;
   switch (fmt) {
     case CSKV_FMT_BF16: return 2u * dim;
-    case CSKV_FMT_FP8_E4M3_E8M0_B32:
-    case CSKV_FMT_FP8_E4M3_E8M0_B32_PAGESPLIT: return dim + dim / 32;
+    case CSKV_FMT_FP8_E4M3_E8M0_B32: return dim + dim / 32;
+    case CSKV_FMT_FP8_E4M3_ROWSCALE_PAGESPLIT: return dim + 4;
     case CSKV_FMT_FP4_E2M1_E4M3_B16: return dim / 2 + dim / 16;
     default: return 0;
   }
@@ -98,7 +98,7 @@ int32_t cskv_encode_rows(const void* src, int32_t src_is_bf16, int32_t n, int32_
   if (n < 0 || (dim != 128 && dim != 512)) return CSKV_ERR_INVALID;
   if (n > 0 && (src == nullptr || !aligned(src, 16))) return CSKV_ERR_INVALID;
   if (!paged_ok(dst, dim, 0xFu)) return CSKV_ERR_INVALID;
-  if (dst.fmt == CSKV_FMT_FP8_E4M3_E8M0_B32_PAGESPLIT && dim != 128) return CSKV_ERR_INVALID;
+  if (dst.fmt == CSKV_FMT_FP8_E4M3_ROWSCALE_PAGESPLIT && dim != 128) return CSKV_ERR_INVALID;
   return cuda_status(launch_encode_rows(src, src_is_bf16 != 0, n, dim, dst_req, dst_row, dst,
                                         static_cast<int>(cskv_row_bytes(dst.fmt, dim)),
                                         static_cast<cudaStream_t>(stream)));
@@ -121,7 +121,7 @@ int32_t cskv_compress(const void* kv, const void* gate, const void* prev_kv, con
   if (prev_kv && (!aligned(prev_kv, 8) || !aligned(prev_gate, 8))) return CSKV_ERR_INVALID;
   if ((norm_w && !aligned(norm_w, 16)) || (rope_cs && !aligned(rope_cs, 16))) return CSKV_ERR_INVALID;
   if (!paged_ok(out, dim, 0xFu)) return CSKV_ERR_INVALID;
-  if (out.fmt == CSKV_FMT_FP8_E4M3_E8M0_B32_PAGESPLIT && dim != 128) return CSKV_ERR_INVALID;
+  if (out.fmt == CSKV_FMT_FP8_E4M3_ROWSCALE_PAGESPLIT && dim != 128) return CSKV_ERR_INVALID;
   return cuda_status(launch_compress(kv, gate, prev_kv, prev_gate, ape, norm_w, eps, rope_cs, S, T,
                                      ratio, overlap, dim, req, first_entry, out,
                                      static_cast<int>(cskv_row_bytes(out.fmt, dim)),
@@ -143,7 +143,7 @@ int32_t cskv_index_topk(const void* q_idx, const float* w, cskv_paged keys, cons
   if (B < 1 || Hi < 1 || ratio < 1 || k < 1 || k > 2048 || max_ctx_len < 0) return CSKV_ERR_INVALID;
   if (Hi > 64) return CSKV_ERR_UNSUPPORTED;
   if (!aligned(q_idx, 16) || !aligned(w, 4)) return CSKV_ERR_INVALID;
-  if (!paged_ok(keys, 128, (1u << CSKV_FMT_BF16) | (1u << CSKV_FMT_FP8_E4M3_E8M0_B32_PAGESPLIT)))
+  if (!paged_ok(keys, 128, (1u << CSKV_FMT_BF16) | (1u << CSKV_FMT_FP8_E4M3_ROWSCALE_PAGESPLIT)))
     return CSKV_ERR_INVALID;
   if (keys.block_table == nullptr) return CSKV_ERR_INVALID;
   const size_t need = index_workspace_bytes(B, max_ctx_len / ratio, Hi, k);
@@ -163,7 +163,7 @@ int32_t cskv_index_topk_noalloc(const void* q_idx, const float* w, cskv_paged ke
   if (B < 1 || Hi < 1 || ratio < 1 || k < 1 || k > 2048 || max_ctx_len < 0) return CSKV_ERR_INVALID;
   if (Hi > 64) return CSKV_ERR_UNSUPPORTED;
   if (!aligned(q_idx, 16) || !aligned(w, 4)) return CSKV_ERR_INVALID;
-  if (!paged_ok(keys, 128, (1u << CSKV_FMT_BF16) | (1u << CSKV_FMT_FP8_E4M3_E8M0_B32_PAGESPLIT)))
+  if (!paged_ok(keys, 128, (1u << CSKV_FMT_BF16) | (1u << CSKV_FMT_FP8_E4M3_ROWSCALE_PAGESPLIT)))
     return CSKV_ERR_INVALID;
   if (keys.block_table == nullptr) return CSKV_ERR_INVALID;
   // the whole workspace must fit in the library's fixed scratch array

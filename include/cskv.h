@@ -66,10 +66,12 @@ typedef enum {
    * then dim/16 float8_e4m3 scale codes (scale j covers channels 16j..16j+15):
    * 288 B at 512, inline per row.  "DeepSeek-V4.1-Flash" diagram, MXFP4. */
   CSKV_FMT_FP4_E2M1_E4M3_B16 = 2,
-  /* the FP8 codes of format 1, but each 64-row page stores its 64 data rows
-   * (dim bytes each) first and then its 64 scale rows (dim/32 bytes each):
-   * 132 B per 128-d index key, 8,448 B per page.  Index keys only. */
-  CSKV_FMT_FP8_E4M3_E8M0_B32_PAGESPLIT = 3
+  /* index keys: dim float8_e4m3 codes with one scale for the whole row, stored
+   * as the fp32 value of a power of two (the rounding rules of format 1 with a
+   * block of dim values): dim + 4 bytes, 132 B per 128-d key (the size of the
+   * V3.2 index key).  Each 64-row page stores its 64 code rows first (dim bytes
+   * each), then its 64 fp32 scales: 8,448 B per page.  Index keys only. */
+  CSKV_FMT_FP8_E4M3_ROWSCALE_PAGESPLIT = 3
 } cskv_format;
 
 /* A paged cache (or, with block_table == NULL, a flat array of rows in which
@@ -172,8 +174,9 @@ CSKV_API int32_t cskv_compress(const void* kv, const void* gate,
  * smaller entry index), in ascending entry order, -1 after them.
  * q_idx: bf16 [B, Hi, 128] device (post-RoPE).  w: fp32 [B, Hi] device (final
  * head weights, any scale included).  keys: 128-d index keys, format
- * FP8_..._PAGESPLIT (queries are then coded e4m3 with one e8m0 scale per head
- * and the products run on the FP8 tensor cores) or BF16.  ctx_len: int32 [B]
+ * FP8_E4M3_ROWSCALE_PAGESPLIT (queries are then coded e4m3 with one power-of-two
+ * scale per head, the products run on the FP8 tensor cores and each key's scale
+ * multiplies its weighted sum) or BF16.  ctx_len: int32 [B]
  * device, each <= max_ctx_len.  Hi in [1, 64]; k in [1, 2048].
  * topk_score: optional fp32 [B, k] (NULL to skip): the kernel's fp32 score of
  * each selected entry (-inf after the selection).

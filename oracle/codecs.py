@@ -21,11 +21,13 @@ Readings where the pages are silent (all stated in the design doc):
   also when the magnitude rounds to zero; NaN codes are never produced.
 * FP4 scale: s = RNE_e4m3(amax / 6) (fp32 division); a zero scale zeroes the
   whole block.  Channel 2i sits in the low nibble of byte i.
-* FP8 index keys (128-d) use the same codes: 128 e4m3 + 4 e8m0 = 132 bytes
-  per key, and in a 64-row page all 64 data rows come first, then the 64
-  scale rows ("page-split"), so the data rows form one dense 8 KiB tile.
-* Query rows of the FP8 indexer are coded with the same rule but one scale
-  per head (block 128).
+* FP8 index keys (128-d): 128 e4m3 codes and one scale for the whole key,
+  stored as the fp32 value of its power of two - 132 bytes per key, the size
+  of the V3.2 index key - with the same rounding rules (the block is the 128
+  values); in a 64-row page all 64 data rows come first, then the 64 fp32
+  scales ("page-split"), so the data rows form one dense 8 KiB tile.
+* Query rows of the FP8 indexer are coded with the same rule, one scale per
+  head (block 128).
 
 Everything here is elementwise numpy on exactly representable values; fp32
 steps are done in np.float32 (IEEE, round-to-nearest-even).
@@ -194,7 +196,7 @@ def fp4_decode(packed, scales, block=16):
 FMT_BF16 = 0
 FMT_FP8 = 1            # e4m3 data then e8m0 per 32, inline per row
 FMT_FP4 = 2            # packed e2m1 data then e4m3 per 16, inline per row
-FMT_FP8_PAGESPLIT = 3  # FP8 codes; each 64-row page holds 64 data rows, then 64 scale rows
+FMT_FP8_PAGESPLIT = 3  # index keys: e4m3 codes + one fp32 power-of-two scale per row, page-split
 
 PAGE_ROWS = 64
 
@@ -202,8 +204,10 @@ PAGE_ROWS = 64
 def row_bytes(fmt, dim):
     if fmt == FMT_BF16:
         return 2 * dim
-    if fmt in (FMT_FP8, FMT_FP8_PAGESPLIT):
+    if fmt == FMT_FP8:
         return dim + dim // 32
+    if fmt == FMT_FP8_PAGESPLIT:
+        return dim + 4
     if fmt == FMT_FP4:
         return dim // 2 + dim // 16
     raise ValueError(fmt)
@@ -236,22 +240,24 @@ def decode_rows(b, fmt, dim):
 
 
 def encode_pagesplit(x):
-    """x [64*p, D] float32 -> bytes [p, 64*(D + D/32)]: per page 64 data rows, then 64 scale rows."""
+    """Index keys x [64*p, D] float32 -> bytes [p, 64*(D + 4)]: per page 64 rows of e4m3
+    codes (one power-of-two scale per row), then the 64 scales as fp32."""
     x = np.asarray(x, dtype=np.float32)
     n, D = x.shape
     assert n % PAGE_ROWS == 0
-    c, s = fp8_encode(x)
+    c, e = fp8_encode(x, block=D)                       # e: scale bytes [n, 1]
+    scale = _pow2_f32(e[:, 0].astype(np.int64) - 127)    # exact powers of two
     p = n // PAGE_ROWS
-    return np.concatenate([c.reshape(p, -1), s.reshape(p, -1)], axis=-1)
+    return np.concatenate([c.reshape(p, -1), scale.view(np.uint8).reshape(p, -1)], axis=-1)
 
 
 def decode_pagesplit(pages, dim):
-    """bytes [p, 64*(D + D/32)] -> float64 [64*p, D]."""
+    """bytes [p, 64*(D + 4)] -> float64 [64*p, D]."""
     pages = np.asarray(pages, dtype=np.uint8)
     p = pages.shape[0]
     c = pages[:, :PAGE_ROWS * dim].reshape(p * PAGE_ROWS, dim)
-    s = pages[:, PAGE_ROWS * dim:].reshape(p * PAGE_ROWS, dim // 32)
-    return fp8_decode(c, s)
+    sc = np.ascontiguousarray(pages[:, PAGE_ROWS * dim:PAGE_ROWS * (dim + 4)]).view(np.float32).reshape(-1)
+    return e4m3_decode(c) * sc.astype(np.float64)[:, None]
 
 
 def encode_q_perhead(q):

@@ -85,7 +85,7 @@ class HostPaged:
         for p in range((n + PAGE - 1) // PAGE):
             pg = pool_bytes[self.block_table[b, p]]
             if self.fmt == codecs.FMT_FP8_PAGESPLIT:
-                out.append(pg[:PAGE * (self.dim + self.dim // 32)])
+                out.append(pg[:PAGE * (self.dim + 4)])
             else:
                 out.append(pg[:PAGE * rb].reshape(PAGE, rb))
         return out

@@ -134,11 +134,19 @@ def test_fp4_rows_roundtrip():
 
 def test_pagesplit_roundtrip():
     rs = np.random.default_rng(4)
-    x = rs.standard_normal((128, 128)).astype(np.float32)
+    x = (rs.standard_normal((128, 128)) * np.exp2(rs.integers(-10, 10, (128, 1)))).astype(np.float32)
+    x[3] = 0.0
     pages = codecs.encode_pagesplit(x)
     assert pages.shape == (2, 64 * 132)
-    assert np.array_equal(codecs.decode_pagesplit(pages, 128), codecs.decode_rows(
-        codecs.encode_rows(x, codecs.FMT_FP8), codecs.FMT_FP8, 128))
+    dec = codecs.decode_pagesplit(pages, 128)
+    # same codes as the block-128 FP8 rule, the scale kept as an fp32 power of two
+    c, e = codecs.fp8_encode(x, block=128)
+    assert np.array_equal(dec, codecs.e4m3_decode(c) * codecs.e8m0_decode(e))
+    sc = np.ascontiguousarray(pages[:, 64 * 128:]).view(np.float32).reshape(-1)
+    assert np.array_equal(np.log2(sc), np.round(np.log2(sc)))
+    amax = np.abs(x).max(-1)
+    nz = amax > 0
+    assert np.all((amax[nz] / sc[nz] > 224) & (amax[nz] / sc[nz] <= 448)) and sc[3] == 1.0
 
 
 def test_byte_layouts(golden):
