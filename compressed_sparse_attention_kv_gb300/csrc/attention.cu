@@ -102,11 +102,37 @@ __device__ __forceinline__ void put16(uint8_t* tile, int row, int l, const float
   *reinterpret_cast<uint4*>(base + sw128_offset(row, c0 + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
-__device__ __forceinline__ void dequant16(int fmt, const uint8_t* row, int l, float (&v)[16]) {
+// Raw bytes lane l needs from one row: codes (16 B FP8 / 8 B FP4 / 32 B bf16) and
+// its scale byte.  Split from the conversion so a warp can issue the loads of
+// several rows before it converts any of them.
+struct RowBytes {
+  uint4 lo, hi;
+  uint32_t scb;
+};
+
+__device__ __forceinline__ RowBytes load16(int fmt, const uint8_t* row, int l) {
+  RowBytes r;
+  r.hi = make_uint4(0u, 0u, 0u, 0u);
   if (fmt == CSKV_FMT_FP8_E4M3_E8M0_B32) {
-    const uint4 c = *reinterpret_cast<const uint4*>(row + 16 * l);
-    const float s = exp2i(static_cast<int>(row[kD + (l >> 1)]) - 127);
-    const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+    r.lo = *reinterpret_cast<const uint4*>(row + 16 * l);
+    r.scb = row[kD + (l >> 1)];
+  } else if (fmt == CSKV_FMT_FP4_E2M1_E4M3_B16) {
+    const uint2 c = *reinterpret_cast<const uint2*>(row + 8 * l);
+    r.lo = make_uint4(c.x, c.y, 0u, 0u);
+    r.scb = row[kD / 2 + l];
+  } else {
+    r.lo = *reinterpret_cast<const uint4*>(row + 32 * l);
+    r.hi = *reinterpret_cast<const uint4*>(row + 32 * l + 16);
+    r.scb = 0;
+  }
+  return r;
+}
+
+// Exact dequantisation of lane l's 16 values (dims 16l .. 16l+15) from its raw bytes.
+__device__ __forceinline__ void convert16(int fmt, const RowBytes& r, float (&v)[16]) {
+  if (fmt == CSKV_FMT_FP8_E4M3_E8M0_B32) {
+    const float s = exp2i(static_cast<int>(r.scb) - 127);
+    const uint32_t cw[4] = {r.lo.x, r.lo.y, r.lo.z, r.lo.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       uint32_t h0, h1;
@@ -118,9 +144,8 @@ __device__ __forceinline__ void dequant16(int fmt, const uint8_t* row, int l, fl
       v[4 * i + 3] = __fmul_rn(__half2float(__ushort_as_half(h1 >> 16)), s);
     }
   } else if (fmt == CSKV_FMT_FP4_E2M1_E4M3_B16) {
-    const uint2 c = *reinterpret_cast<const uint2*>(row + 8 * l);
-    const float s = e4m3_to_f32(row[kD / 2 + l]);
-    const uint32_t cw[2] = {c.x, c.y};
+    const float s = e4m3_to_f32(r.scb);
+    const uint32_t cw[2] = {r.lo.x, r.lo.y};
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
 #pragma unroll
@@ -134,9 +159,7 @@ __device__ __forceinline__ void dequant16(int fmt, const uint8_t* row, int l, fl
       }
     }
   } else {
-    const uint4 c0 = *reinterpret_cast<const uint4*>(row + 32 * l);
-    const uint4 c1 = *reinterpret_cast<const uint4*>(row + 32 * l + 16);
-    const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    const uint32_t cw[8] = {r.lo.x, r.lo.y, r.lo.z, r.lo.w, r.hi.x, r.hi.y, r.hi.z, r.hi.w};
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       v[2 * i] = bf16lo(cw[i]);
@@ -150,7 +173,7 @@ struct AttnSmem {
   uint32_t tmem_base;
   float m[kMaxHeadsPerBlock];
   float l[kMaxHeadsPerBlock];
-  int valid[kKeys];
+  const uint8_t* rowp[kKeys];   // address of each key row of the tile, null = no key
 };
 
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnArgs a) {
@@ -181,35 +204,48 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
   }
   if (warp == 0) tmem_alloc(&sm->tmem_base, 512);
 
-  // ---- rows of this tile: validity and address
+  // ---- rows of this tile: one thread per row resolves its address (the list entry,
+  // then the block table), all rows in parallel
+  const int row_fmt = tile == 0 ? a.swa_fmt : a.kv.fmt;
   for (int r = threadIdx.x; r < kKeys; r += blockDim.x) {
-    int v = 0;
+    const uint8_t* p = nullptr;
     if (tile == 0) {
-      v = (t >= kKeys - 1) || (r <= t);
+      if ((t >= kKeys - 1) || (r <= t)) p = a.swa + (size_t(b) * kWindow + r) * a.swa_row_bytes;
     } else {
       const int li = (tile - 1) * kKeys + r;
       if (li < ncomp) {
-        int e = a.topk ? a.topk[size_t(b) * a.k + li] : li;
+        const int e = a.topk ? a.topk[size_t(b) * a.k + li] : li;
         if (e >= 0) {
-          if (e < ctx / a.ratio) v = 1;
+          if (e < ctx / a.ratio) p = paged_row(a.kv, b, e, a.kv_row_bytes).data;
           else set_err(CSKV_ERR_BOUNDS);
         }
       }
     }
-    sm->valid[r] = v;
+    sm->rowp[r] = p;
   }
 
-  // ---- query: rotate the last 64 dims by the query position, store bf16 (K-major, swizzled)
+  // ---- query: rotate the last 64 dims by the query position, store bf16 (K-major,
+  // swizzled).  Items of 8 consecutive dims, eight items' loads in flight per thread.
   {
     const float* cs = a.q_rope + size_t(b) * 64;
-    for (int idx = threadIdx.x; idx < Nq * 64; idx += blockDim.x) {
-      const int h = idx >> 6, g8 = idx & 63;          // 8 consecutive dims per item
-      const int d0 = g8 * 8;
-      uint4 outw = make_uint4(0u, 0u, 0u, 0u);
-      if (h < Hb) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(a.q + ((size_t(b) * a.H + h0 + h) * kD + d0) * 2);
-        float v[8] = {bf16lo(raw.x), bf16hi(raw.x), bf16lo(raw.y), bf16hi(raw.y),
-                      bf16lo(raw.z), bf16hi(raw.z), bf16lo(raw.w), bf16hi(raw.w)};
+    const int items = Nq * 64;
+    for (int i0 = threadIdx.x; i0 < items; i0 += 8 * blockDim.x) {
+      uint4 raw[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int idx = i0 + u * blockDim.x;
+        const int h = idx >> 6, d0 = (idx & 63) * 8;
+        raw[u] = (idx < items && h < Hb)
+                     ? *reinterpret_cast<const uint4*>(a.q + ((size_t(b) * a.H + h0 + h) * kD + d0) * 2)
+                     : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int idx = i0 + u * blockDim.x;
+        if (idx >= items) break;
+        const int h = idx >> 6, d0 = (idx & 63) * 8;
+        float v[8] = {bf16lo(raw[u].x), bf16hi(raw[u].x), bf16lo(raw[u].y), bf16hi(raw[u].y),
+                      bf16lo(raw[u].z), bf16hi(raw[u].z), bf16lo(raw[u].w), bf16hi(raw[u].w)};
         if (d0 >= kD - 64) {
 #pragma unroll
           for (int p = 0; p < 4; ++p) {
@@ -226,40 +262,42 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
           __nv_bfloat162 hh = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
           w[i] = *reinterpret_cast<uint32_t*>(&hh);
         }
-        outw = make_uint4(w[0], w[1], w[2], w[3]);
+        // dims d0..d0+7 -> chunk d0/64, 16-byte chunk (d0%64)/8
+        *reinterpret_cast<uint4*>(qtile + (d0 >> 6) * (Nq * 128) + sw128_offset(h, (d0 & 63) >> 3)) =
+            make_uint4(w[0], w[1], w[2], w[3]);
       }
-      // dims d0..d0+7 -> chunk d0/64, 16-byte chunk (d0%64)/8
-      *reinterpret_cast<uint4*>(qtile + (d0 >> 6) * (Nq * 128) + sw128_offset(h, (d0 & 63) >> 3)) = outw;
     }
   }
   __syncthreads();
 
-  // ---- gather + dequantise the 128 key rows (warp per row, lane = 16 dims)
+  // ---- gather + dequantise the 128 key rows: warp w owns rows w, w+8, ...; lane = 16
+  // dims; the loads of 8 rows are issued before any is converted
   {
-    const int fmt_c = a.kv.fmt;
-    for (int r = warp; r < kKeys; r += kAttnThreads / 32) {
-      float v[16];
-      const uint8_t* row = nullptr;
-      int fmt = fmt_c;
-      if (sm->valid[r]) {
-        if (tile == 0) {
-          row = a.swa + (size_t(b) * kWindow + r) * a.swa_row_bytes;
-          fmt = a.swa_fmt;
+    constexpr int kWarps = kAttnThreads / 32;
+    for (int r0 = warp; r0 < kKeys; r0 += 8 * kWarps) {
+      RowBytes rb[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint8_t* p = sm->rowp[r0 + u * kWarps];
+        if (p != nullptr) {
+          rb[u] = load16(row_fmt, p, lane);
         } else {
-          const int li = (tile - 1) * kKeys + r;
-          const int e = a.topk ? a.topk[size_t(b) * a.k + li] : li;
-          const RowPtr rp = paged_row(a.kv, b, e, a.kv_row_bytes);
-          row = rp.data;
+          rb[u].lo = make_uint4(0u, 0u, 0u, 0u);
+          rb[u].hi = make_uint4(0u, 0u, 0u, 0u);
+          rb[u].scb = 0;
         }
       }
-      if (row != nullptr) {
-        dequant16(fmt, row, lane, v);
-      } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = 0.f;
-        if (lane == 0 && sm->valid[r]) sm->valid[r] = 0;
+      for (int u = 0; u < 8; ++u) {
+        float v[16];
+        if (sm->rowp[r0 + u * kWarps] != nullptr) {
+          convert16(row_fmt, rb[u], v);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = 0.f;
+        }
+        put16(ktile, r0 + u * kWarps, lane, v);
       }
-      put16(ktile, r, lane, v);
     }
   }
   fence_proxy_async_smem();
@@ -286,7 +324,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
   // ---- logits to smem, transposed [head][key]
   if (warp < 4) {
     const int r = warp * 32 + lane;
-    const bool ok = sm->valid[r] != 0;
+    const bool ok = sm->rowp[r] != nullptr;
     for (int c0 = 0; c0 < Nq; c0 += 16) {
       float s[16];
       tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0, s);
@@ -380,20 +418,40 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
   const int ncomp = comp_keys(a, ctx);
   const int ntiles = 1 + (ncomp + kKeys - 1) / kKeys;
   const size_t slot0 = size_t(b) * a.max_tiles * a.H + h;
-  float M = a.sink ? a.sink[h] * 1.4426950408889634f : -INFINITY;
-  for (int s = 0; s < ntiles; ++s) M = fmaxf(M, a.ml[(slot0 + size_t(s) * a.H) * 2]);
-  float L = (a.sink && M != -INFINITY) ? exp2f(a.sink[h] * 1.4426950408889634f - M) : 0.f;
   const int d = 2 * threadIdx.x;
+  // running (max, sum, output) in base 2, started from the sink; tiles taken in
+  // batches of 8 whose loads are all issued before any is used
+  float M = a.sink ? a.sink[h] * 1.4426950408889634f : -INFINITY;
+  float L = a.sink ? 1.f : 0.f;
   float o0 = 0.f, o1 = 0.f;
-  for (int s = 0; s < ntiles; ++s) {
-    const size_t sl = slot0 + size_t(s) * a.H;
-    const float m = a.ml[sl * 2];
-    if (m == -INFINITY) continue;
-    const float f = exp2f(m - M);
-    L += f * a.ml[sl * 2 + 1];
-    const float2 v = *reinterpret_cast<const float2*>(a.opart + sl * kD + d);
-    o0 += f * v.x;
-    o1 += f * v.y;
+  for (int s0 = 0; s0 < ntiles; s0 += 8) {
+    float m[8], l[8];
+    float2 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const size_t sl = slot0 + size_t(s0 + u) * a.H;
+      const bool in = s0 + u < ntiles;
+      m[u] = in ? a.ml[sl * 2] : -INFINITY;
+      l[u] = in ? a.ml[sl * 2 + 1] : 0.f;
+      v[u] = in ? *reinterpret_cast<const float2*>(a.opart + sl * kD + d) : make_float2(0.f, 0.f);
+    }
+    float Mb = M;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) Mb = fmaxf(Mb, m[u]);
+    if (Mb == -INFINITY) continue;
+    const float f = M == -INFINITY ? 0.f : exp2f(M - Mb);
+    L *= f;
+    o0 *= f;
+    o1 *= f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (m[u] == -INFINITY) continue;
+      const float g = exp2f(m[u] - Mb);
+      L += g * l[u];
+      o0 += g * v[u].x;
+      o1 += g * v[u].y;
+    }
+    M = Mb;
   }
   const float inv = L > 0.f ? 1.0f / L : 0.f;
   o0 *= inv;

@@ -134,31 +134,71 @@ __global__ void __launch_bounds__(128) compress_kernel(const CompressArgs a) {
                        __fadd_rn(g.w, b.w));
   };
 
+  // Loads that do not depend on the slots go first, so their latency (and the
+  // req -> block table -> row chain) overlaps the slot loops.
+  RowPtr dst{nullptr, nullptr};
+  if (live) {
+    const long long row = static_cast<long long>(a.first_entry[s]) + i;
+    dst = paged_row(a.out, a.req[s], row, a.out_row_bytes);
+  }
+  const float4 nw = a.norm_w != nullptr ? *reinterpret_cast<const float4*>(a.norm_w + c0)
+                                        : make_float4(1.f, 1.f, 1.f, 1.f);
+  const bool rotate = a.rope_cs != nullptr && live && c0 >= D - 64;
+  const float4 cs = rotate ? *reinterpret_cast<const float4*>(
+                                 a.rope_cs + ((s * a.n + i) * 32 + (c0 - (D - 64)) / 2) * 2)
+                           : make_float4(1.f, 0.f, 1.f, 0.f);
+
+  // Slots are visited in order, eight at a time with all eight slots' loads issued
+  // before any is used; the arithmetic order is the slot order either way.
+  constexpr int kBatch = 8;
   float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
   float4 den = make_float4(0.f, 0.f, 0.f, 0.f);
   if (live) {
     // pass 1: m = max over slots of the biased scores
     float4 m = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-    for (int j = 0; j < slots; ++j) {
-      const uint8_t *vp, *gp;
-      const float* ap;
-      slot_src(j, vp, gp, ap);
-      const float4 sc = score(gp, ap);
-      m.x = fmaxf(m.x, sc.x); m.y = fmaxf(m.y, sc.y); m.z = fmaxf(m.z, sc.z); m.w = fmaxf(m.w, sc.w);
+    for (int j0 = 0; j0 < slots; j0 += kBatch) {
+      float4 sc[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        sc[u] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        if (j0 + u < slots) {
+          const uint8_t *vp, *gp;
+          const float* ap;
+          slot_src(j0 + u, vp, gp, ap);
+          sc[u] = score(gp, ap);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        m.x = fmaxf(m.x, sc[u].x); m.y = fmaxf(m.y, sc[u].y);
+        m.z = fmaxf(m.z, sc[u].z); m.w = fmaxf(m.w, sc[u].w);
+      }
     }
     // pass 2: weights and slot-ordered sums (the scores are recomputed bit for bit)
-    for (int j = 0; j < slots; ++j) {
-      const uint8_t *vp, *gp;
-      const float* ap;
-      slot_src(j, vp, gp, ap);
-      const float4 sc = score(gp, ap);
-      const float4 v = vp ? load_bf16x4(vp) : make_float4(0.f, 0.f, 0.f, 0.f);
-      const float e0 = exp_own(__fsub_rn(sc.x, m.x)), e1 = exp_own(__fsub_rn(sc.y, m.y));
-      const float e2 = exp_own(__fsub_rn(sc.z, m.z)), e3 = exp_own(__fsub_rn(sc.w, m.w));
-      num.x = __fadd_rn(num.x, __fmul_rn(e0, v.x)); den.x = __fadd_rn(den.x, e0);
-      num.y = __fadd_rn(num.y, __fmul_rn(e1, v.y)); den.y = __fadd_rn(den.y, e1);
-      num.z = __fadd_rn(num.z, __fmul_rn(e2, v.z)); den.z = __fadd_rn(den.z, e2);
-      num.w = __fadd_rn(num.w, __fmul_rn(e3, v.w)); den.w = __fadd_rn(den.w, e3);
+    for (int j0 = 0; j0 < slots; j0 += kBatch) {
+      float4 sc[kBatch], v[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        sc[u] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (j0 + u < slots) {
+          const uint8_t *vp, *gp;
+          const float* ap;
+          slot_src(j0 + u, vp, gp, ap);
+          sc[u] = score(gp, ap);
+          if (vp) v[u] = load_bf16x4(vp);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        if (j0 + u >= slots) break;
+        const float e0 = exp_own(__fsub_rn(sc[u].x, m.x)), e1 = exp_own(__fsub_rn(sc[u].y, m.y));
+        const float e2 = exp_own(__fsub_rn(sc[u].z, m.z)), e3 = exp_own(__fsub_rn(sc[u].w, m.w));
+        num.x = __fadd_rn(num.x, __fmul_rn(e0, v[u].x)); den.x = __fadd_rn(den.x, e0);
+        num.y = __fadd_rn(num.y, __fmul_rn(e1, v[u].y)); den.y = __fadd_rn(den.y, e1);
+        num.z = __fadd_rn(num.z, __fmul_rn(e2, v[u].z)); den.z = __fadd_rn(den.z, e2);
+        num.w = __fadd_rn(num.w, __fmul_rn(e3, v[u].w)); den.w = __fadd_rn(den.w, e3);
+      }
     }
   }
   float4 y = live ? make_float4(__fdiv_rn(num.x, den.x), __fdiv_rn(num.y, den.y),
@@ -170,25 +210,17 @@ __global__ void __launch_bounds__(128) compress_kernel(const CompressArgs a) {
                                   __fadd_rn(__fmul_rn(y.z, y.z), __fmul_rn(y.w, y.w)));
     const float ss = block_sum_pairwise<D>(local, threadIdx.x % 128);
     const float rr = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(D)), a.eps)));
-    const float4 w = *reinterpret_cast<const float4*>(a.norm_w + c0);
-    y.x = __fmul_rn(__fmul_rn(y.x, rr), w.x);
-    y.y = __fmul_rn(__fmul_rn(y.y, rr), w.y);
-    y.z = __fmul_rn(__fmul_rn(y.z, rr), w.z);
-    y.w = __fmul_rn(__fmul_rn(y.w, rr), w.w);
+    y.x = __fmul_rn(__fmul_rn(y.x, rr), nw.x);
+    y.y = __fmul_rn(__fmul_rn(y.y, rr), nw.y);
+    y.z = __fmul_rn(__fmul_rn(y.z, rr), nw.z);
+    y.w = __fmul_rn(__fmul_rn(y.w, rr), nw.w);
   }
-  if (a.rope_cs != nullptr && live && c0 >= D - 64) {
-    const int k = (c0 - (D - 64)) / 2;   // pairs k and k+1
-    const float4 cs = *reinterpret_cast<const float4*>(a.rope_cs + ((s * a.n + i) * 32 + k) * 2);
+  if (rotate) {
     const float y0 = y.x, y1 = y.y, y2 = y.z, y3 = y.w;
     y.x = __fsub_rn(__fmul_rn(y0, cs.x), __fmul_rn(y1, cs.y));
     y.y = __fadd_rn(__fmul_rn(y0, cs.y), __fmul_rn(y1, cs.x));
     y.z = __fsub_rn(__fmul_rn(y2, cs.z), __fmul_rn(y3, cs.w));
     y.w = __fadd_rn(__fmul_rn(y2, cs.w), __fmul_rn(y3, cs.z));
-  }
-  RowPtr dst{nullptr, nullptr};
-  if (live) {
-    const long long row = static_cast<long long>(a.first_entry[s]) + i;
-    dst = paged_row(a.out, a.req[s], row, a.out_row_bytes);
   }
   store_row_values(y, lt, a.out.fmt, D, dst, live && dst.data != nullptr);
 }

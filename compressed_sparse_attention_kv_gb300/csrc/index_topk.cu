@@ -23,14 +23,17 @@
 //       warps 2-5  read the accumulator with tcgen05.ld (one TMEM lane = one
 //                  entry), apply ReLU and the head weights, sum the heads
 //                  inside one thread, multiply by the key's scale, write the
-//                  fp32 score and bin its order-preserving key into a
-//                  4,096-bin shared histogram.
+//                  fp32 score, bin its order-preserving key into a
+//                  4,096-bin shared histogram and keep the largest key of
+//                  each 32-entry segment.
 //     Then, behind a bounded grid barrier, every block finds each request's
-//     threshold bin (the bin holding the k-th score), emits its own entries
-//     above it and stages the ones in it; behind a second barrier the block
-//     owning request b radix-selects the remainder among those 64-bit
-//     (score, ~index) keys (ties -> smaller index), sorts the k indices and
-//     writes indices and scores.
+//     threshold bin T (the bin holding the k-th score), counts its own entries
+//     above T and stages the ones in T as 64-bit (score, ~index) keys; only
+//     segments whose largest key reaches T are read again.  Behind a second
+//     barrier every block radix-selects the exact cut among the request's
+//     candidates (ties -> smaller index), derives its output offset from the
+//     lower blocks' counts and writes its own selected entries in entry
+//     order, so the output needs no sort.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -46,21 +49,30 @@ namespace {
 constexpr int kHistBits = 12;
 constexpr int kHistBins = 1 << kHistBits;
 constexpr int kTileRows = 128;
-constexpr int kStagesFp8 = 4;        // 16 KiB stages
-constexpr int kStagesBf16 = 2;       // 32 KiB stages
-constexpr int kAccs = 4;             // TMEM accumulators in flight
-constexpr int kScaleSlots = 8;       // ring of per-tile scale rows (2 pages x 64 fp32)
-constexpr int kScoreThreads = 192;   // warp 0 producer, warp 1 MMA, warps 2-5 epilogue
+constexpr int kProducers = 2;        // TMA-issuing warps, each with its own stage ring
+constexpr int kGroups = 2;           // epilogue groups of 4 warps (one per TMEM lane quarter)
+constexpr int kStagesFp8 = 4;        // per producer, 16 KiB stages
+constexpr int kStagesBf16 = 2;       // per producer, 32 KiB stages
+constexpr int kAccs = 8;             // TMEM accumulators in flight (8 x 64 columns)
+constexpr int kScaleSlots = 16;      // ring of per-tile scale rows (2 pages x 64 fp32)
+constexpr int kWarpMma = kProducers;
+constexpr int kWarpEpi = kProducers + 1;
+constexpr int kScoreThreads = 32 * (kProducers + 1 + 4 * kGroups);   // 352
 constexpr int kCandCap = 4096;       // per-block staging of threshold-bin candidates
-constexpr int kMaxK = 2048;
 constexpr int kQImageFp8 = 8192;     // e4m3 [64 rows][128 B]
 constexpr int kQImageBf16 = 16384;   // bf16 [2 chunks][64 rows][128 B]
 constexpr int kQSlot = 16384;        // per request in the workspace
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+constexpr int kMaxGrid = 1024;       // bound of the per-block counters' table
+constexpr int kSeg = 32;             // entries per segment (one epilogue warp's rows of a tile)
+constexpr int kSegCap = 4096;        // segments a block tracks in shared memory (1,024 tiles)
+constexpr int kSegCache = 512;       // hit segments whose scores stay in shared memory
+constexpr uint16_t kHitUncached = 0xFFFF;
+
 struct WsLayout {
-  size_t scores, cand, qimg, wq, hist, ctr, sel, gbar, total;
+  size_t scores, segmax, cand, qimg, wq, hist, ctr, abv, gbar, total;
   int n_pad;
 };
 
@@ -70,12 +82,13 @@ __host__ __device__ inline WsLayout ws_layout(int B, int n_max, int k) {
   if (L.n_pad == 0) L.n_pad = kTileRows;
   size_t o = 0;
   L.scores = o; o = align256(o + size_t(B) * L.n_pad * 4);
+  L.segmax = o; o = align256(o + size_t(B) * (L.n_pad / kSeg) * 4);
   L.cand = o;   o = align256(o + size_t(B) * L.n_pad * 8);
   L.qimg = o;   o = align256(o + size_t(B) * kQSlot);
   L.wq = o;     o = align256(o + size_t(B) * 64 * 4);
   L.hist = o;   o = align256(o + size_t(B) * kHistBins * 4);
   L.ctr = o;    o = align256(o + size_t(B) * 4 * 4);
-  L.sel = o;    o = align256(o + size_t(B) * k * 4);
+  L.abv = o;    o = align256(o + size_t(B) * kMaxGrid * 4);
   L.gbar = o;   o = align256(o + 16);
   L.total = o;
   return L;
@@ -165,20 +178,21 @@ __global__ void __launch_bounds__(256) index_prep_kernel(const IndexArgs a) {
 // 2. score kernel (+ fused selection)
 // ---------------------------------------------------------------------------
 struct ScoreSmem {
-  uint64_t full[kStagesFp8], empty[kStagesFp8];
+  uint64_t full[kProducers][kStagesFp8], empty[kProducers][kStagesFp8];
   uint64_t accfull[kAccs], accempty[kAccs];
   uint64_t qfull[2], qempty[2];
   uint64_t sfull[kScaleSlots], sempty[kScaleSlots];
   uint64_t drain;
-  uint64_t hbar;                   // epilogue warps meet here at a request switch
+  uint64_t hbar[kGroups];          // an epilogue group's warps meet here at a request switch
   uint32_t tmem_base;
   volatile int abort;
   int smask[kScaleSlots];          // per tile: bit p = page p of the tile was loaded
-  int ptab[64];                    // producer's prefetched page ids of its current request
-  __align__(16) float wq[64];      // folded head weights of the epilogue's current request
+  int ptab[kProducers][64];        // each producer's prefetched page ids of its current request
+  __align__(16) float wq[kGroups][64];   // folded head weights of each group's current request
   // selection phases
   uint32_t cnt[2];
   uint32_t base[2];
+  uint32_t nlist;
   int T;
   uint32_t above;
   uint32_t need, done, out;
@@ -266,49 +280,68 @@ __device__ void grid_barrier(ScoreSmem* sm, uint32_t* counter, uint32_t target, 
 }
 
 // T = the largest histogram bin with (entries in bins >= T) >= k; above = entries in
-// bins > T; T = -1 if the histogram holds fewer than k entries.  Whole block.
-__device__ void threshold_bin(ScoreSmem* sm, const uint32_t* ghist, int k) {
+// bins > T; T = -1 if the histogram holds fewer than k entries.  Whole block; the
+// request's bins are copied into `hs` (4,096 words of shared memory) in one pass.
+// This code runs once per launch, from a cold instruction cache: it is kept short
+// (rolled loops) rather than unrolled.
+__device__ void threshold_bin(ScoreSmem* sm, const uint32_t* ghist, uint32_t* hs, int k) {
+  constexpr int kVec = kHistBins / 4;
+  constexpr int kPer = (kVec + kScoreThreads - 1) / kScoreThreads;
+  uint4 v[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int i = threadIdx.x + u * kScoreThreads;
+    v[u] = i < kVec ? __ldcg(reinterpret_cast<const uint4*>(ghist) + i) : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int i = threadIdx.x + u * kScoreThreads;
+    if (i < kVec) reinterpret_cast<uint4*>(hs)[i] = v[u];
+  }
+  __syncthreads();
+  // 256 parts of 16 bins, part p = bins 16p .. 16p+15
   for (int t = threadIdx.x; t < 256; t += blockDim.x) {
-    uint32_t hb[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) hb[i] = __ldcg(ghist + t * 16 + i);
+    const uint4* q = reinterpret_cast<const uint4*>(hs + t * 16);
     uint32_t loc = 0;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) loc += hb[i];
+#pragma unroll 1
+    for (int i = 0; i < 4; ++i) {
+      const uint4 x = q[i];
+      loc += x.x + x.y + x.z + x.w;
+    }
     sm->part[t] = loc;
   }
   __syncthreads();
   const int lane = threadIdx.x;
   if (lane < 32) {
     // lane l owns parts 255-8l .. 248-8l (from the top)
-    uint32_t loc[8], sum = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) { loc[i] = sm->part[255 - 8 * lane - i]; sum += loc[i]; }
+    uint32_t sum = 0;
+#pragma unroll 1
+    for (int i = 0; i < 8; ++i) sum += sm->part[255 - 8 * lane - i];
     uint32_t incl = sum;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-      if (lane >= o) incl += v;
+      const uint32_t x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += x;
     }
-    const uint32_t excl = incl - sum;
     const unsigned hit = __ballot_sync(0xFFFFFFFFu, incl >= static_cast<uint32_t>(k));
     if (hit == 0) {
       if (lane == 0) { sm->T = -1; sm->above = 0; }
     } else if (lane == __ffs(hit) - 1) {
-      uint32_t acc = excl;
+      // walk down this lane's parts, then the bins of the part that crosses k
+      uint32_t acc = incl - sum;
       int u = 255 - 8 * lane - 7;
+#pragma unroll 1
       for (int i = 0; i < 8; ++i) {
-        if (acc + loc[i] >= static_cast<uint32_t>(k)) { u = 255 - 8 * lane - i; break; }
-        acc += loc[i];
+        const uint32_t x = sm->part[255 - 8 * lane - i];
+        if (acc + x >= static_cast<uint32_t>(k)) { u = 255 - 8 * lane - i; break; }
+        acc += x;
       }
-      uint32_t hb[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) hb[i] = __ldcg(ghist + u * 16 + i);   // one round trip
       int T = u * 16;
-#pragma unroll
+#pragma unroll 1
       for (int i = 15; i >= 0; --i) {
-        if (acc + hb[i] >= static_cast<uint32_t>(k)) { T = u * 16 + i; break; }
-        acc += hb[i];
+        const uint32_t hb = hs[u * 16 + i];
+        if (acc + hb >= static_cast<uint32_t>(k)) { T = u * 16 + i; break; }
+        acc += hb;
       }
       sm->T = T;
       sm->above = acc;
@@ -317,29 +350,93 @@ __device__ void threshold_bin(ScoreSmem* sm, const uint32_t* ghist, int k) {
   __syncthreads();
 }
 
+// Exclusive scan, in place, of n counters in shared memory (whole block).
+__device__ void block_exclusive_scan(ScoreSmem* sm, uint32_t* x, int n) {
+  const int per = (n + kScoreThreads - 1) / kScoreThreads;
+  const int lo = min(n, static_cast<int>(threadIdx.x) * per), hi = min(n, lo + per);
+  uint32_t sum = 0;
+#pragma unroll 1
+  for (int i = lo; i < hi; ++i) sum += x[i];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) sm->part[warp] = incl;
+  __syncthreads();
+  uint32_t run = incl - sum;
+#pragma unroll 1
+  for (int w = 0; w < warp; ++w) run += sm->part[w];
+#pragma unroll 1
+  for (int i = lo; i < hi; ++i) {
+    const uint32_t v = x[i];
+    x[i] = run;
+    run += v;
+  }
+  __syncthreads();
+}
+
+// The indices q in [0, n) with pred(q), in increasing order, into list (whole
+// block; pred is evaluated twice and must not change in between).  Returns the count.
+template <class Pred>
+__device__ uint32_t ordered_list(ScoreSmem* sm, int n, Pred pred, uint16_t* list) {
+  const int per = (n + kScoreThreads - 1) / kScoreThreads;
+  const int lo = min(n, static_cast<int>(threadIdx.x) * per), hi = min(n, lo + per);
+  uint32_t cnt = 0;
+#pragma unroll 1
+  for (int q = lo; q < hi; ++q) cnt += pred(q) ? 1u : 0u;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) sm->part[warp] = incl;
+  __syncthreads();
+  uint32_t pos = incl - cnt, tot = 0;
+#pragma unroll 1
+  for (int w = 0; w < kScoreThreads / 32; ++w) {
+    const uint32_t x = sm->part[w];
+    if (w < warp) pos += x;
+    tot += x;
+  }
+#pragma unroll 1
+  for (int q = lo; q < hi; ++q)
+    if (pred(q)) list[pos++] = static_cast<uint16_t>(q);
+  __syncthreads();
+  return tot;
+}
+
 template <int FP8>
-__global__ void __launch_bounds__(kScoreThreads, 2)
+__global__ void __launch_bounds__(kScoreThreads, 1)
     index_score_kernel(const __grid_constant__ CUtensorMap tmap, const IndexArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned carve-up
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr int kStageBytes = FP8 ? kTileRows * 128 : kTileRows * 256;
-  constexpr int kStages = FP8 ? kStagesFp8 : kStagesBf16;
+  constexpr int kStages = FP8 ? kStagesFp8 : kStagesBf16;   // per producer
   constexpr int kQImage = FP8 ? kQImageFp8 : kQImageBf16;
-  uint8_t* stages = base;
-  uint8_t* qbuf = stages + kStages * kStageBytes;                         // 2 x kQImage
-  uint32_t* hist = reinterpret_cast<uint32_t*>(qbuf + 2 * kQImage);      // 4096 bins
-  float* sring = reinterpret_cast<float*>(hist + kHistBins);             // kScaleSlots x 128 fp32
-  ScoreSmem* sm = reinterpret_cast<ScoreSmem*>(sring + kScaleSlots * kTileRows);
+  uint8_t* stages = base;                                                  // kProducers x kStages
+  uint8_t* qbuf = stages + kProducers * kStages * kStageBytes;             // 2 x kQImage
+  uint32_t* hist = reinterpret_cast<uint32_t*>(qbuf + 2 * kQImage);       // kGroups x 4096 bins
+  float* sring = reinterpret_cast<float*>(hist + kGroups * kHistBins);    // kScaleSlots x 128 fp32
+  // per segment of the block's range: the bin of its largest key (phase 1), then
+  // 0 / cache slot + 1 / kHitUncached (phase 2 -> 3)
+  uint16_t* s_seg = reinterpret_cast<uint16_t*>(sring + kScaleSlots * kTileRows);   // kSegCap
+  ScoreSmem* sm = reinterpret_cast<ScoreSmem*>(s_seg + kSegCap);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = a.N;
   float* scores_all = reinterpret_cast<float*>(a.ws + a.L.scores);
+  uint32_t* segmax_all = reinterpret_cast<uint32_t*>(a.ws + a.L.segmax);
   uint32_t* ghist = reinterpret_cast<uint32_t*>(a.ws + a.L.hist);
   uint32_t* ctr_all = reinterpret_cast<uint32_t*>(a.ws + a.L.ctr);
   uint32_t* gbar = reinterpret_cast<uint32_t*>(a.ws + a.L.gbar);
 
-  // work range of this block
+  // work range of this block: a contiguous run of the global tile sequence
   long long total = 0;
   for (int b = 0; b < a.B; ++b) total += (visible(a, b) + kTileRows - 1) / kTileRows;
   const long long per = (total + gridDim.x - 1) / gridDim.x;
@@ -347,39 +444,45 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
   const long long end = min(total, start + per);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) { mbar_init(&sm->full[s], 1); mbar_init(&sm->empty[s], 1); }
+    for (int p = 0; p < kProducers; ++p)
+      for (int s = 0; s < kStages; ++s) { mbar_init(&sm->full[p][s], 1); mbar_init(&sm->empty[p][s], 1); }
     for (int c = 0; c < kAccs; ++c) { mbar_init(&sm->accfull[c], 1); mbar_init(&sm->accempty[c], 4); }
     for (int c = 0; c < 2; ++c) { mbar_init(&sm->qfull[c], 1); mbar_init(&sm->qempty[c], 1); }
     for (int s = 0; s < kScaleSlots; ++s) { mbar_init(&sm->sfull[s], 1); mbar_init(&sm->sempty[s], 4); }
     mbar_init(&sm->drain, 1);
-    mbar_init(&sm->hbar, 4);
+    for (int g = 0; g < kGroups; ++g) mbar_init(&sm->hbar[g], 4);
     sm->abort = 0;
     fence_mbar_init();
   }
-  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) hist[i] = 0;
+  for (int i = threadIdx.x; i < kGroups * kHistBins; i += blockDim.x) hist[i] = 0;
   uint32_t ncols = 32;
   while (ncols < static_cast<uint32_t>(kAccs * N)) ncols <<= 1;
-  if (warp == 1) tmem_alloc(&sm->tmem_base, ncols);
+  if (warp == kWarpMma) tmem_alloc(&sm->tmem_base, ncols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm->tmem_base;
 
   // ======================================================= phase 1: scores
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  // Block-local tile i (the i-th tile of [start, end)) is loaded by producer i % 2
+  // into stage (i / 2) % kStages of its ring, scored into accumulator i % 8 and
+  // read back by epilogue group i % 2; its scales use slot i % 16.
+  if (warp < kProducers) {
+    // ------------------------------------------------------------ producers
+    const int pw = warp;
     if (lane == 0 && start < end) {
       prefetch_tmap(&tmap);
       TileWalker tw;
       tw.init(a, start, end);
-      long long issued = 0;
+      long long i = 0, np = 0;
       int nreq = 0;
-      bool need_q = true;
-      int pt_b = -1;           // request and first logical page of sm->ptab
+      bool need_q = pw == 0;
+      int pt_b = -1;           // request and first logical page of this producer's ptab
       long long pt_lp = 0;
-      while (tw.valid()) {
+      bool ok = true;
+      while (tw.valid() && ok) {
         if (need_q) {
-          // query image of the new request into buffer nreq % 2
+          // query image of the new request into buffer nreq % 2 (producer 0 only)
           const int qb = nreq & 1;
           if (nreq >= 2 && !role_wait(sm, &sm->qempty[qb], ((nreq >> 1) - 1) & 1, a.spin)) break;
           mbar_expect_tx(&sm->qfull[qb], kQImage);
@@ -387,79 +490,84 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
           ++nreq;
           need_q = false;
         }
-        const int s = static_cast<int>(issued % kStages);
-        const long long round = issued / kStages;
-        if (round > 0 && !role_wait(sm, &sm->empty[s], (round - 1) & 1, a.spin)) break;
-        const int ss = static_cast<int>(issued % kScaleSlots);
-        const long long su = issued / kScaleSlots;
-        if (su > 0 && !role_wait(sm, &sm->sempty[ss], (su - 1) & 1, a.spin)) break;
-        uint8_t* dst = stages + s * kStageBytes;
-        uint32_t bytes = 0;
-        int pages[2] = {-1, -1};
-        const long long lp0 = static_cast<long long>(tw.t) * 2;
-        if (tw.b != pt_b || lp0 < pt_lp || lp0 + 1 >= pt_lp + 64) {
-          // refill: 64 page ids of this request, two batches of 32 loads in flight
-          pt_b = tw.b;
-          pt_lp = lp0;
-          const int32_t* bt = a.keys.block_table + static_cast<long long>(tw.b) * a.keys.max_pages;
+        if ((i & 1) == pw) {
+          const int s = static_cast<int>(np % kStages);
+          const long long round = np / kStages;
+          if (round > 0 && !role_wait(sm, &sm->empty[pw][s], (round - 1) & 1, a.spin)) break;
+          const int ss = static_cast<int>(i % kScaleSlots);
+          const long long su = i / kScaleSlots;
+          if (su > 0 && !role_wait(sm, &sm->sempty[ss], (su - 1) & 1, a.spin)) break;
+          uint8_t* dst = stages + (pw * kStages + s) * kStageBytes;
+          uint32_t bytes = 0;
+          int pages[2] = {-1, -1};
+          const long long lp0 = static_cast<long long>(tw.t) * 2;
+          int* ptab = sm->ptab[pw];
+          if (tw.b != pt_b || lp0 < pt_lp || lp0 + 1 >= pt_lp + 64) {
+            // refill: 64 page ids of this request, two batches of 32 loads in flight
+            pt_b = tw.b;
+            pt_lp = lp0;
+            const int32_t* bt = a.keys.block_table + static_cast<long long>(tw.b) * a.keys.max_pages;
 #pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            int ids[32];
+            for (int h2 = 0; h2 < 2; ++h2) {
+              int ids[32];
 #pragma unroll
-            for (int u = 0; u < 32; ++u) {
-              const long long lp = lp0 + 32 * h2 + u;
-              ids[u] = (lp * kPageRows < tw.n_b && lp < a.keys.max_pages) ? bt[lp] : -2;
+              for (int u = 0; u < 32; ++u) {
+                const long long lp = lp0 + 32 * h2 + u;
+                ids[u] = (lp * kPageRows < tw.n_b && lp < a.keys.max_pages) ? bt[lp] : -2;
+              }
+#pragma unroll
+              for (int u = 0; u < 32; ++u) ptab[32 * h2 + u] = ids[u];
             }
-#pragma unroll
-            for (int u = 0; u < 32; ++u) sm->ptab[32 * h2 + u] = ids[u];
           }
-        }
-        for (int pg = 0; pg < 2; ++pg) {
-          const long long lp = lp0 + pg;
-          if (lp * kPageRows >= tw.n_b) continue;
-          if (lp >= a.keys.max_pages) { set_err(CSKV_ERR_BOUNDS); continue; }
-          const int pid = sm->ptab[lp - pt_lp];
-          if (pid < 0 || pid >= a.keys.num_pages) { set_err(CSKV_ERR_BOUNDS); continue; }
-          pages[pg] = pid;
-          bytes += FP8 ? 64 * 128 : 64 * 256;
-        }
-        sm->smask[ss] = (pages[0] >= 0 ? 1 : 0) | (pages[1] >= 0 ? 2 : 0);
-        mbar_expect_tx(&sm->full[s], bytes);
-        mbar_expect_tx(&sm->sfull[ss], FP8 ? (pages[0] >= 0 ? 256u : 0u) + (pages[1] >= 0 ? 256u : 0u) : 0u);
-        for (int pg = 0; pg < 2; ++pg) {
-          if (pages[pg] < 0) continue;
-          tma_load_3d(dst + pg * 8192, &tmap, 0, 0, pages[pg], &sm->full[s]);
-          if (!FP8) tma_load_3d(dst + 16384 + pg * 8192, &tmap, 64, 0, pages[pg], &sm->full[s]);
-          if (FP8) {
-            const uint8_t* pgp = static_cast<const uint8_t*>(a.keys.pool) + size_t(pages[pg]) * a.keys.page_bytes;
-            bulk_g2s(sring + ss * kTileRows + pg * kPageRows, pgp + kPageRows * 128, 256, &sm->sfull[ss]);
+          for (int pg = 0; pg < 2; ++pg) {
+            const long long lp = lp0 + pg;
+            if (lp * kPageRows >= tw.n_b) continue;
+            if (lp >= a.keys.max_pages) { set_err(CSKV_ERR_BOUNDS); continue; }
+            const int pid = ptab[lp - pt_lp];
+            if (pid < 0 || pid >= a.keys.num_pages) { set_err(CSKV_ERR_BOUNDS); continue; }
+            pages[pg] = pid;
+            bytes += FP8 ? 64 * 128 : 64 * 256;
           }
+          sm->smask[ss] = (pages[0] >= 0 ? 1 : 0) | (pages[1] >= 0 ? 2 : 0);
+          mbar_expect_tx(&sm->full[pw][s], bytes);
+          mbar_expect_tx(&sm->sfull[ss], FP8 ? (pages[0] >= 0 ? 256u : 0u) + (pages[1] >= 0 ? 256u : 0u) : 0u);
+          for (int pg = 0; pg < 2; ++pg) {
+            if (pages[pg] < 0) continue;
+            tma_load_3d(dst + pg * 8192, &tmap, 0, 0, pages[pg], &sm->full[pw][s]);
+            if (!FP8) tma_load_3d(dst + 16384 + pg * 8192, &tmap, 64, 0, pages[pg], &sm->full[pw][s]);
+            if (FP8) {
+              const uint8_t* pgp = static_cast<const uint8_t*>(a.keys.pool) + size_t(pages[pg]) * a.keys.page_bytes;
+              bulk_g2s(sring + ss * kTileRows + pg * kPageRows, pgp + kPageRows * 128, 256, &sm->sfull[ss]);
+            }
+          }
+          ++np;
         }
-        ++issued;
-        if (tw.next(a)) need_q = true;
+        ++i;
+        if (tw.next(a) && pw == 0) need_q = true;
       }
       // drain: every copy this producer issued must land before the block moves on
-      for (int s = 0; s < kStages && s < issued; ++s) {
-        const long long uses = (issued - s + kStages - 1) / kStages;
-        mbar_wait(&sm->full[s], (uses - 1) & 1, kDefaultSpinLimit);
+      for (int s = 0; s < kStages && s < np; ++s) {
+        const long long uses = (np - s + kStages - 1) / kStages;
+        mbar_wait(&sm->full[pw][s], (uses - 1) & 1, kDefaultSpinLimit);
       }
-      for (int s = 0; s < kScaleSlots && s < issued; ++s) {
-        const long long uses = (issued - s + kScaleSlots - 1) / kScaleSlots;
-        mbar_wait(&sm->sfull[s], (uses - 1) & 1, kDefaultSpinLimit);
+      const long long nsc = (np > 0) ? 2 * (np - 1) + pw + 1 : 0;   // tiles up to this producer's last
+      for (int ss = pw; ss < kScaleSlots; ss += 2) {
+        const long long uses = nsc > ss ? (nsc - ss + kScaleSlots - 1) / kScaleSlots : 0;
+        if (uses > 0) mbar_wait(&sm->sfull[ss], (uses - 1) & 1, kDefaultSpinLimit);
       }
       for (int qb = 0; qb < 2 && qb < nreq; ++qb) {
         const int uses = (nreq - qb + 1) / 2;
         mbar_wait(&sm->qfull[qb], (uses - 1) & 1, kDefaultSpinLimit);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && start < end) {
       constexpr uint32_t idesc = FP8 ? make_idesc(0, 0, 0, 0, 128, 0) : make_idesc(1, 1, 0, 0, 128, 0);
       const uint32_t id = idesc | (static_cast<uint32_t>(N >> 3) << 17);
       TileWalker tw;
       tw.init(a, start, end);
-      long long it = 0;
+      long long i = 0;
       int nreq = 0, qb = 0;
       bool need_q = true;
       while (tw.valid()) {
@@ -469,13 +577,15 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
           ++nreq;
           need_q = false;
         }
-        const int s = static_cast<int>(it % kStages);
-        const int c = static_cast<int>(it % kAccs);
-        const long long use = it / kAccs;
-        if (!role_wait(sm, &sm->full[s], (it / kStages) & 1, a.spin)) break;
+        const int pw = static_cast<int>(i & 1);
+        const long long ip = i >> 1;
+        const int s = static_cast<int>(ip % kStages);
+        const int c = static_cast<int>(i % kAccs);
+        const long long use = i / kAccs;
+        if (!role_wait(sm, &sm->full[pw][s], (ip / kStages) & 1, a.spin)) break;
         if (use > 0 && !role_wait(sm, &sm->accempty[c], (use - 1) & 1, a.spin)) break;
         tc_fence_after();
-        const uint32_t a_addr = smem_u32(stages + s * kStageBytes);
+        const uint32_t a_addr = smem_u32(stages + (pw * kStages + s) * kStageBytes);
         const uint32_t b_addr = smem_u32(qbuf + qb * kQImage);
         const uint32_t d = tmem + c * N;
         if (FP8) {
@@ -492,9 +602,9 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
                     smem_desc_sw128(b_addr + ch * (N * 128) + o, 16, 1024), id, kk > 0);
           }
         }
-        mma_commit(&sm->empty[s]);
+        mma_commit(&sm->empty[pw][s]);
         mma_commit(&sm->accfull[c]);
-        ++it;
+        ++i;
         if (tw.next(a)) {
           mma_commit(&sm->qempty[qb]);
           need_q = true;
@@ -506,104 +616,135 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int sub = warp & 3;                      // TMEM sub-partition of this warp
-    const int row = sub * 32 + lane;               // entry within the tile
-    const int tid = threadIdx.x - 64;              // 0..127
+    const int e = warp - kWarpEpi;               // 0 .. 4 * kGroups - 1
+    const int grp = e >> 2;
+    const int sub = warp & 3;                    // TMEM lane quarter of this warp
+    const int row = sub * 32 + lane;             // entry within the tile
+    const int gtid = (e & 3) * 32 + lane;        // 0..127 within the group
+    uint32_t* ghs = hist + grp * kHistBins;      // this group's histogram
+    float* wq_s = sm->wq[grp];
     const float* wq_all = reinterpret_cast<const float*>(a.ws + a.L.wq);
     if (start < end) {
       TileWalker tw;
       tw.init(a, start, end);
-      long long it = 0;
+      long long i = 0;
       int cur_b = -1;
       uint32_t hphase = 0;
-      // the four epilogue warps meet (bounded: an aborted pass falls through)
-      auto wg_sync = [&]() {
+      // the group's four warps meet (bounded: an aborted pass falls through)
+      auto grp_sync = [&]() {
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm->hbar);
-        role_wait(sm, &sm->hbar, hphase & 1, a.spin);
+        if (lane == 0) mbar_arrive(&sm->hbar[grp]);
+        role_wait(sm, &sm->hbar[grp], hphase & 1, a.spin);
         ++hphase;
       };
+      auto flush = [&](int b) {
+        for (int x = gtid; x < kHistBins; x += 128) {
+          const uint32_t cnt = ghs[x];
+          if (cnt) { atomicAdd(ghist + size_t(b) * kHistBins + x, cnt); ghs[x] = 0; }
+        }
+      };
       while (tw.valid()) {
-        if (tw.b != cur_b) {
-          // request switch: every warp is done with the previous request's tiles
-          wg_sync();
-          if (cur_b >= 0) {
-            for (int i = tid; i < kHistBins; i += 128) {
-              const uint32_t cnt = hist[i];
-              if (cnt) { atomicAdd(ghist + size_t(cur_b) * kHistBins + i, cnt); hist[i] = 0; }
+        if (static_cast<int>(i % kGroups) == grp) {
+          if (tw.b != cur_b) {
+            // request switch: the group is done with the previous request's tiles
+            grp_sync();
+            if (cur_b >= 0) flush(cur_b);
+            cur_b = tw.b;
+            if (gtid < 64) wq_s[gtid] = gtid < N ? wq_all[cur_b * 64 + gtid] : 0.f;
+            grp_sync();
+          }
+          const long long j = static_cast<long long>(tw.t) * kTileRows + row;
+          const int ss = static_cast<int>(i % kScaleSlots);
+          if (!role_wait(sm, &sm->sfull[ss], (i / kScaleSlots) & 1, a.spin)) break;
+          const int pmask = sm->smask[ss];
+          const bool valid = j < tw.n_b && ((pmask >> (row >> 6)) & 1);
+          const float ks = FP8 ? sring[ss * kTileRows + row] : 1.0f;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm->sempty[ss]);   // one arrival per warp
+          const int c = static_cast<int>(i % kAccs);
+          if (!role_wait(sm, &sm->accfull[c], (i / kAccs) & 1, a.spin)) break;
+          tc_fence_after();
+          const uint32_t tb = tmem + (static_cast<uint32_t>(sub * 32) << 16) + c * N;
+          float P[64];
+          if (N == 64) {
+            tmem_ld32(tb, *reinterpret_cast<float(*)[32]>(P));
+            tmem_ld32(tb + 32, *reinterpret_cast<float(*)[32]>(P + 32));
+          } else {
+#pragma unroll
+            for (int c0 = 0; c0 < 64; c0 += 16)
+              if (c0 < N) tmem_ld16(tb + c0, *reinterpret_cast<float(*)[16]>(P + c0));
+          }
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm->accempty[c]);   // this warp's TMEM reads are done
+          float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+          for (int h = 0; h < 64; h += 4) {
+            if (h < N) {
+              const float4 w4 = *reinterpret_cast<const float4*>(&wq_s[h]);
+              s0 = fmaf(w4.x, fmaxf(P[h], 0.f), s0);
+              s1 = fmaf(w4.y, fmaxf(P[h + 1], 0.f), s1);
+              s0 = fmaf(w4.z, fmaxf(P[h + 2], 0.f), s0);
+              s1 = fmaf(w4.w, fmaxf(P[h + 3], 0.f), s1);
             }
           }
-          cur_b = tw.b;
-          if (tid < 64) sm->wq[tid] = tid < N ? wq_all[cur_b * 64 + tid] : 0.f;
-          wg_sync();
-        }
-        const long long j = static_cast<long long>(tw.t) * kTileRows + row;
-        const int ss = static_cast<int>(it % kScaleSlots);
-        if (!role_wait(sm, &sm->sfull[ss], (it / kScaleSlots) & 1, a.spin)) break;
-        const int pmask = sm->smask[ss];
-        const bool valid = j < tw.n_b && ((pmask >> (row >> 6)) & 1);
-        const float ks = FP8 ? sring[ss * kTileRows + row] : 1.0f;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm->sempty[ss]);   // one arrival per warp
-        const int c = static_cast<int>(it % kAccs);
-        if (!role_wait(sm, &sm->accfull[c], (it / kAccs) & 1, a.spin)) break;
-        tc_fence_after();
-        const uint32_t tb = tmem + (static_cast<uint32_t>(sub * 32) << 16) + c * N;
-        float P[64];
-        if (N == 64) {
-          tmem_ld32(tb, *reinterpret_cast<float(*)[32]>(P));
-          tmem_ld32(tb + 32, *reinterpret_cast<float(*)[32]>(P + 32));
-        } else {
-#pragma unroll
-          for (int c0 = 0; c0 < 64; c0 += 16)
-            if (c0 < N) tmem_ld16(tb + c0, *reinterpret_cast<float(*)[16]>(P + c0));
-        }
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm->accempty[c]);   // this warp's TMEM reads are done
-        float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-        for (int h = 0; h < 64; h += 4) {
-          if (h < N) {
-            const float4 w4 = *reinterpret_cast<const float4*>(&sm->wq[h]);
-            s0 = fmaf(w4.x, fmaxf(P[h], 0.f), s0);
-            s1 = fmaf(w4.y, fmaxf(P[h + 1], 0.f), s1);
-            s0 = fmaf(w4.z, fmaxf(P[h + 2], 0.f), s0);
-            s1 = fmaf(w4.w, fmaxf(P[h + 3], 0.f), s1);
+          const float I = (s0 + s1) * ks;   // the key's scale is a positive power of two
+          const uint32_t key = valid ? order_key(I) : 0u;
+          if (valid) {
+            scores_all[size_t(tw.b) * a.L.n_pad + j] = I;
+            atomicAdd(&ghs[key >> (32 - kHistBits)], 1u);
+          }
+          // largest key of this warp's 32 entries: the selection re-reads only
+          // segments that can hold a selected entry
+          const uint32_t kmax = __reduce_max_sync(0xFFFFFFFFu, key);
+          if (lane == 0) {
+            segmax_all[size_t(tw.b) * (a.L.n_pad / kSeg) + (j >> 5)] = kmax;
+            if (i * 4 + sub < kSegCap) s_seg[i * 4 + sub] = static_cast<uint16_t>(kmax >> (32 - kHistBits));
           }
         }
-        const float I = (s0 + s1) * ks;   // the key's scale is a positive power of two
-        if (valid) {
-          scores_all[size_t(tw.b) * a.L.n_pad + j] = I;
-          atomicAdd(&hist[order_key(I) >> (32 - kHistBits)], 1u);
-        }
-        ++it;
+        ++i;
         tw.next(a);
       }
-      wg_sync();
-      for (int i = tid; i < kHistBins; i += 128) {
-        const uint32_t cnt = hist[i];
-        if (cnt) atomicAdd(ghist + size_t(cur_b) * kHistBins + i, cnt);
-      }
+      grp_sync();
+      if (cur_b >= 0) flush(cur_b);
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kWarpMma) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, ncols);
   }
 
-  // ======================================================= phase 2: split by threshold
+  // ======================================================= phase 2: threshold and candidates
+  // Every block takes the same static tile range as in phase 1.  For each request
+  // it touches: the threshold bin T (the bin holding the k-th score), the count of
+  // its entries above T (kept per block, for the output offsets) and its entries
+  // in T, staged as 64-bit (score key, ~index) candidates.  Only segments whose
+  // largest key reaches T ("hit" segments) are read again; the first kSegCache of
+  // them keep their scores in shared memory for phase 3.  Phases 2 and 3 run once
+  // per launch from a cold instruction cache, so their loops stay rolled and work
+  // one entry per lane.
   grid_barrier(sm, gbar, gridDim.x, a.spin);
   const bool aborted2 = sm->abort;   // uniform: only thread 0 sets it, before the barrier's sync
-  int32_t* s_above = reinterpret_cast<int32_t*>(stages);                                   // kMaxK
-  unsigned long long* s_cand = reinterpret_cast<unsigned long long*>(stages + 4 * kMaxK);  // kCandCap
+  unsigned long long* s_cand = reinterpret_cast<unsigned long long*>(stages);   // kCandCap (phase 2)
+  unsigned long long* s_c = s_cand;                                              // kCandCap (phase 3)
+  float* s_cache = reinterpret_cast<float*>(stages + kCandCap * 8);              // kSegCache x 32
+  uint32_t* s_hs = hist;                                                         // histogram copy / counts
+  uint16_t* s_list = reinterpret_cast<uint16_t*>(hist + kHistBins);             // ordered hit list
+  const int segs_pad = a.L.n_pad / kSeg;
+  const bool seg_smem = (end - start) * 4 <= kSegCap;
+  const int nwarps = kScoreThreads / 32;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  constexpr int kChunk = kHistBins - 1;   // segments per pass (the lists hold up to 4,095)
+  uint32_t* abv_all = reinterpret_cast<uint32_t*>(a.ws + a.L.abv);
   {
     long long acc = 0;
+    uint32_t cbase = 0;   // cache slots taken by the block's earlier requests
+#pragma unroll 1
     for (int b = 0; b < a.B && acc < end && !aborted2; ++b) {
       const int nb = visible(a, b);
       const long long tb = (nb + kTileRows - 1) / kTileRows;
@@ -616,188 +757,323 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
       const float* sc = scores_all + size_t(b) * a.L.n_pad;
       if (nb <= a.k) {
         // every visible entry is selected, in order
+#pragma unroll 1
         for (long long j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
           a.topk_idx[size_t(b) * a.k + j] = static_cast<int32_t>(j);
-          if (a.topk_score) a.topk_score[size_t(b) * a.k + j] = sc[j];
+          if (a.topk_score) a.topk_score[size_t(b) * a.k + j] = __ldcg(sc + j);
         }
         continue;
       }
-      threshold_bin(sm, ghist + size_t(b) * kHistBins, a.k);
+      threshold_bin(sm, ghist + size_t(b) * kHistBins, s_hs, a.k);
       const int T = sm->T;
-      if (T < 0) continue;   // inconsistent histogram (an aborted pass)
-      if (threadIdx.x == 0) { sm->cnt[0] = 0; sm->cnt[1] = 0; }
-      __syncthreads();
       uint32_t* ctr = ctr_all + b * 4;
-      unsigned long long* cand = reinterpret_cast<unsigned long long*>(a.ws + a.L.cand) + size_t(b) * a.L.n_pad;
-      for (long long jb = j0 + threadIdx.x; jb < j1; jb += 8 * blockDim.x) {
-        float v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const long long j = jb + static_cast<long long>(u) * blockDim.x;
-          v[u] = j < j1 ? sc[j] : -INFINITY;
+      if (threadIdx.x == 0) {
+        ctr[2] = static_cast<uint32_t>(T);   // every block of the request stores the same values
+        ctr[3] = sm->above;
+        sm->cnt[0] = 0;
+        sm->cnt[1] = 0;
+      }
+      __syncthreads();
+      if (T < 0) {
+        // fewer than k binned entries (an earlier error dropped some): no selection
+#pragma unroll 1
+        for (int j = threadIdx.x; j < a.k; j += blockDim.x) {
+          a.topk_idx[size_t(b) * a.k + j] = -1;
+          if (a.topk_score) a.topk_score[size_t(b) * a.k + j] = -INFINITY;
         }
+        continue;
+      }
+      unsigned long long* cand = reinterpret_cast<unsigned long long*>(a.ws + a.L.cand) + size_t(b) * a.L.n_pad;
+      const uint32_t* smx = segmax_all + size_t(b) * segs_pad;
+      const long long g0 = j0 / kSeg, g1 = (j1 + kSeg - 1) / kSeg;
+      const long long lbase = (first - start) * 4;   // block-local index of request segment 0
+      uint32_t na = 0;
+#pragma unroll 1
+      for (long long gc = g0; gc < g1; gc += kChunk) {
+        const int nseg = static_cast<int>(min(g1, gc + kChunk) - gc);
+        // the hit segments of the chunk, in order
+        const uint32_t nhit = ordered_list(
+            sm, nseg,
+            [&](int q) {
+              const int bin = seg_smem ? static_cast<int>(s_seg[lbase + gc + q])
+                                       : static_cast<int>(__ldcg(smx + gc + q) >> (32 - kHistBits));
+              return bin >= T;
+            },
+            s_list);
+        const uint32_t ncache =
+            seg_smem && cbase < static_cast<uint32_t>(kSegCache) ? min(nhit, kSegCache - cbase) : 0u;
+        // segment table: 0 = no hit, slot + 1 = cached hit, kHitUncached
+        if (seg_smem) {
+#pragma unroll 1
+          for (int q = threadIdx.x; q < nseg; q += blockDim.x) s_seg[lbase + gc + q] = 0;
+          __syncthreads();
+#pragma unroll 1
+          for (uint32_t h = threadIdx.x; h < nhit; h += blockDim.x)
+            s_seg[lbase + gc + s_list[h]] = h < ncache ? static_cast<uint16_t>(cbase + h + 1) : kHitUncached;
+        }
+        // the cached hit segments' scores, all loads issued at once
+        {
+          float4 t4[4];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const long long j = jb + static_cast<long long>(u) * blockDim.x;
-          if (j >= j1) break;
-          const uint32_t key = order_key(v[u]);
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t x = threadIdx.x + u * kScoreThreads;
+            t4[u] = x < ncache * 8
+                        ? __ldcg(reinterpret_cast<const float4*>(sc + (gc + s_list[x >> 3]) * kSeg) + (x & 7))
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t x = threadIdx.x + u * kScoreThreads;
+            if (x < ncache * 8) reinterpret_cast<float4*>(s_cache + (cbase + (x >> 3)) * kSeg)[x & 7] = t4[u];
+          }
+#pragma unroll 1
+          for (uint32_t x = threadIdx.x + 4 * kScoreThreads; x < ncache * 8; x += blockDim.x)
+            reinterpret_cast<float4*>(s_cache + (cbase + (x >> 3)) * kSeg)[x & 7] =
+                __ldcg(reinterpret_cast<const float4*>(sc + (gc + s_list[x >> 3]) * kSeg) + (x & 7));
+        }
+        __syncthreads();
+        // one warp per hit segment, one entry per lane: count above T, stage T's entries
+#pragma unroll 1
+        for (uint32_t h = warp; h < nhit; h += nwarps) {
+          const long long g = gc + s_list[h];
+          const long long j = g * kSeg + lane;
+          const float v = h < ncache ? s_cache[(cbase + h) * kSeg + lane] : __ldcg(sc + j);
+          const uint32_t key = order_key(v);
           const int bin = static_cast<int>(key >> (32 - kHistBits));
-          if (bin > T) {
-            const uint32_t pos = atomicAdd(&sm->cnt[0], 1u);
-            if (pos < kMaxK) s_above[pos] = static_cast<int32_t>(j);
-          } else if (bin == T) {
-            const unsigned long long k64 =
-                (static_cast<unsigned long long>(key) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(j));
-            const uint32_t pos = atomicAdd(&sm->cnt[1], 1u);
-            if (pos < kCandCap) {
-              s_cand[pos] = k64;
-            } else {
-              const uint32_t gp = atomicAdd(&ctr[1], 1u);   // rare: many ties in one bin
-              if (gp < static_cast<uint32_t>(a.L.n_pad)) cand[gp] = k64;
+          const bool ok = j < j1;
+          na += __popc(__ballot_sync(0xFFFFFFFFu, ok && bin > T));
+          const unsigned cm = __ballot_sync(0xFFFFFFFFu, ok && bin == T);
+          if (cm) {
+            uint32_t base0 = 0;
+            if (lane == 0) base0 = atomicAdd(&sm->cnt[1], static_cast<uint32_t>(__popc(cm)));
+            base0 = __shfl_sync(0xFFFFFFFFu, base0, 0);
+            if ((cm >> lane) & 1u) {
+              const uint32_t pos = base0 + __popc(cm & lt_mask);
+              const unsigned long long k64 =
+                  (static_cast<unsigned long long>(key) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(j));
+              if (pos < kCandCap) {
+                s_cand[pos] = k64;
+              } else {
+                const uint32_t gp = atomicAdd(&ctr[1], 1u);   // rare: many ties in one bin
+                if (gp < static_cast<uint32_t>(a.L.n_pad)) cand[gp] = k64;
+              }
             }
           }
         }
+        cbase += ncache;
+        __syncthreads();
       }
+      if (lane == 0 && na) atomicAdd(&sm->cnt[0], na);
       __syncthreads();
       if (threadIdx.x == 0) {
-        const uint32_t na = min(sm->cnt[0], static_cast<uint32_t>(kMaxK));
+        abv_all[size_t(b) * kMaxGrid + blockIdx.x] = sm->cnt[0];
         const uint32_t nc = min(sm->cnt[1], static_cast<uint32_t>(kCandCap));
-        sm->cnt[0] = na;
         sm->cnt[1] = nc;
-        sm->base[0] = na ? atomicAdd(&ctr[0], na) : 0;
         sm->base[1] = nc ? atomicAdd(&ctr[1], nc) : 0;
       }
       __syncthreads();
-      int32_t* sel = reinterpret_cast<int32_t*>(a.ws + a.L.sel) + size_t(b) * a.k;
-      for (uint32_t i = threadIdx.x; i < sm->cnt[0]; i += blockDim.x)
-        if (sm->base[0] + i < static_cast<uint32_t>(a.k)) sel[sm->base[0] + i] = s_above[i];
-      for (uint32_t i = threadIdx.x; i < sm->cnt[1]; i += blockDim.x)
-        if (sm->base[1] + i < static_cast<uint32_t>(a.L.n_pad)) cand[sm->base[1] + i] = s_cand[i];
+#pragma unroll 1
+      for (uint32_t x = threadIdx.x; x < sm->cnt[1]; x += blockDim.x)
+        if (sm->base[1] + x < static_cast<uint32_t>(a.L.n_pad)) cand[sm->base[1] + x] = s_cand[x];
       __syncthreads();
     }
   }
 
-  // ======================================================= phase 3: finish each request
+  // ======================================================= phase 3: ordered output
+  // Each block finds the exact cut among the request's candidates (a radix select
+  // over the 64-bit keys; every block of the request computes the same cut), its
+  // output offset (selected entries of the request before its range) and writes
+  // its own selected entries in entry order: no sort is needed.
   grid_barrier(sm, gbar, 2 * gridDim.x, a.spin);
   const bool aborted3 = sm->abort;
-  int32_t* s_sorted = reinterpret_cast<int32_t*>(stages);                                // kMaxK
-  unsigned long long* s_c = reinterpret_cast<unsigned long long*>(stages + 4 * kMaxK);   // kCandCap
+  // padding of requests with fewer than k visible entries (-1 after them)
+#pragma unroll 1
   for (int b = blockIdx.x; b < a.B && !aborted3; b += gridDim.x) {
     const int nb = visible(a, b);
-    const float* sc = scores_all + size_t(b) * a.L.n_pad;
-    if (nb <= a.k) {
-      for (int j = nb + threadIdx.x; j < a.k; j += blockDim.x) {
-        a.topk_idx[size_t(b) * a.k + j] = -1;
-        if (a.topk_score) a.topk_score[size_t(b) * a.k + j] = -INFINITY;
-      }
-      continue;
+    if (nb >= a.k) continue;
+#pragma unroll 1
+    for (int j = nb + threadIdx.x; j < a.k; j += blockDim.x) {
+      a.topk_idx[size_t(b) * a.k + j] = -1;
+      if (a.topk_score) a.topk_score[size_t(b) * a.k + j] = -INFINITY;
     }
-    uint32_t* ctr = ctr_all + b * 4;
-    int32_t* sel = reinterpret_cast<int32_t*>(a.ws + a.L.sel) + size_t(b) * a.k;
-    const unsigned long long* gcand =
-        reinterpret_cast<const unsigned long long*>(a.ws + a.L.cand) + size_t(b) * a.L.n_pad;
-    const uint32_t above = min(ld_acquire(&ctr[0]), static_cast<uint32_t>(a.k));
-    const uint32_t c = min(ld_acquire(&ctr[1]), static_cast<uint32_t>(a.L.n_pad));
-    const bool in_smem = c <= static_cast<uint32_t>(kCandCap);
-    if (in_smem)
-      for (uint32_t i = threadIdx.x; i < c; i += blockDim.x) s_c[i] = __ldcg(gcand + i);
-    const unsigned long long* cp = in_smem ? s_c : gcand;
-    if (threadIdx.x == 0) {
-      sm->need = min(static_cast<uint32_t>(a.k) - above, c);
-      sm->done = 0;
-      sm->out = 0;
-      sm->mask = c > 0 ? (~0ull << 52) : 0;   // the 12 histogram bits are shared
-      sm->prefix = c > 0 ? (__ldcg(gcand) & sm->mask) : 0;
-    }
-    __syncthreads();
-    // radix passes over the remaining 52 key bits (8-bit digits, a last 4-bit one)
-    for (int shift = 44; shift >= 0; shift = shift >= 8 ? shift - 8 : (shift > 0 ? 0 : -1)) {
-      if (sm->done || sm->need == 0) break;
-      const int width = shift >= 4 ? 8 : 4;
-      const unsigned long long dmask = ((1ull << width) - 1) << shift;
-      for (int i = threadIdx.x; i < 256; i += blockDim.x) sm->dh[i] = 0;
-      __syncthreads();
-      const unsigned long long pm = sm->mask, pp = sm->prefix;
-      for (uint32_t i = threadIdx.x; i < c; i += blockDim.x) {
-        const unsigned long long key = in_smem ? cp[i] : __ldcg(cp + i);
-        if ((key & pm) == pp) atomicAdd(&sm->dh[(key & dmask) >> shift], 1u);
+  }
+  {
+    long long acc = 0;
+#pragma unroll 1
+    for (int b = 0; b < a.B && acc < end && !aborted3; ++b) {
+      const int nb = visible(a, b);
+      const long long tb = (nb + kTileRows - 1) / kTileRows;
+      const long long s0 = max(start, acc), s1 = min(end, acc + tb);
+      const long long first = acc;
+      acc += tb;
+      if (s0 >= s1 || nb <= a.k) continue;
+      const uint32_t* ctr = ctr_all + b * 4;
+      const long long fb = first / per;   // the first block holding tiles of request b
+      // one round trip: the request's counters and the lower blocks' above-T counts
+      const int T = static_cast<int>(__ldcg(ctr + 2));
+      const uint32_t above = min(__ldcg(ctr + 3), static_cast<uint32_t>(a.k));
+      const uint32_t c = min(__ldcg(ctr + 1), static_cast<uint32_t>(a.L.n_pad));
+      uint32_t part = 0;
+#pragma unroll 1
+      for (long long q = fb + threadIdx.x; q < blockIdx.x; q += blockDim.x)
+        part += __ldcg(abv_all + size_t(b) * kMaxGrid + q);
+      if (T < 0) continue;   // uniform: the same word for every thread
+      const long long j0 = (s0 - first) * kTileRows;
+      const long long j1 = min((s1 - first) * kTileRows, static_cast<long long>(nb));
+      const float* sc = scores_all + size_t(b) * a.L.n_pad;
+      const unsigned long long* gcand =
+          reinterpret_cast<const unsigned long long*>(a.ws + a.L.cand) + size_t(b) * a.L.n_pad;
+      const bool in_smem = c <= static_cast<uint32_t>(kCandCap);
+      if (in_smem) {
+        unsigned long long t4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t x = threadIdx.x + u * kScoreThreads;
+          t4[u] = x < c ? __ldcg(gcand + x) : 0ull;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t x = threadIdx.x + u * kScoreThreads;
+          if (x < c) s_c[x] = t4[u];
+        }
+#pragma unroll 1
+        for (uint32_t x = threadIdx.x + 4 * kScoreThreads; x < c; x += blockDim.x) s_c[x] = __ldcg(gcand + x);
+      }
+      if (threadIdx.x == 0) {
+        sm->need = min(static_cast<uint32_t>(a.k) - above, c);
+        sm->done = 0;
+        sm->out = 0;
+        sm->mask = ~0ull << 52;   // the 12 histogram bits are T for every candidate
+        sm->prefix = static_cast<unsigned long long>(T) << 52;
       }
       __syncthreads();
-      if (threadIdx.x < 32) {
-        // lane l owns digits (from the top) nd-1-8l .. nd-8-8l; find the digit holding the need-th key
-        const int nd = 1 << width;
-        uint32_t loc[8], sum = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int dg = nd - 1 - 8 * lane - i;
-          loc[i] = dg >= 0 ? sm->dh[dg] : 0;
-          sum += loc[i];
+      // radix passes over the remaining 52 key bits (8-bit digits, a last 4-bit one)
+#pragma unroll 1
+      for (int shift = 44; shift >= 0; shift = shift >= 8 ? shift - 8 : (shift > 0 ? 0 : -1)) {
+        if (sm->done || sm->need == 0) break;
+        const int width = shift >= 4 ? 8 : 4;
+        const unsigned long long dmask = ((1ull << width) - 1) << shift;
+        for (int x = threadIdx.x; x < 256; x += blockDim.x) sm->dh[x] = 0;
+        __syncthreads();
+        const unsigned long long pm = sm->mask, pp = sm->prefix;
+#pragma unroll 1
+        for (uint32_t x = threadIdx.x; x < c; x += blockDim.x) {
+          const unsigned long long key = in_smem ? s_c[x] : __ldcg(gcand + x);
+          if ((key & pm) == pp) atomicAdd(&sm->dh[(key & dmask) >> shift], 1u);
         }
-        uint32_t incl = sum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-          if (lane >= o) incl += v;
-        }
-        const uint32_t need = sm->need;
-        const unsigned hit = __ballot_sync(0xFFFFFFFFu, incl >= need);
-        const int Ln = hit ? __ffs(hit) - 1 : 31;
-        if (lane == Ln) {
-          uint32_t accd = incl - sum;
-          int d = 0;
-          for (int i = 0; i < 8; ++i) {
-            const int dg = nd - 1 - 8 * lane - i;
-            if (dg < 0) break;
-            if (accd + loc[i] >= need || dg == 0) { d = dg; break; }
-            accd += loc[i];
+        __syncthreads();
+        if (threadIdx.x < 32) {
+          // lane l owns digits (from the top) nd-1-8l .. nd-8-8l; find the digit holding the need-th key
+          const int nd = 1 << width;
+          uint32_t sum = 0;
+#pragma unroll 1
+          for (int x = 0; x < 8; ++x) {
+            const int dg = nd - 1 - 8 * lane - x;
+            if (dg >= 0) sum += sm->dh[dg];
           }
-          sm->need = need - accd;
-          sm->prefix = pp | (static_cast<unsigned long long>(d) << shift);
-          sm->mask = pm | dmask;
-          if (sm->dh[d] == need - accd) sm->done = 1;
+          uint32_t incl = sum;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += v;
+          }
+          const uint32_t need = sm->need;
+          const unsigned hit = __ballot_sync(0xFFFFFFFFu, incl >= need);
+          const int Ln = hit ? __ffs(hit) - 1 : 31;
+          if (lane == Ln) {
+            uint32_t accd = incl - sum;
+            int d = 0;
+#pragma unroll 1
+            for (int x = 0; x < 8; ++x) {
+              const int dg = nd - 1 - 8 * lane - x;
+              if (dg < 0) break;
+              const uint32_t y = sm->dh[dg];
+              if (accd + y >= need || dg == 0) { d = dg; break; }
+              accd += y;
+            }
+            sm->need = need - accd;
+            sm->prefix = pp | (static_cast<unsigned long long>(d) << shift);
+            sm->mask = pm | dmask;
+            if (sm->dh[d] == need - accd) sm->done = 1;
+          }
         }
+        __syncthreads();
+        if (shift == 0) break;
       }
-      __syncthreads();
-      if (shift == 0) break;
-    }
-    {
+      // selected  <=>  (key64 & pm) >= pp   (entries above T included)
       const unsigned long long pm = sm->mask, pp = sm->prefix;
-      const uint32_t room = static_cast<uint32_t>(a.k) - above;
-      for (uint32_t i = threadIdx.x; i < c; i += blockDim.x) {
-        const unsigned long long key = in_smem ? cp[i] : __ldcg(cp + i);
-        if ((key & pm) >= pp) {
-          const uint32_t pos = atomicAdd(&sm->out, 1u);
-          if (pos < room) sel[above + pos] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(key));
-        }
+      // offset: selected entries of this request before j0 = the above-T counts of
+      // the lower blocks + the selected candidates before j0
+#pragma unroll 1
+      for (uint32_t x = threadIdx.x; x < c; x += blockDim.x) {
+        const unsigned long long key = in_smem ? s_c[x] : __ldcg(gcand + x);
+        const long long j = 0xFFFFFFFFu - static_cast<uint32_t>(key);
+        if ((key & pm) >= pp && j < j0) ++part;
       }
-    }
-    __syncthreads();
-    // ascending order of the k selected entries (bitonic; padded with INT_MAX)
-    int P = 1;
-    while (P < a.k) P <<= 1;
-    const uint32_t filled = min(static_cast<uint32_t>(a.k), above + sm->out);
-    for (int i = threadIdx.x; i < P; i += blockDim.x)
-      s_sorted[i] = (i < static_cast<int>(filled)) ? __ldcg(sel + i) : 0x7FFFFFFF;
-    __syncthreads();
-    for (int size = 2; size <= P; size <<= 1) {
-      for (int stride = size >> 1; stride > 0; stride >>= 1) {
-        for (int i = threadIdx.x; i < P / 2; i += blockDim.x) {
-          const int lo = 2 * i - (i & (stride - 1));
-          const int hi = lo + stride;
-          const bool up = (lo & size) == 0;
-          const int x = s_sorted[lo], y = s_sorted[hi];
-          if ((x > y) == up) { s_sorted[lo] = y; s_sorted[hi] = x; }
+      if (part) atomicAdd(&sm->out, part);
+      __syncthreads();
+      uint32_t running = sm->out;
+      const uint32_t* smx = segmax_all + size_t(b) * segs_pad;
+      const long long g0 = j0 / kSeg, g1 = (j1 + kSeg - 1) / kSeg;
+      const long long lbase = (first - start) * 4;
+      uint32_t* s_cnt = s_hs;   // per hit segment: its count (+ a trailing 0), then the exclusive scan
+#pragma unroll 1
+      for (long long gc = g0; gc < g1; gc += kChunk) {
+        const int nseg = static_cast<int>(min(g1, gc + kChunk) - gc);
+        const uint32_t nhit = ordered_list(
+            sm, nseg,
+            [&](int q) {
+              return seg_smem ? s_seg[lbase + gc + q] != 0
+                              : static_cast<int>(__ldcg(smx + gc + q) >> (32 - kHistBits)) >= T;
+            },
+            s_list);
+        // the value of lane `lane` of hit segment h (shared-memory cache or global)
+        auto value = [&](uint32_t h, long long& j) -> float {
+          const long long g = gc + s_list[h];
+          j = g * kSeg + lane;
+          int slot = -1;
+          if (seg_smem) {
+            const uint16_t info = s_seg[lbase + g];
+            if (info != kHitUncached) slot = info - 1;
+          }
+          return slot >= 0 ? s_cache[slot * kSeg + lane] : __ldcg(sc + j);
+        };
+        // counts: one warp per hit segment, one entry per lane
+#pragma unroll 1
+        for (uint32_t h = warp; h < nhit; h += nwarps) {
+          long long j;
+          const float v = value(h, j);
+          const unsigned long long k64 = (static_cast<unsigned long long>(order_key(v)) << 32) |
+                                         (0xFFFFFFFFu - static_cast<uint32_t>(j));
+          const uint32_t n = __popc(__ballot_sync(0xFFFFFFFFu, j < j1 && (k64 & pm) >= pp));
+          if (lane == 0) s_cnt[h] = n;
         }
+        if (threadIdx.x == 0) s_cnt[nhit] = 0;
+        __syncthreads();
+        block_exclusive_scan(sm, s_cnt, static_cast<int>(nhit) + 1);   // s_cnt[nhit] = the chunk's total
+        // write: the selected entries of each hit segment at running + its prefix + rank
+#pragma unroll 1
+        for (uint32_t h = warp; h < nhit; h += nwarps) {
+          const uint32_t pre = s_cnt[h];
+          if (s_cnt[h + 1] == pre) continue;   // no selected entry in this segment
+          long long j;
+          const float v = value(h, j);
+          const unsigned long long k64 = (static_cast<unsigned long long>(order_key(v)) << 32) |
+                                         (0xFFFFFFFFu - static_cast<uint32_t>(j));
+          const bool sel = j < j1 && (k64 & pm) >= pp;
+          const unsigned m = __ballot_sync(0xFFFFFFFFu, sel);
+          if (sel) {
+            const uint32_t pos = running + pre + __popc(m & lt_mask);
+            if (pos < static_cast<uint32_t>(a.k)) {
+              a.topk_idx[size_t(b) * a.k + pos] = static_cast<int32_t>(j);
+              if (a.topk_score) a.topk_score[size_t(b) * a.k + pos] = v;
+            }
+          }
+        }
+        running += s_cnt[nhit];
         __syncthreads();
       }
     }
-    for (int i = threadIdx.x; i < a.k; i += blockDim.x) {
-      const int v = s_sorted[i];
-      const bool ok = v != 0x7FFFFFFF && v >= 0 && v < nb;
-      a.topk_idx[size_t(b) * a.k + i] = ok ? v : -1;
-      if (a.topk_score) a.topk_score[size_t(b) * a.k + i] = ok ? __ldcg(sc + v) : -INFINITY;
-    }
-    __syncthreads();
   }
 }
 
@@ -829,8 +1105,10 @@ size_t score_smem_bytes() {
   constexpr int kStageBytes = FP8 ? kTileRows * 128 : kTileRows * 256;
   constexpr int kStages = FP8 ? kStagesFp8 : kStagesBf16;
   constexpr int kQImage = FP8 ? kQImageFp8 : kQImageBf16;
-  return 1024 + kStages * kStageBytes + 2 * kQImage + kHistBins * 4 + kScaleSlots * kTileRows * 4 +
-         sizeof(ScoreSmem);
+  static_assert(kCandCap * 8 + kSegCache * kSeg * 4 <= kProducers * kStages * kStageBytes,
+                "selection buffers reuse the stage ring");
+  return 1024 + kProducers * kStages * kStageBytes + 2 * kQImage + kGroups * kHistBins * 4 +
+         kScaleSlots * kTileRows * 4 + kSegCap * 2 + sizeof(ScoreSmem);
 }
 
 // Cooperative launch of the score kernel: the selection phases meet at grid
@@ -845,9 +1123,11 @@ cudaError_t launch_score(const CUtensorMap& tmap, const IndexArgs& a, cudaStream
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, index_score_kernel<FP8>, kScoreThreads, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
-  per_sm = per_sm > 2 ? 2 : per_sm;   // TMEM: two blocks of at most 256 columns per SM
+  // one block per SM: it allocates all 512 TMEM columns and most of shared memory
+  const int grid = sm_count();
+  if (grid > kMaxGrid) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(sm_count() * per_sm);
+  cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kScoreThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
