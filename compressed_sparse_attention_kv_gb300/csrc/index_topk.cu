@@ -55,6 +55,8 @@ constexpr int kStagesFp8 = 4;        // per producer, 16 KiB stages
 constexpr int kStagesBf16 = 2;       // per producer, 32 KiB stages
 constexpr int kAccs = 8;             // TMEM accumulators in flight (8 x 64 columns)
 constexpr int kScaleSlots = 16;      // ring of per-tile scale rows (2 pages x 64 fp32)
+constexpr int kPairSlots = 8;        // tile pairs in flight from the scheduling producer to the other
+constexpr int kChunkTiles = 4;       // tiles per grab from a request's work counter
 constexpr int kWarpMma = kProducers;
 constexpr int kWarpEpi = kProducers + 1;
 constexpr int kScoreThreads = 32 * (kProducers + 1 + 4 * kGroups);   // 352
@@ -182,12 +184,14 @@ struct ScoreSmem {
   uint64_t accfull[kAccs], accempty[kAccs];
   uint64_t qfull[2], qempty[2];
   uint64_t sfull[kScaleSlots], sempty[kScaleSlots];
+  uint64_t pfull[kPairSlots], pempty[kPairSlots];   // tile pairs handed from producer 0 to 1
   uint64_t drain;
   uint64_t hbar[kGroups];          // an epilogue group's warps meet here at a request switch
+  int4 pair[kPairSlots];           // (request, tile, page id, page id) handed to producer 1; request -1 = the end
+  int2 tinfo[kScaleSlots];         // (request, tile) of each tile in flight; request -1 = the end
   uint32_t tmem_base;
   volatile int abort;
   int smask[kScaleSlots];          // per tile: bit p = page p of the tile was loaded
-  int ptab[kProducers][64];        // each producer's prefetched page ids of its current request
   __align__(16) float wq[kGroups][64];   // folded head weights of each group's current request
   // selection phases
   uint32_t cnt[2];
@@ -199,41 +203,6 @@ struct ScoreSmem {
   unsigned long long prefix, mask;
   uint32_t part[256];
   uint32_t dh[256];
-};
-
-// Walks the global tile sequence [start, end) over requests (tiles of request b
-// are ceil(n_b / 128)); every role keeps its own walker.
-struct TileWalker {
-  int b, t, tiles_b, n_b;
-  long long g, end;
-  __device__ void init(const IndexArgs& a, long long start, long long end_) {
-    g = start;
-    end = end_;
-    long long acc = 0;
-    t = 0;
-    n_b = 0;
-    tiles_b = 0;
-    for (b = 0; b < a.B; ++b) {
-      n_b = visible(a, b);
-      tiles_b = (n_b + kTileRows - 1) / kTileRows;
-      if (start < acc + tiles_b) { t = static_cast<int>(start - acc); return; }
-      acc += tiles_b;
-    }
-  }
-  __device__ bool valid() const { return g < end; }
-  // advance; returns true if the request changed
-  __device__ bool next(const IndexArgs& a) {
-    ++g;
-    if (g >= end) return false;
-    if (++t < tiles_b) return false;
-    t = 0;
-    do {
-      ++b;
-      n_b = visible(a, b);
-      tiles_b = (n_b + kTileRows - 1) / kTileRows;
-    } while (tiles_b == 0 && b < a.B - 1);
-    return true;
-  }
 };
 
 __device__ __forceinline__ bool role_wait(ScoreSmem* sm, uint64_t* bar, uint32_t parity,
@@ -423,8 +392,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   uint8_t* qbuf = stages + kProducers * kStages * kStageBytes;             // 2 x kQImage
   uint32_t* hist = reinterpret_cast<uint32_t*>(qbuf + 2 * kQImage);       // kGroups x 4096 bins
   float* sring = reinterpret_cast<float*>(hist + kGroups * kHistBins);    // kScaleSlots x 128 fp32
-  // per segment of the block's range: the bin of its largest key (phase 1), then
-  // 0 / cache slot + 1 / kHitUncached (phase 2 -> 3)
+  // per segment of the block's (static) range in phases 2 and 3: the bin of its
+  // largest key, then 0 / cache slot + 1 / kHitUncached
   uint16_t* s_seg = reinterpret_cast<uint16_t*>(sring + kScaleSlots * kTileRows);   // kSegCap
   ScoreSmem* sm = reinterpret_cast<ScoreSmem*>(s_seg + kSegCap);
 
@@ -449,6 +418,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     for (int c = 0; c < kAccs; ++c) { mbar_init(&sm->accfull[c], 1); mbar_init(&sm->accempty[c], 4); }
     for (int c = 0; c < 2; ++c) { mbar_init(&sm->qfull[c], 1); mbar_init(&sm->qempty[c], 1); }
     for (int s = 0; s < kScaleSlots; ++s) { mbar_init(&sm->sfull[s], 1); mbar_init(&sm->sempty[s], 4); }
+    for (int s = 0; s < kPairSlots; ++s) { mbar_init(&sm->pfull[s], 1); mbar_init(&sm->pempty[s], 1); }
     mbar_init(&sm->drain, 1);
     for (int g = 0; g < kGroups; ++g) mbar_init(&sm->hbar[g], 4);
     sm->abort = 0;
@@ -464,96 +434,156 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   const uint32_t tmem = sm->tmem_base;
 
   // ======================================================= phase 1: scores
-  // Block-local tile i (the i-th tile of [start, end)) is loaded by producer i % 2
-  // into stage (i / 2) % kStages of its ring, scored into accumulator i % 8 and
-  // read back by epilogue group i % 2; its scales use slot i % 16.
+  // Tiles are handed out dynamically, in pairs of consecutive tiles of one request:
+  // producer 0 grabs a pair from the request's counter (starting at a home request
+  // spread over the grid, moving on when it is exhausted), keeps the first tile and
+  // hands the second to producer 1.  Block-local tile i goes through producer i % 2
+  // (stage (i / 2) % kStages of its ring), accumulator i % 8, epilogue group i % 2
+  // and slot i % 16 of the scale and tile-info rings.  A tile past the end of its
+  // request is a hole (no pages, no entries); request -1 ends the sequence.
   if (warp < kProducers) {
     // ------------------------------------------------------------ producers
     const int pw = warp;
-    if (lane == 0 && start < end) {
+    if (lane == 0) {
       prefetch_tmap(&tmap);
-      TileWalker tw;
-      tw.init(a, start, end);
-      long long i = 0, np = 0;
-      int nreq = 0;
-      bool need_q = pw == 0;
-      int pt_b = -1;           // request and first logical page of this producer's ptab
-      long long pt_lp = 0;
-      bool ok = true;
-      while (tw.valid() && ok) {
-        if (need_q) {
-          // query image of the new request into buffer nreq % 2 (producer 0 only)
-          const int qb = nreq & 1;
-          if (nreq >= 2 && !role_wait(sm, &sm->qempty[qb], ((nreq >> 1) - 1) & 1, a.spin)) break;
-          mbar_expect_tx(&sm->qfull[qb], kQImage);
-          bulk_g2s(qbuf + qb * kQImage, a.ws + a.L.qimg + size_t(tw.b) * kQSlot, kQImage, &sm->qfull[qb]);
-          ++nreq;
-          need_q = false;
+      long long np = 0;       // tiles this producer posted (the end marker included)
+      int nreq = 0;           // query images loaded (producer 0)
+      // post local tile i = (request b, tile t) with its two page ids (-2: no page,
+      // -3: page outside the block table); b < 0 posts the end marker
+      auto post = [&](long long i, int b, int t, int id0, int id1) -> bool {
+        const int s = static_cast<int>(np % kStages);
+        const long long round = np / kStages;
+        if (round > 0 && !role_wait(sm, &sm->empty[pw][s], (round - 1) & 1, a.spin)) return false;
+        const int ss = static_cast<int>(i % kScaleSlots);
+        const long long su = i / kScaleSlots;
+        if (su > 0 && !role_wait(sm, &sm->sempty[ss], (su - 1) & 1, a.spin)) return false;
+        uint8_t* dst = stages + (pw * kStages + s) * kStageBytes;
+        uint32_t bytes = 0;
+        int pages[2] = {b >= 0 ? id0 : -2, b >= 0 ? id1 : -2};
+        for (int pg = 0; pg < 2; ++pg) {
+          if (pages[pg] == -2) continue;
+          if (pages[pg] < 0 || pages[pg] >= a.keys.num_pages) {
+            set_err(CSKV_ERR_BOUNDS);
+            pages[pg] = -2;
+            continue;
+          }
+          bytes += FP8 ? 64 * 128 : 64 * 256;
         }
-        if ((i & 1) == pw) {
-          const int s = static_cast<int>(np % kStages);
-          const long long round = np / kStages;
-          if (round > 0 && !role_wait(sm, &sm->empty[pw][s], (round - 1) & 1, a.spin)) break;
-          const int ss = static_cast<int>(i % kScaleSlots);
-          const long long su = i / kScaleSlots;
-          if (su > 0 && !role_wait(sm, &sm->sempty[ss], (su - 1) & 1, a.spin)) break;
-          uint8_t* dst = stages + (pw * kStages + s) * kStageBytes;
-          uint32_t bytes = 0;
-          int pages[2] = {-1, -1};
-          const long long lp0 = static_cast<long long>(tw.t) * 2;
-          int* ptab = sm->ptab[pw];
-          if (tw.b != pt_b || lp0 < pt_lp || lp0 + 1 >= pt_lp + 64) {
-            // refill: 64 page ids of this request, two batches of 32 loads in flight
-            pt_b = tw.b;
-            pt_lp = lp0;
-            const int32_t* bt = a.keys.block_table + static_cast<long long>(tw.b) * a.keys.max_pages;
+        sm->tinfo[ss] = make_int2(b, t);
+        sm->smask[ss] = (pages[0] >= 0 ? 1 : 0) | (pages[1] >= 0 ? 2 : 0);
+        mbar_expect_tx(&sm->full[pw][s], bytes);
+        mbar_expect_tx(&sm->sfull[ss], FP8 ? (pages[0] >= 0 ? 256u : 0u) + (pages[1] >= 0 ? 256u : 0u) : 0u);
+        for (int pg = 0; pg < 2; ++pg) {
+          if (pages[pg] < 0) continue;
+          tma_load_3d(dst + pg * 8192, &tmap, 0, 0, pages[pg], &sm->full[pw][s]);
+          if (!FP8) tma_load_3d(dst + 16384 + pg * 8192, &tmap, 64, 0, pages[pg], &sm->full[pw][s]);
+          if (FP8) {
+            const uint8_t* pgp = static_cast<const uint8_t*>(a.keys.pool) + size_t(pages[pg]) * a.keys.page_bytes;
+            bulk_g2s(sring + ss * kTileRows + pg * kPageRows, pgp + kPageRows * 128, 256, &sm->sfull[ss]);
+          }
+        }
+        ++np;
+        return true;
+      };
+      if (pw == 0) {
+        // Scheduler.  Work comes in chunks of kChunkTiles consecutive tiles of one
+        // request, grabbed from the request's counter; the chunk after next is
+        // grabbed, and the next chunk's page ids loaded, while the current one is
+        // posted, so neither the atomic nor the block-table loads stall the stream.
+        auto tiles_of = [&](int b) { return (visible(a, b) + kTileRows - 1) / kTileRows; };
+        // the chunk's 2 x kChunkTiles page ids, all loads in flight
+        auto chunk_ids = [&](int b, int t0, int (&ids)[2 * kChunkTiles]) {
+          const int n_b = b >= 0 ? visible(a, b) : 0;
+          const int32_t* bt = a.keys.block_table + static_cast<long long>(b < 0 ? 0 : b) * a.keys.max_pages;
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-              int ids[32];
+          for (int u = 0; u < 2 * kChunkTiles; ++u) {
+            const long long lp = static_cast<long long>(t0) * 2 + u;
+            ids[u] = (b < 0 || lp * kPageRows >= n_b) ? -2 : (lp >= a.keys.max_pages ? -3 : bt[lp]);
+          }
+        };
+        int req = static_cast<int>((static_cast<long long>(blockIdx.x) * a.B) / gridDim.x);
+        uint32_t pending = atomicAdd(&ctr_all[req * 4], static_cast<uint32_t>(kChunkTiles));
+        // the next chunk: (request, first tile) from the pending grab; request -1 = none left
+        auto resolve = [&](int& b, int& t0) {
+          int tiles = tiles_of(req);
+          int fails = 0;
+          while (pending >= static_cast<uint32_t>(tiles) && ++fails < a.B) {
+            req = (req + 1) % a.B;
+            tiles = tiles_of(req);
+            pending = atomicAdd(&ctr_all[req * 4], static_cast<uint32_t>(kChunkTiles));
+          }
+          if (pending >= static_cast<uint32_t>(tiles)) {
+            b = -1;
+            t0 = 0;
+          } else {
+            b = req;
+            t0 = static_cast<int>(pending);
+            pending = atomicAdd(&ctr_all[req * 4], static_cast<uint32_t>(kChunkTiles));
+          }
+        };
+        int cb, ct;
+        resolve(cb, ct);
+        int ids[2 * kChunkTiles];
+        chunk_ids(cb, ct, ids);
+        int q_b = -1;
+        long long m = 0;   // pairs posted
+        bool ok = true;
+        while (ok) {
+          int nb2 = -1, nt = 0;
+          int nids[2 * kChunkTiles];
+          if (cb >= 0) {
+            resolve(nb2, nt);   // usually already returned: grabbed one chunk ago
+            chunk_ids(nb2, nt, nids);
+          }
+          if (cb >= 0 && cb != q_b) {
+            // query image of the new request into buffer nreq % 2
+            const int qb = nreq & 1;
+            if (nreq >= 2 && !role_wait(sm, &sm->qempty[qb], ((nreq >> 1) - 1) & 1, a.spin)) break;
+            mbar_expect_tx(&sm->qfull[qb], kQImage);
+            bulk_g2s(qbuf + qb * kQImage, a.ws + a.L.qimg + size_t(cb) * kQSlot, kQImage, &sm->qfull[qb]);
+            ++nreq;
+            q_b = cb;
+          }
+          // the chunk's pairs: the first tile here, the second handed to producer 1
 #pragma unroll
-              for (int u = 0; u < 32; ++u) {
-                const long long lp = lp0 + 32 * h2 + u;
-                ids[u] = (lp * kPageRows < tw.n_b && lp < a.keys.max_pages) ? bt[lp] : -2;
-              }
-#pragma unroll
-              for (int u = 0; u < 32; ++u) ptab[32 * h2 + u] = ids[u];
+          for (int pr = 0; pr < kChunkTiles / 2; ++pr, ++m) {
+            if (pr > 0 && cb < 0) break;   // the end marker is one pair
+            const int hs = static_cast<int>(m % kPairSlots);
+            if (m >= kPairSlots && !role_wait(sm, &sm->pempty[hs], ((m / kPairSlots) - 1) & 1, a.spin)) {
+              ok = false;
+              break;
+            }
+            const int t = ct + 2 * pr;
+            sm->pair[hs] = make_int4(cb, t + 1, ids[4 * pr + 2], ids[4 * pr + 3]);
+            mbar_arrive(&sm->pfull[hs]);
+            if (!post(2 * m, cb, t, ids[4 * pr], ids[4 * pr + 1])) {
+              ok = false;
+              break;
             }
           }
-          for (int pg = 0; pg < 2; ++pg) {
-            const long long lp = lp0 + pg;
-            if (lp * kPageRows >= tw.n_b) continue;
-            if (lp >= a.keys.max_pages) { set_err(CSKV_ERR_BOUNDS); continue; }
-            const int pid = ptab[lp - pt_lp];
-            if (pid < 0 || pid >= a.keys.num_pages) { set_err(CSKV_ERR_BOUNDS); continue; }
-            pages[pg] = pid;
-            bytes += FP8 ? 64 * 128 : 64 * 256;
-          }
-          sm->smask[ss] = (pages[0] >= 0 ? 1 : 0) | (pages[1] >= 0 ? 2 : 0);
-          mbar_expect_tx(&sm->full[pw][s], bytes);
-          mbar_expect_tx(&sm->sfull[ss], FP8 ? (pages[0] >= 0 ? 256u : 0u) + (pages[1] >= 0 ? 256u : 0u) : 0u);
-          for (int pg = 0; pg < 2; ++pg) {
-            if (pages[pg] < 0) continue;
-            tma_load_3d(dst + pg * 8192, &tmap, 0, 0, pages[pg], &sm->full[pw][s]);
-            if (!FP8) tma_load_3d(dst + 16384 + pg * 8192, &tmap, 64, 0, pages[pg], &sm->full[pw][s]);
-            if (FP8) {
-              const uint8_t* pgp = static_cast<const uint8_t*>(a.keys.pool) + size_t(pages[pg]) * a.keys.page_bytes;
-              bulk_g2s(sring + ss * kTileRows + pg * kPageRows, pgp + kPageRows * 128, 256, &sm->sfull[ss]);
-            }
-          }
-          ++np;
+          if (cb < 0) break;
+          cb = nb2;
+          ct = nt;
+#pragma unroll
+          for (int u = 0; u < 2 * kChunkTiles; ++u) ids[u] = nids[u];
         }
-        ++i;
-        if (tw.next(a) && pw == 0) need_q = true;
+      } else {
+        for (long long m = 0;; ++m) {
+          const int hs = static_cast<int>(m % kPairSlots);
+          if (!role_wait(sm, &sm->pfull[hs], (m / kPairSlots) & 1, a.spin)) break;
+          const int4 pr = sm->pair[hs];
+          mbar_arrive(&sm->pempty[hs]);
+          if (!post(2 * m + 1, pr.x, pr.y, pr.z, pr.w) || pr.x < 0) break;
+        }
       }
       // drain: every copy this producer issued must land before the block moves on
       for (int s = 0; s < kStages && s < np; ++s) {
         const long long uses = (np - s + kStages - 1) / kStages;
         mbar_wait(&sm->full[pw][s], (uses - 1) & 1, kDefaultSpinLimit);
       }
-      const long long nsc = (np > 0) ? 2 * (np - 1) + pw + 1 : 0;   // tiles up to this producer's last
-      for (int ss = pw; ss < kScaleSlots; ss += 2) {
-        const long long uses = nsc > ss ? (nsc - ss + kScaleSlots - 1) / kScaleSlots : 0;
-        if (uses > 0) mbar_wait(&sm->sfull[ss], (uses - 1) & 1, kDefaultSpinLimit);
+      for (int r = 0; r < kScaleSlots / 2 && r < np; ++r) {   // slot 2r + pw: its tiles are m = r mod 8
+        const long long uses = (np - r + kScaleSlots / 2 - 1) / (kScaleSlots / 2);
+        mbar_wait(&sm->sfull[2 * r + pw], (uses - 1) & 1, kDefaultSpinLimit);
       }
       for (int qb = 0; qb < 2 && qb < nreq; ++qb) {
         const int uses = (nreq - qb + 1) / 2;
@@ -562,27 +592,26 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && start < end) {
+    if (lane == 0) {
       constexpr uint32_t idesc = FP8 ? make_idesc(0, 0, 0, 0, 128, 0) : make_idesc(1, 1, 0, 0, 128, 0);
       const uint32_t id = idesc | (static_cast<uint32_t>(N >> 3) << 17);
-      TileWalker tw;
-      tw.init(a, start, end);
-      long long i = 0;
-      int nreq = 0, qb = 0;
-      bool need_q = true;
-      while (tw.valid()) {
-        if (need_q) {
-          qb = nreq & 1;
-          if (!role_wait(sm, &sm->qfull[qb], (nreq >> 1) & 1, a.spin)) break;
-          ++nreq;
-          need_q = false;
-        }
+      int nreq = 0, qb = 0, cur = -1;
+      for (long long i = 0;; ++i) {
         const int pw = static_cast<int>(i & 1);
         const long long ip = i >> 1;
         const int s = static_cast<int>(ip % kStages);
+        if (!role_wait(sm, &sm->full[pw][s], (ip / kStages) & 1, a.spin)) break;
+        const int2 ti = sm->tinfo[i % kScaleSlots];
+        if (ti.x < 0) break;
+        if (ti.x != cur) {
+          if (cur >= 0) mma_commit(&sm->qempty[qb]);
+          qb = nreq & 1;
+          if (!role_wait(sm, &sm->qfull[qb], (nreq >> 1) & 1, a.spin)) break;
+          ++nreq;
+          cur = ti.x;
+        }
         const int c = static_cast<int>(i % kAccs);
         const long long use = i / kAccs;
-        if (!role_wait(sm, &sm->full[pw][s], (ip / kStages) & 1, a.spin)) break;
         if (use > 0 && !role_wait(sm, &sm->accempty[c], (use - 1) & 1, a.spin)) break;
         tc_fence_after();
         const uint32_t a_addr = smem_u32(stages + (pw * kStages + s) * kStageBytes);
@@ -604,11 +633,6 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         }
         mma_commit(&sm->empty[pw][s]);
         mma_commit(&sm->accfull[c]);
-        ++i;
-        if (tw.next(a)) {
-          mma_commit(&sm->qempty[qb]);
-          need_q = true;
-        }
       }
       // drain: all issued MMAs complete before TMEM is released
       mma_commit(&sm->drain);
@@ -624,91 +648,84 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     uint32_t* ghs = hist + grp * kHistBins;      // this group's histogram
     float* wq_s = sm->wq[grp];
     const float* wq_all = reinterpret_cast<const float*>(a.ws + a.L.wq);
-    if (start < end) {
-      TileWalker tw;
-      tw.init(a, start, end);
-      long long i = 0;
-      int cur_b = -1;
-      uint32_t hphase = 0;
-      // the group's four warps meet (bounded: an aborted pass falls through)
-      auto grp_sync = [&]() {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm->hbar[grp]);
-        role_wait(sm, &sm->hbar[grp], hphase & 1, a.spin);
-        ++hphase;
-      };
-      auto flush = [&](int b) {
-        for (int x = gtid; x < kHistBins; x += 128) {
-          const uint32_t cnt = ghs[x];
-          if (cnt) { atomicAdd(ghist + size_t(b) * kHistBins + x, cnt); ghs[x] = 0; }
-        }
-      };
-      while (tw.valid()) {
-        if (static_cast<int>(i % kGroups) == grp) {
-          if (tw.b != cur_b) {
-            // request switch: the group is done with the previous request's tiles
-            grp_sync();
-            if (cur_b >= 0) flush(cur_b);
-            cur_b = tw.b;
-            if (gtid < 64) wq_s[gtid] = gtid < N ? wq_all[cur_b * 64 + gtid] : 0.f;
-            grp_sync();
-          }
-          const long long j = static_cast<long long>(tw.t) * kTileRows + row;
-          const int ss = static_cast<int>(i % kScaleSlots);
-          if (!role_wait(sm, &sm->sfull[ss], (i / kScaleSlots) & 1, a.spin)) break;
-          const int pmask = sm->smask[ss];
-          const bool valid = j < tw.n_b && ((pmask >> (row >> 6)) & 1);
-          const float ks = FP8 ? sring[ss * kTileRows + row] : 1.0f;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sm->sempty[ss]);   // one arrival per warp
-          const int c = static_cast<int>(i % kAccs);
-          if (!role_wait(sm, &sm->accfull[c], (i / kAccs) & 1, a.spin)) break;
-          tc_fence_after();
-          const uint32_t tb = tmem + (static_cast<uint32_t>(sub * 32) << 16) + c * N;
-          float P[64];
-          if (N == 64) {
-            tmem_ld32(tb, *reinterpret_cast<float(*)[32]>(P));
-            tmem_ld32(tb + 32, *reinterpret_cast<float(*)[32]>(P + 32));
-          } else {
-#pragma unroll
-            for (int c0 = 0; c0 < 64; c0 += 16)
-              if (c0 < N) tmem_ld16(tb + c0, *reinterpret_cast<float(*)[16]>(P + c0));
-          }
-          tmem_wait_ld();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sm->accempty[c]);   // this warp's TMEM reads are done
-          float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-          for (int h = 0; h < 64; h += 4) {
-            if (h < N) {
-              const float4 w4 = *reinterpret_cast<const float4*>(&wq_s[h]);
-              s0 = fmaf(w4.x, fmaxf(P[h], 0.f), s0);
-              s1 = fmaf(w4.y, fmaxf(P[h + 1], 0.f), s1);
-              s0 = fmaf(w4.z, fmaxf(P[h + 2], 0.f), s0);
-              s1 = fmaf(w4.w, fmaxf(P[h + 3], 0.f), s1);
-            }
-          }
-          const float I = (s0 + s1) * ks;   // the key's scale is a positive power of two
-          const uint32_t key = valid ? order_key(I) : 0u;
-          if (valid) {
-            scores_all[size_t(tw.b) * a.L.n_pad + j] = I;
-            atomicAdd(&ghs[key >> (32 - kHistBits)], 1u);
-          }
-          // largest key of this warp's 32 entries: the selection re-reads only
-          // segments that can hold a selected entry
-          const uint32_t kmax = __reduce_max_sync(0xFFFFFFFFu, key);
-          if (lane == 0) {
-            segmax_all[size_t(tw.b) * (a.L.n_pad / kSeg) + (j >> 5)] = kmax;
-            if (i * 4 + sub < kSegCap) s_seg[i * 4 + sub] = static_cast<uint16_t>(kmax >> (32 - kHistBits));
-          }
-        }
-        ++i;
-        tw.next(a);
+    int cur_b = -1, n_b = 0, tiles_b = 0;
+    uint32_t hphase = 0;
+    // the group's four warps meet (bounded: an aborted pass falls through)
+    auto grp_sync = [&]() {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm->hbar[grp]);
+      role_wait(sm, &sm->hbar[grp], hphase & 1, a.spin);
+      ++hphase;
+    };
+    auto flush = [&](int b) {
+      for (int x = gtid; x < kHistBins; x += 128) {
+        const uint32_t cnt = ghs[x];
+        if (cnt) { atomicAdd(ghist + size_t(b) * kHistBins + x, cnt); ghs[x] = 0; }
       }
-      grp_sync();
-      if (cur_b >= 0) flush(cur_b);
+    };
+    for (long long i = grp;; i += kGroups) {
+      const int ss = static_cast<int>(i % kScaleSlots);
+      if (!role_wait(sm, &sm->sfull[ss], (i / kScaleSlots) & 1, a.spin)) break;
+      const int2 ti = sm->tinfo[ss];
+      const int pmask = sm->smask[ss];
+      const float ks = FP8 ? sring[ss * kTileRows + row] : 1.0f;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm->sempty[ss]);   // one arrival per warp
+      if (ti.x < 0) break;
+      if (ti.x != cur_b) {
+        // request switch: the group is done with the previous request's tiles
+        grp_sync();
+        if (cur_b >= 0) flush(cur_b);
+        cur_b = ti.x;
+        n_b = visible(a, cur_b);
+        tiles_b = (n_b + kTileRows - 1) / kTileRows;
+        if (gtid < 64) wq_s[gtid] = gtid < N ? wq_all[cur_b * 64 + gtid] : 0.f;
+        grp_sync();
+      }
+      const long long j = static_cast<long long>(ti.y) * kTileRows + row;
+      const bool real = ti.y < tiles_b;
+      const bool valid = real && j < n_b && ((pmask >> (row >> 6)) & 1);
+      const int c = static_cast<int>(i % kAccs);
+      if (!role_wait(sm, &sm->accfull[c], (i / kAccs) & 1, a.spin)) break;
+      tc_fence_after();
+      const uint32_t tb = tmem + (static_cast<uint32_t>(sub * 32) << 16) + c * N;
+      float P[64];
+      if (N == 64) {
+        tmem_ld32(tb, *reinterpret_cast<float(*)[32]>(P));
+        tmem_ld32(tb + 32, *reinterpret_cast<float(*)[32]>(P + 32));
+      } else {
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 16)
+          if (c0 < N) tmem_ld16(tb + c0, *reinterpret_cast<float(*)[16]>(P + c0));
+      }
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm->accempty[c]);   // this warp's TMEM reads are done
+      float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+      for (int h = 0; h < 64; h += 4) {
+        if (h < N) {
+          const float4 w4 = *reinterpret_cast<const float4*>(&wq_s[h]);
+          s0 = fmaf(w4.x, fmaxf(P[h], 0.f), s0);
+          s1 = fmaf(w4.y, fmaxf(P[h + 1], 0.f), s1);
+          s0 = fmaf(w4.z, fmaxf(P[h + 2], 0.f), s0);
+          s1 = fmaf(w4.w, fmaxf(P[h + 3], 0.f), s1);
+        }
+      }
+      const float I = (s0 + s1) * ks;   // the key's scale is a positive power of two
+      const uint32_t key = valid ? order_key(I) : 0u;
+      if (valid) {
+        scores_all[size_t(cur_b) * a.L.n_pad + j] = I;
+        atomicAdd(&ghs[key >> (32 - kHistBits)], 1u);
+      }
+      // largest key of this warp's 32 entries: the selection re-reads only
+      // segments that can hold a selected entry
+      const uint32_t kmax = __reduce_max_sync(0xFFFFFFFFu, key);
+      if (lane == 0 && real) segmax_all[size_t(cur_b) * (a.L.n_pad / kSeg) + (j >> 5)] = kmax;
     }
+    grp_sync();
+    if (cur_b >= 0) flush(cur_b);
   }
 
   tc_fence_before();
@@ -787,6 +804,25 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       const uint32_t* smx = segmax_all + size_t(b) * segs_pad;
       const long long g0 = j0 / kSeg, g1 = (j1 + kSeg - 1) / kSeg;
       const long long lbase = (first - start) * 4;   // block-local index of request segment 0
+      if (seg_smem) {
+        // the bins of the segments' largest keys, all loads in flight
+        const int nsg = static_cast<int>(g1 - g0);
+        uint32_t t4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int q = threadIdx.x + u * kScoreThreads;
+          t4[u] = q < nsg ? __ldcg(smx + g0 + q) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int q = threadIdx.x + u * kScoreThreads;
+          if (q < nsg) s_seg[lbase + g0 + q] = static_cast<uint16_t>(t4[u] >> (32 - kHistBits));
+        }
+#pragma unroll 1
+        for (int q = threadIdx.x + 4 * kScoreThreads; q < nsg; q += blockDim.x)
+          s_seg[lbase + g0 + q] = static_cast<uint16_t>(__ldcg(smx + g0 + q) >> (32 - kHistBits));
+        __syncthreads();
+      }
       uint32_t na = 0;
 #pragma unroll 1
       for (long long gc = g0; gc < g1; gc += kChunk) {
