@@ -109,12 +109,23 @@ struct IndexArgs {
   const int32_t* ctx_len;
   int B, Hi, N, ratio, k, n_max;
   int fp8;                   // 1: page-split FP8 keys, 0: bf16 keys
+  int grid;                  // blocks of the score kernel
   int32_t* topk_idx;
   float* topk_score;
   uint8_t* ws;
   WsLayout L;
   unsigned long long spin;
 };
+
+// Phase-1 work distribution: block blk starts at its home request blk * B / G and
+// takes chunk r of it without an atomic (r = its rank among the blocks of that
+// home); the request's counter starts after those chunks.
+__device__ __forceinline__ int home_request(int blk, int B, int G) {
+  return static_cast<int>((static_cast<long long>(blk) * B) / G);
+}
+__device__ __forceinline__ int first_home_block(int b, int B, int G) {   // smallest blk with home b
+  return static_cast<int>((static_cast<long long>(b) * G + B - 1) / B);
+}
 
 __device__ __forceinline__ int visible(const IndexArgs& a, int b) {
   long long c = a.ctx_len[b];
@@ -136,7 +147,10 @@ __global__ void __launch_bounds__(256) index_prep_kernel(const IndexArgs a) {
   uint32_t* hist = reinterpret_cast<uint32_t*>(a.ws + a.L.hist) + size_t(b) * kHistBins;
   uint32_t* ctr = reinterpret_cast<uint32_t*>(a.ws + a.L.ctr) + b * 4;
   for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) hist[i] = 0;
-  if (threadIdx.x < 4) ctr[threadIdx.x] = 0;
+  if (threadIdx.x < 4)
+    ctr[threadIdx.x] = threadIdx.x == 0 ? static_cast<uint32_t>(first_home_block(b + 1, a.B, a.grid) -
+                                                             first_home_block(b, a.B, a.grid)) * kChunkTiles
+                                        : 0u;
   if (b == 0 && threadIdx.x == 0) *reinterpret_cast<uint32_t*>(a.ws + a.L.gbar) = 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // warp w owns heads w, w+8, ... (N <= 64); lane l holds dims 4l .. 4l+3.  All loads first.
@@ -347,6 +361,24 @@ __device__ void block_exclusive_scan(ScoreSmem* sm, uint32_t* x, int n) {
   __syncthreads();
 }
 
+// The selection phases split every request's tiles over a run of consecutive
+// blocks, in proportion to its share of all tiles (a request too small for a block
+// of its own shares block fb with its neighbours), so that few blocks work on two
+// requests.  For request b, whose tiles are [C, C + tb) of the total, returns
+// whether block `blk` holds tiles [lo, hi) of it, and the first block fb of its run.
+__device__ __forceinline__ bool block_range(int blk, int G, long long C, long long tb, long long total,
+                                            long long& lo, long long& hi, int& fb) {
+  if (tb <= 0 || total <= 0) return false;
+  fb = static_cast<int>(min(static_cast<long long>(G - 1), C * G / total));
+  int eb = static_cast<int>(((C + tb) * G) / total);
+  if (eb <= fb) eb = fb + 1;
+  if (blk < fb || blk >= eb) return false;
+  const long long per = (tb + (eb - fb) - 1) / (eb - fb);
+  lo = (blk - fb) * per;
+  hi = min(tb, lo + per);
+  return lo < hi;
+}
+
 // The indices q in [0, n) with pred(q), in increasing order, into list (whole
 // block; pred is evaluated twice and must not change in between).  Returns the count.
 template <class Pred>
@@ -408,9 +440,6 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   // work range of this block: a contiguous run of the global tile sequence
   long long total = 0;
   for (int b = 0; b < a.B; ++b) total += (visible(a, b) + kTileRows - 1) / kTileRows;
-  const long long per = (total + gridDim.x - 1) / gridDim.x;
-  const long long start = min(total, per * blockIdx.x);
-  const long long end = min(total, start + per);
 
   if (threadIdx.x == 0) {
     for (int p = 0; p < kProducers; ++p)
@@ -501,8 +530,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             ids[u] = (b < 0 || lp * kPageRows >= n_b) ? -2 : (lp >= a.keys.max_pages ? -3 : bt[lp]);
           }
         };
-        int req = static_cast<int>((static_cast<long long>(blockIdx.x) * a.B) / gridDim.x);
-        uint32_t pending = atomicAdd(&ctr_all[req * 4], static_cast<uint32_t>(kChunkTiles));
+        int req = home_request(blockIdx.x, a.B, gridDim.x);
+        uint32_t pending = 0;
         // the next chunk: (request, first tile) from the pending grab; request -1 = none left
         auto resolve = [&](int& b, int& t0) {
           int tiles = tiles_of(req);
@@ -522,19 +551,22 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           }
         };
         int cb, ct;
-        resolve(cb, ct);
+        {
+          const int r = blockIdx.x - first_home_block(req, a.B, gridDim.x);
+          pending = atomicAdd(&ctr_all[req * 4], static_cast<uint32_t>(kChunkTiles));
+          if (static_cast<long long>(r) * kChunkTiles < tiles_of(req)) {
+            cb = req;   // the block's first chunk, assigned without an atomic
+            ct = r * kChunkTiles;
+          } else {
+            resolve(cb, ct);
+          }
+        }
         int ids[2 * kChunkTiles];
         chunk_ids(cb, ct, ids);
         int q_b = -1;
         long long m = 0;   // pairs posted
         bool ok = true;
         while (ok) {
-          int nb2 = -1, nt = 0;
-          int nids[2 * kChunkTiles];
-          if (cb >= 0) {
-            resolve(nb2, nt);   // usually already returned: grabbed one chunk ago
-            chunk_ids(nb2, nt, nids);
-          }
           if (cb >= 0 && cb != q_b) {
             // query image of the new request into buffer nreq % 2
             const int qb = nreq & 1;
@@ -544,10 +576,17 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             ++nreq;
             q_b = cb;
           }
-          // the chunk's pairs: the first tile here, the second handed to producer 1
+          // the chunk's pairs: the first tile here, the second handed to producer 1;
+          // after the first pair, the next chunk is resolved and its page ids requested
+          int nb2 = -1, nt = 0;
+          int nids[2 * kChunkTiles];
 #pragma unroll
           for (int pr = 0; pr < kChunkTiles / 2; ++pr, ++m) {
             if (pr > 0 && cb < 0) break;   // the end marker is one pair
+            if (pr == 1) {
+              resolve(nb2, nt);   // usually already returned: grabbed one chunk ago
+              chunk_ids(nb2, nt, nids);
+            }
             const int hs = static_cast<int>(m % kPairSlots);
             if (m >= kPairSlots && !role_wait(sm, &sm->pempty[hs], ((m / kPairSlots) - 1) & 1, a.spin)) {
               ok = false;
@@ -561,7 +600,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
               break;
             }
           }
-          if (cb < 0) break;
+          if (cb < 0 || !ok) break;
           cb = nb2;
           ct = nt;
 #pragma unroll
@@ -753,24 +792,25 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   uint32_t* s_hs = hist;                                                         // histogram copy / counts
   uint16_t* s_list = reinterpret_cast<uint16_t*>(hist + kHistBins);             // ordered hit list
   const int segs_pad = a.L.n_pad / kSeg;
-  const bool seg_smem = (end - start) * 4 <= kSegCap;
   const int nwarps = kScoreThreads / 32;
   const uint32_t lt_mask = (1u << lane) - 1u;
   constexpr int kChunk = kHistBins - 1;   // segments per pass (the lists hold up to 4,095)
   uint32_t* abv_all = reinterpret_cast<uint32_t*>(a.ws + a.L.abv);
   {
-    long long acc = 0;
+    long long C = 0;
     uint32_t cbase = 0;   // cache slots taken by the block's earlier requests
+    int lofs = 0;         // shared-memory segment slots taken by the block's earlier requests
 #pragma unroll 1
-    for (int b = 0; b < a.B && acc < end && !aborted2; ++b) {
+    for (int b = 0; b < a.B && !aborted2; ++b) {
       const int nb = visible(a, b);
       const long long tb = (nb + kTileRows - 1) / kTileRows;
-      const long long s0 = max(start, acc), s1 = min(end, acc + tb);
-      const long long first = acc;
-      acc += tb;
-      if (s0 >= s1) continue;
-      const long long j0 = (s0 - first) * kTileRows;
-      const long long j1 = min((s1 - first) * kTileRows, static_cast<long long>(nb));
+      long long lo, hi;
+      int fb;
+      const bool mine = block_range(blockIdx.x, gridDim.x, C, tb, total, lo, hi, fb);
+      C += tb;
+      if (!mine) continue;
+      const long long j0 = lo * kTileRows;
+      const long long j1 = min(hi * kTileRows, static_cast<long long>(nb));
       const float* sc = scores_all + size_t(b) * a.L.n_pad;
       if (nb <= a.k) {
         // every visible entry is selected, in order
@@ -803,7 +843,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       unsigned long long* cand = reinterpret_cast<unsigned long long*>(a.ws + a.L.cand) + size_t(b) * a.L.n_pad;
       const uint32_t* smx = segmax_all + size_t(b) * segs_pad;
       const long long g0 = j0 / kSeg, g1 = (j1 + kSeg - 1) / kSeg;
-      const long long lbase = (first - start) * 4;   // block-local index of request segment 0
+      // block-local slot of request segment g: lbase + g (shared-memory table if it fits)
+      const bool seg_smem = lofs + (g1 - g0) <= kSegCap;
+      const long long lbase = lofs - g0;
+      if (seg_smem) lofs += static_cast<int>(g1 - g0);
       if (seg_smem) {
         // the bins of the segments' largest keys, all loads in flight
         const int nsg = static_cast<int>(g1 - g0);
@@ -934,17 +977,18 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     }
   }
   {
-    long long acc = 0;
+    long long C = 0;
+    int lofs = 0;
 #pragma unroll 1
-    for (int b = 0; b < a.B && acc < end && !aborted3; ++b) {
+    for (int b = 0; b < a.B && !aborted3; ++b) {
       const int nb = visible(a, b);
       const long long tb = (nb + kTileRows - 1) / kTileRows;
-      const long long s0 = max(start, acc), s1 = min(end, acc + tb);
-      const long long first = acc;
-      acc += tb;
-      if (s0 >= s1 || nb <= a.k) continue;
+      long long lo, hi;
+      int fb;   // the first block holding tiles of request b
+      const bool mine = block_range(blockIdx.x, gridDim.x, C, tb, total, lo, hi, fb);
+      C += tb;
+      if (!mine || nb <= a.k) continue;
       const uint32_t* ctr = ctr_all + b * 4;
-      const long long fb = first / per;   // the first block holding tiles of request b
       // one round trip: the request's counters and the lower blocks' above-T counts
       const int T = static_cast<int>(__ldcg(ctr + 2));
       const uint32_t above = min(__ldcg(ctr + 3), static_cast<uint32_t>(a.k));
@@ -954,8 +998,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       for (long long q = fb + threadIdx.x; q < blockIdx.x; q += blockDim.x)
         part += __ldcg(abv_all + size_t(b) * kMaxGrid + q);
       if (T < 0) continue;   // uniform: the same word for every thread
-      const long long j0 = (s0 - first) * kTileRows;
-      const long long j1 = min((s1 - first) * kTileRows, static_cast<long long>(nb));
+      const long long j0 = lo * kTileRows;
+      const long long j1 = min(hi * kTileRows, static_cast<long long>(nb));
       const float* sc = scores_all + size_t(b) * a.L.n_pad;
       const unsigned long long* gcand =
           reinterpret_cast<const unsigned long long*>(a.ws + a.L.cand) + size_t(b) * a.L.n_pad;
@@ -1051,7 +1095,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       uint32_t running = sm->out;
       const uint32_t* smx = segmax_all + size_t(b) * segs_pad;
       const long long g0 = j0 / kSeg, g1 = (j1 + kSeg - 1) / kSeg;
-      const long long lbase = (first - start) * 4;
+      const bool seg_smem = lofs + (g1 - g0) <= kSegCap;   // as in phase 2
+      const long long lbase = lofs - g0;
+      if (seg_smem) lofs += static_cast<int>(g1 - g0);
       uint32_t* s_cnt = s_hs;   // per hit segment: its count (+ a trailing 0), then the exclusive scan
 #pragma unroll 1
       for (long long gc = g0; gc < g1; gc += kChunk) {
@@ -1160,8 +1206,7 @@ cudaError_t launch_score(const CUtensorMap& tmap, const IndexArgs& a, cudaStream
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   // one block per SM: it allocates all 512 TMEM columns and most of shared memory
-  const int grid = sm_count();
-  if (grid > kMaxGrid) return cudaErrorInvalidConfiguration;
+  const int grid = a.grid;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kScoreThreads);
@@ -1231,6 +1276,8 @@ cudaError_t launch_index_topk(const void* q_idx, const float* w, const cskv_page
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
 
+  a.grid = sm_count();   // the score kernel runs one block per SM
+  if (a.grid > kMaxGrid) a.grid = kMaxGrid;
   index_prep_kernel<<<B, 256, 0, stream>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
