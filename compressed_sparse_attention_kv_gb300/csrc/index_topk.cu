@@ -69,12 +69,11 @@ __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_
 
 constexpr int kMaxGrid = 1024;       // bound of the per-block counters' table
 constexpr int kSeg = 32;             // entries per segment (one epilogue warp's rows of a tile)
-constexpr int kSegCap = 4096;        // segments a block tracks in shared memory (1,024 tiles)
-constexpr int kSegCache = 512;       // hit segments whose scores stay in shared memory
-constexpr uint16_t kHitUncached = 0xFFFF;
+constexpr int kSelSegs = 8192;       // segments per selection pass (262,144 entries)
+constexpr int kScratch16 = kSelSegs + 64 - kScaleSlots * kTileRows * 2;   // u16 words after the scale ring
 
 struct WsLayout {
-  size_t scores, segmax, cand, qimg, wq, hist, ctr, abv, gbar, total;
+  size_t scores, segmax, cand, qimg, wq, hist, ctr, slc, gbar, total;
   int n_pad;
 };
 
@@ -90,7 +89,7 @@ __host__ __device__ inline WsLayout ws_layout(int B, int n_max, int k) {
   L.wq = o;     o = align256(o + size_t(B) * 64 * 4);
   L.hist = o;   o = align256(o + size_t(B) * kHistBins * 4);
   L.ctr = o;    o = align256(o + size_t(B) * 4 * 4);
-  L.abv = o;    o = align256(o + size_t(B) * kMaxGrid * 4);
+  L.slc = o;    o = align256(o + size_t(B) * kMaxGrid * 4);
   L.gbar = o;   o = align256(o + 16);
   L.total = o;
   return L;
@@ -100,6 +99,9 @@ __host__ __device__ inline WsLayout ws_layout(int B, int n_max, int k) {
 __device__ __forceinline__ uint32_t order_key(float f) {
   const uint32_t u = __float_as_uint(f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float from_order_key(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
 struct IndexArgs {
@@ -212,8 +214,9 @@ struct ScoreSmem {
   uint32_t base[2];
   uint32_t nlist;
   int T;
-  uint32_t above;
+  uint32_t above, inT;
   uint32_t need, done, out;
+  int last;
   unsigned long long prefix, mask;
   uint32_t part[256];
   uint32_t dh[256];
@@ -328,13 +331,15 @@ __device__ void threshold_bin(ScoreSmem* sm, const uint32_t* ghist, uint32_t* hs
       }
       sm->T = T;
       sm->above = acc;
+      sm->inT = hs[T];
     }
   }
   __syncthreads();
 }
 
-// Exclusive scan, in place, of n counters in shared memory (whole block).
-__device__ void block_exclusive_scan(ScoreSmem* sm, uint32_t* x, int n) {
+// Exclusive scan, in place, of n 16-bit counters in shared memory (whole block;
+// the sums stay below 65,536).
+__device__ void block_exclusive_scan16(ScoreSmem* sm, uint16_t* x, int n) {
   const int per = (n + kScoreThreads - 1) / kScoreThreads;
   const int lo = min(n, static_cast<int>(threadIdx.x) * per), hi = min(n, lo + per);
   uint32_t sum = 0;
@@ -355,28 +360,36 @@ __device__ void block_exclusive_scan(ScoreSmem* sm, uint32_t* x, int n) {
 #pragma unroll 1
   for (int i = lo; i < hi; ++i) {
     const uint32_t v = x[i];
-    x[i] = run;
+    x[i] = static_cast<uint16_t>(run);
     run += v;
   }
   __syncthreads();
 }
 
-// The selection phases split every request's tiles over a run of consecutive
-// blocks, in proportion to its share of all tiles (a request too small for a block
-// of its own shares block fb with its neighbours), so that few blocks work on two
-// requests.  For request b, whose tiles are [C, C + tb) of the total, returns
-// whether block `blk` holds tiles [lo, hi) of it, and the first block fb of its run.
+// The selection splits every request's tiles over a run of consecutive blocks, in
+// proportion to its share of all tiles (a request too small for a block of its own
+// shares block fb with its neighbours), so that few blocks work on two requests.
+// For request b, whose tiles are [C, C + tb) of the total: whether block blk holds
+// tiles [lo, hi) of it; the run's first block fb, its length nbk and tiles per block.
+// An empty request belongs to block fb, so that its output is still written.
 __device__ __forceinline__ bool block_range(int blk, int G, long long C, long long tb, long long total,
-                                            long long& lo, long long& hi, int& fb) {
-  if (tb <= 0 || total <= 0) return false;
-  fb = static_cast<int>(min(static_cast<long long>(G - 1), C * G / total));
+                                            long long& lo, long long& hi, int& fb, int& nbk,
+                                            long long& per) {
+  fb = total > 0 ? static_cast<int>(min(static_cast<long long>(G - 1), C * G / total)) : 0;
+  if (tb <= 0) {   // an empty request: its run is block fb alone, with no tiles
+    nbk = 1;
+    per = 1;
+    lo = hi = 0;
+    return blk == fb;
+  }
   int eb = static_cast<int>(((C + tb) * G) / total);
   if (eb <= fb) eb = fb + 1;
-  if (blk < fb || blk >= eb) return false;
-  const long long per = (tb + (eb - fb) - 1) / (eb - fb);
+  per = (tb + (eb - fb) - 1) / (eb - fb);
+  nbk = static_cast<int>((tb + per - 1) / per);   // blocks of the run that hold tiles
+  if (blk < fb || blk >= fb + nbk) return false;
   lo = (blk - fb) * per;
   hi = min(tb, lo + per);
-  return lo < hi;
+  return true;
 }
 
 // The indices q in [0, n) with pred(q), in increasing order, into list (whole
@@ -424,10 +437,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   uint8_t* qbuf = stages + kProducers * kStages * kStageBytes;             // 2 x kQImage
   uint32_t* hist = reinterpret_cast<uint32_t*>(qbuf + 2 * kQImage);       // kGroups x 4096 bins
   float* sring = reinterpret_cast<float*>(hist + kGroups * kHistBins);    // kScaleSlots x 128 fp32
-  // per segment of the block's (static) range in phases 2 and 3: the bin of its
-  // largest key, then 0 / cache slot + 1 / kHitUncached
-  uint16_t* s_seg = reinterpret_cast<uint16_t*>(sring + kScaleSlots * kTileRows);   // kSegCap
-  ScoreSmem* sm = reinterpret_cast<ScoreSmem*>(s_seg + kSegCap);
+  uint16_t* scratch = reinterpret_cast<uint16_t*>(sring + kScaleSlots * kTileRows);   // kScratch16
+  ScoreSmem* sm = reinterpret_cast<ScoreSmem*>(scratch + kScratch16);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = a.N;
@@ -775,259 +786,258 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     tmem_dealloc(tmem, ncols);
   }
 
-  // ======================================================= phase 2: threshold and candidates
-  // Every block takes the same static tile range as in phase 1.  For each request
-  // it touches: the threshold bin T (the bin holding the k-th score), the count of
-  // its entries above T (kept per block, for the output offsets) and its entries
-  // in T, staged as 64-bit (score key, ~index) candidates.  Only segments whose
-  // largest key reaches T ("hit" segments) are read again; the first kSegCache of
-  // them keep their scores in shared memory for phase 3.  Phases 2 and 3 run once
-  // per launch from a cold instruction cache, so their loops stay rolled and work
-  // one entry per lane.
+  // ======================================================= phase 2: selection
+  // After every request's histogram is complete (the one grid barrier), each request
+  // is selected in two steps:
+  //  - every block of the request's run takes a slice of its tiles: the threshold bin
+  //    T (the bin holding the k-th score) from the request's histogram, the slice's
+  //    "hit" segments (largest key in a bin >= T, about one in nine) from the segment
+  //    table, their scores copied into shared memory with cp.async, and every entry
+  //    in a bin >= T written as a 64-bit (score key, ~index) key, in entry order, to
+  //    the slice's own area of the request's key buffer;
+  //  - the block that finishes its slice last (a per-request counter) gathers the
+  //    slices' keys, radix-selects the exact cut among the keys of bin T (ties ->
+  //    smaller index) and writes the selected entries in entry order.
+  // This code runs once per launch; its loops stay rolled.
   grid_barrier(sm, gbar, gridDim.x, a.spin);
-  const bool aborted2 = sm->abort;   // uniform: only thread 0 sets it, before the barrier's sync
-  unsigned long long* s_cand = reinterpret_cast<unsigned long long*>(stages);   // kCandCap (phase 2)
-  unsigned long long* s_c = s_cand;                                              // kCandCap (phase 3)
-  float* s_cache = reinterpret_cast<float*>(stages + kCandCap * 8);              // kSegCache x 32
-  uint32_t* s_hs = hist;                                                         // histogram copy / counts
-  uint16_t* s_list = reinterpret_cast<uint16_t*>(hist + kHistBins);             // ordered hit list
-  const int segs_pad = a.L.n_pad / kSeg;
-  const int nwarps = kScoreThreads / 32;
-  const uint32_t lt_mask = (1u << lane) - 1u;
-  constexpr int kChunk = kHistBins - 1;   // segments per pass (the lists hold up to 4,095)
-  uint32_t* abv_all = reinterpret_cast<uint32_t*>(a.ws + a.L.abv);
+  const bool aborted = sm->abort;   // uniform: only thread 0 sets it, before the barrier's sync
   {
-    long long C = 0;
-    uint32_t cbase = 0;   // cache slots taken by the block's earlier requests
-    int lofs = 0;         // shared-memory segment slots taken by the block's earlier requests
+    float* s_cache = reinterpret_cast<float*>(stages);                       // the stage ring, 32 fp32 per hit
+    uint16_t* s_list = reinterpret_cast<uint16_t*>(qbuf);                     // kSelSegs
+    unsigned long long* s_cand = reinterpret_cast<unsigned long long*>(hist);   // kCandCap
+    uint16_t* s_cnt = reinterpret_cast<uint16_t*>(sring);                    // kSelSegs + 64
+    uint32_t* s_pre = reinterpret_cast<uint32_t*>(sring);                    // slice offsets (final step)
+    const int segs_pad = a.L.n_pad / kSeg;
+    const int nwarps = kScoreThreads / 32;
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    const int kCache = kProducers * kStages * kStageBytes / (kSeg * 4);   // hit segments per round
+    uint32_t* slc_all = reinterpret_cast<uint32_t*>(a.ws + a.L.slc);
+    // block-wide placement: each thread's count -> its exclusive offset; the total
+    auto place = [&](uint32_t cnt, uint32_t& tot) -> uint32_t {
+      uint32_t incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (lane == 31) sm->part[warp] = incl;
+      __syncthreads();
+      uint32_t pos = incl - cnt;
+      tot = 0;
 #pragma unroll 1
-    for (int b = 0; b < a.B && !aborted2; ++b) {
+      for (int w = 0; w < kScoreThreads / 32; ++w) {
+        const uint32_t x = sm->part[w];
+        if (w < warp) pos += x;
+        tot += x;
+      }
+      __syncthreads();
+      return pos;
+    };
+    long long C = 0;
+#pragma unroll 1
+    for (int b = 0; b < a.B && !aborted; ++b) {
       const int nb = visible(a, b);
       const long long tb = (nb + kTileRows - 1) / kTileRows;
-      long long lo, hi;
-      int fb;
-      const bool mine = block_range(blockIdx.x, gridDim.x, C, tb, total, lo, hi, fb);
+      long long lo, hi, per_b;
+      int fb, nbk;
+      const bool mine = block_range(blockIdx.x, gridDim.x, C, tb, total, lo, hi, fb, nbk, per_b);
       C += tb;
       if (!mine) continue;
-      const long long j0 = lo * kTileRows;
-      const long long j1 = min(hi * kTileRows, static_cast<long long>(nb));
+      const int slice = blockIdx.x - fb;
       const float* sc = scores_all + size_t(b) * a.L.n_pad;
+      int32_t* out_idx = a.topk_idx + size_t(b) * a.k;
+      float* out_sc = a.topk_score ? a.topk_score + size_t(b) * a.k : nullptr;
       if (nb <= a.k) {
-        // every visible entry is selected, in order
+        // every visible entry is selected, in order; the run's first block pads with -1
+        const long long jhi = min(hi * kTileRows, static_cast<long long>(nb));
 #pragma unroll 1
-        for (long long j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
-          a.topk_idx[size_t(b) * a.k + j] = static_cast<int32_t>(j);
-          if (a.topk_score) a.topk_score[size_t(b) * a.k + j] = __ldcg(sc + j);
+        for (long long j = lo * kTileRows + threadIdx.x; j < jhi; j += blockDim.x) {
+          out_idx[j] = static_cast<int32_t>(j);
+          if (out_sc) out_sc[j] = __ldcg(sc + j);
+        }
+        if (slice == 0) {
+#pragma unroll 1
+          for (int j = nb + threadIdx.x; j < a.k; j += blockDim.x) {
+            out_idx[j] = -1;
+            if (out_sc) out_sc[j] = -INFINITY;
+          }
         }
         continue;
       }
-      threshold_bin(sm, ghist + size_t(b) * kHistBins, s_hs, a.k);
+      threshold_bin(sm, ghist + size_t(b) * kHistBins, hist, a.k);
       const int T = sm->T;
-      uint32_t* ctr = ctr_all + b * 4;
-      if (threadIdx.x == 0) {
-        ctr[2] = static_cast<uint32_t>(T);   // every block of the request stores the same values
-        ctr[3] = sm->above;
-        sm->cnt[0] = 0;
-        sm->cnt[1] = 0;
-      }
-      __syncthreads();
+      const uint32_t above = sm->above;
       if (T < 0) {
         // fewer than k binned entries (an earlier error dropped some): no selection
+        if (slice == 0) {
 #pragma unroll 1
-        for (int j = threadIdx.x; j < a.k; j += blockDim.x) {
-          a.topk_idx[size_t(b) * a.k + j] = -1;
-          if (a.topk_score) a.topk_score[size_t(b) * a.k + j] = -INFINITY;
+          for (int j = threadIdx.x; j < a.k; j += blockDim.x) {
+            out_idx[j] = -1;
+            if (out_sc) out_sc[j] = -INFINITY;
+          }
         }
         continue;
       }
-      unsigned long long* cand = reinterpret_cast<unsigned long long*>(a.ws + a.L.cand) + size_t(b) * a.L.n_pad;
       const uint32_t* smx = segmax_all + size_t(b) * segs_pad;
-      const long long g0 = j0 / kSeg, g1 = (j1 + kSeg - 1) / kSeg;
-      // block-local slot of request segment g: lbase + g (shared-memory table if it fits)
-      const bool seg_smem = lofs + (g1 - g0) <= kSegCap;
-      const long long lbase = lofs - g0;
-      if (seg_smem) lofs += static_cast<int>(g1 - g0);
-      if (seg_smem) {
-        // the bins of the segments' largest keys, all loads in flight
-        const int nsg = static_cast<int>(g1 - g0);
-        uint32_t t4[4];
+      unsigned long long* kbuf = reinterpret_cast<unsigned long long*>(a.ws + a.L.cand) + size_t(b) * a.L.n_pad;
+      const int nseg = (nb + kSeg - 1) / kSeg;
+      // the hit segments of [g0, g0 + ns) (g0 a multiple of 4) into s_list, in order:
+      // thread t owns segments 24t .. 24t+23 (six 16-byte loads of the segment table)
+      auto hit_list = [&](long long g0, int ns) -> uint32_t {
+        constexpr int kOwn = 24;
+        static_assert(kOwn * kScoreThreads >= kSelSegs, "every segment of a pass has an owner");
+        const int q0 = threadIdx.x * kOwn;
+        uint32_t m = 0;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int q = threadIdx.x + u * kScoreThreads;
-          t4[u] = q < nsg ? __ldcg(smx + g0 + q) : 0u;
+        for (int u = 0; u < kOwn / 4; ++u) {
+          const int q = q0 + 4 * u;
+          if (q < ns) {   // the table's rows are padded to a multiple of 4 segments
+            const uint4 x = __ldcg(reinterpret_cast<const uint4*>(smx + g0 + q));
+            m |= (static_cast<int>(x.x >> (32 - kHistBits)) >= T ? 1u : 0u) << (4 * u);
+            m |= (static_cast<int>(x.y >> (32 - kHistBits)) >= T ? 2u : 0u) << (4 * u);
+            m |= (static_cast<int>(x.z >> (32 - kHistBits)) >= T ? 4u : 0u) << (4 * u);
+            m |= (static_cast<int>(x.w >> (32 - kHistBits)) >= T ? 8u : 0u) << (4 * u);
+          }
         }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int q = threadIdx.x + u * kScoreThreads;
-          if (q < nsg) s_seg[lbase + g0 + q] = static_cast<uint16_t>(t4[u] >> (32 - kHistBits));
-        }
+        if (ns - q0 < kOwn) m &= ns > q0 ? (1u << (ns - q0)) - 1u : 0u;
+        uint32_t tot;
+        uint32_t pos = place(__popc(m), tot);
 #pragma unroll 1
-        for (int q = threadIdx.x + 4 * kScoreThreads; q < nsg; q += blockDim.x)
-          s_seg[lbase + g0 + q] = static_cast<uint16_t>(__ldcg(smx + g0 + q) >> (32 - kHistBits));
+        while (m) {
+          const int q = __ffs(m) - 1;
+          m &= m - 1;
+          s_list[pos++] = static_cast<uint16_t>(q0 + q);
+        }
         __syncthreads();
-      }
-      uint32_t na = 0;
+        return tot;
+      };
+      // ---- the slice: every entry in a bin >= T as a key, in entry order, into
+      // kbuf[lo * 128 + ...] (the slice's tiles bound its count).  A warp per hit
+      // segment, one entry per lane, four segments per step with their loads first.
+      unsigned long long* kout = kbuf + lo * kTileRows;
+      uint32_t nk = 0;
+      const long long gs1 = min(hi * 4, static_cast<long long>(nseg));
 #pragma unroll 1
-      for (long long gc = g0; gc < g1; gc += kChunk) {
-        const int nseg = static_cast<int>(min(g1, gc + kChunk) - gc);
-        // the hit segments of the chunk, in order
-        const uint32_t nhit = ordered_list(
-            sm, nseg,
-            [&](int q) {
-              const int bin = seg_smem ? static_cast<int>(s_seg[lbase + gc + q])
-                                       : static_cast<int>(__ldcg(smx + gc + q) >> (32 - kHistBits));
-              return bin >= T;
-            },
-            s_list);
-        const uint32_t ncache =
-            seg_smem && cbase < static_cast<uint32_t>(kSegCache) ? min(nhit, kSegCache - cbase) : 0u;
-        // segment table: 0 = no hit, slot + 1 = cached hit, kHitUncached
-        if (seg_smem) {
+      for (long long gc = lo * 4; gc < gs1; gc += kSelSegs) {
+        const int ns = static_cast<int>(min(static_cast<long long>(kSelSegs), gs1 - gc));
+        const uint32_t nhit = hit_list(gc, ns);
 #pragma unroll 1
-          for (int q = threadIdx.x; q < nseg; q += blockDim.x) s_seg[lbase + gc + q] = 0;
+        for (uint32_t h0 = 0; h0 < nhit; h0 += kCache) {
+          const uint32_t nh = min(nhit - h0, static_cast<uint32_t>(kCache));
+#pragma unroll 1
+          for (uint32_t x = threadIdx.x; x < nh * 8; x += blockDim.x)
+            cp_async16(s_cache + (x >> 3) * kSeg + (x & 7) * 4,
+                       sc + (gc + s_list[h0 + (x >> 3)]) * kSeg + (x & 7) * 4);
+          cp_async_wait_all();
           __syncthreads();
+          constexpr int kU = 4;
 #pragma unroll 1
-          for (uint32_t h = threadIdx.x; h < nhit; h += blockDim.x)
-            s_seg[lbase + gc + s_list[h]] = h < ncache ? static_cast<uint16_t>(cbase + h + 1) : kHitUncached;
-        }
-        // the cached hit segments' scores, all loads issued at once
-        {
-          float4 t4[4];
+          for (uint32_t hb = warp * kU; hb < nh; hb += nwarps * kU) {
+            float v[kU];
+            long long j[kU];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const uint32_t x = threadIdx.x + u * kScoreThreads;
-            t4[u] = x < ncache * 8
-                        ? __ldcg(reinterpret_cast<const float4*>(sc + (gc + s_list[x >> 3]) * kSeg) + (x & 7))
-                        : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
+            for (int u = 0; u < kU; ++u) {
+              const uint32_t h = min(hb + u, nh - 1);
+              j[u] = (gc + static_cast<long long>(s_list[h0 + h])) * kSeg + lane;
+              v[u] = s_cache[h * kSeg + lane];
+            }
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const uint32_t x = threadIdx.x + u * kScoreThreads;
-            if (x < ncache * 8) reinterpret_cast<float4*>(s_cache + (cbase + (x >> 3)) * kSeg)[x & 7] = t4[u];
-          }
-#pragma unroll 1
-          for (uint32_t x = threadIdx.x + 4 * kScoreThreads; x < ncache * 8; x += blockDim.x)
-            reinterpret_cast<float4*>(s_cache + (cbase + (x >> 3)) * kSeg)[x & 7] =
-                __ldcg(reinterpret_cast<const float4*>(sc + (gc + s_list[x >> 3]) * kSeg) + (x & 7));
-        }
-        __syncthreads();
-        // one warp per hit segment, one entry per lane: count above T, stage T's entries
-#pragma unroll 1
-        for (uint32_t h = warp; h < nhit; h += nwarps) {
-          const long long g = gc + s_list[h];
-          const long long j = g * kSeg + lane;
-          const float v = h < ncache ? s_cache[(cbase + h) * kSeg + lane] : __ldcg(sc + j);
-          const uint32_t key = order_key(v);
-          const int bin = static_cast<int>(key >> (32 - kHistBits));
-          const bool ok = j < j1;
-          na += __popc(__ballot_sync(0xFFFFFFFFu, ok && bin > T));
-          const unsigned cm = __ballot_sync(0xFFFFFFFFu, ok && bin == T);
-          if (cm) {
-            uint32_t base0 = 0;
-            if (lane == 0) base0 = atomicAdd(&sm->cnt[1], static_cast<uint32_t>(__popc(cm)));
-            base0 = __shfl_sync(0xFFFFFFFFu, base0, 0);
-            if ((cm >> lane) & 1u) {
-              const uint32_t pos = base0 + __popc(cm & lt_mask);
-              const unsigned long long k64 =
-                  (static_cast<unsigned long long>(key) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(j));
-              if (pos < kCandCap) {
-                s_cand[pos] = k64;
-              } else {
-                const uint32_t gp = atomicAdd(&ctr[1], 1u);   // rare: many ties in one bin
-                if (gp < static_cast<uint32_t>(a.L.n_pad)) cand[gp] = k64;
-              }
+            for (int u = 0; u < kU; ++u) {
+              const bool f = hb + u < nh && j[u] < nb &&
+                             static_cast<int>(order_key(v[u]) >> (32 - kHistBits)) >= T;
+              const unsigned m = __ballot_sync(0xFFFFFFFFu, f);
+              if (lane == 0 && hb + u < nh) s_cnt[hb + u] = static_cast<uint16_t>(__popc(m));
             }
           }
+          if (threadIdx.x == 0) s_cnt[nh] = 0;
+          __syncthreads();
+          block_exclusive_scan16(sm, s_cnt, static_cast<int>(nh) + 1);
+#pragma unroll 1
+          for (uint32_t hb = warp * kU; hb < nh; hb += nwarps * kU) {
+            float v[kU];
+            long long j[kU];
+            uint32_t base[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+              const uint32_t h = min(hb + u, nh - 1);
+              j[u] = (gc + static_cast<long long>(s_list[h0 + h])) * kSeg + lane;
+              v[u] = s_cache[h * kSeg + lane];
+              base[u] = s_cnt[h];
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+              const uint32_t key = order_key(v[u]);
+              const bool f = hb + u < nh && j[u] < nb && static_cast<int>(key >> (32 - kHistBits)) >= T;
+              const unsigned m = __ballot_sync(0xFFFFFFFFu, f);
+              if (f)
+                kout[nk + base[u] + __popc(m & lt_mask)] =
+                    (static_cast<unsigned long long>(key) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(j[u]));
+            }
+          }
+          nk += s_cnt[nh];
+          __syncthreads();
         }
-        cbase += ncache;
+      }
+      // publish the slice; the block that completes the request's last slice goes on
+      __threadfence();   // this thread's key writes, before the count and the arrival
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        slc_all[size_t(b) * kMaxGrid + slice] = nk;
+        __threadfence();
+        sm->last = atomicAdd(&ctr_all[b * 4 + 1], 1u) == static_cast<uint32_t>(nbk - 1);
+        __threadfence();
+      }
+      __syncthreads();
+      if (!sm->last) continue;
+      // ---- the final step of request b: slice offsets (a block scan over the run)
+      uint32_t tot = 0;
+      {
+        const int per = (nbk + kScoreThreads - 1) / kScoreThreads;
+        const int s0 = min(nbk, static_cast<int>(threadIdx.x) * per), s1 = min(nbk, s0 + per);
+        uint32_t cnt = 0;
+#pragma unroll 1
+        for (int q = s0; q < s1; ++q) cnt += __ldcg(slc_all + size_t(b) * kMaxGrid + q);
+        uint32_t pos = place(cnt, tot);
+#pragma unroll 1
+        for (int q = s0; q < s1; ++q) {
+          s_pre[q] = pos;
+          pos += __ldcg(slc_all + size_t(b) * kMaxGrid + q);
+        }
+        if (threadIdx.x == 0) s_pre[nbk] = tot;
         __syncthreads();
       }
-      if (lane == 0 && na) atomicAdd(&sm->cnt[0], na);
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        abv_all[size_t(b) * kMaxGrid + blockIdx.x] = sm->cnt[0];
-        const uint32_t nc = min(sm->cnt[1], static_cast<uint32_t>(kCandCap));
-        sm->cnt[1] = nc;
-        sm->base[1] = nc ? atomicAdd(&ctr[1], nc) : 0;
+      const uint32_t nkt = tot;
+      // the first kCandCap keys into shared memory (8-byte cp.async, all in flight)
+#pragma unroll 1
+      for (int q = 0; q < nbk; ++q) {
+        const uint32_t p0 = s_pre[q], n = s_pre[q + 1] - p0;
+        if (p0 >= static_cast<uint32_t>(kCandCap)) break;
+        const unsigned long long* src = kbuf + q * per_b * kTileRows;
+#pragma unroll 1
+        for (uint32_t i = threadIdx.x; i < n && p0 + i < static_cast<uint32_t>(kCandCap); i += blockDim.x)
+          cp_async8(s_cand + p0 + i, src + i);
       }
+      cp_async_wait_all();
       __syncthreads();
-#pragma unroll 1
-      for (uint32_t x = threadIdx.x; x < sm->cnt[1]; x += blockDim.x)
-        if (sm->base[1] + x < static_cast<uint32_t>(a.L.n_pad)) cand[sm->base[1] + x] = s_cand[x];
-      __syncthreads();
-    }
-  }
-
-  // ======================================================= phase 3: ordered output
-  // Each block finds the exact cut among the request's candidates (a radix select
-  // over the 64-bit keys; every block of the request computes the same cut), its
-  // output offset (selected entries of the request before its range) and writes
-  // its own selected entries in entry order: no sort is needed.
-  grid_barrier(sm, gbar, 2 * gridDim.x, a.spin);
-  const bool aborted3 = sm->abort;
-  // padding of requests with fewer than k visible entries (-1 after them)
-#pragma unroll 1
-  for (int b = blockIdx.x; b < a.B && !aborted3; b += gridDim.x) {
-    const int nb = visible(a, b);
-    if (nb >= a.k) continue;
-#pragma unroll 1
-    for (int j = nb + threadIdx.x; j < a.k; j += blockDim.x) {
-      a.topk_idx[size_t(b) * a.k + j] = -1;
-      if (a.topk_score) a.topk_score[size_t(b) * a.k + j] = -INFINITY;
-    }
-  }
-  {
-    long long C = 0;
-    int lofs = 0;
-#pragma unroll 1
-    for (int b = 0; b < a.B && !aborted3; ++b) {
-      const int nb = visible(a, b);
-      const long long tb = (nb + kTileRows - 1) / kTileRows;
-      long long lo, hi;
-      int fb;   // the first block holding tiles of request b
-      const bool mine = block_range(blockIdx.x, gridDim.x, C, tb, total, lo, hi, fb);
-      C += tb;
-      if (!mine || nb <= a.k) continue;
-      const uint32_t* ctr = ctr_all + b * 4;
-      // one round trip: the request's counters and the lower blocks' above-T counts
-      const int T = static_cast<int>(__ldcg(ctr + 2));
-      const uint32_t above = min(__ldcg(ctr + 3), static_cast<uint32_t>(a.k));
-      const uint32_t c = min(__ldcg(ctr + 1), static_cast<uint32_t>(a.L.n_pad));
-      uint32_t part = 0;
-#pragma unroll 1
-      for (long long q = fb + threadIdx.x; q < blockIdx.x; q += blockDim.x)
-        part += __ldcg(abv_all + size_t(b) * kMaxGrid + q);
-      if (T < 0) continue;   // uniform: the same word for every thread
-      const long long j0 = lo * kTileRows;
-      const long long j1 = min(hi * kTileRows, static_cast<long long>(nb));
-      const float* sc = scores_all + size_t(b) * a.L.n_pad;
-      const unsigned long long* gcand =
-          reinterpret_cast<const unsigned long long*>(a.ws + a.L.cand) + size_t(b) * a.L.n_pad;
-      const bool in_smem = c <= static_cast<uint32_t>(kCandCap);
-      if (in_smem) {
-        unsigned long long t4[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint32_t x = threadIdx.x + u * kScoreThreads;
-          t4[u] = x < c ? __ldcg(gcand + x) : 0ull;
+      // key x of the request, in entry order (past kCandCap: found in its slice's area)
+      auto key_at = [&](uint32_t x) -> unsigned long long {
+        if (x < static_cast<uint32_t>(kCandCap)) return s_cand[x];
+        int l = 0, r = nbk - 1;   // the slice q with s_pre[q] <= x < s_pre[q + 1]
+        while (l < r) {
+          const int m = (l + r + 1) >> 1;
+          if (s_pre[m] <= x) l = m; else r = m - 1;
         }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint32_t x = threadIdx.x + u * kScoreThreads;
-          if (x < c) s_c[x] = t4[u];
-        }
-#pragma unroll 1
-        for (uint32_t x = threadIdx.x + 4 * kScoreThreads; x < c; x += blockDim.x) s_c[x] = __ldcg(gcand + x);
-      }
+        return __ldcg(kbuf + l * per_b * kTileRows + (x - s_pre[l]));
+      };
+      // ---- the cut: the need-th largest key in bin T, by 8-bit digits (a last 4-bit
+      // one).  Keys above T never match the prefix, so only bin T's keys are counted.
       if (threadIdx.x == 0) {
-        sm->need = min(static_cast<uint32_t>(a.k) - above, c);
+        sm->need = min(static_cast<uint32_t>(a.k) - above, nkt > above ? nkt - above : 0u);
         sm->done = 0;
-        sm->out = 0;
-        sm->mask = ~0ull << 52;   // the 12 histogram bits are T for every candidate
+        sm->mask = ~0ull << 52;
         sm->prefix = static_cast<unsigned long long>(T) << 52;
       }
       __syncthreads();
-      // radix passes over the remaining 52 key bits (8-bit digits, a last 4-bit one)
 #pragma unroll 1
       for (int shift = 44; shift >= 0; shift = shift >= 8 ? shift - 8 : (shift > 0 ? 0 : -1)) {
         if (sm->done || sm->need == 0) break;
@@ -1037,8 +1047,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         __syncthreads();
         const unsigned long long pm = sm->mask, pp = sm->prefix;
 #pragma unroll 1
-        for (uint32_t x = threadIdx.x; x < c; x += blockDim.x) {
-          const unsigned long long key = in_smem ? s_c[x] : __ldcg(gcand + x);
+        for (uint32_t x = threadIdx.x; x < nkt; x += blockDim.x) {
+          const unsigned long long key = key_at(x);
           if ((key & pm) == pp) atomicAdd(&sm->dh[(key & dmask) >> shift], 1u);
         }
         __syncthreads();
@@ -1080,81 +1090,34 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         __syncthreads();
         if (shift == 0) break;
       }
-      // selected  <=>  (key64 & pm) >= pp   (entries above T included)
-      const unsigned long long pm = sm->mask, pp = sm->prefix;
-      // offset: selected entries of this request before j0 = the above-T counts of
-      // the lower blocks + the selected candidates before j0
+      // ---- the output: selected  <=>  (key64 & pm) >= pp, in entry order
+      {
+        const unsigned long long pm = sm->mask, pp = sm->prefix;
+        const uint32_t per = (nkt + kScoreThreads - 1) / kScoreThreads;
+        const uint32_t x0 = min(nkt, threadIdx.x * per), x1 = min(nkt, x0 + per);
+        uint32_t cnt = 0;
 #pragma unroll 1
-      for (uint32_t x = threadIdx.x; x < c; x += blockDim.x) {
-        const unsigned long long key = in_smem ? s_c[x] : __ldcg(gcand + x);
-        const long long j = 0xFFFFFFFFu - static_cast<uint32_t>(key);
-        if ((key & pm) >= pp && j < j0) ++part;
+        for (uint32_t x = x0; x < x1; ++x) cnt += (key_at(x) & pm) >= pp ? 1u : 0u;
+        uint32_t nsel;
+        uint32_t pos = place(cnt, nsel);
+#pragma unroll 1
+        for (uint32_t x = x0; x < x1; ++x) {
+          const unsigned long long key = key_at(x);
+          if ((key & pm) < pp) continue;
+          if (pos < static_cast<uint32_t>(a.k)) {
+            out_idx[pos] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(key));
+            if (out_sc) out_sc[pos] = from_order_key(static_cast<uint32_t>(key >> 32));
+          }
+          ++pos;
+        }
+        // fewer than k selected (only after an error): -1 after them
+#pragma unroll 1
+        for (uint32_t x = nsel + threadIdx.x; x < static_cast<uint32_t>(a.k); x += blockDim.x) {
+          out_idx[x] = -1;
+          if (out_sc) out_sc[x] = -INFINITY;
+        }
       }
-      if (part) atomicAdd(&sm->out, part);
       __syncthreads();
-      uint32_t running = sm->out;
-      const uint32_t* smx = segmax_all + size_t(b) * segs_pad;
-      const long long g0 = j0 / kSeg, g1 = (j1 + kSeg - 1) / kSeg;
-      const bool seg_smem = lofs + (g1 - g0) <= kSegCap;   // as in phase 2
-      const long long lbase = lofs - g0;
-      if (seg_smem) lofs += static_cast<int>(g1 - g0);
-      uint32_t* s_cnt = s_hs;   // per hit segment: its count (+ a trailing 0), then the exclusive scan
-#pragma unroll 1
-      for (long long gc = g0; gc < g1; gc += kChunk) {
-        const int nseg = static_cast<int>(min(g1, gc + kChunk) - gc);
-        const uint32_t nhit = ordered_list(
-            sm, nseg,
-            [&](int q) {
-              return seg_smem ? s_seg[lbase + gc + q] != 0
-                              : static_cast<int>(__ldcg(smx + gc + q) >> (32 - kHistBits)) >= T;
-            },
-            s_list);
-        // the value of lane `lane` of hit segment h (shared-memory cache or global)
-        auto value = [&](uint32_t h, long long& j) -> float {
-          const long long g = gc + s_list[h];
-          j = g * kSeg + lane;
-          int slot = -1;
-          if (seg_smem) {
-            const uint16_t info = s_seg[lbase + g];
-            if (info != kHitUncached) slot = info - 1;
-          }
-          return slot >= 0 ? s_cache[slot * kSeg + lane] : __ldcg(sc + j);
-        };
-        // counts: one warp per hit segment, one entry per lane
-#pragma unroll 1
-        for (uint32_t h = warp; h < nhit; h += nwarps) {
-          long long j;
-          const float v = value(h, j);
-          const unsigned long long k64 = (static_cast<unsigned long long>(order_key(v)) << 32) |
-                                         (0xFFFFFFFFu - static_cast<uint32_t>(j));
-          const uint32_t n = __popc(__ballot_sync(0xFFFFFFFFu, j < j1 && (k64 & pm) >= pp));
-          if (lane == 0) s_cnt[h] = n;
-        }
-        if (threadIdx.x == 0) s_cnt[nhit] = 0;
-        __syncthreads();
-        block_exclusive_scan(sm, s_cnt, static_cast<int>(nhit) + 1);   // s_cnt[nhit] = the chunk's total
-        // write: the selected entries of each hit segment at running + its prefix + rank
-#pragma unroll 1
-        for (uint32_t h = warp; h < nhit; h += nwarps) {
-          const uint32_t pre = s_cnt[h];
-          if (s_cnt[h + 1] == pre) continue;   // no selected entry in this segment
-          long long j;
-          const float v = value(h, j);
-          const unsigned long long k64 = (static_cast<unsigned long long>(order_key(v)) << 32) |
-                                         (0xFFFFFFFFu - static_cast<uint32_t>(j));
-          const bool sel = j < j1 && (k64 & pm) >= pp;
-          const unsigned m = __ballot_sync(0xFFFFFFFFu, sel);
-          if (sel) {
-            const uint32_t pos = running + pre + __popc(m & lt_mask);
-            if (pos < static_cast<uint32_t>(a.k)) {
-              a.topk_idx[size_t(b) * a.k + pos] = static_cast<int32_t>(j);
-              if (a.topk_score) a.topk_score[size_t(b) * a.k + pos] = v;
-            }
-          }
-        }
-        running += s_cnt[nhit];
-        __syncthreads();
-      }
     }
   }
 }
@@ -1187,10 +1150,10 @@ size_t score_smem_bytes() {
   constexpr int kStageBytes = FP8 ? kTileRows * 128 : kTileRows * 256;
   constexpr int kStages = FP8 ? kStagesFp8 : kStagesBf16;
   constexpr int kQImage = FP8 ? kQImageFp8 : kQImageBf16;
-  static_assert(kCandCap * 8 + kSegCache * kSeg * 4 <= kProducers * kStages * kStageBytes,
-                "selection buffers reuse the stage ring");
+  static_assert(kSelSegs * 2 <= 2 * kQImageFp8, "the hit list reuses the query images");
+  static_assert(kCandCap * 8 <= kGroups * kHistBins * 4, "the candidates reuse the histograms");
   return 1024 + kProducers * kStages * kStageBytes + 2 * kQImage + kGroups * kHistBins * 4 +
-         kScaleSlots * kTileRows * 4 + kSegCap * 2 + sizeof(ScoreSmem);
+         kScaleSlots * kTileRows * 4 + kScratch16 * 2 + sizeof(ScoreSmem);
 }
 
 // Cooperative launch of the score kernel: the selection phases meet at grid
