@@ -8,9 +8,10 @@
 // tokens; then RMSNorm over the channels and RoPE on the last 64 dims at the
 // position of the entry's first token.
 //
-// Design: a bandwidth kernel.  Threads own 4 consecutive channels (8-byte bf16
-// loads, coalesced across the group); an entry of D channels is a group of D/4
-// threads (one warp at D = 128, the whole 128-thread block at D = 512).  The
+// Design: threads own 4 consecutive channels (8-byte bf16 loads, coalesced across
+// the group); an entry of D channels is a group of D/4 threads (one warp at
+// D = 128, the whole 128-thread block at D = 512).  The slots' rows are staged in
+// shared memory by cp.async, eight slots per batch, two batches in flight.  The
 // arithmetic is the bit-exact fp32 contract: separately rounded __f*_rn
 // operations (never contracted to FMA), exp_own below, a pairwise sum of squares
 // that follows the channel order (in-thread pairs, then warp xor-shuffles, then
@@ -85,6 +86,9 @@ __device__ __forceinline__ float block_sum_pairwise(float v, int lt) {
   return v;
 }
 
+constexpr int kBatch = 8;   // slots staged per batch
+constexpr size_t kCompressSmem = 2 * kBatch * 128 * (8 + 8 + 16);   // two batches of kv, gate, bias
+
 template <int D>
 __global__ void __launch_bounds__(128) compress_kernel(const CompressArgs a) {
   constexpr int TPE = D / 4;        // threads per entry
@@ -126,14 +130,6 @@ __global__ void __launch_bounds__(128) compress_kernel(const CompressArgs a) {
       gp = tok_ptr(a.gate, s, a.T, tok, coff, half, D) + 2 * c0;
     }
   };
-  auto score = [&](const uint8_t* gp, const float* ap) -> float4 {
-    if (gp == nullptr) return make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-    const float4 g = load_bf16x4(gp);
-    const float4 b = *reinterpret_cast<const float4*>(ap);
-    return make_float4(__fadd_rn(g.x, b.x), __fadd_rn(g.y, b.y), __fadd_rn(g.z, b.z),
-                       __fadd_rn(g.w, b.w));
-  };
-
   // Loads that do not depend on the slots go first, so their latency (and the
   // req -> block table -> row chain) overlaps the slot loops.
   RowPtr dst{nullptr, nullptr};
@@ -148,58 +144,91 @@ __global__ void __launch_bounds__(128) compress_kernel(const CompressArgs a) {
                                  a.rope_cs + ((s * a.n + i) * 32 + (c0 - (D - 64)) / 2) * 2)
                            : make_float4(1.f, 0.f, 1.f, 0.f);
 
-  // Slots are visited in order, eight at a time with all eight slots' loads issued
-  // before any is used; the arithmetic order is the slot order either way.
-  constexpr int kBatch = 8;
+  // Slots are staged through shared memory in batches of kBatch with cp.async (the
+  // next batch's copies in flight while this one is computed), then taken one at a
+  // time in slot order by a rolled loop: the kernel runs once per decode step from
+  // a cold instruction cache, so its code stays small.  Each thread copies and reads
+  // only its own channels, so no block barrier is needed around the stages.
+  extern __shared__ __align__(16) uint8_t cmp_smem[];
+  uint2* s_kv = reinterpret_cast<uint2*>(cmp_smem);                 // [2][kBatch][128]
+  uint2* s_g = s_kv + 2 * kBatch * 128;                              // [2][kBatch][128]
+  float4* s_ap = reinterpret_cast<float4*>(s_g + 2 * kBatch * 128);  // [2][kBatch][128]
+  const int t = threadIdx.x;
+  const int nbatch = (slots + kBatch - 1) / kBatch;
+  auto issue = [&](int bt) {
+    const int buf = bt & 1;
+#pragma unroll 1
+    for (int u = 0; u < kBatch; ++u) {
+      const int j = bt * kBatch + u;
+      if (live && j < slots) {
+        const uint8_t *vp, *gp;
+        const float* ap;
+        slot_src(j, vp, gp, ap);
+        if (vp != nullptr) {
+          cp_async8(&s_kv[(buf * kBatch + u) * 128 + t], vp);
+          cp_async8(&s_g[(buf * kBatch + u) * 128 + t], gp);
+        }
+        cp_async16(&s_ap[(buf * kBatch + u) * 128 + t], ap);
+      }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  // slot j's biased score (-inf for the empty half) and, if wanted, its value
+  auto slot_at = [&](int j, float4& sc, float4* v) {
+    const int buf = (j / kBatch) & 1, u = j % kBatch;
+    const uint8_t *vp, *gp;
+    const float* ap;
+    slot_src(j, vp, gp, ap);
+    if (vp == nullptr) {
+      sc = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      if (v) *v = make_float4(0.f, 0.f, 0.f, 0.f);
+      return;
+    }
+    const uint2 g = s_g[(buf * kBatch + u) * 128 + t];
+    const float4 b = s_ap[(buf * kBatch + u) * 128 + t];
+    sc = make_float4(__fadd_rn(bf16lo(g.x), b.x), __fadd_rn(bf16hi(g.x), b.y), __fadd_rn(bf16lo(g.y), b.z),
+                     __fadd_rn(bf16hi(g.y), b.w));
+    if (v) {
+      const uint2 x = s_kv[(buf * kBatch + u) * 128 + t];
+      *v = make_float4(bf16lo(x.x), bf16hi(x.x), bf16lo(x.y), bf16hi(x.y));
+    }
+  };
+
   float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
   float4 den = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (live) {
-    // pass 1: m = max over slots of the biased scores
-    float4 m = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-    for (int j0 = 0; j0 < slots; j0 += kBatch) {
-      float4 sc[kBatch];
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        sc[u] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        if (j0 + u < slots) {
-          const uint8_t *vp, *gp;
-          const float* ap;
-          slot_src(j0 + u, vp, gp, ap);
-          sc[u] = score(gp, ap);
+  float4 m = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+  // pass 1: m = max over slots of the biased scores; pass 2: weights and slot-ordered
+  // sums (the scores recomputed bit for bit).  One batch: the stage serves both passes.
+#pragma unroll 1
+  for (int pass = 1; pass <= 2; ++pass) {
+    const bool reuse = pass == 2 && nbatch == 1;
+    if (!reuse) issue(0);
+#pragma unroll 1
+    for (int bt = 0; bt < nbatch; ++bt) {
+      if (!reuse) {
+        if (bt + 1 < nbatch) issue(bt + 1);
+        else asm volatile("cp.async.commit_group;" ::: "memory");
+        asm volatile("cp.async.wait_group 1;" ::: "memory");
+      }
+      if (!live) continue;
+#pragma unroll 1
+      for (int j = bt * kBatch; j < min(slots, (bt + 1) * kBatch); ++j) {
+        float4 sc, v;
+        if (pass == 1) {
+          slot_at(j, sc, nullptr);
+          m.x = fmaxf(m.x, sc.x); m.y = fmaxf(m.y, sc.y); m.z = fmaxf(m.z, sc.z); m.w = fmaxf(m.w, sc.w);
+        } else {
+          slot_at(j, sc, &v);
+          const float e0 = exp_own(__fsub_rn(sc.x, m.x)), e1 = exp_own(__fsub_rn(sc.y, m.y));
+          const float e2 = exp_own(__fsub_rn(sc.z, m.z)), e3 = exp_own(__fsub_rn(sc.w, m.w));
+          num.x = __fadd_rn(num.x, __fmul_rn(e0, v.x)); den.x = __fadd_rn(den.x, e0);
+          num.y = __fadd_rn(num.y, __fmul_rn(e1, v.y)); den.y = __fadd_rn(den.y, e1);
+          num.z = __fadd_rn(num.z, __fmul_rn(e2, v.z)); den.z = __fadd_rn(den.z, e2);
+          num.w = __fadd_rn(num.w, __fmul_rn(e3, v.w)); den.w = __fadd_rn(den.w, e3);
         }
       }
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        m.x = fmaxf(m.x, sc[u].x); m.y = fmaxf(m.y, sc[u].y);
-        m.z = fmaxf(m.z, sc[u].z); m.w = fmaxf(m.w, sc[u].w);
-      }
     }
-    // pass 2: weights and slot-ordered sums (the scores are recomputed bit for bit)
-    for (int j0 = 0; j0 < slots; j0 += kBatch) {
-      float4 sc[kBatch], v[kBatch];
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        sc[u] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (j0 + u < slots) {
-          const uint8_t *vp, *gp;
-          const float* ap;
-          slot_src(j0 + u, vp, gp, ap);
-          sc[u] = score(gp, ap);
-          if (vp) v[u] = load_bf16x4(vp);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        if (j0 + u >= slots) break;
-        const float e0 = exp_own(__fsub_rn(sc[u].x, m.x)), e1 = exp_own(__fsub_rn(sc[u].y, m.y));
-        const float e2 = exp_own(__fsub_rn(sc[u].z, m.z)), e3 = exp_own(__fsub_rn(sc[u].w, m.w));
-        num.x = __fadd_rn(num.x, __fmul_rn(e0, v[u].x)); den.x = __fadd_rn(den.x, e0);
-        num.y = __fadd_rn(num.y, __fmul_rn(e1, v[u].y)); den.y = __fadd_rn(den.y, e1);
-        num.z = __fadd_rn(num.z, __fmul_rn(e2, v[u].z)); den.z = __fadd_rn(den.z, e2);
-        num.w = __fadd_rn(num.w, __fmul_rn(e3, v[u].w)); den.w = __fadd_rn(den.w, e3);
-      }
-    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
   }
   float4 y = live ? make_float4(__fdiv_rn(num.x, den.x), __fdiv_rn(num.y, den.y),
                                 __fdiv_rn(num.z, den.z), __fdiv_rn(num.w, den.w))
@@ -283,9 +312,13 @@ cudaError_t launch_compress(const void* kv, const void* gate, const void* prev_k
   const long long total = static_cast<long long>(S) * a.n;
   if (total == 0) return cudaSuccess;
   if (dim == 512) {
-    compress_kernel<512><<<static_cast<unsigned>(total), 128, 0, stream>>>(a);
+    cudaFuncSetAttribute(compress_kernel<512>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(kCompressSmem));
+    compress_kernel<512><<<static_cast<unsigned>(total), 128, kCompressSmem, stream>>>(a);
   } else {
-    compress_kernel<128><<<static_cast<unsigned>((total + 3) / 4), 128, 0, stream>>>(a);
+    cudaFuncSetAttribute(compress_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(kCompressSmem));
+    compress_kernel<128><<<static_cast<unsigned>((total + 3) / 4), 128, kCompressSmem, stream>>>(a);
   }
   return cudaGetLastError();
 }
