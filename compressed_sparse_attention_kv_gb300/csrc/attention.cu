@@ -10,10 +10,11 @@
 // GB300 design.  A request's key list is cut into 128-key tiles: tile 0 is the
 // 128-slot window ring, tiles 1.. are 128 consecutive list entries.  One block
 // handles one (request, tile, head group of <= 64 heads):
-//   * 8 warps gather the tile's rows (528 B FP8, 288 B FP4 or 1 KiB bf16; the
-//     row addresses come from the block table), dequantise them exactly into
-//     bf16 and store a 128 x 512 K-major tile with 128-byte swizzle;
-//   * the query is rotated (fp32) and stored as bf16 in the same layout;
+//   * the tile's rows (528 B FP8, 288 B FP4 or 1 KiB bf16; the row addresses come
+//     from the block table) and the query are copied into shared memory with
+//     cp.async, all in flight together; the rows are dequantised exactly into
+//     bf16, giving a 128 x 512 K-major tile with 128-byte swizzle, and the query's
+//     last 64 dims are rotated (fp32) in place;
 //   * one thread issues tcgen05 MMAs S^T = K Q^T (M = 128 keys, N = heads,
 //     K = 512) into TMEM - keys are the MMA rows, so 16..64 heads need no padding;
 //   * softmax statistics per head (max, sum of exp2) over the tile, P^T stored
@@ -102,31 +103,12 @@ __device__ __forceinline__ void put16(uint8_t* tile, int row, int l, const float
   *reinterpret_cast<uint4*>(base + sw128_offset(row, c0 + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
-// Raw bytes lane l needs from one row: codes (16 B FP8 / 8 B FP4 / 32 B bf16) and
-// its scale byte.  Split from the conversion so a warp can issue the loads of
-// several rows before it converts any of them.
+// Raw bytes of 16 values of one row: codes (16 B FP8 / 8 B FP4 / 32 B bf16) and
+// their scale byte.
 struct RowBytes {
   uint4 lo, hi;
   uint32_t scb;
 };
-
-__device__ __forceinline__ RowBytes load16(int fmt, const uint8_t* row, int l) {
-  RowBytes r;
-  r.hi = make_uint4(0u, 0u, 0u, 0u);
-  if (fmt == CSKV_FMT_FP8_E4M3_E8M0_B32) {
-    r.lo = *reinterpret_cast<const uint4*>(row + 16 * l);
-    r.scb = row[kD + (l >> 1)];
-  } else if (fmt == CSKV_FMT_FP4_E2M1_E4M3_B16) {
-    const uint2 c = *reinterpret_cast<const uint2*>(row + 8 * l);
-    r.lo = make_uint4(c.x, c.y, 0u, 0u);
-    r.scb = row[kD / 2 + l];
-  } else {
-    r.lo = *reinterpret_cast<const uint4*>(row + 32 * l);
-    r.hi = *reinterpret_cast<const uint4*>(row + 32 * l + 16);
-    r.scb = 0;
-  }
-  return r;
-}
 
 // Exact dequantisation of lane l's 16 values (dims 16l .. 16l+15) from its raw bytes.
 __device__ __forceinline__ void convert16(int fmt, const RowBytes& r, float (&v)[16]) {
@@ -174,6 +156,7 @@ struct AttnSmem {
   float m[kMaxHeadsPerBlock];
   float l[kMaxHeadsPerBlock];
   const uint8_t* rowp[kKeys];   // address of each key row of the tile, null = no key
+  __align__(16) uint8_t scl[kKeys][32];   // staged scale bytes of each row (FP8: 16, FP4: 32)
 };
 
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnArgs a) {
@@ -204,9 +187,31 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
   }
   if (warp == 0) tmem_alloc(&sm->tmem_base, 512);
 
+  // Every global read of this block is a cp.async straight into shared memory, so
+  // the loads are all in flight together and need no registers:
+  //  - the query rows (bf16) into their places in the swizzled Q tile, the last 64
+  //    dims rotated afterwards in shared memory;
+  //  - bf16 key rows into their places in the swizzled K tile;
+  //  - FP8 / FP4 key rows: the codes into the upper half of the K tile region, the
+  //    scale bytes into sm->scl, then dequantised in place in two halves (dims
+  //    0-255 first; the codes of dims 256-511 are read into registers before the
+  //    half they share is overwritten).
+  // The code runs once per block from a cold instruction cache; loops stay rolled.
+  const int row_fmt = tile == 0 ? a.swa_fmt : a.kv.fmt;
+  uint8_t* stage = ktile + 4 * kKeys * 128;   // upper half of the K tile: dims 256-511
+  // ---- query: 64 chunks of 16 bytes per head row, zero rows for padded heads
+  {
+    const uint8_t* qb = a.q + (size_t(b) * a.H + h0) * kD * 2;
+#pragma unroll 1
+    for (int x = threadIdx.x; x < Nq * 64; x += blockDim.x) {
+      const int h = x >> 6, c = x & 63;   // dims 8c .. 8c+7
+      uint8_t* dst = qtile + (c >> 3) * (Nq * 128) + sw128_offset(h, c & 7);
+      if (h < Hb) cp_async16(dst, qb + (size_t(h) * kD + c * 8) * 2);
+      else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
   // ---- rows of this tile: one thread per row resolves its address (the list entry,
   // then the block table), all rows in parallel
-  const int row_fmt = tile == 0 ? a.swa_fmt : a.kv.fmt;
   for (int r = threadIdx.x; r < kKeys; r += blockDim.x) {
     const uint8_t* p = nullptr;
     if (tile == 0) {
@@ -223,81 +228,104 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
     }
     sm->rowp[r] = p;
   }
-
-  // ---- query: rotate the last 64 dims by the query position, store bf16 (K-major,
-  // swizzled).  Items of 8 consecutive dims, eight items' loads in flight per thread.
+  __syncthreads();
+  // ---- key rows
+  const bool bf16_rows = row_fmt == CSKV_FMT_BF16;
+  const int code_bytes = row_fmt == CSKV_FMT_FP8_E4M3_E8M0_B32 ? kD : kD / 2;
+  const int scl_bytes = row_fmt == CSKV_FMT_FP8_E4M3_E8M0_B32 ? kD / 32 : kD / 16;
   {
-    const float* cs = a.q_rope + size_t(b) * 64;
-    const int items = Nq * 64;
-    for (int i0 = threadIdx.x; i0 < items; i0 += 8 * blockDim.x) {
-      uint4 raw[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int idx = i0 + u * blockDim.x;
-        const int h = idx >> 6, d0 = (idx & 63) * 8;
-        raw[u] = (idx < items && h < Hb)
-                     ? *reinterpret_cast<const uint4*>(a.q + ((size_t(b) * a.H + h0 + h) * kD + d0) * 2)
-                     : make_uint4(0u, 0u, 0u, 0u);
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int idx = i0 + u * blockDim.x;
-        if (idx >= items) break;
-        const int h = idx >> 6, d0 = (idx & 63) * 8;
-        float v[8] = {bf16lo(raw[u].x), bf16hi(raw[u].x), bf16lo(raw[u].y), bf16hi(raw[u].y),
-                      bf16lo(raw[u].z), bf16hi(raw[u].z), bf16lo(raw[u].w), bf16hi(raw[u].w)};
-        if (d0 >= kD - 64) {
-#pragma unroll
-          for (int p = 0; p < 4; ++p) {
-            const int kk = (d0 - (kD - 64)) / 2 + p;
-            const float c = cs[2 * kk], s = cs[2 * kk + 1];
-            const float y0 = v[2 * p], y1 = v[2 * p + 1];
-            v[2 * p] = y0 * c - y1 * s;
-            v[2 * p + 1] = y0 * s + y1 * c;
-          }
-        }
-        uint32_t w[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          __nv_bfloat162 hh = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-          w[i] = *reinterpret_cast<uint32_t*>(&hh);
-        }
-        // dims d0..d0+7 -> chunk d0/64, 16-byte chunk (d0%64)/8
-        *reinterpret_cast<uint4*>(qtile + (d0 >> 6) * (Nq * 128) + sw128_offset(h, (d0 & 63) >> 3)) =
-            make_uint4(w[0], w[1], w[2], w[3]);
+    const int cpr = bf16_rows ? 64 : (code_bytes + scl_bytes) / 16;   // 16-byte chunks per row
+#pragma unroll 1
+    for (int x = threadIdx.x; x < kKeys * cpr; x += blockDim.x) {
+      const int r = x / cpr, c = x - r * cpr;
+      const uint8_t* p = sm->rowp[r];
+      if (bf16_rows) {
+        uint8_t* dst = ktile + (c >> 3) * (kKeys * 128) + sw128_offset(r, c & 7);
+        if (p) cp_async16(dst, p + c * 16);
+        else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+      } else if (p) {
+        if (c * 16 < code_bytes) cp_async16(stage + r * code_bytes + c * 16, p + c * 16);
+        else cp_async16(&sm->scl[r][c * 16 - code_bytes], p + c * 16);
       }
     }
   }
+  cp_async_wait_all();
   __syncthreads();
-
-  // ---- gather + dequantise the 128 key rows: warp w owns rows w, w+8, ...; lane = 16
-  // dims; the loads of 8 rows are issued before any is converted
+  // ---- rotate the query's last 64 dims (pairs (2i, 2i+1) by the query position)
   {
-    constexpr int kWarps = kAttnThreads / 32;
-    for (int r0 = warp; r0 < kKeys; r0 += 8 * kWarps) {
-      RowBytes rb[8];
+    const float* cs = a.q_rope + size_t(b) * 64;
+#pragma unroll 1
+    for (int x = threadIdx.x; x < Hb * 8; x += blockDim.x) {
+      const int h = x >> 3, g = x & 7;   // dims 448 + 8g .. +7: chunk 7, 16-byte chunk g
+      uint4* pq = reinterpret_cast<uint4*>(qtile + 7 * (Nq * 128) + sw128_offset(h, g));
+      const uint4 raw = *pq;
+      float v[8] = {bf16lo(raw.x), bf16hi(raw.x), bf16lo(raw.y), bf16hi(raw.y),
+                    bf16lo(raw.z), bf16hi(raw.z), bf16lo(raw.w), bf16hi(raw.w)};
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const uint8_t* p = sm->rowp[r0 + u * kWarps];
-        if (p != nullptr) {
-          rb[u] = load16(row_fmt, p, lane);
-        } else {
-          rb[u].lo = make_uint4(0u, 0u, 0u, 0u);
-          rb[u].hi = make_uint4(0u, 0u, 0u, 0u);
-          rb[u].scb = 0;
-        }
+      for (int p = 0; p < 4; ++p) {
+        const int kk = 4 * g + p;
+        const float c = cs[2 * kk], sn = cs[2 * kk + 1];
+        const float y0 = v[2 * p], y1 = v[2 * p + 1];
+        v[2 * p] = y0 * c - y1 * sn;
+        v[2 * p + 1] = y0 * sn + y1 * c;
       }
+      uint32_t w[4];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        float v[16];
-        if (sm->rowp[r0 + u * kWarps] != nullptr) {
-          convert16(row_fmt, rb[u], v);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] = 0.f;
-        }
-        put16(ktile, r0 + u * kWarps, lane, v);
+      for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 hh = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+        w[i] = *reinterpret_cast<uint32_t*>(&hh);
       }
+      *pq = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+  // ---- dequantise FP8 / FP4 rows in place: item (r, l) = dims 16l .. 16l+15 of row r
+  if (!bf16_rows) {
+    const bool fp8 = row_fmt == CSKV_FMT_FP8_E4M3_E8M0_B32;
+    auto raw_of = [&](int r, int l) -> RowBytes {
+      RowBytes rb;
+      rb.hi = make_uint4(0u, 0u, 0u, 0u);
+      if (fp8) {
+        rb.lo = *reinterpret_cast<const uint4*>(stage + r * kD + 16 * l);
+        rb.scb = sm->scl[r][l >> 1];
+      } else {
+        const uint2 c = *reinterpret_cast<const uint2*>(stage + r * (kD / 2) + 8 * l);
+        rb.lo = make_uint4(c.x, c.y, 0u, 0u);
+        rb.scb = sm->scl[r][l];
+      }
+      return rb;
+    };
+    auto emit = [&](int r, int l, const RowBytes& rb) {
+      float v[16];
+      if (sm->rowp[r] != nullptr) {
+        convert16(row_fmt, rb, v);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = 0.f;
+      }
+      put16(ktile, r, l, v);
+    };
+    // dims 0-255 (l < 16): outputs in the lower half, codes in the upper half
+#pragma unroll 1
+    for (int x = threadIdx.x; x < kKeys * 16; x += blockDim.x) {
+      const int r = x >> 4, l = x & 15;
+      emit(r, l, raw_of(r, l));
+    }
+    // dims 256-511: every thread reads its items' codes before any is overwritten
+    constexpr int kPer = kKeys * 16 / kAttnThreads;   // 8
+    RowBytes rb[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int x = threadIdx.x + u * kAttnThreads;
+      rb[u] = raw_of(x >> 4, 16 + (x & 15));
+    }
+    __syncthreads();
+#pragma unroll 1
+    for (int u = 0; u < kPer; ++u) {
+      const int x = threadIdx.x + u * kAttnThreads;
+      RowBytes cur = rb[0];
+#pragma unroll
+      for (int q = 1; q < kPer; ++q) if (q == u) cur = rb[q];
+      emit(x >> 4, 16 + (x & 15), cur);
     }
   }
   fence_proxy_async_smem();
