@@ -48,6 +48,8 @@ namespace {
 
 constexpr int kHistBits = 12;
 constexpr int kHistBins = 1 << kHistBits;
+constexpr int kCoarseBins = 256;                      // sums of 16 fine bins (the top 8 key bits)
+constexpr int kHistStride = kHistBins + kCoarseBins;  // per request in the workspace
 constexpr int kTileRows = 128;
 constexpr int kProducers = 2;        // TMA-issuing warps, each with its own stage ring
 constexpr int kGroups = 2;           // epilogue groups of 4 warps (one per TMEM lane quarter)
@@ -70,6 +72,7 @@ __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_
 constexpr int kMaxGrid = 1024;       // bound of the per-block counters' table
 constexpr int kSeg = 32;             // entries per segment (one epilogue warp's rows of a tile)
 constexpr int kSelSegs = 8192;       // segments per selection pass (262,144 entries)
+constexpr int kReqCache = 64;        // requests whose visible count is kept in shared memory
 constexpr int kScratch16 = kSelSegs + 64 - kScaleSlots * kTileRows * 2;   // u16 words after the scale ring
 
 struct WsLayout {
@@ -87,7 +90,7 @@ __host__ __device__ inline WsLayout ws_layout(int B, int n_max, int k) {
   L.cand = o;   o = align256(o + size_t(B) * L.n_pad * 8);
   L.qimg = o;   o = align256(o + size_t(B) * kQSlot);
   L.wq = o;     o = align256(o + size_t(B) * 64 * 4);
-  L.hist = o;   o = align256(o + size_t(B) * kHistBins * 4);
+  L.hist = o;   o = align256(o + size_t(B) * kHistStride * 4);
   L.ctr = o;    o = align256(o + size_t(B) * 4 * 4);
   L.slc = o;    o = align256(o + size_t(B) * kMaxGrid * 4);
   L.gbar = o;   o = align256(o + 16);
@@ -146,9 +149,9 @@ __global__ void __launch_bounds__(256) index_prep_kernel(const IndexArgs a) {
   const int b = blockIdx.x;
   uint8_t* img = a.ws + a.L.qimg + size_t(b) * kQSlot;
   float* wq = reinterpret_cast<float*>(a.ws + a.L.wq) + b * 64;
-  uint32_t* hist = reinterpret_cast<uint32_t*>(a.ws + a.L.hist) + size_t(b) * kHistBins;
+  uint32_t* hist = reinterpret_cast<uint32_t*>(a.ws + a.L.hist) + size_t(b) * kHistStride;
   uint32_t* ctr = reinterpret_cast<uint32_t*>(a.ws + a.L.ctr) + b * 4;
-  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) hist[i] = 0;
+  for (int i = threadIdx.x; i < kHistStride; i += blockDim.x) hist[i] = 0;
   if (threadIdx.x < 4)
     ctr[threadIdx.x] = threadIdx.x == 0 ? static_cast<uint32_t>(first_home_block(b + 1, a.B, a.grid) -
                                                              first_home_block(b, a.B, a.grid)) * kChunkTiles
@@ -213,6 +216,7 @@ struct ScoreSmem {
   uint32_t cnt[2];
   uint32_t base[2];
   uint32_t nlist;
+  int nbv[kReqCache];              // visible entries of the first kReqCache requests
   int T;
   uint32_t above, inT;
   uint32_t need, done, out;
@@ -266,43 +270,19 @@ __device__ void grid_barrier(ScoreSmem* sm, uint32_t* counter, uint32_t target, 
 }
 
 // T = the largest histogram bin with (entries in bins >= T) >= k; above = entries in
-// bins > T; T = -1 if the histogram holds fewer than k entries.  Whole block; the
-// request's bins are copied into `hs` (4,096 words of shared memory) in one pass.
-// This code runs once per launch, from a cold instruction cache: it is kept short
-// (rolled loops) rather than unrolled.
-__device__ void threshold_bin(ScoreSmem* sm, const uint32_t* ghist, uint32_t* hs, int k) {
-  constexpr int kVec = kHistBins / 4;
-  constexpr int kPer = (kVec + kScoreThreads - 1) / kScoreThreads;
-  uint4 v[kPer];
-#pragma unroll
-  for (int u = 0; u < kPer; ++u) {
-    const int i = threadIdx.x + u * kScoreThreads;
-    v[u] = i < kVec ? __ldcg(reinterpret_cast<const uint4*>(ghist) + i) : make_uint4(0u, 0u, 0u, 0u);
-  }
-#pragma unroll
-  for (int u = 0; u < kPer; ++u) {
-    const int i = threadIdx.x + u * kScoreThreads;
-    if (i < kVec) reinterpret_cast<uint4*>(hs)[i] = v[u];
-  }
-  __syncthreads();
-  // 256 parts of 16 bins, part p = bins 16p .. 16p+15
-  for (int t = threadIdx.x; t < 256; t += blockDim.x) {
-    const uint4* q = reinterpret_cast<const uint4*>(hs + t * 16);
-    uint32_t loc = 0;
-#pragma unroll 1
-    for (int i = 0; i < 4; ++i) {
-      const uint4 x = q[i];
-      loc += x.x + x.y + x.z + x.w;
-    }
-    sm->part[t] = loc;
-  }
-  __syncthreads();
+// bins > T; inT = entries in bin T; T = -1 if the histogram holds fewer than k
+// entries.  Whole block (warp 0 works): the 256 coarse bins (sums of 16 fine bins),
+// then the 16 fine bins of the coarse bin that crosses k; two small loads.
+__device__ void threshold_bin(ScoreSmem* sm, const uint32_t* gh, int k) {
   const int lane = threadIdx.x;
   if (lane < 32) {
-    // lane l owns parts 255-8l .. 248-8l (from the top)
+    // lane l owns coarse bins 255-8l .. 248-8l (from the top): two 16-byte loads
+    const uint4 c0 = __ldcg(reinterpret_cast<const uint4*>(gh + kHistBins + 248 - 8 * lane));
+    const uint4 c1 = __ldcg(reinterpret_cast<const uint4*>(gh + kHistBins + 252 - 8 * lane));
+    const uint32_t loc[8] = {c1.w, c1.z, c1.y, c1.x, c0.w, c0.z, c0.y, c0.x};   // top first
     uint32_t sum = 0;
-#pragma unroll 1
-    for (int i = 0; i < 8; ++i) sum += sm->part[255 - 8 * lane - i];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sum += loc[i];
     uint32_t incl = sum;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -311,27 +291,30 @@ __device__ void threshold_bin(ScoreSmem* sm, const uint32_t* ghist, uint32_t* hs
     }
     const unsigned hit = __ballot_sync(0xFFFFFFFFu, incl >= static_cast<uint32_t>(k));
     if (hit == 0) {
-      if (lane == 0) { sm->T = -1; sm->above = 0; }
+      if (lane == 0) { sm->T = -1; sm->above = 0; sm->inT = 0; }
     } else if (lane == __ffs(hit) - 1) {
-      // walk down this lane's parts, then the bins of the part that crosses k
       uint32_t acc = incl - sum;
       int u = 255 - 8 * lane - 7;
-#pragma unroll 1
+#pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const uint32_t x = sm->part[255 - 8 * lane - i];
-        if (acc + x >= static_cast<uint32_t>(k)) { u = 255 - 8 * lane - i; break; }
-        acc += x;
+        if (acc + loc[i] >= static_cast<uint32_t>(k)) { u = 255 - 8 * lane - i; break; }
+        acc += loc[i];
       }
+      uint4 f[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) f[q] = __ldcg(reinterpret_cast<const uint4*>(gh + u * 16) + q);
+      const uint32_t fb[16] = {f[0].x, f[0].y, f[0].z, f[0].w, f[1].x, f[1].y, f[1].z, f[1].w,
+                               f[2].x, f[2].y, f[2].z, f[2].w, f[3].x, f[3].y, f[3].z, f[3].w};
       int T = u * 16;
-#pragma unroll 1
+      uint32_t inT = fb[0];
+#pragma unroll
       for (int i = 15; i >= 0; --i) {
-        const uint32_t hb = hs[u * 16 + i];
-        if (acc + hb >= static_cast<uint32_t>(k)) { T = u * 16 + i; break; }
-        acc += hb;
+        if (acc + fb[i] >= static_cast<uint32_t>(k)) { T = u * 16 + i; inT = fb[i]; break; }
+        acc += fb[i];
       }
       sm->T = T;
       sm->above = acc;
-      sm->inT = hs[T];
+      sm->inT = inT;
     }
   }
   __syncthreads();
@@ -375,8 +358,30 @@ __device__ void block_exclusive_scan16(ScoreSmem* sm, uint16_t* x, int n) {
 __device__ __forceinline__ bool block_range(int blk, int G, long long C, long long tb, long long total,
                                             long long& lo, long long& hi, int& fb, int& nbk,
                                             long long& per) {
-  fb = total > 0 ? static_cast<int>(min(static_cast<long long>(G - 1), C * G / total)) : 0;
-  if (tb <= 0) {   // an empty request: its run is block fb alone, with no tiles
+  // 32-bit arithmetic while (C + tb) * G fits (every realistic batch), 64-bit beyond
+  if (total * G < (1ll << 32)) {
+    const uint32_t t32 = static_cast<uint32_t>(total), g32 = static_cast<uint32_t>(G);
+    const uint32_t c32 = static_cast<uint32_t>(C), b32 = static_cast<uint32_t>(tb);
+    const uint32_t f = t32 ? min(g32 - 1, c32 * g32 / t32) : 0u;
+    fb = static_cast<int>(f);
+    if (b32 == 0) {   // an empty request: its run is block fb alone, with no tiles
+      nbk = 1;
+      per = 1;
+      lo = hi = 0;
+      return blk == fb;
+    }
+    uint32_t e = (c32 + b32) * g32 / t32;
+    if (e <= f) e = f + 1;
+    const uint32_t p = (b32 + (e - f) - 1) / (e - f);
+    per = p;
+    nbk = static_cast<int>((b32 + p - 1) / p);
+    if (blk < fb || blk >= fb + nbk) return false;
+    lo = static_cast<long long>(static_cast<uint32_t>(blk - fb) * p);
+    hi = min(tb, lo + p);
+    return true;
+  }
+  fb = static_cast<int>(min(static_cast<long long>(G - 1), C * G / total));
+  if (tb <= 0) {
     nbk = 1;
     per = 1;
     lo = hi = 0;
@@ -385,7 +390,7 @@ __device__ __forceinline__ bool block_range(int blk, int G, long long C, long lo
   int eb = static_cast<int>(((C + tb) * G) / total);
   if (eb <= fb) eb = fb + 1;
   per = (tb + (eb - fb) - 1) / (eb - fb);
-  nbk = static_cast<int>((tb + per - 1) / per);   // blocks of the run that hold tiles
+  nbk = static_cast<int>((tb + per - 1) / per);
   if (blk < fb || blk >= fb + nbk) return false;
   lo = (blk - fb) * per;
   hi = min(tb, lo + per);
@@ -450,7 +455,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 
   // work range of this block: a contiguous run of the global tile sequence
   long long total = 0;
-  for (int b = 0; b < a.B; ++b) total += (visible(a, b) + kTileRows - 1) / kTileRows;
+  for (int b = 0; b < a.B; ++b) {
+    const int v = visible(a, b);
+    total += (v + kTileRows - 1) / kTileRows;
+    if (threadIdx.x == 0 && b < kReqCache) sm->nbv[b] = v;   // read after the set-up barrier
+  }
 
   if (threadIdx.x == 0) {
     for (int p = 0; p < kProducers; ++p)
@@ -708,9 +717,20 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       ++hphase;
     };
     auto flush = [&](int b) {
+      uint32_t* gh = ghist + size_t(b) * kHistStride;
+      // coarse bins c = gtid, gtid + 128: the sums of fine bins 16c .. 16c+15 (rotated
+      // start, so the lanes of a warp spread over the banks)
+#pragma unroll 1
+      for (int c = gtid; c < kCoarseBins; c += 128) {
+        uint32_t sum = 0;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) sum += ghs[16 * c + ((q + c) & 15)];
+        if (sum) atomicAdd(gh + kHistBins + c, sum);
+      }
+#pragma unroll 1
       for (int x = gtid; x < kHistBins; x += 128) {
         const uint32_t cnt = ghs[x];
-        if (cnt) { atomicAdd(ghist + size_t(b) * kHistBins + x, cnt); ghs[x] = 0; }
+        if (cnt) { atomicAdd(gh + x, cnt); ghs[x] = 0; }
       }
     };
     for (long long i = grp;; i += kGroups) {
@@ -836,13 +856,16 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     long long C = 0;
 #pragma unroll 1
     for (int b = 0; b < a.B && !aborted; ++b) {
-      const int nb = visible(a, b);
+      const int nb = b < kReqCache ? sm->nbv[b] : visible(a, b);
       const long long tb = (nb + kTileRows - 1) / kTileRows;
       long long lo, hi, per_b;
       int fb, nbk;
       const bool mine = block_range(blockIdx.x, gridDim.x, C, tb, total, lo, hi, fb, nbk, per_b);
       C += tb;
-      if (!mine) continue;
+      if (!mine) {
+        if (fb > static_cast<int>(blockIdx.x)) break;   // the runs only move further right
+        continue;
+      }
       const int slice = blockIdx.x - fb;
       const float* sc = scores_all + size_t(b) * a.L.n_pad;
       int32_t* out_idx = a.topk_idx + size_t(b) * a.k;
@@ -864,7 +887,23 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         }
         continue;
       }
-      threshold_bin(sm, ghist + size_t(b) * kHistBins, hist, a.k);
+      const uint32_t* smx = segmax_all + size_t(b) * segs_pad;
+      unsigned long long* kbuf = reinterpret_cast<unsigned long long*>(a.ws + a.L.cand) + size_t(b) * a.L.n_pad;
+      const int nseg = (nb + kSeg - 1) / kSeg;
+      const long long gs0 = lo * 4, gs1 = min(hi * 4, static_cast<long long>(nseg));
+      // the slice's segment table into shared memory, in flight with the threshold loads
+      uint32_t* s_seg32 = hist;   // free: the selection keys use it only in the final step
+      const bool pre = gs1 - gs0 <= kSelSegs;
+      if (pre) {
+#pragma unroll 1
+        for (long long x = threadIdx.x; x < (gs1 - gs0 + 3) / 4; x += blockDim.x)
+          cp_async16(s_seg32 + 4 * x, smx + gs0 + 4 * x);
+      }
+      threshold_bin(sm, ghist + size_t(b) * kHistStride, a.k);
+      if (pre) {
+        cp_async_wait_all();
+        __syncthreads();
+      }
       const int T = sm->T;
       const uint32_t above = sm->above;
       if (T < 0) {
@@ -878,9 +917,6 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         }
         continue;
       }
-      const uint32_t* smx = segmax_all + size_t(b) * segs_pad;
-      unsigned long long* kbuf = reinterpret_cast<unsigned long long*>(a.ws + a.L.cand) + size_t(b) * a.L.n_pad;
-      const int nseg = (nb + kSeg - 1) / kSeg;
       // the hit segments of [g0, g0 + ns) (g0 a multiple of 4) into s_list, in order:
       // thread t owns segments 24t .. 24t+23 (six 16-byte loads of the segment table)
       auto hit_list = [&](long long g0, int ns) -> uint32_t {
@@ -892,7 +928,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         for (int u = 0; u < kOwn / 4; ++u) {
           const int q = q0 + 4 * u;
           if (q < ns) {   // the table's rows are padded to a multiple of 4 segments
-            const uint4 x = __ldcg(reinterpret_cast<const uint4*>(smx + g0 + q));
+            const uint4 x = pre ? *reinterpret_cast<const uint4*>(s_seg32 + (g0 - gs0) + q)
+                                : __ldcg(reinterpret_cast<const uint4*>(smx + g0 + q));
             m |= (static_cast<int>(x.x >> (32 - kHistBits)) >= T ? 1u : 0u) << (4 * u);
             m |= (static_cast<int>(x.y >> (32 - kHistBits)) >= T ? 2u : 0u) << (4 * u);
             m |= (static_cast<int>(x.z >> (32 - kHistBits)) >= T ? 4u : 0u) << (4 * u);
@@ -916,9 +953,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       // segment, one entry per lane, four segments per step with their loads first.
       unsigned long long* kout = kbuf + lo * kTileRows;
       uint32_t nk = 0;
-      const long long gs1 = min(hi * 4, static_cast<long long>(nseg));
 #pragma unroll 1
-      for (long long gc = lo * 4; gc < gs1; gc += kSelSegs) {
+      for (long long gc = gs0; gc < gs1; gc += kSelSegs) {
         const int ns = static_cast<int>(min(static_cast<long long>(kSelSegs), gs1 - gc));
         const uint32_t nhit = hit_list(gc, ns);
 #pragma unroll 1
@@ -1029,8 +1065,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         }
         return __ldcg(kbuf + l * per_b * kTileRows + (x - s_pre[l]));
       };
-      // ---- the cut: the need-th largest key in bin T, by 8-bit digits (a last 4-bit
-      // one).  Keys above T never match the prefix, so only bin T's keys are counted.
+      // ---- the cut: the need-th largest key in bin T, by 12-bit digits (bits 51-40,
+      // 39-28, 27-16, 15-4, then 3-0; with a few hundred keys in bin T the first digit
+      // usually decides).  Keys above T never match the prefix, so only bin T's keys
+      // are counted.  The digit histogram uses the stage ring (free by now).
+      uint32_t* dh = reinterpret_cast<uint32_t*>(stages);   // 4,096 bins
       if (threadIdx.x == 0) {
         sm->need = min(static_cast<uint32_t>(a.k) - above, nkt > above ? nkt - above : 0u);
         sm->done = 0;
@@ -1039,53 +1078,44 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       }
       __syncthreads();
 #pragma unroll 1
-      for (int shift = 44; shift >= 0; shift = shift >= 8 ? shift - 8 : (shift > 0 ? 0 : -1)) {
+      for (int shift = 40; shift >= 0; shift = shift >= 12 ? shift - 12 : (shift > 0 ? 0 : -1)) {
         if (sm->done || sm->need == 0) break;
-        const int width = shift >= 4 ? 8 : 4;
-        const unsigned long long dmask = ((1ull << width) - 1) << shift;
-        for (int x = threadIdx.x; x < 256; x += blockDim.x) sm->dh[x] = 0;
+        const int width = shift >= 4 ? 12 : 4;
+        const int nd = 1 << width;
+        const unsigned long long dmask = static_cast<unsigned long long>(nd - 1) << shift;
+#pragma unroll 1
+        for (int x = threadIdx.x; x < nd; x += blockDim.x) dh[x] = 0;
         __syncthreads();
         const unsigned long long pm = sm->mask, pp = sm->prefix;
 #pragma unroll 1
         for (uint32_t x = threadIdx.x; x < nkt; x += blockDim.x) {
           const unsigned long long key = key_at(x);
-          if ((key & pm) == pp) atomicAdd(&sm->dh[(key & dmask) >> shift], 1u);
+          if ((key & pm) == pp) atomicAdd(&dh[(key & dmask) >> shift], 1u);
         }
         __syncthreads();
-        if (threadIdx.x < 32) {
-          // lane l owns digits (from the top) nd-1-8l .. nd-8-8l; find the digit holding the need-th key
-          const int nd = 1 << width;
-          uint32_t sum = 0;
+        // thread t owns digits nd-1-per*t .. (from the top); the one whose run holds
+        // the need-th key walks it
+        const int per = (nd + kScoreThreads - 1) / kScoreThreads;
+        const int d0 = nd - 1 - per * static_cast<int>(threadIdx.x);
+        uint32_t sum = 0;
 #pragma unroll 1
-          for (int x = 0; x < 8; ++x) {
-            const int dg = nd - 1 - 8 * lane - x;
-            if (dg >= 0) sum += sm->dh[dg];
-          }
-          uint32_t incl = sum;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-            if (lane >= o) incl += v;
-          }
-          const uint32_t need = sm->need;
-          const unsigned hit = __ballot_sync(0xFFFFFFFFu, incl >= need);
-          const int Ln = hit ? __ffs(hit) - 1 : 31;
-          if (lane == Ln) {
-            uint32_t accd = incl - sum;
-            int d = 0;
+        for (int q = 0; q < per && d0 - q >= 0; ++q) sum += dh[d0 - q];
+        uint32_t tot;
+        const uint32_t before = place(sum, tot);
+        const uint32_t need = sm->need;
+        if (sum > 0 && before < need && before + sum >= need) {
+          uint32_t accd = before;
+          int d = d0;
 #pragma unroll 1
-            for (int x = 0; x < 8; ++x) {
-              const int dg = nd - 1 - 8 * lane - x;
-              if (dg < 0) break;
-              const uint32_t y = sm->dh[dg];
-              if (accd + y >= need || dg == 0) { d = dg; break; }
-              accd += y;
-            }
-            sm->need = need - accd;
-            sm->prefix = pp | (static_cast<unsigned long long>(d) << shift);
-            sm->mask = pm | dmask;
-            if (sm->dh[d] == need - accd) sm->done = 1;
+          for (int q = 0; q < per && d0 - q >= 0; ++q) {
+            const uint32_t y = dh[d0 - q];
+            if (accd + y >= need) { d = d0 - q; break; }
+            accd += y;
           }
+          sm->need = need - accd;
+          sm->prefix = pp | (static_cast<unsigned long long>(d) << shift);
+          sm->mask = pm | dmask;
+          if (dh[d] == need - accd) sm->done = 1;
         }
         __syncthreads();
         if (shift == 0) break;
