@@ -147,6 +147,22 @@ def build_caches(wl, torch, cskv):
     return keys, main, swa
 
 
+def max_over_ranks(values, world, device="cpu"):
+    """Per-rank timings -> their maxima over the ranks (every rank gets them); the job's
+    time is the slowest replica's."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_throughput(world, per_rank_batch, ms):
+    """Whole-job queries/s: every replica processes its batch in the (slowest) step time."""
+    return world * per_rank_batch / (ms * 1e-3)
+
+
 def run_gpu(args, rank, world):
     import torch
     import compressed_sparse_attention_kv_gb300 as cskv
@@ -291,13 +307,7 @@ def run_gpu(args, rank, world):
         if i >= args.warmup:
             e2e_ms.append(e0.elapsed_time(e1))
 
-    mean_ms = statistics.mean(step_ms)
-    if world > 1:
-        t = torch.tensor([mean_ms, statistics.mean(e2e_ms)], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        mean_ms, e2e_mean = float(t[0]), float(t[1])
-    else:
-        e2e_mean = statistics.mean(e2e_ms)
+    mean_ms, e2e_mean = max_over_ranks([statistics.mean(step_ms), statistics.mean(e2e_ms)], world, dev)
 
     # ---- roofline of the dominant kernel (the indexer score pass): bytes it must read
     algo_bytes = 132 * int(wl.n_entries.sum())
@@ -315,7 +325,7 @@ def run_gpu(args, rank, world):
 
     res = {
         "metric": METRIC,
-        "value": world * B / (mean_ms * 1e-3),
+        "value": job_throughput(world, B, mean_ms),
         "unit": "queries/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -338,7 +348,7 @@ def run_gpu(args, rank, world):
                      "traffic": traffic},
         "kv_read_gbs": path_bytes / (mean_ms * 1e-3) / 1e9,
         "step_frac_of_hbm_roofline": (path_bytes / (peak * 1e9)) / (mean_ms * 1e-3),
-        "e2e": {"value": world * B / (e2e_mean * 1e-3), "unit": "queries/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_throughput(world, B, e2e_mean), "unit": "queries/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,

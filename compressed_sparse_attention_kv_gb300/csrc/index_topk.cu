@@ -62,6 +62,8 @@ constexpr int kChunkTiles = 4;       // tiles per grab from a request's work cou
 constexpr int kWarpMma = kProducers;
 constexpr int kWarpEpi = kProducers + 1;
 constexpr int kScoreThreads = 32 * (kProducers + 1 + 4 * kGroups);   // 352
+// three groups (15 warps) put four warps on a scheduler partition: 128 registers each
+constexpr int kLaunchBound = kGroups >= 3 ? 512 : kScoreThreads;
 constexpr int kCandCap = 4096;       // per-block staging of threshold-bin candidates
 constexpr int kQImageFp8 = 8192;     // e4m3 [64 rows][128 B]
 constexpr int kQImageBf16 = 16384;   // bf16 [2 chunks][64 rows][128 B]
@@ -430,7 +432,7 @@ __device__ uint32_t ordered_list(ScoreSmem* sm, int n, Pred pred, uint16_t* list
 }
 
 template <int FP8>
-__global__ void __launch_bounds__(kScoreThreads, 1)
+__global__ void __launch_bounds__(kLaunchBound, 1)
     index_score_kernel(const __grid_constant__ CUtensorMap tmap, const IndexArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned carve-up
@@ -772,18 +774,19 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm->accempty[c]);   // this warp's TMEM reads are done
-      float s0 = 0.f, s1 = 0.f;
+      // four independent accumulation chains (the epilogue's latency sets the pace)
+      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
       for (int h = 0; h < 64; h += 4) {
         if (h < N) {
           const float4 w4 = *reinterpret_cast<const float4*>(&wq_s[h]);
           s0 = fmaf(w4.x, fmaxf(P[h], 0.f), s0);
           s1 = fmaf(w4.y, fmaxf(P[h + 1], 0.f), s1);
-          s0 = fmaf(w4.z, fmaxf(P[h + 2], 0.f), s0);
-          s1 = fmaf(w4.w, fmaxf(P[h + 3], 0.f), s1);
+          s2 = fmaf(w4.z, fmaxf(P[h + 2], 0.f), s2);
+          s3 = fmaf(w4.w, fmaxf(P[h + 3], 0.f), s3);
         }
       }
-      const float I = (s0 + s1) * ks;   // the key's scale is a positive power of two
+      const float I = ((s0 + s1) + (s2 + s3)) * ks;   // the key's scale is a positive power of two
       const uint32_t key = valid ? order_key(I) : 0u;
       if (valid) {
         scores_all[size_t(cur_b) * a.L.n_pad + j] = I;

@@ -1,0 +1,65 @@
+"""The bench's multi-rank host logic on CPU (gloo, two processes): max over ranks of
+the per-rank step times, whole-job throughput, and the reference arm's rank > 0 exit."""
+
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    # rank r measured step r+1 ms and e2e 10(r+1) ms
+    got = bench.max_over_ranks([1.0 + rank, 10.0 * (1 + rank)], world)
+    q.put((rank, got, bench.job_throughput(world, 8, got[0])))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_job_throughput_gloo():
+    world = 2
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    res = [q.get(timeout=120) for _ in range(world)]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, got, thr in res:
+        assert got == [2.0, 20.0]                  # every rank sees the slowest replica
+        assert thr == pytest.approx(2 * 8 / 2e-3)  # 16 queries per 2 ms
+
+
+def test_single_rank_is_identity():
+    import bench
+    assert bench.max_over_ranks([3.5, 7.0], 1) == [3.5, 7.0]
+    assert bench.job_throughput(1, 8, 0.5) == pytest.approx(16000.0)
+
+
+def test_reference_arm_other_ranks_exit_without_work():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "3"], env=env, capture_output=True, text=True,
+                       timeout=120)
+    assert r.returncode == 0
+    assert r.stdout.strip() == ""
