@@ -217,9 +217,11 @@ def run_gpu(args, rank, world):
                           prev_gate=d["pgate"], norm_w=nw, rope_cs=d["ecs"])
         cskv.compress(d["ikv"], d["igate"], iape, r, True, keys, req, d["first"], prev_kv=d["ipkv"],
                       prev_gate=d["ipgate"], norm_w=inw, rope_cs=d["ecs"])
+        # joined before the indexer, so that the attention's only predecessor is the
+        # indexer (it starts as the indexer's blocks retire)
+        cur.wait_stream(side)
         cskv.index_topk(d["q_idx"], d["w"], keys, d["ctx"], r, k, L, topk_idx=topk, workspace=ws_i,
                         want_scores=False)
-        cur.wait_stream(side)
         cskv.sparse_decode_attn(d["q"], main, swa, cskv.FMT_FP8, d["ctx"], topk, k, r, L, sink,
                                 cskv.DEFAULT_SCALE, d["qcs"], out=out, workspace=ws_a)
 

@@ -210,6 +210,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
       else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
     }
   }
+  grid_dep_launch();   // the combine kernel may be scheduled; it waits for this grid
+  // The selected entries come from the indexer, which may still be finishing (this
+  // kernel is a programmatic dependent of it): compressed tiles wait here, the
+  // window tile does not need it.
+  if (tile > 0) grid_dep_wait();
   // ---- rows of this tile: one thread per row resolves its address (the list entry,
   // then the block table), all rows in parallel
   for (int r = threadIdx.x; r < kKeys; r += blockDim.x) {
@@ -441,6 +446,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
 
 // merge the tiles of (request, head) in tile order, sink, inverse RoPE, bf16
 __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
+  grid_dep_wait();   // the tile kernel's partials
   const int b = blockIdx.x, h = blockIdx.y;
   const int ctx = query_len(a, b);
   const int ncomp = comp_keys(a, ctx);
@@ -534,11 +540,23 @@ cudaError_t launch_sparse_decode_attn(const void* q, const cskv_paged& kv, const
   const size_t smem = attn_smem_bytes();
   cudaFuncSetAttribute(attn_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   dim3 grid(L.max_tiles, B, (H + kMaxHeadsPerBlock - 1) / kMaxHeadsPerBlock);
-  attn_tile_kernel<<<grid, kAttnThreads, smem, stream>>>(a);
-  cudaError_t e = cudaGetLastError();
+  // both kernels are programmatic dependents of the work before them in the stream
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kAttnThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_tile_kernel, a);
   if (e != cudaSuccess) return e;
-  attn_combine_kernel<<<dim3(B, H), 256, 0, stream>>>(a);
-  return cudaGetLastError();
+  cfg.gridDim = dim3(B, H);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  return cudaLaunchKernelEx(&cfg, attn_combine_kernel, a);
 }
 
 unsigned int take_err_attention() { return take_dev_err(); }

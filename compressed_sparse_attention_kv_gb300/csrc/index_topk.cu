@@ -824,6 +824,7 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
   // This code runs once per launch; its loops stay rolled.
   grid_barrier(sm, gbar, gridDim.x, a.spin);
   const bool aborted = sm->abort;   // uniform: only thread 0 sets it, before the barrier's sync
+  grid_dep_launch();   // the next kernel (attention) may be scheduled as blocks retire
   {
     float* s_cache = reinterpret_cast<float*>(stages);                       // the stage ring, 32 fp32 per hit
     uint16_t* s_list = reinterpret_cast<uint16_t*>(qbuf);                     // kSelSegs
