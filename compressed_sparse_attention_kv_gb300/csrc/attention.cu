@@ -159,6 +159,56 @@ struct AttnSmem {
   __align__(16) uint8_t scl[kKeys][32];   // staged scale bytes of each row (FP8: 16, FP4: 32)
 };
 
+// In-place dequantisation of the staged FP8 / FP4 rows into the bf16 K tile.  Item
+// (r, l) = dims 16l .. 16l+15 of row r; each thread takes 8 items of dims 0-255 (their
+// outputs in the lower half, their codes in the upper half), then reads the codes of
+// its 8 items of dims 256-511 before any thread overwrites the upper half.
+template <int FMT>
+__device__ __forceinline__ void dequant_tile(uint8_t* ktile, const uint8_t* stage, const AttnSmem* sm) {
+  constexpr bool kFp8 = FMT == CSKV_FMT_FP8_E4M3_E8M0_B32;
+  auto raw_of = [&](int r, int l) -> RowBytes {
+    RowBytes rb;
+    rb.hi = make_uint4(0u, 0u, 0u, 0u);
+    if (kFp8) {
+      rb.lo = *reinterpret_cast<const uint4*>(stage + r * kD + 16 * l);
+      rb.scb = sm->scl[r][l >> 1];
+    } else {
+      const uint2 c = *reinterpret_cast<const uint2*>(stage + r * (kD / 2) + 8 * l);
+      rb.lo = make_uint4(c.x, c.y, 0u, 0u);
+      rb.scb = sm->scl[r][l];
+    }
+    return rb;
+  };
+  auto emit = [&](int r, int l, const RowBytes& rb) {
+    float v[16];
+    if (sm->rowp[r] != nullptr) {
+      convert16(FMT, rb, v);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = 0.f;
+    }
+    put16(ktile, r, l, v);
+  };
+  constexpr int kPer = kKeys * 16 / kAttnThreads;   // 8
+#pragma unroll 1
+  for (int u = 0; u < kPer; ++u) {
+    const int x = threadIdx.x + u * kAttnThreads;
+    emit(x >> 4, x & 15, raw_of(x >> 4, x & 15));
+  }
+  RowBytes rb[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int x = threadIdx.x + u * kAttnThreads;
+    rb[u] = raw_of(x >> 4, 16 + (x & 15));
+  }
+  __syncthreads();
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int x = threadIdx.x + u * kAttnThreads;
+    emit(x >> 4, 16 + (x & 15), rb[u]);
+  }
+}
+
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -283,56 +333,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
       *pq = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
-  // ---- dequantise FP8 / FP4 rows in place: item (r, l) = dims 16l .. 16l+15 of row r
-  if (!bf16_rows) {
-    const bool fp8 = row_fmt == CSKV_FMT_FP8_E4M3_E8M0_B32;
-    auto raw_of = [&](int r, int l) -> RowBytes {
-      RowBytes rb;
-      rb.hi = make_uint4(0u, 0u, 0u, 0u);
-      if (fp8) {
-        rb.lo = *reinterpret_cast<const uint4*>(stage + r * kD + 16 * l);
-        rb.scb = sm->scl[r][l >> 1];
-      } else {
-        const uint2 c = *reinterpret_cast<const uint2*>(stage + r * (kD / 2) + 8 * l);
-        rb.lo = make_uint4(c.x, c.y, 0u, 0u);
-        rb.scb = sm->scl[r][l];
-      }
-      return rb;
-    };
-    auto emit = [&](int r, int l, const RowBytes& rb) {
-      float v[16];
-      if (sm->rowp[r] != nullptr) {
-        convert16(row_fmt, rb, v);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = 0.f;
-      }
-      put16(ktile, r, l, v);
-    };
-    // dims 0-255 (l < 16): outputs in the lower half, codes in the upper half
-#pragma unroll 1
-    for (int x = threadIdx.x; x < kKeys * 16; x += blockDim.x) {
-      const int r = x >> 4, l = x & 15;
-      emit(r, l, raw_of(r, l));
-    }
-    // dims 256-511: every thread reads its items' codes before any is overwritten
-    constexpr int kPer = kKeys * 16 / kAttnThreads;   // 8
-    RowBytes rb[kPer];
-#pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-      const int x = threadIdx.x + u * kAttnThreads;
-      rb[u] = raw_of(x >> 4, 16 + (x & 15));
-    }
-    __syncthreads();
-#pragma unroll 1
-    for (int u = 0; u < kPer; ++u) {
-      const int x = threadIdx.x + u * kAttnThreads;
-      RowBytes cur = rb[0];
-#pragma unroll
-      for (int q = 1; q < kPer; ++q) if (q == u) cur = rb[q];
-      emit(x >> 4, 16 + (x & 15), cur);
-    }
-  }
+  // ---- dequantise FP8 / FP4 rows in place
+  if (row_fmt == CSKV_FMT_FP8_E4M3_E8M0_B32) dequant_tile<CSKV_FMT_FP8_E4M3_E8M0_B32>(ktile, stage, sm);
+  else if (row_fmt == CSKV_FMT_FP4_E2M1_E4M3_B16) dequant_tile<CSKV_FMT_FP4_E2M1_E4M3_B16>(ktile, stage, sm);
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
@@ -354,17 +357,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
   mbar_wait(&sm->bar_s, 0, kDefaultSpinLimit);
   tc_fence_after();
 
-  // ---- logits to smem, transposed [head][key]
-  if (warp < 4) {
-    const int r = warp * 32 + lane;
+  // ---- logits to smem, transposed [head][key]: warps w and w+4 share TMEM lane
+  // quarter w, each taking half of the head columns, all loads before one wait
+  {
+    const int r = (warp & 3) * 32 + lane;
     const bool ok = sm->rowp[r] != nullptr;
-    for (int c0 = 0; c0 < Nq; c0 += 16) {
-      float s[16];
-      tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0, s);
-      tmem_wait_ld();
+    const int half = Nq >> 1;   // a multiple of 8
+    const int cbase = (warp >> 2) * half;
+    float sv[32];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) zt[(c0 + i) * kZStride + r] = ok ? s[i] * a.scale_log2 : -INFINITY;
-    }
+    for (int c0 = 0; c0 < 32; c0 += 8)
+      if (c0 < half)
+        tmem_ld8(tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + cbase + c0,
+                 *reinterpret_cast<float(*)[8]>(sv + c0));
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < half) zt[(cbase + i) * kZStride + r] = ok ? sv[i] * a.scale_log2 : -INFINITY;
   }
   __syncthreads();
 
@@ -421,14 +430,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
     const int sub = warp & 3;
     for (int mb = (warp >> 2) * 2; mb < (warp >> 2) * 2 + 2; ++mb) {
       const int d = mb * 128 + sub * 32 + lane;
-      for (int c0 = 0; c0 < Nq; c0 += 16) {
-        float o[16];
-        tmem_ld16(tmem + (static_cast<uint32_t>(sub * 32) << 16) + 128 + mb * Nq + c0, o);
-        tmem_wait_ld();
+      // all of the block's head columns, one wait
+      float o[64];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          if (c0 + i < Hb) a.opart[(slot + c0 + i) * kD + d] = o[i];
-        }
+      for (int c0 = 0; c0 < 64; c0 += 16)
+        if (c0 < Nq)
+          tmem_ld16(tmem + (static_cast<uint32_t>(sub * 32) << 16) + 128 + mb * Nq + c0,
+                    *reinterpret_cast<float(*)[16]>(o + c0));
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        if (i < Hb) a.opart[(slot + i) * kD + d] = o[i];
       }
     }
     if (threadIdx.x < Hb) {
