@@ -205,27 +205,20 @@ def run_gpu(args, rank, world):
     out_host = torch.empty_like(out, device="cpu").pin_memory()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
-    side = torch.cuda.Stream()
-
     def step():
-        # the main-cache entry is needed only by the attention: it is compressed on a
-        # second stream, alongside the index-key entry and the indexer
-        cur = torch.cuda.current_stream()
-        side.wait_stream(cur)
-        with torch.cuda.stream(side):
-            cskv.compress(d["kv"], d["gate"], ape, r, True, main, req, d["first"], prev_kv=d["pkv"],
-                          prev_gate=d["pgate"], norm_w=nw, rope_cs=d["ecs"])
-        cskv.compress(d["ikv"], d["igate"], iape, r, True, keys, req, d["first"], prev_kv=d["ipkv"],
-                      prev_gate=d["ipgate"], norm_w=inw, rope_cs=d["ecs"])
-        # joined before the indexer, so that the attention's only predecessor is the
-        # indexer (it starts as the indexer's blocks retire)
-        cur.wait_stream(side)
+        # the completed block's entry of both caches (main, index keys), one launch
+        cskv.compress_many([
+            dict(kv=d["kv"], gate=d["gate"], ape=ape, ratio=r, overlap=True, out=main, req=req,
+                 first_entry=d["first"], prev_kv=d["pkv"], prev_gate=d["pgate"], norm_w=nw, rope_cs=d["ecs"]),
+            dict(kv=d["ikv"], gate=d["igate"], ape=iape, ratio=r, overlap=True, out=keys, req=req,
+                 first_entry=d["first"], prev_kv=d["ipkv"], prev_gate=d["ipgate"], norm_w=inw,
+                 rope_cs=d["ecs"])])
         cskv.index_topk(d["q_idx"], d["w"], keys, d["ctx"], r, k, L, topk_idx=topk, workspace=ws_i,
                         want_scores=False)
         cskv.sparse_decode_attn(d["q"], main, swa, cskv.FMT_FP8, d["ctx"], topk, k, r, L, sink,
                                 cskv.DEFAULT_SCALE, d["qcs"], out=out, workspace=ws_a)
 
-    launches_per_step = 2 + 2 + 2   # compressor x2, indexer prep + fused score/select, attention tiles + combine
+    launches_per_step = 1 + 2 + 2   # compressor (both caches), indexer prep + score/select, attention tiles + combine
     for _ in range(max(1, args.warmup)):
         step()
     torch.cuda.synchronize()

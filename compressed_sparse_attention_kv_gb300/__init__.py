@@ -159,6 +159,29 @@ def compress(kv, gate, ape, ratio, overlap, out, req, first_entry, prev_kv=None,
     _check(st, "cskv_compress")
 
 
+def compress_many(jobs, stream=None):
+    """Several compressor jobs in one launch.  Each job is a dict of compress()'s
+    arguments (kv, gate, ape, ratio, overlap, out, req, first_entry and, optionally,
+    prev_kv, prev_gate, norm_w, eps, rope_cs); same results as separate calls."""
+    import torch
+    arr = (_lib.CompressJob * len(jobs))()
+    for i, j in enumerate(jobs):
+        kv, gate = j["kv"], j["gate"]
+        for t, n in ((kv, "kv"), (gate, "gate"), (j.get("prev_kv"), "prev_kv"), (j.get("prev_gate"), "prev_gate")):
+            _need(t, torch.bfloat16, n)
+        for t, n in ((j["ape"], "ape"), (j.get("norm_w"), "norm_w"), (j.get("rope_cs"), "rope_cs")):
+            _need(t, torch.float32, n)
+        _need(j["req"], torch.int32, "req")
+        _need(j["first_entry"], torch.int32, "first_entry")
+        S, T, coff, dim = kv.shape
+        arr[i] = _lib.CompressJob(kv.data_ptr(), gate.data_ptr(), _ptr(j.get("prev_kv")), _ptr(j.get("prev_gate")),
+                                  j["ape"].data_ptr(), _ptr(j.get("norm_w")), float(j.get("eps", 1e-6)),
+                                  _ptr(j.get("rope_cs")), S, T, int(j["ratio"]), int(bool(j["overlap"])), dim,
+                                  j["req"].data_ptr(), j["first_entry"].data_ptr(), j["out"].desc())
+    st = _lib.lib().cskv_compress_many(arr, len(jobs), _stream(stream))
+    _check(st, "cskv_compress_many")
+
+
 def index_topk_workspace_size(B, max_ctx_len, ratio, Hi, k):
     return int(_lib.lib().cskv_index_topk_workspace_size(B, max_ctx_len, ratio, Hi, k))
 

@@ -26,6 +26,28 @@ class Paged(ctypes.Structure):
     ]
 
 
+class CompressJob(ctypes.Structure):
+    """struct cskv_compress_job (the arguments of one cskv_compress call)."""
+    _fields_ = [
+        ("kv", c_void_p),
+        ("gate", c_void_p),
+        ("prev_kv", c_void_p),
+        ("prev_gate", c_void_p),
+        ("ape", c_void_p),
+        ("norm_w", c_void_p),
+        ("eps", c_float),
+        ("rope_cs", c_void_p),
+        ("S", c_int32),
+        ("T", c_int32),
+        ("ratio", c_int32),
+        ("overlap", c_int32),
+        ("dim", c_int32),
+        ("req", c_void_p),
+        ("first_entry", c_void_p),
+        ("out", Paged),
+    ]
+
+
 # name -> (restype, argtypes); every symbol include/cskv.h declares
 SIGNATURES = {
     "cskv_row_bytes": (c_size_t, [c_int32, c_int32]),
@@ -39,6 +61,7 @@ SIGNATURES = {
     "cskv_compress": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_float,
                                 c_void_p, c_int32, c_int32, c_int32, c_int32, c_int32, c_void_p,
                                 c_void_p, Paged, c_void_p]),
+    "cskv_compress_many": (c_int32, [ctypes.POINTER(CompressJob), c_int32, c_void_p]),
     "cskv_index_topk_workspace_size": (c_size_t, [c_int32, c_int32, c_int32, c_int32, c_int32]),
     "cskv_index_topk": (c_int32, [c_void_p, c_void_p, Paged, c_void_p, c_int32, c_int32, c_int32,
                                   c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),

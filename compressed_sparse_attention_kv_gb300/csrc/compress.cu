@@ -89,12 +89,13 @@ __device__ __forceinline__ float block_sum_pairwise(float v, int lt) {
 constexpr int kBatch = 8;   // slots staged per batch
 constexpr size_t kCompressSmem = 2 * kBatch * 128 * (8 + 8 + 16);   // two batches of kv, gate, bias
 
+// The entries of block `blk` of one compressor job (a whole 128-thread block).
 template <int D>
-__global__ void __launch_bounds__(128) compress_kernel(const CompressArgs a) {
+__device__ __forceinline__ void compress_block(const CompressArgs& a, long long blk) {
   constexpr int TPE = D / 4;        // threads per entry
   constexpr int EPB = 128 / TPE;    // entries per block
   const int lt = threadIdx.x % TPE;
-  const long long gentry = static_cast<long long>(blockIdx.x) * EPB + threadIdx.x / TPE;
+  const long long gentry = blk * EPB + threadIdx.x / TPE;
   const long long total = static_cast<long long>(a.S) * a.n;
   const bool live = gentry < total;
   // D == 512: one entry per block, the whole block stays for the block-wide sum.
@@ -254,6 +255,36 @@ __global__ void __launch_bounds__(128) compress_kernel(const CompressArgs a) {
   store_row_values(y, lt, a.out.fmt, D, dst, live && dst.data != nullptr);
 }
 
+// Blocks of one entry (D = 512) or four entries (D = 128).
+inline long long compress_blocks(int S, int n, int dim) {
+  const long long total = static_cast<long long>(S) * n;
+  return dim == 512 ? total : (total + 3) / 4;
+}
+
+template <int D>
+__global__ void __launch_bounds__(128) compress_kernel(const CompressArgs a) {
+  grid_dep_launch();   // a programmatic dependent (the indexer's query prep) may start
+  compress_block<D>(a, blockIdx.x);
+}
+
+// Several jobs in one launch: block b belongs to the job j with first[j] <= b < first[j + 1].
+constexpr int kMaxCompressJobs = 4;
+struct CompressMany {
+  CompressArgs job[kMaxCompressJobs];
+  int dim[kMaxCompressJobs];
+  long long first[kMaxCompressJobs + 1];
+  int njobs;
+};
+
+__global__ void __launch_bounds__(128) compress_many_kernel(const __grid_constant__ CompressMany m) {
+  grid_dep_launch();
+  int j = 0;
+  while (j + 1 < m.njobs && static_cast<long long>(blockIdx.x) >= m.first[j + 1]) ++j;
+  const long long blk = blockIdx.x - m.first[j];
+  if (m.dim[j] == 512) compress_block<512>(m.job[j], blk);
+  else compress_block<128>(m.job[j], blk);
+}
+
 struct EncodeArgs {
   const uint8_t* src;
   int src_bf16;
@@ -286,11 +317,11 @@ __global__ void __launch_bounds__(128) encode_rows_kernel(const EncodeArgs a) {
 // ---------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------
-cudaError_t launch_compress(const void* kv, const void* gate, const void* prev_kv,
-                            const void* prev_gate, const float* ape, const float* norm_w, float eps,
-                            const float* rope_cs, int S, int T, int ratio, int overlap, int dim,
-                            const int32_t* req, const int32_t* first_entry, const cskv_paged& out,
-                            int out_row_bytes, cudaStream_t stream) {
+static CompressArgs compress_args(const void* kv, const void* gate, const void* prev_kv,
+                                  const void* prev_gate, const float* ape, const float* norm_w, float eps,
+                                  const float* rope_cs, int S, int T, int ratio, int overlap,
+                                  const int32_t* req, const int32_t* first_entry, const cskv_paged& out,
+                                  int out_row_bytes) {
   CompressArgs a;
   a.kv = static_cast<const uint8_t*>(kv);
   a.gate = static_cast<const uint8_t*>(gate);
@@ -309,6 +340,16 @@ cudaError_t launch_compress(const void* kv, const void* gate, const void* prev_k
   a.n = T / ratio;
   a.out = out;
   a.out_row_bytes = out_row_bytes;
+  return a;
+}
+
+cudaError_t launch_compress(const void* kv, const void* gate, const void* prev_kv,
+                            const void* prev_gate, const float* ape, const float* norm_w, float eps,
+                            const float* rope_cs, int S, int T, int ratio, int overlap, int dim,
+                            const int32_t* req, const int32_t* first_entry, const cskv_paged& out,
+                            int out_row_bytes, cudaStream_t stream) {
+  const CompressArgs a = compress_args(kv, gate, prev_kv, prev_gate, ape, norm_w, eps, rope_cs, S, T, ratio,
+                                       overlap, req, first_entry, out, out_row_bytes);
   const long long total = static_cast<long long>(S) * a.n;
   if (total == 0) return cudaSuccess;
   if (dim == 512) {
@@ -320,6 +361,26 @@ cudaError_t launch_compress(const void* kv, const void* gate, const void* prev_k
                          static_cast<int>(kCompressSmem));
     compress_kernel<128><<<static_cast<unsigned>((total + 3) / 4), 128, kCompressSmem, stream>>>(a);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_compress_many(const cskv_compress_job* jobs, int njobs, cudaStream_t stream) {
+  if (njobs < 1 || njobs > kMaxCompressJobs) return cudaErrorInvalidValue;
+  CompressMany m;
+  m.njobs = njobs;
+  m.first[0] = 0;
+  for (int j = 0; j < njobs; ++j) {
+    const cskv_compress_job& q = jobs[j];
+    m.job[j] = compress_args(q.kv, q.gate, q.prev_kv, q.prev_gate, q.ape, q.norm_w, q.eps, q.rope_cs, q.S, q.T,
+                             q.ratio, q.overlap, q.req, q.first_entry, q.out,
+                             static_cast<int>(cskv_row_bytes(q.out.fmt, q.dim)));
+    m.dim[j] = q.dim;
+    m.first[j + 1] = m.first[j] + compress_blocks(q.S, q.T / q.ratio, q.dim);
+  }
+  if (m.first[njobs] == 0) return cudaSuccess;
+  cudaFuncSetAttribute(compress_many_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       static_cast<int>(kCompressSmem));
+  compress_many_kernel<<<static_cast<unsigned>(m.first[njobs]), 128, kCompressSmem, stream>>>(m);
   return cudaGetLastError();
 }
 

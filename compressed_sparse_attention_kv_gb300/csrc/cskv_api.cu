@@ -104,11 +104,10 @@ int32_t cskv_encode_rows(const void* src, int32_t src_is_bf16, int32_t n, int32_
                                         static_cast<cudaStream_t>(stream)));
 }
 
-int32_t cskv_compress(const void* kv, const void* gate, const void* prev_kv, const void* prev_gate,
-                      const float* ape, const float* norm_w, float eps, const float* rope_cs,
-                      int32_t S, int32_t T, int32_t ratio, int32_t overlap, int32_t dim,
-                      const int32_t* req, const int32_t* first_entry, cskv_paged out,
-                      void* stream) {
+static int32_t compress_check(const void* kv, const void* gate, const void* prev_kv, const void* prev_gate,
+                              const float* ape, const float* norm_w, float eps, const float* rope_cs,
+                              int32_t S, int32_t T, int32_t ratio, int32_t overlap, int32_t dim,
+                              const int32_t* req, const int32_t* first_entry, cskv_paged out) {
   if (kv == nullptr || gate == nullptr || ape == nullptr || req == nullptr || first_entry == nullptr)
     return CSKV_ERR_INVALID;
   if (dim != 128 && dim != 512) return CSKV_ERR_INVALID;
@@ -122,10 +121,32 @@ int32_t cskv_compress(const void* kv, const void* gate, const void* prev_kv, con
   if ((norm_w && !aligned(norm_w, 16)) || (rope_cs && !aligned(rope_cs, 16))) return CSKV_ERR_INVALID;
   if (!paged_ok(out, dim, 0xFu)) return CSKV_ERR_INVALID;
   if (out.fmt == CSKV_FMT_FP8_E4M3_ROWSCALE_PAGESPLIT && dim != 128) return CSKV_ERR_INVALID;
+  return CSKV_OK;
+}
+
+int32_t cskv_compress(const void* kv, const void* gate, const void* prev_kv, const void* prev_gate,
+                      const float* ape, const float* norm_w, float eps, const float* rope_cs,
+                      int32_t S, int32_t T, int32_t ratio, int32_t overlap, int32_t dim,
+                      const int32_t* req, const int32_t* first_entry, cskv_paged out,
+                      void* stream) {
+  const int32_t st = compress_check(kv, gate, prev_kv, prev_gate, ape, norm_w, eps, rope_cs, S, T, ratio,
+                                    overlap, dim, req, first_entry, out);
+  if (st != CSKV_OK) return st;
   return cuda_status(launch_compress(kv, gate, prev_kv, prev_gate, ape, norm_w, eps, rope_cs, S, T,
                                      ratio, overlap, dim, req, first_entry, out,
                                      static_cast<int>(cskv_row_bytes(out.fmt, dim)),
                                      static_cast<cudaStream_t>(stream)));
+}
+
+int32_t cskv_compress_many(const cskv_compress_job* jobs, int32_t njobs, void* stream) {
+  if (jobs == nullptr || njobs < 1 || njobs > 4) return CSKV_ERR_INVALID;
+  for (int32_t j = 0; j < njobs; ++j) {
+    const cskv_compress_job& q = jobs[j];
+    const int32_t st = compress_check(q.kv, q.gate, q.prev_kv, q.prev_gate, q.ape, q.norm_w, q.eps, q.rope_cs,
+                                      q.S, q.T, q.ratio, q.overlap, q.dim, q.req, q.first_entry, q.out);
+    if (st != CSKV_OK) return st;
+  }
+  return cuda_status(launch_compress_many(jobs, njobs, static_cast<cudaStream_t>(stream)));
 }
 
 size_t cskv_index_topk_workspace_size(int32_t B, int32_t max_ctx_len, int32_t ratio, int32_t Hi,

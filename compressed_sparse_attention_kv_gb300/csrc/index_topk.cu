@@ -153,12 +153,6 @@ __global__ void __launch_bounds__(256) index_prep_kernel(const IndexArgs a) {
   float* wq = reinterpret_cast<float*>(a.ws + a.L.wq) + b * 64;
   uint32_t* hist = reinterpret_cast<uint32_t*>(a.ws + a.L.hist) + size_t(b) * kHistStride;
   uint32_t* ctr = reinterpret_cast<uint32_t*>(a.ws + a.L.ctr) + b * 4;
-  for (int i = threadIdx.x; i < kHistStride; i += blockDim.x) hist[i] = 0;
-  if (threadIdx.x < 4)
-    ctr[threadIdx.x] = threadIdx.x == 0 ? static_cast<uint32_t>(first_home_block(b + 1, a.B, a.grid) -
-                                                             first_home_block(b, a.B, a.grid)) * kChunkTiles
-                                        : 0u;
-  if (b == 0 && threadIdx.x == 0) *reinterpret_cast<uint32_t*>(a.ws + a.L.gbar) = 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // warp w owns heads w, w+8, ... (N <= 64); lane l holds dims 4l .. 4l+3.  All loads first.
   uint2 raw[8];
@@ -195,6 +189,18 @@ __global__ void __launch_bounds__(256) index_prep_kernel(const IndexArgs a) {
       if (lane == 0) wq[h] = wv[i];
     }
   }
+  // This kernel may run beside the kernel before it in the stream (it is launched as
+  // a programmatic dependent: that kernel writes the keys this indexer reads, not its
+  // queries).  The workspace words that an earlier indexer launch on the same
+  // workspace may still be using are cleared only after the wait, and finishing
+  // after the wait makes the next kernel see the previous one complete.
+  grid_dep_wait();
+  for (int i = threadIdx.x; i < kHistStride; i += blockDim.x) hist[i] = 0;
+  if (threadIdx.x < 4)
+    ctr[threadIdx.x] = threadIdx.x == 0 ? static_cast<uint32_t>(first_home_block(b + 1, a.B, a.grid) -
+                                                             first_home_block(b, a.B, a.grid)) * kChunkTiles
+                                        : 0u;
+  if (b == 0 && threadIdx.x == 0) *reinterpret_cast<uint32_t*>(a.ws + a.L.gbar) = 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -1275,7 +1281,20 @@ cudaError_t launch_index_topk(const void* q_idx, const float* w, const cskv_page
 
   a.grid = sm_count();   // the score kernel runs one block per SM
   if (a.grid > kMaxGrid) a.grid = kMaxGrid;
-  index_prep_kernel<<<B, 256, 0, stream>>>(a);
+  {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(B);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t pe = cudaLaunchKernelEx(&cfg, index_prep_kernel, a);
+    if (pe != cudaSuccess) return pe;
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 

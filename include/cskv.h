@@ -165,6 +165,32 @@ CSKV_API int32_t cskv_compress(const void* kv, const void* gate,
                       cskv_paged out, void* stream);
 
 /* ------------------------------------------------------------------------
+ * cskv_compress_many: several compressor jobs in one launch, e.g. the entry of
+ * the main cache and the entry of the index-key cache that a decode step's
+ * completed block produces ("DeepSeek-V4 deep dive", section 4.1 for the
+ * computation; one launch instead of two is a deployment choice, the pages
+ * have no counterpart).  Each job holds the arguments of one cskv_compress call,
+ * is checked the same way and gives the same bits; jobs must not write the same
+ * rows.  njobs in [1, 4].  Errors: CSKV_ERR_INVALID for a bad job (nothing is
+ * launched), else as cskv_compress.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  const void* kv;
+  const void* gate;
+  const void* prev_kv;
+  const void* prev_gate;
+  const float* ape;
+  const float* norm_w;
+  float eps;
+  const float* rope_cs;
+  int32_t S, T, ratio, overlap, dim;
+  const int32_t* req;
+  const int32_t* first_entry;
+  cskv_paged out;
+} cskv_compress_job;
+CSKV_API int32_t cskv_compress_many(const cskv_compress_job* jobs, int32_t njobs, void* stream);
+
+/* ------------------------------------------------------------------------
  * cskv_index_topk: the lightning indexer and top-k ("DeepSeek-V4 deep dive",
  * section 5.2 "What is different from V3.2's indexer"):
  *   I_{b,j} = sum_h w[b,h] * ReLU(q[b,h,:] . k_{b,j})   for j < n_b,

@@ -26,7 +26,7 @@ def _declared():
 def test_header_and_binding_agree():
     from compressed_sparse_attention_kv_gb300 import _lib
     names = _declared()
-    assert len(names) == 13
+    assert len(names) == 14
     assert sorted(_lib.SIGNATURES) == names
 
 
@@ -73,6 +73,12 @@ def test_invalid_arguments_launch_nothing(lib):
                              fake, fake, good, None) == 1                      # overlap needs ratio <= 8
     assert lib.cskv_compress(fake, fake, None, None, fake, None, -1.0, None, 1, 8, 4, 1, 512,
                              fake, fake, good, None) == 1                      # eps < 0
+    assert lib.cskv_compress_many(None, 1, None) == 1                          # no jobs
+    from compressed_sparse_attention_kv_gb300._lib import CompressJob
+    jobs = (CompressJob * 5)()
+    assert lib.cskv_compress_many(jobs, 5, None) == 1                          # more than 4 jobs
+    jobs[0] = CompressJob(4096, 4096, None, None, 4096, None, 1e-6, None, 1, 6, 4, 1, 512, 4096, 4096, good)
+    assert lib.cskv_compress_many(jobs, 1, None) == 1                          # T % ratio != 0
     keys = Paged(4096, 4096, 64 * 132, 4, 4, 3, 128)
     assert lib.cskv_index_topk(fake, fake, keys, fake, 1, 65, 4, 512, 4096, fake, None, fake, 1 << 30,
                                None) == 2                                       # > 64 heads

@@ -155,3 +155,31 @@ def test_compressor_full_chunk_bit_exact(ratio, fmt):
     got = dst.pool.cpu().numpy()[:, :64 * rb].reshape(-1, rb)[:n]
     bad = np.flatnonzero(np.any(got != rows, axis=1))
     assert bad.size == 0, "rows differ: %s" % bad[:10]
+
+
+def _job(c, ratio, overlap, dev, use_prev):
+    pk, pg = c["prev"]
+    return dict(kv=c["kv"][0].cuda(), gate=c["gate"][0].cuda(), ape=cuda(c["ape"]), ratio=ratio,
+                overlap=overlap, out=dev, req=cuda(c["req"]), first_entry=cuda(c["first"]),
+                prev_kv=pk[0].cuda() if use_prev and overlap else None,
+                prev_gate=pg[0].cuda() if use_prev and overlap else None,
+                norm_w=cuda(c["nw"]), eps=1e-6, rope_cs=cuda(c["cs"]))
+
+
+def test_compress_many_equals_separate_calls():
+    """Three jobs of different widths, ratios and formats in one launch write exactly the
+    bytes three separate compress calls write (the decode step compresses the main and
+    the index-key entry together)."""
+    specs = [(4, 1, 512, codecs.FMT_FP8, True, 96), (4, 1, 128, codecs.FMT_FP8_PAGESPLIT, False, 96),
+             (128, 0, 512, codecs.FMT_FP4, False, 5)]
+    cases = [_compress_case(r, o, d, f, entries=e, seed=10 + i) for i, (r, o, d, f, _, e) in enumerate(specs)]
+    sep = [c["cache"].to_device() for c in cases]
+    many = [c["cache"].to_device() for c in cases]
+    for c, dev, (r, o, d, f, up, e) in zip(cases, sep, specs):
+        j = _job(c, r, o, dev, up)
+        cskv.compress(j.pop("kv"), j.pop("gate"), j.pop("ape"), j.pop("ratio"), j.pop("overlap"), j.pop("out"),
+                      j.pop("req"), j.pop("first_entry"), **j)
+    cskv.compress_many([_job(c, r, o, dev, up) for c, dev, (r, o, d, f, up, e) in zip(cases, many, specs)])
+    assert cskv.device_status() == 0
+    for a, b in zip(sep, many):
+        assert torch.equal(a.pool, b.pool)
