@@ -143,7 +143,8 @@ def encode_rows(src, dst, req=None, row=None, stream=None):
 
 def compress(kv, gate, ape, ratio, overlap, out, req, first_entry, prev_kv=None, prev_gate=None,
              norm_w=None, eps=1e-6, rope_cs=None, stream=None):
-    """Gated per-channel pooling of S sequences of T tokens (kv, gate: bf16 [S, T, coff, dim])."""
+    """Gated per-channel pooling of S sequences of T tokens (kv, gate: bf16 [S, T, coff, dim]);
+    ape None = no slot bias (the V4.1 compressor)."""
     import torch
     for t, n in ((kv, "kv"), (gate, "gate"), (prev_kv, "prev_kv"), (prev_gate, "prev_gate")):
         _need(t, torch.bfloat16, n)
@@ -153,7 +154,7 @@ def compress(kv, gate, ape, ratio, overlap, out, req, first_entry, prev_kv=None,
     _need(first_entry, torch.int32, "first_entry")
     S, T, coff, dim = kv.shape
     st = _lib.lib().cskv_compress(kv.data_ptr(), gate.data_ptr(), _ptr(prev_kv), _ptr(prev_gate),
-                                  ape.data_ptr(), _ptr(norm_w), float(eps), _ptr(rope_cs),
+                                  _ptr(ape), _ptr(norm_w), float(eps), _ptr(rope_cs),
                                   S, T, int(ratio), int(bool(overlap)), dim, req.data_ptr(),
                                   first_entry.data_ptr(), out.desc(), _stream(stream))
     _check(st, "cskv_compress")
@@ -169,13 +170,13 @@ def compress_many(jobs, stream=None):
         kv, gate = j["kv"], j["gate"]
         for t, n in ((kv, "kv"), (gate, "gate"), (j.get("prev_kv"), "prev_kv"), (j.get("prev_gate"), "prev_gate")):
             _need(t, torch.bfloat16, n)
-        for t, n in ((j["ape"], "ape"), (j.get("norm_w"), "norm_w"), (j.get("rope_cs"), "rope_cs")):
+        for t, n in ((j.get("ape"), "ape"), (j.get("norm_w"), "norm_w"), (j.get("rope_cs"), "rope_cs")):
             _need(t, torch.float32, n)
         _need(j["req"], torch.int32, "req")
         _need(j["first_entry"], torch.int32, "first_entry")
         S, T, coff, dim = kv.shape
         arr[i] = _lib.CompressJob(kv.data_ptr(), gate.data_ptr(), _ptr(j.get("prev_kv")), _ptr(j.get("prev_gate")),
-                                  j["ape"].data_ptr(), _ptr(j.get("norm_w")), float(j.get("eps", 1e-6)),
+                                  _ptr(j.get("ape")), _ptr(j.get("norm_w")), float(j.get("eps", 1e-6)),
                                   _ptr(j.get("rope_cs")), S, T, int(j["ratio"]), int(bool(j["overlap"])), dim,
                                   j["req"].data_ptr(), j["first_entry"].data_ptr(), j["out"].desc())
     st = _lib.lib().cskv_compress_many(arr, len(jobs), _stream(stream))

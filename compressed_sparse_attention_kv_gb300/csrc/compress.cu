@@ -107,10 +107,10 @@ __device__ __forceinline__ void compress_block(const CompressArgs& a, long long 
   const int coff = a.overlap ? 2 : 1;
   const int slots = a.overlap ? 2 * r : r;
 
-  // slot j -> (value row, score row, bias row); nullptr value = the empty half
-  auto slot_src = [&](int j, const uint8_t*& vp, const uint8_t*& gp, const float*& ap) {
+  // slot j -> (value row, score row, bias offset in ape); nullptr value = the empty half
+  auto slot_src = [&](int j, const uint8_t*& vp, const uint8_t*& gp, long long& ao) {
     if (a.overlap && j < r) {
-      ap = a.ape + static_cast<long long>(j) * coff * D + c0;   // half 0 bias
+      ao = static_cast<long long>(j) * coff * D + c0;   // half 0 bias
       if (i > 0) {
         const long long tok = static_cast<long long>(i - 1) * r + j;
         vp = tok_ptr(a.kv, s, a.T, tok, coff, 0, D) + 2 * c0;
@@ -126,7 +126,7 @@ __device__ __forceinline__ void compress_block(const CompressArgs& a, long long 
       const int jj = a.overlap ? j - r : j;
       const int half = a.overlap ? 1 : 0;
       const long long tok = static_cast<long long>(i) * r + jj;
-      ap = a.ape + static_cast<long long>(jj) * coff * D + half * D + c0;
+      ao = static_cast<long long>(jj) * coff * D + half * D + c0;
       vp = tok_ptr(a.kv, s, a.T, tok, coff, half, D) + 2 * c0;
       gp = tok_ptr(a.gate, s, a.T, tok, coff, half, D) + 2 * c0;
     }
@@ -163,13 +163,13 @@ __device__ __forceinline__ void compress_block(const CompressArgs& a, long long 
       const int j = bt * kBatch + u;
       if (live && j < slots) {
         const uint8_t *vp, *gp;
-        const float* ap;
-        slot_src(j, vp, gp, ap);
+        long long ao;
+        slot_src(j, vp, gp, ao);
         if (vp != nullptr) {
           cp_async8(&s_kv[(buf * kBatch + u) * 128 + t], vp);
           cp_async8(&s_g[(buf * kBatch + u) * 128 + t], gp);
         }
-        cp_async16(&s_ap[(buf * kBatch + u) * 128 + t], ap);
+        if (a.ape != nullptr) cp_async16(&s_ap[(buf * kBatch + u) * 128 + t], a.ape + ao);
       }
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
@@ -178,15 +178,16 @@ __device__ __forceinline__ void compress_block(const CompressArgs& a, long long 
   auto slot_at = [&](int j, float4& sc, float4* v) {
     const int buf = (j / kBatch) & 1, u = j % kBatch;
     const uint8_t *vp, *gp;
-    const float* ap;
-    slot_src(j, vp, gp, ap);
+    long long ao;
+    slot_src(j, vp, gp, ao);
     if (vp == nullptr) {
       sc = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
       if (v) *v = make_float4(0.f, 0.f, 0.f, 0.f);
       return;
     }
     const uint2 g = s_g[(buf * kBatch + u) * 128 + t];
-    const float4 b = s_ap[(buf * kBatch + u) * 128 + t];
+    // no slot bias (ape == nullptr) adds +0: the same bits as a zero bias table
+    const float4 b = a.ape != nullptr ? s_ap[(buf * kBatch + u) * 128 + t] : make_float4(0.f, 0.f, 0.f, 0.f);
     sc = make_float4(__fadd_rn(bf16lo(g.x), b.x), __fadd_rn(bf16hi(g.x), b.y), __fadd_rn(bf16lo(g.y), b.z),
                      __fadd_rn(bf16hi(g.y), b.w));
     if (v) {

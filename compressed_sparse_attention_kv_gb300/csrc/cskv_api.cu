@@ -108,7 +108,7 @@ static int32_t compress_check(const void* kv, const void* gate, const void* prev
                               const float* ape, const float* norm_w, float eps, const float* rope_cs,
                               int32_t S, int32_t T, int32_t ratio, int32_t overlap, int32_t dim,
                               const int32_t* req, const int32_t* first_entry, cskv_paged out) {
-  if (kv == nullptr || gate == nullptr || ape == nullptr || req == nullptr || first_entry == nullptr)
+  if (kv == nullptr || gate == nullptr || req == nullptr || first_entry == nullptr)
     return CSKV_ERR_INVALID;
   if (dim != 128 && dim != 512) return CSKV_ERR_INVALID;
   if (S < 0 || T < 0 || ratio < 1 || ratio > 1024 || T % ratio != 0) return CSKV_ERR_INVALID;
@@ -116,7 +116,7 @@ static int32_t compress_check(const void* kv, const void* gate, const void* prev
   if (overlap && ratio > 8) return CSKV_ERR_INVALID;
   if ((prev_kv == nullptr) != (prev_gate == nullptr)) return CSKV_ERR_INVALID;
   if (!(eps >= 0.0f)) return CSKV_ERR_INVALID;
-  if (!aligned(kv, 8) || !aligned(gate, 8) || !aligned(ape, 16)) return CSKV_ERR_INVALID;
+  if (!aligned(kv, 8) || !aligned(gate, 8) || (ape && !aligned(ape, 16))) return CSKV_ERR_INVALID;
   if (prev_kv && (!aligned(prev_kv, 8) || !aligned(prev_gate, 8))) return CSKV_ERR_INVALID;
   if ((norm_w && !aligned(norm_w, 16)) || (rope_cs && !aligned(rope_cs, 16))) return CSKV_ERR_INVALID;
   if (!paged_ok(out, dim, 0xFu)) return CSKV_ERR_INVALID;

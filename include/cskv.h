@@ -153,7 +153,12 @@ CSKV_API int32_t cskv_encode_rows(const void* src, int32_t src_is_bf16, int32_t 
  * degree-7 Taylor polynomial); numerator and denominator summed in slot order;
  * division; RMSNorm with a pairwise (recursive halves) sum of squares,
  * 1/sqrt(ss/dim + eps); rotation y0*c - y1*s, y0*s + y1*c.
- * ape: [ratio, coff*dim] fp32.  req, first_entry: device int32 [S].
+ * ape: [ratio, coff*dim] fp32, or NULL for no slot bias (the same bits as a
+ * zero table): the V4.1 compressor of "DeepSeek-V4.1 Flash" (section 1.1,
+ * the sequence dimension) and the deep dive's implementation notes to section
+ * 4 drop both the overlap and the slot bias, and pool 2 adjacent positions
+ * (ratio 2) in the encoder or keep one entry per position (ratio 1) in the
+ * decoder.  req, first_entry: device int32 [S].
  * Alignment: kv, gate, prev_* 8 bytes; ape, norm_w, rope_cs 16 bytes.
  * ------------------------------------------------------------------------ */
 CSKV_API int32_t cskv_compress(const void* kv, const void* gate,

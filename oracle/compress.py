@@ -17,6 +17,9 @@ model choose the weights per channel", and §4.2 "Ratio 4 (CSA) overlaps; ratio
     entry's own 4 tokens through half 1.  The slot bias is added before this
     transform, so slots 0-3 carry ape[:, :D] and slots 4-7 ape[:, D:].  The
     first entry of a sequence has no previous block: value 0, score -inf.
+  * the V4.1 compressor ("DeepSeek-V4.1 Flash", section 1.1; the deep dive's
+    implementation notes to section 4) is the no-overlap case with ratio 2
+    (encoder) or 1 (decoder) and no slot bias, i.e. a zero B.
   * then RMSNorm over the D channels with a learned weight, and RoPE on the
     last 64 dims at the position of the first token of the entry's own block
     (i * r).

@@ -51,6 +51,46 @@ def test_equal_gates_give_mean_and_dominant_gate_gives_token():
     assert np.array_equal(out2[0], kv[37, 0])
 
 
+def test_v41_ratio1_entry_is_the_token():
+    """The V4.1 decoder compressor keeps one entry per position (m = 1, no overlap,
+    no slot bias): the softmax over a single slot is 1, so the pooled entry is the
+    token's projected value itself, in the definition and bit for bit in the contract."""
+    rs = np.random.default_rng(2)
+    kv = rs.standard_normal((40, 1, 32)).astype(np.float32)
+    gate = (3 * rs.standard_normal((40, 1, 32))).astype(np.float32)
+    ape = np.zeros((1, 32), np.float32)
+    assert np.array_equal(compress.compress_fp64(kv, gate, ape, ratio=1, overlap=False), kv[:, 0])
+    assert np.array_equal(compress.compress_contract(kv, gate, ape, ratio=1, overlap=False), kv[:, 0])
+
+
+def test_v41_ratio2_pairs_are_a_logistic_blend():
+    """The V4.1 encoder compressor merges 2 adjacent positions (m = 2, no overlap, no
+    slot bias): entry i = v_{2i} * sigma(g_{2i} - g_{2i+1}) + v_{2i+1} * sigma(g_{2i+1} - g_{2i})
+    per channel (a two-way softmax is a logistic function), and a dominant gate on one
+    token of the pair returns that token."""
+    rs = np.random.default_rng(3)
+    T, D = 64, 16
+    kv = rs.standard_normal((T, 1, D))
+    gate = 2 * rs.standard_normal((T, 1, D))
+    ape = np.zeros((2, D))
+    out = compress.compress_fp64(kv, gate, ape, ratio=2, overlap=False)
+    v0, v1 = kv[0::2, 0], kv[1::2, 0]
+    g0, g1 = gate[0::2, 0], gate[1::2, 0]
+    sig = 1.0 / (1.0 + np.exp(g1 - g0))
+    assert np.allclose(out, v0 * sig + v1 * (1.0 - sig), rtol=0, atol=1e-12)
+    c32 = compress.compress_contract(kv.astype(np.float32), gate.astype(np.float32), ape.astype(np.float32),
+                                     ratio=2, overlap=False)
+    assert np.allclose(c32, out, rtol=0, atol=4e-6 * np.abs(kv).max())
+    g2 = np.zeros((T, 1, D), np.float32)
+    g2[2 * 5 + 1] = 80.0                      # the second token of pair 5
+    g2[2 * 9] = 80.0                          # the first token of pair 9
+    c = compress.compress_contract(kv.astype(np.float32), g2, ape.astype(np.float32), ratio=2, overlap=False)
+    assert np.array_equal(c[5], kv[11, 0].astype(np.float32))
+    assert np.array_equal(c[9], kv[18, 0].astype(np.float32))
+    assert np.array_equal(c[3], ((kv[6, 0].astype(np.float32) + kv[7, 0].astype(np.float32)) / np.float32(2))
+                          .astype(np.float32))
+
+
 def test_ten_token_prompt_overlap_structure(golden):
     g = golden["ten_token_prompt"]
     T = g["tokens"]
