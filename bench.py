@@ -236,8 +236,10 @@ def run_gpu(args, rank, world):
         torch.cuda.synchronize()
         ev_sb, ev_se = live_events(torch)
         graph = torch.cuda.CUDAGraph()
+        # armed outside the capture (it creates the library's timing branch stream),
+        # turned off inside it (that joins the branch into the captured step)
+        cskv.set_timing_events(ev_sb, ev_se)
         with torch.cuda.graph(graph):
-            cskv.set_timing_events(ev_sb, ev_se)
             step()
             cskv.set_timing_events(None, None)
     setup_s = time.time() - t_setup
@@ -272,6 +274,7 @@ def run_gpu(args, rank, world):
         run_once()
         evs[i][1].record()
         evs[i][1].synchronize()
+        ev_se.synchronize()
         score_ms.append(ev_sb.elapsed_time(ev_se))
     torch.cuda.synchronize()
     wall = time.time() - wall0

@@ -3,6 +3,7 @@
 // excepted).
 #include <atomic>
 #include <cstdint>
+#include <mutex>
 
 #include "internal.h"
 
@@ -22,6 +23,69 @@ void record_timing_event(cudaEvent_t ev, cudaStream_t stream) {
   cudaStreamIsCapturing(stream, &cs);
   cudaEventRecordWithFlags(ev, stream,
                            cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault);
+}
+
+// Timing events go on a branch forked from the call's stream, so that each kernel
+// on that stream still depends on the kernel before it alone (an event record
+// between two kernels would keep a programmatic dependent launch from overlapping
+// the kernel before it).  The branch joins the origin stream when the hook is
+// turned off, which inside a stream capture must happen before the capture ends.
+namespace {
+struct TimingBranch {
+  std::mutex mu;
+  int device = -1;
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  cudaStream_t origin = nullptr;
+  bool pending = false;
+};
+TimingBranch g_branch;
+
+void branch_join_locked() {
+  if (!g_branch.pending) return;
+  cudaEventRecord(g_branch.join, g_branch.side);
+  cudaStreamWaitEvent(g_branch.origin, g_branch.join, 0);
+  g_branch.pending = false;
+}
+
+void branch_create_locked() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return;
+  if (g_branch.side != nullptr && g_branch.device == dev) return;
+  if (g_branch.side != nullptr) {   // another device: the old helpers are dropped
+    cudaStreamDestroy(g_branch.side);
+    cudaEventDestroy(g_branch.fork);
+    cudaEventDestroy(g_branch.join);
+    g_branch.side = nullptr;
+  }
+  cudaStream_t st = nullptr;
+  cudaEvent_t f = nullptr, j = nullptr;
+  if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return;
+  if (cudaEventCreateWithFlags(&f, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&j, cudaEventDisableTiming) != cudaSuccess) {
+    cudaStreamDestroy(st);
+    if (f) cudaEventDestroy(f);
+    return;
+  }
+  g_branch.side = st;
+  g_branch.fork = f;
+  g_branch.join = j;
+  g_branch.device = dev;
+}
+}  // namespace
+
+void record_timing_branch(cudaEvent_t ev, cudaStream_t stream) {
+  if (ev == nullptr) return;
+  std::lock_guard<std::mutex> lk(g_branch.mu);
+  if (g_branch.side == nullptr || (g_branch.pending && g_branch.origin != stream)) {
+    record_timing_event(ev, stream);
+    return;
+  }
+  cudaEventRecord(g_branch.fork, stream);
+  cudaStreamWaitEvent(g_branch.side, g_branch.fork, 0);
+  record_timing_event(ev, g_branch.side);
+  g_branch.origin = stream;
+  g_branch.pending = true;
 }
 
 static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -79,6 +143,11 @@ void cskv_set_spin_limit(uint64_t cycles) {
 
 void cskv_set_timing_events(void* begin, void* end) {
   const bool on = begin != nullptr && end != nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_branch.mu);
+    branch_join_locked();
+    if (on) branch_create_locked();
+  }
   g_ev_begin.store(on ? begin : nullptr, std::memory_order_relaxed);
   g_ev_end.store(on ? end : nullptr, std::memory_order_relaxed);
 }

@@ -8,35 +8,40 @@
 //  1. index_prep_kernel   codes each request's queries (e4m3, one e8m0 scale per
 //     head) into the image of a 128-byte-swizzled shared-memory tile, folds the
 //     head scale into the head weight (ReLU(c x) = c ReLU(x) for c > 0) and
-//     clears the request's histogram, counters and the grid-barrier word.
-//  2. index_score_kernel  persistent and cooperative, two blocks per SM (one
-//     TMA-issuing thread per block cannot keep enough copies in flight on its
-//     own; two per SM can), warp-specialised:
-//       warp 0     streams the 64-row key pages with TMA (3-D tensor map over
-//                  the page pool, 128-byte swizzle) into a 4-stage ring, and
-//                  their fp32 row scales with bulk copies into a ring that the
-//                  epilogue releases;
-//       warp 1     issues tcgen05 MMAs: M = 128 entries, N = heads, K = 128 in
+//     clears the request's histogram, counters and the grid-barrier word.  It is
+//     a programmatic dependent of the kernel before it (the compressor that
+//     writes this step's key): the query coding overlaps that kernel.
+//  2. index_score_kernel  persistent and cooperative, one block per SM (all 512
+//     TMEM columns), warp-specialised:
+//       warps 0-1  two TMA producers, each with its own 4-stage ring (one
+//                  TMA-issuing thread per SM cannot keep enough copies in
+//                  flight): 64-row key pages by 3-D TMA (tensor map over the
+//                  page pool, 128-byte swizzle), their fp32 row scales by bulk
+//                  copies into a ring the epilogue releases.  Producer 0 also
+//                  schedules: it grabs chunks of four tiles from the requests'
+//                  work counters and hands every other tile to producer 1;
+//       warp 2     issues tcgen05 MMAs: M = 128 entries, N = heads, K = 128 in
 //                  four K = 32 e4m3 x e4m3 steps into one fp32 TMEM
 //                  accumulator (the key's single scale is applied afterwards),
-//                  four accumulators in flight;
-//       warps 2-5  read the accumulator with tcgen05.ld (one TMEM lane = one
-//                  entry), apply ReLU and the head weights, sum the heads
-//                  inside one thread, multiply by the key's scale, write the
-//                  fp32 score, bin its order-preserving key into a
-//                  4,096-bin shared histogram and keep the largest key of
-//                  each 32-entry segment.
-//     Then, behind a bounded grid barrier, every block finds each request's
-//     threshold bin T (the bin holding the k-th score), counts its own entries
-//     above T and stages the ones in T as 64-bit (score, ~index) keys; only
-//     segments whose largest key reaches T are read again.  Behind a second
-//     barrier every block radix-selects the exact cut among the request's
-//     candidates (ties -> smaller index), derives its output offset from the
-//     lower blocks' counts and writes its own selected entries in entry
-//     order, so the output needs no sort.
+//                  eight accumulators in flight;
+//       warps 3-10 two epilogue groups on alternate tiles: tcgen05.ld (one TMEM
+//                  lane = one entry), ReLU and the head weights, the heads
+//                  summed inside one thread, times the key's scale, the fp32
+//                  score written, its order-preserving key binned into the
+//                  group's 4,096-bin shared histogram (with 256 coarse bins of
+//                  16) and the largest key of each 32-entry segment kept.
+//     Then, behind one bounded grid barrier, every request's tiles are split
+//     over a run of blocks: each finds the threshold bin T (the bin holding the
+//     k-th score), reads again only the segments whose largest key reaches T,
+//     and writes the entries in bins >= T as 64-bit (score, ~index) keys in
+//     entry order; the block that finishes a request's last slice radix-selects
+//     the exact cut among the keys of bin T (12-bit digits, ties -> smaller
+//     index) and writes the k entries in entry order, so the output needs no
+//     sort.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "codec.cuh"
@@ -154,6 +159,8 @@ __global__ void __launch_bounds__(256) index_prep_kernel(const IndexArgs a) {
   uint32_t* hist = reinterpret_cast<uint32_t*>(a.ws + a.L.hist) + size_t(b) * kHistStride;
   uint32_t* ctr = reinterpret_cast<uint32_t*>(a.ws + a.L.ctr) + b * 4;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the score kernel (a programmatic dependent of this one) may start its set-up now
+  grid_dep_launch();
   // warp w owns heads w, w+8, ... (N <= 64); lane l holds dims 4l .. 4l+3.  All loads first.
   uint2 raw[8];
   float wv[8];
@@ -489,12 +496,19 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm->tmem_base;
+  // The kernel is a programmatic dependent of the query prep, which is one of the
+  // compressor that writes this step's keys: the set-up above overlaps them, and no
+  // thread reads what they write (keys, query images, weights, counters) before
+  // this wait.  The scheduling producer first requests its first chunk's page ids
+  // (block tables are inputs) and waits after that.
+  const bool sched_thread = warp == 0 && lane == 0;
+  if (!sched_thread) grid_dep_wait();
 
   // ======================================================= phase 1: scores
-  // Tiles are handed out dynamically, in pairs of consecutive tiles of one request:
-  // producer 0 grabs a pair from the request's counter (starting at a home request
-  // spread over the grid, moving on when it is exhausted), keeps the first tile and
-  // hands the second to producer 1.  Block-local tile i goes through producer i % 2
+  // Tiles are handed out dynamically, in chunks of kChunkTiles consecutive tiles of
+  // one request: producer 0 grabs a chunk from the request's counter (starting at a
+  // home request spread over the grid, moving on when it is exhausted), keeps the
+  // even tiles and hands the odd ones to producer 1.  Block-local tile i goes through producer i % 2
   // (stage (i / 2) % kStages of its ring), accumulator i % 8, epilogue group i % 2
   // and slot i % 16 of the scale and tile-info rings.  A tile past the end of its
   // request is a hole (no pages, no entries); request -1 ends the sequence.
@@ -578,19 +592,21 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
             pending = atomicAdd(&ctr_all[req * 4], static_cast<uint32_t>(kChunkTiles));
           }
         };
-        int cb, ct;
-        {
-          const int r = blockIdx.x - first_home_block(req, a.B, gridDim.x);
-          pending = atomicAdd(&ctr_all[req * 4], static_cast<uint32_t>(kChunkTiles));
-          if (static_cast<long long>(r) * kChunkTiles < tiles_of(req)) {
-            cb = req;   // the block's first chunk, assigned without an atomic
-            ct = r * kChunkTiles;
-          } else {
-            resolve(cb, ct);
-          }
-        }
+        int cb = -1, ct = 0;
         int ids[2 * kChunkTiles];
-        chunk_ids(cb, ct, ids);
+        const int r0 = blockIdx.x - first_home_block(req, a.B, gridDim.x);
+        const bool static_first = static_cast<long long>(r0) * kChunkTiles < tiles_of(req);
+        if (static_first) {
+          cb = req;   // the block's first chunk, assigned without an atomic
+          ct = r0 * kChunkTiles;
+          chunk_ids(cb, ct, ids);
+        }
+        grid_dep_wait();
+        pending = atomicAdd(&ctr_all[req * 4], static_cast<uint32_t>(kChunkTiles));
+        if (!static_first) {
+          resolve(cb, ct);
+          chunk_ids(cb, ct, ids);
+        }
         int q_b = -1;
         long long m = 0;   // pairs posted
         bool ok = true;
@@ -1215,10 +1231,33 @@ cudaError_t launch_score(const CUtensorMap& tmap, const IndexArgs& a, cudaStream
   cfg.blockDim = dim3(kScoreThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
+  // A cooperative launch that is also a programmatic dependent: whether the runtime
+  // takes the pair is learnt from the first launch made outside a stream capture
+  // (a failed launch inside one could end the capture); until then, and if it
+  // refuses, the launch is cooperative only.
+  static std::atomic<int> pdl_ok{-1};
+  int ok = pdl_ok.load(std::memory_order_relaxed);
+  if (ok < 0) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) ok = 0;
+  }
+  if (ok != 0) {
+    cfg.numAttrs = 2;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, index_score_kernel<FP8>, tmap, a);
+    if (e == cudaSuccess) {
+      pdl_ok.store(1, std::memory_order_relaxed);
+      return e;
+    }
+    if (ok == 1) return e;   // the pair was taken before: a real failure
+    cudaGetLastError();      // the refused pair: clear it and launch cooperative only
+    pdl_ok.store(0, std::memory_order_relaxed);
+  }
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, index_score_kernel<FP8>, tmap, a);
 }
@@ -1300,9 +1339,9 @@ cudaError_t launch_index_topk(const void* q_idx, const float* w, const cskv_page
 
   cudaEvent_t ev_begin, ev_end;
   timing_events(&ev_begin, &ev_end);
-  record_timing_event(ev_begin, stream);
+  record_timing_branch(ev_begin, stream);
   e = a.fp8 ? launch_score<1>(tmap, a, stream) : launch_score<0>(tmap, a, stream);
-  record_timing_event(ev_end, stream);
+  record_timing_branch(ev_end, stream);
   return e;
 }
 

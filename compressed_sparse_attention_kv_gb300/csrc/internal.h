@@ -16,6 +16,7 @@ unsigned long long spin_limit();
 // measurement hook around the indexer score kernel (may be null)
 void timing_events(cudaEvent_t* begin, cudaEvent_t* end);
 void record_timing_event(cudaEvent_t ev, cudaStream_t stream);
+void record_timing_branch(cudaEvent_t ev, cudaStream_t stream);
 
 cudaError_t launch_compress(const void* kv, const void* gate, const void* prev_kv,
                             const void* prev_gate, const float* ape, const float* norm_w, float eps,

@@ -108,11 +108,19 @@ CSKV_API int32_t cskv_device_status(void* stream);
 CSKV_API void cskv_set_spin_limit(uint64_t cycles);
 
 /* Measurement hook.  With both non-NULL (cudaEvent_t handles passed as void*),
- * every later cskv_index_topk call records `begin` right before and `end` right
- * after its score kernel - the pass that streams the index keys - on the call's
- * stream; inside a stream capture they become external event-record nodes, so a
- * replayed CUDA graph records them on every replay.  NULL, NULL turns it off.
- * Process-wide; meant for benchmarks, not for concurrent use. */
+ * every later cskv_index_topk call records `begin` when the kernel before its
+ * score kernel (the query prep) completes, and `end` when the score kernel - the
+ * pass that streams the index keys - completes.  Both are recorded on a
+ * library-owned branch stream forked from the call's stream, so each kernel on the
+ * call's stream still depends on the one before it alone and may overlap it as a
+ * programmatic dependent launch (the score kernel's set-up overlaps the prep; the
+ * attention's set-up overlaps the score kernel's tail).  Inside a stream capture both become external
+ * event-record nodes, so a replayed CUDA graph records them on every replay.
+ * NULL, NULL turns the hook off and joins the branch back into the stream of the
+ * last timed call: under stream capture, turn it off before the capture ends.
+ * Turning it on creates the branch stream for the current device: do that
+ * outside any stream capture.  Process-wide; meant for benchmarks, not for
+ * concurrent use. */
 CSKV_API void cskv_set_timing_events(void* begin, void* end);
 
 /* ------------------------------------------------------------------------
