@@ -517,6 +517,9 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
     const int pw = warp;
     if (lane == 0) {
       prefetch_tmap(&tmap);
+      // the keys are read once: evict-first, so the stream does not push the scores,
+      // segment maxima and histograms that the selection reads back out of L2
+      const uint64_t pol = l2_evict_first();
       long long np = 0;       // tiles this producer posted (the end marker included)
       int nreq = 0;           // query images loaded (producer 0)
       // post local tile i = (request b, tile t) with its two page ids (-2: no page,
@@ -546,11 +549,12 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
         mbar_expect_tx(&sm->sfull[ss], FP8 ? (pages[0] >= 0 ? 256u : 0u) + (pages[1] >= 0 ? 256u : 0u) : 0u);
         for (int pg = 0; pg < 2; ++pg) {
           if (pages[pg] < 0) continue;
-          tma_load_3d(dst + pg * 8192, &tmap, 0, 0, pages[pg], &sm->full[pw][s]);
-          if (!FP8) tma_load_3d(dst + 16384 + pg * 8192, &tmap, 64, 0, pages[pg], &sm->full[pw][s]);
+          tma_load_3d_hint(dst + pg * 8192, &tmap, 0, 0, pages[pg], &sm->full[pw][s], pol);
+          if (!FP8) tma_load_3d_hint(dst + 16384 + pg * 8192, &tmap, 64, 0, pages[pg], &sm->full[pw][s], pol);
           if (FP8) {
             const uint8_t* pgp = static_cast<const uint8_t*>(a.keys.pool) + size_t(pages[pg]) * a.keys.page_bytes;
-            bulk_g2s(sring + ss * kTileRows + pg * kPageRows, pgp + kPageRows * 128, 256, &sm->sfull[ss]);
+            bulk_g2s_hint(sring + ss * kTileRows + pg * kPageRows, pgp + kPageRows * 128, 256, &sm->sfull[ss],
+                          pol);
           }
         }
         ++np;
