@@ -119,11 +119,27 @@ class PagedCache:
                           self.fmt, self.dim)
 
 
-def rope_table(positions, theta=160000.0, rope_dim=64):
-    """Host helper: float32 [n, 32, 2] (cos, sin) of positions * theta^(-2k/64), computed in fp64."""
+# YaRN of the compressed layers: 65,536 original positions stretched 16-fold, betas 32 / 1
+YARN_V4 = dict(factor=16.0, original=65536, beta_fast=32.0, beta_slow=1.0)
+
+
+def rope_table(positions, theta=160000.0, rope_dim=64, yarn=None):
+    """Host helper: float32 [n, 32, 2] (cos, sin) of positions * f_k, computed in fp64, with
+    f_k = theta^(-2k/64) or, with yarn (a dict like YARN_V4), the YaRN method's blend: pairs
+    below the correction range keep f_k, pairs above it get f_k / factor, and pairs inside it
+    mix the two along a linear ramp over the pair index."""
     pos = np.asarray(positions, dtype=np.float64)
     k = np.arange(rope_dim // 2, dtype=np.float64)
-    ang = pos[..., None] * (theta ** (-2.0 * k / rope_dim))
+    f = theta ** (-2.0 * k / rope_dim)
+    if yarn is not None:
+        # pair that turns `beta` times over the original length: d * ln(L / (2 pi beta)) / (2 ln theta)
+        lo = rope_dim * np.log(yarn["original"] / (2.0 * np.pi * yarn["beta_fast"])) / (2.0 * np.log(theta))
+        hi = rope_dim * np.log(yarn["original"] / (2.0 * np.pi * yarn["beta_slow"])) / (2.0 * np.log(theta))
+        lo = max(int(np.floor(lo)), 0)
+        hi = min(int(np.ceil(hi)), rope_dim // 2 - 1)
+        ramp = np.clip((k - lo) / max(hi - lo, 1e-3), 0.0, 1.0)
+        f = f / yarn["factor"] * ramp + f * (1.0 - ramp)
+    ang = pos[..., None] * f
     return np.stack([np.cos(ang), np.sin(ang)], axis=-1).astype(np.float32)
 
 
@@ -181,6 +197,44 @@ def compress_many(jobs, stream=None):
                                   j["req"].data_ptr(), j["first_entry"].data_ptr(), j["out"].desc())
     st = _lib.lib().cskv_compress_many(arr, len(jobs), _stream(stream))
     _check(st, "cskv_compress_many")
+
+
+def decode_state(B, ratio, overlap, dim, device="cuda"):
+    """A fresh per-request compressor state ring for decode_append: (state_kv, state_gate),
+    bf16 [B, nblk * ratio, coff, dim] (nblk = coff = 2 with overlap, else 1), kv 0 and gate -inf."""
+    import torch
+    nblk = 2 if overlap else 1
+    coff = 2 if overlap else 1
+    shape = (B, nblk * ratio, coff, dim)
+    return (torch.zeros(shape, dtype=torch.bfloat16, device=device),
+            torch.full(shape, float("-inf"), dtype=torch.bfloat16, device=device))
+
+
+def decode_append(jobs, pos, stream=None):
+    """One decode step's state update.  Each job is a dict: kv, gate (bf16 [B, coff, dim]; gate
+    may be None at ratio 1), state (the (state_kv, state_gate) pair of decode_state; None at
+    ratio 1), ratio, overlap, out (PagedCache), and optionally ape, norm_w, eps, rope_cs
+    (fp32 [B, 32, 2] at the position each request writes), ring_rows.  pos: int32 [B]
+    positions of the new tokens (< 0: no token)."""
+    import torch
+    _need(pos, torch.int32, "pos")
+    arr = (_lib.DecodeJob * len(jobs))()
+    for i, j in enumerate(jobs):
+        kv = j["kv"]
+        _need(kv, torch.bfloat16, "kv")
+        _need(j.get("gate"), torch.bfloat16, "gate")
+        st = j.get("state")
+        sk, sg = (st if st is not None else (None, None))
+        _need(sk, torch.bfloat16, "state_kv")
+        _need(sg, torch.bfloat16, "state_gate")
+        for t, n in ((j.get("ape"), "ape"), (j.get("norm_w"), "norm_w"), (j.get("rope_cs"), "rope_cs")):
+            _need(t, torch.float32, n)
+        arr[i] = _lib.DecodeJob(kv.data_ptr(), _ptr(j.get("gate")), _ptr(sk), _ptr(sg), _ptr(j.get("ape")),
+                                _ptr(j.get("norm_w")), float(j.get("eps", 1e-6)), _ptr(j.get("rope_cs")),
+                                int(j["ratio"]), int(bool(j.get("overlap", 0))), int(kv.shape[-1]),
+                                int(j.get("ring_rows", 0)), j["out"].desc())
+    st = _lib.lib().cskv_decode_append(arr, len(jobs), pos.data_ptr(), int(pos.shape[0]), _stream(stream))
+    _check(st, "cskv_decode_append")
 
 
 def index_topk_workspace_size(B, max_ctx_len, ratio, Hi, k):

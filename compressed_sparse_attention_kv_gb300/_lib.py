@@ -48,6 +48,25 @@ class CompressJob(ctypes.Structure):
     ]
 
 
+class DecodeJob(ctypes.Structure):
+    """struct cskv_decode_job (one compressor, or the window, of a decode step)."""
+    _fields_ = [
+        ("kv", c_void_p),
+        ("gate", c_void_p),
+        ("state_kv", c_void_p),
+        ("state_gate", c_void_p),
+        ("ape", c_void_p),
+        ("norm_w", c_void_p),
+        ("eps", c_float),
+        ("rope_cs", c_void_p),
+        ("ratio", c_int32),
+        ("overlap", c_int32),
+        ("dim", c_int32),
+        ("ring_rows", c_int32),
+        ("out", Paged),
+    ]
+
+
 # name -> (restype, argtypes); every symbol include/cskv.h declares
 SIGNATURES = {
     "cskv_row_bytes": (c_size_t, [c_int32, c_int32]),
@@ -62,6 +81,7 @@ SIGNATURES = {
                                 c_void_p, c_int32, c_int32, c_int32, c_int32, c_int32, c_void_p,
                                 c_void_p, Paged, c_void_p]),
     "cskv_compress_many": (c_int32, [ctypes.POINTER(CompressJob), c_int32, c_void_p]),
+    "cskv_decode_append": (c_int32, [ctypes.POINTER(DecodeJob), c_int32, c_void_p, c_int32, c_void_p]),
     "cskv_index_topk_workspace_size": (c_size_t, [c_int32, c_int32, c_int32, c_int32, c_int32]),
     "cskv_index_topk": (c_int32, [c_void_p, c_void_p, Paged, c_void_p, c_int32, c_int32, c_int32,
                                   c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),

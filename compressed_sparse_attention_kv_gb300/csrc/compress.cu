@@ -62,6 +62,12 @@ struct CompressArgs {
   int S, T, ratio, overlap, n;  // n = T / ratio entries per sequence
   cskv_paged out;
   int out_row_bytes;
+  // Decode mode (pos != nullptr): sequence s is request s's state ring and only its
+  // last entry (i = n - 1) is computed, when the token at position pos[s] completes
+  // its block (always with ring > 0); it goes to row (pos + 1) / ratio - 1 of
+  // request s, or to row pos % ring; rope_cs holds one (cos, sin) row per request.
+  const int32_t* pos;
+  int ring;
 };
 
 // bf16 row pointer of token `tok` (channel half `half`) of sequence s.
@@ -96,12 +102,18 @@ __device__ __forceinline__ void compress_block(const CompressArgs& a, long long 
   constexpr int EPB = 128 / TPE;    // entries per block
   const int lt = threadIdx.x % TPE;
   const long long gentry = blk * EPB + threadIdx.x / TPE;
-  const long long total = static_cast<long long>(a.S) * a.n;
-  const bool live = gentry < total;
+  const bool dec = a.pos != nullptr;
+  const long long total = dec ? a.S : static_cast<long long>(a.S) * a.n;
+  bool live = gentry < total;
+  int p = 0;
+  if (dec && live) {
+    p = a.pos[gentry];
+    live = p >= 0 && (a.ring > 0 || (p + 1) % a.ratio == 0);   // p < 0: no token this step
+  }
   // D == 512: one entry per block, the whole block stays for the block-wide sum.
   if (!live && D != 512) return;
-  const long long s = live ? gentry / a.n : 0;
-  const int i = live ? static_cast<int>(gentry % a.n) : 0;
+  const long long s = live ? (dec ? gentry : gentry / a.n) : 0;
+  const int i = live ? (dec ? a.n - 1 : static_cast<int>(gentry % a.n)) : 0;
   const int c0 = 4 * lt;
   const int r = a.ratio;
   const int coff = a.overlap ? 2 : 1;
@@ -114,7 +126,7 @@ __device__ __forceinline__ void compress_block(const CompressArgs& a, long long 
       if (i > 0) {
         const long long tok = static_cast<long long>(i - 1) * r + j;
         vp = tok_ptr(a.kv, s, a.T, tok, coff, 0, D) + 2 * c0;
-        gp = tok_ptr(a.gate, s, a.T, tok, coff, 0, D) + 2 * c0;
+        gp = a.gate ? tok_ptr(a.gate, s, a.T, tok, coff, 0, D) + 2 * c0 : nullptr;
       } else if (a.prev_kv != nullptr) {
         vp = tok_ptr(a.prev_kv, s, r, j, 2, 0, D) + 2 * c0;
         gp = tok_ptr(a.prev_gate, s, r, j, 2, 0, D) + 2 * c0;
@@ -128,21 +140,22 @@ __device__ __forceinline__ void compress_block(const CompressArgs& a, long long 
       const long long tok = static_cast<long long>(i) * r + jj;
       ao = static_cast<long long>(jj) * coff * D + half * D + c0;
       vp = tok_ptr(a.kv, s, a.T, tok, coff, half, D) + 2 * c0;
-      gp = tok_ptr(a.gate, s, a.T, tok, coff, half, D) + 2 * c0;
+      gp = a.gate ? tok_ptr(a.gate, s, a.T, tok, coff, half, D) + 2 * c0 : nullptr;   // no gate: scores 0
     }
   };
   // Loads that do not depend on the slots go first, so their latency (and the
   // req -> block table -> row chain) overlaps the slot loops.
   RowPtr dst{nullptr, nullptr};
   if (live) {
-    const long long row = static_cast<long long>(a.first_entry[s]) + i;
-    dst = paged_row(a.out, a.req[s], row, a.out_row_bytes);
+    const long long row = dec ? (a.ring > 0 ? p % a.ring : (p + 1) / a.ratio - 1)
+                              : static_cast<long long>(a.first_entry[s]) + i;
+    dst = paged_row(a.out, dec ? static_cast<int>(s) : a.req[s], row, a.out_row_bytes);
   }
   const float4 nw = a.norm_w != nullptr ? *reinterpret_cast<const float4*>(a.norm_w + c0)
                                         : make_float4(1.f, 1.f, 1.f, 1.f);
   const bool rotate = a.rope_cs != nullptr && live && c0 >= D - 64;
   const float4 cs = rotate ? *reinterpret_cast<const float4*>(
-                                 a.rope_cs + ((s * a.n + i) * 32 + (c0 - (D - 64)) / 2) * 2)
+                                 a.rope_cs + ((dec ? s : s * a.n + i) * 32 + (c0 - (D - 64)) / 2) * 2)
                            : make_float4(1.f, 0.f, 1.f, 0.f);
 
   // Slots are staged through shared memory in batches of kBatch with cp.async (the
@@ -167,7 +180,7 @@ __device__ __forceinline__ void compress_block(const CompressArgs& a, long long 
         slot_src(j, vp, gp, ao);
         if (vp != nullptr) {
           cp_async8(&s_kv[(buf * kBatch + u) * 128 + t], vp);
-          cp_async8(&s_g[(buf * kBatch + u) * 128 + t], gp);
+          if (gp != nullptr) cp_async8(&s_g[(buf * kBatch + u) * 128 + t], gp);
         }
         if (a.ape != nullptr) cp_async16(&s_ap[(buf * kBatch + u) * 128 + t], a.ape + ao);
       }
@@ -185,7 +198,7 @@ __device__ __forceinline__ void compress_block(const CompressArgs& a, long long 
       if (v) *v = make_float4(0.f, 0.f, 0.f, 0.f);
       return;
     }
-    const uint2 g = s_g[(buf * kBatch + u) * 128 + t];
+    const uint2 g = gp != nullptr ? s_g[(buf * kBatch + u) * 128 + t] : make_uint2(0u, 0u);
     // no slot bias (ape == nullptr) adds +0: the same bits as a zero bias table
     const float4 b = a.ape != nullptr ? s_ap[(buf * kBatch + u) * 128 + t] : make_float4(0.f, 0.f, 0.f, 0.f);
     sc = make_float4(__fadd_rn(bf16lo(g.x), b.x), __fadd_rn(bf16hi(g.x), b.y), __fadd_rn(bf16lo(g.y), b.z),
@@ -286,6 +299,82 @@ __global__ void __launch_bounds__(128) compress_many_kernel(const __grid_constan
   else compress_block<128>(m.job[j], blk);
 }
 
+// ---------------------------------------------------------------------------
+// The decode step's state update ("DeepSeek-V4 deep dive", section 4.3 and the
+// implementation notes to section 4): each request's new token goes into slot
+// (overlap ? r : 0) + p mod r of its compressor's state ring ([2 blocks or 1] x r
+// tokens x coff x D, bf16); a token that completes its block (p + 1 = 0 mod r)
+// has the block's entry pooled from the ring (the previous block through half 0,
+// this one through half 1) and written as entry (p + 1) / r - 1, and with overlap
+// the block then moves into the previous-block slots.  A ratio-1 job pools
+// nothing: its entry is the token itself, normalised, rotated and coded, written
+// to row p or, with a ring, to row p mod ring (the 128-slot window).
+// ---------------------------------------------------------------------------
+constexpr int kMaxDecodeJobs = 8;
+struct DecodeJob {
+  CompressArgs a;           // decode mode; kv / gate = the state ring (ratio > 1) or the token (ratio 1)
+  const uint8_t* tok_kv;    // bf16 [S, coff, D]: the new tokens (ratio > 1)
+  const uint8_t* tok_gate;
+  int dim;
+};
+struct DecodeMany {
+  DecodeJob job[kMaxDecodeJobs];
+  long long first[kMaxDecodeJobs + 1];
+  int njobs;
+};
+
+template <int D>
+__device__ __forceinline__ void decode_block(const DecodeJob& q, long long blk) {
+  const CompressArgs& a = q.a;
+  constexpr int TPE = D / 4;
+  constexpr int EPB = 128 / TPE;
+  const int lt = threadIdx.x % TPE;
+  const long long s = blk * EPB + threadIdx.x / TPE;
+  const int r = a.ratio;
+  const int coff = a.overlap ? 2 : 1;
+  const int p = s < a.S ? a.pos[s] : -1;
+  const bool ringed = r > 1;
+  uint8_t* ring_kv = const_cast<uint8_t*>(a.kv);
+  uint8_t* ring_gate = const_cast<uint8_t*>(a.gate);
+  // byte offset of (request s, ring slot, half h, this thread's 4 channels)
+  const long long base = (s * a.T * coff * D + 4 * lt) * 2;
+#define CSKV_RING_AT(slot, h) (base + ((static_cast<long long>(slot) * coff + (h)) * D) * 2)
+  if (ringed && p >= 0) {
+    const int slot = (a.overlap ? r : 0) + p % r;
+#pragma unroll 1
+    for (int h = 0; h < coff; ++h) {
+      const long long src = ((s * coff + h) * D + 4 * lt) * 2;
+      *reinterpret_cast<uint2*>(ring_kv + CSKV_RING_AT(slot, h)) = *reinterpret_cast<const uint2*>(q.tok_kv + src);
+      *reinterpret_cast<uint2*>(ring_gate + CSKV_RING_AT(slot, h)) = *reinterpret_cast<const uint2*>(q.tok_gate + src);
+    }
+    __threadfence();   // the pooling below reads this slot back with cp.async
+  }
+  __syncthreads();
+  compress_block<D>(a, blk);
+  // the overlap shift (each thread moves its own channels, which the pooling has
+  // finished reading: compress_block waits for all of its copies)
+  if (ringed && a.overlap && p >= 0 && (p + 1) % r == 0) {
+#pragma unroll 1
+    for (int j = 0; j < r; ++j) {
+#pragma unroll 1
+      for (int h = 0; h < coff; ++h) {
+        *reinterpret_cast<uint2*>(ring_kv + CSKV_RING_AT(j, h)) = *reinterpret_cast<const uint2*>(ring_kv + CSKV_RING_AT(r + j, h));
+        *reinterpret_cast<uint2*>(ring_gate + CSKV_RING_AT(j, h)) = *reinterpret_cast<const uint2*>(ring_gate + CSKV_RING_AT(r + j, h));
+      }
+    }
+  }
+}
+#undef CSKV_RING_AT
+
+__global__ void __launch_bounds__(128, 1) decode_append_kernel(const __grid_constant__ DecodeMany m) {
+  grid_dep_launch();
+  int j = 0;
+  while (j + 1 < m.njobs && static_cast<long long>(blockIdx.x) >= m.first[j + 1]) ++j;
+  const long long blk = blockIdx.x - m.first[j];
+  if (m.job[j].dim == 512) decode_block<512>(m.job[j], blk);
+  else decode_block<128>(m.job[j], blk);
+}
+
 struct EncodeArgs {
   const uint8_t* src;
   int src_bf16;
@@ -341,6 +430,8 @@ static CompressArgs compress_args(const void* kv, const void* gate, const void* 
   a.n = T / ratio;
   a.out = out;
   a.out_row_bytes = out_row_bytes;
+  a.pos = nullptr;
+  a.ring = 0;
   return a;
 }
 
@@ -382,6 +473,33 @@ cudaError_t launch_compress_many(const cskv_compress_job* jobs, int njobs, cudaS
   cudaFuncSetAttribute(compress_many_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        static_cast<int>(kCompressSmem));
   compress_many_kernel<<<static_cast<unsigned>(m.first[njobs]), 128, kCompressSmem, stream>>>(m);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_append(const cskv_decode_job* jobs, int njobs, const int32_t* pos, int B,
+                                 cudaStream_t stream) {
+  if (njobs < 1 || njobs > kMaxDecodeJobs) return cudaErrorInvalidValue;
+  DecodeMany m;
+  m.njobs = njobs;
+  m.first[0] = 0;
+  for (int j = 0; j < njobs; ++j) {
+    const cskv_decode_job& q = jobs[j];
+    const bool ringed = q.ratio > 1;
+    const int T = ringed ? (q.overlap ? 2 : 1) * q.ratio : 1;
+    m.job[j].a = compress_args(ringed ? q.state_kv : q.kv, ringed ? q.state_gate : q.gate, nullptr, nullptr, q.ape,
+                               q.norm_w, q.eps, q.rope_cs, B, T, q.ratio, q.overlap, nullptr, nullptr, q.out,
+                               static_cast<int>(cskv_row_bytes(q.out.fmt, q.dim)));
+    m.job[j].a.pos = pos;
+    m.job[j].a.ring = q.ring_rows;
+    m.job[j].tok_kv = static_cast<const uint8_t*>(q.kv);
+    m.job[j].tok_gate = static_cast<const uint8_t*>(q.gate);
+    m.job[j].dim = q.dim;
+    m.first[j + 1] = m.first[j] + compress_blocks(B, 1, q.dim);
+  }
+  if (m.first[njobs] == 0) return cudaSuccess;
+  cudaFuncSetAttribute(decode_append_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       static_cast<int>(kCompressSmem));
+  decode_append_kernel<<<static_cast<unsigned>(m.first[njobs]), 128, kCompressSmem, stream>>>(m);
   return cudaGetLastError();
 }
 

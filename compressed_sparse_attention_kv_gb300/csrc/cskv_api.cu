@@ -218,6 +218,32 @@ int32_t cskv_compress_many(const cskv_compress_job* jobs, int32_t njobs, void* s
   return cuda_status(launch_compress_many(jobs, njobs, static_cast<cudaStream_t>(stream)));
 }
 
+int32_t cskv_decode_append(const cskv_decode_job* jobs, int32_t njobs, const int32_t* pos, int32_t B,
+                           void* stream) {
+  if (jobs == nullptr || njobs < 1 || njobs > 8 || B < 0) return CSKV_ERR_INVALID;
+  if (B > 0 && pos == nullptr) return CSKV_ERR_INVALID;
+  for (int32_t j = 0; j < njobs; ++j) {
+    const cskv_decode_job& q = jobs[j];
+    if (q.kv == nullptr || (q.dim != 128 && q.dim != 512)) return CSKV_ERR_INVALID;
+    if (q.ratio < 1 || q.ratio > 1024 || (q.overlap != 0 && q.overlap != 1)) return CSKV_ERR_INVALID;
+    if (q.overlap && (q.ratio < 2 || q.ratio > 8)) return CSKV_ERR_INVALID;
+    if (q.ring_rows < 0 || (q.ring_rows > 0 && q.ratio != 1)) return CSKV_ERR_INVALID;
+    if (q.ratio > 1 && (q.gate == nullptr || q.state_kv == nullptr || q.state_gate == nullptr))
+      return CSKV_ERR_INVALID;
+    if (!(q.eps >= 0.0f)) return CSKV_ERR_INVALID;
+    if (!aligned(q.kv, 8) || (q.gate && !aligned(q.gate, 8))) return CSKV_ERR_INVALID;
+    if ((q.state_kv && !aligned(q.state_kv, 8)) || (q.state_gate && !aligned(q.state_gate, 8)))
+      return CSKV_ERR_INVALID;
+    if ((q.ape && !aligned(q.ape, 16)) || (q.norm_w && !aligned(q.norm_w, 16)) ||
+        (q.rope_cs && !aligned(q.rope_cs, 16)))
+      return CSKV_ERR_INVALID;
+    if (!paged_ok(q.out, q.dim, 0xFu)) return CSKV_ERR_INVALID;
+    if (q.out.fmt == CSKV_FMT_FP8_E4M3_ROWSCALE_PAGESPLIT && q.dim != 128) return CSKV_ERR_INVALID;
+  }
+  if (B == 0) return CSKV_OK;
+  return cuda_status(launch_decode_append(jobs, njobs, pos, B, static_cast<cudaStream_t>(stream)));
+}
+
 size_t cskv_index_topk_workspace_size(int32_t B, int32_t max_ctx_len, int32_t ratio, int32_t Hi,
                                       int32_t k) {
   if (B <= 0 || max_ctx_len < 0 || ratio < 1 || Hi < 1 || k < 1) return 0;

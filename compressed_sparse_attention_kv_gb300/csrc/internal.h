@@ -25,6 +25,8 @@ cudaError_t launch_compress(const void* kv, const void* gate, const void* prev_k
                             int out_row_bytes, cudaStream_t stream);
 
 cudaError_t launch_compress_many(const cskv_compress_job* jobs, int njobs, cudaStream_t stream);
+cudaError_t launch_decode_append(const cskv_decode_job* jobs, int njobs, const int32_t* pos, int B,
+                                 cudaStream_t stream);
 
 cudaError_t launch_encode_rows(const void* src, int src_bf16, int n, int dim, const int32_t* req,
                                const int32_t* row, const cskv_paged& out, int out_row_bytes,

@@ -204,6 +204,58 @@ typedef struct {
 CSKV_API int32_t cskv_compress_many(const cskv_compress_job* jobs, int32_t njobs, void* stream);
 
 /* ------------------------------------------------------------------------
+ * cskv_decode_append: the state update of one decode step ("DeepSeek-V4 deep
+ * dive", section 4.3 "What is cached" and its implementation notes to section
+ * 4: every compressor keeps the projected tokens of its unfinished block, and of
+ * the block before it when it overlaps, in a fixed-size per-request state; the
+ * window keeps the last 128 tokens as a ring).
+ *
+ * For each job and each request b with pos[b] >= 0 (the position p of the
+ * request's new token; pos[b] < 0 = no token for b this step):
+ *   - ratio > 1: the token's kv and gate ([B, coff, dim] bf16, coff = 2 with
+ *     overlap) go into slot (overlap ? ratio : 0) + p % ratio of the request's
+ *     state ring state_kv / state_gate ([B, nblk * ratio, coff, dim] bf16,
+ *     nblk = 2 with overlap: the previous block, then the one being filled;
+ *     else 1).  If p + 1 is a multiple of ratio the block is complete: its
+ *     entry is pooled exactly as cskv_compress pools entry 1 of a 2-block
+ *     sequence (overlap) or entry 0 of a 1-block one, and written as row
+ *     (p + 1) / ratio - 1 of request b of `out`; with overlap the completed
+ *     block then moves into the previous-block slots.  A fresh request's ring
+ *     holds kv 0 and gate -inf (bf16 0xFF80) in every slot: the first block
+ *     then sees an empty previous block, as in cskv_compress.
+ *   - ratio 1 (no pooling; state_* unused and may be NULL, gate may be NULL):
+ *     the entry is the token itself, RMSNorm-ed, rotated and coded; it is
+ *     written to row p, or, with ring_rows > 0, to row p % ring_rows (the
+ *     window ring: give it the 128-row window as a paged cache of two 64-row
+ *     pages per request).
+ * RMSNorm (norm_w, eps), RoPE and coding are those of cskv_compress; rope_cs
+ * ([B, 32, 2] fp32, NULL = none) holds, per request, (cos, sin) at the
+ * position of the row it writes this step: p + 1 - ratio (the block's first
+ * token) for ratio > 1, p for ratio 1.  Rows of requests that complete
+ * nothing are ignored.
+ * Arithmetic: bit-exact with cskv_compress (same contract).  Up to 8 jobs
+ * (e.g. the main and index-key compressors of a CSA layer and the window) in
+ * one launch.  pos: device int32 [B].  Alignment: kv, gate, state_* 8 bytes;
+ * ape, norm_w, rope_cs 16 bytes.  Errors: CSKV_ERR_INVALID for bad arguments;
+ * a row outside the block table or the pool sets CSKV_ERR_BOUNDS on the
+ * device (the row is skipped).
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  const void* kv;
+  const void* gate;
+  void* state_kv;
+  void* state_gate;
+  const float* ape;
+  const float* norm_w;
+  float eps;
+  const float* rope_cs;
+  int32_t ratio, overlap, dim, ring_rows;
+  cskv_paged out;
+} cskv_decode_job;
+CSKV_API int32_t cskv_decode_append(const cskv_decode_job* jobs, int32_t njobs, const int32_t* pos, int32_t B,
+                                    void* stream);
+
+/* ------------------------------------------------------------------------
  * cskv_index_topk: the lightning indexer and top-k ("DeepSeek-V4 deep dive",
  * section 5.2 "What is different from V3.2's indexer"):
  *   I_{b,j} = sum_h w[b,h] * ReLU(q[b,h,:] . k_{b,j})   for j < n_b,

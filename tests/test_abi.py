@@ -26,7 +26,7 @@ def _declared():
 def test_header_and_binding_agree():
     from compressed_sparse_attention_kv_gb300 import _lib
     names = _declared()
-    assert len(names) == 14
+    assert len(names) == 15
     assert sorted(_lib.SIGNATURES) == names
 
 
@@ -79,6 +79,20 @@ def test_invalid_arguments_launch_nothing(lib):
     assert lib.cskv_compress_many(jobs, 5, None) == 1                          # more than 4 jobs
     jobs[0] = CompressJob(4096, 4096, None, None, 4096, None, 1e-6, None, 1, 6, 4, 1, 512, 4096, 4096, good)
     assert lib.cskv_compress_many(jobs, 1, None) == 1                          # T % ratio != 0
+    from compressed_sparse_attention_kv_gb300._lib import DecodeJob
+    dj = (DecodeJob * 9)()
+    assert lib.cskv_decode_append(dj, 9, fake, 2, None) == 1                     # more than 8 jobs
+    dj[0] = DecodeJob(4096, 4096, None, None, None, None, 1e-6, None, 4, 1, 512, 0, good)
+    assert lib.cskv_decode_append(dj, 1, fake, 2, None) == 1                     # ratio 4 without a state ring
+    dj[0] = DecodeJob(4096, None, 4096, 4096, None, None, 1e-6, None, 4, 1, 512, 0, good)
+    assert lib.cskv_decode_append(dj, 1, fake, 2, None) == 1                     # ratio 4 without a gate
+    dj[0] = DecodeJob(4096, 4096, 4096, 4096, None, None, 1e-6, None, 4, 1, 512, 128, good)
+    assert lib.cskv_decode_append(dj, 1, fake, 2, None) == 1                     # a ring needs ratio 1
+    dj[0] = DecodeJob(4096, None, None, None, None, None, 1e-6, None, 1, 1, 512, 128, good)
+    assert lib.cskv_decode_append(dj, 1, fake, 2, None) == 1                     # overlap needs ratio 2..8
+    dj[0] = DecodeJob(4096, None, None, None, None, None, 1e-6, None, 1, 0, 512, 128, good)
+    assert lib.cskv_decode_append(dj, 1, None, 2, None) == 1                     # no positions
+    assert lib.cskv_decode_append(dj, 1, None, 0, None) == 0                     # empty batch: nothing to do
     keys = Paged(4096, 4096, 64 * 132, 4, 4, 3, 128)
     assert lib.cskv_index_topk(fake, fake, keys, fake, 1, 65, 4, 512, 4096, fake, None, fake, 1 << 30,
                                None) == 2                                       # > 64 heads

@@ -110,3 +110,12 @@ def test_yarn_pairs_follow_the_printed_split(golden):
     # the plain table is the one without YaRN
     assert np.array_equal(rope.table([12345]), rope.table([12345], yarn=None))
     assert not np.array_equal(rope.table([1_000_000]), rope.table([1_000_000], yarn=yarn))
+
+
+def test_product_rope_tables_equal_the_oracle_tables():
+    """The binding's host table helper (an input generator of the CUDA path) and the oracle's
+    table agree bit for bit, with and without YaRN."""
+    import compressed_sparse_attention_kv_gb300 as cskv
+    pos = np.array([0, 1, 2, 127, 4096, 65535, 65536, 524287, 1048575])
+    assert np.array_equal(cskv.rope_table(pos), rope.table(pos))
+    assert np.array_equal(cskv.rope_table(pos, yarn=cskv.YARN_V4), rope.table(pos, yarn=rope.YARN_V4))
