@@ -213,6 +213,14 @@ __global__ void __launch_bounds__(256) index_prep_kernel(const IndexArgs a) {
 // ---------------------------------------------------------------------------
 // 2. score kernel (+ fused selection)
 // ---------------------------------------------------------------------------
+// One request of this block's selection work: tiles [lo, hi) of request b, whose run
+// of blocks starts at fb and has nbk blocks of `per` tiles.
+struct WorkItem {
+  long long lo, hi, per;
+  int b, fb, nbk, pad;
+};
+constexpr int kWorkItems = 16;
+
 struct ScoreSmem {
   uint64_t full[kProducers][kStagesFp8], empty[kProducers][kStagesFp8];
   uint64_t accfull[kAccs], accempty[kAccs];
@@ -232,6 +240,8 @@ struct ScoreSmem {
   uint32_t base[2];
   uint32_t nlist;
   int nbv[kReqCache];              // visible entries of the first kReqCache requests
+  WorkItem work[kWorkItems];       // this block's selection work, found before the scores
+  int nwork;                       // -1: more than kWorkItems (found again after the barrier)
   int T;
   uint32_t above, inT;
   uint32_t need, done, out;
@@ -502,6 +512,28 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
   // this wait.  The scheduling producer first requests its first chunk's page ids
   // (block tables are inputs) and waits after that.
   const bool sched_thread = warp == 0 && lane == 0;
+  if (threadIdx.x == 32) {
+    // This block's selection work depends on the context lengths alone (inputs): one
+    // thread finds it now, beside the prep, instead of every thread after the barrier.
+    // (Producer 1 has nothing to do until producer 0's first hand-over.)
+    long long C = 0;
+    int nw = 0;
+#pragma unroll 1
+    for (int b = 0; b < a.B; ++b) {
+      const long long tb = (visible(a, b) + kTileRows - 1) / kTileRows;
+      WorkItem wi;
+      const bool mine = block_range(blockIdx.x, gridDim.x, C, tb, total, wi.lo, wi.hi, wi.fb, wi.nbk, wi.per);
+      C += tb;
+      if (!mine) {
+        if (wi.fb > static_cast<int>(blockIdx.x)) break;   // the runs only move further right
+        continue;
+      }
+      wi.b = b;
+      if (nw < kWorkItems) sm->work[nw] = wi;
+      ++nw;
+    }
+    sm->nwork = nw <= kWorkItems ? nw : -1;
+  }
   if (!sched_thread) grid_dep_wait();
 
   // ======================================================= phase 1: scores
@@ -883,19 +915,39 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
       __syncthreads();
       return pos;
     };
+    const int nwork = sm->nwork;
     long long C = 0;
+    int bnext = 0;
 #pragma unroll 1
-    for (int b = 0; b < a.B && !aborted; ++b) {
-      const int nb = b < kReqCache ? sm->nbv[b] : visible(a, b);
-      const long long tb = (nb + kTileRows - 1) / kTileRows;
+    for (int w = 0; !aborted; ++w) {
+      int b = -1, fb, nbk;
       long long lo, hi, per_b;
-      int fb, nbk;
-      const bool mine = block_range(blockIdx.x, gridDim.x, C, tb, total, lo, hi, fb, nbk, per_b);
-      C += tb;
-      if (!mine) {
-        if (fb > static_cast<int>(blockIdx.x)) break;   // the runs only move further right
-        continue;
+      if (nwork >= 0) {
+        if (w >= nwork) break;
+        const WorkItem wi = sm->work[w];
+        b = wi.b;
+        lo = wi.lo;
+        hi = wi.hi;
+        per_b = wi.per;
+        fb = wi.fb;
+        nbk = wi.nbk;
+      } else {
+        // more requests than the list holds: the next one whose run holds this block
+#pragma unroll 1
+        while (bnext < a.B) {
+          const int bb = bnext++;
+          const long long tb = (visible(a, bb) + kTileRows - 1) / kTileRows;
+          const bool mine = block_range(blockIdx.x, gridDim.x, C, tb, total, lo, hi, fb, nbk, per_b);
+          C += tb;
+          if (mine) {
+            b = bb;
+            break;
+          }
+          if (fb > static_cast<int>(blockIdx.x)) bnext = a.B;   // the runs only move further right
+        }
+        if (b < 0) break;
       }
+      const int nb = b < kReqCache ? sm->nbv[b] : visible(a, b);
       const int slice = blockIdx.x - fb;
       const float* sc = scores_all + size_t(b) * a.L.n_pad;
       int32_t* out_idx = a.topk_idx + size_t(b) * a.k;

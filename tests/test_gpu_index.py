@@ -123,3 +123,24 @@ def test_csa_1m_full_size_sampled():
         vals = synth.request_values(wl, b, "index")
         k_hat = codecs.decode_pagesplit(codecs.encode_pagesplit(vals), 128)
         check_topk(idx[b], sc[b], indexer.quantize_queries(q_v[b]), w[b], k_hat, n, wl.k)
+
+
+def test_many_empty_requests_share_a_block():
+    """Twenty empty requests in a row all belong to one block's selection work (more than
+    that block's work list holds), then requests of 125, 0, 175 and 0 entries."""
+    ratio, k, Hi = 4, 16, 4
+    ctx = [0] * 20 + [4 * 125 + 1, 2, 4 * 175, 3]
+    n = [c // ratio for c in ctx]
+    rs = np.random.default_rng(12)
+    q = rs.standard_normal((len(ctx), Hi, 128)).astype(np.float32)
+    w = rs.uniform(0, 1, (len(ctx), Hi)).astype(np.float32)
+    cache = HostPaged(codecs.FMT_FP8_PAGESPLIT, 128, [max(1, x) for x in n], seed=13)
+    for b, nb in enumerate(n):
+        cache.fill(b, rs.standard_normal((max(1, nb), 128)).astype(np.float32))
+    q_t, q_v = bf16_values(q)
+    idx, sc = _run(q_t, w, cache, ctx, ratio, k, max(ctx))
+    for b, nb in enumerate(n):
+        if nb == 0:
+            assert np.all(idx[b] == -1), b
+        else:
+            check_topk(idx[b], sc[b], indexer.quantize_queries(q_v[b]), w[b], cache.decoded[b], nb, k)
