@@ -832,16 +832,15 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm->accempty[c]);   // this warp's TMEM reads are done
-      // four independent accumulation chains (the epilogue's latency sets the pace)
+      // four independent accumulation chains, two per packed fma (the epilogue's
+      // instruction count sets part of the streaming pace)
       float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
       for (int h = 0; h < 64; h += 4) {
         if (h < N) {
           const float4 w4 = *reinterpret_cast<const float4*>(&wq_s[h]);
-          s0 = fmaf(w4.x, fmaxf(P[h], 0.f), s0);
-          s1 = fmaf(w4.y, fmaxf(P[h + 1], 0.f), s1);
-          s2 = fmaf(w4.z, fmaxf(P[h + 2], 0.f), s2);
-          s3 = fmaf(w4.w, fmaxf(P[h + 3], 0.f), s3);
+          fma2(s0, s1, w4.x, w4.y, fmaxf(P[h], 0.f), fmaxf(P[h + 1], 0.f));
+          fma2(s2, s3, w4.z, w4.w, fmaxf(P[h + 2], 0.f), fmaxf(P[h + 3], 0.f));
         }
       }
       const float I = ((s0 + s1) + (s2 + s3)) * ks;   // the key's scale is a positive power of two
