@@ -1,0 +1,141 @@
+"""GPU parity on the named workloads themselves: the tiny CSA layer end to end (compress,
+index, attend; the oracle finishes it in seconds), and the 1M-context and mixed-batch MXFP4
+decode layers at full size, in the bench's launch configuration, checked on sampled
+requests (indexer selection and attention output against the oracle)."""
+
+import concurrent.futures
+
+import numpy as np
+import pytest
+import torch
+
+import compressed_sparse_attention_kv_gb300 as cskv
+from compressed_sparse_attention_kv_gb300 import synth
+from oracle import attention as o_attn, codecs, compress as o_comp, indexer, rope as o_rope
+
+from cases import bf16_values, check_attention, check_topk, cuda, swa_ring
+
+pytestmark = pytest.mark.gpu
+
+SCALE = 512 ** -0.5
+
+
+def _page_bytes(fmt, dim):
+    return (64 * codecs.row_bytes(fmt, dim) + 15) // 16 * 16
+
+
+def _build_lane(wl, lane, fmt, dim):
+    """Device cache of one lane of a (possibly ragged) workload, coded on the GPU from the
+    seeded values, request by request."""
+    bt, num_pages = synth.page_tables(wl, lane)
+    cache = cskv.PagedCache(torch.zeros((num_pages, _page_bytes(fmt, dim)), dtype=torch.uint8, device="cuda"),
+                            cuda(bt), fmt, dim)
+    f = synth.index_page_values if lane == "index" else synth.main_page_values
+    ppr = wl.pages_per_req()
+    with concurrent.futures.ThreadPoolExecutor(max_workers=16) as ex:
+        for b in range(wl.B):
+            pages = list(ex.map(lambda p: f(wl, b, p), range(int(ppr[b]))))
+            vals = torch.from_numpy(np.concatenate(pages)).cuda()
+            rows = torch.arange(vals.shape[0], dtype=torch.int32, device="cuda")
+            cskv.encode_rows(vals, cache, req=torch.full_like(rows, b), row=rows)
+            del vals
+    return cache
+
+
+def _oracle_keys(wl, b):
+    """The oracle's decoded index keys of request b (coded by the oracle's codecs)."""
+    vals = synth.request_values(wl, b, "index")
+    n = int(wl.n_entries[b])
+    return codecs.decode_pagesplit(codecs.encode_pagesplit(vals), 128)[:n]
+
+
+def _oracle_entries(wl, b, rows, fmt):
+    """Decoded main entries of request b at the given rows (others zero): [n_b, 512]."""
+    n = int(wl.n_entries[b])
+    out = np.zeros((n, 512))
+    pages = synth.request_values(wl, b, "main", rows=rows)
+    for p, v in pages.items():
+        dec = codecs.decode_rows(codecs.encode_rows(v, fmt), fmt, 512)
+        lo = p * 64
+        hi = min(n, lo + 64)
+        out[lo:hi] = dec[:hi - lo]
+    return out
+
+
+def _full_size(name, sample):
+    wl = synth.workload(name)
+    keys = _build_lane(wl, "index", synth.FMT_FP8_PAGESPLIT, 128)
+    main = _build_lane(wl, "main", wl.main_fmt, 512)
+    swa_vals = np.stack([synth.swa_values(wl, b) for b in range(wl.B)])
+    swa_b, swa_dec = swa_ring(swa_vals, wl.swa_fmt)
+    q, q_idx, w, sink = synth.queries(wl)
+    q_t, q_v = bf16_values(q)
+    qi_t, qi_v = bf16_values(q_idx)
+    ctx = wl.ctx_len.astype(np.int32)
+    topk, _ = cskv.index_topk(qi_t.cuda(), cuda(w), keys, cuda(ctx), wl.ratio, wl.k, wl.max_ctx, want_scores=False)
+    out = cskv.sparse_decode_attn(q_t.cuda(), main, cuda(swa_b), wl.swa_fmt, cuda(ctx), topk, wl.k, wl.ratio,
+                                  wl.max_ctx, cuda(sink), SCALE, cuda(cskv.rope_table(ctx - 1)))
+    assert cskv.device_status() == 0
+    topk = topk.cpu().numpy()
+    got = out.float().cpu().numpy()
+    for b in sample:
+        n = int(wl.n_entries[b])
+        q_hat = indexer.quantize_queries(qi_v[b])
+        k_hat = _oracle_keys(wl, b)
+        assert check_topk(topk[b], None, q_hat, w[b], k_hat, n, wl.k) == 0, b
+        sel = indexer.select_topk(indexer.scores_fp64(q_hat, w[b], k_hat), wl.k)
+        ent = _oracle_entries(wl, b, sel[sel >= 0], wl.main_fmt)
+        ref = o_attn.request_attention(q_v[b], int(ctx[b]), wl.ratio, swa_dec[b], ent, sel, sink, SCALE)
+        check_attention(got[b], ref, fp4=wl.main_fmt == synth.FMT_FP4)
+
+
+def test_csa_1m_full_size_sampled_layer():
+    """Batch 8 at 1,048,576 tokens: selection and attention of requests 0, 3 and 7."""
+    _full_size("csa_1m", (0, 3, 7))
+
+
+def test_mixed_mxfp4_full_size_sampled_layer():
+    """Batch 64 with contexts from 32,768 to 524,288 tokens, MXFP4 main entries: the
+    shortest, the longest and two other requests."""
+    wl = synth.workload("mixed_mxfp4")
+    order = np.argsort(wl.ctx_len)
+    _full_size("mixed_mxfp4", (int(order[0]), int(order[-1]), 5, 40))
+
+
+def test_tiny_csa_end_to_end():
+    """The tiny CSA layer: 4,096 tokens compressed (ratio 4, overlap) into bf16 main entries
+    and index keys, 4 indexer heads select 512 of the 1,024 entries, 16 heads attend."""
+    wl = synth.workload("tiny_csa")
+    T, r, n = 4096, 4, 1024
+    outs = {}
+    for lane, dim, idx_lane in (("main", 512, False), ("index", 128, True)):
+        kv, gate = synth.compressor_tokens(wl.seed, T, r, True, dim, index_lane=idx_lane)
+        ape, nw = synth.compressor_params(wl.seed, r, True, dim, index_lane=idx_lane)
+        kv_t, kv_v = bf16_values(kv)
+        g_t, g_v = bf16_values(gate)
+        dev = cskv.PagedCache(torch.zeros((n // 64, 64 * dim * 2), dtype=torch.uint8, device="cuda"),
+                              cuda(np.arange(n // 64, dtype=np.int32)[None]), codecs.FMT_BF16, dim)
+        cskv.compress(kv_t[None].cuda(), g_t[None].cuda(), cuda(ape), r, 1, dev, cuda(np.array([0], np.int32)),
+                      cuda(np.array([0], np.int32)), norm_w=cuda(nw), eps=1e-6,
+                      rope_cs=cuda(cskv.rope_table(np.arange(n) * r)[None]))
+        ents = o_comp.compress_contract(kv_v, g_v, ape, r, True, norm_w=nw, eps=1e-6,
+                                        rope_cs=o_rope.table(np.arange(n) * r))
+        want = codecs.encode_rows(ents, codecs.FMT_BF16)
+        got = dev.pool.cpu().numpy()[:, :64 * want.shape[1]].reshape(n, -1)
+        assert np.array_equal(got, want), lane
+        outs[lane] = (dev, codecs.decode_rows(want, codecs.FMT_BF16, dim))
+    swa_b, swa_dec = swa_ring(synth.swa_values(wl, 0)[None], codecs.FMT_BF16)
+    q, q_idx, w, sink = synth.queries(wl)
+    q_t, q_v = bf16_values(q)
+    qi_t, qi_v = bf16_values(q_idx)
+    ctx = np.array([T], np.int32)
+    topk, sc = cskv.index_topk(qi_t.cuda(), cuda(w), outs["index"][0], cuda(ctx), r, wl.k, T)
+    out = cskv.sparse_decode_attn(q_t.cuda(), outs["main"][0], cuda(swa_b), codecs.FMT_BF16, cuda(ctx), topk,
+                                  wl.k, r, T, cuda(sink), SCALE, cuda(cskv.rope_table(ctx - 1)))
+    assert cskv.device_status() == 0
+    k_hat = outs["index"][1]
+    q_hat = qi_v[0].astype(np.float64)          # bf16 keys: the queries are used as given
+    assert check_topk(topk.cpu().numpy()[0], sc.cpu().numpy()[0], q_hat, w[0], k_hat, n, wl.k) == 0
+    sel = indexer.select_topk(indexer.scores_fp64(q_hat, w[0], k_hat), wl.k)
+    ref = o_attn.request_attention(q_v[0], T, r, swa_dec[0], outs["main"][1], sel, sink, SCALE)
+    check_attention(out.float().cpu().numpy()[0], ref)
