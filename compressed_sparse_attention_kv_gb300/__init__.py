@@ -295,4 +295,32 @@ def sparse_decode_attn(q, main_kv, swa, swa_fmt, ctx_len, topk_idx, k, ratio, ma
     return out
 
 
+def sparse_prefill_attn(q, main_kv, window, pos1, topk_idx, k, ratio, max_ctx_len, sink, softmax_scale,
+                        q_rope_cs, req_of=None, out=None, workspace=None, stream=None):
+    """The attention of many prompt queries; query i of request req_of[i] sits at position
+    pos1[i] - 1 and reads its window from `window` (raw rows by position).  Returns out
+    bf16 [T, H, 512]."""
+    import torch
+    _need(q, torch.bfloat16, "q")
+    _need(pos1, torch.int32, "pos1")
+    _need(req_of, torch.int32, "req_of")
+    _need(topk_idx, torch.int32, "topk_idx")
+    _need(sink, torch.float32, "sink")
+    _need(q_rope_cs, torch.float32, "q_rope_cs")
+    T, H, _ = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    kk = int(k) if topk_idx is not None else 0
+    if workspace is None:
+        workspace = torch.empty(sparse_decode_attn_workspace_size(T, H, max_ctx_len, ratio, kk),
+                                dtype=torch.uint8, device=q.device)
+    st = _lib.lib().cskv_sparse_prefill_attn(q.data_ptr(), main_kv.desc(), window.desc(), _ptr(req_of),
+                                             pos1.data_ptr(), _ptr(topk_idx), kk, int(ratio), int(max_ctx_len),
+                                             _ptr(sink), float(softmax_scale), q_rope_cs.data_ptr(), T, H,
+                                             out.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                                             _stream(stream))
+    _check(st, "cskv_sparse_prefill_attn")
+    return out
+
+
 DEFAULT_SCALE = 1.0 / math.sqrt(512.0)

@@ -91,6 +91,9 @@ SIGNATURES = {
     "cskv_sparse_decode_attn": (c_int32, [c_void_p, Paged, c_void_p, c_int32, c_void_p, c_void_p,
                                           c_int32, c_int32, c_int32, c_void_p, c_float, c_void_p,
                                           c_int32, c_int32, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "cskv_sparse_prefill_attn": (c_int32, [c_void_p, Paged, Paged, c_void_p, c_void_p, c_void_p, c_int32,
+                                           c_int32, c_int32, c_void_p, c_float, c_void_p, c_int32, c_int32,
+                                           c_void_p, c_void_p, c_size_t, c_void_p]),
 }
 
 _lib = None

@@ -8,7 +8,12 @@
 // every visible entry).
 //
 // GB300 design.  A request's key list is cut into 128-key tiles: tile 0 is the
-// 128-slot window ring, tiles 1.. are 128 consecutive list entries.  One block
+// 128-slot window ring (in prefill, the query's request's raw rows at positions
+// t-127 .. t, fewer at the start: causal), tiles 1.. are 128 consecutive list
+// entries.  Prefill runs every query as its own list ("DeepSeek-V4 deep dive",
+// section 5.3: the buffer [all raw rows of the prompt ; its compressed entries],
+// the window indices t-127 .. t masked below 0); req_of maps a query to its
+// request.  One block
 // handles one (request, tile, head group of <= 64 heads):
 //   * the tile's rows (528 B FP8, 288 B FP4 or 1 KiB bf16; the row addresses come
 //     from the block table) and the query are copied into shared memory with
@@ -59,8 +64,10 @@ struct AttnArgs {
   const uint8_t* q;
   cskv_paged kv;
   int kv_row_bytes;
-  const uint8_t* swa;
+  const uint8_t* swa;          // decode: the 128-slot window ring [B, 128, row]
   int swa_fmt, swa_row_bytes;
+  cskv_paged win;              // prefill (win.pool != nullptr): raw rows by position, per request
+  const int32_t* req_of;       // request of each query (block tables, window); nullptr = the query's index
   const int32_t* ctx_len;
   const int32_t* topk;
   int k, ratio, max_ctx;
@@ -267,16 +274,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
   if (tile > 0) grid_dep_wait();
   // ---- rows of this tile: one thread per row resolves its address (the list entry,
   // then the block table), all rows in parallel
+  const int rq = a.req_of ? a.req_of[b] : b;
   for (int r = threadIdx.x; r < kKeys; r += blockDim.x) {
     const uint8_t* p = nullptr;
     if (tile == 0) {
-      if ((t >= kKeys - 1) || (r <= t)) p = a.swa + (size_t(b) * kWindow + r) * a.swa_row_bytes;
+      if (a.win.pool == nullptr) {
+        if ((t >= kKeys - 1) || (r <= t)) p = a.swa + (size_t(b) * kWindow + r) * a.swa_row_bytes;
+      } else {
+        const int pos = t - (kKeys - 1) + r;   // positions t-127 .. t; none below 0
+        if (pos >= 0) p = paged_row(a.win, rq, pos, a.swa_row_bytes).data;
+      }
     } else {
       const int li = (tile - 1) * kKeys + r;
       if (li < ncomp) {
         const int e = a.topk ? a.topk[size_t(b) * a.k + li] : li;
         if (e >= 0) {
-          if (e < ctx / a.ratio) p = paged_row(a.kv, b, e, a.kv_row_bytes).data;
+          if (e < ctx / a.ratio) p = paged_row(a.kv, rq, e, a.kv_row_bytes).data;
           else set_err(CSKV_ERR_BOUNDS);
         }
       }
@@ -522,11 +535,11 @@ size_t attn_workspace_bytes(int B, int H, int max_ctx, int ratio, int k) {
   return attn_layout(B, H, max_ctx, ratio, k).total;
 }
 
-cudaError_t launch_sparse_decode_attn(const void* q, const cskv_paged& kv, const void* swa, int swa_fmt,
-                                      const int32_t* ctx_len, const int32_t* topk, int k, int ratio,
-                                      int max_ctx, const float* sink, float softmax_scale,
-                                      const float* q_rope, int B, int H, void* out, void* workspace,
-                                      cudaStream_t stream) {
+static cudaError_t launch_attn(const void* q, const cskv_paged& kv, const void* swa, const cskv_paged* win,
+                               int swa_fmt, const int32_t* req_of, const int32_t* ctx_len, const int32_t* topk,
+                               int k, int ratio, int max_ctx, const float* sink, float softmax_scale,
+                               const float* q_rope, int B, int H, void* out, void* workspace,
+                               cudaStream_t stream) {
   const AttnLayout L = attn_layout(B, H, max_ctx, ratio, topk ? k : 0);
   AttnArgs a;
   a.q = static_cast<const uint8_t*>(q);
@@ -535,6 +548,8 @@ cudaError_t launch_sparse_decode_attn(const void* q, const cskv_paged& kv, const
   a.swa = static_cast<const uint8_t*>(swa);
   a.swa_fmt = swa_fmt;
   a.swa_row_bytes = static_cast<int>(cskv_row_bytes(swa_fmt, kD));
+  a.win = win ? *win : cskv_paged{};
+  a.req_of = req_of;
   a.ctx_len = ctx_len;
   a.topk = topk;
   a.k = k;
@@ -569,6 +584,24 @@ cudaError_t launch_sparse_decode_attn(const void* q, const cskv_paged& kv, const
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
   return cudaLaunchKernelEx(&cfg, attn_combine_kernel, a);
+}
+
+cudaError_t launch_sparse_decode_attn(const void* q, const cskv_paged& kv, const void* swa, int swa_fmt,
+                                      const int32_t* ctx_len, const int32_t* topk, int k, int ratio,
+                                      int max_ctx, const float* sink, float softmax_scale,
+                                      const float* q_rope, int B, int H, void* out, void* workspace,
+                                      cudaStream_t stream) {
+  return launch_attn(q, kv, swa, nullptr, swa_fmt, nullptr, ctx_len, topk, k, ratio, max_ctx, sink,
+                     softmax_scale, q_rope, B, H, out, workspace, stream);
+}
+
+cudaError_t launch_sparse_prefill_attn(const void* q, const cskv_paged& kv, const cskv_paged& win,
+                                       const int32_t* req_of, const int32_t* pos1, const int32_t* topk, int k,
+                                       int ratio, int max_ctx, const float* sink, float softmax_scale,
+                                       const float* q_rope, int T, int H, void* out, void* workspace,
+                                       cudaStream_t stream) {
+  return launch_attn(q, kv, nullptr, &win, win.fmt, req_of, pos1, topk, k, ratio, max_ctx, sink, softmax_scale,
+                     q_rope, T, H, out, workspace, stream);
 }
 
 unsigned int take_err_attention() { return take_dev_err(); }

@@ -320,4 +320,25 @@ int32_t cskv_sparse_decode_attn(const void* q, cskv_paged main_kv, const void* s
                                                static_cast<cudaStream_t>(stream)));
 }
 
+int32_t cskv_sparse_prefill_attn(const void* q, cskv_paged main_kv, cskv_paged window, const int32_t* req_of,
+                                 const int32_t* pos1, const int32_t* topk_idx, int32_t k, int32_t ratio,
+                                 int32_t max_ctx_len, const float* sink, float softmax_scale,
+                                 const float* q_rope_cs, int32_t T, int32_t H, void* out, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  if (q == nullptr || pos1 == nullptr || q_rope_cs == nullptr || out == nullptr) return CSKV_ERR_INVALID;
+  if (T < 1 || T > 65535 || H < 1 || H > 128 || ratio < 1 || max_ctx_len < 0) return CSKV_ERR_INVALID;
+  if (topk_idx != nullptr && (k < 1 || k > 2048)) return CSKV_ERR_INVALID;
+  if (!aligned(q, 16) || !aligned(q_rope_cs, 16) || !aligned(out, 16)) return CSKV_ERR_INVALID;
+  if (!(softmax_scale > 0.0f)) return CSKV_ERR_INVALID;
+  if (!paged_ok(main_kv, 512, (1u << CSKV_FMT_BF16) | (1u << CSKV_FMT_FP8_E4M3_E8M0_B32) |
+                                  (1u << CSKV_FMT_FP4_E2M1_E4M3_B16)))
+    return CSKV_ERR_INVALID;
+  if (!paged_ok(window, 512, (1u << CSKV_FMT_BF16) | (1u << CSKV_FMT_FP8_E4M3_E8M0_B32))) return CSKV_ERR_INVALID;
+  const size_t need = attn_workspace_bytes(T, H, max_ctx_len, ratio, topk_idx ? k : 0);
+  if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < need) return CSKV_ERR_INVALID;
+  return cuda_status(launch_sparse_prefill_attn(q, main_kv, window, req_of, pos1, topk_idx, topk_idx ? k : 0,
+                                                ratio, max_ctx_len, sink, softmax_scale, q_rope_cs, T, H, out,
+                                                workspace, static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

@@ -49,6 +49,11 @@ cudaError_t launch_sparse_decode_attn(const void* q, const cskv_paged& kv, const
                                       int max_ctx, const float* sink, float softmax_scale,
                                       const float* q_rope, int B, int H, void* out, void* workspace,
                                       cudaStream_t stream);
+cudaError_t launch_sparse_prefill_attn(const void* q, const cskv_paged& kv, const cskv_paged& win,
+                                       const int32_t* req_of, const int32_t* pos1, const int32_t* topk, int k,
+                                       int ratio, int max_ctx, const float* sink, float softmax_scale,
+                                       const float* q_rope, int T, int H, void* out, void* workspace,
+                                       cudaStream_t stream);
 
 unsigned int take_err_compress();
 unsigned int take_err_index();

@@ -345,6 +345,32 @@ CSKV_API int32_t cskv_sparse_decode_attn(const void* q, cskv_paged main_kv,
                                 void* out, void* workspace, size_t workspace_bytes,
                                 void* stream);
 
+/* ------------------------------------------------------------------------
+ * cskv_sparse_prefill_attn: the same attention for many queries of a prompt
+ * ("DeepSeek-V4 deep dive", section 5.3: in prefill the buffer is [all raw-token
+ * keys of the prompt ; its compressed entries] and each query's index list is
+ * its window positions t-127 .. t, those below 0 masked, then its selected
+ * entries; section 5.2: a query sees the entries j < floor((t + 1) / ratio)).
+ * Query i (of T) belongs to request req_of[i] (NULL: request i) and sits at
+ * position t = pos1[i] - 1; it attends exactly as cskv_sparse_decode_attn's
+ * request with ctx_len = pos1[i], except that its window rows are rows
+ * max(0, t-127) .. t of its request in `window` (a paged cache of the raw rows
+ * by position, FP8 or BF16, 512-d) and its compressed entries come from its
+ * request's rows of main_kv.  q: bf16 [T, H, 512]; topk_idx: int32 [T, k] (each
+ * query's own selection, e.g. from cskv_index_topk run with one row per query;
+ * NULL: every visible entry); q_rope_cs: fp32 [T, 32, 2] at each query's
+ * position; out: bf16 [T, H, 512].  max_ctx_len >= every pos1[i].  Workspace:
+ * cskv_sparse_decode_attn_workspace_size(T, H, max_ctx_len, ratio, k) bytes.
+ * Errors as cskv_sparse_decode_attn; a window row outside the block table or
+ * the pool sets CSKV_ERR_BOUNDS on the device and is skipped.
+ * ------------------------------------------------------------------------ */
+CSKV_API int32_t cskv_sparse_prefill_attn(const void* q, cskv_paged main_kv, cskv_paged window,
+                                          const int32_t* req_of, const int32_t* pos1,
+                                          const int32_t* topk_idx, int32_t k, int32_t ratio,
+                                          int32_t max_ctx_len, const float* sink, float softmax_scale,
+                                          const float* q_rope_cs, int32_t T, int32_t H, void* out,
+                                          void* workspace, size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

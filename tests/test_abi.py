@@ -26,7 +26,7 @@ def _declared():
 def test_header_and_binding_agree():
     from compressed_sparse_attention_kv_gb300 import _lib
     names = _declared()
-    assert len(names) == 15
+    assert len(names) == 16
     assert sorted(_lib.SIGNATURES) == names
 
 
