@@ -495,6 +495,257 @@ def cpu_baseline_sample():
                       "numpy, BLAS threads for the score product"}
 
 
+# ----------------------------------------------------------------------------- next-row modes
+# Measurements of the rows built beyond the decode step (each prints its own JSON line;
+# the default mode above is the benchmark).
+
+def _graph_timed(torch, step, steps, warmup, flush, timing=None):
+    """CUDA-event times (ms) of a captured step, the L2 flushed (outside the events) before
+    each replay; timing = (cskv, ev_b, ev_e) records the score kernel live."""
+    for _ in range(max(1, warmup)):
+        step()
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    if timing:
+        timing[0].set_timing_events(timing[1], timing[2])
+    with torch.cuda.graph(graph):
+        step()
+        if timing:
+            timing[0].set_timing_events(None, None)
+    for _ in range(warmup):
+        flush.zero_()
+        graph.replay()
+    torch.cuda.synchronize()
+    clk = ClockSampler(os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0])
+    clk.start()
+    time.sleep(0.3)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    inner = []
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record()
+        graph.replay()
+        e1.record()
+        e1.synchronize()
+        if timing:
+            timing[2].synchronize()
+            inner.append(timing[1].elapsed_time(timing[2]))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs], inner, clk.stop()
+
+
+def _lane(torch, cskv, wl, lane, fmt, dim, fill=True):
+    """A paged cache of one lane of a workload, coded on the GPU from the seeded values."""
+    bt, num_pages = synth.page_tables(wl, lane)
+    rb = cskv.row_bytes(fmt, dim)
+    cache = cskv.PagedCache(torch.zeros((num_pages, (64 * rb + 15) // 16 * 16), dtype=torch.uint8, device="cuda"),
+                            torch.from_numpy(bt).cuda(), fmt, dim)
+    if fill:
+        f = synth.index_page_values if lane == "index" else synth.main_page_values
+        ppr = wl.pages_per_req()
+        for b in range(wl.B):
+            vals = torch.from_numpy(np.concatenate(gen_parallel(lambda p: f(wl, b, p), range(int(ppr[b]))))).cuda()
+            rows = torch.arange(vals.shape[0], dtype=torch.int32, device="cuda")
+            cskv.encode_rows(vals, cache, req=torch.full_like(rows, b), row=rows)
+            del vals
+    return cache
+
+
+def _ring(torch, cskv, wl, fmt):
+    """The window rings as a paged cache (two 64-row pages per request), coded from the seeded values."""
+    rb = cskv.row_bytes(fmt, 512)
+    pool = torch.zeros((2 * wl.B, 64 * rb), dtype=torch.uint8, device="cuda")
+    bt = torch.arange(2 * wl.B, dtype=torch.int32, device="cuda").view(wl.B, 2)
+    ring = cskv.PagedCache(pool, bt, fmt, 512)
+    vals = torch.from_numpy(np.stack([synth.swa_values(wl, b) for b in range(wl.B)])).cuda().reshape(-1, 512)
+    rows = torch.arange(128, dtype=torch.int32, device="cuda").repeat(wl.B)
+    req = torch.arange(wl.B, dtype=torch.int32, device="cuda").repeat_interleave(128)
+    cskv.encode_rows(vals, ring, req=req, row=rows)
+    return ring, pool
+
+
+def _line(mode, metric, value, unit, ms, hib, config, roofline, clocks, launches, args):
+    return {"mode": mode, "metric": metric, "value": value, "unit": unit, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": hib, "data": "synthetic",
+            "config": config, "roofline": roofline, "clocks": clocks, "gpu_launches": launches}
+
+
+def run_next_row(args):
+    import torch
+    import compressed_sparse_attention_kv_gb300 as cskv
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except OSError:
+        pass
+    peak = peaks.get("hbm_gbs", 6800.0)
+    psrc = "measured" if "hbm_gbs" in peaks else "fallback"
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    dev = "cuda"
+    if args.mode == "csa2":
+        # V4.1's CSA2 at 1M context, m = 2: the step updates the state (main and index
+        # compressors without overlap or slot bias, the window), selects once and attends
+        # in two layers that share the selection (Full, then Reuse)
+        L, r, B, k, H, Hi = 1 << 20, 2, 8, 512, 64, 64
+        wl = synth.custom_workload("csa2_1m", 5, [L] * B, r, k, H, Hi, synth.FMT_FP4, synth.FMT_FP8,
+                                   synth.FMT_FP8_PAGESPLIT)
+        keys = _lane(torch, cskv, wl, "index", cskv.FMT_FP8_PAGESPLIT, 128)
+        main = _lane(torch, cskv, wl, "main", cskv.FMT_FP4, 512)
+        ring, ring_pool = _ring(torch, cskv, wl, cskv.FMT_FP8)
+        q, q_idx, w, sink = synth.queries(wl)
+        bf = torch.bfloat16
+        q = torch.from_numpy(q).to(bf).cuda()
+        q2 = torch.roll(q, 1, dims=1).contiguous()            # the Reuse layer's own queries
+        q_idx, w, sink = torch.from_numpy(q_idx).to(bf).cuda(), torch.from_numpy(w).cuda(), torch.from_numpy(sink).cuda()
+        pos = torch.full((B,), L - 1, dtype=torch.int32, device=dev)
+        ctx = torch.full((B,), L, dtype=torch.int32, device=dev)
+        g = torch.Generator().manual_seed(5)
+        tok = lambda c, d: torch.randn((B, c, d), generator=g).to(bf).cuda()   # noqa: E731
+        nw = torch.from_numpy(synth.compressor_params(5, r, False, 512)[1]).cuda()
+        inw = torch.from_numpy(synth.compressor_params(5, r, False, 128, index_lane=True)[1]).cuda()
+        st_m, st_i = cskv.decode_state(B, r, 0, 512), cskv.decode_state(B, r, 0, 128)
+        cs_e = torch.from_numpy(cskv.rope_table(np.full(B, L - r), yarn=cskv.YARN_V4)).cuda()
+        cs_q = torch.from_numpy(cskv.rope_table(np.full(B, L - 1), yarn=cskv.YARN_V4)).cuda()
+        jobs = [dict(kv=tok(1, 512), gate=tok(1, 512), state=st_m, ratio=r, overlap=0, out=main, norm_w=nw,
+                     rope_cs=cs_e),
+                dict(kv=tok(1, 128), gate=tok(1, 128), state=st_i, ratio=r, overlap=0, out=keys, norm_w=inw,
+                     rope_cs=cs_e),
+                dict(kv=tok(1, 512), gate=None, state=None, ratio=1, overlap=0, out=ring, norm_w=nw,
+                     rope_cs=cs_q, ring_rows=128)]
+        topk = torch.empty((B, k), dtype=torch.int32, device=dev)
+        ws_i = torch.empty(cskv.index_topk_workspace_size(B, L, r, Hi, k), dtype=torch.uint8, device=dev)
+        ws_a = torch.empty(cskv.sparse_decode_attn_workspace_size(B, H, L, r, k), dtype=torch.uint8, device=dev)
+        out1, out2 = torch.empty_like(q), torch.empty_like(q)
+        swa = ring_pool.view(B, 128, -1)
+
+        def step():
+            cskv.decode_append(jobs, pos)
+            cskv.index_topk(q_idx, w, keys, ctx, r, k, L, topk_idx=topk, workspace=ws_i, want_scores=False)
+            cskv.sparse_decode_attn(q, main, swa, cskv.FMT_FP8, ctx, topk, k, r, L, sink, cskv.DEFAULT_SCALE,
+                                    cs_q, out=out1, workspace=ws_a)
+            cskv.sparse_decode_attn(q2, main, swa, cskv.FMT_FP8, ctx, topk, k, r, L, sink, cskv.DEFAULT_SCALE,
+                                    cs_q, out=out2, workspace=ws_a)
+
+        evb, eve = live_events(torch)
+        ms, inner, clocks = _graph_timed(torch, step, args.steps, args.warmup, flush, (cskv, evb, eve))
+        st = cskv.device_status()
+        assert st == 0, st
+        m = statistics.mean(ms)
+        sm_ = statistics.mean(inner)
+        algo = 132 * B * (L // r)
+        ach = algo / (sm_ * 1e-3) / 1e9
+        return _line("csa2", "CSA2 (m=2) decode step at 1M context: queries/s (one Full + one Reuse layer)",
+                     B / (m * 1e-3), "queries/s", m, True,
+                     {"workload": "CSA2 m=2 at 1M context: batch 8, 1048576 tokens -> 524288 entries, 64 indexer "
+                                  "heads x 128 FP8 keys (132 B), top-512 shared by two layers, 64 heads x 512 over "
+                                  "MXFP4-288 entries + FP8 window; per step: decode_append (main, index key, window), "
+                                  "index_topk, two sparse_decode_attn", "l2": "flushed before every step"},
+                     {"kernel": "index_score_kernel", "bound": "hbm", "achieved": ach, "peak": peak,
+                      "unit": "GB/s", "frac": ach / peak, "peak_source": psrc, "algorithmic_bytes_per_launch": algo,
+                      "ms_per_launch": sm_, "traffic": None}, clocks, 1 + 2 + 2 + 2, args)
+    if args.mode == "state":
+        # one CSA layer's decode-state update for the 1M-context batch: every request's new
+        # token completes a block (the costliest step: ring write, pooling, shift, window)
+        wl = synth.workload(WORKLOAD)
+        B, r, L = wl.B, wl.ratio, int(wl.ctx_len[0])
+        keys = _lane(torch, cskv, wl, "index", cskv.FMT_FP8_PAGESPLIT, 128, fill=False)
+        main = _lane(torch, cskv, wl, "main", cskv.FMT_FP8, 512, fill=False)
+        ring, _ = _ring(torch, cskv, wl, cskv.FMT_FP8)
+        bf = torch.bfloat16
+        g = torch.Generator().manual_seed(6)
+        tok = lambda c, d: torch.randn((B, c, d), generator=g).to(bf).cuda()   # noqa: E731
+        ape, nw = (torch.from_numpy(x).cuda() for x in synth.compressor_params(wl.seed, r, True, 512))
+        iape, inw = (torch.from_numpy(x).cuda() for x in synth.compressor_params(wl.seed, r, True, 128, True))
+        pos = torch.full((B,), L - 1, dtype=torch.int32, device=dev)
+        cs_e = torch.from_numpy(cskv.rope_table(np.full(B, L - r), yarn=cskv.YARN_V4)).cuda()
+        cs_q = torch.from_numpy(cskv.rope_table(np.full(B, L - 1), yarn=cskv.YARN_V4)).cuda()
+        jobs = [dict(kv=tok(2, 512), gate=tok(2, 512), state=cskv.decode_state(B, r, 1, 512), ratio=r, overlap=1,
+                     out=main, ape=ape, norm_w=nw, rope_cs=cs_e),
+                dict(kv=tok(2, 128), gate=tok(2, 128), state=cskv.decode_state(B, r, 1, 128), ratio=r, overlap=1,
+                     out=keys, ape=iape, norm_w=inw, rope_cs=cs_e),
+                dict(kv=tok(1, 512), gate=None, state=None, ratio=1, overlap=0, out=ring, norm_w=nw, rope_cs=cs_q,
+                     ring_rows=128)]
+
+        def step():
+            cskv.decode_append(jobs, pos)
+
+        ms, _, clocks = _graph_timed(torch, step, args.steps, args.warmup, flush)
+        assert cskv.device_status() == 0
+        m = statistics.mean(ms)
+        # bytes the step must move: the new tokens, the rings read and shifted, the rows written
+        per_req = (2 * 2 * 512 * 2 + 2 * 2 * 128 * 2 + 512 * 2          # new kv / gate tokens, window token
+                   + 2 * (8 * 2 * 512 * 2 + 8 * 2 * 128 * 2)            # rings read (kv, gate)
+                   + 2 * (4 * 2 * 512 * 2 + 4 * 2 * 128 * 2) * 2        # shift: read + write
+                   + 4 * 1024 + 4 * 256                                 # slot biases
+                   + 528 + 132 + 528)                                   # rows written
+        algo = B * per_req
+        ach = algo / (m * 1e-3) / 1e9
+        return _line("state", "decode-step state update of a CSA layer (batch 8, every request completes a block): "
+                     "us per step", m * 1e3, "us", m, False,
+                     {"workload": "csa_1m batch 8 at position 1048575: main (ratio 4, overlap, FP8-528) and index-key "
+                                  "(128-d, FP8-132) compressor state rings, window ring write; one decode_append launch",
+                      "l2": "flushed before every step"},
+                     {"kernel": "decode_append_kernel", "bound": "latency", "achieved": ach, "peak": peak,
+                      "unit": "GB/s", "frac": ach / peak, "peak_source": psrc, "algorithmic_bytes_per_launch": algo,
+                      "ms_per_launch": m, "traffic": None}, clocks, 1, args)
+    # prefill: the last 2,048 queries of an 8,192-token prompt (one chunk), each with its
+    # own selection (indexer rows per query) and causal window
+    Lp, r, k, H, Hi, T = 8192, 4, 512, 64, 64, 2048
+    wl = synth.custom_workload("prefill_8k", 6, [Lp], r, k, H, Hi, synth.FMT_FP8, synth.FMT_FP8,
+                               synth.FMT_FP8_PAGESPLIT)
+    keys = _lane(torch, cskv, wl, "index", cskv.FMT_FP8_PAGESPLIT, 128)
+    main = _lane(torch, cskv, wl, "main", cskv.FMT_FP8, 512)
+    rawwl = synth.custom_workload("prefill_8k_raw", 7, [Lp], 1, k, H, Hi, synth.FMT_FP8, synth.FMT_FP8,
+                                  synth.FMT_FP8)
+    raw = _lane(torch, cskv, rawwl, "main", cskv.FMT_FP8, 512)
+    rs = np.random.default_rng(8)
+    bf = torch.bfloat16
+    q = torch.from_numpy(rs.standard_normal((T, H, 512)).astype(np.float32)).to(bf).cuda()
+    q_idx = torch.from_numpy(rs.standard_normal((T, Hi, 128)).astype(np.float32)).to(bf).cuda()
+    w = torch.from_numpy(rs.uniform(0, 1, (T, Hi)).astype(np.float32)).cuda()
+    sink = torch.from_numpy(rs.standard_normal(H).astype(np.float32)).cuda()
+    posn = np.arange(Lp - T, Lp)
+    pos1 = torch.from_numpy((posn + 1).astype(np.int32)).cuda()
+    cs = torch.from_numpy(cskv.rope_table(posn)).cuda()
+    kq = cskv.PagedCache(keys.pool, keys.block_table[torch.zeros(T, dtype=torch.long, device=dev)].contiguous(),
+                         keys.fmt, keys.dim)
+    topk = torch.empty((T, k), dtype=torch.int32, device=dev)
+    ws_i = torch.empty(cskv.index_topk_workspace_size(T, Lp, r, Hi, k), dtype=torch.uint8, device=dev)
+    ws_a = torch.empty(cskv.sparse_decode_attn_workspace_size(T, H, Lp, r, k), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(q)
+    req_of = torch.zeros(T, dtype=torch.int32, device=dev)   # every query belongs to the one prompt
+
+    def step():
+        cskv.index_topk(q_idx, w, kq, pos1, r, k, Lp, topk_idx=topk, workspace=ws_i, want_scores=False)
+        cskv.sparse_prefill_attn(q, main, raw, pos1, topk, k, r, Lp, sink, cskv.DEFAULT_SCALE, cs, req_of=req_of,
+                                 out=out, workspace=ws_a)
+
+    ms, _, clocks = _graph_timed(torch, step, args.steps, args.warmup, flush)
+    st = cskv.device_status()
+    assert st == 0, st
+    m = statistics.mean(ms)
+    # bytes a prefill chunk must move at least: the queries in, the outputs out, the prompt's
+    # raw rows, entries and index keys once, the indexer queries
+    algo = T * H * 512 * 2 * 2 + Lp * 528 + (Lp // r) * (528 + 132) + T * Hi * 128 * 2
+    ach = algo / (m * 1e-3) / 1e9
+    return _line("prefill", "prefill chunk: prompt queries/s (2,048 queries of an 8,192-token prompt)",
+                 T / (m * 1e-3), "queries/s", m, True,
+                 {"workload": "prefill of an 8192-token prompt, last 2048 positions: ratio 4 (2048 entries), 64 "
+                              "indexer heads x 128 FP8 keys, top-512 per query, 64 heads x 512 over FP8-528 entries "
+                              "+ FP8 raw window rows; per step: index_topk (one row per query), sparse_prefill_attn",
+                  "l2": "flushed before every step"},
+                 {"kernel": "whole step", "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
+                  "frac": ach / peak, "peak_source": psrc, "algorithmic_bytes_per_launch": algo,
+                  "ms_per_launch": m, "traffic": None}, clocks, 2 + 2, args)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -503,6 +754,8 @@ def main():
     ap.add_argument("--impl", choices=["cskv", "reference"], default="cskv")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mode", choices=["decode", "csa2", "state", "prefill"], default="decode",
+                    help="decode: the benchmark; the others measure the rows built beyond it")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     rank = int(os.environ.get("RANK", "0"))
@@ -516,6 +769,10 @@ def main():
     import torch
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
+    if args.mode != "decode":
+        if rank == 0:
+            print(json.dumps(run_next_row(args)))
+        return
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
     res = run_gpu(args, rank, world)
