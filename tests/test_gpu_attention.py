@@ -118,3 +118,13 @@ def test_hca_128k_full_size_sampled():
         dec = codecs.decode_rows(codecs.encode_rows(vals, codecs.FMT_FP8), codecs.FMT_FP8, 512)
         ref = o_attn.request_attention(q_v[b], int(ctx[b]), wl.ratio, swa_dec[b], dec, None, sink, SCALE)
         check_attention(got[b], ref)
+
+
+def test_largest_selection_k2048():
+    """k = 2048: seventeen 128-key tiles per request, merged by the combine kernel."""
+    ctx = [4 * 3000 + 1, 4 * 2048, 4 * 100 + 3]
+    k = 2048
+    c = _case(ctx, 4, k, 64, codecs.FMT_FP8, codecs.FMT_FP8, True, seed=70)
+    got = _gpu(c, 4, k, codecs.FMT_FP8, max(ctx))
+    for b in range(len(ctx)):
+        check_attention(got[b], _oracle(c, b, 4))

@@ -144,3 +144,23 @@ def test_many_empty_requests_share_a_block():
             assert np.all(idx[b] == -1), b
         else:
             check_topk(idx[b], sc[b], indexer.quantize_queries(q_v[b]), w[b], cache.decoded[b], nb, k)
+
+
+@pytest.mark.parametrize("Hi,k", [(1, 2048), (64, 2048), (3, 1)])
+def test_extreme_k_and_heads(Hi, k):
+    """The largest selection (k = 2048), a single indexer head, and k = 1."""
+    ratio = 4
+    ctx = [4 * 9000 + 3, 4 * 2048, 4 * 2047 + 1, 4 * 5000]
+    n = [c // ratio for c in ctx]
+    rs = np.random.default_rng(60 + Hi + k)
+    q = rs.standard_normal((len(ctx), Hi, 128)).astype(np.float32)
+    w = rs.uniform(0, 1, (len(ctx), Hi)).astype(np.float32)
+    cache = HostPaged(codecs.FMT_FP8_PAGESPLIT, 128, n, seed=61)
+    for b, nb in enumerate(n):
+        cache.fill(b, rs.standard_normal((nb, 128)).astype(np.float32))
+    q_t, q_v = bf16_values(q)
+    idx, sc = _run(q_t, w, cache, ctx, ratio, k, max(ctx))
+    swaps = 0
+    for b, nb in enumerate(n):
+        swaps += check_topk(idx[b], sc[b], indexer.quantize_queries(q_v[b]), w[b], cache.decoded[b], nb, k)
+    assert swaps <= 1
