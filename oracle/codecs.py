@@ -11,7 +11,7 @@ Formats fixed by the pages:
   "The four compression axes"; the same FlashMLA record gives 288 B/token).
 * bf16 rows (the unquantised case of the tiny configuration).
 
-Readings where the pages are silent (all stated in the design doc):
+Readings where the pages are silent:
 
 * e8m0 scale: the smallest power of two 2^e with amax <= 448 * 2^e (rounded
   up, so no value saturates); byte = e + 127, e clamped to [-127, 127]; an

@@ -10,7 +10,7 @@ window in one softmax":
 k_j is one 128-d key shared by all indexer heads.  The selector keeps
 min(k, n) entries; missing slots are -1.
 
-Readings (the design doc lists them): larger score first, ties to the smaller
+Readings: larger score first, ties to the smaller
 entry index; the output is a set, returned here in ascending entry order.
 With FP8 keys the queries are coded e4m3 with one e8m0 scale per head, and
 the exact values of the coded operands enter the fp64 score.

@@ -62,7 +62,7 @@ def test_e2m1_tables_and_brute_force():
         best = np.flatnonzero(d == d.min())
         want = best[0] if len(best) == 1 else [b for b in best if b % 2 == 0][0]
         assert ci == want, (xi, ci, want)
-    # ties named in the design doc
+    # e2m1 midpoints: each rounds to the even neighbour
     ties = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], np.float32)
     assert list(codecs.e2m1_decode(codecs.e2m1_encode(ties))) == [0, 1, 1, 2, 2, 4, 4]
 
