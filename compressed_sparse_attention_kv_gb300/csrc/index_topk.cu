@@ -242,7 +242,7 @@ struct ScoreSmem {
   int nbv[kReqCache];              // visible entries of the first kReqCache requests
   WorkItem work[kWorkItems];       // this block's selection work, found before the scores
   int nwork;                       // -1: more than kWorkItems (found again after the barrier)
-  int T;
+  int T, cbin;
   uint32_t above, inT;
   uint32_t need, done, out;
   int last;
@@ -297,8 +297,10 @@ __device__ void grid_barrier(ScoreSmem* sm, uint32_t* counter, uint32_t target, 
 // T = the largest histogram bin with (entries in bins >= T) >= k; above = entries in
 // bins > T; inT = entries in bin T; T = -1 if the histogram holds fewer than k
 // entries.  Whole block (warp 0 works): the 256 coarse bins (sums of 16 fine bins),
-// then the 16 fine bins of the coarse bin that crosses k; two small loads.
-__device__ void threshold_bin(ScoreSmem* sm, const uint32_t* gh, int k) {
+// then the 16 fine bins of the coarse bin that crosses k, read from s_fine: the
+// request's 4,096 fine bins, whose cp.async copies the caller issued beside the
+// coarse loads (this function waits for every copy the thread has in flight).
+__device__ void threshold_bin(ScoreSmem* sm, const uint32_t* gh, int k, const uint32_t* s_fine) {
   const int lane = threadIdx.x;
   if (lane < 32) {
     // lane l owns coarse bins 255-8l .. 248-8l (from the top): two 16-byte loads
@@ -316,7 +318,7 @@ __device__ void threshold_bin(ScoreSmem* sm, const uint32_t* gh, int k) {
     }
     const unsigned hit = __ballot_sync(0xFFFFFFFFu, incl >= static_cast<uint32_t>(k));
     if (hit == 0) {
-      if (lane == 0) { sm->T = -1; sm->above = 0; sm->inT = 0; }
+      if (lane == 0) { sm->T = -1; sm->above = 0; sm->inT = 0; sm->cbin = -1; }
     } else if (lane == __ffs(hit) - 1) {
       uint32_t acc = incl - sum;
       int u = 255 - 8 * lane - 7;
@@ -325,22 +327,26 @@ __device__ void threshold_bin(ScoreSmem* sm, const uint32_t* gh, int k) {
         if (acc + loc[i] >= static_cast<uint32_t>(k)) { u = 255 - 8 * lane - i; break; }
         acc += loc[i];
       }
-      uint4 f[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) f[q] = __ldcg(reinterpret_cast<const uint4*>(gh + u * 16) + q);
-      const uint32_t fb[16] = {f[0].x, f[0].y, f[0].z, f[0].w, f[1].x, f[1].y, f[1].z, f[1].w,
-                               f[2].x, f[2].y, f[2].z, f[2].w, f[3].x, f[3].y, f[3].z, f[3].w};
-      int T = u * 16;
-      uint32_t inT = fb[0];
-#pragma unroll
-      for (int i = 15; i >= 0; --i) {
-        if (acc + fb[i] >= static_cast<uint32_t>(k)) { T = u * 16 + i; inT = fb[i]; break; }
-        acc += fb[i];
-      }
-      sm->T = T;
+      sm->cbin = u;   // the coarse bin that crosses k
       sm->above = acc;
-      sm->inT = inT;
     }
+  }
+  cp_async_wait_all();
+  __syncthreads();
+  if (threadIdx.x == 0 && sm->cbin >= 0) {
+    const int u = sm->cbin;
+    uint32_t acc = sm->above;
+    int T = u * 16;
+    uint32_t inT = s_fine[u * 16];
+#pragma unroll 1
+    for (int i = 15; i >= 0; --i) {
+      const uint32_t f = s_fine[u * 16 + i];
+      if (acc + f >= static_cast<uint32_t>(k)) { T = u * 16 + i; inT = f; break; }
+      acc += f;
+    }
+    sm->T = T;
+    sm->above = acc;
+    sm->inT = inT;
   }
   __syncthreads();
 }
@@ -980,11 +986,13 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
         for (long long x = threadIdx.x; x < (gs1 - gs0 + 3) / 4; x += blockDim.x)
           cp_async16(s_seg32 + 4 * x, smx + gs0 + 4 * x);
       }
-      threshold_bin(sm, ghist + size_t(b) * kHistStride, a.k);
-      if (pre) {
-        cp_async_wait_all();
-        __syncthreads();
-      }
+      // the request's fine histogram into the (free) stage ring, in flight with the
+      // coarse loads; threshold_bin waits for both tables
+      uint32_t* s_fine = reinterpret_cast<uint32_t*>(stages);
+      const uint32_t* ghb = ghist + size_t(b) * kHistStride;
+#pragma unroll 1
+      for (int x = threadIdx.x; x < kHistBins / 4; x += blockDim.x) cp_async16(s_fine + 4 * x, ghb + 4 * x);
+      threshold_bin(sm, ghb, a.k, s_fine);
       const int T = sm->T;
       const uint32_t above = sm->above;
       if (T < 0) {
