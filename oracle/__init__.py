@@ -11,10 +11,11 @@ Modules
 -------
 codecs     FP8 (e4m3 + e8m0 per 32), FP4 (e2m1 + e4m3 per 16) and bf16 row codecs
 expo       exp_own: the Cody-Waite exponential of the bit-exact compressor contract
-rope       partial-RoPE tables and rotations
+rope       partial-RoPE tables (plain and YaRN) and rotations
 compress   the gated per-channel pooling compressor (fp64 definition, fp32 contract)
 indexer    lightning-indexer scores and top-k selection
 attention  shared-KV sparse decode attention with window and sink
+decode_state  the decode step's compressor state ring and window row
 
 Precision: definitions run in fp64.  The one place that must be bit-exact
 against the GPU - the bytes the compressor writes - is computed in the fp32
