@@ -460,6 +460,29 @@ __device__ uint32_t ordered_list(ScoreSmem* sm, int n, Pred pred, uint16_t* list
   return tot;
 }
 
+// Exclusive scan of one 32-bit value per thread over the whole block; tot = the sum.
+__device__ __forceinline__ uint32_t block_scan_excl(ScoreSmem* sm, uint32_t v, uint32_t& tot) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += x;
+  }
+  if (lane == 31) sm->part[warp] = incl;
+  __syncthreads();
+  uint32_t pos = incl - v;
+  tot = 0;
+#pragma unroll 1
+  for (int w = 0; w < kScoreThreads / 32; ++w) {
+    const uint32_t x = sm->part[w];
+    if (w < warp) pos += x;
+    tot += x;
+  }
+  __syncthreads();
+  return pos;
+}
+
 template <int FP8>
 __global__ void __launch_bounds__(kLaunchBound, 1)
     index_score_kernel(const __grid_constant__ CUtensorMap tmap, const IndexArgs a) {
@@ -484,12 +507,16 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
   uint32_t* ctr_all = reinterpret_cast<uint32_t*>(a.ws + a.L.ctr);
   uint32_t* gbar = reinterpret_cast<uint32_t*>(a.ws + a.L.gbar);
 
-  // work range of this block: a contiguous run of the global tile sequence
+  // tiles of all requests; for small batches every thread sums them here, for large
+  // ones the block does, after the set-up barrier
   long long total = 0;
-  for (int b = 0; b < a.B; ++b) {
-    const int v = visible(a, b);
-    total += (v + kTileRows - 1) / kTileRows;
-    if (threadIdx.x == 0 && b < kReqCache) sm->nbv[b] = v;   // read after the set-up barrier
+  if (a.B <= kReqCache) {
+#pragma unroll 1
+    for (int b = 0; b < a.B; ++b) {
+      const int v = visible(a, b);
+      total += (v + kTileRows - 1) / kTileRows;
+      if (threadIdx.x == 0) sm->nbv[b] = v;   // read after the set-up barrier
+    }
   }
 
   if (threadIdx.x == 0) {
@@ -518,27 +545,73 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
   // this wait.  The scheduling producer first requests its first chunk's page ids
   // (block tables are inputs) and waits after that.
   const bool sched_thread = warp == 0 && lane == 0;
-  if (threadIdx.x == 32) {
-    // This block's selection work depends on the context lengths alone (inputs): one
-    // thread finds it now, beside the prep, instead of every thread after the barrier.
-    // (Producer 1 has nothing to do until producer 0's first hand-over.)
-    long long C = 0;
-    int nw = 0;
+  if (a.B <= kReqCache) {
+    if (threadIdx.x == 32) {
+      // This block's selection work depends on the context lengths alone (inputs): one
+      // thread finds it now, beside the prep, instead of every thread after the barrier.
+      // (Producer 1 has nothing to do until producer 0's first hand-over.)
+      long long C = 0;
+      int nw = 0;
 #pragma unroll 1
-    for (int b = 0; b < a.B; ++b) {
+      for (int b = 0; b < a.B; ++b) {
+        const long long tb = (sm->nbv[b] + kTileRows - 1) / kTileRows;
+        WorkItem wi;
+        const bool mine = block_range(blockIdx.x, gridDim.x, C, tb, total, wi.lo, wi.hi, wi.fb, wi.nbk, wi.per);
+        C += tb;
+        if (!mine) {
+          if (wi.fb > static_cast<int>(blockIdx.x)) break;   // the runs only move further right
+          continue;
+        }
+        wi.b = b;
+        if (nw < kWorkItems) sm->work[nw] = wi;
+        ++nw;
+      }
+      sm->nwork = nw <= kWorkItems ? nw : -1;
+    }
+  } else {
+    // Large batches: the requests' tile counts, their total, and this block's selection
+    // work are found by the whole block (each thread a contiguous range of requests,
+    // block scans for the prefixes), so the cost grows with the batch divided by the
+    // block, not with the batch.
+    const int per = (a.B + kScoreThreads - 1) / kScoreThreads;
+    const int rb0 = min(a.B, static_cast<int>(threadIdx.x) * per), rb1 = min(a.B, rb0 + per);
+    uint32_t cnt = 0;
+#pragma unroll 1
+    for (int b = rb0; b < rb1; ++b) {
+      const int v = visible(a, b);
+      cnt += static_cast<uint32_t>((v + kTileRows - 1) / kTileRows);
+      if (b < kReqCache) sm->nbv[b] = v;
+    }
+    uint32_t tot;
+    const uint32_t c0 = block_scan_excl(sm, cnt, tot);
+    total = tot;
+    long long C = c0;
+    uint32_t nmine = 0;
+#pragma unroll 1
+    for (int b = rb0; b < rb1; ++b) {
       const long long tb = (visible(a, b) + kTileRows - 1) / kTileRows;
       WorkItem wi;
-      const bool mine = block_range(blockIdx.x, gridDim.x, C, tb, total, wi.lo, wi.hi, wi.fb, wi.nbk, wi.per);
+      nmine += block_range(blockIdx.x, gridDim.x, C, tb, total, wi.lo, wi.hi, wi.fb, wi.nbk, wi.per) ? 1u : 0u;
       C += tb;
-      if (!mine) {
-        if (wi.fb > static_cast<int>(blockIdx.x)) break;   // the runs only move further right
-        continue;
-      }
-      wi.b = b;
-      if (nw < kWorkItems) sm->work[nw] = wi;
-      ++nw;
     }
-    sm->nwork = nw <= kWorkItems ? nw : -1;
+    uint32_t nw;
+    uint32_t pos = block_scan_excl(sm, nmine, nw);
+    if (nmine) {
+      C = c0;
+#pragma unroll 1
+      for (int b = rb0; b < rb1; ++b) {
+        const long long tb = (visible(a, b) + kTileRows - 1) / kTileRows;
+        WorkItem wi;
+        if (block_range(blockIdx.x, gridDim.x, C, tb, total, wi.lo, wi.hi, wi.fb, wi.nbk, wi.per)) {
+          wi.b = b;
+          if (pos < static_cast<uint32_t>(kWorkItems)) sm->work[pos] = wi;
+          ++pos;
+        }
+        C += tb;
+      }
+    }
+    if (threadIdx.x == 0) sm->nwork = nw <= static_cast<uint32_t>(kWorkItems) ? static_cast<int>(nw) : -1;
+    __syncthreads();
   }
   if (!sched_thread) grid_dep_wait();
 
