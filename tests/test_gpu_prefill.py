@@ -63,3 +63,32 @@ def test_prefill_queries_of_two_prompts(main_fmt, win_fmt):
             ring[p % 128] = raw.decoded[b][p]
         ref = o_attn.request_attention(q_v[i], t + 1, ratio, ring, main.decoded[b], sel, sink, SCALE)
         check_attention(got[i], ref, fp4=main_fmt == codecs.FMT_FP4)
+
+
+def test_hca_prefill_reads_every_visible_entry():
+    """HCA prefill (ratio 128, no selection): each query attends its causal window and
+    every entry complete before it (j < floor((t + 1) / 128))."""
+    rs = np.random.default_rng(45)
+    ratio, H = 128, 16
+    L = [128 * 9 + 40]
+    n = [L[0] // ratio]
+    raw = HostPaged(codecs.FMT_FP8, 512, L, seed=4)
+    main = HostPaged(codecs.FMT_FP8, 512, n, seed=5)
+    raw.fill(0, rs.standard_normal((L[0], 512)).astype(np.float32))
+    main.fill(0, rs.standard_normal((n[0], 512)).astype(np.float32))
+    pos = np.array([0, 100, 127, 128, 255, 256, 700, L[0] - 1], np.int64)
+    T = len(pos)
+    pos1 = (pos + 1).astype(np.int32)
+    q_t, q_v = bf16_values(rs.standard_normal((T, H, 512)).astype(np.float32))
+    sink = rs.standard_normal(H).astype(np.float32)
+    out = cskv.sparse_prefill_attn(q_t.cuda(), main.to_device(), raw.to_device(), cuda(pos1), None, 0, ratio,
+                                   L[0], cuda(sink), SCALE, cuda(cskv.rope_table(pos)),
+                                   req_of=cuda(np.zeros(T, np.int32)))
+    assert cskv.device_status() == 0
+    got = out.float().cpu().numpy()
+    for i, t in enumerate(pos):
+        ring = np.zeros((128, 512))
+        for p in range(max(0, int(t) - 127), int(t) + 1):
+            ring[p % 128] = raw.decoded[0][p]
+        ref = o_attn.request_attention(q_v[i], int(t) + 1, ratio, ring, main.decoded[0], None, sink, SCALE)
+        check_attention(got[i], ref)
