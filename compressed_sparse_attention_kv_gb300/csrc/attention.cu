@@ -170,8 +170,11 @@ struct AttnSmem {
 // (r, l) = dims 16l .. 16l+15 of row r; each thread takes 8 items of dims 0-255 (their
 // outputs in the lower half, their codes in the upper half), then reads the codes of
 // its 8 items of dims 256-511 before any thread overwrites the upper half.
-template <int FMT>
-__device__ __forceinline__ void dequant_tile(uint8_t* ktile, const uint8_t* stage, const AttnSmem* sm) {
+// mid() runs once the first half (dims 0-255) is in place and fenced for the tensor
+// core, before the second half is written: the first half's products may start.
+template <int FMT, class Mid>
+__device__ __forceinline__ void dequant_tile(uint8_t* ktile, const uint8_t* stage, const AttnSmem* sm,
+                                             Mid&& mid) {
   constexpr bool kFp8 = FMT == CSKV_FMT_FP8_E4M3_E8M0_B32;
   auto raw_of = [&](int r, int l) -> RowBytes {
     RowBytes rb;
@@ -208,7 +211,10 @@ __device__ __forceinline__ void dequant_tile(uint8_t* ktile, const uint8_t* stag
     const int x = threadIdx.x + u * kAttnThreads;
     rb[u] = raw_of(x >> 4, 16 + (x & 15));
   }
+  fence_proxy_async_smem();
+  tc_fence_before();
   __syncthreads();
+  mid();
 #pragma unroll
   for (int u = 0; u < kPer; ++u) {
     const int x = threadIdx.x + u * kAttnThreads;
@@ -346,27 +352,38 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
       *pq = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
+  // ---- S^T = K Q^T : M = 128 keys, N = Nq, K = 512, issued by one thread in two
+  // halves of K: dims 0-255 as soon as the dequantisation has written them (the tensor
+  // core works while the second half is dequantised), then dims 256-511
+  auto issue_s = [&](int kk0, int kk1, bool last) {
+    if (threadIdx.x == 0) {
+      tc_fence_after();
+      const uint32_t id = make_idesc(1, 1, 0, 0, 128, 0) | (static_cast<uint32_t>(Nq >> 3) << 17);
+      const uint32_t ka = smem_u32(ktile), qa = smem_u32(qtile);
+#pragma unroll 1
+      for (int kk = kk0; kk < kk1; ++kk) {
+        const int c = kk >> 2, o = (kk & 3) * 32;
+        mma_f16(sm->tmem_base, smem_desc_sw128(ka + c * (kKeys * 128) + o, 16, 1024),
+                smem_desc_sw128(qa + c * (Nq * 128) + o, 16, 1024), id, kk > 0);
+      }
+      if (last) mma_commit(&sm->bar_s);
+    }
+  };
   // ---- dequantise FP8 / FP4 rows in place
-  if (row_fmt == CSKV_FMT_FP8_E4M3_E8M0_B32) dequant_tile<CSKV_FMT_FP8_E4M3_E8M0_B32>(ktile, stage, sm);
-  else if (row_fmt == CSKV_FMT_FP4_E2M1_E4M3_B16) dequant_tile<CSKV_FMT_FP4_E2M1_E4M3_B16>(ktile, stage, sm);
+  int kk_done = 0;
+  if (row_fmt == CSKV_FMT_FP8_E4M3_E8M0_B32) {
+    dequant_tile<CSKV_FMT_FP8_E4M3_E8M0_B32>(ktile, stage, sm, [&]() { issue_s(0, 16, false); });
+    kk_done = 16;
+  } else if (row_fmt == CSKV_FMT_FP4_E2M1_E4M3_B16) {
+    dequant_tile<CSKV_FMT_FP4_E2M1_E4M3_B16>(ktile, stage, sm, [&]() { issue_s(0, 16, false); });
+    kk_done = 16;
+  }
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm->tmem_base;
-
-  // ---- S^T = K Q^T : M = 128 keys, N = Nq, K = 512
-  if (threadIdx.x == 0) {
-    const uint32_t id = make_idesc(1, 1, 0, 0, 128, 0) | (static_cast<uint32_t>(Nq >> 3) << 17);
-    const uint32_t ka = smem_u32(ktile), qa = smem_u32(qtile);
-#pragma unroll
-    for (int kk = 0; kk < 32; ++kk) {
-      const int c = kk >> 2, o = (kk & 3) * 32;
-      mma_f16(tmem, smem_desc_sw128(ka + c * (kKeys * 128) + o, 16, 1024),
-              smem_desc_sw128(qa + c * (Nq * 128) + o, 16, 1024), id, kk > 0);
-    }
-    mma_commit(&sm->bar_s);
-  }
+  issue_s(kk_done, 32, true);
   mbar_wait(&sm->bar_s, 0, kDefaultSpinLimit);
   tc_fence_after();
 
