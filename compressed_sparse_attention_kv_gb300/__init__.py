@@ -9,11 +9,16 @@ built raises.
 Calls (same names as the C ABI, without the ``cskv_`` prefix):
 
     compress(...)            gated per-channel pooling compressor -> cache rows
+    compress_many(...)       several compressor jobs in one launch
+    decode_append(...)       one decode step's compressor state ring and window update
     index_topk(...)          lightning-indexer scores + top-k selection
     sparse_decode_attn(...)  shared-KV attention over window + compressed entries
+    sparse_prefill_attn(...) the same attention for many prompt queries
+    decode_layer(...)        one layer's decode step, host buffers in and out
     encode_rows(...)         code rows of values into a cache format
 """
 
+import ctypes
 import math
 
 import numpy as np
@@ -180,8 +185,15 @@ def compress_many(jobs, stream=None):
     """Several compressor jobs in one launch.  Each job is a dict of compress()'s
     arguments (kv, gate, ape, ratio, overlap, out, req, first_entry and, optionally,
     prev_kv, prev_gate, norm_w, eps, rope_cs); same results as separate calls."""
+    arr = _compress_jobs(jobs)
+    st = _lib.lib().cskv_compress_many(arr, len(jobs), _stream(stream))
+    _check(st, "cskv_compress_many")
+
+
+def _compress_jobs(jobs):
+    """ctypes array of struct cskv_compress_job for compress()-style job dicts."""
     import torch
-    arr = (_lib.CompressJob * len(jobs))()
+    arr = (_lib.CompressJob * max(1, len(jobs)))()
     for i, j in enumerate(jobs):
         kv, gate = j["kv"], j["gate"]
         for t, n in ((kv, "kv"), (gate, "gate"), (j.get("prev_kv"), "prev_kv"), (j.get("prev_gate"), "prev_gate")):
@@ -195,8 +207,7 @@ def compress_many(jobs, stream=None):
                                   _ptr(j.get("ape")), _ptr(j.get("norm_w")), float(j.get("eps", 1e-6)),
                                   _ptr(j.get("rope_cs")), S, T, int(j["ratio"]), int(bool(j["overlap"])), dim,
                                   j["req"].data_ptr(), j["first_entry"].data_ptr(), j["out"].desc())
-    st = _lib.lib().cskv_compress_many(arr, len(jobs), _stream(stream))
-    _check(st, "cskv_compress_many")
+    return arr
 
 
 def decode_state(B, ratio, overlap, dim, device="cuda"):
@@ -321,6 +332,57 @@ def sparse_prefill_attn(q, main_kv, window, pos1, topk_idx, k, ratio, max_ctx_le
                                              _stream(stream))
     _check(st, "cskv_sparse_prefill_attn")
     return out
+
+
+def decode_layer(jobs, q_idx, w, keys, q, main_kv, swa, swa_fmt, ctx_len, k, ratio, max_ctx_len, sink,
+                 softmax_scale, q_rope_cs, topk_idx=None, out=None, index_workspace=None, attn_workspace=None,
+                 h_in=None, d_in=None, h_out=None, stream=None):
+    """One decode step of one layer in one call (cskv_decode_layer): h_in (host uint8) is
+    copied into d_in (device uint8, which the other tensors may view), then compress_many(jobs)
+    (jobs may be empty), index_topk (skipped when q_idx is None: HCA) and sparse_decode_attn
+    run, and out is copied into h_out (host, out's dtype and size or less) last.  Host
+    buffers should be pinned.  Returns (out, topk_idx); h_out holds the output once the
+    stream has synchronised."""
+    import torch
+    for t, dt, n in ((q_idx, torch.bfloat16, "q_idx"), (w, torch.float32, "w"), (q, torch.bfloat16, "q"),
+                     (swa, torch.uint8, "swa"), (ctx_len, torch.int32, "ctx_len"), (sink, torch.float32, "sink"),
+                     (q_rope_cs, torch.float32, "q_rope_cs"), (d_in, torch.uint8, "d_in")):
+        _need(t, dt, n)
+    _need(h_in, torch.uint8, "h_in", device=False)
+    _need(h_out, None, "h_out", device=False)
+    for t, n in ((h_in, "h_in"), (h_out, "h_out")):
+        if t is not None and t.is_cuda:
+            raise ValueError("%s must be a host tensor" % n)
+    if h_in is not None and (d_in is None or d_in.numel() < h_in.numel()):
+        raise ValueError("d_in must be a device buffer at least as large as h_in")
+    B, H, _ = q.shape
+    dev = q.device
+    csa = q_idx is not None
+    Hi = q_idx.shape[1] if csa else 0
+    if out is None:
+        out = torch.empty_like(q)
+    if csa and topk_idx is None:
+        topk_idx = torch.empty((B, k), dtype=torch.int32, device=dev)
+    if csa and index_workspace is None:
+        index_workspace = torch.empty(index_topk_workspace_size(B, max_ctx_len, ratio, Hi, k), dtype=torch.uint8,
+                                      device=dev)
+    kk = int(k) if csa else 0
+    if attn_workspace is None:
+        attn_workspace = torch.empty(sparse_decode_attn_workspace_size(B, H, max_ctx_len, ratio, kk),
+                                     dtype=torch.uint8, device=dev)
+    arr = _compress_jobs(jobs)
+    empty = _lib.Paged(None, None, 0, 0, 0, 0, 128)
+    a = _lib.DecodeLayerArgs(
+        ctypes.cast(arr, ctypes.POINTER(_lib.CompressJob)) if jobs else None, len(jobs), _ptr(q_idx), _ptr(w), keys.desc() if csa else empty, Hi, kk,
+        _ptr(topk_idx) if csa else None, _ptr(index_workspace) if csa else None,
+        index_workspace.numel() if csa else 0, q.data_ptr(), main_kv.desc(), swa.data_ptr(), int(swa_fmt),
+        ctx_len.data_ptr(), int(ratio), int(max_ctx_len), _ptr(sink), float(softmax_scale), q_rope_cs.data_ptr(),
+        B, H, out.data_ptr(), attn_workspace.data_ptr(), attn_workspace.numel(),
+        _ptr(h_in), _ptr(d_in), h_in.numel() if h_in is not None else 0,
+        _ptr(h_out), h_out.numel() * h_out.element_size() if h_out is not None else 0)
+    st = _lib.lib().cskv_decode_layer(ctypes.byref(a), _stream(stream))
+    _check(st, "cskv_decode_layer")
+    return out, topk_idx
 
 
 DEFAULT_SCALE = 1.0 / math.sqrt(512.0)

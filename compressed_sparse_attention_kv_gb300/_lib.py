@@ -67,6 +67,42 @@ class DecodeJob(ctypes.Structure):
     ]
 
 
+class DecodeLayerArgs(ctypes.Structure):
+    """struct cskv_decode_layer_args (one decode step of one layer, host to host)."""
+    _fields_ = [
+        ("jobs", ctypes.POINTER(CompressJob)),
+        ("njobs", c_int32),
+        ("q_idx", c_void_p),
+        ("w", c_void_p),
+        ("keys", Paged),
+        ("Hi", c_int32),
+        ("k", c_int32),
+        ("topk_idx", c_void_p),
+        ("index_workspace", c_void_p),
+        ("index_workspace_bytes", c_size_t),
+        ("q", c_void_p),
+        ("main_kv", Paged),
+        ("swa", c_void_p),
+        ("swa_fmt", c_int32),
+        ("ctx_len", c_void_p),
+        ("ratio", c_int32),
+        ("max_ctx_len", c_int32),
+        ("sink", c_void_p),
+        ("softmax_scale", c_float),
+        ("q_rope_cs", c_void_p),
+        ("B", c_int32),
+        ("H", c_int32),
+        ("out", c_void_p),
+        ("attn_workspace", c_void_p),
+        ("attn_workspace_bytes", c_size_t),
+        ("h_in", c_void_p),
+        ("d_in", c_void_p),
+        ("in_bytes", c_size_t),
+        ("h_out", c_void_p),
+        ("out_bytes", c_size_t),
+    ]
+
+
 # name -> (restype, argtypes); every symbol include/cskv.h declares
 SIGNATURES = {
     "cskv_row_bytes": (c_size_t, [c_int32, c_int32]),
@@ -94,6 +130,7 @@ SIGNATURES = {
     "cskv_sparse_prefill_attn": (c_int32, [c_void_p, Paged, Paged, c_void_p, c_void_p, c_void_p, c_int32,
                                            c_int32, c_int32, c_void_p, c_float, c_void_p, c_int32, c_int32,
                                            c_void_p, c_void_p, c_size_t, c_void_p]),
+    "cskv_decode_layer": (c_int32, [ctypes.POINTER(DecodeLayerArgs), c_void_p]),
 }
 
 _lib = None

@@ -207,7 +207,7 @@ int32_t cskv_compress(const void* kv, const void* gate, const void* prev_kv, con
                                      static_cast<cudaStream_t>(stream)));
 }
 
-int32_t cskv_compress_many(const cskv_compress_job* jobs, int32_t njobs, void* stream) {
+static int32_t compress_many_check(const cskv_compress_job* jobs, int32_t njobs) {
   if (jobs == nullptr || njobs < 1 || njobs > 4) return CSKV_ERR_INVALID;
   for (int32_t j = 0; j < njobs; ++j) {
     const cskv_compress_job& q = jobs[j];
@@ -215,6 +215,12 @@ int32_t cskv_compress_many(const cskv_compress_job* jobs, int32_t njobs, void* s
                                       q.S, q.T, q.ratio, q.overlap, q.dim, q.req, q.first_entry, q.out);
     if (st != CSKV_OK) return st;
   }
+  return CSKV_OK;
+}
+
+int32_t cskv_compress_many(const cskv_compress_job* jobs, int32_t njobs, void* stream) {
+  const int32_t st = compress_many_check(jobs, njobs);
+  if (st != CSKV_OK) return st;
   return cuda_status(launch_compress_many(jobs, njobs, static_cast<cudaStream_t>(stream)));
 }
 
@@ -250,10 +256,9 @@ size_t cskv_index_topk_workspace_size(int32_t B, int32_t max_ctx_len, int32_t ra
   return index_workspace_bytes(B, max_ctx_len / ratio, Hi, k);
 }
 
-int32_t cskv_index_topk(const void* q_idx, const float* w, cskv_paged keys, const int32_t* ctx_len,
-                        int32_t B, int32_t Hi, int32_t ratio, int32_t k, int32_t max_ctx_len,
-                        int32_t* topk_idx, float* topk_score, void* workspace,
-                        size_t workspace_bytes, void* stream) {
+static int32_t index_check(const void* q_idx, const float* w, const cskv_paged& keys, const int32_t* ctx_len,
+                           int32_t B, int32_t Hi, int32_t ratio, int32_t k, int32_t max_ctx_len,
+                           const int32_t* topk_idx, const void* workspace, size_t workspace_bytes) {
   if (q_idx == nullptr || w == nullptr || ctx_len == nullptr || topk_idx == nullptr)
     return CSKV_ERR_INVALID;
   if (B < 1 || Hi < 1 || ratio < 1 || k < 1 || k > 2048 || max_ctx_len < 0) return CSKV_ERR_INVALID;
@@ -265,6 +270,16 @@ int32_t cskv_index_topk(const void* q_idx, const float* w, cskv_paged keys, cons
   const size_t need = index_workspace_bytes(B, max_ctx_len / ratio, Hi, k);
   if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < need)
     return CSKV_ERR_INVALID;
+  return CSKV_OK;
+}
+
+int32_t cskv_index_topk(const void* q_idx, const float* w, cskv_paged keys, const int32_t* ctx_len,
+                        int32_t B, int32_t Hi, int32_t ratio, int32_t k, int32_t max_ctx_len,
+                        int32_t* topk_idx, float* topk_score, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  const int32_t st = index_check(q_idx, w, keys, ctx_len, B, Hi, ratio, k, max_ctx_len, topk_idx, workspace,
+                                 workspace_bytes);
+  if (st != CSKV_OK) return st;
   return cuda_status(launch_index_topk(q_idx, w, keys, ctx_len, B, Hi, ratio, k, max_ctx_len,
                                        topk_idx, topk_score, workspace,
                                        static_cast<cudaStream_t>(stream)));
@@ -295,11 +310,10 @@ size_t cskv_sparse_decode_attn_workspace_size(int32_t B, int32_t H, int32_t max_
   return attn_workspace_bytes(B, H, max_ctx_len, ratio, k);
 }
 
-int32_t cskv_sparse_decode_attn(const void* q, cskv_paged main_kv, const void* swa, int32_t swa_fmt,
-                                const int32_t* ctx_len, const int32_t* topk_idx, int32_t k,
-                                int32_t ratio, int32_t max_ctx_len, const float* sink,
-                                float softmax_scale, const float* q_rope_cs, int32_t B, int32_t H,
-                                void* out, void* workspace, size_t workspace_bytes, void* stream) {
+static int32_t attn_check(const void* q, const cskv_paged& main_kv, const void* swa, int32_t swa_fmt,
+                          const int32_t* ctx_len, const int32_t* topk_idx, int32_t k, int32_t ratio,
+                          int32_t max_ctx_len, float softmax_scale, const float* q_rope_cs, int32_t B,
+                          int32_t H, const void* out, const void* workspace, size_t workspace_bytes) {
   if (q == nullptr || swa == nullptr || ctx_len == nullptr || q_rope_cs == nullptr || out == nullptr)
     return CSKV_ERR_INVALID;
   if (B < 1 || H < 1 || H > 128 || ratio < 1 || max_ctx_len < 0) return CSKV_ERR_INVALID;
@@ -314,6 +328,17 @@ int32_t cskv_sparse_decode_attn(const void* q, cskv_paged main_kv, const void* s
   const size_t need = attn_workspace_bytes(B, H, max_ctx_len, ratio, topk_idx ? k : 0);
   if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < need)
     return CSKV_ERR_INVALID;
+  return CSKV_OK;
+}
+
+int32_t cskv_sparse_decode_attn(const void* q, cskv_paged main_kv, const void* swa, int32_t swa_fmt,
+                                const int32_t* ctx_len, const int32_t* topk_idx, int32_t k,
+                                int32_t ratio, int32_t max_ctx_len, const float* sink,
+                                float softmax_scale, const float* q_rope_cs, int32_t B, int32_t H,
+                                void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  const int32_t st = attn_check(q, main_kv, swa, swa_fmt, ctx_len, topk_idx, k, ratio, max_ctx_len, softmax_scale,
+                                q_rope_cs, B, H, out, workspace, workspace_bytes);
+  if (st != CSKV_OK) return st;
   return cuda_status(launch_sparse_decode_attn(q, main_kv, swa, swa_fmt, ctx_len, topk_idx,
                                                topk_idx ? k : 0, ratio, max_ctx_len, sink,
                                                softmax_scale, q_rope_cs, B, H, out, workspace,
@@ -339,6 +364,50 @@ int32_t cskv_sparse_prefill_attn(const void* q, cskv_paged main_kv, cskv_paged w
   return cuda_status(launch_sparse_prefill_attn(q, main_kv, window, req_of, pos1, topk_idx, topk_idx ? k : 0,
                                                 ratio, max_ctx_len, sink, softmax_scale, q_rope_cs, T, H, out,
                                                 workspace, static_cast<cudaStream_t>(stream)));
+}
+
+int32_t cskv_decode_layer(const cskv_decode_layer_args* args, void* stream) {
+  if (args == nullptr) return CSKV_ERR_INVALID;
+  const cskv_decode_layer_args& a = *args;
+  // every stage's arguments before anything is enqueued
+  if (a.njobs < 0 || a.njobs > 4) return CSKV_ERR_INVALID;
+  if (a.njobs > 0) {
+    const int32_t st = compress_many_check(a.jobs, a.njobs);
+    if (st != CSKV_OK) return st;
+  }
+  const bool csa = a.q_idx != nullptr;
+  if (csa) {
+    const int32_t st = index_check(a.q_idx, a.w, a.keys, a.ctx_len, a.B, a.Hi, a.ratio, a.k, a.max_ctx_len,
+                                   a.topk_idx, a.index_workspace, a.index_workspace_bytes);
+    if (st != CSKV_OK) return st;
+  }
+  {
+    const int32_t st = attn_check(a.q, a.main_kv, a.swa, a.swa_fmt, a.ctx_len, csa ? a.topk_idx : nullptr, a.k,
+                                  a.ratio, a.max_ctx_len, a.softmax_scale, a.q_rope_cs, a.B, a.H, a.out,
+                                  a.attn_workspace, a.attn_workspace_bytes);
+    if (st != CSKV_OK) return st;
+  }
+  if (a.in_bytes > 0 && (a.h_in == nullptr || a.d_in == nullptr)) return CSKV_ERR_INVALID;
+  if (a.out_bytes > 0 && (a.h_out == nullptr || a.out_bytes > size_t(a.B) * a.H * 512 * 2)) return CSKV_ERR_INVALID;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (a.in_bytes > 0) {
+    const cudaError_t e = cudaMemcpyAsync(a.d_in, a.h_in, a.in_bytes, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return CSKV_ERR_CUDA;
+  }
+  if (a.njobs > 0 && launch_compress_many(a.jobs, a.njobs, st) != cudaSuccess) return CSKV_ERR_CUDA;
+  if (csa && launch_index_topk(a.q_idx, a.w, a.keys, a.ctx_len, a.B, a.Hi, a.ratio, a.k, a.max_ctx_len,
+                               a.topk_idx, nullptr, a.index_workspace, st) != cudaSuccess)
+    return CSKV_ERR_CUDA;
+  const int32_t kk = csa ? a.k : 0;
+  if (launch_sparse_decode_attn(a.q, a.main_kv, a.swa, a.swa_fmt, a.ctx_len, csa ? a.topk_idx : nullptr, kk,
+                                a.ratio, a.max_ctx_len, a.sink, a.softmax_scale, a.q_rope_cs, a.B, a.H, a.out,
+                                a.attn_workspace, st) != cudaSuccess)
+    return CSKV_ERR_CUDA;
+  if (a.out_bytes > 0) {
+    const cudaError_t e = cudaMemcpyAsync(a.h_out, a.out, a.out_bytes, cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) return CSKV_ERR_CUDA;
+  }
+  return CSKV_OK;
 }
 
 }  // extern "C"

@@ -371,6 +371,67 @@ CSKV_API int32_t cskv_sparse_prefill_attn(const void* q, cskv_paged main_kv, csk
                                           const float* q_rope_cs, int32_t T, int32_t H, void* out,
                                           void* workspace, size_t workspace_bytes, void* stream);
 
+/* ------------------------------------------------------------------------
+ * cskv_decode_layer: one decode step of one compressed-attention layer, from
+ * host memory to host memory ("DeepSeek-V4 deep dive", section 4.1 for the
+ * entries a step completes, section 5.2 for the indexer, sections 3.4 and 5.3
+ * for the attention; section 6.1: an HCA layer has no indexer).  In stream
+ * order, on `stream`:
+ *   1. in_bytes bytes from h_in (host) to d_in (device), if in_bytes > 0;
+ *   2. cskv_compress_many(jobs, njobs), if njobs > 0 (the entries whose blocks
+ *      complete at this step; written before they are read below);
+ *   3. cskv_index_topk(q_idx, w, keys, ctx_len, B, Hi, ratio, k, max_ctx_len,
+ *      topk_idx, NULL, index_workspace, ...), if q_idx != NULL (CSA); with
+ *      q_idx == NULL (HCA) the attention reads every visible entry;
+ *   4. cskv_sparse_decode_attn(q, main_kv, swa, swa_fmt, ctx_len, topk_idx or
+ *      NULL, k, ratio, max_ctx_len, sink, softmax_scale, q_rope_cs, B, H, out,
+ *      attn_workspace, ...);
+ *   5. out_bytes bytes from out (device) to h_out (host), if out_bytes > 0
+ *      (at most B * H * 512 * 2, the bf16 output).
+ * The device pointers of steps 2-4 may point into d_in: the copy of step 1 is
+ * ordered before every kernel that reads them.  Each stage takes exactly the
+ * arguments, layouts, results and bits of its own entry point above.
+ * Ownership: every buffer is the caller's; h_in and h_out should be page-locked
+ * (cudaHostAlloc / cudaHostRegister) for the copies to be asynchronous and to be
+ * capturable into a CUDA graph.  The call returns once everything is enqueued;
+ * h_out holds the output after the stream has synchronised.
+ * Errors: the arguments of every stage are checked before anything is
+ * enqueued (CSKV_ERR_INVALID / CSKV_ERR_UNSUPPORTED as the stage's own entry
+ * point would return, and CSKV_ERR_INVALID for a NULL h_in / d_in / h_out with
+ * a non-zero byte count or an out_bytes above the output's size); a CUDA error
+ * while enqueueing returns CSKV_ERR_CUDA and leaves the later stages unqueued.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  const cskv_compress_job* jobs; /* njobs entries (0..4); NULL when njobs == 0 */
+  int32_t njobs;
+  const void* q_idx;             /* bf16 [B, Hi, 128]; NULL: HCA (no indexer) */
+  const float* w;                /* fp32 [B, Hi] */
+  cskv_paged keys;               /* index keys (read only when q_idx != NULL) */
+  int32_t Hi, k;                 /* indexer heads; entries selected (and read) per query */
+  int32_t* topk_idx;             /* int32 [B, k] device, the selection (written) */
+  void* index_workspace;
+  size_t index_workspace_bytes;
+  const void* q;                 /* bf16 [B, H, 512] */
+  cskv_paged main_kv;
+  const void* swa;               /* [B, 128, row_bytes(swa_fmt, 512)] window ring */
+  int32_t swa_fmt;
+  const int32_t* ctx_len;        /* int32 [B] */
+  int32_t ratio, max_ctx_len;
+  const float* sink;             /* fp32 [H] or NULL */
+  float softmax_scale;
+  const float* q_rope_cs;        /* fp32 [B, 32, 2] */
+  int32_t B, H;
+  void* out;                     /* bf16 [B, H, 512] device */
+  void* attn_workspace;
+  size_t attn_workspace_bytes;
+  const void* h_in;              /* host source of step 1 */
+  void* d_in;                    /* device destination of step 1 */
+  size_t in_bytes;
+  void* h_out;                   /* host destination of step 5 */
+  size_t out_bytes;
+} cskv_decode_layer_args;
+CSKV_API int32_t cskv_decode_layer(const cskv_decode_layer_args* args, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

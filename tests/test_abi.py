@@ -26,7 +26,7 @@ def _declared():
 def test_header_and_binding_agree():
     from compressed_sparse_attention_kv_gb300 import _lib
     names = _declared()
-    assert len(names) == 16
+    assert len(names) == 17
     assert sorted(_lib.SIGNATURES) == names
 
 
@@ -108,6 +108,29 @@ def test_invalid_arguments_launch_nothing(lib):
                                        1, 64, fake, fake, 1 << 30, None) == 1    # FP4 window not allowed
     assert lib.cskv_sparse_decode_attn(fake, main, fake, 1, fake, None, 0, 128, 4096, None, 0.04, fake,
                                        1, 129, fake, fake, 1 << 30, None) == 1   # H > 128
+    # the layer step checks every stage before it enqueues anything
+    from compressed_sparse_attention_kv_gb300._lib import DecodeLayerArgs
+    assert lib.cskv_decode_layer(None, None) == 1
+    la = DecodeLayerArgs()
+    la.q, la.main_kv, la.swa, la.swa_fmt, la.ctx_len = 4096, main, 4096, 1, 4096
+    la.ratio, la.max_ctx_len, la.softmax_scale, la.q_rope_cs, la.B, la.H = 128, 4096, 0.04, 4096, 1, 64
+    la.out, la.attn_workspace, la.attn_workspace_bytes = 4096, 4096, 1 << 30
+    la.njobs = 5
+    assert lib.cskv_decode_layer(ctypes.byref(la), None) == 1                  # more than 4 jobs
+    la.njobs = 1
+    assert lib.cskv_decode_layer(ctypes.byref(la), None) == 1                  # jobs NULL
+    la.njobs = 0
+    la.H = 129
+    assert lib.cskv_decode_layer(ctypes.byref(la), None) == 1                  # the attention's H > 128
+    la.H = 64
+    la.q_idx, la.w, la.keys, la.Hi, la.k, la.topk_idx = 4096, 4096, keys, 65, 512, 4096
+    la.index_workspace, la.index_workspace_bytes = 4096, 1 << 30
+    assert lib.cskv_decode_layer(ctypes.byref(la), None) == 2                  # the indexer's > 64 heads
+    la.Hi = 4
+    la.in_bytes = 1024
+    assert lib.cskv_decode_layer(ctypes.byref(la), None) == 1                  # input bytes without buffers
+    la.in_bytes, la.h_out, la.out_bytes = 0, 4096, 64 * 512 * 2 + 2
+    assert lib.cskv_decode_layer(ctypes.byref(la), None) == 1                  # more bytes out than the output
 
 
 def test_binding_refuses_without_library(tmp_path, monkeypatch):
