@@ -1,6 +1,6 @@
-// C-ABI front end of libcskv: synchronous argument checks, then launches.
-// Nothing here allocates device memory or synchronises (cskv_device_status
-// excepted).
+// C-ABI front end of libcskv: synchronous argument checks, then launches (and the
+// host staging copy of cskv_decode_layer).  Nothing here allocates device memory or
+// synchronises (cskv_device_status excepted).
 #include <atomic>
 #include <cstdint>
 #include <mutex>
@@ -104,6 +104,49 @@ static bool paged_ok(const cskv_paged& c, int dim, unsigned formats) {
   if (c.num_pages <= 0) return false;
   if (c.block_table != nullptr && (c.max_pages <= 0 || !aligned(c.block_table, 4))) return false;
   return true;
+}
+
+// Host <-> device staging of a layer step's inputs and output.  Page-locked host
+// memory is addressable from kernels on a unified-address system (over the coherent
+// CPU-GPU link on Grace machines), so the copy runs on the SMs: a grid-stride loop of
+// 16-byte loads and stores, one or two per thread, all in flight together, in place of a
+// copy-engine transfer whose set-up dominates at a megabyte.  Other host memory is
+// copied with cudaMemcpyAsync.
+__global__ void __launch_bounds__(256) stage_copy_kernel(uint8_t* dst, const uint8_t* src, size_t n, int vec) {
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  const size_t t0 = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const size_t n16 = vec ? n >> 4 : 0;
+  for (size_t i = t0; i < n16; i += stride)
+    reinterpret_cast<uint4*>(dst)[i] = reinterpret_cast<const uint4*>(src)[i];
+  for (size_t i = (n16 << 4) + t0; i < n; i += stride) dst[i] = src[i];
+}
+
+// The address a kernel uses for host pointer p, or nullptr if p is not page-locked.
+static void* host_alias(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
+// n bytes from src to dst, one of them host memory (to_device: src is the host side).
+static cudaError_t stage_copy(void* dst, const void* src, size_t n, bool to_device, cudaStream_t st) {
+  void* alias = host_alias(to_device ? src : dst);
+  if (alias == nullptr)
+    return cudaMemcpyAsync(dst, src, n, to_device ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToHost, st);
+  uint8_t* d = static_cast<uint8_t*>(to_device ? dst : alias);
+  const uint8_t* s = static_cast<const uint8_t*>(to_device ? alias : src);
+  const int vec = aligned(d, 16) && aligned(s, 16);
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const size_t units = vec ? (n + 15) / 16 : n;
+  const size_t want = (units + 255) / 256;
+  const unsigned blocks = static_cast<unsigned>(want < size_t(4) * sms ? want : size_t(4) * sms);
+  stage_copy_kernel<<<blocks > 0 ? blocks : 1, 256, 0, st>>>(d, s, n, vec);
+  return cudaGetLastError();
 }
 
 }  // namespace cskv
@@ -390,10 +433,7 @@ int32_t cskv_decode_layer(const cskv_decode_layer_args* args, void* stream) {
   if (a.in_bytes > 0 && (a.h_in == nullptr || a.d_in == nullptr)) return CSKV_ERR_INVALID;
   if (a.out_bytes > 0 && (a.h_out == nullptr || a.out_bytes > size_t(a.B) * a.H * 512 * 2)) return CSKV_ERR_INVALID;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (a.in_bytes > 0) {
-    const cudaError_t e = cudaMemcpyAsync(a.d_in, a.h_in, a.in_bytes, cudaMemcpyHostToDevice, st);
-    if (e != cudaSuccess) return CSKV_ERR_CUDA;
-  }
+  if (a.in_bytes > 0 && stage_copy(a.d_in, a.h_in, a.in_bytes, true, st) != cudaSuccess) return CSKV_ERR_CUDA;
   if (a.njobs > 0 && launch_compress_many(a.jobs, a.njobs, st) != cudaSuccess) return CSKV_ERR_CUDA;
   if (csa && launch_index_topk(a.q_idx, a.w, a.keys, a.ctx_len, a.B, a.Hi, a.ratio, a.k, a.max_ctx_len,
                                a.topk_idx, nullptr, a.index_workspace, st) != cudaSuccess)
@@ -403,10 +443,7 @@ int32_t cskv_decode_layer(const cskv_decode_layer_args* args, void* stream) {
                                 a.ratio, a.max_ctx_len, a.sink, a.softmax_scale, a.q_rope_cs, a.B, a.H, a.out,
                                 a.attn_workspace, st) != cudaSuccess)
     return CSKV_ERR_CUDA;
-  if (a.out_bytes > 0) {
-    const cudaError_t e = cudaMemcpyAsync(a.h_out, a.out, a.out_bytes, cudaMemcpyDeviceToHost, st);
-    if (e != cudaSuccess) return CSKV_ERR_CUDA;
-  }
+  if (a.out_bytes > 0 && stage_copy(a.h_out, a.out, a.out_bytes, false, st) != cudaSuccess) return CSKV_ERR_CUDA;
   return CSKV_OK;
 }
 

@@ -391,9 +391,12 @@ CSKV_API int32_t cskv_sparse_prefill_attn(const void* q, cskv_paged main_kv, csk
  * The device pointers of steps 2-4 may point into d_in: the copy of step 1 is
  * ordered before every kernel that reads them.  Each stage takes exactly the
  * arguments, layouts, results and bits of its own entry point above.
- * Ownership: every buffer is the caller's; h_in and h_out should be page-locked
- * (cudaHostAlloc / cudaHostRegister) for the copies to be asynchronous and to be
- * capturable into a CUDA graph.  The call returns once everything is enqueued;
+ * Copies: page-locked host memory (cudaHostAlloc / cudaMallocHost /
+ * cudaHostRegister) is read or written by a copy kernel on the SMs through its
+ * device alias; any other host memory goes through cudaMemcpyAsync (synchronous
+ * for pageable memory, and not capturable into a CUDA graph).
+ * Ownership: every buffer is the caller's; h_in must hold in_bytes bytes, d_in at
+ * least as many, h_out out_bytes.  The call returns once everything is enqueued;
  * h_out holds the output after the stream has synchronised.
  * Errors: the arguments of every stage are checked before anything is
  * enqueued (CSKV_ERR_INVALID / CSKV_ERR_UNSUPPORTED as the stage's own entry

@@ -19,14 +19,15 @@ pytestmark = pytest.mark.gpu
 SCALE = 512 ** -0.5
 
 
-def _stage(items):
-    """Host tensors packed into one pinned buffer (256-byte aligned parts) and an
-    uninitialised device buffer of the same size; returns (h_in, d_in, device views)."""
+def _stage(items, pinned=True):
+    """Host tensors packed into one host buffer (256-byte aligned parts; page-locked unless
+    pinned is False) and an uninitialised device buffer of the same size; returns
+    (h_in, d_in, device views)."""
     offs, tot = [], 0
     for t in items.values():
         offs.append(tot)
         tot = (tot + t.numel() * t.element_size() + 255) // 256 * 256
-    h = torch.empty(tot, dtype=torch.uint8, pin_memory=True)
+    h = torch.empty(tot, dtype=torch.uint8, pin_memory=pinned)
     d = torch.empty(tot, dtype=torch.uint8, device="cuda")
     views = {}
     for (name, t), o in zip(items.items(), offs):
@@ -130,9 +131,11 @@ def test_csa_layer_step_host_to_host(main_fmt):
         check_attention(got[b], ref, fp4=main_fmt == codecs.FMT_FP4)
 
 
-def test_hca_layer_steps_with_and_without_a_completed_block():
+@pytest.mark.parametrize("pinned", [True, False])
+def test_hca_layer_steps_with_and_without_a_completed_block(pinned):
     """HCA (ratio 128, no indexer): a step that completes each request's last entry, then
-    a step five tokens later that completes none (no compressor job)."""
+    a step five tokens later that completes none (no compressor job).  Page-locked host
+    buffers are copied by the library's copy kernel, pageable ones by the copy engine."""
     rs = np.random.default_rng(67)
     ratio, H = 128, 16
     n = [9, 3]
@@ -153,13 +156,13 @@ def test_hca_layer_steps_with_and_without_a_completed_block():
             items.update({"kv": blk["kv"][0], "gate": blk["gate"][0], "first": torch.from_numpy(first),
                           "req": torch.arange(B, dtype=torch.int32),
                           "ecs": torch.from_numpy(cskv.rope_table(first[:, None] * ratio))})
-        h_in, d_in, v = _stage(items)
+        h_in, d_in, v = _stage(items, pinned)
         jobs = []
         if with_job:
             jobs = [dict(kv=v["kv"], gate=v["gate"], ape=cuda(blk["ape"]), ratio=ratio, overlap=False,
                          out=dev_main, req=v["req"], first_entry=v["first"], norm_w=cuda(blk["nw"]),
                          rope_cs=v["ecs"])]
-        h_out = torch.empty((B, H, 512), dtype=torch.bfloat16, pin_memory=True)
+        h_out = torch.empty((B, H, 512), dtype=torch.bfloat16, pin_memory=pinned)
         out, topk = cskv.decode_layer(jobs, None, None, None, v["q"], dev_main, cuda(swa_b), codecs.FMT_FP8,
                                       v["ctx"], 0, ratio, int(ctx.max()), cuda(sink), SCALE, v["qcs"],
                                       h_in=h_in, d_in=d_in, h_out=h_out)
