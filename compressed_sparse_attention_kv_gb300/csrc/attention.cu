@@ -79,6 +79,7 @@ struct AttnArgs {
   float* opart;
   float* ml;
   int max_tiles;
+  uint8_t* out_host;           // optional second copy of out (a host buffer's device alias), or nullptr
 };
 
 __device__ __forceinline__ int query_len(const AttnArgs& a, int b) {
@@ -540,7 +541,9 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
     o1 = -y0 * s + y1 * c;
   }
   __nv_bfloat162 r = __floats2bfloat162_rn(o0, o1);
-  *reinterpret_cast<__nv_bfloat162*>(a.out + ((size_t(b) * a.H + h) * kD + d) * 2) = r;
+  const size_t off = ((size_t(b) * a.H + h) * kD + d) * 2;
+  *reinterpret_cast<__nv_bfloat162*>(a.out + off) = r;
+  if (a.out_host != nullptr) *reinterpret_cast<__nv_bfloat162*>(a.out_host + off) = r;
 }
 
 // 16 KiB of slack keeps every descriptor-addressed read inside the allocation
@@ -555,7 +558,7 @@ size_t attn_workspace_bytes(int B, int H, int max_ctx, int ratio, int k) {
 static cudaError_t launch_attn(const void* q, const cskv_paged& kv, const void* swa, const cskv_paged* win,
                                int swa_fmt, const int32_t* req_of, const int32_t* ctx_len, const int32_t* topk,
                                int k, int ratio, int max_ctx, const float* sink, float softmax_scale,
-                               const float* q_rope, int B, int H, void* out, void* workspace,
+                               const float* q_rope, int B, int H, void* out, void* out_host, void* workspace,
                                cudaStream_t stream) {
   const AttnLayout L = attn_layout(B, H, max_ctx, ratio, topk ? k : 0);
   AttnArgs a;
@@ -581,6 +584,7 @@ static cudaError_t launch_attn(const void* q, const cskv_paged& kv, const void* 
   a.opart = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + L.opart);
   a.ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + L.ml);
   a.max_tiles = L.max_tiles;
+  a.out_host = static_cast<uint8_t*>(out_host);
   const size_t smem = attn_smem_bytes();
   cudaFuncSetAttribute(attn_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   dim3 grid(L.max_tiles, B, (H + kMaxHeadsPerBlock - 1) / kMaxHeadsPerBlock);
@@ -607,9 +611,9 @@ cudaError_t launch_sparse_decode_attn(const void* q, const cskv_paged& kv, const
                                       const int32_t* ctx_len, const int32_t* topk, int k, int ratio,
                                       int max_ctx, const float* sink, float softmax_scale,
                                       const float* q_rope, int B, int H, void* out, void* workspace,
-                                      cudaStream_t stream) {
+                                      cudaStream_t stream, void* out_host) {
   return launch_attn(q, kv, swa, nullptr, swa_fmt, nullptr, ctx_len, topk, k, ratio, max_ctx, sink,
-                     softmax_scale, q_rope, B, H, out, workspace, stream);
+                     softmax_scale, q_rope, B, H, out, out_host, workspace, stream);
 }
 
 cudaError_t launch_sparse_prefill_attn(const void* q, const cskv_paged& kv, const cskv_paged& win,
@@ -618,7 +622,7 @@ cudaError_t launch_sparse_prefill_attn(const void* q, const cskv_paged& kv, cons
                                        const float* q_rope, int T, int H, void* out, void* workspace,
                                        cudaStream_t stream) {
   return launch_attn(q, kv, nullptr, &win, win.fmt, req_of, pos1, topk, k, ratio, max_ctx, sink, softmax_scale,
-                     q_rope, T, H, out, workspace, stream);
+                     q_rope, T, H, out, nullptr, workspace, stream);
 }
 
 unsigned int take_err_attention() { return take_dev_err(); }

@@ -439,11 +439,15 @@ int32_t cskv_decode_layer(const cskv_decode_layer_args* args, void* stream) {
                                a.topk_idx, nullptr, a.index_workspace, st) != cudaSuccess)
     return CSKV_ERR_CUDA;
   const int32_t kk = csa ? a.k : 0;
+  // a whole page-locked output buffer is written by the combine kernel itself, beside out
+  void* out_alias = nullptr;
+  if (a.out_bytes > 0 && a.out_bytes == size_t(a.B) * a.H * 512 * 2) out_alias = host_alias(a.h_out);
   if (launch_sparse_decode_attn(a.q, a.main_kv, a.swa, a.swa_fmt, a.ctx_len, csa ? a.topk_idx : nullptr, kk,
                                 a.ratio, a.max_ctx_len, a.sink, a.softmax_scale, a.q_rope_cs, a.B, a.H, a.out,
-                                a.attn_workspace, st) != cudaSuccess)
+                                a.attn_workspace, st, out_alias) != cudaSuccess)
     return CSKV_ERR_CUDA;
-  if (a.out_bytes > 0 && stage_copy(a.h_out, a.out, a.out_bytes, false, st) != cudaSuccess) return CSKV_ERR_CUDA;
+  if (a.out_bytes > 0 && out_alias == nullptr && stage_copy(a.h_out, a.out, a.out_bytes, false, st) != cudaSuccess)
+    return CSKV_ERR_CUDA;
   return CSKV_OK;
 }
 

@@ -48,7 +48,7 @@ cudaError_t launch_sparse_decode_attn(const void* q, const cskv_paged& kv, const
                                       const int32_t* ctx_len, const int32_t* topk, int k, int ratio,
                                       int max_ctx, const float* sink, float softmax_scale,
                                       const float* q_rope, int B, int H, void* out, void* workspace,
-                                      cudaStream_t stream);
+                                      cudaStream_t stream, void* out_host = nullptr);
 cudaError_t launch_sparse_prefill_attn(const void* q, const cskv_paged& kv, const cskv_paged& win,
                                        const int32_t* req_of, const int32_t* pos1, const int32_t* topk, int k,
                                        int ratio, int max_ctx, const float* sink, float softmax_scale,

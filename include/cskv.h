@@ -393,8 +393,10 @@ CSKV_API int32_t cskv_sparse_prefill_attn(const void* q, cskv_paged main_kv, csk
  * arguments, layouts, results and bits of its own entry point above.
  * Copies: page-locked host memory (cudaHostAlloc / cudaMallocHost /
  * cudaHostRegister) is read or written by a copy kernel on the SMs through its
- * device alias; any other host memory goes through cudaMemcpyAsync (synchronous
- * for pageable memory, and not capturable into a CUDA graph).
+ * device alias, and a page-locked h_out of the whole output's size is written
+ * by the attention's last kernel itself, beside `out`; any other host memory
+ * goes through cudaMemcpyAsync (synchronous for pageable memory, and not
+ * capturable into a CUDA graph).
  * Ownership: every buffer is the caller's; h_in must hold in_bytes bytes, d_in at
  * least as many, h_out out_bytes.  The call returns once everything is enqueued;
  * h_out holds the output after the stream has synchronised.

@@ -134,8 +134,10 @@ def test_csa_layer_step_host_to_host(main_fmt):
 @pytest.mark.parametrize("pinned", [True, False])
 def test_hca_layer_steps_with_and_without_a_completed_block(pinned):
     """HCA (ratio 128, no indexer): a step that completes each request's last entry, then
-    a step five tokens later that completes none (no compressor job).  Page-locked host
-    buffers are copied by the library's copy kernel, pageable ones by the copy engine."""
+    a step five tokens later that completes none (no compressor job), which copies back
+    only the first request's output.  Page-locked host buffers are read by the library's
+    copy kernel and a whole page-locked output is written by the attention's last kernel
+    (a part of one by the copy kernel); pageable buffers go through the copy engine."""
     rs = np.random.default_rng(67)
     ratio, H = 128, 16
     n = [9, 3]
@@ -162,7 +164,8 @@ def test_hca_layer_steps_with_and_without_a_completed_block(pinned):
             jobs = [dict(kv=v["kv"], gate=v["gate"], ape=cuda(blk["ape"]), ratio=ratio, overlap=False,
                          out=dev_main, req=v["req"], first_entry=v["first"], norm_w=cuda(blk["nw"]),
                          rope_cs=v["ecs"])]
-        h_out = torch.empty((B, H, 512), dtype=torch.bfloat16, pin_memory=pinned)
+        nout = B if with_job else 1
+        h_out = torch.empty((nout, H, 512), dtype=torch.bfloat16, pin_memory=pinned)
         out, topk = cskv.decode_layer(jobs, None, None, None, v["q"], dev_main, cuda(swa_b), codecs.FMT_FP8,
                                       v["ctx"], 0, ratio, int(ctx.max()), cuda(sink), SCALE, v["qcs"],
                                       h_in=h_in, d_in=d_in, h_out=h_out)
@@ -170,8 +173,9 @@ def test_hca_layer_steps_with_and_without_a_completed_block(pinned):
         assert cskv.device_status() == 0
         assert topk is None
         assert np.array_equal(dev_main.pool.cpu().numpy(), host_main.pool)
+        assert torch.equal(h_out, out[:nout].cpu())
         got = h_out.float().numpy()
-        for b in range(B):
+        for b in range(nout):
             ref = o_attn.request_attention(q_v[b], int(ctx[b]), ratio, swa_dec[b], host_main.decoded[b], None,
                                            sink, SCALE)
             check_attention(got[b], ref)
