@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(256) index_prep_kernel(const IndexArgs a) {
     ctr[threadIdx.x] = threadIdx.x == 0 ? static_cast<uint32_t>(first_home_block(b + 1, a.B, a.grid) -
                                                              first_home_block(b, a.B, a.grid)) * kChunkTiles
                                         : 0u;
-  if (b == 0 && threadIdx.x == 0) *reinterpret_cast<uint32_t*>(a.ws + a.L.gbar) = 0;
+  if (b == 0 && threadIdx.x < 2) reinterpret_cast<uint32_t*>(a.ws + a.L.gbar)[threadIdx.x] = 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -483,7 +483,11 @@ __device__ __forceinline__ uint32_t block_scan_excl(ScoreSmem* sm, uint32_t v, u
   return pos;
 }
 
-template <int FP8>
+// LARGE (batches of more than kReqCache requests, e.g. one request per prompt query in
+// prefill): the scheduler also counts the tiles handed out, so that a block that finds
+// its requests exhausted stops as soon as every tile has an owner instead of visiting
+// every request (one atomic each) before it concludes there is no work left.
+template <int FP8, bool LARGE>
 __global__ void __launch_bounds__(kLaunchBound, 1)
     index_score_kernel(const __grid_constant__ CUtensorMap tmap, const IndexArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -689,13 +693,19 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
         };
         int req = home_request(blockIdx.x, a.B, gridDim.x);
         uint32_t pending = 0;
+        uint32_t* handed = gbar + 1;   // LARGE: tiles handed out so far (cleared by the prep)
         // the next chunk: (request, first tile) from the pending grab; request -1 = none left
         auto resolve = [&](int& b, int& t0) {
           int tiles = tiles_of(req);
           int fails = 0;
+          uint32_t seen = 0;   // LARGE: the handed-out count read during the previous step
           while (pending >= static_cast<uint32_t>(tiles) && ++fails < a.B) {
+            if constexpr (LARGE) {
+              if (seen >= static_cast<uint32_t>(total)) break;
+            }
             req = (req + 1) % a.B;
             tiles = tiles_of(req);
+            if constexpr (LARGE) seen = *reinterpret_cast<volatile uint32_t*>(handed);
             pending = atomicAdd(&ctr_all[req * 4], static_cast<uint32_t>(kChunkTiles));
           }
           if (pending >= static_cast<uint32_t>(tiles)) {
@@ -704,6 +714,7 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
           } else {
             b = req;
             t0 = static_cast<int>(pending);
+            if constexpr (LARGE) atomicAdd(handed, static_cast<uint32_t>(min(kChunkTiles, tiles - t0)));
             pending = atomicAdd(&ctr_all[req * 4], static_cast<uint32_t>(kChunkTiles));
           }
         };
@@ -717,6 +728,9 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
           chunk_ids(cb, ct, ids);
         }
         grid_dep_wait();
+        if constexpr (LARGE) {
+          if (static_first) atomicAdd(handed, static_cast<uint32_t>(min(kChunkTiles, tiles_of(cb) - ct)));
+        }
         pending = atomicAdd(&ctr_all[req * 4], static_cast<uint32_t>(kChunkTiles));
         if (!static_first) {
           resolve(cb, ct);
@@ -1350,14 +1364,14 @@ size_t score_smem_bytes() {
 
 // Cooperative launch of the score kernel: the selection phases meet at grid
 // barriers, so the grid is the number of blocks that fit on the GPU at once.
-template <int FP8>
+template <int FP8, bool LARGE>
 cudaError_t launch_score(const CUtensorMap& tmap, const IndexArgs& a, cudaStream_t stream) {
   const size_t smem = score_smem_bytes<FP8>();
-  cudaError_t e = cudaFuncSetAttribute(index_score_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(index_score_kernel<FP8, LARGE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, index_score_kernel<FP8>, kScoreThreads, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, index_score_kernel<FP8, LARGE>, kScoreThreads, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   // one block per SM: it allocates all 512 TMEM columns and most of shared memory
@@ -1385,7 +1399,7 @@ cudaError_t launch_score(const CUtensorMap& tmap, const IndexArgs& a, cudaStream
   }
   if (ok != 0) {
     cfg.numAttrs = 2;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, index_score_kernel<FP8>, tmap, a);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, index_score_kernel<FP8, LARGE>, tmap, a);
     if (e == cudaSuccess) {
       pdl_ok.store(1, std::memory_order_relaxed);
       return e;
@@ -1395,7 +1409,7 @@ cudaError_t launch_score(const CUtensorMap& tmap, const IndexArgs& a, cudaStream
     pdl_ok.store(0, std::memory_order_relaxed);
   }
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, index_score_kernel<FP8>, tmap, a);
+  return cudaLaunchKernelEx(&cfg, index_score_kernel<FP8, LARGE>, tmap, a);
 }
 
 }  // namespace
@@ -1476,7 +1490,8 @@ cudaError_t launch_index_topk(const void* q_idx, const float* w, const cskv_page
   cudaEvent_t ev_begin, ev_end;
   timing_events(&ev_begin, &ev_end);
   record_timing_branch(ev_begin, stream);
-  e = a.fp8 ? launch_score<1>(tmap, a, stream) : launch_score<0>(tmap, a, stream);
+  e = !a.fp8 ? launch_score<0, false>(tmap, a, stream)
+             : (B > kReqCache ? launch_score<1, true>(tmap, a, stream) : launch_score<1, false>(tmap, a, stream));
   record_timing_branch(ev_end, stream);
   return e;
 }
