@@ -487,30 +487,57 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
   }
 }
 
-// merge the tiles of (request, head) in tile order, sink, inverse RoPE, bf16
+// merge the tiles of (request, head) in tile order, sink, inverse RoPE, bf16.  DPT dims
+// per thread: 2 (one head per 256-thread block, for decode batches, where the block
+// count is small and each block's latency sets the time) or 8 (four heads per block,
+// 16-byte loads and stores, for launches with many queries, where the block count does)
+template <int DPT>
 __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
   grid_dep_wait();   // the tile kernel's partials
-  const int b = blockIdx.x, h = blockIdx.y;
+  constexpr int kThreadsPerHead = kD / DPT;
+  constexpr int kHeadsPerBlock = 256 / kThreadsPerHead;
+  const int b = blockIdx.x;
+  const int h = blockIdx.y * kHeadsPerBlock + static_cast<int>(threadIdx.x) / kThreadsPerHead;
+  if (h >= a.H) return;
   const int ctx = query_len(a, b);
   const int ncomp = comp_keys(a, ctx);
   const int ntiles = 1 + (ncomp + kKeys - 1) / kKeys;
   const size_t slot0 = size_t(b) * a.max_tiles * a.H + h;
-  const int d = 2 * threadIdx.x;
+  const int d = DPT * (static_cast<int>(threadIdx.x) % kThreadsPerHead);
   // running (max, sum, output) in base 2, started from the sink; tiles taken in
   // batches of 8 whose loads are all issued before any is used
   float M = a.sink ? a.sink[h] * 1.4426950408889634f : -INFINITY;
   float L = a.sink ? 1.f : 0.f;
-  float o0 = 0.f, o1 = 0.f;
+  float o[DPT];
+#pragma unroll
+  for (int i = 0; i < DPT; ++i) o[i] = 0.f;
   for (int s0 = 0; s0 < ntiles; s0 += 8) {
     float m[8], l[8];
-    float2 v[8];
+    float v[8][DPT];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const size_t sl = slot0 + size_t(s0 + u) * a.H;
       const bool in = s0 + u < ntiles;
       m[u] = in ? a.ml[sl * 2] : -INFINITY;
       l[u] = in ? a.ml[sl * 2 + 1] : 0.f;
-      v[u] = in ? *reinterpret_cast<const float2*>(a.opart + sl * kD + d) : make_float2(0.f, 0.f);
+      if constexpr (DPT % 4 == 0) {
+#pragma unroll
+        for (int i = 0; i < DPT; i += 4) {
+          const float4 x = in ? *reinterpret_cast<const float4*>(a.opart + sl * kD + d + i)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+          v[u][i] = x.x;
+          v[u][i + 1] = x.y;
+          v[u][i + 2] = x.z;
+          v[u][i + 3] = x.w;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < DPT; i += 2) {
+          const float2 x = in ? *reinterpret_cast<const float2*>(a.opart + sl * kD + d + i) : make_float2(0.f, 0.f);
+          v[u][i] = x.x;
+          v[u][i + 1] = x.y;
+        }
+      }
     }
     float Mb = M;
 #pragma unroll
@@ -518,32 +545,47 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
     if (Mb == -INFINITY) continue;
     const float f = M == -INFINITY ? 0.f : exp2f(M - Mb);
     L *= f;
-    o0 *= f;
-    o1 *= f;
+#pragma unroll
+    for (int i = 0; i < DPT; ++i) o[i] *= f;
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       if (m[u] == -INFINITY) continue;
       const float g = exp2f(m[u] - Mb);
       L += g * l[u];
-      o0 += g * v[u].x;
-      o1 += g * v[u].y;
+#pragma unroll
+      for (int i = 0; i < DPT; ++i) o[i] += g * v[u][i];
     }
     M = Mb;
   }
   const float inv = L > 0.f ? 1.0f / L : 0.f;
-  o0 *= inv;
-  o1 *= inv;
-  if (d >= kD - 64) {
-    const int kk = (d - (kD - 64)) / 2;
-    const float c = a.q_rope[size_t(b) * 64 + 2 * kk], s = a.q_rope[size_t(b) * 64 + 2 * kk + 1];
-    const float y0 = o0, y1 = o1;
-    o0 = y0 * c + y1 * s;
-    o1 = -y0 * s + y1 * c;
+#pragma unroll
+  for (int i = 0; i < DPT; ++i) o[i] *= inv;
+  if (d >= kD - 64) {   // the rotated dims: pairs (2i, 2i+1) lie inside one thread's dims
+#pragma unroll
+    for (int i = 0; i < DPT; i += 2) {
+      const int kk = (d + i - (kD - 64)) / 2;
+      const float c = a.q_rope[size_t(b) * 64 + 2 * kk], s = a.q_rope[size_t(b) * 64 + 2 * kk + 1];
+      const float y0 = o[i], y1 = o[i + 1];
+      o[i] = y0 * c + y1 * s;
+      o[i + 1] = -y0 * s + y1 * c;
+    }
   }
-  __nv_bfloat162 r = __floats2bfloat162_rn(o0, o1);
+  uint32_t r[DPT / 2];
+#pragma unroll
+  for (int i = 0; i < DPT; i += 2) {
+    __nv_bfloat162 x = __floats2bfloat162_rn(o[i], o[i + 1]);
+    r[i / 2] = *reinterpret_cast<uint32_t*>(&x);
+  }
   const size_t off = ((size_t(b) * a.H + h) * kD + d) * 2;
-  *reinterpret_cast<__nv_bfloat162*>(a.out + off) = r;
-  if (a.out_host != nullptr) *reinterpret_cast<__nv_bfloat162*>(a.out_host + off) = r;
+  if constexpr (DPT == 2) {
+    *reinterpret_cast<uint32_t*>(a.out + off) = r[0];
+    if (a.out_host != nullptr) *reinterpret_cast<uint32_t*>(a.out_host + off) = r[0];
+  } else {
+    static_assert(DPT == 8, "2 or 8 dims per thread");
+    const uint4 x = make_uint4(r[0], r[1], r[2], r[3]);
+    *reinterpret_cast<uint4*>(a.out + off) = x;
+    if (a.out_host != nullptr) *reinterpret_cast<uint4*>(a.out_host + off) = x;
+  }
 }
 
 // 16 KiB of slack keeps every descriptor-addressed read inside the allocation
@@ -601,10 +643,14 @@ static cudaError_t launch_attn(const void* q, const cskv_paged& kv, const void* 
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, attn_tile_kernel, a);
   if (e != cudaSuccess) return e;
-  cfg.gridDim = dim3(B, H);
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
-  return cudaLaunchKernelEx(&cfg, attn_combine_kernel, a);
+  if (B <= 64) {   // decode batches: one head per block
+    cfg.gridDim = dim3(B, H);
+    return cudaLaunchKernelEx(&cfg, attn_combine_kernel<2>, a);
+  }
+  cfg.gridDim = dim3(B, (H + 3) / 4);   // many queries: four heads per block
+  return cudaLaunchKernelEx(&cfg, attn_combine_kernel<8>, a);
 }
 
 cudaError_t launch_sparse_decode_attn(const void* q, const cskv_paged& kv, const void* swa, int swa_fmt,
