@@ -20,6 +20,7 @@ shards by request; no collective); rank 0 prints one JSON line.
 
 import argparse
 import concurrent.futures
+import datetime
 import hashlib
 import json
 import os
@@ -70,7 +71,9 @@ def step_inputs(wl):
 # ----------------------------------------------------------------------------- clocks
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples every 50 ms; stop() keeps those taken between mark("t0") and
+    mark("t1") (the timed region), or all of them if the region was too short to hold one."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -95,14 +98,25 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
         self.proc.terminate()
         out, _ = self.proc.communicate(timeout=10)
-        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 8]
-        sm = [float(r[1].split()[0]) for r in rows if r[1].split()[0].replace(".", "").isdigit()]
-        mx = [float(r[2].split()[0]) for r in rows if r[2].split()[0].replace(".", "").isdigit()]
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 9]
+
+        def when(r):
+            try:
+                return datetime.datetime.strptime(r[0].strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                return None
+        inside = [r for r in rows if self.t0 is not None and self.t1 is not None and when(r) is not None
+                  and self.t0 <= when(r) <= self.t1]
+        window = "timed region" if inside else "around the timed region"
+        rows = inside or rows
+        sm = [float(r[2].split()[0]) for r in rows if r[2].split()[0].replace(".", "").isdigit()]
+        mx = [float(r[3].split()[0]) for r in rows if r[3].split()[0].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip().lower() == "active"})
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].strip().lower() == "active"})
         loaded = [s for s in sm if mx and s >= 0.3 * max(mx)] or sm
         return {"sm_mhz": statistics.median(loaded) if loaded else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows),
+                "window": window}
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -284,6 +298,7 @@ def run_gpu(args, rank, world):
         ev_sb, ev_se = live_events(torch)
         cskv.set_timing_events(ev_sb, ev_se)
     wall0 = time.time()
+    clk.mark("t0")
     for i in range(args.steps):
         flush.zero_()
         evs[i][0].record()
@@ -293,6 +308,7 @@ def run_gpu(args, rank, world):
         ev_se.synchronize()
         score_ms.append(ev_sb.elapsed_time(ev_se))
     torch.cuda.synchronize()
+    clk.mark("t1")
     wall = time.time() - wall0
     if world > 1:
         torch.distributed.barrier()
@@ -565,6 +581,7 @@ def _graph_timed(torch, step, steps, warmup, flush, timing=None):
     time.sleep(0.3)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     inner = []
+    clk.mark("t0")
     for e0, e1 in evs:
         flush.zero_()
         e0.record()
@@ -575,6 +592,7 @@ def _graph_timed(torch, step, steps, warmup, flush, timing=None):
             timing[2].synchronize()
             inner.append(timing[1].elapsed_time(timing[2]))
     torch.cuda.synchronize()
+    clk.mark("t1")
     return [a.elapsed_time(b) for a, b in evs], inner, clk.stop()
 
 
@@ -787,7 +805,9 @@ def run_next_row(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: 1000 for the GPU decode benchmark, so that the clock samples "
+                         "fall inside the timed region; 50 for the oracle arm and the other modes)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["cskv", "reference"], default="cskv")
     ap.add_argument("--no-graph", action="store_true")
@@ -796,6 +816,8 @@ def main():
                     help="decode: the benchmark; the others measure the rows built beyond it")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.steps is None:
+        args.steps = 1000 if (args.impl == "cskv" and args.mode == "decode") else 50
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
 

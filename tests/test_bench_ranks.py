@@ -1,5 +1,6 @@
-"""The bench's multi-rank host logic on CPU (gloo, two processes): max over ranks of
-the per-rank step times, whole-job throughput, and the reference arm's rank > 0 exit."""
+"""The bench's host logic on CPU: max over ranks of the per-rank step times (gloo, two
+processes), whole-job throughput, the reference arm's rank > 0 exit, and the clock
+record's window."""
 
 import os
 import socket
@@ -63,3 +64,38 @@ def test_reference_arm_other_ranks_exit_without_work():
                        timeout=120)
     assert r.returncode == 0
     assert r.stdout.strip() == ""
+
+
+def test_clock_samples_are_taken_from_the_timed_region():
+    """The clock record keeps the nvidia-smi samples stamped inside the timed region (a
+    throttle reason seen only outside it is not reported), and falls back to every
+    sample when none falls inside."""
+    import datetime
+    import time
+    import bench
+
+    now = datetime.datetime.now()
+    inside = now.strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+    outside = (now - datetime.timedelta(seconds=30)).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+    text = (inside + ", 0, 2070 MHz, 2070 MHz, 900.00 W, 0x0, Not Active, Not Active, Not Active, Not Active\n"
+            + outside + ", 0, 1200 MHz, 2070 MHz, 300.00 W, 0x0, Not Active, Not Active, Active, Not Active\n")
+
+    class FakeSmi:
+        def terminate(self):
+            pass
+
+        def communicate(self, timeout=None):
+            return text, ""
+
+    c = bench.ClockSampler("0")
+    c.proc = FakeSmi()
+    c.t0, c.t1 = time.time() - 5, time.time() + 5
+    got = c.stop()
+    assert got["window"] == "timed region" and got["samples"] == 1
+    assert got["sm_mhz"] == 2070.0 and got["reasons"] == []
+    c = bench.ClockSampler("0")
+    c.proc = FakeSmi()
+    c.t0, c.t1 = time.time() + 100, time.time() + 101   # a region no sample falls in
+    got = c.stop()
+    assert got["window"] == "around the timed region" and got["samples"] == 2
+    assert got["reasons"] == ["sw_thermal_slowdown"]
