@@ -164,3 +164,31 @@ def test_extreme_k_and_heads(Hi, k):
     for b, nb in enumerate(n):
         swaps += check_topk(idx[b], sc[b], indexer.quantize_queries(q_v[b]), w[b], cache.decoded[b], nb, k)
     assert swaps <= 1
+
+
+@pytest.mark.parametrize("fmt", [codecs.FMT_FP8_PAGESPLIT, codecs.FMT_BF16])
+def test_large_ragged_batch(fmt):
+    """A batch of 700 requests (the large-batch prologue; for FP8 keys also the scheduler
+    that counts the tiles handed out): empty, tiny and long contexts mixed, most requests
+    shorter than one 128-entry tile, a few hundred times longer."""
+    ratio, k, Hi = 4, 64, 8
+    rs = np.random.default_rng(70 + fmt)
+    n = rs.choice([0, 1, 5, 63, 64, 65, 127, 128, 129, 300, 1000], size=700).tolist()
+    for b in rs.choice(700, 6, replace=False):
+        n[b] = int(rs.integers(20000, 40000))
+    ctx = [ratio * nb + int(rs.integers(0, ratio)) for nb in n]
+    q = rs.standard_normal((len(ctx), Hi, 128)).astype(np.float32)
+    w = rs.uniform(0, 1, (len(ctx), Hi)).astype(np.float32)
+    cache = HostPaged(fmt, 128, [max(1, x) for x in n], seed=71)
+    for b, nb in enumerate(n):
+        cache.fill(b, rs.standard_normal((max(1, nb), 128)).astype(np.float32))
+    q_t, q_v = bf16_values(q)
+    idx, sc = _run(q_t, w, cache, ctx, ratio, k, max(ctx))
+    swaps = 0
+    for b, nb in enumerate(n):
+        if nb == 0:
+            assert np.all(idx[b] == -1), b
+            continue
+        q_hat = indexer.quantize_queries(q_v[b]) if fmt == codecs.FMT_FP8_PAGESPLIT else q_v[b].astype(np.float64)
+        swaps += check_topk(idx[b], sc[b], q_hat, w[b], cache.decoded[b][:nb], nb, k)
+    assert swaps <= 2
