@@ -187,18 +187,21 @@ __device__ __forceinline__ void compress_block(const CompressArgs& a, long long 
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
   };
+  // which slots are the empty half, and which have gate scores (the same cases as
+  // slot_src, without its addresses): slot_at reads the staged copies by these alone
+  const bool first_half_empty = a.overlap && i == 0 && a.prev_kv == nullptr;
+  const bool first_half_gated = i > 0 ? a.gate != nullptr : a.prev_kv != nullptr;
   // slot j's biased score (-inf for the empty half) and, if wanted, its value
   auto slot_at = [&](int j, float4& sc, float4* v) {
     const int buf = (j / kBatch) & 1, u = j % kBatch;
-    const uint8_t *vp, *gp;
-    long long ao;
-    slot_src(j, vp, gp, ao);
-    if (vp == nullptr) {
+    const bool first = a.overlap && j < r;
+    if (first && first_half_empty) {
       sc = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
       if (v) *v = make_float4(0.f, 0.f, 0.f, 0.f);
       return;
     }
-    const uint2 g = gp != nullptr ? s_g[(buf * kBatch + u) * 128 + t] : make_uint2(0u, 0u);
+    const bool gated = first ? first_half_gated : a.gate != nullptr;
+    const uint2 g = gated ? s_g[(buf * kBatch + u) * 128 + t] : make_uint2(0u, 0u);
     // no slot bias (ape == nullptr) adds +0: the same bits as a zero bias table
     const float4 b = a.ape != nullptr ? s_ap[(buf * kBatch + u) * 128 + t] : make_float4(0.f, 0.f, 0.f, 0.f);
     sc = make_float4(__fadd_rn(bf16lo(g.x), b.x), __fadd_rn(bf16hi(g.x), b.y), __fadd_rn(bf16lo(g.y), b.z),
