@@ -124,4 +124,71 @@ __device__ __forceinline__ void store_row_values(const float4& y, int lt, int fm
   (void)dim;
 }
 
+// store_row_values for threads that own 2 consecutive channels (c0 = 2 lt) of a
+// D-channel entry of D / 2 threads (whole warps): the same codes and scales.  The
+// row-scaled index key (D = 128, two warps) takes its row maximum across the two
+// warps through shared memory, so every thread of the block must call this.
+template <int D>
+__device__ __forceinline__ void store_row_values2(float y0, float y1, int lt, int fmt, RowPtr dst, bool valid) {
+  const unsigned full = 0xFFFFFFFFu;
+  if (fmt == CSKV_FMT_BF16) {
+    if (valid) {
+      __nv_bfloat162 a = __floats2bfloat162_rn(y0, y1);
+      *reinterpret_cast<uint32_t*>(dst.data + 4 * lt) = *reinterpret_cast<uint32_t*>(&a);
+    }
+    return;
+  }
+  float amax = fmaxf(fabsf(y0), fabsf(y1));
+  if (fmt == CSKV_FMT_FP4_E2M1_E4M3_B16) {
+    // blocks of 16 channels = 8 threads
+    amax = fmaxf(amax, __shfl_xor_sync(full, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(full, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(full, amax, 4));
+    const uint32_t scode = e4m3x2(__fdiv_rn(amax, 6.0f), 0.f) & 0xFF;
+    const float s = e4m3_to_f32(scode);
+    const uint32_t packed = s > 0.f ? e2m1x2(__fdiv_rn(y0, s), __fdiv_rn(y1, s)) : 0u;
+    if (valid) {
+      dst.data[lt] = static_cast<uint8_t>(packed);
+      if ((lt & 7) == 0) dst.scale[lt >> 3] = static_cast<uint8_t>(scode);
+    }
+    return;
+  }
+  if (fmt == CSKV_FMT_FP8_E4M3_ROWSCALE_PAGESPLIT) {
+    // index key: one power-of-two scale for the whole row (D / 2 threads)
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(full, amax, o));
+    constexpr int kWarps = D / 2 / 32;
+    if constexpr (kWarps > 1) {
+      __shared__ float wmax[8];
+      const int w = threadIdx.x >> 5;
+      if ((threadIdx.x & 31) == 0) wmax[w] = amax;
+      __syncthreads();
+      const float* q = wmax + (w / kWarps) * kWarps;
+#pragma unroll
+      for (int u = 0; u < kWarps; ++u) amax = fmaxf(amax, q[u]);
+      __syncthreads();
+    }
+    const int e = e8m0_exponent(amax);
+    const float inv = exp2i(-e);
+    const uint32_t codes = e4m3x2(__fmul_rn(y0, inv), __fmul_rn(y1, inv));
+    if (valid) {
+      *reinterpret_cast<uint16_t*>(dst.data + 2 * lt) = static_cast<uint16_t>(codes);
+      if (lt == 0) *reinterpret_cast<float*>(dst.scale) = exp2i(e);
+    }
+    return;
+  }
+  // FP8 inline rows: blocks of 32 channels = 16 threads
+  amax = fmaxf(amax, __shfl_xor_sync(full, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(full, amax, 2));
+  amax = fmaxf(amax, __shfl_xor_sync(full, amax, 4));
+  amax = fmaxf(amax, __shfl_xor_sync(full, amax, 8));
+  const int e = e8m0_exponent(amax);
+  const float inv = exp2i(-e);
+  const uint32_t codes = e4m3x2(__fmul_rn(y0, inv), __fmul_rn(y1, inv));
+  if (valid) {
+    *reinterpret_cast<uint16_t*>(dst.data + 2 * lt) = static_cast<uint16_t>(codes);
+    if ((lt & 15) == 0) dst.scale[lt >> 4] = static_cast<uint8_t>(e + 127);
+  }
+}
+
 }  // namespace cskv

@@ -8,9 +8,10 @@
 // tokens; then RMSNorm over the channels and RoPE on the last 64 dims at the
 // position of the entry's first token.
 //
-// Design: threads own 4 consecutive channels (8-byte bf16 loads, coalesced across
-// the group); an entry of D channels is a group of D/4 threads (one warp at
-// D = 128, the whole 128-thread block at D = 512).  The slots' rows are staged in
+// Design: threads own CPT consecutive channels (CPT = 2 for the compressor launches,
+// 256-thread blocks; 4 for the decode state update, 128-thread blocks); an entry of
+// D channels is a group of D/CPT threads (a whole block at D = 512; at D = 128 one
+// warp with CPT = 4, two with CPT = 2).  The slots' rows are staged in
 // shared memory by cp.async, eight slots per batch, two batches in flight.  The
 // arithmetic is the bit-exact fp32 contract: separately rounded __f*_rn
 // operations (never contracted to FMA), exp_own below, a pairwise sum of squares
@@ -76,30 +77,71 @@ __device__ __forceinline__ const uint8_t* tok_ptr(const uint8_t* base, long long
   return base + (((s * T + tok) * coff + half) * D) * 2;
 }
 
-template <int D>
-__device__ __forceinline__ float block_sum_pairwise(float v, int lt) {
-  // channel groups of 4 are already reduced in-thread; now threads in channel
-  // order: xor 1, 2, 4, 8, 16 inside a warp ...
+template <int D, int CPT>
+__device__ __forceinline__ float block_sum_pairwise(float v) {
+  // channel groups of CPT are already reduced in-thread (pairwise); now threads in
+  // channel order: xor 1, 2, 4, 8, 16 inside a warp ...
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-  if constexpr (D == 512) {
-    // ... then the four warps of the block: (w0 + w1) + (w2 + w3)
-    __shared__ float part[4];
-    if ((lt & 31) == 0) part[lt >> 5] = v;
+  // ... then the warps of the entry, pairwise in channel order (every level of the
+  // tree sums two halves of equal size, as in the in-thread and shuffle levels)
+  constexpr int kWarps = D / CPT / 32;
+  if constexpr (kWarps > 1) {
+    __shared__ float part[8];
+    const int w = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) part[w] = v;
     __syncthreads();
-    v = __fadd_rn(__fadd_rn(part[0], part[1]), __fadd_rn(part[2], part[3]));
+    const float* q = part + (w / kWarps) * kWarps;   // this entry's warps
+    if constexpr (kWarps == 2) {
+      v = __fadd_rn(q[0], q[1]);
+    } else if constexpr (kWarps == 4) {
+      v = __fadd_rn(__fadd_rn(q[0], q[1]), __fadd_rn(q[2], q[3]));
+    } else {
+      static_assert(kWarps == 8, "2, 4 or 8 warps per entry");
+      v = __fadd_rn(__fadd_rn(__fadd_rn(q[0], q[1]), __fadd_rn(q[2], q[3])),
+                    __fadd_rn(__fadd_rn(q[4], q[5]), __fadd_rn(q[6], q[7])));
+    }
+    __syncthreads();   // part is reused by the next sum
   }
   return v;
 }
 
 constexpr int kBatch = 8;   // slots staged per batch
-constexpr size_t kCompressSmem = 2 * kBatch * 128 * (8 + 8 + 16);   // two batches of kv, gate, bias
+// two batches of kv, gate, bias for 128 threads x 4 channels or 256 threads x 2
+constexpr size_t kCompressSmem = 2 * kBatch * 128 * (8 + 8 + 16);
 
-// The entries of block `blk` of one compressor job (a whole 128-thread block).
-template <int D>
+// This thread's CPT channels of a staged bf16 row (KvT) and of the fp32 bias (BiasT).
+template <int CPT> struct Lanes;
+template <> struct Lanes<4> {
+  using KvT = uint2;
+  using BiasT = float4;
+  static __device__ __forceinline__ void kv(const KvT& x, float (&v)[4]) {
+    v[0] = bf16lo(x.x); v[1] = bf16hi(x.x); v[2] = bf16lo(x.y); v[3] = bf16hi(x.y);
+  }
+  static __device__ __forceinline__ void bias(const BiasT& b, float (&v)[4]) {
+    v[0] = b.x; v[1] = b.y; v[2] = b.z; v[3] = b.w;
+  }
+  static __device__ __forceinline__ void copy_kv(void* dst, const void* src) { cp_async8(dst, src); }
+  static __device__ __forceinline__ void copy_bias(void* dst, const void* src) { cp_async16(dst, src); }
+};
+template <> struct Lanes<2> {
+  using KvT = uint32_t;
+  using BiasT = float2;
+  static __device__ __forceinline__ void kv(const KvT& x, float (&v)[2]) { v[0] = bf16lo(x); v[1] = bf16hi(x); }
+  static __device__ __forceinline__ void bias(const BiasT& b, float (&v)[2]) { v[0] = b.x; v[1] = b.y; }
+  static __device__ __forceinline__ void copy_kv(void* dst, const void* src) { cp_async4(dst, src); }
+  static __device__ __forceinline__ void copy_bias(void* dst, const void* src) { cp_async8(dst, src); }
+};
+
+// The entries of block `blk` of one compressor job (a whole block of 512 / CPT threads).
+template <int D, int CPT>
 __device__ __forceinline__ void compress_block(const CompressArgs& a, long long blk) {
-  constexpr int TPE = D / 4;        // threads per entry
-  constexpr int EPB = 128 / TPE;    // entries per block
+  constexpr int kThreads = 512 / CPT;
+  constexpr int TPE = D / CPT;            // threads per entry
+  constexpr int EPB = kThreads / TPE;     // entries per block
+  using L = Lanes<CPT>;
+  using KvT = typename L::KvT;
+  using BiasT = typename L::BiasT;
   const int lt = threadIdx.x % TPE;
   const long long gentry = blk * EPB + threadIdx.x / TPE;
   const bool dec = a.pos != nullptr;
@@ -110,11 +152,11 @@ __device__ __forceinline__ void compress_block(const CompressArgs& a, long long 
     p = a.pos[gentry];
     live = p >= 0 && (a.ring > 0 || (p + 1) % a.ratio == 0);   // p < 0: no token this step
   }
-  // D == 512: one entry per block, the whole block stays for the block-wide sum.
-  if (!live && D != 512) return;
+  // An entry of more than one warp stays for the block-wide sums.
+  if (!live && TPE <= 32) return;
   const long long s = live ? (dec ? gentry : gentry / a.n) : 0;
   const int i = live ? (dec ? a.n - 1 : static_cast<int>(gentry % a.n)) : 0;
-  const int c0 = 4 * lt;
+  const int c0 = CPT * lt;
   const int r = a.ratio;
   const int coff = a.overlap ? 2 : 1;
   const int slots = a.overlap ? 2 * r : r;
@@ -151,12 +193,20 @@ __device__ __forceinline__ void compress_block(const CompressArgs& a, long long 
                               : static_cast<long long>(a.first_entry[s]) + i;
     dst = paged_row(a.out, dec ? static_cast<int>(s) : a.req[s], row, a.out_row_bytes);
   }
-  const float4 nw = a.norm_w != nullptr ? *reinterpret_cast<const float4*>(a.norm_w + c0)
-                                        : make_float4(1.f, 1.f, 1.f, 1.f);
+  float nw[CPT], cs[CPT];   // norm weights; (cos, sin) of this thread's CPT / 2 pairs
+  if (a.norm_w != nullptr) L::bias(*reinterpret_cast<const BiasT*>(a.norm_w + c0), nw);
+  else {
+#pragma unroll
+    for (int c = 0; c < CPT; ++c) nw[c] = 1.f;
+  }
   const bool rotate = a.rope_cs != nullptr && live && c0 >= D - 64;
-  const float4 cs = rotate ? *reinterpret_cast<const float4*>(
-                                 a.rope_cs + ((dec ? s : s * a.n + i) * 32 + (c0 - (D - 64)) / 2) * 2)
-                           : make_float4(1.f, 0.f, 1.f, 0.f);
+  if (rotate) {
+    L::bias(*reinterpret_cast<const BiasT*>(a.rope_cs + ((dec ? s : s * a.n + i) * 32 + (c0 - (D - 64)) / 2) * 2),
+            cs);
+  } else {
+#pragma unroll
+    for (int c = 0; c < CPT; c += 2) { cs[c] = 1.f; cs[c + 1] = 0.f; }
+  }
 
   // Slots are staged through shared memory in batches of kBatch with cp.async (the
   // next batch's copies in flight while this one is computed), then taken one at a
@@ -164,9 +214,9 @@ __device__ __forceinline__ void compress_block(const CompressArgs& a, long long 
   // a cold instruction cache, so its code stays small.  Each thread copies and reads
   // only its own channels, so no block barrier is needed around the stages.
   extern __shared__ __align__(16) uint8_t cmp_smem[];
-  uint2* s_kv = reinterpret_cast<uint2*>(cmp_smem);                 // [2][kBatch][128]
-  uint2* s_g = s_kv + 2 * kBatch * 128;                              // [2][kBatch][128]
-  float4* s_ap = reinterpret_cast<float4*>(s_g + 2 * kBatch * 128);  // [2][kBatch][128]
+  KvT* s_kv = reinterpret_cast<KvT*>(cmp_smem);                         // [2][kBatch][kThreads]
+  KvT* s_g = s_kv + 2 * kBatch * kThreads;                              // [2][kBatch][kThreads]
+  BiasT* s_ap = reinterpret_cast<BiasT*>(s_g + 2 * kBatch * kThreads);  // [2][kBatch][kThreads]
   const int t = threadIdx.x;
   const int nbatch = (slots + kBatch - 1) / kBatch;
   auto issue = [&](int bt) {
@@ -179,10 +229,10 @@ __device__ __forceinline__ void compress_block(const CompressArgs& a, long long 
         long long ao;
         slot_src(j, vp, gp, ao);
         if (vp != nullptr) {
-          cp_async8(&s_kv[(buf * kBatch + u) * 128 + t], vp);
-          if (gp != nullptr) cp_async8(&s_g[(buf * kBatch + u) * 128 + t], gp);
+          L::copy_kv(&s_kv[(buf * kBatch + u) * kThreads + t], vp);
+          if (gp != nullptr) L::copy_kv(&s_g[(buf * kBatch + u) * kThreads + t], gp);
         }
-        if (a.ape != nullptr) cp_async16(&s_ap[(buf * kBatch + u) * 128 + t], a.ape + ao);
+        if (a.ape != nullptr) L::copy_bias(&s_ap[(buf * kBatch + u) * kThreads + t], a.ape + ao);
       }
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
@@ -191,30 +241,48 @@ __device__ __forceinline__ void compress_block(const CompressArgs& a, long long 
   // slot_src, without its addresses): slot_at reads the staged copies by these alone
   const bool first_half_empty = a.overlap && i == 0 && a.prev_kv == nullptr;
   const bool first_half_gated = i > 0 ? a.gate != nullptr : a.prev_kv != nullptr;
-  // slot j's biased score (-inf for the empty half) and, if wanted, its value
-  auto slot_at = [&](int j, float4& sc, float4* v) {
+  // slot j's biased scores (-inf for the empty half) and, if wanted, its values
+  auto slot_at = [&](int j, float (&sc)[CPT], float* v) {
     const int buf = (j / kBatch) & 1, u = j % kBatch;
     const bool first = a.overlap && j < r;
     if (first && first_half_empty) {
-      sc = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-      if (v) *v = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int c = 0; c < CPT; ++c) {
+        sc[c] = -INFINITY;
+        if (v) v[c] = 0.f;
+      }
       return;
     }
     const bool gated = first ? first_half_gated : a.gate != nullptr;
-    const uint2 g = gated ? s_g[(buf * kBatch + u) * 128 + t] : make_uint2(0u, 0u);
+    float g[CPT], bb[CPT];
+    if (gated) L::kv(s_g[(buf * kBatch + u) * kThreads + t], g);
+    else {
+#pragma unroll
+      for (int c = 0; c < CPT; ++c) g[c] = 0.f;
+    }
     // no slot bias (ape == nullptr) adds +0: the same bits as a zero bias table
-    const float4 b = a.ape != nullptr ? s_ap[(buf * kBatch + u) * 128 + t] : make_float4(0.f, 0.f, 0.f, 0.f);
-    sc = make_float4(__fadd_rn(bf16lo(g.x), b.x), __fadd_rn(bf16hi(g.x), b.y), __fadd_rn(bf16lo(g.y), b.z),
-                     __fadd_rn(bf16hi(g.y), b.w));
+    if (a.ape != nullptr) L::bias(s_ap[(buf * kBatch + u) * kThreads + t], bb);
+    else {
+#pragma unroll
+      for (int c = 0; c < CPT; ++c) bb[c] = 0.f;
+    }
+#pragma unroll
+    for (int c = 0; c < CPT; ++c) sc[c] = __fadd_rn(g[c], bb[c]);
     if (v) {
-      const uint2 x = s_kv[(buf * kBatch + u) * 128 + t];
-      *v = make_float4(bf16lo(x.x), bf16hi(x.x), bf16lo(x.y), bf16hi(x.y));
+      float x[CPT];
+      L::kv(s_kv[(buf * kBatch + u) * kThreads + t], x);
+#pragma unroll
+      for (int c = 0; c < CPT; ++c) v[c] = x[c];
     }
   };
 
-  float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
-  float4 den = make_float4(0.f, 0.f, 0.f, 0.f);
-  float4 m = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+  float num[CPT], den[CPT], m[CPT];
+#pragma unroll
+  for (int c = 0; c < CPT; ++c) {
+    num[c] = 0.f;
+    den[c] = 0.f;
+    m[c] = -INFINITY;
+  }
   // pass 1: m = max over slots of the biased scores; pass 2: weights and slot-ordered
   // sums (the scores recomputed bit for bit).  One batch: the stage serves both passes.
 #pragma unroll 1
@@ -231,45 +299,54 @@ __device__ __forceinline__ void compress_block(const CompressArgs& a, long long 
       if (!live) continue;
 #pragma unroll 1
       for (int j = bt * kBatch; j < min(slots, (bt + 1) * kBatch); ++j) {
-        float4 sc, v;
+        float sc[CPT], v[CPT];
         if (pass == 1) {
           slot_at(j, sc, nullptr);
-          m.x = fmaxf(m.x, sc.x); m.y = fmaxf(m.y, sc.y); m.z = fmaxf(m.z, sc.z); m.w = fmaxf(m.w, sc.w);
+#pragma unroll
+          for (int c = 0; c < CPT; ++c) m[c] = fmaxf(m[c], sc[c]);
         } else {
-          slot_at(j, sc, &v);
-          const float e0 = exp_own(__fsub_rn(sc.x, m.x)), e1 = exp_own(__fsub_rn(sc.y, m.y));
-          const float e2 = exp_own(__fsub_rn(sc.z, m.z)), e3 = exp_own(__fsub_rn(sc.w, m.w));
-          num.x = __fadd_rn(num.x, __fmul_rn(e0, v.x)); den.x = __fadd_rn(den.x, e0);
-          num.y = __fadd_rn(num.y, __fmul_rn(e1, v.y)); den.y = __fadd_rn(den.y, e1);
-          num.z = __fadd_rn(num.z, __fmul_rn(e2, v.z)); den.z = __fadd_rn(den.z, e2);
-          num.w = __fadd_rn(num.w, __fmul_rn(e3, v.w)); den.w = __fadd_rn(den.w, e3);
+          slot_at(j, sc, v);
+#pragma unroll
+          for (int c = 0; c < CPT; ++c) {
+            const float e = exp_own(__fsub_rn(sc[c], m[c]));
+            num[c] = __fadd_rn(num[c], __fmul_rn(e, v[c]));
+            den[c] = __fadd_rn(den[c], e);
+          }
         }
       }
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
   }
-  float4 y = live ? make_float4(__fdiv_rn(num.x, den.x), __fdiv_rn(num.y, den.y),
-                                __fdiv_rn(num.z, den.z), __fdiv_rn(num.w, den.w))
-                  : make_float4(0.f, 0.f, 0.f, 0.f);
+  float y[CPT];
+#pragma unroll
+  for (int c = 0; c < CPT; ++c) y[c] = live ? __fdiv_rn(num[c], den[c]) : 0.f;
 
   if (a.norm_w != nullptr) {
-    const float local = __fadd_rn(__fadd_rn(__fmul_rn(y.x, y.x), __fmul_rn(y.y, y.y)),
-                                  __fadd_rn(__fmul_rn(y.z, y.z), __fmul_rn(y.w, y.w)));
-    const float ss = block_sum_pairwise<D>(local, threadIdx.x % 128);
+    float local;
+    if constexpr (CPT == 4) {
+      local = __fadd_rn(__fadd_rn(__fmul_rn(y[0], y[0]), __fmul_rn(y[1], y[1])),
+                        __fadd_rn(__fmul_rn(y[2], y[2]), __fmul_rn(y[3], y[3])));
+    } else {
+      local = __fadd_rn(__fmul_rn(y[0], y[0]), __fmul_rn(y[1], y[1]));
+    }
+    const float ss = block_sum_pairwise<D, CPT>(local);
     const float rr = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(D)), a.eps)));
-    y.x = __fmul_rn(__fmul_rn(y.x, rr), nw.x);
-    y.y = __fmul_rn(__fmul_rn(y.y, rr), nw.y);
-    y.z = __fmul_rn(__fmul_rn(y.z, rr), nw.z);
-    y.w = __fmul_rn(__fmul_rn(y.w, rr), nw.w);
+#pragma unroll
+    for (int c = 0; c < CPT; ++c) y[c] = __fmul_rn(__fmul_rn(y[c], rr), nw[c]);
   }
   if (rotate) {
-    const float y0 = y.x, y1 = y.y, y2 = y.z, y3 = y.w;
-    y.x = __fsub_rn(__fmul_rn(y0, cs.x), __fmul_rn(y1, cs.y));
-    y.y = __fadd_rn(__fmul_rn(y0, cs.y), __fmul_rn(y1, cs.x));
-    y.z = __fsub_rn(__fmul_rn(y2, cs.z), __fmul_rn(y3, cs.w));
-    y.w = __fadd_rn(__fmul_rn(y2, cs.w), __fmul_rn(y3, cs.z));
+#pragma unroll
+    for (int c = 0; c < CPT; c += 2) {
+      const float y0 = y[c], y1 = y[c + 1];
+      y[c] = __fsub_rn(__fmul_rn(y0, cs[c]), __fmul_rn(y1, cs[c + 1]));
+      y[c + 1] = __fadd_rn(__fmul_rn(y0, cs[c + 1]), __fmul_rn(y1, cs[c]));
+    }
   }
-  store_row_values(y, lt, a.out.fmt, D, dst, live && dst.data != nullptr);
+  if constexpr (CPT == 4) {
+    store_row_values(make_float4(y[0], y[1], y[2], y[3]), lt, a.out.fmt, D, dst, live && dst.data != nullptr);
+  } else {
+    store_row_values2<D>(y[0], y[1], lt, a.out.fmt, dst, live && dst.data != nullptr);
+  }
 }
 
 // Blocks of one entry (D = 512) or four entries (D = 128).
@@ -279,9 +356,9 @@ inline long long compress_blocks(int S, int n, int dim) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(128) compress_kernel(const CompressArgs a) {
+__global__ void __launch_bounds__(256) compress_kernel(const CompressArgs a) {
   grid_dep_launch();   // a programmatic dependent (the indexer's query prep) may start
-  compress_block<D>(a, blockIdx.x);
+  compress_block<D, 2>(a, blockIdx.x);
 }
 
 // Several jobs in one launch: block b belongs to the job j with first[j] <= b < first[j + 1].
@@ -293,13 +370,13 @@ struct CompressMany {
   int njobs;
 };
 
-__global__ void __launch_bounds__(128) compress_many_kernel(const __grid_constant__ CompressMany m) {
+__global__ void __launch_bounds__(256) compress_many_kernel(const __grid_constant__ CompressMany m) {
   grid_dep_launch();
   int j = 0;
   while (j + 1 < m.njobs && static_cast<long long>(blockIdx.x) >= m.first[j + 1]) ++j;
   const long long blk = blockIdx.x - m.first[j];
-  if (m.dim[j] == 512) compress_block<512>(m.job[j], blk);
-  else compress_block<128>(m.job[j], blk);
+  if (m.dim[j] == 512) compress_block<512, 2>(m.job[j], blk);
+  else compress_block<128, 2>(m.job[j], blk);
 }
 
 // ---------------------------------------------------------------------------
@@ -353,7 +430,7 @@ __device__ __forceinline__ void decode_block(const DecodeJob& q, long long blk) 
     __threadfence();   // the pooling below reads this slot back with cp.async
   }
   __syncthreads();
-  compress_block<D>(a, blk);
+  compress_block<D, 4>(a, blk);
   // the overlap shift (each thread moves its own channels, which the pooling has
   // finished reading: compress_block waits for all of its copies)
   if (ringed && a.overlap && p >= 0 && (p + 1) % r == 0) {
@@ -450,11 +527,11 @@ cudaError_t launch_compress(const void* kv, const void* gate, const void* prev_k
   if (dim == 512) {
     cudaFuncSetAttribute(compress_kernel<512>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          static_cast<int>(kCompressSmem));
-    compress_kernel<512><<<static_cast<unsigned>(total), 128, kCompressSmem, stream>>>(a);
+    compress_kernel<512><<<static_cast<unsigned>(total), 256, kCompressSmem, stream>>>(a);
   } else {
     cudaFuncSetAttribute(compress_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          static_cast<int>(kCompressSmem));
-    compress_kernel<128><<<static_cast<unsigned>((total + 3) / 4), 128, kCompressSmem, stream>>>(a);
+    compress_kernel<128><<<static_cast<unsigned>((total + 3) / 4), 256, kCompressSmem, stream>>>(a);
   }
   return cudaGetLastError();
 }
@@ -475,7 +552,7 @@ cudaError_t launch_compress_many(const cskv_compress_job* jobs, int njobs, cudaS
   if (m.first[njobs] == 0) return cudaSuccess;
   cudaFuncSetAttribute(compress_many_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        static_cast<int>(kCompressSmem));
-  compress_many_kernel<<<static_cast<unsigned>(m.first[njobs]), 128, kCompressSmem, stream>>>(m);
+  compress_many_kernel<<<static_cast<unsigned>(m.first[njobs]), 256, kCompressSmem, stream>>>(m);
   return cudaGetLastError();
 }
 
