@@ -179,3 +179,53 @@ def test_hca_layer_steps_with_and_without_a_completed_block(pinned):
             ref = o_attn.request_attention(q_v[b], int(ctx[b]), ratio, swa_dec[b], host_main.decoded[b], None,
                                            sink, SCALE)
             check_attention(got[b], ref)
+
+
+def test_captured_layer_step_reads_the_host_buffers_at_every_replay():
+    """The call captured once into a CUDA graph (as a serving loop, or the benchmark, runs
+    it): each replay copies the host buffer's current contents in and writes the current
+    output back, so new queries written into the same pinned buffer give new results."""
+    rs = np.random.default_rng(73)
+    ratio, H = 128, 16
+    n = [6, 2, 4]
+    B = len(n)
+    host_main, dev_main, _ = _caches(rs, codecs.FMT_FP8, 512, n, seed=14)
+    sink = rs.standard_normal(H).astype(np.float32)
+    swa_b, swa_dec = swa_ring(rs.standard_normal((B, 128, 512)).astype(np.float32), codecs.FMT_FP8)
+    ctx = np.array([ratio * x + 7 for x in n], np.int32)           # no block completes: no compressor job
+    q0_t, _ = bf16_values(rs.standard_normal((B, H, 512)).astype(np.float32))
+    h_in, d_in, v = _stage({"q": q0_t, "ctx": torch.from_numpy(ctx),
+                            "qcs": torch.from_numpy(cskv.rope_table(ctx - 1))})
+    h_out = torch.empty((B, H, 512), dtype=torch.bfloat16, pin_memory=True)
+    out = torch.empty((B, H, 512), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(cskv.sparse_decode_attn_workspace_size(B, H, int(ctx.max()), ratio, 0), dtype=torch.uint8,
+                     device="cuda")
+
+    swa_d, sink_d = cuda(swa_b), cuda(sink)   # device copies made before the capture
+
+    def call():
+        cskv.decode_layer([], None, None, None, v["q"], dev_main, swa_d, codecs.FMT_FP8, v["ctx"], 0, ratio,
+                          int(ctx.max()), sink_d, SCALE, v["qcs"], out=out, attn_workspace=ws,
+                          h_in=h_in, d_in=d_in, h_out=h_out)
+
+    call()                                        # outside the capture first
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call()
+    torch.cuda.synchronize()
+    q_view = h_in[:q0_t.numel() * 2].view(torch.bfloat16).view(q0_t.shape)   # "q" is the first part
+    for rep in range(3):
+        q_t, q_v = bf16_values(rs.standard_normal((B, H, 512)).astype(np.float32))
+        q_view.copy_(q_t)
+        h_out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert cskv.device_status() == 0
+        got = h_out.float().numpy()
+        for b in range(B):
+            ref = o_attn.request_attention(q_v[b], int(ctx[b]), ratio, swa_dec[b], host_main.decoded[b], None,
+                                           sink, SCALE)
+            check_attention(got[b], ref)
