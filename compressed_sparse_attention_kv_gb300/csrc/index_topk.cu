@@ -80,6 +80,7 @@ constexpr int kMaxGrid = 1024;       // bound of the per-block counters' table
 constexpr int kSeg = 32;             // entries per segment (one epilogue warp's rows of a tile)
 constexpr int kSelSegs = 8192;       // segments per selection pass (262,144 entries)
 constexpr int kReqCache = 64;        // requests whose visible count is kept in shared memory
+constexpr int kFastN = 2048;         // LARGE: requests of at most this many entries are selected by one warp
 constexpr int kScratch16 = kSelSegs + 64 - kScaleSlots * kTileRows * 2;   // u16 words after the scale ring
 
 struct WsLayout {
@@ -1061,6 +1062,9 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
         }
         continue;
       }
+      if constexpr (LARGE) {
+        if (nb <= kFastN) continue;   // one warp selects it, after this loop
+      }
       const uint32_t* smx = segmax_all + size_t(b) * segs_pad;
       unsigned long long* kbuf = reinterpret_cast<unsigned long long*>(a.ws + a.L.cand) + size_t(b) * a.L.n_pad;
       const int nseg = (nb + kSeg - 1) / kSeg;
@@ -1324,6 +1328,115 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
         }
       }
       __syncthreads();
+    }
+    if constexpr (LARGE) {
+      // Requests of more than k and at most kFastN visible entries (e.g. one prompt query
+      // each in prefill): one warp selects each from its scores in the workspace, the
+      // block's such requests taken by its warps in turn (a request belongs to the first
+      // block of its run).  Radix select on the order keys, four 8-bit digits from the
+      // top: the k-th largest key K and how many of the entries equal to K are taken (the
+      // ones of smallest index); then every entry above K and those, in entry order.
+      __syncthreads();   // the stage ring is free
+      uint32_t* wkeys = reinterpret_cast<uint32_t*>(stages) + warp * (kFastN + 256);
+      uint32_t* whist = wkeys + kFastN;
+      const unsigned full = 0xFFFFFFFFu;
+      int f = 0;
+      long long C2 = 0;
+      int bnext2 = 0;
+#pragma unroll 1
+      for (int w = 0; !aborted; ++w) {
+        int b = -1, fb = 0, nbk = 0;
+        long long lo = 0, hi = 0, per_b = 0;
+        if (nwork >= 0) {
+          if (w >= nwork) break;
+          const WorkItem wi = sm->work[w];
+          b = wi.b;
+          fb = wi.fb;
+        } else {
+#pragma unroll 1
+          while (bnext2 < a.B) {
+            const int bb = bnext2++;
+            const long long tb = (visible(a, bb) + kTileRows - 1) / kTileRows;
+            const bool mine = block_range(blockIdx.x, gridDim.x, C2, tb, total, lo, hi, fb, nbk, per_b);
+            C2 += tb;
+            if (mine) {
+              b = bb;
+              break;
+            }
+            if (fb > static_cast<int>(blockIdx.x)) bnext2 = a.B;
+          }
+          if (b < 0) break;
+        }
+        const int nb = b < kReqCache ? sm->nbv[b] : visible(a, b);
+        if (nb <= a.k || nb > kFastN || fb != static_cast<int>(blockIdx.x)) continue;
+        if ((f++ % nwarps) != warp) continue;
+        const float* sc = scores_all + size_t(b) * a.L.n_pad;
+        int32_t* out_idx = a.topk_idx + size_t(b) * a.k;
+        float* out_sc = a.topk_score ? a.topk_score + size_t(b) * a.k : nullptr;
+#pragma unroll 1
+        for (int j = lane; j < nb; j += 32) wkeys[j] = order_key(__ldcg(sc + j));
+        uint32_t prefix = 0, pmask = 0, need = static_cast<uint32_t>(a.k);
+#pragma unroll 1
+        for (int shift = 24; shift >= 0; shift -= 8) {
+#pragma unroll
+          for (int x = lane; x < 256; x += 32) whist[x] = 0;
+          __syncwarp();
+#pragma unroll 1
+          for (int j = lane; j < nb; j += 32) {
+            const uint32_t key = wkeys[j];
+            if ((key & pmask) == prefix) atomicAdd(&whist[(key >> shift) & 255u], 1u);
+          }
+          __syncwarp();
+          // lane l owns digits 255 - 8l down to 248 - 8l
+          uint32_t sum = 0;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) sum += whist[255 - 8 * lane - q];
+          uint32_t incl = sum;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t x = __shfl_up_sync(full, incl, o);
+            if (lane >= o) incl += x;
+          }
+          // never empty: the keys under the prefix number at least need
+          const unsigned hit = __ballot_sync(full, incl >= need);
+          const int src = __ffs(hit) - 1;
+          uint32_t d = 0, acc = incl - sum;
+          if (lane == src) {
+#pragma unroll 1
+            for (int q = 0; q < 8; ++q) {
+              const uint32_t c = whist[255 - 8 * lane - q];
+              if (acc + c >= need) {
+                d = static_cast<uint32_t>(255 - 8 * lane - q);
+                break;
+              }
+              acc += c;
+            }
+          }
+          d = __shfl_sync(full, d, src);
+          acc = __shfl_sync(full, acc, src);
+          need -= acc;
+          prefix |= d << shift;
+          pmask |= 255u << shift;
+          __syncwarp();
+        }
+        uint32_t pos = 0, eq_seen = 0;
+#pragma unroll 1
+        for (int base = 0; base < nb; base += 32) {
+          const int j = base + lane;
+          const uint32_t key = j < nb ? wkeys[j] : 0u;
+          const bool eq = j < nb && key == prefix;
+          const unsigned em = __ballot_sync(full, eq);
+          const bool take = (j < nb && key > prefix) || (eq && eq_seen + __popc(em & lt_mask) < need);
+          const unsigned tm = __ballot_sync(full, take);
+          if (take) {
+            const uint32_t p = pos + __popc(tm & lt_mask);
+            out_idx[p] = j;
+            if (out_sc) out_sc[p] = from_order_key(key);
+          }
+          pos += __popc(tm);
+          eq_seen += __popc(em);
+        }
+      }
     }
   }
 }
