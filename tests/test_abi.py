@@ -139,3 +139,25 @@ def test_binding_refuses_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(_lib, "_lib", None)
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         _lib.lib()
+
+
+def test_binding_refuses_host_tensors_for_device_arguments(lib):
+    """No silent CPU path: caches and every entry point's device arguments must be CUDA
+    tensors, and the binding says so before anything reaches the library."""
+    import torch
+    import compressed_sparse_attention_kv_gb300 as cskv
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        cskv.PagedCache(torch.zeros((1, 64 * 132), dtype=torch.uint8), torch.zeros((1, 1), dtype=torch.int32),
+                        cskv.FMT_FP8_PAGESPLIT, 128)
+    q = torch.zeros((1, 4, 128), dtype=torch.bfloat16)
+    w = torch.zeros((1, 4), dtype=torch.float32)
+    ctx = torch.ones(1, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        cskv.index_topk(q, w, None, ctx, 4, 1, 4)
+    qa = torch.zeros((1, 16, 512), dtype=torch.bfloat16)
+    swa = torch.zeros((1, 128, 528), dtype=torch.uint8)
+    cs = torch.zeros((1, 32, 2), dtype=torch.float32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        cskv.sparse_decode_attn(qa, None, swa, cskv.FMT_FP8, ctx, None, 0, 128, 4, None, 0.04, cs)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        cskv.decode_layer([], None, None, None, qa, None, swa, cskv.FMT_FP8, ctx, 0, 128, 4, None, 0.04, cs)
