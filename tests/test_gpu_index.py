@@ -8,7 +8,7 @@ import compressed_sparse_attention_kv_gb300 as cskv
 from compressed_sparse_attention_kv_gb300 import synth
 from oracle import codecs, indexer
 
-from cases import HostPaged, bf16_values, check_topk, cuda
+from cases import HostPaged, bf16_values, check_topk, cuda, swa_ring
 
 pytestmark = pytest.mark.gpu
 
@@ -192,3 +192,37 @@ def test_large_ragged_batch(fmt):
         q_hat = indexer.quantize_queries(q_v[b]) if fmt == codecs.FMT_FP8_PAGESPLIT else q_v[b].astype(np.float64)
         swaps += check_topk(idx[b], sc[b], q_hat, w[b], cache.decoded[b][:nb], nb, k)
     assert swaps <= 2
+
+
+def test_results_are_identical_run_to_run():
+    """Dynamic tile scheduling and atomic histograms leave no trace in the results: two
+    runs of the indexer and the attention give the same bits (each score is one thread's
+    fixed-order sum, the counts are order-free, partials are merged in tile order)."""
+    ratio, k, Hi, H = 4, 512, 64, 64
+    ctx = [4 * 60000 + 1, 4 * 41000, 4 * 9000 + 3, 4 * 70000 + 2, 4 * 513, 4 * 30000]
+    n = [c // ratio for c in ctx]
+    rs = np.random.default_rng(80)
+    keys = HostPaged(codecs.FMT_FP8_PAGESPLIT, 128, n, seed=81)
+    main = HostPaged(codecs.FMT_FP8, 512, n, seed=82)
+    for b, nb in enumerate(n):
+        keys.fill(b, rs.standard_normal((nb, 128)).astype(np.float32))
+        main.fill(b, rs.standard_normal((nb, 512)).astype(np.float32))
+    qi_t, _ = bf16_values(rs.standard_normal((len(ctx), Hi, 128)).astype(np.float32))
+    q_t, _ = bf16_values(rs.standard_normal((len(ctx), H, 512)).astype(np.float32))
+    w = cuda(rs.uniform(0, 1, (len(ctx), Hi)).astype(np.float32))
+    swa = cuda(swa_ring(rs.standard_normal((len(ctx), 128, 512)).astype(np.float32), codecs.FMT_FP8)[0])
+    sink = cuda(rs.standard_normal(H).astype(np.float32))
+    ctx_d = cuda(np.asarray(ctx, np.int32))
+    cs = cuda(cskv.rope_table(np.asarray(ctx) - 1))
+    kd, md = keys.to_device(), main.to_device()
+    runs = []
+    for _ in range(3):
+        idx, sc = cskv.index_topk(qi_t.cuda(), w, kd, ctx_d, ratio, k, max(ctx))
+        out = cskv.sparse_decode_attn(q_t.cuda(), md, swa, codecs.FMT_FP8, ctx_d, idx, k, ratio, max(ctx), sink,
+                                      512 ** -0.5, cs)
+        runs.append((idx.clone(), sc.clone(), out.clone()))
+    assert cskv.device_status() == 0
+    for idx, sc, out in runs[1:]:
+        assert torch.equal(idx, runs[0][0])
+        assert torch.equal(sc.view(torch.int32), runs[0][1].view(torch.int32))
+        assert torch.equal(out.view(torch.int16), runs[0][2].view(torch.int16))
