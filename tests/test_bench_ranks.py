@@ -1,6 +1,6 @@
 """The bench's host logic on CPU: max over ranks of the per-rank step times (gloo, two
-processes), whole-job throughput, the reference arm's rank > 0 exit, and the clock
-record's window."""
+processes), whole-job throughput, the reference arm's rank > 0 exit and its JSON line,
+and the clock record's window."""
 
 import os
 import socket
@@ -99,3 +99,22 @@ def test_clock_samples_are_taken_from_the_timed_region():
     got = c.stop()
     assert got["window"] == "around the timed region" and got["samples"] == 2
     assert got["reasons"] == ["sw_thermal_slowdown"]
+
+
+def test_reference_arm_prints_the_contract_line():
+    """`bench.py --impl reference` (the oracle on the host cores) prints one JSON line with
+    the benchmark's metric and unit, its own cpu_baseline and a zero-copy e2e object."""
+    import json
+    import bench
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "3"], capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC and line["unit"] == "queries/s"
+    assert line["higher_is_better"] is True and line["steps"] == 1 and line["warmup"] == 3
+    assert line["value"] > 0 and line["ms_per_step"] > 0
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": "queries/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    assert "workload" in line["config"]
