@@ -165,3 +165,31 @@ def test_v41_global_kv_decomposition(golden):
     copies = g["encoder_copies"] / g["encoder_merge"] + g["decoder_copies"] / g["decoder_merge"]
     fp4_index_key = 128 // 2 + 128 // 32
     assert copies * (codecs.row_bytes(codecs.FMT_FP4, 512) + fp4_index_key) == g["bytes_per_token"]
+
+
+def test_fp4_scale_is_rne_e4m3_of_amax_over_six():
+    """The FP4 block scale ("DeepSeek-V4.1-Flash" diagram: an E4M3 scale per 16
+    channels) is read as RNE_e4m3(fp32(amax / 6)).  Pinned against PyTorch's own
+    float8_e4m3fn cast of the same fp32 quotient: every e4m3 value, every midpoint
+    between neighbours (ties go to the even code, so a rounding-up rule fails here)
+    and random amax values."""
+    vals = codecs.e4m3_decode(np.arange(1, 0x7F, dtype=np.uint8))
+    mids = (vals[:-1] + vals[1:]) / 2
+    # values and midpoints times 6 are exact in fp32, and so are their quotients by 6
+    exact = np.concatenate([vals, mids]) * 6.0
+    assert np.all(exact.astype(np.float32).astype(np.float64) == exact)
+    rs = np.random.default_rng(17)
+    amax = np.concatenate([exact, rs.uniform(2.0 ** -9, 2640.0, 4000),
+                           6.0 * np.exp2(rs.uniform(-9, 8.7, 4000))]).astype(np.float32)
+    x = np.zeros((len(amax), 16), np.float32)
+    x[:, 3] = amax
+    x[:, 7] = -amax * np.float32(0.5)
+    _, s_code = codecs.fp4_encode(x)
+    want = _torch_e4m3_bits((amax / np.float32(6.0)).astype(np.float32))
+    assert np.array_equal(s_code[:, 0], want)
+    # the midpoints, alone: the even neighbour (an upward rounding would take the odd one)
+    mid_amax = (mids * 6.0).astype(np.float32)
+    xm = np.zeros((len(mids), 16), np.float32)
+    xm[:, 0] = mid_amax
+    _, mcode = codecs.fp4_encode(xm)
+    assert np.all(mcode[:, 0] % 2 == 0)

@@ -227,3 +227,60 @@ def test_rope_table_and_frequencies():
     n0 = np.hypot(y[:, -64::2], y[:, -63::2])
     n1 = np.hypot(r[:, -64::2], r[:, -63::2])
     assert np.allclose(n0, n1, rtol=1e-6) and np.array_equal(y[:, :448], r[:, :448])
+
+
+# ---------------------------------------------------------------- overlap halves
+
+@pytest.mark.parametrize("render", ["fp64", "contract"])
+def test_overlap_channel_halves_by_perturbation(render):
+    """"DeepSeek-V4 deep dive", section 4.2 (the overlap transform): every token feeds two
+    entries - the next block's entry through channel half 0 (as part of its previous
+    block) and its own block's entry through half 1.  So perturbing half 0 of token 4i+j
+    may change entry i+1 only (and must change it), and perturbing half 1 may change
+    entry i only (and must change it).  The halves are perturbed one at a time."""
+    rs = np.random.default_rng(12)
+    D, T = 8, 24
+    kv = rs.standard_normal((T, 2, D)).astype(np.float32)
+    gate = rs.standard_normal((T, 2, D)).astype(np.float32)
+    ape = rs.standard_normal((4, 2 * D)).astype(np.float32)
+    run = ((lambda k, g, a: compress.compress_fp64(k, g, a, 4, True)) if render == "fp64"
+           else (lambda k, g, a: compress.compress_contract(k, g, a, 4, True)))
+    base = run(kv, gate, ape)
+    n = T // 4
+    for tok in range(T):
+        i = tok // 4
+        for half, expect in ((0, i + 1), (1, i)):
+            kv2 = kv.copy()
+            kv2[tok, half] += np.float32(0.75)
+            out = run(kv2, gate, ape)
+            changed = [e for e in range(n) if not np.array_equal(out[e], base[e])]
+            want = [expect] if expect < n else []
+            assert changed == want, (render, tok, half, changed, want)
+
+
+def test_overlap_slot_bias_halves_pick_the_right_tokens():
+    """The slot bias is added before the overlap transform (section 4.2): slots 0-3 (the
+    previous block, channel half 0) carry ape[:, :D], slots 4-7 (the entry's own block,
+    half 1) carry ape[:, D:].  A dominant bias on one slot of one half makes that slot's
+    token win the softmax, so the pooled channel equals that token's value in that half:
+    ape[j, c] (half 0) gives token 4(i-1)+j's half-0 value to entry i >= 1, and
+    ape[j, D + c] gives token 4i+j's half-1 value to entry i."""
+    rs = np.random.default_rng(13)
+    D, T = 16, 20
+    kv = rs.standard_normal((T, 2, D)).astype(np.float32)
+    gate = (0.1 * rs.standard_normal((T, 2, D))).astype(np.float32)
+    for j in range(4):
+        for c in (0, 5, D - 1):
+            for half in (0, 1):
+                ape = np.zeros((4, 2 * D), np.float32)
+                ape[j, half * D + c] = 80.0
+                for render in (compress.compress_fp64, compress.compress_contract):
+                    out = render(kv, gate, ape, 4, True)
+                    for i in range(T // 4):
+                        if half == 0:
+                            if i == 0:
+                                continue      # no previous block: its slots weigh nothing
+                            want = kv[4 * (i - 1) + j, 0, c]
+                        else:
+                            want = kv[4 * i + j, 1, c]
+                        assert np.float32(out[i, c]) == want, (render.__name__, j, c, half, i)
