@@ -1280,9 +1280,11 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
         uint32_t sum = 0;
 #pragma unroll 1
         for (int q = 0; q < per && d0 - q >= 0; ++q) sum += dh[d0 - q];
+        // read before place(): its barriers order every thread's read before the
+        // owning thread's update below, so no thread can see the updated count
+        const uint32_t need = sm->need;
         uint32_t tot;
         const uint32_t before = place(sum, tot);
-        const uint32_t need = sm->need;
         if (sum > 0 && before < need && before + sum >= need) {
           uint32_t accd = before;
           int d = d0;
