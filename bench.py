@@ -37,11 +37,19 @@ sys.path.insert(0, ROOT)
 from compressed_sparse_attention_kv_gb300 import synth  # noqa: E402
 
 METRIC = "decode attn queries/s per layer at 1M ctx; KV-read GB/s and % of HBM/FP8 roofline"
+MIXED_METRIC = "mixed-batch MXFP4 CSA decode: queries/s per layer (batch 64, contexts 32K-512K)"
 WORKLOAD = "csa_1m"
 L2_FLUSH_BYTES = 512 << 20
 
 
 def workload_desc(wl):
+    if wl.name == "mixed_mxfp4":
+        return ("Mixed-batch MXFP4 CSA decode: batch %d, contexts %d..%d tokens (U{32768..524288}, seed 4; "
+                "%d entries in all) at ratio %d, paged 64-row blocks shuffled in a pool, indexer %d heads x 128 "
+                "FP8 keys (132 B), top-%d, %d query heads x 512 over MXFP4-288 entries (E2M1 + E4M3 per 16) + "
+                "FP8 window 128, sink; per step: compress the completed block (main + index key), index_topk, "
+                "sparse_decode_attn" % (wl.B, int(wl.ctx_len.min()), int(wl.ctx_len.max()),
+                                        int(wl.n_entries.sum()), wl.ratio, wl.Hi, wl.k, wl.H))
     return ("CSA decode at 1M context: batch %d, %d tokens -> %d entries at ratio %d, indexer %d heads "
             "x 128 FP8 keys (132 B) w~U(0,1), top-%d, %d query heads x 512 over FP8-528 entries "
             "+ FP8 window 128, sink; per step: compress the completed block (main + index key), "
@@ -136,19 +144,21 @@ def gen_parallel(fn, items, threads=16):
 
 
 def build_caches(wl, torch, cskv):
-    """Resident caches: index keys (FP8 page-split), main entries (FP8-528), window ring (FP8-528)."""
+    """Resident caches: index keys (FP8 page-split), main entries (the workload's format), window ring (FP8-528)."""
     dev = "cuda"
     bt_i, np_i = synth.page_tables(wl, "index")
     bt_m, np_m = synth.page_tables(wl, "main")
     keys = cskv.PagedCache(torch.zeros((np_i, 64 * 132), dtype=torch.uint8, device=dev),
                            torch.from_numpy(bt_i).to(dev), cskv.FMT_FP8_PAGESPLIT, 128)
-    main = cskv.PagedCache(torch.zeros((np_m, 64 * 528), dtype=torch.uint8, device=dev),
-                           torch.from_numpy(bt_m).to(dev), cskv.FMT_FP8, 512)
-    ppr = int(wl.pages_per_req()[0])
-    rows = torch.arange(ppr * 64, dtype=torch.int32, device=dev)
+    mrb = cskv.row_bytes(wl.main_fmt, 512)
+    main = cskv.PagedCache(torch.zeros((np_m, (64 * mrb + 15) // 16 * 16), dtype=torch.uint8, device=dev),
+                           torch.from_numpy(bt_m).to(dev), wl.main_fmt, 512)
+    pprs = wl.pages_per_req()
     for lane, cache, dim in (("index", keys, 128), ("main", main, 512)):
         f = synth.index_page_values if lane == "index" else synth.main_page_values
         for b in range(wl.B):
+            ppr = int(pprs[b])
+            rows = torch.arange(ppr * 64, dtype=torch.int32, device=dev)
             pages = gen_parallel(lambda p: f(wl, b, p), range(ppr))
             vals = torch.from_numpy(np.concatenate(pages)).to(dev)
             cskv.encode_rows(vals, cache, req=torch.full_like(rows, b), row=rows)
@@ -177,17 +187,17 @@ def job_throughput(world, per_rank_batch, ms):
     return world * per_rank_batch / (ms * 1e-3)
 
 
-def run_gpu(args, rank, world):
+def run_gpu(args, rank, world, workload=WORKLOAD):
     import torch
     import compressed_sparse_attention_kv_gb300 as cskv
     from compressed_sparse_attention_kv_gb300 import _lib
 
     _lib.lib()
     dev = "cuda"
-    wl = synth.workload(WORKLOAD)
+    wl = synth.workload(workload)
     B, H, Hi, k, r = wl.B, wl.H, wl.Hi, wl.k, wl.ratio
-    L = int(wl.ctx_len[0])
-    n = L // r
+    L = wl.max_ctx
+    n_b = wl.n_entries.astype(np.int64)
     t_setup = time.time()
     keys, main, swa = build_caches(wl, torch, cskv)
     inp = step_inputs(wl)
@@ -201,10 +211,10 @@ def run_gpu(args, rank, world):
         "pgate": torch.from_numpy(inp["pgate"]).to(bf), "ikv": torch.from_numpy(inp["ikv"]).to(bf),
         "igate": torch.from_numpy(inp["igate"]).to(bf), "ipkv": torch.from_numpy(inp["ipkv"]).to(bf),
         "ipgate": torch.from_numpy(inp["ipgate"]).to(bf),
-        "ecs": torch.from_numpy(cskv.rope_table(np.full((B, 1), (n - 1) * r))),
+        "ecs": torch.from_numpy(cskv.rope_table(((n_b - 1) * r)[:, None])),
         "qcs": torch.from_numpy(cskv.rope_table(wl.ctx_len - 1)),
         "ctx": torch.from_numpy(wl.ctx_len.astype(np.int32)),
-        "first": torch.full((B,), n - 1, dtype=torch.int32),
+        "first": torch.from_numpy((n_b - 1).astype(np.int32)),
     }
     # the step's inputs live in one pinned host buffer and one device buffer (views at
     # 256-byte offsets), so that the end-to-end leg moves them with a single copy
@@ -245,7 +255,7 @@ def run_gpu(args, rank, world):
         cskv.compress_many(jobs)
         cskv.index_topk(d["q_idx"], d["w"], keys, d["ctx"], r, k, L, topk_idx=topk, workspace=ws_i,
                         want_scores=False)
-        cskv.sparse_decode_attn(d["q"], main, swa, cskv.FMT_FP8, d["ctx"], topk, k, r, L, sink,
+        cskv.sparse_decode_attn(d["q"], main, swa, wl.swa_fmt, d["ctx"], topk, k, r, L, sink,
                                 cskv.DEFAULT_SCALE, d["qcs"], out=out, workspace=ws_a)
 
     launches_per_step = 1 + 2 + 2   # compressor (both caches), indexer prep + score/select, attention tiles + combine
@@ -327,7 +337,7 @@ def run_gpu(args, rank, world):
     d2h = out.numel() * out.element_size()
 
     def layer_call():
-        cskv.decode_layer(jobs, d["q_idx"], d["w"], keys, d["q"], main, swa, cskv.FMT_FP8, d["ctx"], k, r, L, sink,
+        cskv.decode_layer(jobs, d["q_idx"], d["w"], keys, d["q"], main, swa, wl.swa_fmt, d["ctx"], k, r, L, sink,
                           cskv.DEFAULT_SCALE, d["qcs"], topk_idx=topk, out=out, index_workspace=ws_i,
                           attn_workspace=ws_a, h_in=host_buf, d_in=dev_buf, h_out=out_host)
 
@@ -372,10 +382,11 @@ def run_gpu(args, rank, world):
     peak = peaks.get("hbm_gbs", 6800.0)
     achieved = algo_bytes / (score_mean * 1e-3) / 1e9
     traffic = profiled_traffic()
-    path_bytes = algo_bytes + B * (640 * 528 + 2 * 64 * 512 + 64 * 128 * 2)
+    path_bytes = algo_bytes + B * (512 * cskv.row_bytes(wl.main_fmt, 512) + 128 * 528 + 2 * H * 512 * 2
+                                   + Hi * 128 * 2)
 
     res = {
-        "metric": METRIC,
+        "metric": METRIC if workload == WORKLOAD else MIXED_METRIC,
         "value": job_throughput(world, B, mean_ms),
         "unit": "queries/s",
         "n_gpus": world,
@@ -389,7 +400,7 @@ def run_gpu(args, rank, world):
         "data": "synthetic (seeded N(0,1) caches and queries, U(0,1) head weights)",
         "config": {"workload": workload_desc(wl), "batch_per_gpu": B, "context": L,
                    "l2": "flushed before every timed step (512 MB write, outside the timed region); "
-                         "inputs (277 MB of index keys) also exceed L2",
+                         "inputs (%d MB of index keys) also exceed L2" % (algo_bytes // 1000000),
                    "timing": "CUDA events per step around a CUDA-graph replay" if graph else "CUDA events per step",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"kernel": "index_score_kernel (FP8 keys, tcgen05 e4m3 MMA)", "bound": "hbm",
@@ -441,12 +452,12 @@ class OracleRunner:
         for b in self.req:
             vals = synth.request_values(wl, b, "index")
             self.keys[b] = codecs.encode_pagesplit(vals)
-            self.swa[b] = codecs.encode_rows(synth.swa_values(wl, b), codecs.FMT_FP8)
+            self.swa[b] = codecs.encode_rows(synth.swa_values(wl, b), wl.swa_fmt)
             # cache preparation (untimed): code the main pages this request's selection reads
             ent, ik = self._compress(b)
             top = self._topk(b, ik)
             pages = sorted(set(int(j) // 64 for j in top if j >= 0))
-            self.main_pages[b] = {p: codecs.encode_rows(synth.main_page_values(wl, b, p), codecs.FMT_FP8)
+            self.main_pages[b] = {p: codecs.encode_rows(synth.main_page_values(wl, b, p), wl.main_fmt)
                                   for p in pages}
 
     @staticmethod
@@ -474,7 +485,7 @@ class OracleRunner:
         wl, inp = self.wl, self.inp
         n = int(wl.n_entries[b])
         k_hat = codecs.decode_pagesplit(self.keys[b], 128)
-        k_hat[n - 1] = codecs.fp8_decode(*codecs.fp8_encode(ik))[0]
+        k_hat[n - 1] = codecs.fp8_decode(*codecs.fp8_encode(ik, block=128), block=128)[0]   # one scale per key
         top, _ = indexer.index_topk(self._bf(inp["q_idx"][b]), inp["w"][b], k_hat, int(wl.ctx_len[b]),
                                     wl.ratio, wl.k, True)
         return top
@@ -487,7 +498,8 @@ class OracleRunner:
         ent, ik = self._compress(b)
         top = self._topk(b, ik)
         pages = self.main_pages[b]
-        ent_row = codecs.decode_rows(codecs.encode_rows(ent, codecs.FMT_FP8), codecs.FMT_FP8, 512)[0]
+        mf = wl.main_fmt
+        ent_row = codecs.decode_rows(codecs.encode_rows(ent, mf), mf, 512)[0]
 
         def rows(ids):
             out = np.empty((len(ids), 512))
@@ -496,10 +508,10 @@ class OracleRunner:
                 if j == n - 1:
                     out[i] = ent_row
                 else:
-                    out[i] = codecs.decode_rows(pages[j // 64][j % 64:j % 64 + 1], codecs.FMT_FP8, 512)[0]
+                    out[i] = codecs.decode_rows(pages[j // 64][j % 64:j % 64 + 1], mf, 512)[0]
             return out
 
-        swa_dec = codecs.decode_rows(self.swa[b], codecs.FMT_FP8, 512)
+        swa_dec = codecs.decode_rows(self.swa[b], wl.swa_fmt, 512)
         return attention.request_attention(self._bf(inp["q"][b]), int(wl.ctx_len[b]), wl.ratio, swa_dec, rows,
                                            top, inp["sink"], 512 ** -0.5)
 
@@ -536,17 +548,123 @@ def run_reference(args):
     }
 
 
+ONE_CORE_VARS = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS",
+                 "NUMEXPR_NUM_THREADS", "VECLIB_MAXIMUM_THREADS")
+
+
+def _bf32(x):
+    from oracle import codecs
+    return codecs.bf16_decode(codecs.bf16_encode(x)).astype(np.float32)
+
+
+def oracle_sample(mode):
+    """The oracle timed on a bounded sample of a mode's workload (set-up untimed).
+    Returns dict(value, unit, higher_is_better, sample)."""
+    from oracle import attention, codecs, compress, indexer, rope
+    if mode in ("decode", "mixed"):
+        wl = synth.workload(WORKLOAD if mode == "decode" else "mixed_mxfp4")
+        reqs = [0, 1]
+        runner = OracleRunner(wl, reqs)
+        t0 = time.perf_counter()
+        for b in reqs:
+            runner.query(b)
+        dt = (time.perf_counter() - t0) / len(reqs)
+        ctx = ", ".join("%d" % int(wl.ctx_len[b]) for b in reqs)
+        return dict(value=1.0 / dt, unit="queries/s", higher_is_better=True,
+                    sample="requests 0 and 1 of the batch (contexts %s tokens): compress the completed block "
+                           "(main entry + index key), index_topk over every visible key, attention; numpy" % ctx)
+    if mode == "tiny":
+        wl = synth.workload("tiny_csa")
+        T, r, n = 4096, 4, 1024
+        lanes = {}
+        for lane, dim, il in (("main", 512, False), ("index", 128, True)):
+            kv, gate = synth.compressor_tokens(wl.seed, T, r, True, dim, index_lane=il)
+            ape, nw = synth.compressor_params(wl.seed, r, True, dim, index_lane=il)
+            kv, gate = _bf32(kv), _bf32(gate)
+            ents = compress.compress_contract(kv, gate, ape, r, True, norm_w=nw, rope_cs=rope.table(np.arange(n) * r))
+            lanes[lane] = (kv, gate, ape, nw, codecs.encode_rows(ents, codecs.FMT_BF16))
+        q, q_idx, w, sink = synth.queries(wl)
+        swa = codecs.encode_rows(synth.swa_values(wl, 0), codecs.FMT_BF16)
+
+        def step():
+            rows = {}
+            for lane, dim in (("main", 512), ("index", 128)):
+                kv, gate, ape, nw, cache = lanes[lane]
+                e = compress.compress_contract(kv[-4:], gate[-4:], ape, r, True, prev_kv=kv[-8:-4], prev_gate=gate[-8:-4],
+                                               norm_w=nw, rope_cs=rope.table(np.array([(n - 1) * r])))
+                c = cache.copy()
+                c[n - 1] = codecs.encode_rows(e, codecs.FMT_BF16)[0]
+                rows[lane] = codecs.decode_rows(c, codecs.FMT_BF16, dim)
+            top, _ = indexer.index_topk(_bf32(q_idx[0]), w[0], rows["index"], T, r, wl.k, False)
+            return attention.request_attention(_bf32(q[0]), T, r, codecs.decode_rows(swa, codecs.FMT_BF16, 512),
+                                               rows["main"], top, sink, 512 ** -0.5)
+        step()
+        reps = 3
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            step()
+        dt = (time.perf_counter() - t0) / reps
+        return dict(value=dt * 1e6, unit="us", higher_is_better=False,
+                    sample="the whole step of the one request, 3 repetitions (compress main entry + index key, "
+                           "index_topk over 1024 bf16 keys, attention over 128 + 512 bf16 rows); numpy")
+    if mode == "hca":
+        wl = synth.workload("hca_128k")
+        reqs = [0, 1]
+        data = {}
+        for b in reqs:
+            main = codecs.encode_rows(synth.request_values(wl, b, "main"), codecs.FMT_FP8)
+            data[b] = (main, codecs.encode_rows(synth.swa_values(wl, b), codecs.FMT_FP8))
+        q, _, _, sink = synth.queries(wl)
+        t0 = time.perf_counter()
+        for b in reqs:
+            main, swa = data[b]
+            attention.request_attention(_bf32(q[b]), int(wl.ctx_len[b]), wl.ratio,
+                                        codecs.decode_rows(swa, codecs.FMT_FP8, 512),
+                                        codecs.decode_rows(main, codecs.FMT_FP8, 512), None, sink, 512 ** -0.5)
+        dt = (time.perf_counter() - t0) / len(reqs)
+        return dict(value=1.0 / dt, unit="queries/s", higher_is_better=True,
+                    sample="requests 0 and 1: decode of the 1,024 FP8 entries and 128 window rows, attention over "
+                           "all of them with 64 heads; numpy")
+    if mode.startswith("compress"):
+        _, r, fmt = mode.split(":")
+        r, fmt = int(r), int(fmt)
+        overlap = r == 4
+        T = 2048 if r == 4 else 8192
+        kv, gate = synth.compressor_tokens(3, T, r, overlap, 512)
+        ape, nw = synth.compressor_params(3, r, overlap, 512)
+        kv, gate = _bf32(kv), _bf32(gate)
+        cs = rope.table(np.arange(T // r) * r)
+        t0 = time.perf_counter()
+        ents = compress.compress_contract(kv, gate, ape, r, overlap, norm_w=nw, rope_cs=cs)
+        codecs.encode_rows(ents, fmt)
+        dt = time.perf_counter() - t0
+        return dict(value=T / dt, unit="tokens/s", higher_is_better=True,
+                    sample="the first %d tokens of the chunk (%d entries), fp32 contract + coding; numpy" % (T, T // r))
+    raise ValueError(mode)
+
+
+def cpu_baseline(mode="decode"):
+    """The oracle on a bounded sample of the mode's workload: on every host core (this
+    process, BLAS threads as numpy starts them) and on one core (a child process pinned to
+    one CPU, every BLAS / OpenMP thread count set to 1)."""
+    allc = oracle_sample(mode)
+    res = {"value": allc["value"], "unit": allc["unit"], "cores": cores_used(), "kind": "oracle",
+           "sample": allc["sample"]}
+    env = dict(os.environ)
+    for v in ONE_CORE_VARS:
+        env[v] = "1"
+    try:
+        out = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample", mode, "--one-core"],
+                             env=env, capture_output=True, text=True, timeout=600)
+        one = json.loads(out.stdout.strip().splitlines()[-1])
+        res["one_core"] = {"value": one["value"], "unit": one["unit"], "cores": 1}
+    except Exception as e:  # the all-cores figure stands on its own
+        res["one_core"] = {"value": None, "error": repr(e)[:200]}
+    return res
+
+
 def cpu_baseline_sample():
-    """The oracle timed on a bounded sample (2 queries) of the benchmark workload."""
-    wl = synth.workload(WORKLOAD)
-    runner = OracleRunner(wl, [0, 1])
-    t0 = time.perf_counter()
-    for b in (0, 1):
-        runner.query(b)
-    dt = time.perf_counter() - t0
-    return {"value": 2.0 / dt, "unit": "queries/s", "cores": cores_used(), "kind": "oracle",
-            "sample": "2 of the 8 queries of one batch (requests 0 and 1), full 1M context each; "
-                      "numpy, BLAS threads for the score product"}
+    return cpu_baseline("decode")
 
 
 # ----------------------------------------------------------------------------- next-row modes
@@ -802,6 +920,175 @@ def run_next_row(args):
                   "ms_per_launch": m, "traffic": None}, clocks, 2 + 2, args)
 
 
+# ----------------------------------------------------------------------------- the other configurations
+# The tiny CSA layer, the HCA layer at 128K, the compressor's 65,536-token chunk and the
+# mixed-batch MXFP4 layer (the last through run_gpu, the decode step's own path).  Each
+# prints a JSON line of its own with the roofline of its step, the oracle's CPU figure and
+# the clocks; they are measurements of the other named workloads, not the benchmark.
+
+def _peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return pk["hbm_gbs"], "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def run_config_mode(args):
+    import torch
+    import compressed_sparse_attention_kv_gb300 as cskv
+    peak, psrc = _peak()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    bf = torch.bfloat16
+    dev = "cuda"
+
+    def roof(kernel, algo, ms, bound="hbm"):
+        ach = algo / (ms * 1e-3) / 1e9
+        return {"kernel": kernel, "bound": bound, "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
+                "peak_source": psrc, "algorithmic_bytes_per_launch": algo, "ms_per_launch": ms, "traffic": None}
+
+    def finish(line, mode):
+        if not args.no_cpu_baseline:
+            try:
+                line["cpu_baseline"] = cpu_baseline(mode)
+            except Exception as e:
+                line["cpu_baseline"] = {"value": None, "error": repr(e)[:200]}
+        return line
+
+    if args.mode == "tiny":
+        wl = synth.workload("tiny_csa")
+        T, r, n, k, H, Hi = 4096, 4, 1024, wl.k, wl.H, wl.Hi
+        zero = torch.zeros(1, dtype=torch.int32, device=dev)
+        caches, jobs = {}, []
+        for lane, dim, il in (("main", 512, False), ("index", 128, True)):
+            kv, gate = synth.compressor_tokens(wl.seed, T, r, True, dim, index_lane=il)
+            ape, nw = synth.compressor_params(wl.seed, r, True, dim, index_lane=il)
+            kv_t = torch.from_numpy(kv).to(bf)[None].to(dev)
+            g_t = torch.from_numpy(gate).to(bf)[None].to(dev)
+            ape_t, nw_t = torch.from_numpy(ape).to(dev), torch.from_numpy(nw).to(dev)
+            cache = cskv.PagedCache(torch.zeros((n // 64, 64 * dim * 2), dtype=torch.uint8, device=dev),
+                                    torch.arange(n // 64, dtype=torch.int32, device=dev)[None], cskv.FMT_BF16, dim)
+            cskv.compress(kv_t, g_t, ape_t, r, True, cache, zero, zero, norm_w=nw_t,
+                          rope_cs=torch.from_numpy(cskv.rope_table(np.arange(n) * r)[None]).to(dev))
+            caches[lane] = cache
+            # the step's completed block: the last 4 tokens, with the 4 before them as the previous block
+            jobs.append(dict(kv=kv_t[:, -4:].contiguous(), gate=g_t[:, -4:].contiguous(), ape=ape_t, ratio=r,
+                             overlap=True, out=cache, req=zero,
+                             first_entry=torch.full((1,), n - 1, dtype=torch.int32, device=dev),
+                             prev_kv=kv_t[:, -8:-4].contiguous(), prev_gate=g_t[:, -8:-4].contiguous(), norm_w=nw_t,
+                             rope_cs=torch.from_numpy(cskv.rope_table(np.array([[(n - 1) * r]]))).to(dev)))
+        q, q_idx, w, sink = synth.queries(wl)
+        q = torch.from_numpy(q).to(bf).to(dev)
+        q_idx = torch.from_numpy(q_idx).to(bf).to(dev)
+        w, sink = torch.from_numpy(w).to(dev), torch.from_numpy(sink).to(dev)
+        swa = torch.zeros((1, 128, 1024), dtype=torch.uint8, device=dev)
+        cskv.encode_rows(torch.from_numpy(synth.swa_values(wl, 0)).to(dev),
+                         cskv.PagedCache(swa.view(2, 64 * 1024), None, cskv.FMT_BF16, 512))
+        ctx = torch.full((1,), T, dtype=torch.int32, device=dev)
+        qcs = torch.from_numpy(cskv.rope_table(np.array([T - 1]))).to(dev)
+        topk = torch.empty((1, k), dtype=torch.int32, device=dev)
+        out = torch.empty_like(q)
+        ws_i = torch.empty(cskv.index_topk_workspace_size(1, T, r, Hi, k), dtype=torch.uint8, device=dev)
+        ws_a = torch.empty(cskv.sparse_decode_attn_workspace_size(1, H, T, r, k), dtype=torch.uint8, device=dev)
+
+        def step():
+            cskv.compress_many(jobs)
+            cskv.index_topk(q_idx, w, caches["index"], ctx, r, k, T, topk_idx=topk, workspace=ws_i, want_scores=False)
+            cskv.sparse_decode_attn(q, caches["main"], swa, cskv.FMT_BF16, ctx, topk, k, r, T, sink,
+                                    cskv.DEFAULT_SCALE, qcs, out=out, workspace=ws_a)
+
+        ms, _, clocks = _graph_timed(torch, step, args.steps, args.warmup, flush)
+        assert cskv.device_status() == 0
+        m = statistics.mean(ms)
+        # bytes the step must move: the completed block's tokens (2 lanes, 8 slots x 2 halves x kv+gate),
+        # the index keys, the 640 bf16 rows attended, queries and output
+        algo = (8 * 2 * 2 * (512 + 128) * 2 + n * 256 + 640 * 1024 + 2 * H * 512 * 2 + Hi * 128 * 2)
+        line = _line("tiny", "tiny CSA decode layer (batch 1, 4096 tokens): step latency", m * 1e3, "us", m, False,
+                     {"workload": "Tiny CSA decode layer: batch 1, context 4096 tokens, ratio 4 (1024 entries), "
+                                  "top-512, 16 query heads x 512 (last 64 RoPE, theta 160000), 4 indexer heads x "
+                                  "128, SWA 128, bf16 KV and queries N(0,1), gate logits N(0,1), seed 0; caches "
+                                  "compressed from the 4096 tokens; per step: compress the completed block "
+                                  "(main + index key), index_topk, sparse_decode_attn",
+                      "l2": "flushed before every step (the workload is L2-sized)"},
+                     roof("whole step", algo, m, bound="latency"), clocks, 1 + 2 + 2, args)
+        return finish(line, "tiny")
+
+    if args.mode == "hca":
+        wl = synth.workload("hca_128k")
+        B, r, H, L = wl.B, wl.ratio, wl.H, wl.max_ctx
+        n = L // r
+        main = _lane(torch, cskv, wl, "main", cskv.FMT_FP8, 512)
+        swa = torch.zeros((B, 128, 528), dtype=torch.uint8, device=dev)
+        cskv.encode_rows(torch.from_numpy(np.stack([synth.swa_values(wl, b) for b in range(B)])).to(dev).reshape(-1, 512),
+                         cskv.PagedCache(swa.view(B * 2, 64 * 528), None, cskv.FMT_FP8, 512))
+        q, _, _, sink = synth.queries(wl)
+        q = torch.from_numpy(q).to(bf).to(dev)
+        sink = torch.from_numpy(sink).to(dev)
+        ctx = torch.from_numpy(wl.ctx_len.astype(np.int32)).to(dev)
+        qcs = torch.from_numpy(cskv.rope_table(wl.ctx_len - 1)).to(dev)
+        out = torch.empty_like(q)
+        ws_a = torch.empty(cskv.sparse_decode_attn_workspace_size(B, H, L, r, 0), dtype=torch.uint8, device=dev)
+
+        def step():
+            cskv.sparse_decode_attn(q, main, swa, cskv.FMT_FP8, ctx, None, 0, r, L, sink, cskv.DEFAULT_SCALE, qcs,
+                                    out=out, workspace=ws_a)
+
+        ms, _, clocks = _graph_timed(torch, step, args.steps, args.warmup, flush)
+        assert cskv.device_status() == 0
+        m = statistics.mean(ms)
+        per_q = (n + 128) * 528 + 2 * H * 512 * 2      # every visible entry and the window, query in, output out
+        line = _line("hca", "HCA decode layer at 128K context: queries/s per layer (batch 32)", B / (m * 1e-3),
+                     "queries/s", m, True,
+                     {"workload": "HCA decode layer: batch 32, context 131072 (1024 entries at ratio 128, all read) "
+                                  "+ SWA 128, 64 query heads x 512, KV FP8 e4m3 + e8m0 per 32 values (528 B/token), "
+                                  "values N(0,1), shuffled 64-row pages, sink; per step: sparse_decode_attn over "
+                                  "every visible entry",
+                      "l2": "flushed before every step (the 23.7 MB working set would otherwise sit in L2)"},
+                     roof("attn_tile_kernel + attn_combine_kernel", B * per_q, m), clocks, 2, args)
+        return finish(line, "hca")
+
+    if args.mode == "compress":
+        T = 65536
+        lines = []
+        for r, overlap in ((4, True), (128, False)):
+            coff = 2 if overlap else 1
+            kv, gate = synth.compressor_tokens(3, T, r, overlap, 512)
+            ape, nw = synth.compressor_params(3, r, overlap, 512)
+            kv_t = torch.from_numpy(kv).to(bf)[None].to(dev)
+            g_t = torch.from_numpy(gate).to(bf)[None].to(dev)
+            ape_t, nw_t = torch.from_numpy(ape).to(dev), torch.from_numpy(nw).to(dev)
+            n = T // r
+            cs = torch.from_numpy(cskv.rope_table(np.arange(n) * r)[None]).to(dev)
+            zero = torch.zeros(1, dtype=torch.int32, device=dev)
+            for fmt, fname in ((cskv.FMT_FP8, "FP8-528"), (cskv.FMT_FP4, "MXFP4-288")):
+                pages = (n + 63) // 64
+                out = cskv.PagedCache.allocate(pages, fmt, 512,
+                                               block_table=torch.randperm(pages, dtype=torch.int32).to(dev)[None])
+
+                def step():
+                    cskv.compress(kv_t, g_t, ape_t, r, overlap, out, zero, zero, norm_w=nw_t, rope_cs=cs)
+
+                ms, _, clocks = _graph_timed(torch, step, args.steps, args.warmup, flush)
+                assert cskv.device_status() == 0
+                m = statistics.mean(ms)
+                rb = cskv.row_bytes(fmt, 512)
+                algo = T * coff * 512 * 2 * 2 + n * rb + r * coff * 512 * 4 + n * 64 * 4 + 512 * 4
+                line = _line("compress", "compressor throughput: tokens/s (65,536-token chunk, ratio %d -> %s)"
+                             % (r, fname), T / (m * 1e-3), "tokens/s", m, True,
+                             {"workload": "Compressor throughput: 65536-token chunk of 512-dim bf16 kv + gate "
+                                          "(N(0,1), seed 3), slot bias 0.5 N(0,1), RMSNorm weight U(0.5, 1.5), "
+                                          "ratio %d%s, RoPE at each entry's first token, coded %s into shuffled "
+                                          "64-row pages; one cskv_compress launch"
+                                          % (r, " with overlap (coff 2)" if overlap else "", fname),
+                              "l2": "flushed before every step; the %d MB read exceeds L2 at ratio 4"
+                                    % (T * coff * 512 * 4 // 1000000)},
+                             roof("compress_kernel<512>", algo, m), clocks, 1, args)
+                lines.append(finish(line, "compress:%d:%d" % (r, fmt)))
+        return lines
+    raise ValueError(args.mode)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -812,12 +1099,22 @@ def main():
     ap.add_argument("--impl", choices=["cskv", "reference"], default="cskv")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--mode", choices=["decode", "csa2", "state", "prefill"], default="decode",
-                    help="decode: the benchmark; the others measure the rows built beyond it")
+    ap.add_argument("--mode", choices=["decode", "tiny", "hca", "compress", "mixed", "csa2", "state", "prefill"],
+                    default="decode",
+                    help="decode: the benchmark (1M context); tiny / hca / compress / mixed: the other named "
+                         "workloads; csa2 / state / prefill: the rows built beyond the decode step")
+    ap.add_argument("--oracle-sample", default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--one-core", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.oracle_sample is not None:
+        # child of cpu_baseline(): the oracle's sample on one core (thread counts come from the environment)
+        if args.one_core and hasattr(os, "sched_setaffinity"):
+            os.sched_setaffinity(0, {min(os.sched_getaffinity(0))})
+        print(json.dumps(oracle_sample(args.oracle_sample)))
+        return
     args.warmup = max(3, args.warmup)
     if args.steps is None:
-        args.steps = 1000 if (args.impl == "cskv" and args.mode == "decode") else 50
+        args.steps = 1000 if (args.impl == "cskv" and args.mode in ("decode", "mixed")) else 50
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
 
@@ -829,6 +1126,22 @@ def main():
     import torch
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
+    if args.mode in ("tiny", "hca", "compress"):
+        if rank == 0:
+            res = run_config_mode(args)
+            for line in (res if isinstance(res, list) else [res]):
+                print(json.dumps(line))
+        return
+    if args.mode == "mixed":
+        res = run_gpu(args, 0, 1, workload="mixed_mxfp4")
+        res["mode"] = "mixed"
+        if not args.no_cpu_baseline:
+            try:
+                res["cpu_baseline"] = cpu_baseline("mixed")
+            except Exception as e:
+                res["cpu_baseline"] = {"value": None, "error": repr(e)[:200]}
+        print(json.dumps(res))
+        return
     if args.mode != "decode":
         if rank == 0:
             print(json.dumps(run_next_row(args)))
