@@ -129,23 +129,19 @@ YARN_V4 = dict(factor=16.0, original=65536, beta_fast=32.0, beta_slow=1.0)
 
 
 def rope_table(positions, theta=160000.0, rope_dim=64, yarn=None):
-    """Host helper: float32 [n, 32, 2] (cos, sin) of positions * f_k, computed in fp64, with
-    f_k = theta^(-2k/64) or, with yarn (a dict like YARN_V4), the YaRN method's blend: pairs
-    below the correction range keep f_k, pairs above it get f_k / factor, and pairs inside it
-    mix the two along a linear ramp over the pair index."""
-    pos = np.asarray(positions, dtype=np.float64)
-    k = np.arange(rope_dim // 2, dtype=np.float64)
-    f = theta ** (-2.0 * k / rope_dim)
-    if yarn is not None:
-        # pair that turns `beta` times over the original length: d * ln(L / (2 pi beta)) / (2 ln theta)
-        lo = rope_dim * np.log(yarn["original"] / (2.0 * np.pi * yarn["beta_fast"])) / (2.0 * np.log(theta))
-        hi = rope_dim * np.log(yarn["original"] / (2.0 * np.pi * yarn["beta_slow"])) / (2.0 * np.log(theta))
-        lo = max(int(np.floor(lo)), 0)
-        hi = min(int(np.ceil(hi)), rope_dim // 2 - 1)
-        ramp = np.clip((k - lo) / max(hi - lo, 1e-3), 0.0, 1.0)
-        f = f / yarn["factor"] * ramp + f * (1.0 - ramp)
-    ang = pos[..., None] * f
-    return np.stack([np.cos(ang), np.sin(ang)], axis=-1).astype(np.float32)
+    """float32 [..., 32, 2] (cos, sin) of every position, from cskv_rope_table (host code in
+    the library): plain frequencies theta^(-2k/64), or with yarn (a dict like YARN_V4) the
+    YaRN blend over the pair index."""
+    if rope_dim != 64:
+        raise ValueError("the kernels rotate 64 dims")
+    pos = np.ascontiguousarray(np.asarray(positions), dtype=np.int64)
+    out = np.empty(pos.shape + (32, 2), dtype=np.float32)
+    y = yarn or {}
+    st = _lib.lib().cskv_rope_table(pos.ctypes.data, int(pos.size), float(theta), float(y.get("factor", 1.0)),
+                                    float(y.get("original", 1.0)), float(y.get("beta_fast", 1.0)),
+                                    float(y.get("beta_slow", 1.0)), out.ctypes.data)
+    _check(st, "cskv_rope_table")
+    return out
 
 
 def encode_rows(src, dst, req=None, row=None, stream=None):

@@ -111,6 +111,8 @@ SIGNATURES = {
     "cskv_device_status": (c_int32, [c_void_p]),
     "cskv_set_spin_limit": (None, [ctypes.c_uint64]),
     "cskv_set_timing_events": (None, [c_void_p, c_void_p]),
+    "cskv_rope_table": (c_int32, [c_void_p, c_int32, ctypes.c_double, ctypes.c_double, ctypes.c_double,
+                                  ctypes.c_double, ctypes.c_double, c_void_p]),
     "cskv_encode_rows": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, Paged,
                                    c_void_p]),
     "cskv_compress": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_float,

@@ -42,7 +42,6 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
-#include <mutex>
 
 #include "codec.cuh"
 #include "internal.h"
@@ -1620,27 +1619,15 @@ unsigned int take_err_index() { return take_dev_err(); }
 // ---------------------------------------------------------------------------
 static __device__ __align__(256) uint8_t g_noalloc_scratch[CSKV_NOALLOC_SCRATCH_BYTES];
 
-// Device address of g_noalloc_scratch on the current device.  Host code must not
-// use the symbol itself (it is a host-side stand-in, not a device address); the
-// address is looked up once per device, with that device current, and cached.
+// Device address of g_noalloc_scratch in the current device's context.  Host code
+// must not use the symbol itself (it is a host-side stand-in, not a device address).
+// The address is looked up on every call, with the call's device current: the lookup
+// allocates nothing, and a cached address would outlive a cudaDeviceReset, after
+// which the context (and the array's place in it) is new.
 static void* noalloc_scratch_address(cudaError_t* err) {
-  static std::mutex mu;
-  static void* addr[256] = {};
-  int dev = 0;
-  *err = cudaGetDevice(&dev);
-  if (*err != cudaSuccess) return nullptr;
-  if (dev < 0 || dev >= 256) {
-    *err = cudaErrorInvalidDevice;
-    return nullptr;
-  }
-  std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
-    void* p = nullptr;
-    *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (*err != cudaSuccess) return nullptr;
-    addr[dev] = p;
-  }
-  return addr[dev];
+  void* p = nullptr;
+  *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  return *err == cudaSuccess ? p : nullptr;
 }
 
 cudaError_t launch_index_topk_noalloc(const void* q_idx, const float* w, const cskv_paged& keys,

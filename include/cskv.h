@@ -101,10 +101,17 @@ CSKV_API int32_t cskv_version(void);
  * that blocks. */
 CSKV_API int32_t cskv_device_status(void* stream);
 
+/* Process-wide state.  The library keeps no per-call state between calls; two
+ * settings are the exceptions, both process-wide (every device, every thread):
+ * the spin limit below and the measurement hook cskv_set_timing_events.  Set them
+ * before launching work from several threads; changing them while other threads
+ * launch is safe (each launch reads them once) but the launch may see either value. */
+
 /* Upper bound, in SM clock cycles, of every spin-wait on an mbarrier inside the
  * library's kernels (default 2^31, about one second).  A wait that runs out sets
  * CSKV_ERR_TIMEOUT, drains the copies its block has in flight and returns.
- * 0 restores the default.  Applies to launches made after the call. */
+ * 0 restores the default.  Applies to launches made after the call.
+ * Process-wide. */
 CSKV_API void cskv_set_spin_limit(uint64_t cycles);
 
 /* Measurement hook.  With both non-NULL (cudaEvent_t handles passed as void*),
@@ -122,6 +129,28 @@ CSKV_API void cskv_set_spin_limit(uint64_t cycles);
  * outside any stream capture.  Process-wide; meant for benchmarks, not for
  * concurrent use. */
 CSKV_API void cskv_set_timing_events(void* begin, void* end);
+
+/* ------------------------------------------------------------------------
+ * cskv_rope_table: the (cos, sin) table that the kernels take as their RoPE
+ * input ("DeepSeek-V4 deep dive", section 3.3 "Partial RoPE and the inverse
+ * rotation on the output": the last 64 dims are 32 adjacent pairs (2k, 2k+1),
+ * pair k turning by position * f_k with f_k = theta^(-2k/64); compressed layers
+ * use theta = 160,000; section 9.1 "Positions to 1M": YaRN, factor 16 over
+ * 65,536 original positions, betas 32 and 1).  Host code, no GPU needed.
+ *   out[i, k, 0] = (float) cos(positions[i] * f_k), out[i, k, 1] = (float) sin(...),
+ * angles and functions in double precision, rounded to float once.
+ * With yarn_factor > 1 the frequencies are YaRN-blended over the pair index:
+ * low = floor(kb(beta_fast)), high = ceil(kb(beta_slow)), kb(beta) =
+ * 64 ln(yarn_original / (2 pi beta)) / (2 ln theta), both kept in [0, 31];
+ * ramp_k = clamp((k - low) / max(high - low, 0.001), 0, 1);
+ * f_k <- f_k / yarn_factor * ramp_k + f_k * (1 - ramp_k).  yarn_factor <= 1:
+ * plain frequencies (the other YaRN arguments are ignored).
+ * positions: host int64 [n] (any value); out: host float [n, 32, 2]; n >= 0.
+ * Errors: CSKV_ERR_INVALID for NULL pointers with n > 0, n < 0, theta <= 1, or
+ * YaRN arguments that are not positive.
+ * ------------------------------------------------------------------------ */
+CSKV_API int32_t cskv_rope_table(const int64_t* positions, int32_t n, double theta, double yarn_factor,
+                                 double yarn_original, double beta_fast, double beta_slow, float* out);
 
 /* ------------------------------------------------------------------------
  * cskv_encode_rows: code rows of values into a cache.
@@ -292,13 +321,17 @@ CSKV_API int32_t cskv_index_topk(const void* q_idx, const float* w, cskv_paged k
  * memory and expose no allocator, and latency-critical threads that must never
  * block on the driver.  They get the workspace from a fixed array inside the
  * library instead: CSKV_NOALLOC_SCRATCH_BYTES (32 MiB) of device memory that
- * every GPU which loads the library holds until the process exits.  Sizes
- * whose workspace (cskv_index_topk_workspace_size) would exceed it are
- * rejected with CSKV_ERR_INVALID before anything is launched - about 2.6
- * million visible entries in total over the batch, e.g. 8 requests at 1M tokens.
- * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture.  Every call uses the same array and leaves its last contents
+ * every GPU which loads the library holds until the process exits.  The limit:
+ * a call is accepted when cskv_index_topk_workspace_size(B, max_ctx_len, ratio,
+ * Hi, k) <= CSKV_NOALLOC_SCRATCH_BYTES, i.e. about 12.1 bytes per entry of
+ * B * ceil(max_ctx_len / ratio) (every request is sized at the batch's longest
+ * context) plus about 38 KB per request - e.g. 8 requests at 1M tokens (ratio 4)
+ * or 1 request at 11M.  Larger sizes are rejected with CSKV_ERR_INVALID before
+ * anything is launched.  The array's device address is looked up in the current
+ * context on every call (cudaGetSymbolAddress; it allocates nothing), so a
+ * cudaDeviceReset between calls is harmless.  The first call on a device may also
+ * load the library's device code there (lazy module loading): make it before any
+ * stream capture.  Every call uses the same array and leaves its last contents
  * behind; each call clears what must start at zero itself, but calls whose
  * kernels overlap on the GPU (different streams, or graphs replayed
  * concurrently) race on the array and give wrong results.  The call allocates
