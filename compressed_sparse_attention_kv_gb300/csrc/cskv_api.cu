@@ -1,7 +1,9 @@
 // C-ABI front end of libcskv: synchronous argument checks, then launches (and the
 // host staging copy of cskv_decode_layer).  Nothing here allocates device memory or
 // synchronises (cskv_device_status excepted).
+#include <algorithm>
 #include <atomic>
+#include <cmath>
 #include <cstdint>
 #include <mutex>
 
@@ -193,6 +195,39 @@ void cskv_set_timing_events(void* begin, void* end) {
   }
   g_ev_begin.store(on ? begin : nullptr, std::memory_order_relaxed);
   g_ev_end.store(on ? end : nullptr, std::memory_order_relaxed);
+}
+
+int32_t cskv_rope_table(const int64_t* positions, int32_t n, double theta, double yarn_factor,
+                        double yarn_original, double beta_fast, double beta_slow, float* out) {
+  if (n < 0 || (n > 0 && (positions == nullptr || out == nullptr))) return CSKV_ERR_INVALID;
+  if (!(theta > 1.0)) return CSKV_ERR_INVALID;
+  const bool yarn = yarn_factor > 1.0;
+  if (yarn && !(yarn_original > 0.0 && beta_fast > 0.0 && beta_slow > 0.0)) return CSKV_ERR_INVALID;
+  constexpr int kPairs = 32, kRopeDim = 64;
+  double f[kPairs];
+  for (int k = 0; k < kPairs; ++k) f[k] = std::pow(theta, -2.0 * k / kRopeDim);
+  if (yarn) {
+    // the pair that turns `beta` times over the original length (the YaRN correction range)
+    auto kb = [&](double beta) {
+      return kRopeDim * std::log(yarn_original / (2.0 * M_PI * beta)) / (2.0 * std::log(theta));
+    };
+    const int lo = std::max(static_cast<int>(std::floor(kb(beta_fast))), 0);
+    const int hi = std::min(static_cast<int>(std::ceil(kb(beta_slow))), kPairs - 1);
+    const double span = std::max(static_cast<double>(hi - lo), 1e-3);
+    for (int k = 0; k < kPairs; ++k) {
+      const double ramp = std::min(std::max((k - lo) / span, 0.0), 1.0);
+      f[k] = f[k] / yarn_factor * ramp + f[k] * (1.0 - ramp);
+    }
+  }
+  for (int32_t i = 0; i < n; ++i) {
+    const double p = static_cast<double>(positions[i]);
+    for (int k = 0; k < kPairs; ++k) {
+      const double a = p * f[k];
+      out[(static_cast<size_t>(i) * kPairs + k) * 2 + 0] = static_cast<float>(std::cos(a));
+      out[(static_cast<size_t>(i) * kPairs + k) * 2 + 1] = static_cast<float>(std::sin(a));
+    }
+  }
+  return CSKV_OK;
 }
 
 int32_t cskv_device_status(void* stream) {

@@ -26,7 +26,7 @@ def _declared():
 def test_header_and_binding_agree():
     from compressed_sparse_attention_kv_gb300 import _lib
     names = _declared()
-    assert len(names) == 17
+    assert len(names) == 18
     assert sorted(_lib.SIGNATURES) == names
 
 
@@ -161,3 +161,17 @@ def test_binding_refuses_host_tensors_for_device_arguments(lib):
         cskv.sparse_decode_attn(qa, None, swa, cskv.FMT_FP8, ctx, None, 0, 128, 4, None, 0.04, cs)
     with pytest.raises(ValueError, match="CUDA tensor"):
         cskv.decode_layer([], None, None, None, qa, None, swa, cskv.FMT_FP8, ctx, 0, 128, 4, None, 0.04, cs)
+
+
+def test_rope_table_is_host_code_and_checks_its_arguments(lib):
+    """cskv_rope_table runs on the host (no GPU here) and rejects bad arguments."""
+    import numpy as np
+    pos = np.array([0, 1, 1 << 20], dtype=np.int64)
+    out = np.zeros((3, 32, 2), dtype=np.float32)
+    assert lib.cskv_rope_table(pos.ctypes.data, 3, 160000.0, 1.0, 1.0, 1.0, 1.0, out.ctypes.data) == 0
+    assert out[0, :, 0].tolist() == [1.0] * 32 and out[0, :, 1].tolist() == [0.0] * 32
+    assert lib.cskv_rope_table(None, 3, 160000.0, 1.0, 1.0, 1.0, 1.0, out.ctypes.data) == 1
+    assert lib.cskv_rope_table(pos.ctypes.data, -1, 160000.0, 1.0, 1.0, 1.0, 1.0, out.ctypes.data) == 1
+    assert lib.cskv_rope_table(pos.ctypes.data, 3, 1.0, 1.0, 1.0, 1.0, 1.0, out.ctypes.data) == 1
+    assert lib.cskv_rope_table(pos.ctypes.data, 3, 160000.0, 16.0, 0.0, 32.0, 1.0, out.ctypes.data) == 1
+    assert lib.cskv_rope_table(None, 0, 160000.0, 1.0, 1.0, 1.0, 1.0, None) == 0
