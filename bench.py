@@ -2,7 +2,8 @@
 """Decode-attention benchmark: queries/s per layer at 1M context on one GB300.
 
 One step = one decode token through one CSA layer for a batch of 8 requests at
-1,048,576 tokens (262,144 compressed entries each), i.e. every row of the hot path:
+1,048,576 tokens (262,144 compressed entries each), i.e. every row of the hot path,
+run by one cskv_decode_layer call (device buffers; the kernels overlap):
   1. compress the block that the new token completes (main 512-d entry -> FP8-528,
      index 128-d key -> FP8-132),
   2. index_topk: score all 262,144 FP8 keys per request with 64 indexer heads, keep 512,
@@ -252,13 +253,13 @@ def run_gpu(args, rank, world, workload=WORKLOAD):
                  rope_cs=d["ecs"])]
 
     def step():
-        cskv.compress_many(jobs)
-        cskv.index_topk(d["q_idx"], d["w"], keys, d["ctx"], r, k, L, topk_idx=topk, workspace=ws_i,
-                        want_scores=False)
-        cskv.sparse_decode_attn(d["q"], main, swa, wl.swa_fmt, d["ctx"], topk, k, r, L, sink,
-                                cskv.DEFAULT_SCALE, d["qcs"], out=out, workspace=ws_a)
+        # one cskv_decode_layer call without host buffers: the indexer's query prep, the
+        # compressor (both caches), the score kernel (selection included), attention tiles, combine
+        cskv.decode_layer(jobs, d["q_idx"], d["w"], keys, d["q"], main, swa, wl.swa_fmt, d["ctx"], k, r, L, sink,
+                          cskv.DEFAULT_SCALE, d["qcs"], topk_idx=topk, out=out, index_workspace=ws_i,
+                          attn_workspace=ws_a)
 
-    launches_per_step = 1 + 2 + 2   # compressor (both caches), indexer prep + score/select, attention tiles + combine
+    launches_per_step = 1 + 2 + 2   # query prep, compressor, score/select, attention tiles, combine
     for _ in range(max(1, args.warmup)):
         step()
     torch.cuda.synchronize()

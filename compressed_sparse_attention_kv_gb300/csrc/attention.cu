@@ -80,7 +80,18 @@ struct AttnArgs {
   float* ml;
   int max_tiles;
   uint8_t* out_host;           // optional second copy of out (a host buffer's device alias), or nullptr
+  // Fused decode step: ready[b] turns 1 once the indexer has written request b's
+  // selection; list tiles wait for it (bounded by spin cycles) instead of for the
+  // whole indexer grid.  nullptr: list tiles wait for the kernel before to complete.
+  const uint32_t* ready;
+  unsigned long long spin;
 };
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 
 __device__ __forceinline__ int query_len(const AttnArgs& a, int b) {
   int c = a.ctx_len[b];
@@ -109,6 +120,37 @@ __device__ __forceinline__ void put16(uint8_t* tile, int row, int l, const float
   const int c0 = (l & 3) * 2;
   *reinterpret_cast<uint4*>(base + sw128_offset(row, c0)) = make_uint4(w[0], w[1], w[2], w[3]);
   *reinterpret_cast<uint4*>(base + sw128_offset(row, c0 + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// 16 values already packed as 8 bf16 pairs -> the same places as put16
+__device__ __forceinline__ void put16w(uint8_t* tile, int row, int l, const uint32_t (&w)[8]) {
+  uint8_t* base = tile + (l >> 2) * (kKeys * 128);
+  const int c0 = (l & 3) * 2;
+  *reinterpret_cast<uint4*>(base + sw128_offset(row, c0)) = make_uint4(w[0], w[1], w[2], w[3]);
+  *reinterpret_cast<uint4*>(base + sw128_offset(row, c0 + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// 16 e4m3 codes times the power of two 2^(scb - 127), straight into bf16 bit patterns:
+// a normal code s.eeee.mmm is (-1)^s 2^(eeee-7) (1 + mmm/8), so its bf16 image has sign s,
+// exponent field eeee + 120 + (scb - 127) and mantissa mmm << 4 - the code's low 7 bits
+// shifted left by 4, plus a constant.  Two codes per 32-bit word (byte permutes, one
+// shift, one logic op, one add).  Exact wherever it applies; returns false (nothing
+// written) when a code is zero or subnormal or the scale is below 2^-119, for the
+// general conversion to take over.
+__device__ __forceinline__ bool e4m3x16_to_bf16(const uint4 codes, uint32_t scb, uint32_t (&w)[8]) {
+  if (scb < 8u) return false;
+  const uint32_t bias2 = ((scb - 7u) << 7) * 0x00010001u;
+  const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
+  uint32_t bad = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t v0 = __byte_perm(cw[i], 0u, 0x1404);   // [code1 << 8 | code0 << 8] per half
+    const uint32_t v1 = __byte_perm(cw[i], 0u, 0x3424);
+    bad |= __vcmpeq2(v0 & 0x78007800u, 0u) | __vcmpeq2(v1 & 0x78007800u, 0u);
+    w[2 * i] = ((v0 & 0x80008000u) | ((v0 >> 4) & 0x07F007F0u)) + bias2;
+    w[2 * i + 1] = ((v1 & 0x80008000u) | ((v1 >> 4) & 0x07F007F0u)) + bias2;
+  }
+  return bad == 0;
 }
 
 // Raw bytes of 16 values of one row: codes (16 B FP8 / 8 B FP4 / 32 B bf16) and
@@ -192,6 +234,13 @@ __device__ __forceinline__ void dequant_tile(uint8_t* ktile, const uint8_t* stag
   };
   auto emit = [&](int r, int l, const RowBytes& rb) {
     float v[16];
+    if (kFp8 && sm->rowp[r] != nullptr) {
+      uint32_t w[8];
+      if (e4m3x16_to_bf16(rb.lo, rb.scb, w)) {
+        put16w(ktile, r, l, w);
+        return;
+      }
+    }
     if (sm->rowp[r] != nullptr) {
       convert16(FMT, rb, v);
     } else {
@@ -201,7 +250,7 @@ __device__ __forceinline__ void dequant_tile(uint8_t* ktile, const uint8_t* stag
     put16(ktile, r, l, v);
   };
   constexpr int kPer = kKeys * 16 / kAttnThreads;   // 8
-#pragma unroll 1
+#pragma unroll 4
   for (int u = 0; u < kPer; ++u) {
     const int x = threadIdx.x + u * kAttnThreads;
     emit(x >> 4, x & 15, raw_of(x >> 4, x & 15));
@@ -225,7 +274,9 @@ __device__ __forceinline__ void dequant_tile(uint8_t* ktile, const uint8_t* stag
 
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned by pointer arithmetic on the shared array (an integer round trip
+  // would lose the address space and turn every access into a generic one)
+  uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* ktile = base;                                   // 8 chunks x 128 rows x 128 B = 128 KiB
   uint8_t* qtile = ktile + 8 * kKeys * 128;                // 8 chunks x Nq rows x 128 B <= 64 KiB
   float* zt = reinterpret_cast<float*>(qtile);             // reused after S: [Nq][kZStride]
@@ -277,8 +328,33 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
   grid_dep_launch();   // the combine kernel may be scheduled; it waits for this grid
   // The selected entries come from the indexer, which may still be finishing (this
   // kernel is a programmatic dependent of it): compressed tiles wait here, the
-  // window tile does not need it.
-  if (tile > 0) grid_dep_wait();
+  // window tile does not need it.  In a fused step each request's flag says when its
+  // own selection is written.
+  if (tile > 0) {
+    if (a.ready == nullptr) {
+      grid_dep_wait();
+    } else {
+      // while the selection is being written: the request's block-table row into L2, so
+      // that the row lookups after it do not wait on HBM
+      if (a.kv.block_table != nullptr) {
+        const int32_t* bt = a.kv.block_table + static_cast<long long>(b) * a.kv.max_pages;
+        const int np = min(a.kv.max_pages, (ctx / a.ratio + kPageRows - 1) / kPageRows);
+        for (int x = threadIdx.x * 32; x < np; x += blockDim.x * 32)
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(bt + x));
+      }
+      if (threadIdx.x == 0 && ld_acquire_gpu(a.ready + b) == 0) {
+        const unsigned long long t0 = clock64();
+        while (ld_acquire_gpu(a.ready + b) == 0) {
+          if (clock64() - t0 > a.spin) {
+            set_err(CSKV_ERR_TIMEOUT);
+            break;
+          }
+          __nanosleep(100);
+        }
+      }
+      __syncthreads();
+    }
+  }
   // ---- rows of this tile: one thread per row resolves its address (the list entry,
   // then the block table), all rows in parallel
   const int rq = a.req_of ? a.req_of[b] : b;
@@ -409,6 +485,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
   __syncthreads();
 
   // ---- per head: max, exp2, sum; P^T stored as the MN-major B operand [key][head]
+  // (unrolled: the shuffle chains of a warp's heads overlap)
+#pragma unroll 8
   for (int h = warp; h < Nq; h += kAttnThreads / 32) {
     float z[4];
 #pragma unroll
@@ -485,6 +563,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  // fused step: this grid completes only after the indexer has (the next step's prep
+  // clears the indexer's workspace once the kernels before it are complete)
+  if (a.ready != nullptr && threadIdx.x == 0) grid_dep_wait();
 }
 
 // merge the tiles of (request, head) in tile order, sink, inverse RoPE, bf16.  DPT dims
@@ -601,7 +682,7 @@ static cudaError_t launch_attn(const void* q, const cskv_paged& kv, const void* 
                                int swa_fmt, const int32_t* req_of, const int32_t* ctx_len, const int32_t* topk,
                                int k, int ratio, int max_ctx, const float* sink, float softmax_scale,
                                const float* q_rope, int B, int H, void* out, void* out_host, void* workspace,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, const uint32_t* ready) {
   const AttnLayout L = attn_layout(B, H, max_ctx, ratio, topk ? k : 0);
   AttnArgs a;
   a.q = static_cast<const uint8_t*>(q);
@@ -627,6 +708,8 @@ static cudaError_t launch_attn(const void* q, const cskv_paged& kv, const void* 
   a.ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + L.ml);
   a.max_tiles = L.max_tiles;
   a.out_host = static_cast<uint8_t*>(out_host);
+  a.ready = ready;
+  a.spin = spin_limit();
   const size_t smem = attn_smem_bytes();
   cudaFuncSetAttribute(attn_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   dim3 grid(L.max_tiles, B, (H + kMaxHeadsPerBlock - 1) / kMaxHeadsPerBlock);
@@ -657,9 +740,9 @@ cudaError_t launch_sparse_decode_attn(const void* q, const cskv_paged& kv, const
                                       const int32_t* ctx_len, const int32_t* topk, int k, int ratio,
                                       int max_ctx, const float* sink, float softmax_scale,
                                       const float* q_rope, int B, int H, void* out, void* workspace,
-                                      cudaStream_t stream, void* out_host) {
+                                      cudaStream_t stream, void* out_host, const uint32_t* ready) {
   return launch_attn(q, kv, swa, nullptr, swa_fmt, nullptr, ctx_len, topk, k, ratio, max_ctx, sink,
-                     softmax_scale, q_rope, B, H, out, out_host, workspace, stream);
+                     softmax_scale, q_rope, B, H, out, out_host, workspace, stream, ready);
 }
 
 cudaError_t launch_sparse_prefill_attn(const void* q, const cskv_paged& kv, const cskv_paged& win,
@@ -668,7 +751,7 @@ cudaError_t launch_sparse_prefill_attn(const void* q, const cskv_paged& kv, cons
                                        const float* q_rope, int T, int H, void* out, void* workspace,
                                        cudaStream_t stream) {
   return launch_attn(q, kv, nullptr, &win, win.fmt, req_of, pos1, topk, k, ratio, max_ctx, sink, softmax_scale,
-                     q_rope, T, H, out, nullptr, workspace, stream);
+                     q_rope, T, H, out, nullptr, workspace, stream, nullptr);
 }
 
 unsigned int take_err_attention() { return take_dev_err(); }

@@ -174,6 +174,11 @@ __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Orders this thread's view of global memory (written through the generic proxy, e.g.
+// by an earlier kernel) before its later asynchronous-proxy copies (TMA / bulk).
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 
 // 16-byte asynchronous copy global -> shared (cp.async, L2 only); completion is
 // awaited with cp_async_wait_all() by the issuing thread, then a barrier.

@@ -371,6 +371,12 @@ struct CompressMany {
 };
 
 __global__ void __launch_bounds__(256) compress_many_kernel(const __grid_constant__ CompressMany m) {
+  // Launched as a programmatic dependent (a fused decode step, after the indexer's
+  // query prep), the kernel lets its own dependent (the score kernel) start only once
+  // the kernel before it has completed: the score kernel then reads the prep's output
+  // freely and waits for this kernel only before the index keys it writes.  In a
+  // plain launch the wait returns at once.
+  grid_dep_wait();
   grid_dep_launch();
   int j = 0;
   while (j + 1 < m.njobs && static_cast<long long>(blockIdx.x) >= m.first[j + 1]) ++j;
@@ -536,7 +542,7 @@ cudaError_t launch_compress(const void* kv, const void* gate, const void* prev_k
   return cudaGetLastError();
 }
 
-cudaError_t launch_compress_many(const cskv_compress_job* jobs, int njobs, cudaStream_t stream) {
+cudaError_t launch_compress_many(const cskv_compress_job* jobs, int njobs, cudaStream_t stream, bool dependent) {
   if (njobs < 1 || njobs > kMaxCompressJobs) return cudaErrorInvalidValue;
   CompressMany m;
   m.njobs = njobs;
@@ -552,8 +558,21 @@ cudaError_t launch_compress_many(const cskv_compress_job* jobs, int njobs, cudaS
   if (m.first[njobs] == 0) return cudaSuccess;
   cudaFuncSetAttribute(compress_many_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        static_cast<int>(kCompressSmem));
-  compress_many_kernel<<<static_cast<unsigned>(m.first[njobs]), 256, kCompressSmem, stream>>>(m);
-  return cudaGetLastError();
+  if (!dependent) {
+    compress_many_kernel<<<static_cast<unsigned>(m.first[njobs]), 256, kCompressSmem, stream>>>(m);
+    return cudaGetLastError();
+  }
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(m.first[njobs]));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = kCompressSmem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, compress_many_kernel, m);
 }
 
 cudaError_t launch_decode_append(const cskv_decode_job* jobs, int njobs, const int32_t* pos, int B,

@@ -469,17 +469,24 @@ int32_t cskv_decode_layer(const cskv_decode_layer_args* args, void* stream) {
   if (a.out_bytes > 0 && (a.h_out == nullptr || a.out_bytes > size_t(a.B) * a.H * 512 * 2)) return CSKV_ERR_INVALID;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (a.in_bytes > 0 && stage_copy(a.d_in, a.h_in, a.in_bytes, true, st) != cudaSuccess) return CSKV_ERR_CUDA;
-  if (a.njobs > 0 && launch_compress_many(a.jobs, a.njobs, st) != cudaSuccess) return CSKV_ERR_CUDA;
-  if (csa && launch_index_topk(a.q_idx, a.w, a.keys, a.ctx_len, a.B, a.Hi, a.ratio, a.k, a.max_ctx_len,
-                               a.topk_idx, nullptr, a.index_workspace, st) != cudaSuccess)
+  // CSA: the indexer's prep, the compressor and the score kernel overlap (the score kernel
+  // waits for the compressor only before the tiles holding the index keys it writes),
+  // and each request's attention starts as soon as its own selection is written
+  const uint32_t* ready = nullptr;
+  if (csa) {
+    if (launch_index_topk_fused(a.q_idx, a.w, a.keys, a.ctx_len, a.B, a.Hi, a.ratio, a.k, a.max_ctx_len,
+                                a.topk_idx, nullptr, a.index_workspace, a.jobs, a.njobs, st, &ready) != cudaSuccess)
+      return CSKV_ERR_CUDA;
+  } else if (a.njobs > 0 && launch_compress_many(a.jobs, a.njobs, st) != cudaSuccess) {
     return CSKV_ERR_CUDA;
+  }
   const int32_t kk = csa ? a.k : 0;
   // a whole page-locked output buffer is written by the combine kernel itself, beside out
   void* out_alias = nullptr;
   if (a.out_bytes > 0 && a.out_bytes == size_t(a.B) * a.H * 512 * 2) out_alias = host_alias(a.h_out);
   if (launch_sparse_decode_attn(a.q, a.main_kv, a.swa, a.swa_fmt, a.ctx_len, csa ? a.topk_idx : nullptr, kk,
                                 a.ratio, a.max_ctx_len, a.sink, a.softmax_scale, a.q_rope_cs, a.B, a.H, a.out,
-                                a.attn_workspace, st, out_alias) != cudaSuccess)
+                                a.attn_workspace, st, out_alias, ready) != cudaSuccess)
     return CSKV_ERR_CUDA;
   if (a.out_bytes > 0 && out_alias == nullptr && stage_copy(a.h_out, a.out, a.out_bytes, false, st) != cudaSuccess)
     return CSKV_ERR_CUDA;

@@ -83,7 +83,7 @@ constexpr int kFastN = 2048;         // LARGE: requests of at most this many ent
 constexpr int kScratch16 = kSelSegs + 64 - kScaleSlots * kTileRows * 2;   // u16 words after the scale ring
 
 struct WsLayout {
-  size_t scores, segmax, cand, qimg, wq, hist, ctr, slc, gbar, total;
+  size_t scores, segmax, segmeta, cand, qimg, wq, hist, ctr, slc, gbar, done, ready, fresh, queue, total;
   int n_pad;
 };
 
@@ -94,6 +94,8 @@ __host__ __device__ inline WsLayout ws_layout(int B, int n_max, int k) {
   size_t o = 0;
   L.scores = o; o = align256(o + size_t(B) * L.n_pad * 4);
   L.segmax = o; o = align256(o + size_t(B) * (L.n_pad / kSeg) * 4);
+  // streaming mode: per segment (max key << 32) | (bin of the second largest key << 8) | lane of the max
+  L.segmeta = o; o = align256(o + size_t(B) * (L.n_pad / kSeg) * 8);
   L.cand = o;   o = align256(o + size_t(B) * L.n_pad * 8);
   L.qimg = o;   o = align256(o + size_t(B) * kQSlot);
   L.wq = o;     o = align256(o + size_t(B) * 64 * 4);
@@ -101,6 +103,11 @@ __host__ __device__ inline WsLayout ws_layout(int B, int n_max, int k) {
   L.ctr = o;    o = align256(o + size_t(B) * 4 * 4);
   L.slc = o;    o = align256(o + size_t(B) * kMaxGrid * 4);
   L.gbar = o;   o = align256(o + 16);
+  L.done = o;   o = align256(o + size_t(B) * 4);   // per request: tiles scored and flushed
+  L.ready = o;  o = align256(o + size_t(B) * 4);   // per request: 1 once its selection is written
+  L.fresh = o;  o = align256(o + size_t(B) * 4);   // per request: first entry the kernel before may write
+  // selection queue: [0] slots claimed, [1] slots filled, then B requests in completion order (-1: not yet)
+  L.queue = o;  o = align256(o + size_t(B + 2) * 4);
   L.total = o;
   return L;
 }
@@ -127,6 +134,17 @@ struct IndexArgs {
   uint8_t* ws;
   WsLayout L;
   unsigned long long spin;
+  // Streaming mode (batches of at most kReqCache requests): no grid barrier; the block
+  // that completes a request's last tile selects it and raises ready[b].  With
+  // wait_fresh, the kernel before the score kernel in the stream (the compressor of a
+  // fused decode step) may still be writing index keys: tiles holding entries at or
+  // after fresh[b] are read only after it has completed; nothing else waits for it.
+  int wait_fresh;
+  int fused;                       // the prep waits for the kernel before it first (its queries may come from it)
+  int nfresh;                      // jobs that write this step's index keys (prep input)
+  const int32_t* fresh_req[4];     // [S] request of each sequence of the job
+  const int32_t* fresh_first[4];   // [S] first entry the sequence writes
+  int fresh_S[4];
 };
 
 // Phase-1 work distribution: block blk starts at its home request blk * B / G and
@@ -159,6 +177,8 @@ __global__ void __launch_bounds__(256) index_prep_kernel(const IndexArgs a) {
   uint32_t* hist = reinterpret_cast<uint32_t*>(a.ws + a.L.hist) + size_t(b) * kHistStride;
   uint32_t* ctr = reinterpret_cast<uint32_t*>(a.ws + a.L.ctr) + b * 4;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // in a fused decode step the queries may come from the kernel before (a staging copy)
+  if (a.fused) grid_dep_wait();
   // the score kernel (a programmatic dependent of this one) may start its set-up now
   grid_dep_launch();
   // warp w owns heads w, w+8, ... (N <= 64); lane l holds dims 4l .. 4l+3.  All loads first.
@@ -208,6 +228,22 @@ __global__ void __launch_bounds__(256) index_prep_kernel(const IndexArgs a) {
                                                              first_home_block(b, a.B, a.grid)) * kChunkTiles
                                         : 0u;
   if (b == 0 && threadIdx.x < 2) reinterpret_cast<uint32_t*>(a.ws + a.L.gbar)[threadIdx.x] = 0;
+  if (threadIdx.x == 0) {
+    reinterpret_cast<uint32_t*>(a.ws + a.L.done)[b] = 0;
+    reinterpret_cast<uint32_t*>(a.ws + a.L.ready)[b] = 0;
+    reinterpret_cast<int32_t*>(a.ws + a.L.queue)[2 + b] = -1;
+    if (b == 0) reinterpret_cast<uint32_t*>(a.ws + a.L.queue)[0] = reinterpret_cast<uint32_t*>(a.ws + a.L.queue)[1] = 0;
+  }
+  if (a.wait_fresh && warp == 0) {
+    // the first index key of request b that this step's compressor writes (none: INT_MAX)
+    int fr = 0x7FFFFFFF;
+    for (int j = 0; j < a.nfresh; ++j)
+      for (int q = lane; q < a.fresh_S[j]; q += 32)
+        if (a.fresh_req[j][q] == b) fr = min(fr, a.fresh_first[j][q]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) fr = min(fr, __shfl_xor_sync(0xFFFFFFFFu, fr, o));
+    if (lane == 0) reinterpret_cast<int32_t*>(a.ws + a.L.fresh)[b] = fr;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -240,6 +276,11 @@ struct ScoreSmem {
   uint32_t base[2];
   uint32_t nlist;
   int nbv[kReqCache];              // visible entries of the first kReqCache requests
+  uint32_t wcnt[16];               // streaming-mode selection: per-warp candidate counts, then selected counts
+  int wovf[16];                    // per warp: more multi segments than it holds
+  uint32_t d256[256];              // 8-bit digit histogram of the cut
+  int qreq;                        // streaming mode: the request this block selects next (-1: none)
+  int fresh[kReqCache];            // streaming mode: first entry of each request the compressor may write
   WorkItem work[kWorkItems];       // this block's selection work, found before the scores
   int nwork;                       // -1: more than kWorkItems (found again after the barrier)
   int T, cbin;
@@ -275,7 +316,7 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
 // All blocks of the (cooperatively launched, hence co-resident) grid meet here.
 // Bounded: a wait that runs out sets CSKV_ERR_TIMEOUT and the block carries on
 // with abort set, so nothing hangs.
-__device__ void grid_barrier(ScoreSmem* sm, uint32_t* counter, uint32_t target, unsigned long long limit) {
+__device__ __forceinline__ void grid_barrier(ScoreSmem* sm, uint32_t* counter, uint32_t target, unsigned long long limit) {
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
@@ -300,7 +341,7 @@ __device__ void grid_barrier(ScoreSmem* sm, uint32_t* counter, uint32_t target, 
 // then the 16 fine bins of the coarse bin that crosses k, read from s_fine: the
 // request's 4,096 fine bins, whose cp.async copies the caller issued beside the
 // coarse loads (this function waits for every copy the thread has in flight).
-__device__ void threshold_bin(ScoreSmem* sm, const uint32_t* gh, int k, const uint32_t* s_fine) {
+__device__ __forceinline__ void threshold_bin(ScoreSmem* sm, const uint32_t* gh, int k, const uint32_t* s_fine) {
   const int lane = threadIdx.x;
   if (lane < 32) {
     // lane l owns coarse bins 255-8l .. 248-8l (from the top): two 16-byte loads
@@ -353,7 +394,7 @@ __device__ void threshold_bin(ScoreSmem* sm, const uint32_t* gh, int k, const ui
 
 // Exclusive scan, in place, of n 16-bit counters in shared memory (whole block;
 // the sums stay below 65,536).
-__device__ void block_exclusive_scan16(ScoreSmem* sm, uint16_t* x, int n) {
+__device__ __forceinline__ void block_exclusive_scan16(ScoreSmem* sm, uint16_t* x, int n) {
   const int per = (n + kScoreThreads - 1) / kScoreThreads;
   const int lo = min(n, static_cast<int>(threadIdx.x) * per), hi = min(n, lo + per);
   uint32_t sum = 0;
@@ -483,25 +524,651 @@ __device__ __forceinline__ uint32_t block_scan_excl(ScoreSmem* sm, uint32_t v, u
   return pos;
 }
 
+// The score kernel's shared memory, 1024-byte aligned, derived from the extern array by
+// pointer arithmetic so that every access stays a shared-memory access (an integer
+// round trip would make them generic).  The selection, which runs out of line, carves
+// the same layout from the same array.
+struct ScoreCarve {
+  uint8_t* stages;     // kProducers x kStages stage tiles
+  uint8_t* qbuf;       // 2 query images
+  uint32_t* hist;      // kGroups x 4,096 bins
+  float* sring;        // kScaleSlots x 128 fp32 key scales
+  uint16_t* scratch;   // kScratch16
+  ScoreSmem* sm;
+};
+template <int FP8>
+__device__ __forceinline__ ScoreCarve score_carve() {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  constexpr int kStageBytes = FP8 ? kTileRows * 128 : kTileRows * 256;
+  constexpr int kStages = FP8 ? kStagesFp8 : kStagesBf16;   // per producer
+  constexpr int kQImage = FP8 ? kQImageFp8 : kQImageBf16;
+  ScoreCarve c;
+  c.stages = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  c.qbuf = c.stages + kProducers * kStages * kStageBytes;
+  c.hist = reinterpret_cast<uint32_t*>(c.qbuf + 2 * kQImage);
+  c.sring = reinterpret_cast<float*>(c.hist + kGroups * kHistBins);
+  c.scratch = reinterpret_cast<uint16_t*>(c.sring + kScaleSlots * kTileRows);
+  c.sm = reinterpret_cast<ScoreSmem*>(c.scratch + kScratch16);
+  return c;
+}
+
+__device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_s32(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Appends request b to the selection queue (its scores, bins and metadata are complete
+// and were acquired by this thread).
+__device__ __forceinline__ void queue_push(const IndexArgs& a, int b) {
+  uint32_t* qctl = reinterpret_cast<uint32_t*>(a.ws + a.L.queue);
+  const uint32_t slot = atomicAdd(qctl + 1, 1u);
+  if (slot < static_cast<uint32_t>(a.B)) st_release(reinterpret_cast<uint32_t*>(qctl + 2 + slot), static_cast<uint32_t>(b));
+}
+
+constexpr int kSelCand = 8192;    // candidates kept in shared memory (64 KiB of the stage ring)
+constexpr int kHitRound = 512;    // general path: hit segments whose scores are copied in at once (64 KiB)
+constexpr int kMetaSegs = 8192;   // fast path: segments whose metadata fits in shared memory (64 KiB)
+constexpr int kMulti = 256;       // fast path: segments with two or more entries at the threshold (32 KiB)
+
+// Exclusive prefix sums, in place, of n <= 1024 counters (whole block; warp 0 works,
+// each lane a contiguous run of up to 32); returns the total.
+template <class C>
+__device__ __forceinline__ uint32_t scan_rows(ScoreSmem* sm, C* x, int n) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int per = (n + 31) / 32;
+    const int lo = min(n, lane * per), hi = min(n, lo + per);
+    uint32_t sum = 0;
+#pragma unroll 1
+    for (int i = lo; i < hi; ++i) sum += x[i];
+    uint32_t incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    uint32_t run = incl - sum;
+#pragma unroll 1
+    for (int i = lo; i < hi; ++i) {
+      const uint32_t v = x[i];
+      x[i] = static_cast<C>(run);
+      run += v;
+    }
+    if (lane == 31) sm->cnt[0] = incl;
+  }
+  __syncthreads();
+  return sm->cnt[0];
+}
+
+// The cut among the candidates (each a 64-bit key: order key << 32 | ~entry, so that
+// larger keys are larger scores and, on a tie, smaller entries) and the output, in entry
+// order (the candidates are in entry order): `above` candidates lie in bins above T and
+// are all taken; among those of bin T the need-th largest key is found by 12-bit radix
+// digits (bits 51-40, 39-28, 27-16, 15-4, then 3-0); selected <=> (key & mask) >= prefix.
+// Every pass over an array goes by rows of 32 (a warp per row, a lane per element), so
+// the shared-memory accesses are conflict-free.
+__device__ __forceinline__ void cut_and_write(const IndexArgs& a, ScoreSmem* sm, const unsigned long long* cand, uint32_t nkt,
+                              int T, uint32_t above, uint32_t* dh, uint32_t* rows, int32_t* out_idx, float* out_sc) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int nwarps = kScoreThreads / 32;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  if (threadIdx.x == 0) {
+    sm->need = min(static_cast<uint32_t>(a.k) - above, nkt > above ? nkt - above : 0u);
+    sm->done = 0;
+    sm->mask = ~0ull << 52;
+    sm->prefix = static_cast<unsigned long long>(T) << 52;
+  }
+  __syncthreads();
+#pragma unroll 1
+  for (int shift = 40; shift >= 0; shift = shift >= 12 ? shift - 12 : (shift > 0 ? 0 : -1)) {
+    if (sm->done || sm->need == 0) break;
+    const int width = shift >= 4 ? 12 : 4;
+    const int nd = 1 << width;
+    const unsigned long long dmask = static_cast<unsigned long long>(nd - 1) << shift;
+#pragma unroll 1
+    for (int x = threadIdx.x; x < nd; x += blockDim.x) dh[x] = 0;
+    __syncthreads();
+    const unsigned long long pm = sm->mask, pp = sm->prefix;
+#pragma unroll 1
+    for (uint32_t x = threadIdx.x; x < nkt; x += blockDim.x) {
+      const unsigned long long key = cand[x];
+      if ((key & pm) == pp) atomicAdd(&dh[(key & dmask) >> shift], 1u);
+    }
+    __syncthreads();
+    // digit rows of 32 from the top: row i holds digits nd-1-32i .. nd-32-32i
+    const int nrow = (nd + 31) / 32;
+#pragma unroll 1
+    for (int r = warp; r < nrow; r += nwarps) {
+      const int d = nd - 1 - (32 * r + lane);
+      const uint32_t v = d >= 0 ? dh[d] : 0u;
+      const uint32_t tot = __reduce_add_sync(0xFFFFFFFFu, v);
+      if (lane == 0) rows[r] = tot;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // the row that holds the need-th key (from the top), then the digit in it
+      const uint32_t need = sm->need;
+      uint32_t acc = 0;
+      int rr = nrow - 1;
+#pragma unroll 1
+      for (int r0 = 0; r0 < nrow; r0 += 32) {
+        const uint32_t v = r0 + lane < nrow ? rows[r0 + lane] : 0u;
+        uint32_t incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const unsigned hit = __ballot_sync(0xFFFFFFFFu, acc + incl >= need);
+        if (hit) {
+          const int l = __ffs(hit) - 1;
+          rr = r0 + l;
+          acc += __shfl_sync(0xFFFFFFFFu, incl - v, l);
+          break;
+        }
+        acc += __shfl_sync(0xFFFFFFFFu, incl, 31);
+      }
+      const int d = nd - 1 - (32 * rr + lane);
+      const uint32_t v = d >= 0 ? dh[d] : 0u;
+      uint32_t incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const unsigned hit = __ballot_sync(0xFFFFFFFFu, acc + incl >= need);
+      const int l = hit ? __ffs(hit) - 1 : 31;
+      const uint32_t before = acc + __shfl_sync(0xFFFFFFFFu, incl - v, l);
+      const uint32_t dv = __shfl_sync(0xFFFFFFFFu, v, l);
+      if (lane == 0) {
+        const int dd = nd - 1 - (32 * rr + l);
+        sm->need = need - before;
+        sm->prefix = pp | (static_cast<unsigned long long>(dd) << shift);
+        sm->mask = pm | dmask;
+        if (dv == need - before) sm->done = 1;
+      }
+    }
+    __syncthreads();
+    if (shift == 0) break;
+  }
+  // the output, in entry order: selected candidates counted per row of 32, rows scanned
+  // (in chunks of 1,024 rows)
+  const unsigned long long pm = sm->mask, pp = sm->prefix;
+  uint32_t nsel = 0;
+#pragma unroll 1
+  for (uint32_t c0 = 0; c0 < nkt; c0 += 32768u) {
+    const uint32_t cn = min(nkt - c0, 32768u);
+    const int nrow = static_cast<int>((cn + 31) / 32);
+#pragma unroll 1
+    for (int r = warp; r < nrow; r += nwarps) {
+      const uint32_t x = c0 + 32u * r + lane;
+      const bool sel = x < nkt && (cand[x] & pm) >= pp;
+      const unsigned m = __ballot_sync(0xFFFFFFFFu, sel);
+      if (lane == 0) rows[r] = static_cast<uint32_t>(__popc(m));
+    }
+    __syncthreads();
+    const uint32_t tot = scan_rows(sm, rows, nrow);
+#pragma unroll 1
+    for (int r = warp; r < nrow; r += nwarps) {
+      const uint32_t x = c0 + 32u * r + lane;
+      const unsigned long long key = x < nkt ? cand[x] : 0ull;
+      const bool sel = x < nkt && (key & pm) >= pp;
+      const unsigned m = __ballot_sync(0xFFFFFFFFu, sel);
+      const uint32_t pos = nsel + rows[r] + __popc(m & lt_mask);
+      if (sel && pos < static_cast<uint32_t>(a.k)) {
+        out_idx[pos] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(key));
+        if (out_sc) out_sc[pos] = from_order_key(static_cast<uint32_t>(key >> 32));
+      }
+    }
+    nsel += tot;
+    __syncthreads();
+  }
+  // fewer than k selected (only after an error): -1 after them
+#pragma unroll 1
+  for (uint32_t j = min(nsel, static_cast<uint32_t>(a.k)) + threadIdx.x; j < static_cast<uint32_t>(a.k);
+       j += blockDim.x) {
+    out_idx[j] = -1;
+    if (out_sc) out_sc[j] = -INFINITY;
+  }
+}
+
+// Streaming mode (batches of at most kReqCache requests; no grid barrier).  This block
+// selects every request whose last tile it scored - all of that request's tiles are
+// scored and their bins flushed - then the requests without entries that fall to it
+// (b % gridDim.x), and raises ready[b] after each.  For request b:
+//  - T, the histogram bin holding the k-th score, with `above` entries in bins > T and
+//    inT in bin T (the request's 4,096 fine and 256 coarse bins in the workspace);
+//  - the candidates, every entry in a bin >= T, in entry order, as 64-bit keys.  Fast
+//    path (the usual case): the segment metadata the epilogue kept (each 32-entry
+//    segment's largest key, its lane, and the bin of the second largest key) is read
+//    with the histogram; a segment whose largest key is in a bin >= T and whose second
+//    is not gives its one candidate straight from the metadata, and only segments with
+//    two or more such entries have their scores read again.  General path (bin T too
+//    full, too many segments): the scores of every segment whose largest key reaches T
+//    are read again, in rounds, and the candidates may spill to the workspace;
+//  - cut_and_write: the exact cut in bin T and the k entries in entry order.
+// It runs once per request from a cold instruction cache: loops stay rolled.
+template <int FP8>
+__device__ __noinline__ void select_completed(const IndexArgs& a) {
+  const ScoreCarve cv = score_carve<FP8>();
+  ScoreSmem* sm = cv.sm;
+  uint8_t* stages = cv.stages;
+  uint8_t* qbuf = cv.qbuf;
+  uint32_t* hist = cv.hist;
+  uint16_t* scratch = cv.scratch;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int nwarps = kScoreThreads / 32;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  const float* scores_all = reinterpret_cast<const float*>(a.ws + a.L.scores);
+  const uint64_t* segmeta_all = reinterpret_cast<const uint64_t*>(a.ws + a.L.segmeta);
+  const uint32_t* ghist = reinterpret_cast<const uint32_t*>(a.ws + a.L.hist);
+  uint32_t* ready = reinterpret_cast<uint32_t*>(a.ws + a.L.ready);
+  const int segs_pad = a.L.n_pad / kSeg;
+  // The threads that saw a request's count complete read it with an acquire-release
+  // atomic; this fence and barrier order every read below after it for the whole block.
+  __threadfence();
+  // In a fused step the attention reads the main entries this step's compressor writes
+  // as soon as a ready flag is up: raise none before that kernel has completed.
+  if (a.wait_fresh && threadIdx.x == 0) grid_dep_wait();
+  __syncthreads();
+  auto raise_ready = [&](int b) {
+    __threadfence();   // this thread's output, before the flag
+    __syncthreads();
+    if (threadIdx.x == 0) st_release(ready + b, 1u);
+  };
+  auto pad_out = [&](int b, int from) {
+    int32_t* out_idx = a.topk_idx + size_t(b) * a.k;
+    float* out_sc = a.topk_score ? a.topk_score + size_t(b) * a.k : nullptr;
+#pragma unroll 1
+    for (int j = from + threadIdx.x; j < a.k; j += blockDim.x) {
+      out_idx[j] = -1;
+      if (out_sc) out_sc[j] = -INFINITY;
+    }
+  };
+  // Requests come from the selection queue, in completion order: a block that is done
+  // streaming claims the next slot and waits (bounded) for the request that fills it, so
+  // the selections of a batch run on as many blocks as there are requests, each starting
+  // as soon as its request is complete.
+  uint32_t* qctl = reinterpret_cast<uint32_t*>(a.ws + a.L.queue);
+  const int32_t* qslot = reinterpret_cast<const int32_t*>(qctl + 2);
+#pragma unroll 1
+  for (;;) {
+    if (threadIdx.x == 0) {
+      int q = -1;
+      const uint32_t slot = atomicAdd(qctl, 1u);
+      if (slot < static_cast<uint32_t>(a.B)) {
+        q = ld_acquire_s32(qslot + slot);
+        if (q < 0) {
+          const unsigned long long t0 = clock64();
+          while ((q = ld_acquire_s32(qslot + slot)) < 0) {
+            if (clock64() - t0 > a.spin) {
+              set_err(CSKV_ERR_TIMEOUT);
+              break;
+            }
+            __nanosleep(64);
+          }
+        }
+      }
+      sm->qreq = q;
+    }
+    __threadfence();
+    __syncthreads();
+    const int b = sm->qreq;
+    __syncthreads();
+    if (b < 0) break;
+    const int nb = sm->nbv[b];
+    const float* sc = scores_all + size_t(b) * a.L.n_pad;
+    const uint64_t* meta = segmeta_all + size_t(b) * segs_pad;
+    int32_t* out_idx = a.topk_idx + size_t(b) * a.k;
+    float* out_sc = a.topk_score ? a.topk_score + size_t(b) * a.k : nullptr;
+    if (nb <= a.k) {
+      // every visible entry is selected, in order
+#pragma unroll 1
+      for (int j = threadIdx.x; j < nb; j += blockDim.x) {
+        out_idx[j] = j;
+        if (out_sc) out_sc[j] = __ldcg(sc + j);
+      }
+      pad_out(b, nb);
+      raise_ready(b);
+      continue;
+    }
+    const int nseg = (nb + kSeg - 1) / kSeg;
+    const bool meta_fits = nseg <= kMetaSegs;
+    // ---- threshold bin; the segment metadata comes in beside the fine bins
+    uint64_t* s_meta = reinterpret_cast<uint64_t*>(stages);   // [0, 64 KiB)
+    const uint32_t* ghb = ghist + size_t(b) * kHistStride;
+    uint32_t* s_fine = hist;
+#pragma unroll 1
+    for (int x = threadIdx.x; x < kHistBins / 4; x += blockDim.x) cp_async16(s_fine + 4 * x, ghb + 4 * x);
+    if (meta_fits) {
+#pragma unroll 1
+      for (int x = threadIdx.x; x < (nseg + 1) / 2; x += blockDim.x) cp_async16(s_meta + 2 * x, meta + 2 * x);
+    }
+    threshold_bin(sm, ghb, a.k, s_fine);   // waits for every copy above
+    const int T = sm->T;
+    const uint32_t above = sm->above;
+    if (T < 0) {   // fewer than k binned entries (an earlier error dropped some)
+      pad_out(b, 0);
+      raise_ready(b);
+      continue;
+    }
+    const uint32_t nexp = above + sm->inT;
+    // ---- fast path.  Each warp owns a contiguous run of rows of 32 segments (a lane per
+    // segment), so its candidates are contiguous and in entry order once the eleven warp
+    // totals are scanned.  single = largest key in a bin >= T and the second not (its one
+    // candidate comes from the metadata); multi = both (the warp reads that segment's
+    // scores again itself, up to kWarpMulti of them).
+    constexpr int kWarpMulti = 16;
+    const bool fast = meta_fits && nexp <= static_cast<uint32_t>(kSelCand);
+    if (fast) {
+      unsigned long long* s_cand = reinterpret_cast<unsigned long long*>(stages + kMetaSegs * 8);
+      uint16_t* wl = scratch + warp * kWarpMulti;                        // this warp's multi segments
+      uint16_t* wmc = scratch + nwarps * kWarpMulti + warp * kWarpMulti; // their candidate counts
+      float* wsc = reinterpret_cast<float*>(hist) + warp * kWarpMulti * kSeg;   // their scores
+      const int nrows = (nseg + 31) / 32;
+      const int rpw = (nrows + nwarps - 1) / nwarps;
+      const int r0 = min(nrows, warp * rpw), r1 = min(nrows, r0 + rpw);
+      auto classify = [&](int q, bool& single, bool& multi) -> uint64_t {
+        const uint64_t m = q < nseg ? s_meta[q] : 0ull;
+        const int b1 = static_cast<int>(m >> (64 - kHistBits));
+        const int b2 = static_cast<int>((m >> 8) & (kHistBins - 1));
+        single = b1 >= T && b2 < T;
+        multi = b1 >= T && b2 >= T;
+        return m;
+      };
+      uint32_t nsingle = 0, nm = 0;
+#pragma unroll 4
+      for (int r = r0; r < r1; ++r) {
+        bool single, multi;
+        classify(32 * r + lane, single, multi);
+        const unsigned sb = __ballot_sync(0xFFFFFFFFu, single), mb = __ballot_sync(0xFFFFFFFFu, multi);
+        if (multi) {
+          const uint32_t at = nm + __popc(mb & lt_mask);
+          if (at < static_cast<uint32_t>(kWarpMulti)) wl[at] = static_cast<uint16_t>(32 * r + lane);
+        }
+        nsingle += __popc(sb);
+        nm += __popc(mb);
+      }
+      const uint32_t nmw = min(nm, static_cast<uint32_t>(kWarpMulti));
+      __syncwarp();
+#pragma unroll 1
+      for (uint32_t x = lane; x < nmw * 8; x += 32)
+        cp_async16(wsc + (x >> 3) * kSeg + (x & 7) * 4, sc + static_cast<long long>(wl[x >> 3]) * kSeg + (x & 7) * 4);
+      cp_async_wait_all();
+      __syncwarp();
+      uint32_t nmc = 0;
+#pragma unroll 1
+      for (uint32_t h = 0; h < nmw; ++h) {
+        const long long j = static_cast<long long>(wl[h]) * kSeg + lane;
+        const bool f = j < nb && static_cast<int>(order_key(wsc[h * kSeg + lane]) >> (32 - kHistBits)) >= T;
+        const unsigned mm = __ballot_sync(0xFFFFFFFFu, f);
+        if (lane == 0) wmc[h] = static_cast<uint16_t>(__popc(mm));
+        nmc += __popc(mm);
+      }
+      if (lane == 0) {
+        sm->wcnt[warp] = nsingle + nmc;
+        sm->wovf[warp] = nm > static_cast<uint32_t>(kWarpMulti);
+      }
+      __syncthreads();
+      bool ovf = false;
+      uint32_t off = 0, total = 0;
+#pragma unroll 1
+      for (int w2 = 0; w2 < nwarps; ++w2) {
+        ovf |= sm->wovf[w2] != 0;
+        off += w2 < warp ? sm->wcnt[w2] : 0u;
+        total += sm->wcnt[w2];
+      }
+      if (!ovf && total <= static_cast<uint32_t>(kSelCand)) {
+        // the candidates, in entry order, at this warp's offset
+        uint32_t run = off, hb = 0;
+#pragma unroll 4
+        for (int r = r0; r < r1; ++r) {
+          bool single, multi;
+          const int q = 32 * r + lane;
+          const uint64_t m = classify(q, single, multi);
+          const unsigned mb = __ballot_sync(0xFFFFFFFFu, multi);
+          const uint32_t h = hb + __popc(mb & lt_mask);
+          const uint32_t c = single ? 1u : (multi ? wmc[h] : 0u);
+          uint32_t incl = c;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += y;
+          }
+          const uint32_t at = run + incl - c;
+          if (single) {
+            const uint32_t j = static_cast<uint32_t>(q) * kSeg + static_cast<uint32_t>(m & 31u);
+            s_cand[at] = (m & 0xFFFFFFFF00000000ull) | (0xFFFFFFFFu - j);
+          }
+          // a rare segment with two or more: the whole warp writes it (a lane per entry)
+#pragma unroll 1
+          for (unsigned rest = mb; rest != 0; rest &= rest - 1) {
+            const int l = __ffs(rest) - 1;
+            const uint32_t base = __shfl_sync(0xFFFFFFFFu, at, l);
+            const uint32_t hh = __shfl_sync(0xFFFFFFFFu, h, l);
+            const long long j = static_cast<long long>(32 * r + l) * kSeg + lane;
+            const uint32_t key = order_key(wsc[hh * kSeg + lane]);
+            const bool f = j < nb && static_cast<int>(key >> (32 - kHistBits)) >= T;
+            const unsigned fm = __ballot_sync(0xFFFFFFFFu, f);
+            if (f)
+              s_cand[base + __popc(fm & lt_mask)] =
+                  (static_cast<unsigned long long>(key) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(j));
+          }
+          run += __shfl_sync(0xFFFFFFFFu, incl, 31);
+          hb += __popc(mb);
+        }
+        const uint32_t mine = sm->wcnt[warp];
+        __syncthreads();
+        // ---- the cut among bin T's keys by 8-bit digits (bits 51-44, 43-36, ..., 11-4, 3-0);
+        // keys above bin T never match the prefix and are all taken
+        if (threadIdx.x == 0) {
+          sm->need = min(static_cast<uint32_t>(a.k) - above, total > above ? total - above : 0u);
+          sm->done = 0;
+          sm->mask = ~0ull << 52;
+          sm->prefix = static_cast<unsigned long long>(T) << 52;
+        }
+        __syncthreads();
+#pragma unroll 1
+        for (int shift = 44; shift >= 0; shift = shift >= 8 ? shift - 8 : (shift > 0 ? 0 : -1)) {
+          if (sm->done || sm->need == 0) break;
+          const int nd = shift >= 4 ? 256 : 16;
+          const unsigned long long dmask = static_cast<unsigned long long>(nd - 1) << shift;
+          if (threadIdx.x < 256) sm->d256[threadIdx.x] = 0;
+          __syncthreads();
+          const unsigned long long pm = sm->mask, pp = sm->prefix;
+#pragma unroll 1
+          for (uint32_t x = threadIdx.x; x < total; x += blockDim.x) {
+            const unsigned long long key = s_cand[x];
+            if ((key & pm) == pp) atomicAdd(&sm->d256[(key & dmask) >> shift], 1u);
+          }
+          __syncthreads();
+          if (warp == 0) {
+            // lane l owns digits nd-1-8l .. nd-8-8l (from the top)
+            const uint32_t need = sm->need;
+            uint32_t v[8], sum = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int d = nd - 1 - 8 * lane - i;
+              v[i] = d >= 0 ? sm->d256[d] : 0u;
+              sum += v[i];
+            }
+            uint32_t incl = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+              if (lane >= o) incl += y;
+            }
+            const unsigned hit = __ballot_sync(0xFFFFFFFFu, incl >= need);
+            if (hit != 0 && lane == __ffs(hit) - 1) {
+              uint32_t acc = incl - sum, dv = v[7];
+              int di = 7;
+              bool got = false;
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {   // unrolled: v stays in registers
+                if (!got) {
+                  if (acc + v[i] >= need) {
+                    got = true;
+                    di = i;
+                    dv = v[i];
+                  } else {
+                    acc += v[i];
+                  }
+                }
+              }
+              const int d = nd - 1 - 8 * lane - di;
+              sm->need = need - acc;
+              sm->prefix = pp | (static_cast<unsigned long long>(d) << shift);
+              sm->mask = pm | dmask;
+              if (dv == need - acc) sm->done = 1;
+            }
+          }
+          __syncthreads();
+          if (shift == 0) break;
+        }
+        // ---- the output: selected <=> (key & mask) >= prefix; each warp its own range, in order
+        const unsigned long long pm = sm->mask, pp = sm->prefix;
+        uint32_t nsel_w = 0;
+#pragma unroll 1
+        for (uint32_t x0 = off; x0 < off + mine; x0 += 32) {
+          const uint32_t x = x0 + lane;
+          const bool sel = x < off + mine && (s_cand[x] & pm) >= pp;
+          nsel_w += __popc(__ballot_sync(0xFFFFFFFFu, sel));
+        }
+        __syncthreads();   // every warp has read the cut before the counts are reused
+        if (lane == 0) sm->wcnt[warp] = nsel_w;
+        __syncthreads();
+        uint32_t pos = 0, nsel = 0;
+#pragma unroll 1
+        for (int w2 = 0; w2 < nwarps; ++w2) {
+          pos += w2 < warp ? sm->wcnt[w2] : 0u;
+          nsel += sm->wcnt[w2];
+        }
+#pragma unroll 1
+        for (uint32_t x0 = off; x0 < off + mine; x0 += 32) {
+          const uint32_t x = x0 + lane;
+          const unsigned long long key = x < off + mine ? s_cand[x] : 0ull;
+          const bool sel = x < off + mine && (key & pm) >= pp;
+          const unsigned m = __ballot_sync(0xFFFFFFFFu, sel);
+          const uint32_t p = pos + __popc(m & lt_mask);
+          if (sel && p < static_cast<uint32_t>(a.k)) {
+            out_idx[p] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(key));
+            if (out_sc) out_sc[p] = from_order_key(static_cast<uint32_t>(key >> 32));
+          }
+          pos += __popc(m);
+        }
+        pad_out(b, static_cast<int>(min(nsel, static_cast<uint32_t>(a.k))));   // only after an error
+        raise_ready(b);
+        continue;
+      }
+      __syncthreads();   // an overflowing warp: every warp is past the counts before the general path
+    }
+    // ---- general path: every segment whose largest key reaches T is read again, in rounds
+    unsigned long long* cand = nexp <= static_cast<uint32_t>(kSelCand)
+                                   ? reinterpret_cast<unsigned long long*>(stages + kMetaSegs * 8)
+                                   : reinterpret_cast<unsigned long long*>(a.ws + a.L.cand) + size_t(b) * a.L.n_pad;
+    float* s_score = reinterpret_cast<float*>(stages);   // [0, 64 KiB): the metadata is not needed here
+    uint16_t* s_list = reinterpret_cast<uint16_t*>(qbuf);
+    uint16_t* g_cnt = scratch;
+    uint32_t nk = 0;
+#pragma unroll 1
+    for (int gc = 0; gc < nseg; gc += kSelSegs) {
+      const int ns = min(kSelSegs, nseg - gc);
+      // the hit segments of [gc, gc + ns), in order: thread t owns segments 24t .. 24t+23
+      uint32_t nhit;
+      {
+        constexpr int kOwn = 24;
+        static_assert(kOwn * kScoreThreads >= kSelSegs, "every segment of a pass has an owner");
+        const int q0 = threadIdx.x * kOwn;
+        uint32_t m = 0;
+#pragma unroll
+        for (int u = 0; u < kOwn / 2; ++u) {
+          const int q = q0 + 2 * u;
+          if (q < ns) {   // the table's rows are padded to a multiple of 4 segments
+            const uint4 x = __ldcg(reinterpret_cast<const uint4*>(meta + gc + q));
+            m |= (static_cast<int>(x.y >> (32 - kHistBits)) >= T ? 1u : 0u) << (2 * u);
+            m |= (static_cast<int>(x.w >> (32 - kHistBits)) >= T ? 2u : 0u) << (2 * u);
+          }
+        }
+        if (ns - q0 < kOwn) m &= ns > q0 ? (1u << (ns - q0)) - 1u : 0u;
+        uint32_t pos = block_scan_excl(sm, __popc(m), nhit);
+#pragma unroll 1
+        while (m) {
+          const int q = __ffs(m) - 1;
+          m &= m - 1;
+          s_list[pos++] = static_cast<uint16_t>(q0 + q);
+        }
+        __syncthreads();
+      }
+#pragma unroll 1
+      for (uint32_t h0 = 0; h0 < nhit; h0 += kHitRound) {
+        const uint32_t nh = min(nhit - h0, static_cast<uint32_t>(kHitRound));
+#pragma unroll 1
+        for (uint32_t x = threadIdx.x; x < nh * 8; x += blockDim.x)
+          cp_async16(s_score + (x >> 3) * kSeg + (x & 7) * 4,
+                     sc + (static_cast<long long>(gc) + s_list[h0 + (x >> 3)]) * kSeg + (x & 7) * 4);
+        cp_async_wait_all();
+        __syncthreads();
+        // per hit segment (a warp, a lane per entry): how many of its entries are in bins >= T
+        constexpr int kU = 4;
+#pragma unroll 1
+        for (uint32_t hb = warp * kU; hb < nh; hb += nwarps * kU) {
+#pragma unroll
+          for (int u = 0; u < kU; ++u) {
+            const uint32_t h = min(hb + u, nh - 1);
+            const long long j = (static_cast<long long>(gc) + s_list[h0 + h]) * kSeg + lane;
+            const bool f = hb + u < nh && j < nb &&
+                           static_cast<int>(order_key(s_score[h * kSeg + lane]) >> (32 - kHistBits)) >= T;
+            const unsigned mm = __ballot_sync(0xFFFFFFFFu, f);
+            if (lane == 0 && hb + u < nh) g_cnt[hb + u] = static_cast<uint16_t>(__popc(mm));
+          }
+        }
+        if (threadIdx.x == 0) g_cnt[nh] = 0;
+        __syncthreads();
+        block_exclusive_scan16(sm, g_cnt, static_cast<int>(nh) + 1);
+#pragma unroll 1
+        for (uint32_t hb = warp * kU; hb < nh; hb += nwarps * kU) {
+#pragma unroll
+          for (int u = 0; u < kU; ++u) {
+            const uint32_t h = min(hb + u, nh - 1);
+            const long long j = (static_cast<long long>(gc) + s_list[h0 + h]) * kSeg + lane;
+            const uint32_t key = order_key(s_score[h * kSeg + lane]);
+            const bool f = hb + u < nh && j < nb && static_cast<int>(key >> (32 - kHistBits)) >= T;
+            const unsigned mm = __ballot_sync(0xFFFFFFFFu, f);
+            const uint32_t at = nk + g_cnt[h] + __popc(mm & lt_mask);
+            if (f && at < nexp)   // at most the binned count (guards a histogram short of the scores)
+              cand[at] = (static_cast<unsigned long long>(key) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(j));
+          }
+        }
+        nk += g_cnt[nh];
+        __syncthreads();
+      }
+    }
+    cut_and_write(a, sm, cand, min(nk, nexp), T, above, reinterpret_cast<uint32_t*>(hist),
+                  reinterpret_cast<uint32_t*>(qbuf + 1024), out_idx, out_sc);
+    raise_ready(b);
+  }
+}
+
 // LARGE (batches of more than kReqCache requests, e.g. one request per prompt query in
 // prefill): the scheduler also counts the tiles handed out, so that a block that finds
 // its requests exhausted stops as soon as every tile has an owner instead of visiting
 // every request (one atomic each) before it concludes there is no work left.
 template <int FP8, bool LARGE>
 __global__ void __launch_bounds__(kLaunchBound, 1)
-    index_score_kernel(const __grid_constant__ CUtensorMap tmap, const IndexArgs a) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  // 1024-byte aligned carve-up
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    index_score_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ IndexArgs a) {
   constexpr int kStageBytes = FP8 ? kTileRows * 128 : kTileRows * 256;
   constexpr int kStages = FP8 ? kStagesFp8 : kStagesBf16;   // per producer
   constexpr int kQImage = FP8 ? kQImageFp8 : kQImageBf16;
-  uint8_t* stages = base;                                                  // kProducers x kStages
-  uint8_t* qbuf = stages + kProducers * kStages * kStageBytes;             // 2 x kQImage
-  uint32_t* hist = reinterpret_cast<uint32_t*>(qbuf + 2 * kQImage);       // kGroups x 4096 bins
-  float* sring = reinterpret_cast<float*>(hist + kGroups * kHistBins);    // kScaleSlots x 128 fp32
-  uint16_t* scratch = reinterpret_cast<uint16_t*>(sring + kScaleSlots * kTileRows);   // kScratch16
-  ScoreSmem* sm = reinterpret_cast<ScoreSmem*>(scratch + kScratch16);
+  const ScoreCarve cv = score_carve<FP8>();
+  uint8_t* stages = cv.stages;
+  uint8_t* qbuf = cv.qbuf;
+  uint32_t* hist = cv.hist;
+  float* sring = cv.sring;
+  uint16_t* scratch = cv.scratch;
+  ScoreSmem* sm = cv.sm;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = a.N;
@@ -523,6 +1190,16 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
     }
   }
 
+  if constexpr (!LARGE) {
+    // requests without a visible entry have no tile to complete: block 0 queues them
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+      if (!a.wait_fresh) grid_dep_wait();   // the prep cleared the queue
+      for (int b = 0; b < a.B; ++b)
+        if (sm->nbv[b] == 0) queue_push(a, b);
+    }
+    // the prep (complete before this kernel starts) wrote the fresh bounds
+    if (a.wait_fresh && threadIdx.x < a.B) sm->fresh[threadIdx.x] = reinterpret_cast<const int32_t*>(a.ws + a.L.fresh)[threadIdx.x];
+  }
   if (threadIdx.x == 0) {
     for (int p = 0; p < kProducers; ++p)
       for (int s = 0; s < kStages; ++s) { mbar_init(&sm->full[p][s], 1); mbar_init(&sm->empty[p][s], 1); }
@@ -549,30 +1226,14 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
   // this wait.  The scheduling producer first requests its first chunk's page ids
   // (block tables are inputs) and waits after that.
   const bool sched_thread = warp == 0 && lane == 0;
-  if (a.B <= kReqCache) {
-    if (threadIdx.x == 32) {
-      // This block's selection work depends on the context lengths alone (inputs): one
-      // thread finds it now, beside the prep, instead of every thread after the barrier.
-      // (Producer 1 has nothing to do until producer 0's first hand-over.)
-      long long C = 0;
-      int nw = 0;
-#pragma unroll 1
-      for (int b = 0; b < a.B; ++b) {
-        const long long tb = (sm->nbv[b] + kTileRows - 1) / kTileRows;
-        WorkItem wi;
-        const bool mine = block_range(blockIdx.x, gridDim.x, C, tb, total, wi.lo, wi.hi, wi.fb, wi.nbk, wi.per);
-        C += tb;
-        if (!mine) {
-          if (wi.fb > static_cast<int>(blockIdx.x)) break;   // the runs only move further right
-          continue;
-        }
-        wi.b = b;
-        if (nw < kWorkItems) sm->work[nw] = wi;
-        ++nw;
-      }
-      sm->nwork = nw <= kWorkItems ? nw : -1;
-    }
-  } else {
+  // Streaming mode reads its predecessor's output (query images, counters) only after
+  // waiting for it, unless that predecessor is the compressor of a fused step (the
+  // prep before it has completed; only tiles with fresh keys wait, below).
+  const bool wait_at_start = LARGE || !a.wait_fresh;
+  // In a fused step the next kernel is the attention, which touches nothing of the
+  // indexer's workspace: it may be scheduled as soon as SMs free up.
+  if (!LARGE && a.wait_fresh) grid_dep_launch();
+  if constexpr (LARGE) {
     // Large batches: the requests' tile counts, their total, and this block's selection
     // work are found by the whole block (each thread a contiguous range of requests,
     // block scans for the prefixes), so the cost grows with the batch divided by the
@@ -617,7 +1278,7 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
     if (threadIdx.x == 0) sm->nwork = nw <= static_cast<uint32_t>(kWorkItems) ? static_cast<int>(nw) : -1;
     __syncthreads();
   }
-  if (!sched_thread) grid_dep_wait();
+  if (!sched_thread && wait_at_start) grid_dep_wait();
 
   // ======================================================= phase 1: scores
   // Tiles are handed out dynamically, in chunks of kChunkTiles consecutive tiles of
@@ -637,6 +1298,7 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
       const uint64_t pol = l2_evict_first();
       long long np = 0;       // tiles this producer posted (the end marker included)
       int nreq = 0;           // query images loaded (producer 0)
+      bool waited = wait_at_start;   // this thread has seen the kernel before complete
       // post local tile i = (request b, tile t) with its two page ids (-2: no page,
       // -3: page outside the block table); b < 0 posts the end marker
       auto post = [&](long long i, int b, int t, int id0, int id1) -> bool {
@@ -646,6 +1308,14 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
         const int ss = static_cast<int>(i % kScaleSlots);
         const long long su = i / kScaleSlots;
         if (su > 0 && !role_wait(sm, &sm->sempty[ss], (su - 1) & 1, a.spin)) return false;
+        if (!waited && b >= 0) {
+          // a tile holding entries the compressor before this kernel may still write
+          if (static_cast<long long>(t + 1) * kTileRows > sm->fresh[b]) {
+            grid_dep_wait();
+            fence_proxy_async_global();   // its generic-proxy writes, before the tensor copies read them
+            waited = true;
+          }
+        }
         uint8_t* dst = stages + (pw * kStages + s) * kStageBytes;
         uint32_t bytes = 0;
         int pages[2] = {b >= 0 ? id0 : -2, b >= 0 ? id1 : -2};
@@ -727,7 +1397,7 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
           ct = r0 * kChunkTiles;
           chunk_ids(cb, ct, ids);
         }
-        grid_dep_wait();
+        if (wait_at_start) grid_dep_wait();
         if constexpr (LARGE) {
           if (static_first) atomicAdd(handed, static_cast<uint32_t>(min(kChunkTiles, tiles_of(cb) - ct)));
         }
@@ -861,6 +1531,13 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
     float* wq_s = sm->wq[grp];
     const float* wq_all = reinterpret_cast<const float*>(a.ws + a.L.wq);
     int cur_b = -1, n_b = 0, tiles_b = 0;
+    uint32_t tcount = 0;                         // streaming mode: real tiles of cur_b since the last flush
+    uint32_t* done_all = reinterpret_cast<uint32_t*>(a.ws + a.L.done);
+    uint64_t* segmeta_all = reinterpret_cast<uint64_t*>(a.ws + a.L.segmeta);
+    // the count published at the last switch: its result is looked at one switch later,
+    // so the atomic's round trip does not hold up the group
+    int pend_b = -1;
+    uint32_t pend_old = 0, pend_cnt = 0, pend_tiles = 0;
     uint32_t hphase = 0;
     // the group's four warps meet (bounded: an aborted pass falls through)
     auto grp_sync = [&]() {
@@ -868,6 +1545,30 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
       if (lane == 0) mbar_arrive(&sm->hbar[grp]);
       role_wait(sm, &sm->hbar[grp], hphase & 1, a.spin);
       ++hphase;
+    };
+    // streaming mode: the group's tiles of request b are scored and flushed; the group
+    // whose count completes the request hands it to its block's selection
+    auto settle = [&]() {
+      if (gtid == 0 && pend_b >= 0) {
+        if (pend_old + pend_cnt == pend_tiles) queue_push(a, pend_b);
+        pend_b = -1;
+      }
+    };
+    // The group's tiles of b are scored and its bins flushed (its four warps met after
+    // that): one thread adds their count with release semantics, which orders the whole
+    // group's stores and bin atomics before it.  The group whose count completes the
+    // request hands it to its block's selection.
+    auto publish = [&](int b) {
+      if (gtid == 0 && tcount > 0) {
+        settle();
+        uint32_t old;
+        asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(done_all + b), "r"(tcount) : "memory");
+        pend_b = b;
+        pend_old = old;
+        pend_cnt = tcount;
+        pend_tiles = static_cast<uint32_t>(tiles_b);
+      }
+      tcount = 0;
     };
     auto flush = [&](int b) {
       uint32_t* gh = ghist + size_t(b) * kHistStride;
@@ -899,6 +1600,10 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
         // request switch: the group is done with the previous request's tiles
         grp_sync();
         if (cur_b >= 0) flush(cur_b);
+        if constexpr (!LARGE) {
+          grp_sync();
+          if (cur_b >= 0) publish(cur_b);
+        }
         cur_b = ti.x;
         n_b = visible(a, cur_b);
         tiles_b = (n_b + kTileRows - 1) / kTileRows;
@@ -907,6 +1612,7 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
       }
       const long long j = static_cast<long long>(ti.y) * kTileRows + row;
       const bool real = ti.y < tiles_b;
+      if constexpr (!LARGE) tcount += real ? 1u : 0u;
       const bool valid = real && j < n_b && ((pmask >> (row >> 6)) & 1);
       const int c = static_cast<int>(i % kAccs);
       if (!role_wait(sm, &sm->accfull[c], (i / kAccs) & 1, a.spin)) break;
@@ -945,10 +1651,25 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
       // largest key of this warp's 32 entries: the selection re-reads only
       // segments that can hold a selected entry
       const uint32_t kmax = __reduce_max_sync(0xFFFFFFFFu, key);
-      if (lane == 0 && real) segmax_all[size_t(cur_b) * (a.L.n_pad / kSeg) + (j >> 5)] = kmax;
+      if constexpr (LARGE) {
+        if (lane == 0 && real) segmax_all[size_t(cur_b) * (a.L.n_pad / kSeg) + (j >> 5)] = kmax;
+      } else {
+        // streaming mode keeps the max with its lane and the bin of the runner-up: a
+        // segment with one entry at the threshold needs no second look at its scores
+        const int l1 = __ffs(__ballot_sync(0xFFFFFFFFu, key == kmax)) - 1;
+        const uint32_t k2 = __reduce_max_sync(0xFFFFFFFFu, lane == l1 ? 0u : key);
+        if (lane == 0 && real)
+          segmeta_all[size_t(cur_b) * (a.L.n_pad / kSeg) + (j >> 5)] =
+              (static_cast<uint64_t>(kmax) << 32) | ((k2 >> (32 - kHistBits)) << 8) | static_cast<uint32_t>(l1);
+      }
     }
     grp_sync();
     if (cur_b >= 0) flush(cur_b);
+    if constexpr (!LARGE) {
+      grp_sync();
+      if (cur_b >= 0) publish(cur_b);
+      settle();
+    }
   }
 
   tc_fence_before();
@@ -957,6 +1678,14 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, ncols);
+  }
+  if constexpr (!LARGE) {
+    // plain call: this block reads no more query images; once every block is past its
+    // stream, the next kernel may start (a following prep waits before clearing)
+    if (!a.wait_fresh) grid_dep_launch();
+    select_completed<FP8>(a);
+    if (a.wait_fresh && threadIdx.x == 0) grid_dep_wait();   // complete only after the compressor
+    return;
   }
 
   // ======================================================= phase 2: selection
@@ -1495,6 +2224,16 @@ cudaError_t launch_score(const CUtensorMap& tmap, const IndexArgs& a, cudaStream
   cfg.blockDim = dim3(kScoreThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
+  if constexpr (!LARGE) {
+    // streaming mode: no grid barrier, so no co-residency is needed; blocks are placed
+    // as SMs free up (beside a compressor that is still running, in a fused step)
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, index_score_kernel<FP8, LARGE>, tmap, a);
+  }
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
@@ -1533,11 +2272,18 @@ size_t index_workspace_bytes(int B, int n_max, int Hi, int k) {
   return ws_layout(B, n_max, k).total;
 }
 
-cudaError_t launch_index_topk(const void* q_idx, const float* w, const cskv_paged& keys,
-                              const int32_t* ctx_len, int B, int Hi, int ratio, int k,
-                              int max_ctx_len, int32_t* topk_idx, float* topk_score,
-                              void* workspace, cudaStream_t stream) {
+namespace {
+
+struct IndexLaunch {
   IndexArgs a;
+  CUtensorMap tmap;
+};
+
+cudaError_t index_setup(IndexLaunch& L, const void* q_idx, const float* w, const cskv_paged& keys,
+                        const int32_t* ctx_len, int B, int Hi, int ratio, int k, int max_ctx_len,
+                        int32_t* topk_idx, float* topk_score, void* workspace) {
+  IndexArgs& a = L.a;
+  a = IndexArgs{};
   a.q = static_cast<const uint8_t*>(q_idx);
   a.w = w;
   a.keys = keys;
@@ -1554,59 +2300,111 @@ cudaError_t launch_index_topk(const void* q_idx, const float* w, const cskv_page
   a.ws = static_cast<uint8_t*>(workspace);
   a.L = ws_layout(B, a.n_max, k);
   a.spin = spin_limit();
-
-  CUtensorMap tmap;
-  auto enc = encode_fn();
-  if (enc == nullptr) return cudaErrorNotSupported;
-  {
-    cuuint64_t dims[3], strides[2];
-    cuuint32_t box[3], estr[3] = {1, 1, 1};
-    CUtensorMapDataType dt;
-    if (a.fp8) {
-      dims[0] = 128; strides[0] = 128;
-      box[0] = 128;
-      dt = CU_TENSOR_MAP_DATA_TYPE_UINT8;
-    } else {
-      dims[0] = 128; strides[0] = 256;
-      box[0] = 64;
-      dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    }
-    dims[1] = 64;
-    dims[2] = static_cast<cuuint64_t>(keys.num_pages);
-    strides[1] = static_cast<cuuint64_t>(keys.page_bytes);
-    box[1] = 64;
-    box[2] = 1;
-    CUresult r = enc(&tmap, dt, 3, keys.pool, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  }
-
   a.grid = sm_count();   // the score kernel runs one block per SM
   if (a.grid > kMaxGrid) a.grid = kMaxGrid;
-  {
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(B);
-    cfg.blockDim = dim3(256);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t pe = cudaLaunchKernelEx(&cfg, index_prep_kernel, a);
-    if (pe != cudaSuccess) return pe;
-  }
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
 
+  auto enc = encode_fn();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  cuuint64_t dims[3], strides[2];
+  cuuint32_t box[3], estr[3] = {1, 1, 1};
+  CUtensorMapDataType dt;
+  if (a.fp8) {
+    dims[0] = 128; strides[0] = 128;
+    box[0] = 128;
+    dt = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  } else {
+    dims[0] = 128; strides[0] = 256;
+    box[0] = 64;
+    dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  }
+  dims[1] = 64;
+  dims[2] = static_cast<cuuint64_t>(keys.num_pages);
+  strides[1] = static_cast<cuuint64_t>(keys.page_bytes);
+  box[1] = 64;
+  box[2] = 1;
+  CUresult r = enc(&L.tmap, dt, 3, keys.pool, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t index_launch_prep(const IndexLaunch& L, cudaStream_t stream) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(L.a.B);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, index_prep_kernel, L.a);
+}
+
+cudaError_t index_launch_score(const IndexLaunch& L, cudaStream_t stream) {
+  const IndexArgs& a = L.a;
+  // streaming mode for batches of at most kReqCache requests; the cooperative kernel
+  // (grid barrier, sliced selection) above that, whatever the key format
+  if (a.B > kReqCache) return a.fp8 ? launch_score<1, true>(L.tmap, a, stream) : launch_score<0, true>(L.tmap, a, stream);
+  return a.fp8 ? launch_score<1, false>(L.tmap, a, stream) : launch_score<0, false>(L.tmap, a, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_index_topk(const void* q_idx, const float* w, const cskv_paged& keys,
+                              const int32_t* ctx_len, int B, int Hi, int ratio, int k,
+                              int max_ctx_len, int32_t* topk_idx, float* topk_score,
+                              void* workspace, cudaStream_t stream) {
+  IndexLaunch L;
+  cudaError_t e = index_setup(L, q_idx, w, keys, ctx_len, B, Hi, ratio, k, max_ctx_len, topk_idx, topk_score,
+                              workspace);
+  if (e != cudaSuccess) return e;
+  e = index_launch_prep(L, stream);
+  if (e != cudaSuccess) return e;
   cudaEvent_t ev_begin, ev_end;
   timing_events(&ev_begin, &ev_end);
   record_timing_branch(ev_begin, stream);
-  e = !a.fp8 ? launch_score<0, false>(tmap, a, stream)
-             : (B > kReqCache ? launch_score<1, true>(tmap, a, stream) : launch_score<1, false>(tmap, a, stream));
+  e = index_launch_score(L, stream);
   record_timing_branch(ev_end, stream);
+  return e;
+}
+
+cudaError_t launch_index_topk_fused(const void* q_idx, const float* w, const cskv_paged& keys,
+                                    const int32_t* ctx_len, int B, int Hi, int ratio, int k, int max_ctx_len,
+                                    int32_t* topk_idx, float* topk_score, void* workspace,
+                                    const cskv_compress_job* jobs, int njobs, cudaStream_t stream,
+                                    const uint32_t** ready) {
+  IndexLaunch L;
+  cudaError_t e = index_setup(L, q_idx, w, keys, ctx_len, B, Hi, ratio, k, max_ctx_len, topk_idx, topk_score,
+                              workspace);
+  if (e != cudaSuccess) return e;
+  const bool streaming = B <= kReqCache;
+  L.a.fused = 1;
+  if (streaming) {
+    // the score kernel overlaps the compressor: it waits for it only before the index
+    // keys that the jobs writing into this key cache produce
+    L.a.wait_fresh = 1;
+    for (int j = 0; j < njobs; ++j) {
+      if (jobs[j].out.pool != keys.pool || L.a.nfresh >= 4) continue;
+      L.a.fresh_req[L.a.nfresh] = jobs[j].req;
+      L.a.fresh_first[L.a.nfresh] = jobs[j].first_entry;
+      L.a.fresh_S[L.a.nfresh] = jobs[j].S;
+      ++L.a.nfresh;
+    }
+  }
+  // prep, compressor (a programmatic dependent of the prep), score kernel (of the compressor)
+  e = index_launch_prep(L, stream);
+  if (e != cudaSuccess) return e;
+  cudaEvent_t ev_begin, ev_end;
+  timing_events(&ev_begin, &ev_end);
+  record_timing_branch(ev_begin, stream);
+  if (njobs > 0) {
+    e = launch_compress_many(jobs, njobs, stream, true);
+    if (e != cudaSuccess) return e;
+  }
+  e = index_launch_score(L, stream);
+  record_timing_branch(ev_end, stream);
+  if (ready) *ready = streaming ? reinterpret_cast<const uint32_t*>(L.a.ws + L.a.L.ready) : nullptr;
   return e;
 }
 

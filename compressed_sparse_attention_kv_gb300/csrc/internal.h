@@ -24,7 +24,8 @@ cudaError_t launch_compress(const void* kv, const void* gate, const void* prev_k
                             const int32_t* req, const int32_t* first_entry, const cskv_paged& out,
                             int out_row_bytes, cudaStream_t stream);
 
-cudaError_t launch_compress_many(const cskv_compress_job* jobs, int njobs, cudaStream_t stream);
+cudaError_t launch_compress_many(const cskv_compress_job* jobs, int njobs, cudaStream_t stream,
+                                 bool dependent = false);
 cudaError_t launch_decode_append(const cskv_decode_job* jobs, int njobs, const int32_t* pos, int B,
                                  cudaStream_t stream);
 
@@ -38,6 +39,18 @@ cudaError_t launch_index_topk(const void* q_idx, const float* w, const cskv_page
                               int max_ctx_len, int32_t* topk_idx, float* topk_score,
                               void* workspace, cudaStream_t stream);
 
+// One decode step's compressor and indexer, overlapped (cskv_decode_layer): the query
+// prep, then compress_many(jobs) as a programmatic dependent of it, then the score
+// kernel, which reads the index keys these jobs write only after they are complete.
+// *ready receives the per-request flags that the selection raises (nullptr when the
+// batch takes the cooperative large-batch kernel; the attention then waits for the
+// whole indexer instead).
+cudaError_t launch_index_topk_fused(const void* q_idx, const float* w, const cskv_paged& keys,
+                                    const int32_t* ctx_len, int B, int Hi, int ratio, int k, int max_ctx_len,
+                                    int32_t* topk_idx, float* topk_score, void* workspace,
+                                    const cskv_compress_job* jobs, int njobs, cudaStream_t stream,
+                                    const uint32_t** ready);
+
 cudaError_t launch_index_topk_noalloc(const void* q_idx, const float* w, const cskv_paged& keys,
                                       const int32_t* ctx_len, int B, int Hi, int ratio, int k,
                                       int max_ctx_len, int32_t* topk_idx, float* topk_score,
@@ -48,7 +61,8 @@ cudaError_t launch_sparse_decode_attn(const void* q, const cskv_paged& kv, const
                                       const int32_t* ctx_len, const int32_t* topk, int k, int ratio,
                                       int max_ctx, const float* sink, float softmax_scale,
                                       const float* q_rope, int B, int H, void* out, void* workspace,
-                                      cudaStream_t stream, void* out_host = nullptr);
+                                      cudaStream_t stream, void* out_host = nullptr,
+                                      const uint32_t* ready = nullptr);
 cudaError_t launch_sparse_prefill_attn(const void* q, const cskv_paged& kv, const cskv_paged& win,
                                        const int32_t* req_of, const int32_t* pos1, const int32_t* topk, int k,
                                        int ratio, int max_ctx, const float* sink, float softmax_scale,
