@@ -1,7 +1,7 @@
 """GPU parity on the named workloads themselves: the tiny CSA layer end to end (compress,
 index, attend; the oracle finishes it in seconds), and the 1M-context and mixed-batch MXFP4
-decode layers at full size, in the bench's launch configuration, checked on sampled
-requests (indexer selection and attention output against the oracle)."""
+decode layers at full size, every request's selection and attention output against the
+oracle - also through the fused decode step the benchmark times."""
 
 import concurrent.futures
 
@@ -89,17 +89,77 @@ def _full_size(name, sample):
         check_attention(got[b], ref, fp4=wl.main_fmt == synth.FMT_FP4)
 
 
-def test_csa_1m_full_size_sampled_layer():
-    """Batch 8 at 1,048,576 tokens: selection and attention of requests 0, 3 and 7."""
-    _full_size("csa_1m", (0, 3, 7))
+def test_csa_1m_full_size_every_request():
+    """Batch 8 at 1,048,576 tokens: the selection and the attention output of every
+    request against the oracle."""
+    _full_size("csa_1m", range(8))
 
 
-def test_mixed_mxfp4_full_size_sampled_layer():
+def test_mixed_mxfp4_full_size_every_request():
     """Batch 64 with contexts from 32,768 to 524,288 tokens, MXFP4 main entries: the
-    shortest, the longest and two other requests."""
-    wl = synth.workload("mixed_mxfp4")
-    order = np.argsort(wl.ctx_len)
-    _full_size("mixed_mxfp4", (int(order[0]), int(order[-1]), 5, 40))
+    selection and the attention output of every request against the oracle."""
+    _full_size("mixed_mxfp4", range(64))
+
+
+def test_csa_1m_fused_decode_step_every_request():
+    """The same batch through one cskv_decode_layer call (device buffers): the indexer's
+    prep, the compressor writing every request's newest main entry and index key, the
+    score kernel overlapping it, the attention starting per request on its ready flag.
+    Every request's selection and output against the oracle, which codes the same
+    newest entries itself."""
+    wl = synth.workload("csa_1m")
+    keys = _build_lane(wl, "index", synth.FMT_FP8_PAGESPLIT, 128)
+    main = _build_lane(wl, "main", wl.main_fmt, 512)
+    swa_vals = np.stack([synth.swa_values(wl, b) for b in range(wl.B)])
+    swa_b, swa_dec = swa_ring(swa_vals, wl.swa_fmt)
+    q, q_idx, w, sink = synth.queries(wl)
+    q_t, q_v = bf16_values(q)
+    qi_t, qi_v = bf16_values(q_idx)
+    ctx = wl.ctx_len.astype(np.int32)
+    r, B = wl.ratio, wl.B
+    n = (ctx // r).astype(np.int64)
+    first = (n - 1).astype(np.int32)
+    lanes = {}
+    for lane, dim, il in (("main", 512, False), ("index", 128, True)):
+        kv, gate, pkv, pgate = [], [], [], []
+        for b in range(B):
+            a_, g_ = synth.compressor_tokens(wl.seed, r, r, True, dim, index_lane=il, seq=b)
+            pa, pg = synth.compressor_prev(wl.seed, r, dim, index_lane=il, seq=b)
+            kv.append(a_); gate.append(g_); pkv.append(pa); pgate.append(pg)
+        ape, nw = synth.compressor_params(wl.seed, r, True, dim, index_lane=il)
+        lanes[lane] = dict(kv=bf16_values(np.stack(kv)), gate=bf16_values(np.stack(gate)),
+                           pkv=bf16_values(np.stack(pkv)), pgate=bf16_values(np.stack(pgate)), ape=ape, nw=nw)
+    ecs = cskv.rope_table((first.astype(np.int64) * r)[:, None])
+    jobs = []
+    for lane, cache in (("main", main), ("index", keys)):
+        L_ = lanes[lane]
+        jobs.append(dict(kv=L_["kv"][0].cuda(), gate=L_["gate"][0].cuda(), ape=cuda(L_["ape"]), ratio=r, overlap=True,
+                         out=cache, req=cuda(np.arange(B, dtype=np.int32)), first_entry=cuda(first),
+                         prev_kv=L_["pkv"][0].cuda(), prev_gate=L_["pgate"][0].cuda(), norm_w=cuda(L_["nw"]),
+                         rope_cs=cuda(ecs)))
+    out, topk = cskv.decode_layer(jobs, qi_t.cuda(), cuda(w), keys, q_t.cuda(), main, cuda(swa_b), wl.swa_fmt,
+                                  cuda(ctx), wl.k, r, wl.max_ctx, cuda(sink), SCALE, cuda(cskv.rope_table(ctx - 1)))
+    assert cskv.device_status() == 0
+    topk = topk.cpu().numpy()
+    got = out.float().cpu().numpy()
+    for b in range(B):
+        nb = int(n[b])
+        cs = o_rope.table(np.array([int(first[b]) * r]))
+        ents = {}
+        for lane in ("main", "index"):
+            L_ = lanes[lane]
+            ents[lane] = o_comp.compress_contract(L_["kv"][1][b], L_["gate"][1][b], L_["ape"], r, True,
+                                                  prev_kv=L_["pkv"][1][b], prev_gate=L_["pgate"][1][b],
+                                                  norm_w=L_["nw"], eps=1e-6, rope_cs=cs)[0]
+        k_hat = _oracle_keys(wl, b)
+        k_hat[nb - 1] = codecs.decode_pagesplit(codecs.encode_pagesplit(np.tile(ents["index"], (64, 1))), 128)[0]
+        q_hat = indexer.quantize_queries(qi_v[b])
+        assert check_topk(topk[b], None, q_hat, w[b], k_hat, nb, wl.k) == 0, b
+        sel = indexer.select_topk(indexer.scores_fp64(q_hat, w[b], k_hat), wl.k)
+        ent = _oracle_entries(wl, b, sel[sel >= 0], wl.main_fmt)
+        ent[nb - 1] = codecs.decode_rows(codecs.encode_rows(ents["main"][None], wl.main_fmt), wl.main_fmt, 512)[0]
+        ref = o_attn.request_attention(q_v[b], int(ctx[b]), r, swa_dec[b], ent, sel, sink, SCALE)
+        check_attention(got[b], ref, fp4=wl.main_fmt == synth.FMT_FP4)
 
 
 def test_tiny_csa_end_to_end():
