@@ -276,8 +276,7 @@ struct ScoreSmem {
   uint32_t base[2];
   uint32_t nlist;
   int nbv[kReqCache];              // visible entries of the first kReqCache requests
-  uint32_t wcnt[16];               // streaming-mode selection: per-warp candidate counts, then selected counts
-  int wovf[16];                    // per warp: more multi segments than it holds
+  uint32_t wcnt[16];               // streaming-mode selection: per-warp selected counts
   uint32_t d256[256];              // 8-bit digit histogram of the cut
   int qreq;                        // streaming mode: the request this block selects next (-1: none)
   int fresh[kReqCache];            // streaming mode: first entry of each request the compressor may write
@@ -856,112 +855,124 @@ __device__ __noinline__ void select_completed(const IndexArgs& a) {
       continue;
     }
     const uint32_t nexp = above + sm->inT;
-    // ---- fast path.  Each warp owns a contiguous run of rows of 32 segments (a lane per
-    // segment), so its candidates are contiguous and in entry order once the eleven warp
-    // totals are scanned.  single = largest key in a bin >= T and the second not (its one
-    // candidate comes from the metadata); multi = both (the warp reads that segment's
-    // scores again itself, up to kWarpMulti of them).
-    constexpr int kWarpMulti = 16;
+    // ---- fast path (the usual case).  Thread t owns the kOwn consecutive segments from
+    // kOwn * t, so its candidates are consecutive and in entry order once the threads'
+    // counts are scanned; it visits them in an order rotated by t, so that a warp's
+    // metadata loads spread over the banks.  single = largest key in a bin >= T and the
+    // second not: its one candidate comes from the metadata, written by the owner.
+    // multi = both (rare): the owner lists the segment and copies its 32 scores into
+    // shared memory (up to kMulti in the block); a warp per listed segment counts and
+    // writes its entries (a lane per entry).
+    constexpr int kOwn = (kMetaSegs + kScoreThreads - 1) / kScoreThreads;
+    static_assert(kOwn <= 32, "a thread's segments fit a 32-bit mask");
     const bool fast = meta_fits && nexp <= static_cast<uint32_t>(kSelCand);
     if (fast) {
       unsigned long long* s_cand = reinterpret_cast<unsigned long long*>(stages + kMetaSegs * 8);
-      uint16_t* wl = scratch + warp * kWarpMulti;                        // this warp's multi segments
-      uint16_t* wmc = scratch + nwarps * kWarpMulti + warp * kWarpMulti; // their candidate counts
-      float* wsc = reinterpret_cast<float*>(hist) + warp * kWarpMulti * kSeg;   // their scores
-      const int nrows = (nseg + 31) / 32;
-      const int rpw = (nrows + nwarps - 1) / nwarps;
-      const int r0 = min(nrows, warp * rpw), r1 = min(nrows, r0 + rpw);
-      auto classify = [&](int q, bool& single, bool& multi) -> uint64_t {
-        const uint64_t m = q < nseg ? s_meta[q] : 0ull;
-        const int b1 = static_cast<int>(m >> (64 - kHistBits));
-        const int b2 = static_cast<int>((m >> 8) & (kHistBins - 1));
-        single = b1 >= T && b2 < T;
-        multi = b1 >= T && b2 >= T;
-        return m;
-      };
-      uint32_t nsingle = 0, nm = 0;
-#pragma unroll 4
-      for (int r = r0; r < r1; ++r) {
-        bool single, multi;
-        classify(32 * r + lane, single, multi);
-        const unsigned sb = __ballot_sync(0xFFFFFFFFu, single), mb = __ballot_sync(0xFFFFFFFFu, multi);
-        if (multi) {
-          const uint32_t at = nm + __popc(mb & lt_mask);
-          if (at < static_cast<uint32_t>(kWarpMulti)) wl[at] = static_cast<uint16_t>(32 * r + lane);
-        }
-        nsingle += __popc(sb);
-        nm += __popc(mb);
-      }
-      const uint32_t nmw = min(nm, static_cast<uint32_t>(kWarpMulti));
-      __syncwarp();
-#pragma unroll 1
-      for (uint32_t x = lane; x < nmw * 8; x += 32)
-        cp_async16(wsc + (x >> 3) * kSeg + (x & 7) * 4, sc + static_cast<long long>(wl[x >> 3]) * kSeg + (x & 7) * 4);
-      cp_async_wait_all();
-      __syncwarp();
-      uint32_t nmc = 0;
-#pragma unroll 1
-      for (uint32_t h = 0; h < nmw; ++h) {
-        const long long j = static_cast<long long>(wl[h]) * kSeg + lane;
-        const bool f = j < nb && static_cast<int>(order_key(wsc[h * kSeg + lane]) >> (32 - kHistBits)) >= T;
-        const unsigned mm = __ballot_sync(0xFFFFFFFFu, f);
-        if (lane == 0) wmc[h] = static_cast<uint16_t>(__popc(mm));
-        nmc += __popc(mm);
-      }
-      if (lane == 0) {
-        sm->wcnt[warp] = nsingle + nmc;
-        sm->wovf[warp] = nm > static_cast<uint32_t>(kWarpMulti);
-      }
+      float* s_msc = reinterpret_cast<float*>(hist);         // [kMulti][32] scores of the multi segments
+      uint16_t* s_mseg = scratch;                            // [kMulti] their segments
+      uint16_t* s_mc = scratch + kMulti;                     // [kMulti] their candidate counts
+      uint32_t* s_mbits = reinterpret_cast<uint32_t*>(qbuf);   // [kMulti] their candidates' lanes
+      uint32_t* s_mpos = s_mbits + kMulti;                   // [kMulti] position of their first candidate
+      const int q0 = min(nseg, static_cast<int>(threadIdx.x) * kOwn);
+      const int no = min(nseg - q0, kOwn);
+      const int rot = static_cast<int>(threadIdx.x) % kOwn;
+      if (threadIdx.x == 0) sm->cnt[1] = 0;
       __syncthreads();
-      bool ovf = false;
-      uint32_t off = 0, total = 0;
+      // The loops below issue their shared-memory loads in groups of eight before any use
+      // (the latency of one load, not of eight, per group).
+      constexpr int kGrp = 8;
+      static_assert(kOwn % kGrp == 0, "whole groups");
+      uint32_t smask = 0, mmask = 0;   // bit i: segment q0 + i is single / multi
 #pragma unroll 1
-      for (int w2 = 0; w2 < nwarps; ++w2) {
-        ovf |= sm->wovf[w2] != 0;
-        off += w2 < warp ? sm->wcnt[w2] : 0u;
-        total += sm->wcnt[w2];
-      }
-      if (!ovf && total <= static_cast<uint32_t>(kSelCand)) {
-        // the candidates, in entry order, at this warp's offset
-        uint32_t run = off, hb = 0;
-#pragma unroll 4
-        for (int r = r0; r < r1; ++r) {
-          bool single, multi;
-          const int q = 32 * r + lane;
-          const uint64_t m = classify(q, single, multi);
-          const unsigned mb = __ballot_sync(0xFFFFFFFFu, multi);
-          const uint32_t h = hb + __popc(mb & lt_mask);
-          const uint32_t c = single ? 1u : (multi ? wmc[h] : 0u);
-          uint32_t incl = c;
+      for (int g0 = 0; g0 < kOwn; g0 += kGrp) {
+        uint64_t mv[kGrp];
 #pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-            if (lane >= o) incl += y;
-          }
-          const uint32_t at = run + incl - c;
-          if (single) {
-            const uint32_t j = static_cast<uint32_t>(q) * kSeg + static_cast<uint32_t>(m & 31u);
-            s_cand[at] = (m & 0xFFFFFFFF00000000ull) | (0xFFFFFFFFu - j);
-          }
-          // a rare segment with two or more: the whole warp writes it (a lane per entry)
-#pragma unroll 1
-          for (unsigned rest = mb; rest != 0; rest &= rest - 1) {
-            const int l = __ffs(rest) - 1;
-            const uint32_t base = __shfl_sync(0xFFFFFFFFu, at, l);
-            const uint32_t hh = __shfl_sync(0xFFFFFFFFu, h, l);
-            const long long j = static_cast<long long>(32 * r + l) * kSeg + lane;
-            const uint32_t key = order_key(wsc[hh * kSeg + lane]);
-            const bool f = j < nb && static_cast<int>(key >> (32 - kHistBits)) >= T;
-            const unsigned fm = __ballot_sync(0xFFFFFFFFu, f);
-            if (f)
-              s_cand[base + __popc(fm & lt_mask)] =
-                  (static_cast<unsigned long long>(key) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(j));
-          }
-          run += __shfl_sync(0xFFFFFFFFu, incl, 31);
-          hb += __popc(mb);
+        for (int u = 0; u < kGrp; ++u) {
+          const int i = (g0 + u + rot) % kOwn;
+          mv[u] = i < no ? s_meta[q0 + i] : 0ull;
         }
-        const uint32_t mine = sm->wcnt[warp];
+#pragma unroll
+        for (int u = 0; u < kGrp; ++u) {
+          const int i = (g0 + u + rot) % kOwn;
+          const int b1 = static_cast<int>(mv[u] >> (64 - kHistBits));
+          const int b2 = static_cast<int>((mv[u] >> 8) & (kHistBins - 1));
+          if (i < no && b1 >= T) {
+            if (b2 < T) smask |= 1u << i;
+            else mmask |= 1u << i;
+          }
+        }
+      }
+      const uint32_t nm = static_cast<uint32_t>(__popc(mmask));
+      const uint32_t mslot = nm ? atomicAdd(&sm->cnt[1], nm) : 0u;
+      if (nm != 0 && mslot + nm <= static_cast<uint32_t>(kMulti)) {
+        uint32_t h = mslot;
+#pragma unroll 1
+        for (uint32_t mb = mmask; mb != 0; mb &= mb - 1, ++h) {
+          const int q = q0 + __ffs(mb) - 1;
+          s_mseg[h] = static_cast<uint16_t>(q);
+          const float* src = sc + static_cast<long long>(q) * kSeg;
+#pragma unroll
+          for (int x = 0; x < kSeg / 4; ++x) cp_async16(s_msc + h * kSeg + 4 * x, src + 4 * x);
+        }
+      }
+      cp_async_wait_all();
+      __syncthreads();
+      const uint32_t nmulti = sm->cnt[1];
+      if (nmulti <= static_cast<uint32_t>(kMulti)) {   // uniform
+        // the multi segments' entries in bins >= T: a warp per segment
+#pragma unroll 1
+        for (uint32_t h = warp; h < nmulti; h += nwarps) {
+          const long long j = static_cast<long long>(s_mseg[h]) * kSeg + lane;
+          const bool f = j < nb && static_cast<int>(order_key(s_msc[h * kSeg + lane]) >> (32 - kHistBits)) >= T;
+          const unsigned fm = __ballot_sync(0xFFFFFFFFu, f);
+          if (lane == 0) {
+            s_mbits[h] = fm;
+            s_mc[h] = static_cast<uint16_t>(__popc(fm));
+          }
+        }
         __syncthreads();
+        uint32_t c = static_cast<uint32_t>(__popc(smask));
+#pragma unroll 1
+        for (uint32_t r = 0; r < nm; ++r) c += s_mc[mslot + r];
+        uint32_t total;
+        const uint32_t pos = block_scan_excl(sm, c, total);
+        if (total <= static_cast<uint32_t>(kSelCand)) {   // uniform; only an earlier error breaks it
+          // singles by their owners (a visit per candidate segment, not per segment); each
+          // multi segment's first position noted.  The candidates of the thread's first two
+          // multi segments come in by selects, more (rare) by a loop.
+          const uint32_t mb1 = mmask & (0u - mmask);   // lowest multi bit (0: none)
+          const uint32_t mrest = mmask & ~mb1;
+          const uint32_t mb2 = mrest & (0u - mrest);   // second lowest
+          const uint32_t mc1 = nm > 0 ? s_mc[mslot] : 0u;
+          const uint32_t mc2 = nm > 1 ? s_mc[mslot + 1] : 0u;
+#pragma unroll 1
+          for (uint32_t rem = smask | mmask; rem != 0; rem &= rem - 1u) {
+            const int i = __ffs(rem) - 1;
+            const uint32_t bit = 1u << i;
+            uint32_t p = pos + static_cast<uint32_t>(__popc(smask & (bit - 1u))) + (mb1 != 0u && mb1 < bit ? mc1 : 0u) +
+                         (mb2 != 0u && mb2 < bit ? mc2 : 0u);
+            const uint32_t nbefore = static_cast<uint32_t>(__popc(mmask & (bit - 1u)));
+#pragma unroll 1
+            for (uint32_t r = 2; r < nbefore; ++r) p += s_mc[mslot + r];
+            if (smask & bit) {
+              const uint64_t m = s_meta[q0 + i];
+              const uint32_t j = static_cast<uint32_t>(q0 + i) * kSeg + static_cast<uint32_t>(m & 31u);
+              s_cand[p] = (m & 0xFFFFFFFF00000000ull) | (0xFFFFFFFFu - j);
+            } else {
+              s_mpos[mslot + nbefore] = p;
+            }
+          }
+          __syncthreads();
+#pragma unroll 1
+          for (uint32_t h = warp; h < nmulti; h += nwarps) {
+            const uint32_t fm = s_mbits[h];
+            if ((fm >> lane) & 1u) {
+              const uint32_t j = static_cast<uint32_t>(s_mseg[h]) * kSeg + static_cast<uint32_t>(lane);
+              s_cand[s_mpos[h] + __popc(fm & lt_mask)] =
+                  (static_cast<unsigned long long>(order_key(s_msc[h * kSeg + lane])) << 32) | (0xFFFFFFFFu - j);
+            }
+          }
+          __syncthreads();
         // ---- the cut among bin T's keys by 8-bit digits (bits 51-44, 43-36, ..., 11-4, 3-0);
         // keys above bin T never match the prefix and are all taken
         if (threadIdx.x == 0) {
@@ -1028,42 +1039,45 @@ __device__ __noinline__ void select_completed(const IndexArgs& a) {
           __syncthreads();
           if (shift == 0) break;
         }
-        // ---- the output: selected <=> (key & mask) >= prefix; each warp its own range, in order
+        // ---- the output: selected <=> (key & mask) >= prefix; each warp a contiguous
+        // range of the candidates, in order
         const unsigned long long pm = sm->mask, pp = sm->prefix;
+        const uint32_t off = static_cast<uint32_t>((static_cast<unsigned long long>(total) * warp) / nwarps);
+        const uint32_t end = static_cast<uint32_t>((static_cast<unsigned long long>(total) * (warp + 1)) / nwarps);
         uint32_t nsel_w = 0;
 #pragma unroll 1
-        for (uint32_t x0 = off; x0 < off + mine; x0 += 32) {
+        for (uint32_t x0 = off; x0 < end; x0 += 32) {
           const uint32_t x = x0 + lane;
-          const bool sel = x < off + mine && (s_cand[x] & pm) >= pp;
+          const bool sel = x < end && (s_cand[x] & pm) >= pp;
           nsel_w += __popc(__ballot_sync(0xFFFFFFFFu, sel));
         }
-        __syncthreads();   // every warp has read the cut before the counts are reused
         if (lane == 0) sm->wcnt[warp] = nsel_w;
         __syncthreads();
-        uint32_t pos = 0, nsel = 0;
+        uint32_t opos = 0, nsel = 0;
 #pragma unroll 1
         for (int w2 = 0; w2 < nwarps; ++w2) {
-          pos += w2 < warp ? sm->wcnt[w2] : 0u;
+          opos += w2 < warp ? sm->wcnt[w2] : 0u;
           nsel += sm->wcnt[w2];
         }
 #pragma unroll 1
-        for (uint32_t x0 = off; x0 < off + mine; x0 += 32) {
+        for (uint32_t x0 = off; x0 < end; x0 += 32) {
           const uint32_t x = x0 + lane;
-          const unsigned long long key = x < off + mine ? s_cand[x] : 0ull;
-          const bool sel = x < off + mine && (key & pm) >= pp;
+          const unsigned long long key = x < end ? s_cand[x] : 0ull;
+          const bool sel = x < end && (key & pm) >= pp;
           const unsigned m = __ballot_sync(0xFFFFFFFFu, sel);
-          const uint32_t p = pos + __popc(m & lt_mask);
+          const uint32_t p = opos + __popc(m & lt_mask);
           if (sel && p < static_cast<uint32_t>(a.k)) {
             out_idx[p] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(key));
             if (out_sc) out_sc[p] = from_order_key(static_cast<uint32_t>(key >> 32));
           }
-          pos += __popc(m);
+          opos += __popc(m);
         }
         pad_out(b, static_cast<int>(min(nsel, static_cast<uint32_t>(a.k))));   // only after an error
         raise_ready(b);
         continue;
+        }
       }
-      __syncthreads();   // an overflowing warp: every warp is past the counts before the general path
+      __syncthreads();   // too many multi segments: every thread is past the counts before the general path
     }
     // ---- general path: every segment whose largest key reaches T is read again, in rounds
     unsigned long long* cand = nexp <= static_cast<uint32_t>(kSelCand)
@@ -1279,6 +1293,24 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
     __syncthreads();
   }
   if (!sched_thread && wait_at_start) grid_dep_wait();
+  // visible entries of request b: the first kReqCache requests' counts were kept in
+  // shared memory by the set-up (a global load and a 64-bit division fewer on the
+  // scheduler's path)
+  auto nvis = [&](int b) { return b < kReqCache ? sm->nbv[b] : visible(a, b); };
+  if constexpr (!LARGE) {
+    // the home request's block-table row goes to L2 before the scheduler reads it (its
+    // loads then return in one L2 round trip): each of the request's home blocks
+    // prefetches its share of the row's 128-byte lines
+    const int hb = home_request(blockIdx.x, a.B, gridDim.x);
+    const int f0 = first_home_block(hb, a.B, gridDim.x);
+    const int nh = first_home_block(hb + 1, a.B, gridDim.x) - f0;
+    const int pages = min(a.keys.max_pages, (nvis(hb) + kPageRows - 1) / kPageRows);
+    const int32_t* row = a.keys.block_table + static_cast<long long>(hb) * a.keys.max_pages;
+#pragma unroll 1
+    for (int x = static_cast<int>(blockIdx.x) - f0 + nh * static_cast<int>(threadIdx.x); 32 * x < pages;
+         x += nh * static_cast<int>(blockDim.x))
+      prefetch_l2(row + 32 * x);
+  }
 
   // ======================================================= phase 1: scores
   // Tiles are handed out dynamically, in chunks of kChunkTiles consecutive tiles of
@@ -1347,13 +1379,13 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
       };
       if (pw == 0) {
         // Scheduler.  Work comes in chunks of kChunkTiles consecutive tiles of one
-        // request, grabbed from the request's counter; the chunk after next is
+        // request, grabbed from the request's counter; the chunks after next are
         // grabbed, and the next chunk's page ids loaded, while the current one is
-        // posted, so neither the atomic nor the block-table loads stall the stream.
-        auto tiles_of = [&](int b) { return (visible(a, b) + kTileRows - 1) / kTileRows; };
+        // posted, so neither the atomics nor the block-table loads stall the stream.
+        auto tiles_of = [&](int b) { return (nvis(b) + kTileRows - 1) / kTileRows; };
         // the chunk's 2 x kChunkTiles page ids, all loads in flight
         auto chunk_ids = [&](int b, int t0, int (&ids)[2 * kChunkTiles]) {
-          const int n_b = b >= 0 ? visible(a, b) : 0;
+          const int n_b = b >= 0 ? nvis(b) : 0;
           const int32_t* bt = a.keys.block_table + static_cast<long long>(b < 0 ? 0 : b) * a.keys.max_pages;
 #pragma unroll
           for (int u = 0; u < 2 * kChunkTiles; ++u) {
@@ -1363,6 +1395,11 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
         };
         int req = home_request(blockIdx.x, a.B, gridDim.x);
         uint32_t pending = 0;
+        // streaming mode keeps a second grab of the same request in flight, so that an
+        // atomic has two chunks' time to return before its result is needed
+        constexpr uint32_t kNoGrab = 0xFFFFFFFFu;
+        uint32_t pending2 = kNoGrab;
+        auto grab = [&]() { return atomicAdd(&ctr_all[req * 4], static_cast<uint32_t>(kChunkTiles)); };
         uint32_t* handed = gbar + 1;   // LARGE: tiles handed out so far (cleared by the prep)
         // the next chunk: (request, first tile) from the pending grab; request -1 = none left
         auto resolve = [&](int& b, int& t0) {
@@ -1376,7 +1413,8 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
             req = (req + 1) % a.B;
             tiles = tiles_of(req);
             if constexpr (LARGE) seen = *reinterpret_cast<volatile uint32_t*>(handed);
-            pending = atomicAdd(&ctr_all[req * 4], static_cast<uint32_t>(kChunkTiles));
+            pending = grab();
+            pending2 = kNoGrab;
           }
           if (pending >= static_cast<uint32_t>(tiles)) {
             b = -1;
@@ -1384,8 +1422,13 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
           } else {
             b = req;
             t0 = static_cast<int>(pending);
-            if constexpr (LARGE) atomicAdd(handed, static_cast<uint32_t>(min(kChunkTiles, tiles - t0)));
-            pending = atomicAdd(&ctr_all[req * 4], static_cast<uint32_t>(kChunkTiles));
+            if constexpr (LARGE) {
+              atomicAdd(handed, static_cast<uint32_t>(min(kChunkTiles, tiles - t0)));
+              pending = grab();
+            } else {
+              pending = pending2 != kNoGrab ? pending2 : grab();
+              pending2 = grab();
+            }
           }
         };
         int cb = -1, ct = 0;
@@ -1419,17 +1462,18 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
             ++nreq;
             q_b = cb;
           }
-          // the chunk's pairs: the first tile here, the second handed to producer 1;
-          // after the first pair, the next chunk is resolved and its page ids requested
+          // the next chunk is resolved and its page ids requested first (they have the
+          // whole chunk's time to arrive); then the chunk's pairs: the first tile here,
+          // the second handed to producer 1
           int nb2 = -1, nt = 0;
           int nids[2 * kChunkTiles];
+          if (cb >= 0) {
+            resolve(nb2, nt);   // usually already returned: grabbed two chunks ago
+            chunk_ids(nb2, nt, nids);
+          }
 #pragma unroll
           for (int pr = 0; pr < kChunkTiles / 2; ++pr, ++m) {
             if (pr > 0 && cb < 0) break;   // the end marker is one pair
-            if (pr == 1) {
-              resolve(nb2, nt);   // usually already returned: grabbed one chunk ago
-              chunk_ids(nb2, nt, nids);
-            }
             const int hs = static_cast<int>(m % kPairSlots);
             if (m >= kPairSlots && !role_wait(sm, &sm->pempty[hs], ((m / kPairSlots) - 1) & 1, a.spin)) {
               ok = false;
@@ -1539,6 +1583,7 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
     int pend_b = -1;
     uint32_t pend_old = 0, pend_cnt = 0, pend_tiles = 0;
     uint32_t hphase = 0;
+    float wr[64];   // the current request's head weights (query scales folded in)
     // the group's four warps meet (bounded: an aborted pass falls through)
     auto grp_sync = [&]() {
       __syncwarp();
@@ -1605,10 +1650,12 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
           if (cur_b >= 0) publish(cur_b);
         }
         cur_b = ti.x;
-        n_b = visible(a, cur_b);
+        n_b = cur_b < kReqCache ? sm->nbv[cur_b] : visible(a, cur_b);
         tiles_b = (n_b + kTileRows - 1) / kTileRows;
         if (gtid < 64) wq_s[gtid] = gtid < N ? wq_all[cur_b * 64 + gtid] : 0.f;
         grp_sync();
+#pragma unroll
+        for (int h = 0; h < 64; ++h) wr[h] = wq_s[h];
       }
       const long long j = static_cast<long long>(ti.y) * kTileRows + row;
       const bool real = ti.y < tiles_b;
@@ -1618,28 +1665,45 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
       if (!role_wait(sm, &sm->accfull[c], (i / kAccs) & 1, a.spin)) break;
       tc_fence_after();
       const uint32_t tb = tmem + (static_cast<uint32_t>(sub * 32) << 16) + c * N;
-      float P[64];
-      if (N == 64) {
-        tmem_ld32(tb, *reinterpret_cast<float(*)[32]>(P));
-        tmem_ld32(tb + 32, *reinterpret_cast<float(*)[32]>(P + 32));
+      // Heads 0-31, then 32-63: half the logits in registers at a time (the weights stay
+      // in registers for the whole request).  Four independent accumulation chains, two
+      // per packed fma (the epilogue's instruction count and latency set part of the
+      // streaming pace).
+      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+      float P[32];
+      auto release_acc = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm->accempty[c]);   // this warp's TMEM reads are done
+      };
+      if (N >= 32) {
+        tmem_ld32(tb, P);
       } else {
-#pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 16)
-          if (c0 < N) tmem_ld16(tb + c0, *reinterpret_cast<float(*)[16]>(P + c0));
+        tmem_ld16(tb, *reinterpret_cast<float(*)[16]>(P));
       }
       tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm->accempty[c]);   // this warp's TMEM reads are done
-      // four independent accumulation chains, two per packed fma (the epilogue's
-      // instruction count sets part of the streaming pace)
-      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+      if (N <= 32) release_acc();
 #pragma unroll
-      for (int h = 0; h < 64; h += 4) {
+      for (int h = 0; h < 32; h += 4) {
         if (h < N) {
-          const float4 w4 = *reinterpret_cast<const float4*>(&wq_s[h]);
-          fma2(s0, s1, w4.x, w4.y, fmaxf(P[h], 0.f), fmaxf(P[h + 1], 0.f));
-          fma2(s2, s3, w4.z, w4.w, fmaxf(P[h + 2], 0.f), fmaxf(P[h + 3], 0.f));
+          fma2(s0, s1, wr[h], wr[h + 1], fmaxf(P[h], 0.f), fmaxf(P[h + 1], 0.f));
+          fma2(s2, s3, wr[h + 2], wr[h + 3], fmaxf(P[h + 2], 0.f), fmaxf(P[h + 3], 0.f));
+        }
+      }
+      if (N > 32) {
+        if (N == 64) {
+          tmem_ld32(tb + 32, P);
+        } else {
+          tmem_ld16(tb + 32, *reinterpret_cast<float(*)[16]>(P));
+        }
+        tmem_wait_ld();
+        release_acc();
+#pragma unroll
+        for (int h = 0; h < 32; h += 4) {
+          if (32 + h < N) {
+            fma2(s0, s1, wr[32 + h], wr[33 + h], fmaxf(P[h], 0.f), fmaxf(P[h + 1], 0.f));
+            fma2(s2, s3, wr[34 + h], wr[35 + h], fmaxf(P[h + 2], 0.f), fmaxf(P[h + 3], 0.f));
+          }
         }
       }
       const float I = ((s0 + s1) + (s2 + s3)) * ks;   // the key's scale is a positive power of two
