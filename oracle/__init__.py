@@ -9,7 +9,8 @@ imports the CUDA library or its Python binding.
 
 Modules
 -------
-codecs     FP8 (e4m3 + e8m0 per 32), FP4 (e2m1 + e4m3 per 16) and bf16 row codecs
+codecs     FP8 (e4m3 + e8m0 per 32), FP4 (e2m1 + e4m3 per 16) and bf16 row codecs; the
+           index keys' page-split FP8 and Hadamard-rotated FP4 (e2m1 + e8m0 per 32)
 expo       exp_own: the Cody-Waite exponential of the bit-exact compressor contract
 rope       partial-RoPE tables (plain and YaRN) and rotations
 compress   the gated per-channel pooling compressor (fp64 definition, fp32 contract)

@@ -28,6 +28,18 @@ Readings where the pages are silent:
   scales ("page-split"), so the data rows form one dense 8 KiB tile.
 * Query rows of the FP8 indexer are coded with the same rule, one scale per
   head (block 128).
+* FP4 index keys ("DeepSeek-V4 deep dive", section 5.2: the indexer's keys and
+  queries go through a Hadamard rotation and then FP4 rounding with block size
+  32; "DeepSeek-V4.1 Flash", section 10.4: MXFP4, E2M1 values sharing a scale per
+  1 x 32): the 128-d key is rotated by H / sqrt(128) (H the Sylvester Hadamard
+  matrix), then coded as 128 e2m1 values with one e8m0 scale per 32 - 64 + 4 = 68
+  bytes.  The scale follows the FP8 rule with 6 in place of 448: the smallest
+  power of two 2^e with amax <= 6 * 2^e (nothing saturates).  Page-split like the
+  FP8 keys: in a 64-row page the 64 rows of 64 code bytes come first, then the 64
+  rows of 4 scale bytes.  The rotation's fp32 rendering (the order fixed so that
+  the codes are reproducible bit for bit) is the fast Walsh-Hadamard butterfly
+  with strides 1, 2, 4, ..., 64, each (a, b) -> (a + b, a - b) rounded to fp32,
+  then one multiplication by fp32(1 / sqrt(128)).
 
 Everything here is elementwise numpy on exactly representable values; fp32
 steps are done in np.float32 (IEEE, round-to-nearest-even).
@@ -197,6 +209,7 @@ FMT_BF16 = 0
 FMT_FP8 = 1            # e4m3 data then e8m0 per 32, inline per row
 FMT_FP4 = 2            # packed e2m1 data then e4m3 per 16, inline per row
 FMT_FP8_PAGESPLIT = 3  # index keys: e4m3 codes + one fp32 power-of-two scale per row, page-split
+FMT_FP4H_PAGESPLIT = 4  # index keys: Hadamard-rotated, e2m1 codes + e8m0 per 32, page-split
 
 PAGE_ROWS = 64
 
@@ -210,6 +223,8 @@ def row_bytes(fmt, dim):
         return dim + 4
     if fmt == FMT_FP4:
         return dim // 2 + dim // 16
+    if fmt == FMT_FP4H_PAGESPLIT:
+        return dim // 2 + dim // 32
     raise ValueError(fmt)
 
 
@@ -267,3 +282,111 @@ def encode_q_perhead(q):
     """
     c, s = fp8_encode(q, block=q.shape[-1])
     return c, s[..., 0]
+
+
+# ----------------------------------------------------------------------------
+# FP4 index keys: Hadamard rotation, e2m1 + e8m0 per 32
+# ----------------------------------------------------------------------------
+
+def hadamard_matrix(n):
+    """Sylvester Hadamard matrix: H[i, j] = (-1)^popcount(i & j), n a power of two."""
+    i = np.arange(n)
+    bits = np.bitwise_and(i[:, None], i[None, :])
+    pop = np.zeros_like(bits)
+    while np.any(bits):
+        pop += bits & 1
+        bits >>= 1
+    return np.where(pop % 2 == 0, 1.0, -1.0)
+
+
+def hadamard_fp64(x):
+    """The rotation by definition: y = H x / sqrt(n) along the last axis (fp64)."""
+    x = np.asarray(x, np.float64)
+    n = x.shape[-1]
+    return x @ hadamard_matrix(n).T / np.sqrt(n)
+
+
+def hadamard_contract(x):
+    """fp32 rendering of the rotation in the fixed order: butterflies of stride 1, 2,
+    ..., n/2 on the pairs (i, i + h) with i & h == 0, each (a, b) -> (a + b, a - b)
+    rounded to fp32, then a multiplication by fp32(1 / sqrt(n))."""
+    y = np.array(x, dtype=np.float32, copy=True)
+    n = y.shape[-1]
+    h = 1
+    while h < n:
+        idx = np.arange(n)
+        lo = idx[(idx & h) == 0]
+        a = y[..., lo].copy()
+        b = y[..., lo + h].copy()
+        y[..., lo] = (a + b).astype(np.float32)
+        y[..., lo + h] = (a - b).astype(np.float32)
+        h *= 2
+    return (y * np.float32(1.0 / np.sqrt(float(n)))).astype(np.float32)
+
+
+def e8m0_exponent_fp4(amax):
+    """Scale exponent of an FP4 block: the smallest integer e with amax <= 6 * 2^e.
+
+    amax is a non-negative fp32 value; 6 = 1.5 * 2^2.  Returns int64 e in
+    [-127, 127]; amax == 0 returns 0 (scale byte 127).
+    """
+    a = np.asarray(amax, dtype=np.float32)
+    bits = a.view(np.uint32).astype(np.int64)
+    biased = bits >> 23
+    mant = bits & 0x7FFFFF
+    e = np.where(mant <= 0x400000, biased - 127 - 2, biased - 127 - 1)
+    e = np.where(biased == 0, -127, e)              # fp32 subnormal amax: clamp
+    e = np.clip(e, -127, 127)
+    return np.where(a == 0, 0, e).astype(np.int64)
+
+
+def fp4b32_encode(x, block=32):
+    """x [..., D] float32 -> (packed e2m1 uint8 [..., D/2], e8m0 scale bytes uint8 [..., D/block]).
+
+    Channel 2i sits in the low nibble of byte i."""
+    x = np.asarray(x, dtype=np.float32)
+    D = x.shape[-1]
+    xb = x.reshape(x.shape[:-1] + (D // block, block))
+    e = e8m0_exponent_fp4(np.max(np.abs(xb), axis=-1))
+    y = (xb * _pow2_f32(-e)[..., None]).astype(np.float32)     # exact power-of-two scaling
+    nib = e2m1_encode(y).astype(np.uint8).reshape(x.shape)
+    packed = (nib[..., 0::2] | (nib[..., 1::2] << 4)).astype(np.uint8)
+    return packed, (e + 127).astype(np.uint8)
+
+
+def fp4b32_decode(packed, scales, block=32):
+    """Inverse of fp4b32_encode (exact) -> float64 [..., D]."""
+    packed = np.asarray(packed)
+    lo = e2m1_decode(packed & 0xF)
+    hi = e2m1_decode(packed >> 4)
+    v = np.stack([lo, hi], axis=-1).reshape(packed.shape[:-1] + (packed.shape[-1] * 2,))
+    D = v.shape[-1]
+    v = v.reshape(v.shape[:-1] + (D // block, block)) * e8m0_decode(scales)[..., None]
+    return v.reshape(v.shape[:-2] + (D,))
+
+
+def encode_fp4h_pagesplit(x):
+    """Index keys x [64*p, 128] float32 (not yet rotated) -> bytes [p, 64*68]: per page
+    64 rows of 64 code bytes, then 64 rows of 4 scale bytes."""
+    x = np.asarray(x, dtype=np.float32)
+    n, D = x.shape
+    assert n % PAGE_ROWS == 0
+    c, s = fp4b32_encode(hadamard_contract(x))
+    p = n // PAGE_ROWS
+    return np.concatenate([c.reshape(p, -1), s.reshape(p, -1)], axis=-1)
+
+
+def decode_fp4h_pagesplit(pages, dim):
+    """bytes [p, 64*(D/2 + D/32)] -> the rotated key values, float64 [64*p, D]."""
+    pages = np.asarray(pages, dtype=np.uint8)
+    p = pages.shape[0]
+    cb = dim // 2
+    c = pages[:, :PAGE_ROWS * cb].reshape(p * PAGE_ROWS, cb)
+    s = pages[:, PAGE_ROWS * cb:PAGE_ROWS * (cb + dim // 32)].reshape(p * PAGE_ROWS, dim // 32)
+    return fp4b32_decode(c, s)
+
+
+def encode_q_fp4h(q):
+    """Indexer queries [..., H, 128] float32 -> (packed codes [..., H, 64], e8m0 bytes [..., H, 4]):
+    rotated like the keys, then coded with one scale per 32."""
+    return fp4b32_encode(hadamard_contract(q))

@@ -134,4 +134,6 @@ def entries_to_bytes(entries, fmt):
     """Contract entries [n, D] float32 -> stored bytes (inline rows, or pages for page-split)."""
     if fmt == codecs.FMT_FP8_PAGESPLIT:
         return codecs.encode_pagesplit(entries)
+    if fmt == codecs.FMT_FP4H_PAGESPLIT:
+        return codecs.encode_fp4h_pagesplit(entries)   # rotated, then coded
     return codecs.encode_rows(entries, fmt)

@@ -13,7 +13,11 @@ min(k, n) entries; missing slots are -1.
 Readings: larger score first, ties to the smaller
 entry index; the output is a set, returned here in ascending entry order.
 With FP8 keys the queries are coded e4m3 with one e8m0 scale per head, and
-the exact values of the coded operands enter the fp64 score.
+the exact values of the coded operands enter the fp64 score.  With FP4 index
+keys ("DeepSeek-V4 deep dive", section 5.2) the queries are rotated and coded
+like the keys (e2m1, e8m0 per 32), and the scores are stored in BF16 before the
+selection ("DeepSeek-V4.1 Flash", section 10.4), so that ties between equal
+bf16 scores go to the smaller entry.
 """
 
 import numpy as np
@@ -48,6 +52,31 @@ def quantize_queries(q):
     q32 = np.asarray(q, np.float32)
     c, s = codecs.encode_q_perhead(q32)
     return codecs.e4m3_decode(c) * codecs.e8m0_decode(s)[..., None]
+
+
+def quantize_queries_fp4(q):
+    """Indexer queries [Hi, 128] (bf16 values) -> exact values of their rotated FP4 coding."""
+    c, s = codecs.encode_q_fp4h(np.asarray(q, np.float32))
+    return codecs.fp4b32_decode(c, s)
+
+
+def bf16_scores(I):
+    """Index scores stored in BF16 ("DeepSeek-V4.1 Flash", section 10.4): the score,
+    rounded to fp32 (the precision it is computed in), then to bf16, RNE both times."""
+    return codecs.bf16_decode(codecs.bf16_encode(np.asarray(I, np.float64).astype(np.float32)))
+
+
+def index_topk_fp4(q, w, k_hat, ctx_len, ratio, k):
+    """One request with FP4 index keys: the rotated FP4 queries against the rotated
+    FP4 keys (exact values, fp64 score), the scores rounded to bf16, top-k on those.
+
+    k_hat  [>= n, 128] exact (rotated) key values in entry order
+    Returns (topk [k] int64, bf16 scores [n] float64, fp64 scores [n]).
+    """
+    n = int(visible_entries(ctx_len, ratio))
+    I = scores_fp64(quantize_queries_fp4(q), w, np.asarray(k_hat)[:n])
+    Ib = bf16_scores(I)
+    return select_topk(Ib, k), Ib, I
 
 
 def index_topk(q, w, k_hat, ctx_len, ratio, k, fp8_keys):

@@ -163,7 +163,7 @@ def test_v41_global_kv_decomposition(golden):
     # with one e8m0 scale per 32)
     g = golden["v41_global_kv"]
     copies = g["encoder_copies"] / g["encoder_merge"] + g["decoder_copies"] / g["decoder_merge"]
-    fp4_index_key = 128 // 2 + 128 // 32
+    fp4_index_key = codecs.row_bytes(codecs.FMT_FP4H_PAGESPLIT, 128)   # 64 code bytes + 4 scale bytes
     assert copies * (codecs.row_bytes(codecs.FMT_FP4, 512) + fp4_index_key) == g["bytes_per_token"]
 
 
