@@ -39,6 +39,7 @@ from compressed_sparse_attention_kv_gb300 import synth  # noqa: E402
 
 METRIC = "decode attn queries/s per layer at 1M ctx; KV-read GB/s and % of HBM/FP8 roofline"
 MIXED_METRIC = "mixed-batch MXFP4 CSA decode: queries/s per layer (batch 64, contexts 32K-512K)"
+FP4_METRIC = "decode attn queries/s per layer at 1M ctx with FP4 index keys (68 B, BF16 scores)"
 WORKLOAD = "csa_1m"
 L2_FLUSH_BYTES = 512 << 20
 
@@ -51,11 +52,13 @@ def workload_desc(wl):
                 "FP8 window 128, sink; per step: compress the completed block (main + index key), index_topk, "
                 "sparse_decode_attn" % (wl.B, int(wl.ctx_len.min()), int(wl.ctx_len.max()),
                                         int(wl.n_entries.sum()), wl.ratio, wl.Hi, wl.k, wl.H))
-    return ("CSA decode at 1M context: batch %d, %d tokens -> %d entries at ratio %d, indexer %d heads "
-            "x 128 FP8 keys (132 B) w~U(0,1), top-%d, %d query heads x 512 over FP8-528 entries "
+    keys = ("FP4 keys (68 B: Hadamard-rotated e2m1 + e8m0 per 32, BF16 scores)"
+            if wl.key_fmt == synth.FMT_FP4H_PAGESPLIT else "FP8 keys (132 B)")
+    return (("CSA decode at 1M context: batch %d, %d tokens -> %d entries at ratio %d, indexer %d heads "
+             "x 128 " + keys + " w~U(0,1), top-%d, %d query heads x 512 over FP8-528 entries "
             "+ FP8 window 128, sink; per step: compress the completed block (main + index key), "
-            "index_topk, sparse_decode_attn" % (wl.B, int(wl.ctx_len[0]), int(wl.n_entries[0]), wl.ratio,
-                                               wl.Hi, wl.k, wl.H))
+            "index_topk, sparse_decode_attn") % (wl.B, int(wl.ctx_len[0]), int(wl.n_entries[0]), wl.ratio,
+                                                wl.Hi, wl.k, wl.H))
 
 
 def step_inputs(wl):
@@ -145,12 +148,13 @@ def gen_parallel(fn, items, threads=16):
 
 
 def build_caches(wl, torch, cskv):
-    """Resident caches: index keys (FP8 page-split), main entries (the workload's format), window ring (FP8-528)."""
+    """Resident caches: index keys and main entries (the workload's formats), window ring (FP8-528)."""
     dev = "cuda"
     bt_i, np_i = synth.page_tables(wl, "index")
     bt_m, np_m = synth.page_tables(wl, "main")
-    keys = cskv.PagedCache(torch.zeros((np_i, 64 * 132), dtype=torch.uint8, device=dev),
-                           torch.from_numpy(bt_i).to(dev), cskv.FMT_FP8_PAGESPLIT, 128)
+    krb = cskv.row_bytes(wl.key_fmt, 128)
+    keys = cskv.PagedCache(torch.zeros((np_i, (64 * krb + 15) // 16 * 16), dtype=torch.uint8, device=dev),
+                           torch.from_numpy(bt_i).to(dev), wl.key_fmt, 128)
     mrb = cskv.row_bytes(wl.main_fmt, 512)
     main = cskv.PagedCache(torch.zeros((np_m, (64 * mrb + 15) // 16 * 16), dtype=torch.uint8, device=dev),
                            torch.from_numpy(bt_m).to(dev), wl.main_fmt, 512)
@@ -372,7 +376,8 @@ def run_gpu(args, rank, world, workload=WORKLOAD):
     mean_ms, e2e_mean = max_over_ranks([statistics.mean(step_ms), statistics.mean(e2e_ms)], world, dev)
 
     # ---- roofline of the dominant kernel (the indexer score pass): bytes it must read
-    algo_bytes = 132 * int(wl.n_entries.sum())
+    fp4_keys = wl.key_fmt == synth.FMT_FP4H_PAGESPLIT
+    algo_bytes = cskv.row_bytes(wl.key_fmt, 128) * int(wl.n_entries.sum())
     score_mean = statistics.mean(score_ms)
     peaks = {}
     try:
@@ -382,12 +387,12 @@ def run_gpu(args, rank, world, workload=WORKLOAD):
         pass
     peak = peaks.get("hbm_gbs", 6800.0)
     achieved = algo_bytes / (score_mean * 1e-3) / 1e9
-    traffic = profiled_traffic()
+    traffic = None if fp4_keys else profiled_traffic()
     path_bytes = algo_bytes + B * (512 * cskv.row_bytes(wl.main_fmt, 512) + 128 * 528 + 2 * H * 512 * 2
                                    + Hi * 128 * 2)
 
     res = {
-        "metric": METRIC if workload == WORKLOAD else MIXED_METRIC,
+        "metric": METRIC if workload == WORKLOAD else (FP4_METRIC if fp4_keys else MIXED_METRIC),
         "value": job_throughput(world, B, mean_ms),
         "unit": "queries/s",
         "n_gpus": world,
@@ -397,14 +402,16 @@ def run_gpu(args, rank, world, workload=WORKLOAD):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "e4m3 (indexer MMA) + bf16 (attention MMA), fp32 accumulate",
+        "dtype": ("e2m1 block-scaled (indexer MMA)" if fp4_keys else "e4m3 (indexer MMA)")
+                 + " + bf16 (attention MMA), fp32 accumulate",
         "data": "synthetic (seeded N(0,1) caches and queries, U(0,1) head weights)",
         "config": {"workload": workload_desc(wl), "batch_per_gpu": B, "context": L,
                    "l2": "flushed before every timed step (512 MB write, outside the timed region); "
                          "inputs (%d MB of index keys) also exceed L2" % (algo_bytes // 1000000),
                    "timing": "CUDA events per step around a CUDA-graph replay" if graph else "CUDA events per step",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": {"kernel": "index_score_kernel (FP8 keys, tcgen05 e4m3 MMA)", "bound": "hbm",
+        "roofline": {"kernel": ("index_score_kernel (FP4 keys, tcgen05 kind::mxf4 block-scaled MMA)" if fp4_keys
+                                else "index_score_kernel (FP8 keys, tcgen05 e4m3 MMA)"), "bound": "hbm",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": "measured" if "hbm_gbs" in peaks else "fallback",
                      "algorithmic_bytes_per_launch": algo_bytes, "ms_per_launch": score_mean,
@@ -450,9 +457,10 @@ class OracleRunner:
         self.inp = step_inputs(wl)
         self.req = list(requests)
         self.keys, self.main_pages, self.swa = {}, {}, {}
+        self.fp4 = wl.key_fmt == codecs.FMT_FP4H_PAGESPLIT
         for b in self.req:
             vals = synth.request_values(wl, b, "index")
-            self.keys[b] = codecs.encode_pagesplit(vals)
+            self.keys[b] = codecs.encode_fp4h_pagesplit(vals) if self.fp4 else codecs.encode_pagesplit(vals)
             self.swa[b] = codecs.encode_rows(synth.swa_values(wl, b), wl.swa_fmt)
             # cache preparation (untimed): code the main pages this request's selection reads
             ent, ik = self._compress(b)
@@ -485,6 +493,11 @@ class OracleRunner:
         from oracle import codecs, indexer
         wl, inp = self.wl, self.inp
         n = int(wl.n_entries[b])
+        if self.fp4:
+            k_hat = codecs.decode_fp4h_pagesplit(self.keys[b], 128)
+            k_hat[n - 1] = codecs.fp4b32_decode(*codecs.fp4b32_encode(codecs.hadamard_contract(ik)))[0]
+            return indexer.index_topk_fp4(self._bf(inp["q_idx"][b]), inp["w"][b], k_hat, int(wl.ctx_len[b]),
+                                          wl.ratio, wl.k)[0]
         k_hat = codecs.decode_pagesplit(self.keys[b], 128)
         k_hat[n - 1] = codecs.fp8_decode(*codecs.fp8_encode(ik, block=128), block=128)[0]   # one scale per key
         top, _ = indexer.index_topk(self._bf(inp["q_idx"][b]), inp["w"][b], k_hat, int(wl.ctx_len[b]),
@@ -562,8 +575,8 @@ def oracle_sample(mode):
     """The oracle timed on a bounded sample of a mode's workload (set-up untimed).
     Returns dict(value, unit, higher_is_better, sample)."""
     from oracle import attention, codecs, compress, indexer, rope
-    if mode in ("decode", "mixed"):
-        wl = synth.workload(WORKLOAD if mode == "decode" else "mixed_mxfp4")
+    if mode in ("decode", "mixed", "csa_fp4"):
+        wl = synth.workload({"decode": WORKLOAD, "mixed": "mixed_mxfp4", "csa_fp4": "csa_fp4"}[mode])
         reqs = [0, 1]
         runner = OracleRunner(wl, reqs)
         t0 = time.perf_counter()
@@ -1100,7 +1113,8 @@ def main():
     ap.add_argument("--impl", choices=["cskv", "reference"], default="cskv")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--mode", choices=["decode", "tiny", "hca", "compress", "mixed", "csa2", "state", "prefill"],
+    ap.add_argument("--mode", choices=["decode", "tiny", "hca", "compress", "mixed", "csa_fp4", "csa2", "state",
+                                       "prefill"],
                     default="decode",
                     help="decode: the benchmark (1M context); tiny / hca / compress / mixed: the other named "
                          "workloads; csa2 / state / prefill: the rows built beyond the decode step")
@@ -1115,7 +1129,7 @@ def main():
         return
     args.warmup = max(3, args.warmup)
     if args.steps is None:
-        args.steps = 1000 if (args.impl == "cskv" and args.mode in ("decode", "mixed")) else 50
+        args.steps = 1000 if (args.impl == "cskv" and args.mode in ("decode", "mixed", "csa_fp4")) else 50
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
 
@@ -1133,12 +1147,12 @@ def main():
             for line in (res if isinstance(res, list) else [res]):
                 print(json.dumps(line))
         return
-    if args.mode == "mixed":
-        res = run_gpu(args, 0, 1, workload="mixed_mxfp4")
-        res["mode"] = "mixed"
+    if args.mode in ("mixed", "csa_fp4"):
+        res = run_gpu(args, 0, 1, workload="mixed_mxfp4" if args.mode == "mixed" else "csa_fp4")
+        res["mode"] = args.mode
         if not args.no_cpu_baseline:
             try:
-                res["cpu_baseline"] = cpu_baseline("mixed")
+                res["cpu_baseline"] = cpu_baseline(args.mode)
             except Exception as e:
                 res["cpu_baseline"] = {"value": None, "error": repr(e)[:200]}
         print(json.dumps(res))

@@ -29,6 +29,7 @@ FMT_BF16 = 0
 FMT_FP8 = 1
 FMT_FP4 = 2
 FMT_FP8_PAGESPLIT = 3
+FMT_FP4H_PAGESPLIT = 4
 PAGE_ROWS = 64
 WINDOW = 128
 

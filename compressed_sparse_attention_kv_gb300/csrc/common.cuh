@@ -71,6 +71,9 @@ __device__ __forceinline__ RowPtr paged_row(const cskv_paged& c, int req, long l
   if (c.fmt == CSKV_FMT_FP8_E4M3_ROWSCALE_PAGESPLIT) {
     r.data = page + static_cast<long long>(slot) * c.dim;
     r.scale = page + static_cast<long long>(kPageRows) * c.dim + slot * 4;   // one fp32 per row
+  } else if (c.fmt == CSKV_FMT_FP4_E2M1_E8M0_HADAMARD_PAGESPLIT) {
+    r.data = page + static_cast<long long>(slot) * (c.dim / 2);
+    r.scale = page + static_cast<long long>(kPageRows) * (c.dim / 2) + slot * (c.dim / 32);   // e8m0 per 32
   } else {
     r.data = page + static_cast<long long>(slot) * row_bytes;
     r.scale = r.data + (c.fmt == CSKV_FMT_FP8_E4M3_E8M0_B32 ? c.dim
@@ -249,6 +252,25 @@ __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// kind::mxf4 with block scales (e2m1 x e2m1, an e8m0 scale per 32 of K for every row of
+// A and of B, read from TMEM at sfa / sfb; fp32 accumulate): K = 64 per instruction.
+__device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+// Copy of a 32-row x 16-byte block of shared memory (described by `sdesc`) into TMEM at
+// `taddr`, the same rows in each of the four lane quarters: the scale-factor layout of
+// the block-scaled MMA (row r's four 32-bit words = the factors of MMA rows r, r + 32,
+// r + 64 and r + 96, one per column).  Ordered with this thread's MMAs.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
 // Arrive on `bar` once all previously issued MMAs of this thread have completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
@@ -314,6 +336,34 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   d |= static_cast<uint64_t>(1) << 46;
   d |= static_cast<uint64_t>(2) << 61;
   return d;
+}
+
+// Shared-memory descriptor of a K-major operand in the 64-byte swizzle (rows of 64 B,
+// 8-row atoms of 512 B: sbo = 512).
+__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFF);
+  d |= static_cast<uint64_t>(1) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFF) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(4) << 61;
+  return d;
+}
+// Shared-memory descriptor without swizzle: 8-row groups of 16-byte rows, `sbo` apart.
+__device__ __forceinline__ uint64_t smem_desc_plain(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFF);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFF) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFF) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
+// Instruction descriptor of kind::mxf4 (block-scaled): A and B e2m1, K-major, e8m0
+// scale factors, fp32 accumulate, K = 64; sf_id selects the scale factors' byte pair
+// in their TMEM words (0: blocks 0-1 of K, 2: blocks 2-3) for A and B alike.
+__host__ __device__ constexpr uint32_t make_idesc_mxf4(int M, int N, int sf_id) {
+  return (static_cast<uint32_t>(sf_id) << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24) | (static_cast<uint32_t>(sf_id) << 29);
 }
 
 // Instruction descriptor, dense MMA with fp32 accumulator.

@@ -96,9 +96,13 @@ static int32_t cuda_status(cudaError_t e) { return e == cudaSuccess ? CSKV_OK : 
 
 // Checks a paged-cache descriptor for a lane of dimension `dim`; `formats` is a
 // bit mask of the accepted cskv_format values.
+static bool index_key_format(int fmt) {
+  return fmt == CSKV_FMT_FP8_E4M3_ROWSCALE_PAGESPLIT || fmt == CSKV_FMT_FP4_E2M1_E8M0_HADAMARD_PAGESPLIT;
+}
+
 static bool paged_ok(const cskv_paged& c, int dim, unsigned formats) {
   if (c.pool == nullptr || !aligned(c.pool, 16)) return false;
-  if (c.fmt < 0 || c.fmt > 3 || !((formats >> c.fmt) & 1u)) return false;
+  if (c.fmt < 0 || c.fmt > 4 || !((formats >> c.fmt) & 1u)) return false;
   if (c.dim != dim) return false;
   const size_t rb = cskv_row_bytes(c.fmt, c.dim);
   if (rb == 0) return false;
@@ -164,6 +168,7 @@ size_t cskv_row_bytes(int32_t fmt, int32_t dim) {
     case CSKV_FMT_FP8_E4M3_E8M0_B32: return dim + dim / 32;
     case CSKV_FMT_FP8_E4M3_ROWSCALE_PAGESPLIT: return dim + 4;
     case CSKV_FMT_FP4_E2M1_E4M3_B16: return dim / 2 + dim / 16;
+    case CSKV_FMT_FP4_E2M1_E8M0_HADAMARD_PAGESPLIT: return dim == 128 ? dim / 2 + dim / 32 : 0;
     default: return 0;
   }
 }
@@ -244,8 +249,8 @@ int32_t cskv_encode_rows(const void* src, int32_t src_is_bf16, int32_t n, int32_
                          void* stream) {
   if (n < 0 || (dim != 128 && dim != 512)) return CSKV_ERR_INVALID;
   if (n > 0 && (src == nullptr || !aligned(src, 16))) return CSKV_ERR_INVALID;
-  if (!paged_ok(dst, dim, 0xFu)) return CSKV_ERR_INVALID;
-  if (dst.fmt == CSKV_FMT_FP8_E4M3_ROWSCALE_PAGESPLIT && dim != 128) return CSKV_ERR_INVALID;
+  if (!paged_ok(dst, dim, 0x1Fu)) return CSKV_ERR_INVALID;
+  if (index_key_format(dst.fmt) && dim != 128) return CSKV_ERR_INVALID;
   return cuda_status(launch_encode_rows(src, src_is_bf16 != 0, n, dim, dst_req, dst_row, dst,
                                         static_cast<int>(cskv_row_bytes(dst.fmt, dim)),
                                         static_cast<cudaStream_t>(stream)));
@@ -266,8 +271,8 @@ static int32_t compress_check(const void* kv, const void* gate, const void* prev
   if (!aligned(kv, 8) || !aligned(gate, 8) || (ape && !aligned(ape, 16))) return CSKV_ERR_INVALID;
   if (prev_kv && (!aligned(prev_kv, 8) || !aligned(prev_gate, 8))) return CSKV_ERR_INVALID;
   if ((norm_w && !aligned(norm_w, 16)) || (rope_cs && !aligned(rope_cs, 16))) return CSKV_ERR_INVALID;
-  if (!paged_ok(out, dim, 0xFu)) return CSKV_ERR_INVALID;
-  if (out.fmt == CSKV_FMT_FP8_E4M3_ROWSCALE_PAGESPLIT && dim != 128) return CSKV_ERR_INVALID;
+  if (!paged_ok(out, dim, 0x1Fu)) return CSKV_ERR_INVALID;
+  if (index_key_format(out.fmt) && dim != 128) return CSKV_ERR_INVALID;
   return CSKV_OK;
 }
 
@@ -321,8 +326,8 @@ int32_t cskv_decode_append(const cskv_decode_job* jobs, int32_t njobs, const int
     if ((q.ape && !aligned(q.ape, 16)) || (q.norm_w && !aligned(q.norm_w, 16)) ||
         (q.rope_cs && !aligned(q.rope_cs, 16)))
       return CSKV_ERR_INVALID;
-    if (!paged_ok(q.out, q.dim, 0xFu)) return CSKV_ERR_INVALID;
-    if (q.out.fmt == CSKV_FMT_FP8_E4M3_ROWSCALE_PAGESPLIT && q.dim != 128) return CSKV_ERR_INVALID;
+    if (!paged_ok(q.out, q.dim, 0x1Fu)) return CSKV_ERR_INVALID;
+    if (index_key_format(q.out.fmt) && q.dim != 128) return CSKV_ERR_INVALID;
   }
   if (B == 0) return CSKV_OK;
   return cuda_status(launch_decode_append(jobs, njobs, pos, B, static_cast<cudaStream_t>(stream)));
@@ -342,7 +347,8 @@ static int32_t index_check(const void* q_idx, const float* w, const cskv_paged& 
   if (B < 1 || Hi < 1 || ratio < 1 || k < 1 || k > 2048 || max_ctx_len < 0) return CSKV_ERR_INVALID;
   if (Hi > 64) return CSKV_ERR_UNSUPPORTED;
   if (!aligned(q_idx, 16) || !aligned(w, 4)) return CSKV_ERR_INVALID;
-  if (!paged_ok(keys, 128, (1u << CSKV_FMT_BF16) | (1u << CSKV_FMT_FP8_E4M3_ROWSCALE_PAGESPLIT)))
+  if (!paged_ok(keys, 128, (1u << CSKV_FMT_BF16) | (1u << CSKV_FMT_FP8_E4M3_ROWSCALE_PAGESPLIT) |
+                                 (1u << CSKV_FMT_FP4_E2M1_E8M0_HADAMARD_PAGESPLIT)))
     return CSKV_ERR_INVALID;
   if (keys.block_table == nullptr) return CSKV_ERR_INVALID;
   const size_t need = index_workspace_bytes(B, max_ctx_len / ratio, Hi, k);
@@ -372,7 +378,8 @@ int32_t cskv_index_topk_noalloc(const void* q_idx, const float* w, cskv_paged ke
   if (B < 1 || Hi < 1 || ratio < 1 || k < 1 || k > 2048 || max_ctx_len < 0) return CSKV_ERR_INVALID;
   if (Hi > 64) return CSKV_ERR_UNSUPPORTED;
   if (!aligned(q_idx, 16) || !aligned(w, 4)) return CSKV_ERR_INVALID;
-  if (!paged_ok(keys, 128, (1u << CSKV_FMT_BF16) | (1u << CSKV_FMT_FP8_E4M3_ROWSCALE_PAGESPLIT)))
+  if (!paged_ok(keys, 128, (1u << CSKV_FMT_BF16) | (1u << CSKV_FMT_FP8_E4M3_ROWSCALE_PAGESPLIT) |
+                                 (1u << CSKV_FMT_FP4_E2M1_E8M0_HADAMARD_PAGESPLIT)))
     return CSKV_ERR_INVALID;
   if (keys.block_table == nullptr) return CSKV_ERR_INVALID;
   // the whole workspace must fit in the library's fixed scratch array

@@ -59,18 +59,38 @@ constexpr int kProducers = 2;        // TMA-issuing warps, each with its own sta
 constexpr int kGroups = 2;           // epilogue groups of 4 warps (one per TMEM lane quarter)
 constexpr int kStagesFp8 = 4;        // per producer, 16 KiB stages
 constexpr int kStagesBf16 = 2;       // per producer, 32 KiB stages
-constexpr int kAccs = 8;             // TMEM accumulators in flight (8 x 64 columns)
+constexpr int kStagesFp4 = 8;        // per producer, 9 KiB stages
+constexpr int kStagesMax = 8;
+constexpr int kAccsMax = 8;          // TMEM accumulators in flight (8 x 64 columns)
 constexpr int kScaleSlots = 16;      // ring of per-tile scale rows (2 pages x 64 fp32)
-constexpr int kPairSlots = 8;        // tile pairs in flight from the scheduling producer to the other
+constexpr int kRecSlots = 32;        // tile records in flight from the scheduler to the producers
 constexpr int kChunkTiles = 4;       // tiles per grab from a request's work counter
 constexpr int kWarpMma = kProducers;
 constexpr int kWarpEpi = kProducers + 1;
-constexpr int kScoreThreads = 32 * (kProducers + 1 + 4 * kGroups);   // 352
+constexpr int kWarpSched = kWarpEpi + 4 * kGroups;
+constexpr int kScoreThreads = 32 * (kProducers + 1 + 4 * kGroups + 1);   // 384
 // three groups (15 warps) put four warps on a scheduler partition: 128 registers each
 constexpr int kLaunchBound = kGroups >= 3 ? 512 : kScoreThreads;
 constexpr int kCandCap = 4096;       // per-block staging of threshold-bin candidates
 constexpr int kQImageFp8 = 8192;     // e4m3 [64 rows][128 B]
 constexpr int kQImageBf16 = 16384;   // bf16 [2 chunks][64 rows][128 B]
+constexpr int kQImageFp4 = 4608;     // e2m1 [64 rows][64 B], then the heads' scale factors [32][16 B]
+
+// Key formats of the score kernel (its template parameter KF) and what they size.
+constexpr int kKfBf16 = 0, kKfFp8 = 1, kKfFp4 = 2;
+template <int KF>
+struct KeyFmt {
+  // one stage holds a tile of 128 keys: FP4 = 8 KiB of codes, their 512 scale bytes and
+  // the same bytes in the scale-factor copy's layout
+  static constexpr int kStageBytes = KF == kKfFp8 ? kTileRows * 128 : KF == kKfBf16 ? kTileRows * 256 : kTileRows * 64 + 1024;
+  static constexpr int kStages = KF == kKfFp8 ? kStagesFp8 : KF == kKfBf16 ? kStagesBf16 : kStagesFp4;
+  static constexpr int kQImage = KF == kKfFp8 ? kQImageFp8 : KF == kKfBf16 ? kQImageBf16 : kQImageFp4;
+  static constexpr int kQBuf = 2 * kQImage > 16384 ? 2 * kQImage : 16384;   // the selection reuses 16 KiB of it
+  // FP4: six accumulators (384 columns), their keys' scale factors (4 columns each) and
+  // the two query buffers' (4 each) in one 512-column allocation
+  static constexpr int kAccs = KF == kKfFp4 ? 6 : 8;
+};
+constexpr int kSfaCol = 384;         // FP4: first TMEM column of the keys' scale factors
 constexpr int kQSlot = 16384;        // per request in the workspace
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -127,7 +147,7 @@ struct IndexArgs {
   cskv_paged keys;
   const int32_t* ctx_len;
   int B, Hi, N, ratio, k, n_max;
-  int fp8;                   // 1: page-split FP8 keys, 0: bf16 keys
+  int kfmt;                  // key format: 0 bf16, 1 page-split FP8, 2 page-split rotated FP4
   int grid;                  // blocks of the score kernel
   int32_t* topk_idx;
   float* topk_score;
@@ -196,7 +216,23 @@ __global__ void __launch_bounds__(256) index_prep_kernel(const IndexArgs a) {
   for (int i = 0; i < 8; ++i) {
     const int h = warp + 8 * i;
     if (h >= a.N) break;
-    if (a.fp8) {
+    if (a.kfmt == kKfFp4) {
+      // rotated like the keys, then e2m1 with an e8m0 scale per 32 (8 lanes); row h of the
+      // 64-byte swizzled image (16-byte chunk c of row h at chunk c ^ ((h >> 1) & 3)), the
+      // scale bytes in the scale-factor copy's layout after the image (row h % 32, word h / 32)
+      float y[4] = {bf16lo(raw[i].x), bf16hi(raw[i].x), bf16lo(raw[i].y), bf16hi(raw[i].y)};
+      hadamard128_x4(y, lane);
+      float am = fmaxf(fmaxf(fabsf(y[0]), fabsf(y[1])), fmaxf(fabsf(y[2]), fabsf(y[3])));
+      am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
+      am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
+      am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 4));
+      const int e = e8m0_exponent_fp4(am);
+      const uint32_t codes = e2m1x4_scaled(y, e);
+      *reinterpret_cast<uint16_t*>(img + h * 64 + ((((lane >> 3) ^ ((h >> 1) & 3))) << 4) + ((2 * lane) & 15)) =
+          static_cast<uint16_t>(codes);
+      if ((lane & 7) == 0) img[4096 + 16 * (h & 31) + 4 * (h >> 5) + (lane >> 3)] = static_cast<uint8_t>(e + 127);
+      if (lane == 0) wq[h] = wv[i];
+    } else if (a.kfmt == kKfFp8) {
       const float4 v = make_float4(bf16lo(raw[i].x), bf16hi(raw[i].x), bf16lo(raw[i].y), bf16hi(raw[i].y));
       float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
 #pragma unroll
@@ -258,14 +294,14 @@ struct WorkItem {
 constexpr int kWorkItems = 16;
 
 struct ScoreSmem {
-  uint64_t full[kProducers][kStagesFp8], empty[kProducers][kStagesFp8];
-  uint64_t accfull[kAccs], accempty[kAccs];
+  uint64_t full[kProducers][kStagesMax], empty[kProducers][kStagesMax];
+  uint64_t accfull[kAccsMax], accempty[kAccsMax];
   uint64_t qfull[2], qempty[2];
   uint64_t sfull[kScaleSlots], sempty[kScaleSlots];
-  uint64_t pfull[kPairSlots], pempty[kPairSlots];   // tile pairs handed from producer 0 to 1
+  uint64_t rfull[kRecSlots], rempty[kRecSlots];     // tile records from the scheduler
   uint64_t drain;
   uint64_t hbar[kGroups];          // an epilogue group's warps meet here at a request switch
-  int4 pair[kPairSlots];           // (request, tile, page id, page id) handed to producer 1; request -1 = the end
+  int4 rec[kRecSlots];             // (request, tile, page id, page id) of local tile i at i % kRecSlots; request -1 = the end
   int2 tinfo[kScaleSlots];         // (request, tile) of each tile in flight; request -1 = the end
   uint32_t tmem_base;
   volatile int abort;
@@ -535,16 +571,14 @@ struct ScoreCarve {
   uint16_t* scratch;   // kScratch16
   ScoreSmem* sm;
 };
-template <int FP8>
+template <int KF>
 __device__ __forceinline__ ScoreCarve score_carve() {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  constexpr int kStageBytes = FP8 ? kTileRows * 128 : kTileRows * 256;
-  constexpr int kStages = FP8 ? kStagesFp8 : kStagesBf16;   // per producer
-  constexpr int kQImage = FP8 ? kQImageFp8 : kQImageBf16;
+  using F = KeyFmt<KF>;
   ScoreCarve c;
   c.stages = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  c.qbuf = c.stages + kProducers * kStages * kStageBytes;
-  c.hist = reinterpret_cast<uint32_t*>(c.qbuf + 2 * kQImage);
+  c.qbuf = c.stages + kProducers * F::kStages * F::kStageBytes;
+  c.hist = reinterpret_cast<uint32_t*>(c.qbuf + F::kQBuf);
   c.sring = reinterpret_cast<float*>(c.hist + kGroups * kHistBins);
   c.scratch = reinterpret_cast<uint16_t*>(c.sring + kScaleSlots * kTileRows);
   c.sm = reinterpret_cast<ScoreSmem*>(c.scratch + kScratch16);
@@ -750,9 +784,9 @@ __device__ __forceinline__ void cut_and_write(const IndexArgs& a, ScoreSmem* sm,
 //    are read again, in rounds, and the candidates may spill to the workspace;
 //  - cut_and_write: the exact cut in bin T and the k entries in entry order.
 // It runs once per request from a cold instruction cache: loops stay rolled.
-template <int FP8>
+template <int KF>
 __device__ __noinline__ void select_completed(const IndexArgs& a) {
-  const ScoreCarve cv = score_carve<FP8>();
+  const ScoreCarve cv = score_carve<KF>();
   ScoreSmem* sm = cv.sm;
   uint8_t* stages = cv.stages;
   uint8_t* qbuf = cv.qbuf;
@@ -863,7 +897,8 @@ __device__ __noinline__ void select_completed(const IndexArgs& a) {
     // multi = both (rare): the owner lists the segment and copies its 32 scores into
     // shared memory (up to kMulti in the block); a warp per listed segment counts and
     // writes its entries (a lane per entry).
-    constexpr int kOwn = (kMetaSegs + kScoreThreads - 1) / kScoreThreads;
+    constexpr int kGrp = 8;   // shared-memory loads issued together in the passes below
+    constexpr int kOwn = ((kMetaSegs + kScoreThreads - 1) / kScoreThreads + kGrp - 1) / kGrp * kGrp;
     static_assert(kOwn <= 32, "a thread's segments fit a 32-bit mask");
     const bool fast = meta_fits && nexp <= static_cast<uint32_t>(kSelCand);
     if (fast) {
@@ -880,7 +915,6 @@ __device__ __noinline__ void select_completed(const IndexArgs& a) {
       __syncthreads();
       // The loops below issue their shared-memory loads in groups of eight before any use
       // (the latency of one load, not of eight, per group).
-      constexpr int kGrp = 8;
       static_assert(kOwn % kGrp == 0, "whole groups");
       uint32_t smask = 0, mmask = 0;   // bit i: segment q0 + i is single / multi
 #pragma unroll 1
@@ -1170,13 +1204,20 @@ __device__ __noinline__ void select_completed(const IndexArgs& a) {
 // prefill): the scheduler also counts the tiles handed out, so that a block that finds
 // its requests exhausted stops as soon as every tile has an owner instead of visiting
 // every request (one atomic each) before it concludes there is no work left.
-template <int FP8, bool LARGE>
+template <int KF, bool LARGE>
 __global__ void __launch_bounds__(kLaunchBound, 1)
     index_score_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ IndexArgs a) {
-  constexpr int kStageBytes = FP8 ? kTileRows * 128 : kTileRows * 256;
-  constexpr int kStages = FP8 ? kStagesFp8 : kStagesBf16;   // per producer
-  constexpr int kQImage = FP8 ? kQImageFp8 : kQImageBf16;
-  const ScoreCarve cv = score_carve<FP8>();
+  constexpr int kStageBytes = KeyFmt<KF>::kStageBytes;
+  constexpr int kStages = KeyFmt<KF>::kStages;   // per producer
+  constexpr int kQImage = KeyFmt<KF>::kQImage;
+  constexpr int kAccs = KeyFmt<KF>::kAccs;
+  constexpr bool FP8 = KF == kKfFp8;
+  constexpr bool FP4 = KF == kKfFp4;
+  // With as many accumulators as stages (FP8), tile i's stage and accumulator are
+  // released by the same event - its MMAs completing - so the MMA warp commits once per
+  // tile (to accfull[i % kAccs]) and the producers wait on that barrier for the stage.
+  constexpr bool kMerged = kAccs == kProducers * kStages;
+  const ScoreCarve cv = score_carve<KF>();
   uint8_t* stages = cv.stages;
   uint8_t* qbuf = cv.qbuf;
   uint32_t* hist = cv.hist;
@@ -1220,7 +1261,7 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
     for (int c = 0; c < kAccs; ++c) { mbar_init(&sm->accfull[c], 1); mbar_init(&sm->accempty[c], 4); }
     for (int c = 0; c < 2; ++c) { mbar_init(&sm->qfull[c], 1); mbar_init(&sm->qempty[c], 1); }
     for (int s = 0; s < kScaleSlots; ++s) { mbar_init(&sm->sfull[s], 1); mbar_init(&sm->sempty[s], 4); }
-    for (int s = 0; s < kPairSlots; ++s) { mbar_init(&sm->pfull[s], 1); mbar_init(&sm->pempty[s], 1); }
+    for (int s = 0; s < kRecSlots; ++s) { mbar_init(&sm->rfull[s], 1); mbar_init(&sm->rempty[s], 1); }
     mbar_init(&sm->drain, 1);
     for (int g = 0; g < kGroups; ++g) mbar_init(&sm->hbar[g], 4);
     sm->abort = 0;
@@ -1229,6 +1270,7 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
   for (int i = threadIdx.x; i < kGroups * kHistBins; i += blockDim.x) hist[i] = 0;
   uint32_t ncols = 32;
   while (ncols < static_cast<uint32_t>(kAccs * N)) ncols <<= 1;
+  if (FP4) ncols = 512;   // the scale factors sit above the accumulators
   if (warp == kWarpMma) tmem_alloc(&sm->tmem_base, ncols);
   tc_fence_before();
   __syncthreads();
@@ -1239,7 +1281,7 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
   // thread reads what they write (keys, query images, weights, counters) before
   // this wait.  The scheduling producer first requests its first chunk's page ids
   // (block tables are inputs) and waits after that.
-  const bool sched_thread = warp == 0 && lane == 0;
+  const bool sched_thread = warp == kWarpSched && lane == 0;
   // Streaming mode reads its predecessor's output (query images, counters) only after
   // waiting for it, unless that predecessor is the compressor of a fused step (the
   // prep before it has completed; only tiles with fresh keys wait, below).
@@ -1314,12 +1356,14 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
 
   // ======================================================= phase 1: scores
   // Tiles are handed out dynamically, in chunks of kChunkTiles consecutive tiles of
-  // one request: producer 0 grabs a chunk from the request's counter (starting at a
-  // home request spread over the grid, moving on when it is exhausted), keeps the
-  // even tiles and hands the odd ones to producer 1.  Block-local tile i goes through producer i % 2
-  // (stage (i / 2) % kStages of its ring), accumulator i % 8, epilogue group i % 2
-  // and slot i % 16 of the scale and tile-info rings.  A tile past the end of its
-  // request is a hole (no pages, no entries); request -1 ends the sequence.
+  // one request: the scheduler warp grabs a chunk from the request's counter (starting
+  // at a home request spread over the grid, moving on when it is exhausted), loads its
+  // page ids and writes one record per tile of the request into a ring that runs up to
+  // kRecSlots tiles ahead of the copies, so that neither its atomics nor its
+  // block-table loads hold up a tile.  Block-local tile i goes through producer i % 2
+  // (stage (i / 2) % kStages of its ring), accumulator i % kAccs, epilogue group i % 2
+  // and slot i % 16 of the scale and tile-info rings; request -1 ends the sequence
+  // (one end record per producer).
   if (warp < kProducers) {
     // ------------------------------------------------------------ producers
     const int pw = warp;
@@ -1329,14 +1373,14 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
       // segment maxima and histograms that the selection reads back out of L2
       const uint64_t pol = l2_evict_first();
       long long np = 0;       // tiles this producer posted (the end marker included)
-      int nreq = 0;           // query images loaded (producer 0)
       bool waited = wait_at_start;   // this thread has seen the kernel before complete
       // post local tile i = (request b, tile t) with its two page ids (-2: no page,
       // -3: page outside the block table); b < 0 posts the end marker
       auto post = [&](long long i, int b, int t, int id0, int id1) -> bool {
         const int s = static_cast<int>(np % kStages);
         const long long round = np / kStages;
-        if (round > 0 && !role_wait(sm, &sm->empty[pw][s], (round - 1) & 1, a.spin)) return false;
+        if (round > 0 && !role_wait(sm, kMerged ? &sm->accfull[i % kAccs] : &sm->empty[pw][s], (round - 1) & 1, a.spin))
+          return false;
         const int ss = static_cast<int>(i % kScaleSlots);
         const long long su = i / kScaleSlots;
         if (su > 0 && !role_wait(sm, &sm->sempty[ss], (su - 1) & 1, a.spin)) return false;
@@ -1358,7 +1402,7 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
             pages[pg] = -2;
             continue;
           }
-          bytes += FP8 ? 64 * 128 : 64 * 256;
+          bytes += FP8 ? 64 * 128 : FP4 ? 64 * 64 + 256 : 64 * 256;
         }
         sm->tinfo[ss] = make_int2(b, t);
         sm->smask[ss] = (pages[0] >= 0 ? 1 : 0) | (pages[1] >= 0 ? 2 : 0);
@@ -1366,6 +1410,13 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
         mbar_expect_tx(&sm->sfull[ss], FP8 ? (pages[0] >= 0 ? 256u : 0u) + (pages[1] >= 0 ? 256u : 0u) : 0u);
         for (int pg = 0; pg < 2; ++pg) {
           if (pages[pg] < 0) continue;
+          if (FP4) {
+            // the page's 64 code rows (64-byte swizzle) and its 64 rows of 4 scale bytes
+            const uint8_t* pgp = static_cast<const uint8_t*>(a.keys.pool) + size_t(pages[pg]) * a.keys.page_bytes;
+            tma_load_3d_hint(dst + pg * 4096, &tmap, 0, 0, pages[pg], &sm->full[pw][s], pol);
+            bulk_g2s_hint(dst + 8192 + pg * 256, pgp + kPageRows * 64, 256, &sm->full[pw][s], pol);
+            continue;
+          }
           tma_load_3d_hint(dst + pg * 8192, &tmap, 0, 0, pages[pg], &sm->full[pw][s], pol);
           if (!FP8) tma_load_3d_hint(dst + 16384 + pg * 8192, &tmap, 64, 0, pages[pg], &sm->full[pw][s], pol);
           if (FP8) {
@@ -1377,130 +1428,12 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
         ++np;
         return true;
       };
-      if (pw == 0) {
-        // Scheduler.  Work comes in chunks of kChunkTiles consecutive tiles of one
-        // request, grabbed from the request's counter; the chunks after next are
-        // grabbed, and the next chunk's page ids loaded, while the current one is
-        // posted, so neither the atomics nor the block-table loads stall the stream.
-        auto tiles_of = [&](int b) { return (nvis(b) + kTileRows - 1) / kTileRows; };
-        // the chunk's 2 x kChunkTiles page ids, all loads in flight
-        auto chunk_ids = [&](int b, int t0, int (&ids)[2 * kChunkTiles]) {
-          const int n_b = b >= 0 ? nvis(b) : 0;
-          const int32_t* bt = a.keys.block_table + static_cast<long long>(b < 0 ? 0 : b) * a.keys.max_pages;
-#pragma unroll
-          for (int u = 0; u < 2 * kChunkTiles; ++u) {
-            const long long lp = static_cast<long long>(t0) * 2 + u;
-            ids[u] = (b < 0 || lp * kPageRows >= n_b) ? -2 : (lp >= a.keys.max_pages ? -3 : bt[lp]);
-          }
-        };
-        int req = home_request(blockIdx.x, a.B, gridDim.x);
-        uint32_t pending = 0;
-        // streaming mode keeps a second grab of the same request in flight, so that an
-        // atomic has two chunks' time to return before its result is needed
-        constexpr uint32_t kNoGrab = 0xFFFFFFFFu;
-        uint32_t pending2 = kNoGrab;
-        auto grab = [&]() { return atomicAdd(&ctr_all[req * 4], static_cast<uint32_t>(kChunkTiles)); };
-        uint32_t* handed = gbar + 1;   // LARGE: tiles handed out so far (cleared by the prep)
-        // the next chunk: (request, first tile) from the pending grab; request -1 = none left
-        auto resolve = [&](int& b, int& t0) {
-          int tiles = tiles_of(req);
-          int fails = 0;
-          uint32_t seen = 0;   // LARGE: the handed-out count read during the previous step
-          while (pending >= static_cast<uint32_t>(tiles) && ++fails < a.B) {
-            if constexpr (LARGE) {
-              if (seen >= static_cast<uint32_t>(total)) break;
-            }
-            req = (req + 1) % a.B;
-            tiles = tiles_of(req);
-            if constexpr (LARGE) seen = *reinterpret_cast<volatile uint32_t*>(handed);
-            pending = grab();
-            pending2 = kNoGrab;
-          }
-          if (pending >= static_cast<uint32_t>(tiles)) {
-            b = -1;
-            t0 = 0;
-          } else {
-            b = req;
-            t0 = static_cast<int>(pending);
-            if constexpr (LARGE) {
-              atomicAdd(handed, static_cast<uint32_t>(min(kChunkTiles, tiles - t0)));
-              pending = grab();
-            } else {
-              pending = pending2 != kNoGrab ? pending2 : grab();
-              pending2 = grab();
-            }
-          }
-        };
-        int cb = -1, ct = 0;
-        int ids[2 * kChunkTiles];
-        const int r0 = blockIdx.x - first_home_block(req, a.B, gridDim.x);
-        const bool static_first = static_cast<long long>(r0) * kChunkTiles < tiles_of(req);
-        if (static_first) {
-          cb = req;   // the block's first chunk, assigned without an atomic
-          ct = r0 * kChunkTiles;
-          chunk_ids(cb, ct, ids);
-        }
-        if (wait_at_start) grid_dep_wait();
-        if constexpr (LARGE) {
-          if (static_first) atomicAdd(handed, static_cast<uint32_t>(min(kChunkTiles, tiles_of(cb) - ct)));
-        }
-        pending = atomicAdd(&ctr_all[req * 4], static_cast<uint32_t>(kChunkTiles));
-        if (!static_first) {
-          resolve(cb, ct);
-          chunk_ids(cb, ct, ids);
-        }
-        int q_b = -1;
-        long long m = 0;   // pairs posted
-        bool ok = true;
-        while (ok) {
-          if (cb >= 0 && cb != q_b) {
-            // query image of the new request into buffer nreq % 2
-            const int qb = nreq & 1;
-            if (nreq >= 2 && !role_wait(sm, &sm->qempty[qb], ((nreq >> 1) - 1) & 1, a.spin)) break;
-            mbar_expect_tx(&sm->qfull[qb], kQImage);
-            bulk_g2s(qbuf + qb * kQImage, a.ws + a.L.qimg + size_t(cb) * kQSlot, kQImage, &sm->qfull[qb]);
-            ++nreq;
-            q_b = cb;
-          }
-          // the next chunk is resolved and its page ids requested first (they have the
-          // whole chunk's time to arrive); then the chunk's pairs: the first tile here,
-          // the second handed to producer 1
-          int nb2 = -1, nt = 0;
-          int nids[2 * kChunkTiles];
-          if (cb >= 0) {
-            resolve(nb2, nt);   // usually already returned: grabbed two chunks ago
-            chunk_ids(nb2, nt, nids);
-          }
-#pragma unroll
-          for (int pr = 0; pr < kChunkTiles / 2; ++pr, ++m) {
-            if (pr > 0 && cb < 0) break;   // the end marker is one pair
-            const int hs = static_cast<int>(m % kPairSlots);
-            if (m >= kPairSlots && !role_wait(sm, &sm->pempty[hs], ((m / kPairSlots) - 1) & 1, a.spin)) {
-              ok = false;
-              break;
-            }
-            const int t = ct + 2 * pr;
-            sm->pair[hs] = make_int4(cb, t + 1, ids[4 * pr + 2], ids[4 * pr + 3]);
-            mbar_arrive(&sm->pfull[hs]);
-            if (!post(2 * m, cb, t, ids[4 * pr], ids[4 * pr + 1])) {
-              ok = false;
-              break;
-            }
-          }
-          if (cb < 0 || !ok) break;
-          cb = nb2;
-          ct = nt;
-#pragma unroll
-          for (int u = 0; u < 2 * kChunkTiles; ++u) ids[u] = nids[u];
-        }
-      } else {
-        for (long long m = 0;; ++m) {
-          const int hs = static_cast<int>(m % kPairSlots);
-          if (!role_wait(sm, &sm->pfull[hs], (m / kPairSlots) & 1, a.spin)) break;
-          const int4 pr = sm->pair[hs];
-          mbar_arrive(&sm->pempty[hs]);
-          if (!post(2 * m + 1, pr.x, pr.y, pr.z, pr.w) || pr.x < 0) break;
-        }
+      for (long long i = pw;; i += kProducers) {
+        const int rs = static_cast<int>(i % kRecSlots);
+        if (!role_wait(sm, &sm->rfull[rs], (i / kRecSlots) & 1, a.spin)) break;
+        const int4 r = sm->rec[rs];
+        mbar_arrive(&sm->rempty[rs]);
+        if (!post(i, r.x, r.y, r.z, r.w) || r.x < 0) break;
       }
       // drain: every copy this producer issued must land before the block moves on
       for (int s = 0; s < kStages && s < np; ++s) {
@@ -1511,6 +1444,120 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
         const long long uses = (np - r + kScaleSlots / 2 - 1) / (kScaleSlots / 2);
         mbar_wait(&sm->sfull[2 * r + pw], (uses - 1) & 1, kDefaultSpinLimit);
       }
+    }
+  } else if (warp == kWarpSched) {
+    // ------------------------------------------------------------ scheduler
+    if (lane == 0) {
+      int nreq = 0;   // query images loaded
+      auto tiles_of = [&](int b) { return (nvis(b) + kTileRows - 1) / kTileRows; };
+      // the chunk's 2 x kChunkTiles page ids, all loads in flight
+      auto chunk_ids = [&](int b, int t0, int (&ids)[2 * kChunkTiles]) {
+        const int n_b = b >= 0 ? nvis(b) : 0;
+        const int32_t* bt = a.keys.block_table + static_cast<long long>(b < 0 ? 0 : b) * a.keys.max_pages;
+#pragma unroll
+        for (int u = 0; u < 2 * kChunkTiles; ++u) {
+          const long long lp = static_cast<long long>(t0) * 2 + u;
+          ids[u] = (b < 0 || lp * kPageRows >= n_b) ? -2 : (lp >= a.keys.max_pages ? -3 : bt[lp]);
+        }
+      };
+      int req = home_request(blockIdx.x, a.B, gridDim.x);
+      uint32_t pending = 0;
+      // streaming mode keeps a second grab of the same request in flight
+      constexpr uint32_t kNoGrab = 0xFFFFFFFFu;
+      uint32_t pending2 = kNoGrab;
+      auto grab = [&]() { return atomicAdd(&ctr_all[req * 4], static_cast<uint32_t>(kChunkTiles)); };
+      uint32_t* handed = gbar + 1;   // LARGE: tiles handed out so far (cleared by the prep)
+      // the next chunk: (request, first tile) from the pending grab; request -1 = none left
+      auto resolve = [&](int& b, int& t0) {
+        int tiles = tiles_of(req);
+        int fails = 0;
+        uint32_t seen = 0;   // LARGE: the handed-out count read during the previous step
+        while (pending >= static_cast<uint32_t>(tiles) && ++fails < a.B) {
+          if constexpr (LARGE) {
+            if (seen >= static_cast<uint32_t>(total)) break;
+          }
+          req = (req + 1) % a.B;
+          tiles = tiles_of(req);
+          if constexpr (LARGE) seen = *reinterpret_cast<volatile uint32_t*>(handed);
+          pending = grab();
+          pending2 = kNoGrab;
+        }
+        if (pending >= static_cast<uint32_t>(tiles)) {
+          b = -1;
+          t0 = 0;
+        } else {
+          b = req;
+          t0 = static_cast<int>(pending);
+          if constexpr (LARGE) {
+            atomicAdd(handed, static_cast<uint32_t>(min(kChunkTiles, tiles - t0)));
+            pending = grab();
+          } else {
+            pending = pending2 != kNoGrab ? pending2 : grab();
+            pending2 = grab();
+          }
+        }
+      };
+      // record of local tile i (waits for its slot to be free)
+      auto emit = [&](long long i, int b, int t, int id0, int id1) -> bool {
+        const int rs = static_cast<int>(i % kRecSlots);
+        const long long u = i / kRecSlots;
+        if (u > 0 && !role_wait(sm, &sm->rempty[rs], (u - 1) & 1, a.spin)) return false;
+        sm->rec[rs] = make_int4(b, t, id0, id1);
+        mbar_arrive(&sm->rfull[rs]);
+        return true;
+      };
+      int cb = -1, ct = 0;
+      int ids[2 * kChunkTiles];
+      const int r0 = blockIdx.x - first_home_block(req, a.B, gridDim.x);
+      const bool static_first = static_cast<long long>(r0) * kChunkTiles < tiles_of(req);
+      if (static_first) {
+        cb = req;   // the block's first chunk, assigned without an atomic
+        ct = r0 * kChunkTiles;
+        chunk_ids(cb, ct, ids);
+      }
+      if (wait_at_start) grid_dep_wait();
+      if constexpr (LARGE) {
+        if (static_first) atomicAdd(handed, static_cast<uint32_t>(min(kChunkTiles, tiles_of(cb) - ct)));
+      }
+      pending = grab();
+      if (!static_first) {
+        resolve(cb, ct);
+        chunk_ids(cb, ct, ids);
+      }
+      int q_b = -1;
+      long long i = 0;   // records written
+      bool ok = true;
+      while (ok && cb >= 0) {
+        if (cb != q_b) {
+          // query image of the new request into buffer nreq % 2
+          const int qb = nreq & 1;
+          if (nreq >= 2 && !role_wait(sm, &sm->qempty[qb], ((nreq >> 1) - 1) & 1, a.spin)) break;
+          mbar_expect_tx(&sm->qfull[qb], kQImage);
+          bulk_g2s(qbuf + qb * kQImage, a.ws + a.L.qimg + size_t(cb) * kQSlot, kQImage, &sm->qfull[qb]);
+          ++nreq;
+          q_b = cb;
+        }
+        // the next chunk is resolved and its page ids requested before this one's records
+        int nb2 = -1, nt = 0;
+        int nids[2 * kChunkTiles];
+        resolve(nb2, nt);
+        chunk_ids(nb2, nt, nids);
+        const int tiles = tiles_of(cb);
+#pragma unroll
+        for (int u = 0; u < kChunkTiles; ++u) {
+          if (ct + u < tiles && !emit(i++, cb, ct + u, ids[2 * u], ids[2 * u + 1])) {
+            ok = false;
+            break;
+          }
+        }
+        cb = nb2;
+        ct = nt;
+#pragma unroll
+        for (int u = 0; u < 2 * kChunkTiles; ++u) ids[u] = nids[u];
+      }
+      // one end record per producer
+      if (ok) ok = emit(i, -1, 0, -2, -2);
+      if (ok) emit(i + 1, -1, 0, -2, -2);
       for (int qb = 0; qb < 2 && qb < nreq; ++qb) {
         const int uses = (nreq - qb + 1) / 2;
         mbar_wait(&sm->qfull[qb], (uses - 1) & 1, kDefaultSpinLimit);
@@ -1518,7 +1565,63 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if constexpr (FP4) {
+      // The whole warp: per tile it first lays the keys' scale bytes out for the
+      // scale-factor copy (lane r: the words of keys r, r + 32, r + 64, r + 96), then
+      // lane 0 copies them to TMEM and issues the two K = 64 block-scaled MMAs.
+      const uint32_t id0 = make_idesc_mxf4(128, 0, 0) | (static_cast<uint32_t>(N >> 3) << 17);
+      const uint32_t id1 = make_idesc_mxf4(128, 0, 2) | (static_cast<uint32_t>(N >> 3) << 17);
+      int nreq = 0, qb = 0, cur = -1;
+      for (long long i = 0;; ++i) {
+        const int pw = static_cast<int>(i & 1);
+        const long long ip = i >> 1;
+        const int s = static_cast<int>(ip % kStages);
+        // every lane waits (each reads the landed bytes); a give-up is taken by all
+        if (!__all_sync(0xFFFFFFFFu, role_wait(sm, &sm->full[pw][s], (ip / kStages) & 1, a.spin))) break;
+        const int2 ti = sm->tinfo[i % kScaleSlots];
+        if (ti.x < 0) break;
+        uint8_t* st = stages + (pw * kStages + s) * kStageBytes;
+        {
+          const uint32_t* raw = reinterpret_cast<const uint32_t*>(st + 8192);
+          const uint4 v = make_uint4(raw[lane], raw[lane + 32], raw[lane + 64], raw[lane + 96]);
+          *reinterpret_cast<uint4*>(st + 8704 + 16 * lane) = v;
+        }
+        fence_proxy_async_smem();   // generic-proxy writes, before the copy reads them
+        __syncwarp();
+        const bool sw = ti.x != cur;
+        if (sw) {
+          if (cur >= 0 && lane == 0) mma_commit(&sm->qempty[qb]);
+          qb = nreq & 1;
+          if (!__all_sync(0xFFFFFFFFu, role_wait(sm, &sm->qfull[qb], (nreq >> 1) & 1, a.spin))) break;
+          ++nreq;
+          cur = ti.x;
+        }
+        const int c = static_cast<int>(i % kAccs);
+        const long long use = i / kAccs;
+        if (use > 0 && !__all_sync(0xFFFFFFFFu, role_wait(sm, &sm->accempty[c], (use - 1) & 1, a.spin))) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t a_addr = smem_u32(st);
+          const uint32_t b_addr = smem_u32(qbuf + qb * kQImage);
+          const uint32_t sfa = tmem + kSfaCol + 4 * c;
+          const uint32_t sfb = tmem + kSfaCol + 4 * kAccs + 4 * qb;
+          if (sw) tmem_cp_32x128b_x4(sfb, smem_desc_plain(b_addr + 4096, 16, 128));
+          tmem_cp_32x128b_x4(sfa, smem_desc_plain(smem_u32(st + 8704), 16, 128));
+          const uint32_t d = tmem + c * N;
+          const uint64_t da = smem_desc_sw64(a_addr, 512), db = smem_desc_sw64(b_addr, 512);
+          mma_mxf4(d, da, db, id0, sfa, sfb, 0);
+          mma_mxf4(d, da + 2, db + 2, id1, sfa, sfb, 1);   // K step of 32 bytes
+          mma_commit(&sm->empty[pw][s]);
+          mma_commit(&sm->accfull[c]);
+        }
+        __syncwarp();
+      }
+      if (lane == 0) {
+        // drain: all issued MMAs complete before TMEM is released
+        mma_commit(&sm->drain);
+        mbar_wait(&sm->drain, 0, kDefaultSpinLimit);
+      }
+    } else if (lane == 0) {
       constexpr uint32_t idesc = FP8 ? make_idesc(0, 0, 0, 0, 128, 0) : make_idesc(1, 1, 0, 0, 128, 0);
       const uint32_t id = idesc | (static_cast<uint32_t>(N >> 3) << 17);
       int nreq = 0, qb = 0, cur = -1;
@@ -1543,21 +1646,20 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
         const uint32_t a_addr = smem_u32(stages + (pw * kStages + s) * kStageBytes);
         const uint32_t b_addr = smem_u32(qbuf + qb * kQImage);
         const uint32_t d = tmem + c * N;
+        // the descriptors' start-address field counts 16-byte units: a 32-byte K step
+        // within the swizzle atom adds 2 (the fields never carry: shared memory < 256 KiB)
+        const uint64_t da = smem_desc_sw128(a_addr, 16, 1024), db = smem_desc_sw128(b_addr, 16, 1024);
         if (FP8) {
 #pragma unroll
-          for (int kb = 0; kb < 4; ++kb) {
-            mma_f8(d, smem_desc_sw128(a_addr + kb * 32, 16, 1024), smem_desc_sw128(b_addr + kb * 32, 16, 1024),
-                   id, kb > 0);
-          }
+          for (int kb = 0; kb < 4; ++kb) mma_f8(d, da + 2 * kb, db + 2 * kb, id, kb > 0);
         } else {
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            const int ch = kk >> 2, o = (kk & 3) * 32;
-            mma_f16(d, smem_desc_sw128(a_addr + ch * 16384 + o, 16, 1024),
-                    smem_desc_sw128(b_addr + ch * (N * 128) + o, 16, 1024), id, kk > 0);
+            const int ch = kk >> 2, o = (kk & 3) * 2;
+            mma_f16(d, da + ch * (16384 >> 4) + o, db + ch * ((N * 128) >> 4) + o, id, kk > 0);
           }
         }
-        mma_commit(&sm->empty[pw][s]);
+        if (!kMerged) mma_commit(&sm->empty[pw][s]);
         mma_commit(&sm->accfull[c]);
       }
       // drain: all issued MMAs complete before TMEM is released
@@ -1637,7 +1739,7 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
       if (!role_wait(sm, &sm->sfull[ss], (i / kScaleSlots) & 1, a.spin)) break;
       const int2 ti = sm->tinfo[ss];
       const int pmask = sm->smask[ss];
-      const float ks = FP8 ? sring[ss * kTileRows + row] : 1.0f;
+      const float ks = FP8 ? sring[ss * kTileRows + row] : 1.0f;   // FP4: inside the MMA
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm->sempty[ss]);   // one arrival per warp
       if (ti.x < 0) break;
@@ -1706,7 +1808,9 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
           }
         }
       }
-      const float I = ((s0 + s1) + (s2 + s3)) * ks;   // the key's scale is a positive power of two
+      float I = ((s0 + s1) + (s2 + s3)) * ks;   // the key's scale is a positive power of two
+      // FP4 index keys keep their scores in bf16 ("DeepSeek-V4.1 Flash", section 10.4)
+      if (FP4) I = __bfloat162float(__float2bfloat16_rn(I));
       const uint32_t key = valid ? order_key(I) : 0u;
       if (valid) {
         scores_all[size_t(cur_b) * a.L.n_pad + j] = I;
@@ -1747,7 +1851,7 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
     // plain call: this block reads no more query images; once every block is past its
     // stream, the next kernel may start (a following prep waits before clearing)
     if (!a.wait_fresh) grid_dep_launch();
-    select_completed<FP8>(a);
+    select_completed<KF>(a);
     if (a.wait_fresh && threadIdx.x == 0) grid_dep_wait();   // complete only after the compressor
     return;
   }
@@ -2258,27 +2362,27 @@ int sm_count() {
   return n > 0 ? n : 1;
 }
 
-template <int FP8>
+template <int KF>
 size_t score_smem_bytes() {
-  constexpr int kStageBytes = FP8 ? kTileRows * 128 : kTileRows * 256;
-  constexpr int kStages = FP8 ? kStagesFp8 : kStagesBf16;
-  constexpr int kQImage = FP8 ? kQImageFp8 : kQImageBf16;
-  static_assert(kSelSegs * 2 <= 2 * kQImageFp8, "the hit list reuses the query images");
+  using F = KeyFmt<KF>;
+  static_assert(kSelSegs * 2 <= F::kQBuf, "the hit list reuses the query images");
   static_assert(kCandCap * 8 <= kGroups * kHistBins * 4, "the candidates reuse the histograms");
-  return 1024 + kProducers * kStages * kStageBytes + 2 * kQImage + kGroups * kHistBins * 4 +
+  static_assert(kProducers * F::kStages * F::kStageBytes >= kMetaSegs * 8 + kSelCand * 8,
+                "the selection's metadata and candidates reuse the stage ring");
+  return 1024 + kProducers * F::kStages * F::kStageBytes + F::kQBuf + kGroups * kHistBins * 4 +
          kScaleSlots * kTileRows * 4 + kScratch16 * 2 + sizeof(ScoreSmem);
 }
 
 // Cooperative launch of the score kernel: the selection phases meet at grid
 // barriers, so the grid is the number of blocks that fit on the GPU at once.
-template <int FP8, bool LARGE>
+template <int KF, bool LARGE>
 cudaError_t launch_score(const CUtensorMap& tmap, const IndexArgs& a, cudaStream_t stream) {
-  const size_t smem = score_smem_bytes<FP8>();
-  cudaError_t e = cudaFuncSetAttribute(index_score_kernel<FP8, LARGE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const size_t smem = score_smem_bytes<KF>();
+  cudaError_t e = cudaFuncSetAttribute(index_score_kernel<KF, LARGE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, index_score_kernel<FP8, LARGE>, kScoreThreads, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, index_score_kernel<KF, LARGE>, kScoreThreads, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   // one block per SM: it allocates all 512 TMEM columns and most of shared memory
@@ -2296,7 +2400,7 @@ cudaError_t launch_score(const CUtensorMap& tmap, const IndexArgs& a, cudaStream
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, index_score_kernel<FP8, LARGE>, tmap, a);
+    return cudaLaunchKernelEx(&cfg, index_score_kernel<KF, LARGE>, tmap, a);
   }
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
@@ -2316,7 +2420,7 @@ cudaError_t launch_score(const CUtensorMap& tmap, const IndexArgs& a, cudaStream
   }
   if (ok != 0) {
     cfg.numAttrs = 2;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, index_score_kernel<FP8, LARGE>, tmap, a);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, index_score_kernel<KF, LARGE>, tmap, a);
     if (e == cudaSuccess) {
       pdl_ok.store(1, std::memory_order_relaxed);
       return e;
@@ -2326,7 +2430,7 @@ cudaError_t launch_score(const CUtensorMap& tmap, const IndexArgs& a, cudaStream
     pdl_ok.store(0, std::memory_order_relaxed);
   }
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, index_score_kernel<FP8, LARGE>, tmap, a);
+  return cudaLaunchKernelEx(&cfg, index_score_kernel<KF, LARGE>, tmap, a);
 }
 
 }  // namespace
@@ -2358,7 +2462,9 @@ cudaError_t index_setup(IndexLaunch& L, const void* q_idx, const float* w, const
   a.ratio = ratio;
   a.k = k;
   a.n_max = max_ctx_len / ratio;
-  a.fp8 = keys.fmt == CSKV_FMT_FP8_E4M3_ROWSCALE_PAGESPLIT;
+  a.kfmt = keys.fmt == CSKV_FMT_FP8_E4M3_ROWSCALE_PAGESPLIT          ? kKfFp8
+           : keys.fmt == CSKV_FMT_FP4_E2M1_E8M0_HADAMARD_PAGESPLIT ? kKfFp4
+                                                                    : kKfBf16;
   a.topk_idx = topk_idx;
   a.topk_score = topk_score;
   a.ws = static_cast<uint8_t*>(workspace);
@@ -2372,10 +2478,16 @@ cudaError_t index_setup(IndexLaunch& L, const void* q_idx, const float* w, const
   cuuint64_t dims[3], strides[2];
   cuuint32_t box[3], estr[3] = {1, 1, 1};
   CUtensorMapDataType dt;
-  if (a.fp8) {
+  CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B;
+  if (a.kfmt == kKfFp8) {
     dims[0] = 128; strides[0] = 128;
     box[0] = 128;
     dt = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  } else if (a.kfmt == kKfFp4) {
+    dims[0] = 64; strides[0] = 64;   // 64 code bytes per key
+    box[0] = 64;
+    dt = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    swz = CU_TENSOR_MAP_SWIZZLE_64B;
   } else {
     dims[0] = 128; strides[0] = 256;
     box[0] = 64;
@@ -2387,7 +2499,7 @@ cudaError_t index_setup(IndexLaunch& L, const void* q_idx, const float* w, const
   box[1] = 64;
   box[2] = 1;
   CUresult r = enc(&L.tmap, dt, 3, keys.pool, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                   swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
@@ -2409,8 +2521,14 @@ cudaError_t index_launch_score(const IndexLaunch& L, cudaStream_t stream) {
   const IndexArgs& a = L.a;
   // streaming mode for batches of at most kReqCache requests; the cooperative kernel
   // (grid barrier, sliced selection) above that, whatever the key format
-  if (a.B > kReqCache) return a.fp8 ? launch_score<1, true>(L.tmap, a, stream) : launch_score<0, true>(L.tmap, a, stream);
-  return a.fp8 ? launch_score<1, false>(L.tmap, a, stream) : launch_score<0, false>(L.tmap, a, stream);
+  if (a.B > kReqCache) {
+    if (a.kfmt == kKfFp8) return launch_score<kKfFp8, true>(L.tmap, a, stream);
+    if (a.kfmt == kKfFp4) return launch_score<kKfFp4, true>(L.tmap, a, stream);
+    return launch_score<kKfBf16, true>(L.tmap, a, stream);
+  }
+  if (a.kfmt == kKfFp8) return launch_score<kKfFp8, false>(L.tmap, a, stream);
+  if (a.kfmt == kKfFp4) return launch_score<kKfFp4, false>(L.tmap, a, stream);
+  return launch_score<kKfBf16, false>(L.tmap, a, stream);
 }
 
 }  // namespace

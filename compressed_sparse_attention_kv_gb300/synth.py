@@ -20,6 +20,8 @@ Workloads (seed n - 1 for workload n):
                  and ratio 128, out FP8-528 / FP4-288 / bf16.
 5. mixed_mxfp4   batch 64, contexts ~ U{32,768 .. 524,288}, FP4-288 entries,
                  FP8 window, FP8-132 index keys, top-512, 64 heads.
+6. csa_fp4       csa_1m with FP4 index keys (rotated, e2m1 + e8m0 per 32,
+                 68 bytes per key); the same seed and values as csa_1m.
 
 The pages measure on model layers over real text and name no dataset for this
 path; these seeded inputs stand in with the shapes the pages give.  Value
@@ -42,6 +44,7 @@ FMT_BF16 = 0
 FMT_FP8 = 1
 FMT_FP4 = 2
 FMT_FP8_PAGESPLIT = 3
+FMT_FP4H_PAGESPLIT = 4
 
 # stream tags
 T_CTX, T_PAGES, T_MAIN, T_INDEX, T_SWA, T_Q, T_QIDX, T_W, T_SINK = range(1, 10)
@@ -99,6 +102,9 @@ def workload(name, batch=None):
                            np.full(32, 131072, dtype=np.int64))
     elif name == "csa_1m":
         w = DecodeWorkload(name, 2, 8, 4, 512, 64, 64, FMT_FP8, FMT_FP8, FMT_FP8_PAGESPLIT,
+                           np.full(8, 1 << 20, dtype=np.int64))
+    elif name == "csa_fp4":
+        w = DecodeWorkload(name, 2, 8, 4, 512, 64, 64, FMT_FP8, FMT_FP8, FMT_FP4H_PAGESPLIT,
                            np.full(8, 1 << 20, dtype=np.int64))
     elif name == "mixed_mxfp4":
         L = rng(4, T_CTX).integers(32768, 524288, size=64, endpoint=True).astype(np.int64)

@@ -71,7 +71,21 @@ typedef enum {
    * block of dim values): dim + 4 bytes, 132 B per 128-d key (the size of the
    * V3.2 index key).  Each 64-row page stores its 64 code rows first (dim bytes
    * each), then its 64 fp32 scales: 8,448 B per page.  Index keys only. */
-  CSKV_FMT_FP8_E4M3_ROWSCALE_PAGESPLIT = 3
+  CSKV_FMT_FP8_E4M3_ROWSCALE_PAGESPLIT = 3,
+  /* index keys rotated and coded in FP4 ("DeepSeek-V4 deep dive", section 5.2:
+   * the indexer's keys and queries go through a Hadamard rotation, then FP4
+   * rounding with block size 32; "DeepSeek-V4.1 Flash", section 10.4: MXFP4).
+   * A written row is rotated by H / sqrt(dim) (H the Sylvester Hadamard matrix,
+   * H[i][j] = (-1)^popcount(i & j)) in a fixed fp32 order - butterflies of
+   * stride 1, 2, ..., dim/2, each (a, b) -> (a + b, a - b), then one product by
+   * fp32(1 / sqrt(dim)) - then coded as dim/2 bytes of packed float4_e2m1
+   * (channel 2i in the low nibble of byte i) and dim/32 float8_e8m0 scales (scale
+   * j covers channels 32j..32j+31: the smallest 2^e with amax <= 6 * 2^e; codes
+   * RNE(x * 2^-e)): 68 B per 128-d key.  Each 64-row page stores its 64 code rows
+   * first (dim/2 bytes each), then its 64 scale rows (dim/32 bytes each): 4,352 B
+   * per page.  The indexer rotates and codes its queries the same way and keeps
+   * its scores in bf16.  Index keys only (dim 128). */
+  CSKV_FMT_FP4_E2M1_E8M0_HADAMARD_PAGESPLIT = 4
 } cskv_format;
 
 /* A paged cache (or, with block_table == NULL, a flat array of rows in which

@@ -67,6 +67,11 @@ class HostPaged:
             for p in range(pages.shape[0]):
                 self.pool[self.block_table[b, p], :pages.shape[1]] = pages[p]
             self.decoded[b] = codecs.decode_pagesplit(pages, self.dim)[:n]
+        elif self.fmt == codecs.FMT_FP4H_PAGESPLIT:
+            pages = codecs.encode_fp4h_pagesplit(v)
+            for p in range(pages.shape[0]):
+                self.pool[self.block_table[b, p], :pages.shape[1]] = pages[p]
+            self.decoded[b] = codecs.decode_fp4h_pagesplit(pages, self.dim)[:n]   # rotated values
         else:
             rows = codecs.encode_rows(v, self.fmt)
             rb = rows.shape[1]
@@ -84,8 +89,8 @@ class HostPaged:
         rb = codecs.row_bytes(self.fmt, self.dim)
         for p in range((n + PAGE - 1) // PAGE):
             pg = pool_bytes[self.block_table[b, p]]
-            if self.fmt == codecs.FMT_FP8_PAGESPLIT:
-                out.append(pg[:PAGE * (self.dim + 4)])
+            if self.fmt in (codecs.FMT_FP8_PAGESPLIT, codecs.FMT_FP4H_PAGESPLIT):
+                out.append(pg[:PAGE * rb])
             else:
                 out.append(pg[:PAGE * rb].reshape(PAGE, rb))
         return out
@@ -139,3 +144,43 @@ def check_topk(got_idx, got_score, q_hat, w, k_hat, n, k):
         bound = indexer.accumulation_bound(q_hat, w, k_hat[:n])
         assert np.all(np.abs(sc - I[gs]) <= bound[gs] + 1e-30)
     return len(diff) // 2
+
+
+def check_topk_fp4(got_idx, got_score, q, w, k_hat, n, k):
+    """Top-k parity for FP4 index keys (rotated FP4 queries and keys, BF16 scores).
+
+    The GPU's fp32 score of entry j lies within the accumulation bound e_j of the fp64
+    score I_j, and bf16 rounding is monotone, so its bf16 score lies in
+    [lo_j, hi_j] = [bf16(I_j - e_j), bf16(I_j + e_j)].  The returned set must be the top
+    min(k, n) of some scores in those intervals with ties to the smaller entry: its
+    weakest member (smallest hi, then largest index) must beat the strongest entry left
+    out (largest lo, then smallest index).  Returned scores lie in their intervals.
+    Returns the number of entries that differ from the oracle's own selection.
+    """
+    q_hat = indexer.quantize_queries_fp4(q)
+    I = indexer.scores_fp64(q_hat, w, k_hat[:n])
+    ref = indexer.select_topk(indexer.bf16_scores(I), k)
+    bound = indexer.accumulation_bound(q_hat, w, k_hat[:n])
+    lo = indexer.bf16_scores(I - bound)
+    hi = indexer.bf16_scores(I + bound)
+    got = np.asarray(got_idx, np.int64)
+    m = min(k, n)
+    assert np.all(got[m:] == -1)
+    gs = got[:m]
+    assert np.all(np.diff(gs) > 0), "indices not ascending/unique"
+    assert np.all((gs >= 0) & (gs < n))
+    if m < n:
+        inset = np.zeros(n, bool)
+        inset[gs] = True
+        g_hi, g_idx = hi[inset], np.flatnonzero(inset)
+        weakest = np.lexsort((-g_idx, g_hi))[0]          # smallest hi, then largest index
+        o_lo, o_idx = lo[~inset], np.flatnonzero(~inset)
+        strongest = np.lexsort((o_idx, -o_lo))[0]        # largest lo, then smallest index
+        a_s, a_j = g_hi[weakest], g_idx[weakest]
+        b_s, b_j = o_lo[strongest], o_idx[strongest]
+        assert a_s > b_s or (a_s == b_s and a_j < b_j), (a_j, a_s, b_j, b_s)
+    if got_score is not None:
+        sc = np.asarray(got_score, np.float64)[:m]
+        assert np.all((sc >= lo[gs]) & (sc <= hi[gs]))
+        assert np.array_equal(sc, indexer.bf16_scores(sc))   # bf16 values
+    return len(set(gs.tolist()) ^ set(ref[:m].tolist()))

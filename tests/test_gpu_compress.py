@@ -14,7 +14,7 @@ pytestmark = pytest.mark.gpu
 
 FMTS = [(codecs.FMT_FP8, 512), (codecs.FMT_FP4, 512), (codecs.FMT_BF16, 512),
         (codecs.FMT_FP8_PAGESPLIT, 128), (codecs.FMT_FP8, 128), (codecs.FMT_BF16, 128),
-        (codecs.FMT_FP4, 128)]
+        (codecs.FMT_FP4, 128), (codecs.FMT_FP4H_PAGESPLIT, 128)]
 
 
 def _edge_rows(dim, rs):
@@ -45,6 +45,10 @@ def test_encode_rows_bit_exact(fmt, dim):
     if fmt == codecs.FMT_FP8_PAGESPLIT:
         want = codecs.encode_pagesplit(x)
         assert np.array_equal(got[:, :want.shape[1]], want)
+    elif fmt == codecs.FMT_FP4H_PAGESPLIT:
+        want = codecs.encode_fp4h_pagesplit(x)   # rotated, then coded
+        bad = np.flatnonzero(np.any(got[:, :want.shape[1]] != want, axis=1))
+        assert bad.size == 0, bad
     else:
         rows = codecs.encode_rows(x, fmt)
         rb = rows.shape[1]
@@ -89,6 +93,7 @@ def _compress_case(ratio, overlap, dim, fmt, S=2, entries=96, seed=0):
     (4, 1, 512, codecs.FMT_FP8, True), (4, 1, 512, codecs.FMT_FP4, False),
     (4, 1, 512, codecs.FMT_BF16, True), (4, 1, 128, codecs.FMT_FP8_PAGESPLIT, True),
     (4, 1, 128, codecs.FMT_FP8_PAGESPLIT, False), (4, 1, 128, codecs.FMT_BF16, False),
+    (4, 1, 128, codecs.FMT_FP4H_PAGESPLIT, True), (4, 1, 128, codecs.FMT_FP4H_PAGESPLIT, False),
     (128, 0, 512, codecs.FMT_FP8, False), (128, 0, 512, codecs.FMT_FP4, False),
     (4, 0, 512, codecs.FMT_FP8, False)])
 def test_compress_bit_exact(ratio, overlap, dim, fmt, use_prev):
@@ -124,6 +129,11 @@ def test_compress_bit_exact(ratio, overlap, dim, fmt, use_prev):
                 got_d = page[slot * dim:(slot + 1) * dim]
                 got_s = page[64 * dim + slot * 4:64 * dim + (slot + 1) * 4].view(np.float32)[0]
                 assert np.array_equal(got_d, cd[0]) and got_s == codecs.e8m0_decode(e[0, 0]), (s, i)
+            elif fmt == codecs.FMT_FP4H_PAGESPLIT:
+                cd, sb = codecs.fp4b32_encode(codecs.hadamard_contract(ents[i:i + 1]))
+                got_d = page[slot * 64:(slot + 1) * 64]
+                got_s = page[64 * 64 + slot * 4:64 * 64 + (slot + 1) * 4]
+                assert np.array_equal(got_d, cd[0]) and np.array_equal(got_s, sb[0]), (s, i)
             else:
                 want = codecs.encode_rows(ents[i:i + 1], fmt)[0]
                 assert np.array_equal(page[slot * rb:(slot + 1) * rb], want), (s, i)
@@ -171,7 +181,7 @@ def test_compress_many_equals_separate_calls():
     bytes three separate compress calls write (the decode step compresses the main and
     the index-key entry together)."""
     specs = [(4, 1, 512, codecs.FMT_FP8, True, 96), (4, 1, 128, codecs.FMT_FP8_PAGESPLIT, False, 96),
-             (128, 0, 512, codecs.FMT_FP4, False, 5)]
+             (128, 0, 512, codecs.FMT_FP4, False, 5), (4, 1, 128, codecs.FMT_FP4H_PAGESPLIT, True, 96)]
     cases = [_compress_case(r, o, d, f, entries=e, seed=10 + i) for i, (r, o, d, f, _, e) in enumerate(specs)]
     sep = [c["cache"].to_device() for c in cases]
     many = [c["cache"].to_device() for c in cases]

@@ -12,7 +12,7 @@ import torch
 import compressed_sparse_attention_kv_gb300 as cskv
 from oracle import attention as o_attn, codecs, compress as o_comp, indexer, rope as o_rope
 
-from cases import HostPaged, bf16_values, check_attention, check_topk, cuda, swa_ring
+from cases import check_topk_fp4, HostPaged, bf16_values, check_attention, check_topk, cuda, swa_ring
 
 pytestmark = pytest.mark.gpu
 
@@ -73,8 +73,10 @@ def _caches(rs, fmt, dim, n, seed):
     return host, host.to_device(), vals
 
 
-@pytest.mark.parametrize("main_fmt", [codecs.FMT_FP8, codecs.FMT_FP4])
-def test_csa_layer_step_host_to_host(main_fmt):
+@pytest.mark.parametrize("main_fmt,key_fmt", [(codecs.FMT_FP8, codecs.FMT_FP8_PAGESPLIT),
+                                               (codecs.FMT_FP4, codecs.FMT_FP8_PAGESPLIT),
+                                               (codecs.FMT_FP8, codecs.FMT_FP4H_PAGESPLIT)])
+def test_csa_layer_step_host_to_host(main_fmt, key_fmt):
     rs = np.random.default_rng(61 + main_fmt)
     ratio, k, H, Hi = 4, 512, 64, 64
     n = [300, 1029, 64]                       # entries after this step (the last one is new)
@@ -82,7 +84,7 @@ def test_csa_layer_step_host_to_host(main_fmt):
     ctx = np.array([ratio * x for x in n], np.int32)
     max_ctx = int(ctx.max())
     host_main, dev_main, main_vals = _caches(rs, main_fmt, 512, n, seed=11)
-    host_idx, dev_idx, idx_vals = _caches(rs, codecs.FMT_FP8_PAGESPLIT, 128, n, seed=12)
+    host_idx, dev_idx, idx_vals = _caches(rs, key_fmt, 128, n, seed=12)
     blk_m = _block_inputs(rs, B, ratio, True, 512)
     blk_i = _block_inputs(rs, B, ratio, True, 128)
     q_t, q_v = bf16_values(rs.standard_normal((B, H, 512)).astype(np.float32))
@@ -123,9 +125,13 @@ def test_csa_layer_step_host_to_host(main_fmt):
     topk = topk.cpu().numpy()
     got = h_out.float().numpy()
     for b in range(B):
-        q_hat = indexer.quantize_queries(qi_v[b])
-        assert check_topk(topk[b], None, q_hat, w[b], host_idx.decoded[b], n[b], k) == 0, b
-        sel = indexer.select_topk(indexer.scores_fp64(q_hat, w[b], host_idx.decoded[b]), k)
+        if key_fmt == codecs.FMT_FP4H_PAGESPLIT:
+            assert check_topk_fp4(topk[b], None, qi_v[b], w[b], host_idx.decoded[b], n[b], k) == 0, b
+            sel = indexer.index_topk_fp4(qi_v[b], w[b], host_idx.decoded[b], int(ctx[b]), ratio, k)[0]
+        else:
+            q_hat = indexer.quantize_queries(qi_v[b])
+            assert check_topk(topk[b], None, q_hat, w[b], host_idx.decoded[b], n[b], k) == 0, b
+            sel = indexer.select_topk(indexer.scores_fp64(q_hat, w[b], host_idx.decoded[b]), k)
         ref = o_attn.request_attention(q_v[b], int(ctx[b]), ratio, swa_dec[b], host_main.decoded[b], sel, sink,
                                        SCALE)
         check_attention(got[b], ref, fp4=main_fmt == codecs.FMT_FP4)

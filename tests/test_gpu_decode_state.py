@@ -24,6 +24,7 @@ SPECS = [  # name, ratio, overlap, dim, format, slot bias, window ring rows
     ("hca", 128, 0, 512, codecs.FMT_FP8, True, 0),
     ("csa2", 2, 0, 512, codecs.FMT_FP4, False, 0),
     ("window", 1, 0, 512, codecs.FMT_FP8, False, 128),
+    ("index_fp4", 4, 1, 128, codecs.FMT_FP4H_PAGESPLIT, True, 0),
 ]
 
 
@@ -33,6 +34,9 @@ def _row_bytes(pool, cache, b, row):
     if cache.fmt == codecs.FMT_FP8_PAGESPLIT:
         d = cache.dim
         return pg[slot * d:(slot + 1) * d], pg[PAGE * d + 4 * slot:PAGE * d + 4 * slot + 4]
+    if cache.fmt == codecs.FMT_FP4H_PAGESPLIT:
+        h = cache.dim // 2
+        return pg[slot * h:(slot + 1) * h], pg[PAGE * h + 4 * slot:PAGE * h + 4 * slot + 4]
     rb = codecs.row_bytes(cache.fmt, cache.dim)
     return pg[slot * rb:(slot + 1) * rb], None
 
@@ -41,6 +45,9 @@ def _want_bytes(entry, fmt, dim):
     if fmt == codecs.FMT_FP8_PAGESPLIT:
         cd, e = codecs.fp8_encode(entry[None], block=dim)
         return cd[0], np.array([codecs.e8m0_decode(e[0, 0])], np.float32).view(np.uint8)
+    if fmt == codecs.FMT_FP4H_PAGESPLIT:
+        cd, sb = codecs.fp4b32_encode(codecs.hadamard_contract(entry[None]))
+        return cd[0], sb[0]
     return codecs.encode_rows(entry[None], fmt)[0], None
 
 

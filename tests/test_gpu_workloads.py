@@ -13,7 +13,7 @@ import compressed_sparse_attention_kv_gb300 as cskv
 from compressed_sparse_attention_kv_gb300 import synth
 from oracle import attention as o_attn, codecs, compress as o_comp, indexer, rope as o_rope
 
-from cases import bf16_values, check_attention, check_topk, cuda, swa_ring
+from cases import bf16_values, check_attention, check_topk, check_topk_fp4, cuda, swa_ring
 
 pytestmark = pytest.mark.gpu
 
@@ -43,10 +43,23 @@ def _build_lane(wl, lane, fmt, dim):
 
 
 def _oracle_keys(wl, b):
-    """The oracle's decoded index keys of request b (coded by the oracle's codecs)."""
+    """The oracle's decoded index keys of request b (coded by the oracle's codecs; FP4
+    keys come out rotated)."""
     vals = synth.request_values(wl, b, "index")
     n = int(wl.n_entries[b])
+    if wl.key_fmt == codecs.FMT_FP4H_PAGESPLIT:
+        return codecs.decode_fp4h_pagesplit(codecs.encode_fp4h_pagesplit(vals), 128)[:n]
     return codecs.decode_pagesplit(codecs.encode_pagesplit(vals), 128)[:n]
+
+
+def _check_selection(wl, b, got, qi, w, k_hat, n, ctx):
+    """The GPU's selection of request b against the oracle; returns the oracle's selection."""
+    if wl.key_fmt == codecs.FMT_FP4H_PAGESPLIT:
+        assert check_topk_fp4(got, None, qi, w, k_hat, n, wl.k) == 0, b
+        return indexer.index_topk_fp4(qi, w, k_hat, ctx, wl.ratio, wl.k)[0]
+    q_hat = indexer.quantize_queries(qi)
+    assert check_topk(got, None, q_hat, w, k_hat, n, wl.k) == 0, b
+    return indexer.select_topk(indexer.scores_fp64(q_hat, w, k_hat), wl.k)
 
 
 def _oracle_entries(wl, b, rows, fmt):
@@ -64,7 +77,7 @@ def _oracle_entries(wl, b, rows, fmt):
 
 def _full_size(name, sample):
     wl = synth.workload(name)
-    keys = _build_lane(wl, "index", synth.FMT_FP8_PAGESPLIT, 128)
+    keys = _build_lane(wl, "index", wl.key_fmt, 128)
     main = _build_lane(wl, "main", wl.main_fmt, 512)
     swa_vals = np.stack([synth.swa_values(wl, b) for b in range(wl.B)])
     swa_b, swa_dec = swa_ring(swa_vals, wl.swa_fmt)
@@ -80,10 +93,8 @@ def _full_size(name, sample):
     got = out.float().cpu().numpy()
     for b in sample:
         n = int(wl.n_entries[b])
-        q_hat = indexer.quantize_queries(qi_v[b])
         k_hat = _oracle_keys(wl, b)
-        assert check_topk(topk[b], None, q_hat, w[b], k_hat, n, wl.k) == 0, b
-        sel = indexer.select_topk(indexer.scores_fp64(q_hat, w[b], k_hat), wl.k)
+        sel = _check_selection(wl, b, topk[b], qi_v[b], w[b], k_hat, n, int(ctx[b]))
         ent = _oracle_entries(wl, b, sel[sel >= 0], wl.main_fmt)
         ref = o_attn.request_attention(q_v[b], int(ctx[b]), wl.ratio, swa_dec[b], ent, sel, sink, SCALE)
         check_attention(got[b], ref, fp4=wl.main_fmt == synth.FMT_FP4)
@@ -93,6 +104,12 @@ def test_csa_1m_full_size_every_request():
     """Batch 8 at 1,048,576 tokens: the selection and the attention output of every
     request against the oracle."""
     _full_size("csa_1m", range(8))
+
+
+def test_csa_fp4_keys_full_size_every_request():
+    """The 1M-context batch with FP4 index keys (rotated, e2m1 + e8m0 per 32, BF16
+    scores): every request's selection and attention output against the oracle."""
+    _full_size("csa_fp4", range(8))
 
 
 def test_mixed_mxfp4_full_size_every_request():
