@@ -63,7 +63,8 @@ constexpr int kStagesFp4 = 8;        // per producer, 9 KiB stages
 constexpr int kStagesMax = 8;
 constexpr int kAccsMax = 8;          // TMEM accumulators in flight (8 x 64 columns)
 constexpr int kScaleSlots = 16;      // ring of per-tile scale rows (2 pages x 64 fp32)
-constexpr int kRecSlots = 32;        // tile records in flight from the scheduler to the producers
+constexpr int kRecSlots = 8;         // tile records in flight from the scheduler to the producers (two chunks:
+                                     // a deeper lookahead commits work to a block too early)
 constexpr int kChunkTiles = 4;       // tiles per grab from a request's work counter
 constexpr int kWarpMma = kProducers;
 constexpr int kWarpEpi = kProducers + 1;
@@ -1461,10 +1462,7 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
         }
       };
       int req = home_request(blockIdx.x, a.B, gridDim.x);
-      uint32_t pending = 0;
-      // streaming mode keeps a second grab of the same request in flight
-      constexpr uint32_t kNoGrab = 0xFFFFFFFFu;
-      uint32_t pending2 = kNoGrab;
+      uint32_t pending = 0;   // the next grab (one in flight: the record ring hides its latency)
       auto grab = [&]() { return atomicAdd(&ctr_all[req * 4], static_cast<uint32_t>(kChunkTiles)); };
       uint32_t* handed = gbar + 1;   // LARGE: tiles handed out so far (cleared by the prep)
       // the next chunk: (request, first tile) from the pending grab; request -1 = none left
@@ -1480,7 +1478,6 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
           tiles = tiles_of(req);
           if constexpr (LARGE) seen = *reinterpret_cast<volatile uint32_t*>(handed);
           pending = grab();
-          pending2 = kNoGrab;
         }
         if (pending >= static_cast<uint32_t>(tiles)) {
           b = -1;
@@ -1488,13 +1485,8 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
         } else {
           b = req;
           t0 = static_cast<int>(pending);
-          if constexpr (LARGE) {
-            atomicAdd(handed, static_cast<uint32_t>(min(kChunkTiles, tiles - t0)));
-            pending = grab();
-          } else {
-            pending = pending2 != kNoGrab ? pending2 : grab();
-            pending2 = grab();
-          }
+          if constexpr (LARGE) atomicAdd(handed, static_cast<uint32_t>(min(kChunkTiles, tiles - t0)));
+          pending = grab();
         }
       };
       // record of local tile i (waits for its slot to be free)
