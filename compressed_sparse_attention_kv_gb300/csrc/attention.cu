@@ -38,7 +38,7 @@ namespace {
 
 constexpr int kD = 512;
 constexpr int kKeys = 128;
-constexpr int kAttnThreads = 256;
+constexpr int kAttnThreads = 512;   // 16 warps: four per TMEM lane quarter
 constexpr int kMaxHeadsPerBlock = 64;
 constexpr int kZStride = kKeys + 1;   // fp32 logits, transposed [head][key], padded
 
@@ -249,7 +249,7 @@ __device__ __forceinline__ void dequant_tile(uint8_t* ktile, const uint8_t* stag
     }
     put16(ktile, r, l, v);
   };
-  constexpr int kPer = kKeys * 16 / kAttnThreads;   // 8
+  constexpr int kPer = kKeys * 16 / kAttnThreads;   // 4
 #pragma unroll 4
   for (int u = 0; u < kPer; ++u) {
     const int x = threadIdx.x + u * kAttnThreads;
@@ -464,23 +464,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
   mbar_wait(&sm->bar_s, 0, kDefaultSpinLimit);
   tc_fence_after();
 
-  // ---- logits to smem, transposed [head][key]: warps w and w+4 share TMEM lane
-  // quarter w, each taking half of the head columns, all loads before one wait
+  // ---- logits to smem, transposed [head][key]: warps w, w+4, w+8, w+12 share TMEM lane
+  // quarter w, each taking a quarter of the head columns, all loads before one wait
   {
     const int r = (warp & 3) * 32 + lane;
     const bool ok = sm->rowp[r] != nullptr;
-    const int half = Nq >> 1;   // a multiple of 8
-    const int cbase = (warp >> 2) * half;
-    float sv[32];
+    const int quarter = Nq >> 2;   // a multiple of 4
+    const int cbase = (warp >> 2) * quarter;
+    float sv[16];
 #pragma unroll
-    for (int c0 = 0; c0 < 32; c0 += 8)
-      if (c0 < half)
-        tmem_ld8(tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + cbase + c0,
-                 *reinterpret_cast<float(*)[8]>(sv + c0));
+    for (int c0 = 0; c0 < 16; c0 += 4)
+      if (c0 < quarter)
+        tmem_ld4(tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + cbase + c0,
+                 *reinterpret_cast<float(*)[4]>(sv + c0));
     tmem_wait_ld();
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (i < half) zt[(cbase + i) * kZStride + r] = ok ? sv[i] * a.scale_log2 : -INFINITY;
+    for (int i = 0; i < 16; ++i)
+      if (i < quarter) zt[(cbase + i) * kZStride + r] = ok ? sv[i] * a.scale_log2 : -INFINITY;
   }
   __syncthreads();
 
@@ -533,11 +533,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
   mbar_wait(&sm->bar_o, 0, kDefaultSpinLimit);
   tc_fence_after();
 
-  // ---- partial out: O^T lanes = dims; warps 0-3 blocks 0,1; warps 4-7 blocks 2,3
+  // ---- partial out: O^T lanes = dims; warps 4m .. 4m+3 block m of 128 dims
   {
     const size_t slot = (size_t(b) * a.max_tiles + tile) * a.H + h0;
     const int sub = warp & 3;
-    for (int mb = (warp >> 2) * 2; mb < (warp >> 2) * 2 + 2; ++mb) {
+    {
+      const int mb = warp >> 2;
       const int d = mb * 128 + sub * 32 + lane;
       // all of the block's head columns, one wait
       float o[64];
