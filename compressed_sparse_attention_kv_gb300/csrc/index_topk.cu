@@ -2509,11 +2509,21 @@ cudaError_t index_launch_prep(const IndexLaunch& L, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, index_prep_kernel, L.a);
 }
 
+// Streaming mode (per-request selection as requests complete, no grid barrier) needs
+// the batch's visible counts in shared memory and each request's segment table in the
+// fast selection's shared-memory area; larger batches or requests take the cooperative
+// kernel.
+bool streaming_mode(const IndexArgs& a) {
+  return a.B <= kReqCache && static_cast<long long>(a.n_max) <= static_cast<long long>(kMetaSegs) * kSeg;
+}
+
 cudaError_t index_launch_score(const IndexLaunch& L, cudaStream_t stream) {
   const IndexArgs& a = L.a;
-  // streaming mode for batches of at most kReqCache requests; the cooperative kernel
+  // streaming mode for batches of at most kReqCache requests of at most kMetaSegs
+  // segments each (the fast selection keeps a request's segment table in shared memory);
+  // the cooperative kernel (grid barrier, selection sliced over the grid) otherwise
   // (grid barrier, sliced selection) above that, whatever the key format
-  if (a.B > kReqCache) {
+  if (!streaming_mode(a)) {
     if (a.kfmt == kKfFp8) return launch_score<kKfFp8, true>(L.tmap, a, stream);
     if (a.kfmt == kKfFp4) return launch_score<kKfFp4, true>(L.tmap, a, stream);
     return launch_score<kKfBf16, true>(L.tmap, a, stream);
@@ -2552,7 +2562,7 @@ cudaError_t launch_index_topk_fused(const void* q_idx, const float* w, const csk
   cudaError_t e = index_setup(L, q_idx, w, keys, ctx_len, B, Hi, ratio, k, max_ctx_len, topk_idx, topk_score,
                               workspace);
   if (e != cudaSuccess) return e;
-  const bool streaming = B <= kReqCache;
+  const bool streaming = streaming_mode(L.a);
   L.a.fused = 1;
   if (streaming) {
     // the score kernel overlaps the compressor: it waits for it only before the index
