@@ -387,7 +387,7 @@ def run_gpu(args, rank, world, workload=WORKLOAD):
         pass
     peak = peaks.get("hbm_gbs", 6800.0)
     achieved = algo_bytes / (score_mean * 1e-3) / 1e9
-    traffic = None if fp4_keys else profiled_traffic()
+    traffic = profiled_traffic() if workload == WORKLOAD else None   # the capture is of the csa_1m launch
     path_bytes = algo_bytes + B * (512 * cskv.row_bytes(wl.main_fmt, 512) + 128 * 528 + 2 * H * 512 * 2
                                    + Hi * 128 * 2)
 
