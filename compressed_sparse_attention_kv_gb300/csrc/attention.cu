@@ -15,18 +15,19 @@
 // the window indices t-127 .. t masked below 0); req_of maps a query to its
 // request.  One block
 // handles one (request, tile, head group of <= 64 heads):
-//   * the tile's rows (528 B FP8, 288 B FP4 or 1 KiB bf16; the row addresses come
-//     from the block table) and the query are copied into shared memory with
-//     cp.async, all in flight together; the rows are dequantised exactly into
-//     bf16, giving a 128 x 512 K-major tile with 128-byte swizzle, and the query's
-//     last 64 dims are rotated (fp32) in place;
+//   * the query is copied into shared memory and its last 64 dims rotated (fp32) in
+//     place, and a list tile's block-table row staged beside it, before the tile
+//     waits for its selection; then the tile's rows (528 B FP8, 288 B FP4 or 1 KiB
+//     bf16) are copied in with cp.async, all in flight together, and dequantised
+//     exactly into bf16, giving a 128 x 512 K-major tile with 128-byte swizzle;
 //   * one thread issues tcgen05 MMAs S^T = K Q^T (M = 128 keys, N = heads,
 //     K = 512) into TMEM - keys are the MMA rows, so 16..64 heads need no padding;
 //   * softmax statistics per head (max, sum of exp2) over the tile, P^T stored
 //     as the bf16 MN-major B operand;
 //   * O^T = V^T P^T (M = 128 dims x 4 blocks, N = heads, K = 128 keys): the same
 //     smem tile is read a second time as the MN-major A operand (K = V);
-//   * the partial (m, l, O) goes to the workspace.
+//   * the partial (m, l, O) goes to the workspace, O through shared memory by one
+//     bulk copy per head.
 // attn_combine_kernel merges the partials of a request in a fixed order with
 // the sink, applies the inverse rotation and writes bf16.
 #include "codec.cuh"
@@ -41,6 +42,7 @@ constexpr int kKeys = 128;
 constexpr int kAttnThreads = 512;   // 16 warps: four per TMEM lane quarter
 constexpr int kMaxHeadsPerBlock = 64;
 constexpr int kZStride = kKeys + 1;   // fp32 logits, transposed [head][key], padded
+constexpr int kBtStage = kKeys * 128;  // block-table entries staged in the K tile's lower half (64 KiB)
 
 __host__ __device__ inline size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -325,80 +327,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
       else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
     }
   }
-  grid_dep_launch();   // the combine kernel may be scheduled; it waits for this grid
-  // The selected entries come from the indexer, which may still be finishing (this
-  // kernel is a programmatic dependent of it): compressed tiles wait here, the
-  // window tile does not need it.  In a fused step each request's flag says when its
-  // own selection is written.
-  if (tile > 0) {
-    if (a.ready == nullptr) {
-      grid_dep_wait();
-    } else {
-      // while the selection is being written: the request's block-table row into L2, so
-      // that the row lookups after it do not wait on HBM
-      if (a.kv.block_table != nullptr) {
-        const int32_t* bt = a.kv.block_table + static_cast<long long>(b) * a.kv.max_pages;
-        const int np = min(a.kv.max_pages, (ctx / a.ratio + kPageRows - 1) / kPageRows);
-        for (int x = threadIdx.x * 32; x < np; x += blockDim.x * 32)
-          asm volatile("prefetch.global.L2 [%0];" ::"l"(bt + x));
-      }
-      if (threadIdx.x == 0 && ld_acquire_gpu(a.ready + b) == 0) {
-        const unsigned long long t0 = clock64();
-        while (ld_acquire_gpu(a.ready + b) == 0) {
-          if (clock64() - t0 > a.spin) {
-            set_err(CSKV_ERR_TIMEOUT);
-            break;
-          }
-          __nanosleep(100);
-        }
-      }
-      __syncthreads();
-    }
-  }
-  // ---- rows of this tile: one thread per row resolves its address (the list entry,
-  // then the block table), all rows in parallel
+  // ---- list tiles: the request's block-table row into the lower half of the K tile
+  // (untouched until the rows are resolved), so that the lookups after the selection
+  // read shared memory
   const int rq = a.req_of ? a.req_of[b] : b;
-  for (int r = threadIdx.x; r < kKeys; r += blockDim.x) {
-    const uint8_t* p = nullptr;
-    if (tile == 0) {
-      if (a.win.pool == nullptr) {
-        if ((t >= kKeys - 1) || (r <= t)) p = a.swa + (size_t(b) * kWindow + r) * a.swa_row_bytes;
-      } else {
-        const int pos = t - (kKeys - 1) + r;   // positions t-127 .. t; none below 0
-        if (pos >= 0) p = paged_row(a.win, rq, pos, a.swa_row_bytes).data;
-      }
-    } else {
-      const int li = (tile - 1) * kKeys + r;
-      if (li < ncomp) {
-        const int e = a.topk ? a.topk[size_t(b) * a.k + li] : li;
-        if (e >= 0) {
-          if (e < ctx / a.ratio) p = paged_row(a.kv, rq, e, a.kv_row_bytes).data;
-          else set_err(CSKV_ERR_BOUNDS);
-        }
-      }
-    }
-    sm->rowp[r] = p;
-  }
-  __syncthreads();
-  // ---- key rows
-  const bool bf16_rows = row_fmt == CSKV_FMT_BF16;
-  const int code_bytes = row_fmt == CSKV_FMT_FP8_E4M3_E8M0_B32 ? kD : kD / 2;
-  const int scl_bytes = row_fmt == CSKV_FMT_FP8_E4M3_E8M0_B32 ? kD / 32 : kD / 16;
-  {
-    const int cpr = bf16_rows ? 64 : (code_bytes + scl_bytes) / 16;   // 16-byte chunks per row
+  const int32_t* bt_s = reinterpret_cast<const int32_t*>(ktile);
+  const int np = tile > 0 && a.kv.block_table != nullptr
+                     ? min(a.kv.max_pages, (ctx / a.ratio + kPageRows - 1) / kPageRows)
+                     : 0;
+  const bool bt_staged = np > 0 && np <= kBtStage;
+  if (bt_staged) {
+    const int32_t* bt = a.kv.block_table + static_cast<long long>(rq) * a.kv.max_pages;
 #pragma unroll 1
-    for (int x = threadIdx.x; x < kKeys * cpr; x += blockDim.x) {
-      const int r = x / cpr, c = x - r * cpr;
-      const uint8_t* p = sm->rowp[r];
-      if (bf16_rows) {
-        uint8_t* dst = ktile + (c >> 3) * (kKeys * 128) + sw128_offset(r, c & 7);
-        if (p) cp_async16(dst, p + c * 16);
-        else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
-      } else if (p) {
-        if (c * 16 < code_bytes) cp_async16(stage + r * code_bytes + c * 16, p + c * 16);
-        else cp_async16(&sm->scl[r][c * 16 - code_bytes], p + c * 16);
-      }
-    }
+    for (int x = threadIdx.x; x < np; x += blockDim.x) cp_async4(ktile + 4 * x, bt + x);
   }
   cp_async_wait_all();
   __syncthreads();
@@ -429,6 +370,88 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
       *pq = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
+  grid_dep_launch();   // the combine kernel may be scheduled; it waits for this grid
+  // The selected entries come from the indexer, which may still be finishing (this
+  // kernel is a programmatic dependent of it): compressed tiles wait here, the
+  // window tile does not need it.  In a fused step each request's flag says when its
+  // own selection is written.
+  if (tile > 0) {
+    if (a.ready == nullptr) {
+      grid_dep_wait();
+    } else {
+      // a block-table row too long to stage: into L2 while the selection is being
+      // written, so that the row lookups after it do not wait on HBM
+      if (a.kv.block_table != nullptr && !bt_staged) {
+        const int32_t* bt = a.kv.block_table + static_cast<long long>(rq) * a.kv.max_pages;
+        for (int x = threadIdx.x * 32; x < np; x += blockDim.x * 32)
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(bt + x));
+      }
+      if (threadIdx.x == 0 && ld_acquire_gpu(a.ready + b) == 0) {
+        const unsigned long long t0 = clock64();
+        while (ld_acquire_gpu(a.ready + b) == 0) {
+          if (clock64() - t0 > a.spin) {
+            set_err(CSKV_ERR_TIMEOUT);
+            break;
+          }
+          __nanosleep(100);
+        }
+      }
+      __syncthreads();
+    }
+  }
+  // ---- rows of this tile: one thread per row resolves its address (the list entry,
+  // then the block table), all rows in parallel
+  for (int r = threadIdx.x; r < kKeys; r += blockDim.x) {
+    const uint8_t* p = nullptr;
+    if (tile == 0) {
+      if (a.win.pool == nullptr) {
+        if ((t >= kKeys - 1) || (r <= t)) p = a.swa + (size_t(b) * kWindow + r) * a.swa_row_bytes;
+      } else {
+        const int pos = t - (kKeys - 1) + r;   // positions t-127 .. t; none below 0
+        if (pos >= 0) p = paged_row(a.win, rq, pos, a.swa_row_bytes).data;
+      }
+    } else {
+      const int li = (tile - 1) * kKeys + r;
+      if (li < ncomp) {
+        const int e = a.topk ? a.topk[size_t(b) * a.k + li] : li;
+        if (e >= 0) {
+          if (e >= ctx / a.ratio) {
+            set_err(CSKV_ERR_BOUNDS);
+          } else if (bt_staged) {   // the same checks as paged_row
+            const int lp = e / kPageRows, pp = lp < np ? bt_s[lp] : -1;
+            if (pp >= 0 && pp < a.kv.num_pages) p = page_row(a.kv, pp, e % kPageRows, a.kv_row_bytes).data;
+            else set_err(CSKV_ERR_BOUNDS);
+          } else {
+            p = paged_row(a.kv, rq, e, a.kv_row_bytes).data;
+          }
+        }
+      }
+    }
+    sm->rowp[r] = p;
+  }
+  __syncthreads();
+  // ---- key rows
+  const bool bf16_rows = row_fmt == CSKV_FMT_BF16;
+  const int code_bytes = row_fmt == CSKV_FMT_FP8_E4M3_E8M0_B32 ? kD : kD / 2;
+  const int scl_bytes = row_fmt == CSKV_FMT_FP8_E4M3_E8M0_B32 ? kD / 32 : kD / 16;
+  {
+    const int cpr = bf16_rows ? 64 : (code_bytes + scl_bytes) / 16;   // 16-byte chunks per row
+#pragma unroll 1
+    for (int x = threadIdx.x; x < kKeys * cpr; x += blockDim.x) {
+      const int r = x / cpr, c = x - r * cpr;
+      const uint8_t* p = sm->rowp[r];
+      if (bf16_rows) {
+        uint8_t* dst = ktile + (c >> 3) * (kKeys * 128) + sw128_offset(r, c & 7);
+        if (p) cp_async16(dst, p + c * 16);
+        else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+      } else if (p) {
+        if (c * 16 < code_bytes) cp_async16(stage + r * code_bytes + c * 16, p + c * 16);
+        else cp_async16(&sm->scl[r][c * 16 - code_bytes], p + c * 16);
+      }
+    }
+  }
+  cp_async_wait_all();
+  __syncthreads();
   // ---- S^T = K Q^T : M = 128 keys, N = Nq, K = 512, issued by one thread in two
   // halves of K: dims 0-255 as soon as the dequantisation has written them (the tensor
   // core works while the second half is dequantised), then dims 256-511
@@ -436,12 +459,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
     if (threadIdx.x == 0) {
       tc_fence_after();
       const uint32_t id = make_idesc(1, 1, 0, 0, 128, 0) | (static_cast<uint32_t>(Nq >> 3) << 17);
-      const uint32_t ka = smem_u32(ktile), qa = smem_u32(qtile);
-#pragma unroll 1
+      // the descriptors' start-address field counts 16-byte units (no carry: shared
+      // memory < 256 KiB): a 32-byte K step adds 2, a 128-row chunk kKeys * 8 / Nq * 8
+      const uint64_t da = smem_desc_sw128(smem_u32(ktile), 16, 1024);
+      const uint64_t dq = smem_desc_sw128(smem_u32(qtile), 16, 1024);
+#pragma unroll 4
       for (int kk = kk0; kk < kk1; ++kk) {
-        const int c = kk >> 2, o = (kk & 3) * 32;
-        mma_f16(sm->tmem_base, smem_desc_sw128(ka + c * (kKeys * 128) + o, 16, 1024),
-                smem_desc_sw128(qa + c * (Nq * 128) + o, 16, 1024), id, kk > 0);
+        const int c = kk >> 2, o = (kk & 3) * 2;
+        mma_f16(sm->tmem_base, da + c * (kKeys * 8) + o, dq + c * (Nq * 8) + o, id, kk > 0);
       }
       if (last) mma_commit(&sm->bar_s);
     }
@@ -518,15 +543,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
   // ---- O^T = V^T P^T : 4 blocks of 128 dims, N = Nq, K = 128 keys; both operands MN-major
   if (threadIdx.x == 0) {
     const uint32_t id = make_idesc(1, 1, 1, 1, 128, 0) | (static_cast<uint32_t>(Nq >> 3) << 17);
-    const uint32_t ka = smem_u32(ktile), pa = smem_u32(ptile);
+    const uint64_t dv = smem_desc_sw128(smem_u32(ktile), kKeys * 128, 1024);
+    const uint64_t dp = smem_desc_sw128(smem_u32(ptile), kKeys * 128, 1024);
 #pragma unroll
     for (int mb = 0; mb < 4; ++mb) {
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        mma_f16(tmem + 128 + mb * Nq,
-                smem_desc_sw128(ka + 2 * mb * (kKeys * 128) + ks * 2048, kKeys * 128, 1024),
-                smem_desc_sw128(pa + ks * 2048, kKeys * 128, 1024), id, ks > 0);
-      }
+      for (int ks = 0; ks < 8; ++ks)
+        mma_f16(tmem + 128 + mb * Nq, dv + mb * (kKeys * 16) + ks * 128, dp + ks * 128, id, ks > 0);
     }
     mma_commit(&sm->bar_o);
   }
@@ -548,18 +571,28 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
           tmem_ld16(tmem + (static_cast<uint32_t>(sub * 32) << 16) + 128 + mb * Nq + c0,
                     *reinterpret_cast<float(*)[16]>(o + c0));
       tmem_wait_ld();
+      // into the K tile (free once the O product has completed) as [head][dim], then
+      // out by one bulk copy per head: the rows of the partial are contiguous
+      float* ostage = reinterpret_cast<float*>(ktile);
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
-        if (i < Hb) a.opart[(slot + i) * kD + d] = o[i];
+        if (i < Hb) ostage[i * kD + d] = o[i];
       }
     }
     if (threadIdx.x < Hb) {
       a.ml[(slot + threadIdx.x) * 2 + 0] = sm->m[threadIdx.x];
       a.ml[(slot + threadIdx.x) * 2 + 1] = sm->l[threadIdx.x];
     }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+#pragma unroll 1
+      for (int i = lane; i < Hb; i += 32)
+        bulk_s2g(a.opart + (slot + i) * kD, ktile + size_t(i) * kD * 4, kD * 4);
+      bulk_commit_wait_all();   // complete before the block's shared memory goes away
+    }
   }
-  tc_fence_before();
-  __syncthreads();
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);

@@ -54,19 +54,9 @@ struct RowPtr {
   uint8_t* scale;  // first scale byte of the row (formats with scales)
 };
 
-// Address of row `row` of request `req` in a paged cache; nullptr (and a sticky
-// error) when the row is outside the request's table or the page outside the pool.
-__device__ __forceinline__ RowPtr paged_row(const cskv_paged& c, int req, long long row,
-                                            int row_bytes) {
-  RowPtr r{nullptr, nullptr};
-  long long lp = row / kPageRows;
-  int slot = static_cast<int>(row % kPageRows);
-  long long pp = lp;
-  if (c.block_table != nullptr) {
-    if (lp >= c.max_pages || row < 0) { set_err(CSKV_ERR_BOUNDS); return r; }
-    pp = c.block_table[static_cast<long long>(req) * c.max_pages + lp];
-  }
-  if (pp < 0 || pp >= c.num_pages) { set_err(CSKV_ERR_BOUNDS); return r; }
+// Address of slot `slot` of physical page pp (already checked against the pool).
+__device__ __forceinline__ RowPtr page_row(const cskv_paged& c, long long pp, int slot, int row_bytes) {
+  RowPtr r;
   uint8_t* page = static_cast<uint8_t*>(c.pool) + pp * c.page_bytes;
   if (c.fmt == CSKV_FMT_FP8_E4M3_ROWSCALE_PAGESPLIT) {
     r.data = page + static_cast<long long>(slot) * c.dim;
@@ -80,6 +70,20 @@ __device__ __forceinline__ RowPtr paged_row(const cskv_paged& c, int req, long l
                         : c.fmt == CSKV_FMT_FP4_E2M1_E4M3_B16 ? c.dim / 2 : 0);
   }
   return r;
+}
+
+// Address of row `row` of request `req` in a paged cache; nullptr (and a sticky
+// error) when the row is outside the request's table or the page outside the pool.
+__device__ __forceinline__ RowPtr paged_row(const cskv_paged& c, int req, long long row,
+                                            int row_bytes) {
+  long long lp = row / kPageRows;
+  long long pp = lp;
+  if (c.block_table != nullptr) {
+    if (lp >= c.max_pages || row < 0) { set_err(CSKV_ERR_BOUNDS); return RowPtr{nullptr, nullptr}; }
+    pp = c.block_table[static_cast<long long>(req) * c.max_pages + lp];
+  }
+  if (pp < 0 || pp >= c.num_pages) { set_err(CSKV_ERR_BOUNDS); return RowPtr{nullptr, nullptr}; }
+  return page_row(c, pp, static_cast<int>(row % kPageRows), row_bytes);
 }
 
 // ---------------------------------------------------------------------------
@@ -202,6 +206,19 @@ __device__ __forceinline__ void cp_async8(void* smem_dst, const void* gmem_src) 
 }
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// Bulk copy shared -> global through the asynchronous proxy, tracked by the issuing
+// thread's bulk groups: both addresses 16-byte aligned, bytes a multiple of 16.  The
+// shared source must be fenced (fence_proxy_async_smem) and synchronised before.
+__device__ __forceinline__ void bulk_s2g(void* gmem_dst, const void* smem_src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gmem_dst),
+               "r"(smem_u32(smem_src)), "r"(bytes)
+               : "memory");
+}
+// this thread's bulk copies so far: committed as a group, then awaited to completion
+__device__ __forceinline__ void bulk_commit_wait_all() {
+  asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // Programmatic dependent launch: a kernel launched with programmatic stream
