@@ -17,9 +17,10 @@
 // handles one (request, tile, head group of <= 64 heads):
 //   * the query is copied into shared memory and its last 64 dims rotated (fp32) in
 //     place, and a list tile's block-table row staged beside it, before the tile
-//     waits for its selection; then the tile's rows (528 B FP8, 288 B FP4 or 1 KiB
-//     bf16) are copied in with cp.async, all in flight together, and dequantised
-//     exactly into bf16, giving a 128 x 512 K-major tile with 128-byte swizzle;
+//     waits for its selection; then the tile's rows (528 B FP8 or 288 B FP4: two bulk
+//     copies per row on one mbarrier; 1 KiB bf16 rows by 16-byte copies into place)
+//     come in, all in flight together, and are dequantised exactly into bf16, giving
+//     a 128 x 512 K-major tile with 128-byte swizzle;
 //   * one thread issues tcgen05 MMAs S^T = K Q^T (M = 128 keys, N = heads,
 //     K = 512) into TMEM - keys are the MMA rows, so 16..64 heads need no padding;
 //   * softmax statistics per head (max, sum of exp2) over the tile, P^T stored
@@ -124,37 +125,6 @@ __device__ __forceinline__ void put16(uint8_t* tile, int row, int l, const float
   *reinterpret_cast<uint4*>(base + sw128_offset(row, c0 + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
-// 16 values already packed as 8 bf16 pairs -> the same places as put16
-__device__ __forceinline__ void put16w(uint8_t* tile, int row, int l, const uint32_t (&w)[8]) {
-  uint8_t* base = tile + (l >> 2) * (kKeys * 128);
-  const int c0 = (l & 3) * 2;
-  *reinterpret_cast<uint4*>(base + sw128_offset(row, c0)) = make_uint4(w[0], w[1], w[2], w[3]);
-  *reinterpret_cast<uint4*>(base + sw128_offset(row, c0 + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
-}
-
-// 16 e4m3 codes times the power of two 2^(scb - 127), straight into bf16 bit patterns:
-// a normal code s.eeee.mmm is (-1)^s 2^(eeee-7) (1 + mmm/8), so its bf16 image has sign s,
-// exponent field eeee + 120 + (scb - 127) and mantissa mmm << 4 - the code's low 7 bits
-// shifted left by 4, plus a constant.  Two codes per 32-bit word (byte permutes, one
-// shift, one logic op, one add).  Exact wherever it applies; returns false (nothing
-// written) when a code is zero or subnormal or the scale is below 2^-119, for the
-// general conversion to take over.
-__device__ __forceinline__ bool e4m3x16_to_bf16(const uint4 codes, uint32_t scb, uint32_t (&w)[8]) {
-  if (scb < 8u) return false;
-  const uint32_t bias2 = ((scb - 7u) << 7) * 0x00010001u;
-  const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
-  uint32_t bad = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t v0 = __byte_perm(cw[i], 0u, 0x1404);   // [code1 << 8 | code0 << 8] per half
-    const uint32_t v1 = __byte_perm(cw[i], 0u, 0x3424);
-    bad |= __vcmpeq2(v0 & 0x78007800u, 0u) | __vcmpeq2(v1 & 0x78007800u, 0u);
-    w[2 * i] = ((v0 & 0x80008000u) | ((v0 >> 4) & 0x07F007F0u)) + bias2;
-    w[2 * i + 1] = ((v1 & 0x80008000u) | ((v1 >> 4) & 0x07F007F0u)) + bias2;
-  }
-  return bad == 0;
-}
-
 // Raw bytes of 16 values of one row: codes (16 B FP8 / 8 B FP4 / 32 B bf16) and
 // their scale byte.
 struct RowBytes {
@@ -203,7 +173,7 @@ __device__ __forceinline__ void convert16(int fmt, const RowBytes& r, float (&v)
 }
 
 struct AttnSmem {
-  uint64_t bar_s, bar_o;
+  uint64_t bar_s, bar_o, bar_rows;
   uint32_t tmem_base;
   float m[kMaxHeadsPerBlock];
   float l[kMaxHeadsPerBlock];
@@ -212,11 +182,14 @@ struct AttnSmem {
 };
 
 // In-place dequantisation of the staged FP8 / FP4 rows into the bf16 K tile.  Item
-// (r, l) = dims 16l .. 16l+15 of row r; each thread takes 8 items of dims 0-255 (their
-// outputs in the lower half, their codes in the upper half), then reads the codes of
-// its 8 items of dims 256-511 before any thread overwrites the upper half.
-// mid() runs once the first half (dims 0-255) is in place and fenced for the tensor
-// core, before the second half is written: the first half's products may start.
+// (r, l) = dims 16l .. 16l+15 of row r, converted exactly by the hardware conversions
+// (e4m3 / e2m1 pairs to f16, times the block scale in fp32, rounded to bf16, which
+// holds every such product).  The first half (dims 0-255: outputs in the lower half,
+// codes in the upper half) is spread over all threads; each thread then reads the codes
+// of its second-half items before any thread overwrites the upper half.  mid() - thread
+// 0 issuing the first half's products - runs once the first half is in place and fenced
+// for the tensor core; warp 0 takes no second-half item, so that the issue overlaps the
+// other warps' conversions instead of following its own.
 template <int FMT, class Mid>
 __device__ __forceinline__ void dequant_tile(uint8_t* ktile, const uint8_t* stage, const AttnSmem* sm,
                                              Mid&& mid) {
@@ -236,13 +209,6 @@ __device__ __forceinline__ void dequant_tile(uint8_t* ktile, const uint8_t* stag
   };
   auto emit = [&](int r, int l, const RowBytes& rb) {
     float v[16];
-    if (kFp8 && sm->rowp[r] != nullptr) {
-      uint32_t w[8];
-      if (e4m3x16_to_bf16(rb.lo, rb.scb, w)) {
-        put16w(ktile, r, l, w);
-        return;
-      }
-    }
     if (sm->rowp[r] != nullptr) {
       convert16(FMT, rb, v);
     } else {
@@ -251,26 +217,34 @@ __device__ __forceinline__ void dequant_tile(uint8_t* ktile, const uint8_t* stag
     }
     put16(ktile, r, l, v);
   };
-  constexpr int kPer = kKeys * 16 / kAttnThreads;   // 4
+  constexpr int kItems = kKeys * 16;                    // items per half
+  constexpr int kPer = kItems / kAttnThreads;           // 4
 #pragma unroll 4
   for (int u = 0; u < kPer; ++u) {
     const int x = threadIdx.x + u * kAttnThreads;
     emit(x >> 4, x & 15, raw_of(x >> 4, x & 15));
   }
-  RowBytes rb[kPer];
+  constexpr int kThreads2 = kAttnThreads - 32;          // the second half: warps 1..
+  constexpr int kPer2 = (kItems + kThreads2 - 1) / kThreads2;   // 5
+  const int t2 = static_cast<int>(threadIdx.x) - 32;
+  RowBytes rb[kPer2];
+  if (t2 >= 0) {
 #pragma unroll
-  for (int u = 0; u < kPer; ++u) {
-    const int x = threadIdx.x + u * kAttnThreads;
-    rb[u] = raw_of(x >> 4, 16 + (x & 15));
+    for (int u = 0; u < kPer2; ++u) {
+      const int x = t2 + u * kThreads2;
+      if (x < kItems) rb[u] = raw_of(x >> 4, 16 + (x & 15));
+    }
   }
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   mid();
+  if (t2 >= 0) {
 #pragma unroll
-  for (int u = 0; u < kPer; ++u) {
-    const int x = threadIdx.x + u * kAttnThreads;
-    emit(x >> 4, 16 + (x & 15), rb[u]);
+    for (int u = 0; u < kPer2; ++u) {
+      const int x = t2 + u * kThreads2;
+      if (x < kItems) emit(x >> 4, 16 + (x & 15), rb[u]);
+    }
   }
 }
 
@@ -300,19 +274,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
   if (threadIdx.x == 0) {
     mbar_init(&sm->bar_s, 1);
     mbar_init(&sm->bar_o, 1);
+    mbar_init(&sm->bar_rows, kKeys);
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(&sm->tmem_base, 512);
 
-  // Every global read of this block is a cp.async straight into shared memory, so
-  // the loads are all in flight together and need no registers:
+  // Every global read of this block is an asynchronous copy straight into shared
+  // memory, so the loads are all in flight together and need no registers:
   //  - the query rows (bf16) into their places in the swizzled Q tile, the last 64
   //    dims rotated afterwards in shared memory;
-  //  - bf16 key rows into their places in the swizzled K tile;
-  //  - FP8 / FP4 key rows: the codes into the upper half of the K tile region, the
-  //    scale bytes into sm->scl, then dequantised in place in two halves (dims
-  //    0-255 first; the codes of dims 256-511 are read into registers before the
-  //    half they share is overwritten).
+  //  - bf16 key rows into their places in the swizzled K tile (16-byte copies);
+  //  - FP8 / FP4 key rows (bulk copies): the codes into the upper half of the K tile
+  //    region, the scale bytes into sm->scl, then dequantised in place in two halves
+  //    (dims 0-255 first; the codes of dims 256-511 are read into registers before
+  //    the half they share is overwritten).
   // The code runs once per block from a cold instruction cache; loops stay rolled.
   const int row_fmt = tile == 0 ? a.swa_fmt : a.kv.fmt;
   uint8_t* stage = ktile + 4 * kKeys * 128;   // upper half of the K tile: dims 256-511
@@ -399,9 +374,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
       __syncthreads();
     }
   }
-  // ---- rows of this tile: one thread per row resolves its address (the list entry,
-  // then the block table), all rows in parallel
-  for (int r = threadIdx.x; r < kKeys; r += blockDim.x) {
+  // ---- rows of this tile: thread r < 128 resolves row r's address (the list entry,
+  // then the block table), all rows in parallel.  FP8 / FP4 rows: the same thread copies
+  // the row in by two bulk copies, its codes into the staging half and its scale bytes
+  // beside, on bar_rows (one arrival per row thread with the bytes it expects; the wait
+  // also orders the row addresses for the whole block).  bf16 rows go straight into
+  // their swizzled places by 16-byte copies.
+  const bool bf16_rows = row_fmt == CSKV_FMT_BF16;
+  const int code_bytes = row_fmt == CSKV_FMT_FP8_E4M3_E8M0_B32 ? kD : kD / 2;
+  const int scl_bytes = row_fmt == CSKV_FMT_FP8_E4M3_E8M0_B32 ? kD / 32 : kD / 16;
+  static_assert(kKeys <= kAttnThreads, "a thread per row");
+  if (threadIdx.x < kKeys) {
+    const int r = threadIdx.x;
     const uint8_t* p = nullptr;
     if (tile == 0) {
       if (a.win.pool == nullptr) {
@@ -428,30 +412,29 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
       }
     }
     sm->rowp[r] = p;
-  }
-  __syncthreads();
-  // ---- key rows
-  const bool bf16_rows = row_fmt == CSKV_FMT_BF16;
-  const int code_bytes = row_fmt == CSKV_FMT_FP8_E4M3_E8M0_B32 ? kD : kD / 2;
-  const int scl_bytes = row_fmt == CSKV_FMT_FP8_E4M3_E8M0_B32 ? kD / 32 : kD / 16;
-  {
-    const int cpr = bf16_rows ? 64 : (code_bytes + scl_bytes) / 16;   // 16-byte chunks per row
-#pragma unroll 1
-    for (int x = threadIdx.x; x < kKeys * cpr; x += blockDim.x) {
-      const int r = x / cpr, c = x - r * cpr;
-      const uint8_t* p = sm->rowp[r];
-      if (bf16_rows) {
-        uint8_t* dst = ktile + (c >> 3) * (kKeys * 128) + sw128_offset(r, c & 7);
-        if (p) cp_async16(dst, p + c * 16);
-        else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
-      } else if (p) {
-        if (c * 16 < code_bytes) cp_async16(stage + r * code_bytes + c * 16, p + c * 16);
-        else cp_async16(&sm->scl[r][c * 16 - code_bytes], p + c * 16);
+    if (!bf16_rows) {
+      mbar_expect_tx(&sm->bar_rows, p ? static_cast<uint32_t>(code_bytes + scl_bytes) : 0u);
+      if (p) {
+        bulk_g2s(stage + r * code_bytes, p, static_cast<uint32_t>(code_bytes), &sm->bar_rows);
+        bulk_g2s(&sm->scl[r][0], p + code_bytes, static_cast<uint32_t>(scl_bytes), &sm->bar_rows);
       }
     }
   }
-  cp_async_wait_all();
-  __syncthreads();
+  if (bf16_rows) {
+    __syncthreads();
+#pragma unroll 1
+    for (int x = threadIdx.x; x < kKeys * 64; x += blockDim.x) {
+      const int r = x >> 6, c = x & 63;   // 16-byte chunk c of row r
+      const uint8_t* p = sm->rowp[r];
+      uint8_t* dst = ktile + (c >> 3) * (kKeys * 128) + sw128_offset(r, c & 7);
+      if (p) cp_async16(dst, p + c * 16);
+      else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    cp_async_wait_all();
+    __syncthreads();
+  } else {
+    mbar_wait(&sm->bar_rows, 0, kDefaultSpinLimit);
+  }
   // ---- S^T = K Q^T : M = 128 keys, N = Nq, K = 512, issued by one thread in two
   // halves of K: dims 0-255 as soon as the dequantisation has written them (the tensor
   // core works while the second half is dequantised), then dims 256-511
