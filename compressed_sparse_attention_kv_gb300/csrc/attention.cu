@@ -17,20 +17,21 @@
 // handles one (request, tile, head group of <= 64 heads):
 //   * the query is copied into shared memory and its last 64 dims rotated (fp32) in
 //     place, and a list tile's block-table row staged beside it, before the tile
-//     waits for its selection; then the tile's rows (528 B FP8 or 288 B FP4: two bulk
-//     copies per row on one mbarrier; 1 KiB bf16 rows by 16-byte copies into place)
-//     come in, all in flight together, and are dequantised exactly into bf16, giving
-//     a 128 x 512 K-major tile with 128-byte swizzle;
+//     waits for its selection; then the tile's rows (528 B FP8, 288 B FP4 or 1 KiB
+//     bf16) come in by 16-byte asynchronous copies, all in flight together, and are
+//     dequantised exactly into bf16, giving a 128 x 512 K-major tile with 128-byte
+//     swizzle;
 //   * one thread issues tcgen05 MMAs S^T = K Q^T (M = 128 keys, N = heads,
 //     K = 512) into TMEM - keys are the MMA rows, so 16..64 heads need no padding;
 //   * softmax statistics per head (max, sum of exp2) over the tile, P^T stored
 //     as the bf16 MN-major B operand;
 //   * O^T = V^T P^T (M = 128 dims x 4 blocks, N = heads, K = 128 keys): the same
 //     smem tile is read a second time as the MN-major A operand (K = V);
-//   * the partial (m, l, O) goes to the workspace, O through shared memory by one
-//     bulk copy per head.
+//   * the partial (m, l, O) goes to the workspace.
 // attn_combine_kernel merges the partials of a request in a fixed order with
 // the sink, applies the inverse rotation and writes bf16.
+#include <type_traits>
+
 #include "codec.cuh"
 #include "internal.h"
 
@@ -42,7 +43,6 @@ constexpr int kD = 512;
 constexpr int kKeys = 128;
 constexpr int kAttnThreads = 512;   // 16 warps: four per TMEM lane quarter
 constexpr int kMaxHeadsPerBlock = 64;
-constexpr int kZStride = kKeys + 1;   // fp32 logits, transposed [head][key], padded
 constexpr int kBtStage = kKeys * 128;  // block-table entries staged in the K tile's lower half (64 KiB)
 
 __host__ __device__ inline size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -173,10 +173,10 @@ __device__ __forceinline__ void convert16(int fmt, const RowBytes& r, float (&v)
 }
 
 struct AttnSmem {
-  uint64_t bar_s, bar_o, bar_rows;
+  uint64_t bar_s, bar_o;
   uint32_t tmem_base;
-  float m[kMaxHeadsPerBlock];
-  float l[kMaxHeadsPerBlock];
+  __align__(16) float mpart[4][kMaxHeadsPerBlock];   // per lane quarter: the largest logit of each head
+  float lpart[4][kMaxHeadsPerBlock];                 // per lane quarter: the sum of exp2 of each head
   const uint8_t* rowp[kKeys];   // address of each key row of the tile, null = no key
   __align__(16) uint8_t scl[kKeys][32];   // staged scale bytes of each row (FP8: 16, FP4: 32)
 };
@@ -255,7 +255,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* ktile = base;                                   // 8 chunks x 128 rows x 128 B = 128 KiB
   uint8_t* qtile = ktile + 8 * kKeys * 128;                // 8 chunks x Nq rows x 128 B <= 64 KiB
-  float* zt = reinterpret_cast<float*>(qtile);             // reused after S: [Nq][kZStride]
   uint8_t* ptile = qtile + 40960;                          // reused after S: 128 keys x 128 B (1024-aligned)
   AttnSmem* sm = reinterpret_cast<AttnSmem*>(qtile + 8 * kMaxHeadsPerBlock * 128);
 
@@ -273,19 +272,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(&sm->bar_s, 1);
-    mbar_init(&sm->bar_o, 1);
-    mbar_init(&sm->bar_rows, kKeys);
+    mbar_init(&sm->bar_o, 4);
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(&sm->tmem_base, 512);
 
-  // Every global read of this block is an asynchronous copy straight into shared
-  // memory, so the loads are all in flight together and need no registers:
+  // Every global read of this block is a cp.async straight into shared memory, so
+  // the loads are all in flight together and need no registers:
   //  - the query rows (bf16) into their places in the swizzled Q tile, the last 64
   //    dims rotated afterwards in shared memory;
-  //  - bf16 key rows into their places in the swizzled K tile (16-byte copies);
-  //  - FP8 / FP4 key rows (bulk copies): the codes into the upper half of the K tile
-  //    region, the scale bytes into sm->scl, then dequantised in place in two halves
+  //  - bf16 key rows into their places in the swizzled K tile;
+  //  - FP8 / FP4 key rows: the codes into the upper half of the K tile region, the
+  //    scale bytes into sm->scl, then dequantised in place in two halves
   //    (dims 0-255 first; the codes of dims 256-511 are read into registers before
   //    the half they share is overwritten).
   // The code runs once per block from a cold instruction cache; loops stay rolled.
@@ -375,14 +373,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
     }
   }
   // ---- rows of this tile: thread r < 128 resolves row r's address (the list entry,
-  // then the block table), all rows in parallel.  FP8 / FP4 rows: the same thread copies
-  // the row in by two bulk copies, its codes into the staging half and its scale bytes
-  // beside, on bar_rows (one arrival per row thread with the bytes it expects; the wait
-  // also orders the row addresses for the whole block).  bf16 rows go straight into
-  // their swizzled places by 16-byte copies.
+  // then the block table), all rows in parallel
   const bool bf16_rows = row_fmt == CSKV_FMT_BF16;
   const int code_bytes = row_fmt == CSKV_FMT_FP8_E4M3_E8M0_B32 ? kD : kD / 2;
-  const int scl_bytes = row_fmt == CSKV_FMT_FP8_E4M3_E8M0_B32 ? kD / 32 : kD / 16;
   static_assert(kKeys <= kAttnThreads, "a thread per row");
   if (threadIdx.x < kKeys) {
     const int r = threadIdx.x;
@@ -412,29 +405,31 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
       }
     }
     sm->rowp[r] = p;
-    if (!bf16_rows) {
-      mbar_expect_tx(&sm->bar_rows, p ? static_cast<uint32_t>(code_bytes + scl_bytes) : 0u);
-      if (p) {
-        bulk_g2s(stage + r * code_bytes, p, static_cast<uint32_t>(code_bytes), &sm->bar_rows);
-        bulk_g2s(&sm->scl[r][0], p + code_bytes, static_cast<uint32_t>(scl_bytes), &sm->bar_rows);
+  }
+  __syncthreads();
+  // ---- key rows: consecutive threads take consecutive 16-byte chunks of a row, so that
+  // each warp's copies cover whole rows (CPR chunks per row, a constant divisor)
+  auto copy_rows = [&](auto cpr_const) {
+    constexpr int CPR = decltype(cpr_const)::value;
+#pragma unroll 1
+    for (int x = threadIdx.x; x < kKeys * CPR; x += blockDim.x) {
+      const int r = x / CPR, c = x - r * CPR;
+      const uint8_t* p = sm->rowp[r];
+      if (CPR == 64) {   // bf16: straight into the row's swizzled places
+        uint8_t* dst = ktile + (c >> 3) * (kKeys * 128) + sw128_offset(r, c & 7);
+        if (p) cp_async16(dst, p + c * 16);
+        else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+      } else if (p) {    // FP8 / FP4: the codes into the staging half, the scale bytes beside
+        if (c * 16 < code_bytes) cp_async16(stage + r * code_bytes + c * 16, p + c * 16);
+        else cp_async16(&sm->scl[r][c * 16 - code_bytes], p + c * 16);
       }
     }
-  }
-  if (bf16_rows) {
-    __syncthreads();
-#pragma unroll 1
-    for (int x = threadIdx.x; x < kKeys * 64; x += blockDim.x) {
-      const int r = x >> 6, c = x & 63;   // 16-byte chunk c of row r
-      const uint8_t* p = sm->rowp[r];
-      uint8_t* dst = ktile + (c >> 3) * (kKeys * 128) + sw128_offset(r, c & 7);
-      if (p) cp_async16(dst, p + c * 16);
-      else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
-    }
-    cp_async_wait_all();
-    __syncthreads();
-  } else {
-    mbar_wait(&sm->bar_rows, 0, kDefaultSpinLimit);
-  }
+  };
+  if (bf16_rows) copy_rows(std::integral_constant<int, 64>{});
+  else if (row_fmt == CSKV_FMT_FP8_E4M3_E8M0_B32) copy_rows(std::integral_constant<int, (kD + kD / 32) / 16>{});
+  else copy_rows(std::integral_constant<int, (kD / 2 + kD / 16) / 16>{});
+  cp_async_wait_all();
+  __syncthreads();
   // ---- S^T = K Q^T : M = 128 keys, N = Nq, K = 512, issued by one thread in two
   // halves of K: dims 0-255 as soon as the dequantisation has written them (the tensor
   // core works while the second half is dequantised), then dims 256-511
@@ -472,68 +467,100 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
   mbar_wait(&sm->bar_s, 0, kDefaultSpinLimit);
   tc_fence_after();
 
-  // ---- logits to smem, transposed [head][key]: warps w, w+4, w+8, w+12 share TMEM lane
-  // quarter w, each taking a quarter of the head columns, all loads before one wait
+  // ---- softmax over the tile's keys, straight from TMEM.  Thread (lane quarter
+  // warp & 3, lane) holds key r's logits for the warp's heads [cbase, cbase + quarter);
+  // warps w, w+4, w+8, w+12 share lane quarter w and split the head columns.  Per head,
+  // the largest logit and the sum of exp2 over the warp's 32 keys come from a
+  // transposing butterfly (16 shuffles for all of a thread's heads), the four lane
+  // quarters' partials meet in shared memory; P^T is stored as the MN-major B operand
+  // [key][head], four heads per 8-byte store.
   {
     const int r = (warp & 3) * 32 + lane;
+    const int qid = warp & 3;
     const bool ok = sm->rowp[r] != nullptr;
-    const int quarter = Nq >> 2;   // a multiple of 4
+    const int quarter = Nq >> 2;   // 4, 8, 12 or 16
     const int cbase = (warp >> 2) * quarter;
-    float sv[16];
+    float z[16];
 #pragma unroll
     for (int c0 = 0; c0 < 16; c0 += 4)
       if (c0 < quarter)
-        tmem_ld4(tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + cbase + c0,
-                 *reinterpret_cast<float(*)[4]>(sv + c0));
+        tmem_ld4(tmem + (static_cast<uint32_t>(qid * 32) << 16) + cbase + c0, *reinterpret_cast<float(*)[4]>(z + c0));
     tmem_wait_ld();
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-      if (i < quarter) zt[(cbase + i) * kZStride + r] = ok ? sv[i] * a.scale_log2 : -INFINITY;
-  }
-  __syncthreads();
-
-  // ---- per head: max, exp2, sum; P^T stored as the MN-major B operand [key][head]
-  // (unrolled: the shuffle chains of a warp's heads overlap)
-#pragma unroll 8
-  for (int h = warp; h < Nq; h += kAttnThreads / 32) {
-    float z[4];
+    for (int i = 0; i < 16; ++i) z[i] = (i < quarter && ok) ? z[i] * a.scale_log2 : -INFINITY;
+    // the reduction of slot j over the warp's 32 lanes ends in lanes 2j and 2j + 1
+    const int hs = (lane >> 1) & 15;
+    auto butterfly = [&](float (&t)[16], auto op) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) z[i] = zt[h * kZStride + lane + 32 * i];
-    float m = fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3]));
+      for (int w = 8; w >= 1; w >>= 1) {   // offsets 16, 8, 4, 2: keep half the slots
+        const int off = 2 * w;
+        const bool hi = (lane & off) != 0;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-    float p[4], l = 0.f;
+        for (int j = 0; j < w; ++j) {
+          const float send = hi ? t[j] : t[j + w];
+          const float keep = hi ? t[j + w] : t[j];
+          t[j] = op(keep, __shfl_xor_sync(0xFFFFFFFFu, send, off));
+        }
+      }
+      return op(t[0], __shfl_xor_sync(0xFFFFFFFFu, t[0], 1));
+    };
+    float t[16];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      p[i] = (m == -INFINITY || h >= Hb) ? 0.f : exp2f(z[i] - m);
-      l += p[i];
+    for (int i = 0; i < 16; ++i) t[i] = z[i];
+    const float mw = butterfly(t, [](float x, float y) { return fmaxf(x, y); });
+    if ((lane & 1) == 0 && hs < quarter) sm->mpart[qid][cbase + hs] = mw;
+    __syncthreads();
+    float mh[16];
+#pragma unroll
+    for (int g = 0; g < 16; g += 4) {
+      if (g < quarter) {
+        float4 mx = *reinterpret_cast<const float4*>(&sm->mpart[0][cbase + g]);
+#pragma unroll
+        for (int q = 1; q < 4; ++q) {
+          const float4 v = *reinterpret_cast<const float4*>(&sm->mpart[q][cbase + g]);
+          mx = make_float4(fmaxf(mx.x, v.x), fmaxf(mx.y, v.y), fmaxf(mx.z, v.z), fmaxf(mx.w, v.w));
+        }
+        mh[g] = mx.x;
+        mh[g + 1] = mx.y;
+        mh[g + 2] = mx.z;
+        mh[g + 3] = mx.w;
+      } else {
+        mh[g] = mh[g + 1] = mh[g + 2] = mh[g + 3] = -INFINITY;
+      }
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, o);
-    if (lane == 0) { sm->m[h] = m; sm->l[h] = l; }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int key = lane + 32 * i;
-      const __nv_bfloat16 pb = __float2bfloat16_rn(p[i]);
-      *reinterpret_cast<__nv_bfloat16*>(ptile + sw128_offset(key, h >> 3) + (h & 7) * 2) = pb;
+    for (int i = 0; i < 16; ++i) {
+      const int h = cbase + i;
+      t[i] = (i >= quarter || mh[i] == -INFINITY || h >= Hb) ? 0.f : exp2f(z[i] - mh[i]);
     }
+#pragma unroll
+    for (int g = 0; g < 16; g += 4) {
+      if (g < quarter) {
+        const int h = cbase + g;   // a multiple of 4: the 8 bytes lie inside one 16-byte chunk
+        __nv_bfloat162 lo = __floats2bfloat162_rn(t[g], t[g + 1]);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(t[g + 2], t[g + 3]);
+        *reinterpret_cast<uint2*>(ptile + sw128_offset(r, h >> 3) + (h & 7) * 2) =
+            make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+      }
+    }
+    const float lw = butterfly(t, [](float x, float y) { return x + y; });
+    if ((lane & 1) == 0 && hs < quarter) sm->lpart[qid][cbase + hs] = lw;
   }
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
 
-  // ---- O^T = V^T P^T : 4 blocks of 128 dims, N = Nq, K = 128 keys; both operands MN-major
-  if (threadIdx.x == 0) {
+  // ---- O^T = V^T P^T : 4 blocks of 128 dims, N = Nq, K = 128 keys; both operands MN-major.
+  // The blocks write disjoint accumulators, so lane 0 of warps 0-3 issues one each and
+  // commits it (bar_o counts four): four issuers instead of one serial chain of 32.
+  if (lane == 0 && warp < 4) {
+    const int mb = warp;
     const uint32_t id = make_idesc(1, 1, 1, 1, 128, 0) | (static_cast<uint32_t>(Nq >> 3) << 17);
-    const uint64_t dv = smem_desc_sw128(smem_u32(ktile), kKeys * 128, 1024);
+    const uint64_t dv = smem_desc_sw128(smem_u32(ktile), kKeys * 128, 1024) + mb * (kKeys * 16);
     const uint64_t dp = smem_desc_sw128(smem_u32(ptile), kKeys * 128, 1024);
 #pragma unroll
-    for (int mb = 0; mb < 4; ++mb) {
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks)
-        mma_f16(tmem + 128 + mb * Nq, dv + mb * (kKeys * 16) + ks * 128, dp + ks * 128, id, ks > 0);
-    }
+    for (int ks = 0; ks < 8; ++ks) mma_f16(tmem + 128 + mb * Nq, dv + ks * 128, dp + ks * 128, id, ks > 0);
     mma_commit(&sm->bar_o);
   }
   mbar_wait(&sm->bar_o, 0, kDefaultSpinLimit);
@@ -554,28 +581,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
           tmem_ld16(tmem + (static_cast<uint32_t>(sub * 32) << 16) + 128 + mb * Nq + c0,
                     *reinterpret_cast<float(*)[16]>(o + c0));
       tmem_wait_ld();
-      // into the K tile (free once the O product has completed) as [head][dim], then
-      // out by one bulk copy per head: the rows of the partial are contiguous
-      float* ostage = reinterpret_cast<float*>(ktile);
+      // straight out: for each head the warp's 32 dims are one 128-byte line
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
-        if (i < Hb) ostage[i * kD + d] = o[i];
+        if (i < Hb) a.opart[(slot + i) * kD + d] = o[i];
       }
     }
-    if (threadIdx.x < Hb) {
-      a.ml[(slot + threadIdx.x) * 2 + 0] = sm->m[threadIdx.x];
-      a.ml[(slot + threadIdx.x) * 2 + 1] = sm->l[threadIdx.x];
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-#pragma unroll 1
-      for (int i = lane; i < Hb; i += 32)
-        bulk_s2g(a.opart + (slot + i) * kD, ktile + size_t(i) * kD * 4, kD * 4);
-      bulk_commit_wait_all();   // complete before the block's shared memory goes away
+    if (threadIdx.x < Hb) {   // the head's statistics over the tile: lane quarters in order
+      const int h = threadIdx.x;
+      const float m = fmaxf(fmaxf(sm->mpart[0][h], sm->mpart[1][h]), fmaxf(sm->mpart[2][h], sm->mpart[3][h]));
+      const float l = ((sm->lpart[0][h] + sm->lpart[1][h]) + sm->lpart[2][h]) + sm->lpart[3][h];
+      a.ml[(slot + h) * 2 + 0] = m;
+      a.ml[(slot + h) * 2 + 1] = l;
     }
   }
+  tc_fence_before();
+  __syncthreads();
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);

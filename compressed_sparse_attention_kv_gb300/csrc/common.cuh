@@ -208,19 +208,6 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
-// Bulk copy shared -> global through the asynchronous proxy, tracked by the issuing
-// thread's bulk groups: both addresses 16-byte aligned, bytes a multiple of 16.  The
-// shared source must be fenced (fence_proxy_async_smem) and synchronised before.
-__device__ __forceinline__ void bulk_s2g(void* gmem_dst, const void* smem_src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gmem_dst),
-               "r"(smem_u32(smem_src)), "r"(bytes)
-               : "memory");
-}
-// this thread's bulk copies so far: committed as a group, then awaited to completion
-__device__ __forceinline__ void bulk_commit_wait_all() {
-  asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group 0;" ::: "memory");
-}
-
 // Programmatic dependent launch: a kernel launched with programmatic stream
 // serialization may start while the previous kernel of its stream still runs;
 // grid_dep_wait() returns once that kernel has completed and its writes are
