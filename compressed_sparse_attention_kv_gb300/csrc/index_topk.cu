@@ -188,6 +188,19 @@ __device__ __forceinline__ int visible(const IndexArgs& a, int b) {
   return static_cast<int>(n);
 }
 
+// The page ids of tiles t0 .. t0 + kChunkTiles - 1 of request b (n_b visible entries),
+// two per tile; -2: no page (past the request's entries, or b < 0), -3: outside the
+// block table.  All loads are issued before any is used.
+template <int kChunk>
+__device__ __forceinline__ void chunk_page_ids(const IndexArgs& a, int b, int n_b, int t0, int (&ids)[2 * kChunk]) {
+  const int32_t* bt = a.keys.block_table + static_cast<long long>(b < 0 ? 0 : b) * a.keys.max_pages;
+#pragma unroll
+  for (int u = 0; u < 2 * kChunk; ++u) {
+    const long long lp = static_cast<long long>(t0) * 2 + u;
+    ids[u] = (b < 0 || lp * kPageRows >= n_b) ? -2 : (lp >= a.keys.max_pages ? -3 : bt[lp]);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // 1. prep: query image, folded head weights, histogram / counters / barrier cleared
 // ---------------------------------------------------------------------------
@@ -1268,6 +1281,31 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
     sm->abort = 0;
     fence_mbar_init();
   }
+  // The scheduler's first chunk - chunk r of its home request, r = its rank among that
+  // request's home blocks, taken without an atomic - has its page ids requested here,
+  // so that their loads overlap the set-up (block tables are inputs); and the home
+  // request's block-table row goes to L2 (the scheduler reads it next), each of its home
+  // blocks prefetching a share of the row's 128-byte lines.
+  const int home = home_request(blockIdx.x, a.B, gridDim.x);
+  int first_ids[2 * kChunkTiles];
+  int first_n = 0;
+  if (warp == kWarpSched && lane == 0) {
+    first_n = visible(a, home);
+    const int r0 = blockIdx.x - first_home_block(home, a.B, gridDim.x);
+    chunk_page_ids<kChunkTiles>(a, home, first_n, r0 * kChunkTiles, first_ids);
+  }
+  if constexpr (!LARGE) {
+    const int f0 = first_home_block(home, a.B, gridDim.x);
+    const int nh = first_home_block(home + 1, a.B, gridDim.x) - f0;
+    const int pages = min(a.keys.max_pages, static_cast<int>((a.n_max + kPageRows - 1) / kPageRows));
+    const int32_t* row = a.keys.block_table + static_cast<long long>(home) * a.keys.max_pages;
+    if (a.keys.block_table != nullptr) {
+#pragma unroll 1
+      for (int x = static_cast<int>(blockIdx.x) - f0 + nh * static_cast<int>(threadIdx.x); 32 * x < pages;
+           x += nh * static_cast<int>(blockDim.x))
+        prefetch_l2(row + 32 * x);
+    }
+  }
   for (int i = threadIdx.x; i < kGroups * kHistBins; i += blockDim.x) hist[i] = 0;
   uint32_t ncols = 32;
   while (ncols < static_cast<uint32_t>(kAccs * N)) ncols <<= 1;
@@ -1340,20 +1378,6 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
   // shared memory by the set-up (a global load and a 64-bit division fewer on the
   // scheduler's path)
   auto nvis = [&](int b) { return b < kReqCache ? sm->nbv[b] : visible(a, b); };
-  if constexpr (!LARGE) {
-    // the home request's block-table row goes to L2 before the scheduler reads it (its
-    // loads then return in one L2 round trip): each of the request's home blocks
-    // prefetches its share of the row's 128-byte lines
-    const int hb = home_request(blockIdx.x, a.B, gridDim.x);
-    const int f0 = first_home_block(hb, a.B, gridDim.x);
-    const int nh = first_home_block(hb + 1, a.B, gridDim.x) - f0;
-    const int pages = min(a.keys.max_pages, (nvis(hb) + kPageRows - 1) / kPageRows);
-    const int32_t* row = a.keys.block_table + static_cast<long long>(hb) * a.keys.max_pages;
-#pragma unroll 1
-    for (int x = static_cast<int>(blockIdx.x) - f0 + nh * static_cast<int>(threadIdx.x); 32 * x < pages;
-         x += nh * static_cast<int>(blockDim.x))
-      prefetch_l2(row + 32 * x);
-  }
 
   // ======================================================= phase 1: scores
   // Tiles are handed out dynamically, in chunks of kChunkTiles consecutive tiles of
@@ -1453,15 +1477,9 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
       auto tiles_of = [&](int b) { return (nvis(b) + kTileRows - 1) / kTileRows; };
       // the chunk's 2 x kChunkTiles page ids, all loads in flight
       auto chunk_ids = [&](int b, int t0, int (&ids)[2 * kChunkTiles]) {
-        const int n_b = b >= 0 ? nvis(b) : 0;
-        const int32_t* bt = a.keys.block_table + static_cast<long long>(b < 0 ? 0 : b) * a.keys.max_pages;
-#pragma unroll
-        for (int u = 0; u < 2 * kChunkTiles; ++u) {
-          const long long lp = static_cast<long long>(t0) * 2 + u;
-          ids[u] = (b < 0 || lp * kPageRows >= n_b) ? -2 : (lp >= a.keys.max_pages ? -3 : bt[lp]);
-        }
+        chunk_page_ids<kChunkTiles>(a, b, b >= 0 ? nvis(b) : 0, t0, ids);
       };
-      int req = home_request(blockIdx.x, a.B, gridDim.x);
+      int req = home;
       uint32_t pending = 0;   // the next grab (one in flight: the record ring hides its latency)
       auto grab = [&]() { return atomicAdd(&ctr_all[req * 4], static_cast<uint32_t>(kChunkTiles)); };
       uint32_t* handed = gbar + 1;   // LARGE: tiles handed out so far (cleared by the prep)
@@ -1503,9 +1521,10 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
       const int r0 = blockIdx.x - first_home_block(req, a.B, gridDim.x);
       const bool static_first = static_cast<long long>(r0) * kChunkTiles < tiles_of(req);
       if (static_first) {
-        cb = req;   // the block's first chunk, assigned without an atomic
+        cb = req;   // the block's first chunk, assigned without an atomic (page ids requested above)
         ct = r0 * kChunkTiles;
-        chunk_ids(cb, ct, ids);
+#pragma unroll
+        for (int u = 0; u < 2 * kChunkTiles; ++u) ids[u] = first_ids[u];
       }
       if (wait_at_start) grid_dep_wait();
       if constexpr (LARGE) {
