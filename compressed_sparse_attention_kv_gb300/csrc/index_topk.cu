@@ -215,6 +215,14 @@ __global__ void __launch_bounds__(256) index_prep_kernel(const IndexArgs a) {
   if (a.fused) grid_dep_wait();
   // the score kernel (a programmatic dependent of this one) may start its set-up now
   grid_dep_launch();
+  // what that set-up and its first chunks read, into L2 (no load waits on it here): the
+  // requests' context lengths and request b's block-table row
+  if (threadIdx.x == 0) prefetch_l2(a.ctx_len + b);
+  if (a.keys.block_table != nullptr) {
+    const int pages = min(a.keys.max_pages, static_cast<int>((a.n_max + kPageRows - 1) / kPageRows));
+    const int32_t* row = a.keys.block_table + static_cast<long long>(b) * a.keys.max_pages;
+    for (int x = threadIdx.x * 32; x < pages; x += blockDim.x * 32) prefetch_l2(row + x);
+  }
   // warp w owns heads w, w+8, ... (N <= 64); lane l holds dims 4l .. 4l+3.  All loads first.
   uint2 raw[8];
   float wv[8];
@@ -1287,12 +1295,10 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
   // request's block-table row goes to L2 (the scheduler reads it next), each of its home
   // blocks prefetching a share of the row's 128-byte lines.
   const int home = home_request(blockIdx.x, a.B, gridDim.x);
-  int first_ids[2 * kChunkTiles];
-  int first_n = 0;
+  int first_ids[2 * kChunkTiles];   // before the request's visible count is known: masked below
   if (warp == kWarpSched && lane == 0) {
-    first_n = visible(a, home);
     const int r0 = blockIdx.x - first_home_block(home, a.B, gridDim.x);
-    chunk_page_ids<kChunkTiles>(a, home, first_n, r0 * kChunkTiles, first_ids);
+    chunk_page_ids<kChunkTiles>(a, home, 0x7FFFFFFF, r0 * kChunkTiles, first_ids);
   }
   if constexpr (!LARGE) {
     const int f0 = first_home_block(home, a.B, gridDim.x);
@@ -1523,8 +1529,10 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
       if (static_first) {
         cb = req;   // the block's first chunk, assigned without an atomic (page ids requested above)
         ct = r0 * kChunkTiles;
+        const int n_b = nvis(req);
 #pragma unroll
-        for (int u = 0; u < 2 * kChunkTiles; ++u) ids[u] = first_ids[u];
+        for (int u = 0; u < 2 * kChunkTiles; ++u)
+          ids[u] = (static_cast<long long>(ct) * 2 + u) * kPageRows >= n_b ? -2 : first_ids[u];
       }
       if (wait_at_start) grid_dep_wait();
       if constexpr (LARGE) {
@@ -1549,10 +1557,15 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
           q_b = cb;
         }
         // the next chunk is resolved and its page ids requested before this one's records
+        // (after them for the block's first chunk, whose records go out at once: the
+        // ring is empty, and resolving waits for a grab's round trip)
         int nb2 = -1, nt = 0;
         int nids[2 * kChunkTiles];
-        resolve(nb2, nt);
-        chunk_ids(nb2, nt, nids);
+        const bool first = i == 0;
+        if (!first) {
+          resolve(nb2, nt);
+          chunk_ids(nb2, nt, nids);
+        }
         const int tiles = tiles_of(cb);
 #pragma unroll
         for (int u = 0; u < kChunkTiles; ++u) {
@@ -1560,6 +1573,10 @@ __global__ void __launch_bounds__(kLaunchBound, 1)
             ok = false;
             break;
           }
+        }
+        if (first) {
+          resolve(nb2, nt);
+          chunk_ids(nb2, nt, nids);
         }
         cb = nb2;
         ct = nt;
