@@ -207,6 +207,10 @@ __device__ __forceinline__ void cp_async8(void* smem_dst, const void* gmem_src) 
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
+// this thread's copies so far close a group; wait_prior1() then returns once every
+// group but the newest has landed
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_prior1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 // Programmatic dependent launch: a kernel launched with programmatic stream
 // serialization may start while the previous kernel of its stream still runs;

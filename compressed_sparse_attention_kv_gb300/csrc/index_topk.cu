@@ -398,7 +398,10 @@ __device__ __forceinline__ void grid_barrier(ScoreSmem* sm, uint32_t* counter, u
 // then the 16 fine bins of the coarse bin that crosses k, read from s_fine: the
 // request's 4,096 fine bins, whose cp.async copies the caller issued beside the
 // coarse loads (this function waits for every copy the thread has in flight).
-__device__ __forceinline__ void threshold_bin(ScoreSmem* sm, const uint32_t* gh, int k, const uint32_t* s_fine) {
+// newest_pending: the caller's copies form two groups, the fine bins first; only that
+// group is awaited (the newer one lands meanwhile).  Otherwise every copy is awaited.
+__device__ __forceinline__ void threshold_bin(ScoreSmem* sm, const uint32_t* gh, int k, const uint32_t* s_fine,
+                                              bool newest_pending = false) {
   const int lane = threadIdx.x;
   if (lane < 32) {
     // lane l owns coarse bins 255-8l .. 248-8l (from the top): two 16-byte loads
@@ -429,22 +432,33 @@ __device__ __forceinline__ void threshold_bin(ScoreSmem* sm, const uint32_t* gh,
       sm->above = acc;
     }
   }
-  cp_async_wait_all();
+  if (newest_pending) cp_async_wait_prior1();
+  else cp_async_wait_all();
   __syncthreads();
-  if (threadIdx.x == 0 && sm->cbin >= 0) {
+  if (threadIdx.x < 32 && sm->cbin >= 0) {
+    // the 16 fine bins of coarse bin u, lane l = fine bin 15 - l (from the top): the
+    // first whose running count reaches k is T
     const int u = sm->cbin;
-    uint32_t acc = sm->above;
-    int T = u * 16;
-    uint32_t inT = s_fine[u * 16];
-#pragma unroll 1
-    for (int i = 15; i >= 0; --i) {
-      const uint32_t f = s_fine[u * 16 + i];
-      if (acc + f >= static_cast<uint32_t>(k)) { T = u * 16 + i; inT = f; break; }
-      acc += f;
+    const uint32_t acc0 = sm->above;
+    const uint32_t f = lane < 16 ? s_fine[u * 16 + 15 - lane] : 0u;
+    uint32_t incl = f;
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1) {
+      const uint32_t x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += x;
     }
-    sm->T = T;
-    sm->above = acc;
-    sm->inT = inT;
+    const unsigned hit = __ballot_sync(0xFFFFFFFFu, lane < 16 && acc0 + incl >= static_cast<uint32_t>(k));
+    if (hit != 0) {
+      if (lane == __ffs(hit) - 1) {
+        sm->T = u * 16 + 15 - lane;
+        sm->above = acc0 + incl - f;
+        sm->inT = f;
+      }
+    } else if (lane == 15) {   // inconsistent tables (only after an earlier error)
+      sm->T = u * 16;
+      sm->above = acc0 + incl;
+      sm->inT = s_fine[u * 16];
+    }
   }
   __syncthreads();
 }
@@ -898,14 +912,17 @@ __device__ __noinline__ void select_completed(const IndexArgs& a) {
     uint32_t* s_fine = hist;
 #pragma unroll 1
     for (int x = threadIdx.x; x < kHistBins / 4; x += blockDim.x) cp_async16(s_fine + 4 * x, ghb + 4 * x);
+    cp_async_commit();
     if (meta_fits) {
 #pragma unroll 1
       for (int x = threadIdx.x; x < (nseg + 1) / 2; x += blockDim.x) cp_async16(s_meta + 2 * x, meta + 2 * x);
     }
-    threshold_bin(sm, ghb, a.k, s_fine);   // waits for every copy above
+    cp_async_commit();
+    threshold_bin(sm, ghb, a.k, s_fine, true);   // waits for the fine bins; the metadata lands meanwhile
     const int T = sm->T;
     const uint32_t above = sm->above;
     if (T < 0) {   // fewer than k binned entries (an earlier error dropped some)
+      cp_async_wait_all();   // the metadata copies land before the next request reuses their place
       pad_out(b, 0);
       raise_ready(b);
       continue;
@@ -934,6 +951,7 @@ __device__ __noinline__ void select_completed(const IndexArgs& a) {
       const int no = min(nseg - q0, kOwn);
       const int rot = static_cast<int>(threadIdx.x) % kOwn;
       if (threadIdx.x == 0) sm->cnt[1] = 0;
+      cp_async_wait_all();   // the segment metadata
       __syncthreads();
       // The loops below issue their shared-memory loads in groups of eight before any use
       // (the latency of one load, not of eight, per group).
@@ -1136,6 +1154,8 @@ __device__ __noinline__ void select_completed(const IndexArgs& a) {
       __syncthreads();   // too many multi segments: every thread is past the counts before the general path
     }
     // ---- general path: every segment whose largest key reaches T is read again, in rounds
+    cp_async_wait_all();   // the metadata copies (unused here) land before the stage ring is reused
+    __syncthreads();
     unsigned long long* cand = nexp <= static_cast<uint32_t>(kSelCand)
                                    ? reinterpret_cast<unsigned long long*>(stages + kMetaSegs * 8)
                                    : reinterpret_cast<unsigned long long*>(a.ws + a.L.cand) + size_t(b) * a.L.n_pad;
