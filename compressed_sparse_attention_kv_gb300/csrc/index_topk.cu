@@ -5,39 +5,50 @@
 // indexer heads; the selector keeps min(k, n) entries (section 5.3).
 //
 // GB300 design (HBM-bound: at 1M context the keys are 34.6 MB per query):
-//  1. index_prep_kernel   codes each request's queries (e4m3, one e8m0 scale per
-//     head) into the image of a 128-byte-swizzled shared-memory tile, folds the
-//     head scale into the head weight (ReLU(c x) = c ReLU(x) for c > 0) and
-//     clears the request's histogram, counters and the grid-barrier word.  It is
-//     a programmatic dependent of the kernel before it (the compressor that
-//     writes this step's key): the query coding overlaps that kernel.
-//  2. index_score_kernel  persistent and cooperative, one block per SM (all 512
-//     TMEM columns), warp-specialised:
-//       warps 0-1  two TMA producers, each with its own 4-stage ring (one
-//                  TMA-issuing thread per SM cannot keep enough copies in
-//                  flight): 64-row key pages by 3-D TMA (tensor map over the
-//                  page pool, 128-byte swizzle), their fp32 row scales by bulk
-//                  copies into a ring the epilogue releases.  Producer 0 also
-//                  schedules: it grabs chunks of four tiles from the requests'
-//                  work counters and hands every other tile to producer 1;
-//       warp 2     issues tcgen05 MMAs: M = 128 entries, N = heads, K = 128 in
-//                  four K = 32 e4m3 x e4m3 steps into one fp32 TMEM
-//                  accumulator (the key's single scale is applied afterwards),
-//                  eight accumulators in flight;
+//  1. index_prep_kernel   codes each request's queries into the image of the score
+//     kernel's shared-memory query tile (FP8 keys: e4m3 with one e8m0 scale per
+//     head, the scale folded into the head weight since ReLU(c x) = c ReLU(x) for
+//     c > 0; FP4 keys: rotated like the keys, then e2m1 with an e8m0 scale per 32;
+//     bf16: as they are), clears the request's histogram, counters, flags and queue
+//     slot, and puts what the score kernel reads first (context lengths, block-table
+//     rows) into L2.
+//  2. index_score_kernel  persistent, one block per SM (all 512 TMEM columns),
+//     warp-specialised:
+//       warp 11    the scheduler: takes chunks of four tiles from the requests' work
+//                  counters (the block's first chunk without an atomic, its page ids
+//                  requested before the set-up barrier) and writes one record per
+//                  tile - request, tile, two page ids - into an 8-record ring;
+//       warps 0-1  two TMA producers on alternate records, each with its own stage
+//                  ring (one TMA-issuing thread per SM cannot keep enough copies in
+//                  flight): 64-row key pages by 3-D TMA (tensor map over the page
+//                  pool, 128-byte swizzle; FP4: 64-byte), the pages' scales by bulk
+//                  copies, all L2 evict-first;
+//       warp 2     issues tcgen05 MMAs: M = 128 entries, N = heads, K = 128 (FP8:
+//                  four K = 32 e4m3 x e4m3 steps, the key's single scale applied
+//                  afterwards; FP4: two K = 64 block-scaled e2m1 steps with the
+//                  scale factors copied into TMEM; bf16: eight K = 16 steps) into
+//                  one fp32 TMEM accumulator, up to eight in flight;
 //       warps 3-10 two epilogue groups on alternate tiles: tcgen05.ld (one TMEM
-//                  lane = one entry), ReLU and the head weights, the heads
-//                  summed inside one thread, times the key's scale, the fp32
-//                  score written, its order-preserving key binned into the
-//                  group's 4,096-bin shared histogram (with 256 coarse bins of
-//                  16) and the largest key of each 32-entry segment kept.
-//     Then, behind one bounded grid barrier, every request's tiles are split
-//     over a run of blocks: each finds the threshold bin T (the bin holding the
-//     k-th score), reads again only the segments whose largest key reaches T,
-//     and writes the entries in bins >= T as 64-bit (score, ~index) keys in
-//     entry order; the block that finishes a request's last slice radix-selects
-//     the exact cut among the keys of bin T (12-bit digits, ties -> smaller
-//     index) and writes the k entries in entry order, so the output needs no
-//     sort.
+//                  lane = one entry), ReLU and the head weights, the heads summed
+//                  inside one thread, times the key's scale, the score written
+//                  (FP4: rounded to bf16), its order-preserving key binned into the
+//                  group's 4,096-bin shared histogram (with 256 coarse bins of 16)
+//                  and per 32-entry segment the largest key, its lane and the bin
+//                  of the runner-up kept.
+//     Streaming (batches of at most 64 requests of at most 262,144 entries): a group
+//     that leaves a request adds its tile count to the request's counter; the count
+//     that completes it queues the request, and a block done with its stream takes it
+//     from the queue: the threshold bin T (the bin holding the k-th score), the
+//     candidates (a segment with one key in a bin >= T gives it from the metadata,
+//     one with more has its scores read), the exact cut among the keys of bin T
+//     (ties -> smaller index), the k entries in entry order and the request's ready
+//     flag, on which the attention's tiles of that request start.
+//     LARGE (more or longer requests; a cooperative launch): behind one bounded grid
+//     barrier every request's tiles are split over a run of blocks: each finds T,
+//     reads again only the segments whose largest key reaches T and writes the
+//     entries in bins >= T as 64-bit (score, ~index) keys in entry order; the block
+//     that finishes a request's last slice radix-selects the cut among the keys of
+//     bin T and writes the k entries in entry order, so the output needs no sort.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
