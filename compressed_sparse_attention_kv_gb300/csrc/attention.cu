@@ -87,6 +87,7 @@ struct AttnArgs {
   // selection; list tiles wait for it (bounded by spin cycles) instead of for the
   // whole indexer grid.  nullptr: list tiles wait for the kernel before to complete.
   const uint32_t* ready;
+  int heads_per_block;         // 32 or 64 (the launch's choice, below)
   unsigned long long spin;
 };
 
@@ -255,13 +256,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* ktile = base;                                   // 8 chunks x 128 rows x 128 B = 128 KiB
   uint8_t* qtile = ktile + 8 * kKeys * 128;                // 8 chunks x Nq rows x 128 B <= 64 KiB
-  uint8_t* ptile = qtile + 40960;                          // reused after S: 128 keys x 128 B (1024-aligned)
+  uint8_t* ptile = qtile;                                  // reused after S: 128 keys x 128 B (1024-aligned)
   AttnSmem* sm = reinterpret_cast<AttnSmem*>(qtile + 8 * kMaxHeadsPerBlock * 128);
 
   const int b = blockIdx.y;
   const int tile = blockIdx.x;
-  const int h0 = blockIdx.z * kMaxHeadsPerBlock;
-  const int Hb = min(kMaxHeadsPerBlock, a.H - h0);
+  const int h0 = blockIdx.z * a.heads_per_block;
+  const int Hb = min(a.heads_per_block, a.H - h0);
   const int Nq = (Hb + 15) / 16 * 16;
   const int ctx = query_len(a, b);
   const int t = ctx - 1;
@@ -707,6 +708,13 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
   }
 }
 
+int num_sms() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
 // 16 KiB of slack keeps every descriptor-addressed read inside the allocation
 size_t attn_smem_bytes() { return 1024 + 8 * kKeys * 128 + 8 * kMaxHeadsPerBlock * 128 + sizeof(AttnSmem) + 16384; }
 
@@ -750,7 +758,13 @@ static cudaError_t launch_attn(const void* q, const cskv_paged& kv, const void* 
   a.spin = spin_limit();
   const size_t smem = attn_smem_bytes();
   cudaFuncSetAttribute(attn_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  dim3 grid(L.max_tiles, B, (H + kMaxHeadsPerBlock - 1) / kMaxHeadsPerBlock);
+  // A tile's heads in one block, or in blocks of 32 when the grid would otherwise leave
+  // most SMs idle (a decode batch of a few long requests): each block then repeats the
+  // tile's gather and dequantisation, but its products, softmax and partial are half as
+  // long, and the tile's latency is what the step waits for.
+  a.heads_per_block = (H > 32 && static_cast<long long>(L.max_tiles) * B * ((H + 31) / 32) <= num_sms())
+                          ? 32 : kMaxHeadsPerBlock;
+  dim3 grid(L.max_tiles, B, (H + a.heads_per_block - 1) / a.heads_per_block);
   // both kernels are programmatic dependents of the work before them in the stream
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
