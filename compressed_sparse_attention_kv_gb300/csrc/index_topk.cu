@@ -245,6 +245,18 @@ __global__ void __launch_bounds__(256) index_prep_kernel(const IndexArgs a) {
                   : make_uint2(0u, 0u);
     wv[i] = real ? a.w[size_t(b) * a.Hi + h] : 0.f;
   }
+  if (a.wait_fresh && warp == 0) {
+    // the first index key of request b that this step's compressor writes (none:
+    // INT_MAX); its loads overlap the queries'.  (A fused step waited above for the
+    // kernels before it, so the workspace word is free.)
+    int fr = 0x7FFFFFFF;
+    for (int j = 0; j < a.nfresh; ++j)
+      for (int q = lane; q < a.fresh_S[j]; q += 32)
+        if (a.fresh_req[j][q] == b) fr = min(fr, a.fresh_first[j][q]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) fr = min(fr, __shfl_xor_sync(0xFFFFFFFFu, fr, o));
+    if (lane == 0) reinterpret_cast<int32_t*>(a.ws + a.L.fresh)[b] = fr;
+  }
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int h = warp + 8 * i;
@@ -302,16 +314,6 @@ __global__ void __launch_bounds__(256) index_prep_kernel(const IndexArgs a) {
     reinterpret_cast<uint32_t*>(a.ws + a.L.ready)[b] = 0;
     reinterpret_cast<int32_t*>(a.ws + a.L.queue)[2 + b] = -1;
     if (b == 0) reinterpret_cast<uint32_t*>(a.ws + a.L.queue)[0] = reinterpret_cast<uint32_t*>(a.ws + a.L.queue)[1] = 0;
-  }
-  if (a.wait_fresh && warp == 0) {
-    // the first index key of request b that this step's compressor writes (none: INT_MAX)
-    int fr = 0x7FFFFFFF;
-    for (int j = 0; j < a.nfresh; ++j)
-      for (int q = lane; q < a.fresh_S[j]; q += 32)
-        if (a.fresh_req[j][q] == b) fr = min(fr, a.fresh_first[j][q]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) fr = min(fr, __shfl_xor_sync(0xFFFFFFFFu, fr, o));
-    if (lane == 0) reinterpret_cast<int32_t*>(a.ws + a.L.fresh)[b] = fr;
   }
 }
 
