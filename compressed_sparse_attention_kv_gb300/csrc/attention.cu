@@ -608,9 +608,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
 }
 
 // merge the tiles of (request, head) in tile order, sink, inverse RoPE, bf16.  DPT dims
-// per thread: 2 (one head per 256-thread block, for decode batches, where the block
-// count is small and each block's latency sets the time) or 8 (four heads per block,
-// 16-byte loads and stores, for launches with many queries, where the block count does)
+// per thread (launched with 8: four heads per 256-thread block, 16-byte loads and stores)
 template <int DPT>
 __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
   grid_dep_wait();   // the tile kernel's partials
@@ -780,11 +778,10 @@ static cudaError_t launch_attn(const void* q, const cskv_paged& kv, const void* 
   if (e != cudaSuccess) return e;
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
-  if (B <= 64) {   // decode batches: one head per block
-    cfg.gridDim = dim3(B, H);
-    return cudaLaunchKernelEx(&cfg, attn_combine_kernel<2>, a);
-  }
-  cfg.gridDim = dim3(B, (H + 3) / 4);   // many queries: four heads per block
+  // four heads per block: few enough blocks to be resident beside the tiles from the
+  // start (a decode step's 128 for 8 requests), so that they begin the moment the tiles'
+  // grid completes
+  cfg.gridDim = dim3(B, (H + 3) / 4);
   return cudaLaunchKernelEx(&cfg, attn_combine_kernel<8>, a);
 }
 
