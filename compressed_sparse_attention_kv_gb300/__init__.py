@@ -338,13 +338,17 @@ def decode_layer(jobs, q_idx, w, keys, q, main_kv, swa, swa_fmt, ctx_len, k, rat
     copied into d_in (device uint8, which the other tensors may view), then compress_many(jobs)
     (jobs may be empty), index_topk (skipped when q_idx is None: HCA) and sparse_decode_attn
     run, and out is copied into h_out (host, out's dtype and size or less) last.  Host
-    buffers should be pinned.  Returns (out, topk_idx); h_out holds the output once the
-    stream has synchronised."""
+    buffers should be pinned; q may be a pinned host tensor (read in place by the
+    attention).  Returns (out, topk_idx); h_out holds the output once the stream has
+    synchronised."""
     import torch
-    for t, dt, n in ((q_idx, torch.bfloat16, "q_idx"), (w, torch.float32, "w"), (q, torch.bfloat16, "q"),
+    for t, dt, n in ((q_idx, torch.bfloat16, "q_idx"), (w, torch.float32, "w"),
                      (swa, torch.uint8, "swa"), (ctx_len, torch.int32, "ctx_len"), (sink, torch.float32, "sink"),
                      (q_rope_cs, torch.float32, "q_rope_cs"), (d_in, torch.uint8, "d_in")):
         _need(t, dt, n)
+    _need(q, torch.bfloat16, "q", device=False)
+    if not q.is_cuda and not q.is_pinned():
+        raise ValueError("q must be a CUDA tensor or a pinned host tensor")
     _need(h_in, torch.uint8, "h_in", device=False)
     _need(h_out, None, "h_out", device=False)
     for t, n in ((h_in, "h_in"), (h_out, "h_out")):
@@ -353,11 +357,11 @@ def decode_layer(jobs, q_idx, w, keys, q, main_kv, swa, swa_fmt, ctx_len, k, rat
     if h_in is not None and (d_in is None or d_in.numel() < h_in.numel()):
         raise ValueError("d_in must be a device buffer at least as large as h_in")
     B, H, _ = q.shape
-    dev = q.device
+    dev = ctx_len.device
     csa = q_idx is not None
     Hi = q_idx.shape[1] if csa else 0
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(q.shape, dtype=q.dtype, device=dev)
     if csa and topk_idx is None:
         topk_idx = torch.empty((B, k), dtype=torch.int32, device=dev)
     if csa and index_workspace is None:

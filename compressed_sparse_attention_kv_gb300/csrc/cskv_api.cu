@@ -488,10 +488,12 @@ int32_t cskv_decode_layer(const cskv_decode_layer_args* args, void* stream) {
     return CSKV_ERR_CUDA;
   }
   const int32_t kk = csa ? a.k : 0;
-  // a whole page-locked output buffer is written by the combine kernel itself, beside out
+  // a whole page-locked output buffer is written by the combine kernel itself, beside out;
+  // page-locked host queries are read in place through their device alias
   void* out_alias = nullptr;
   if (a.out_bytes > 0 && a.out_bytes == size_t(a.B) * a.H * 512 * 2) out_alias = host_alias(a.h_out);
-  if (launch_sparse_decode_attn(a.q, a.main_kv, a.swa, a.swa_fmt, a.ctx_len, csa ? a.topk_idx : nullptr, kk,
+  const void* q_alias = host_alias(a.q);
+  if (launch_sparse_decode_attn(q_alias != nullptr ? q_alias : a.q, a.main_kv, a.swa, a.swa_fmt, a.ctx_len, csa ? a.topk_idx : nullptr, kk,
                                 a.ratio, a.max_ctx_len, a.sink, a.softmax_scale, a.q_rope_cs, a.B, a.H, a.out,
                                 a.attn_workspace, st, out_alias, ready) != cudaSuccess)
     return CSKV_ERR_CUDA;

@@ -443,7 +443,9 @@ CSKV_API int32_t cskv_sparse_prefill_attn(const void* q, cskv_paged main_kv, csk
  * device alias, and a page-locked h_out of the whole output's size is written
  * by the attention's last kernel itself, beside `out`; any other host memory
  * goes through cudaMemcpyAsync (synchronous for pageable memory, and not
- * capturable into a CUDA graph).
+ * capturable into a CUDA graph).  `q` alone may also be page-locked host memory
+ * outside h_in: the attention reads it in place through its device alias, before
+ * it waits for its selection (so the transfer is off the step's critical path).
  * Ownership: every buffer is the caller's; h_in must hold in_bytes bytes, d_in at
  * least as many, h_out out_bytes.  The call returns once everything is enqueued;
  * h_out holds the output after the stream has synchronised.
@@ -463,7 +465,7 @@ typedef struct {
   int32_t* topk_idx;             /* int32 [B, k] device, the selection (written) */
   void* index_workspace;
   size_t index_workspace_bytes;
-  const void* q;                 /* bf16 [B, H, 512] */
+  const void* q;                 /* bf16 [B, H, 512] device, or page-locked host memory */
   cskv_paged main_kv;
   const void* swa;               /* [B, 128, row_bytes(swa_fmt, 512)] window ring */
   int32_t swa_fmt;

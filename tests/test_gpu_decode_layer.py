@@ -114,6 +114,18 @@ def test_csa_layer_step_host_to_host(main_fmt, key_fmt):
     torch.cuda.synchronize()
     assert cskv.device_status() == 0
     assert torch.equal(h_out, out.cpu())
+    # the same step with the attention queries left in pinned host memory (read in place
+    # by the attention): the same selection and the same output bits (the step's
+    # compressor writes the same entries again)
+    q_pin = q_t.clone().pin_memory()
+    h_out2 = torch.empty((B, H, 512), dtype=torch.bfloat16, pin_memory=True)
+    _, topk2 = cskv.decode_layer(jobs, v["q_idx"], v["w"], dev_idx, q_pin, dev_main, cuda(swa_b), codecs.FMT_FP8,
+                                 v["ctx"], k, ratio, max_ctx, cuda(sink), SCALE, v["qcs"],
+                                 h_in=h_in, d_in=d_in, h_out=h_out2)
+    torch.cuda.synchronize()
+    assert cskv.device_status() == 0
+    assert torch.equal(topk2, topk)
+    assert torch.equal(h_out2, h_out)
     # the caches now hold the oracle's entries, bit for bit
     for b in range(B):
         main_vals[b][n[b] - 1] = _oracle_entry(blk_m, b, ratio, n[b] - 1)
