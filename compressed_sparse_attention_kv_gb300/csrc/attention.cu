@@ -13,8 +13,8 @@
 // entries.  Prefill runs every query as its own list ("DeepSeek-V4 deep dive",
 // section 5.3: the buffer [all raw rows of the prompt ; its compressed entries],
 // the window indices t-127 .. t masked below 0); req_of maps a query to its
-// request.  One block
-// handles one (request, tile, head group of <= 64 heads):
+// request.  One block handles one (request, tile, head group: 64 heads, or 32 when
+// the grid would otherwise leave most SMs idle):
 //   * the query is copied into shared memory and its last 64 dims rotated (fp32) in
 //     place, and a list tile's block-table row staged beside it, before the tile
 //     waits for its selection; then the tile's rows (528 B FP8, 288 B FP4 or 1 KiB
@@ -23,8 +23,9 @@
 //     swizzle;
 //   * one thread issues tcgen05 MMAs S^T = K Q^T (M = 128 keys, N = heads,
 //     K = 512) into TMEM - keys are the MMA rows, so 16..64 heads need no padding;
-//   * softmax statistics per head (max, sum of exp2) over the tile, P^T stored
-//     as the bf16 MN-major B operand;
+//   * softmax statistics per head (max, sum of exp2) over the tile, straight from
+//     TMEM by a transposing butterfly per warp, P^T stored as the bf16 MN-major B
+//     operand;
 //   * O^T = V^T P^T (M = 128 dims x 4 blocks, N = heads, K = 128 keys): the same
 //     smem tile is read a second time as the MN-major A operand (K = V);
 //   * the partial (m, l, O) goes to the workspace.
