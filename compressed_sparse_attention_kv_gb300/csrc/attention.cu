@@ -28,7 +28,9 @@
 //     operand;
 //   * O^T = V^T P^T (M = 128 dims x 4 blocks, N = heads, K = 128 keys): the same
 //     smem tile is read a second time as the MN-major A operand (K = V);
-//   * the partial (m, l, O) goes to the workspace.
+//   * the partial goes to the workspace: the head's (m, l) in fp32 and O / l in bf16
+//     (a convex combination of the tile's values, so it has their range; half the
+//     bytes of fp32 to write here and to read back in the merge).
 // attn_combine_kernel merges the partials of a request in a fixed order with
 // the sink, applies the inverse rotation and writes bf16.
 #include <type_traits>
@@ -58,7 +60,7 @@ __host__ __device__ inline AttnLayout attn_layout(int B, int H, int max_ctx, int
   const int comp = k > 0 ? k : (ratio > 0 ? max_ctx / ratio : 0);
   L.max_tiles = 1 + (comp + kKeys - 1) / kKeys;
   size_t o = 0;
-  L.opart = o; o = a256(o + size_t(B) * L.max_tiles * H * kD * 4);
+  L.opart = o; o = a256(o + size_t(B) * L.max_tiles * H * kD * 2);
   L.ml = o;    o = a256(o + size_t(B) * L.max_tiles * H * 2 * 4);
   L.total = o;
   return L;
@@ -80,8 +82,8 @@ struct AttnArgs {
   const float* q_rope;
   int B, H;
   uint8_t* out;
-  float* opart;
-  float* ml;
+  __nv_bfloat16* opart;   // per (request, tile, head): O / l, bf16
+  float* ml;              // per (request, tile, head): m (base 2) and l, fp32
   int max_tiles;
   uint8_t* out_host;           // optional second copy of out (a host buffer's device alias), or nullptr
   // Fused decode step: ready[b] turns 1 once the indexer has written request b's
@@ -179,6 +181,7 @@ struct AttnSmem {
   uint32_t tmem_base;
   __align__(16) float mpart[4][kMaxHeadsPerBlock];   // per lane quarter: the largest logit of each head
   float lpart[4][kMaxHeadsPerBlock];                 // per lane quarter: the sum of exp2 of each head
+  __align__(16) float linv[kMaxHeadsPerBlock];       // 1 / l of each head over the tile (0: no key)
   const uint8_t* rowp[kKeys];   // address of each key row of the tile, null = no key
   __align__(16) uint8_t scl[kKeys][32];   // staged scale bytes of each row (FP8: 16, FP4: 32)
 };
@@ -565,12 +568,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
     for (int ks = 0; ks < 8; ++ks) mma_f16(tmem + 128 + mb * Nq, dv + ks * 128, dp + ks * 128, id, ks > 0);
     mma_commit(&sm->bar_o);
   }
+  // the heads' statistics over the tile (lane quarters in order) while the product runs
+  const size_t slot = (size_t(b) * a.max_tiles + tile) * a.H + h0;
+  if (threadIdx.x < Hb) {
+    const int h = threadIdx.x;
+    const float m = fmaxf(fmaxf(sm->mpart[0][h], sm->mpart[1][h]), fmaxf(sm->mpart[2][h], sm->mpart[3][h]));
+    const float l = ((sm->lpart[0][h] + sm->lpart[1][h]) + sm->lpart[2][h]) + sm->lpart[3][h];
+    a.ml[(slot + h) * 2 + 0] = m;
+    a.ml[(slot + h) * 2 + 1] = l;
+    sm->linv[h] = l > 0.f ? 1.0f / l : 0.f;
+  }
+  __syncthreads();
   mbar_wait(&sm->bar_o, 0, kDefaultSpinLimit);
   tc_fence_after();
 
   // ---- partial out: O^T lanes = dims; warps 4m .. 4m+3 block m of 128 dims
   {
-    const size_t slot = (size_t(b) * a.max_tiles + tile) * a.H + h0;
     const int sub = warp & 3;
     {
       const int mb = warp >> 2;
@@ -583,18 +596,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tile_kernel(const AttnAr
           tmem_ld16(tmem + (static_cast<uint32_t>(sub * 32) << 16) + 128 + mb * Nq + c0,
                     *reinterpret_cast<float(*)[16]>(o + c0));
       tmem_wait_ld();
-      // straight out: for each head the warp's 32 dims are one 128-byte line
+      // straight out: for each head the warp's 32 dims are one 64-byte run
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        if (i < Hb) a.opart[(slot + i) * kD + d] = o[i];
+      for (int c0 = 0; c0 < 64; c0 += 4) {
+        if (c0 < Hb) {
+          const float4 r = *reinterpret_cast<const float4*>(&sm->linv[c0]);
+          const float rv[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+          for (int i = c0; i < c0 + 4; ++i)
+            if (i < Hb) a.opart[(slot + i) * kD + d] = __float2bfloat16_rn(o[i] * rv[i - c0]);
+        }
       }
-    }
-    if (threadIdx.x < Hb) {   // the head's statistics over the tile: lane quarters in order
-      const int h = threadIdx.x;
-      const float m = fmaxf(fmaxf(sm->mpart[0][h], sm->mpart[1][h]), fmaxf(sm->mpart[2][h], sm->mpart[3][h]));
-      const float l = ((sm->lpart[0][h] + sm->lpart[1][h]) + sm->lpart[2][h]) + sm->lpart[3][h];
-      a.ml[(slot + h) * 2 + 0] = m;
-      a.ml[(slot + h) * 2 + 1] = l;
     }
   }
   tc_fence_before();
@@ -624,7 +636,8 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
   const size_t slot0 = size_t(b) * a.max_tiles * a.H + h;
   const int d = DPT * (static_cast<int>(threadIdx.x) % kThreadsPerHead);
   // running (max, sum, output) in base 2, started from the sink; tiles taken in
-  // batches of 8 whose loads are all issued before any is used
+  // batches of 8 whose loads are all issued before any is used.  A tile's partial is
+  // O / l: it enters with weight exp2(m - M) * l.
   float M = a.sink ? a.sink[h] * 1.4426950408889634f : -INFINITY;
   float L = a.sink ? 1.f : 0.f;
   float o[DPT];
@@ -639,22 +652,23 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
       const bool in = s0 + u < ntiles;
       m[u] = in ? a.ml[sl * 2] : -INFINITY;
       l[u] = in ? a.ml[sl * 2 + 1] : 0.f;
-      if constexpr (DPT % 4 == 0) {
+      if constexpr (DPT % 8 == 0) {
 #pragma unroll
-        for (int i = 0; i < DPT; i += 4) {
-          const float4 x = in ? *reinterpret_cast<const float4*>(a.opart + sl * kD + d + i)
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
-          v[u][i] = x.x;
-          v[u][i + 1] = x.y;
-          v[u][i + 2] = x.z;
-          v[u][i + 3] = x.w;
+        for (int i = 0; i < DPT; i += 8) {
+          const uint4 x = in ? *reinterpret_cast<const uint4*>(a.opart + sl * kD + d + i) : make_uint4(0, 0, 0, 0);
+          const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            v[u][i + 2 * j] = bf16lo(w[j]);
+            v[u][i + 2 * j + 1] = bf16hi(w[j]);
+          }
         }
       } else {
 #pragma unroll
         for (int i = 0; i < DPT; i += 2) {
-          const float2 x = in ? *reinterpret_cast<const float2*>(a.opart + sl * kD + d + i) : make_float2(0.f, 0.f);
-          v[u][i] = x.x;
-          v[u][i + 1] = x.y;
+          const uint32_t x = in ? *reinterpret_cast<const uint32_t*>(a.opart + sl * kD + d + i) : 0u;
+          v[u][i] = bf16lo(x);
+          v[u][i + 1] = bf16hi(x);
         }
       }
     }
@@ -669,8 +683,8 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       if (m[u] == -INFINITY) continue;
-      const float g = exp2f(m[u] - Mb);
-      L += g * l[u];
+      const float g = exp2f(m[u] - Mb) * l[u];
+      L += g;
 #pragma unroll
       for (int i = 0; i < DPT; ++i) o[i] += g * v[u][i];
     }
@@ -749,7 +763,7 @@ static cudaError_t launch_attn(const void* q, const cskv_paged& kv, const void* 
   a.B = B;
   a.H = H;
   a.out = static_cast<uint8_t*>(out);
-  a.opart = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + L.opart);
+  a.opart = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(workspace) + L.opart);
   a.ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + L.ml);
   a.max_tiles = L.max_tiles;
   a.out_host = static_cast<uint8_t*>(out_host);

@@ -377,7 +377,9 @@ CSKV_API int32_t cskv_index_topk_noalloc(const void* q_idx, const float* w, cskv
  * BF16.  sink: fp32 [H] or NULL (no sink).  q_rope_cs: fp32 [B, 32, 2] (cos,
  * sin) of each query position.  out: bf16 [B, H, 512] device.  H in [1, 128].
  * Dequantised keys and values are exact in bf16; products run as tcgen05
- * bf16 MMAs with fp32 accumulation; the query is rounded to bf16 after RoPE.
+ * bf16 MMAs with fp32 accumulation; the query is rounded to bf16 after RoPE;
+ * each 128-key tile's partial output is kept as O / l in bf16 (with its fp32
+ * max and sum) until the tiles are merged in fp32.
  * workspace: >= cskv_sparse_decode_attn_workspace_size(...) bytes, 256-byte
  * aligned, no initialisation needed.
  * ------------------------------------------------------------------------ */

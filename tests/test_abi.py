@@ -55,7 +55,8 @@ def test_workspace_sizes(lib):
     assert 0 < small < big
     # scores + candidates dominate: 12 bytes per visible entry
     assert big >= 8 * (1 << 18) * 12
-    assert lib.cskv_sparse_decode_attn_workspace_size(8, 64, 1 << 20, 4, 512) >= 8 * 5 * 64 * 512 * 4
+    # bf16 partials (O / l) of every (request, tile, head) plus fp32 (m, l)
+    assert lib.cskv_sparse_decode_attn_workspace_size(8, 64, 1 << 20, 4, 512) >= 8 * 5 * 64 * (512 * 2 + 8)
     assert lib.cskv_index_topk_workspace_size(0, 10, 4, 4, 4) == 0
 
 
