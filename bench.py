@@ -210,22 +210,25 @@ def run_gpu(args, rank, world, workload=WORKLOAD):
     # ---- static device buffers (graph-capture safe) and pinned host copies of the step inputs
     bf = torch.bfloat16
     host = {
-        "q_idx": torch.from_numpy(inp["q_idx"]).to(bf),
-        "w": torch.from_numpy(inp["w"]), "kv": torch.from_numpy(inp["kv"]).to(bf),
+        "q_idx": torch.from_numpy(inp["q_idx"]).to(bf), "w": torch.from_numpy(inp["w"]),
+        "qcs": torch.from_numpy(cskv.rope_table(wl.ctx_len - 1)),
+        "ctx": torch.from_numpy(wl.ctx_len.astype(np.int32)),
+        "first": torch.from_numpy((n_b - 1).astype(np.int32)),
+        "q": torch.from_numpy(inp["q"]).to(bf),
+        # from here on the compressor's per-step inputs, which the end-to-end leg leaves in place
+        "kv": torch.from_numpy(inp["kv"]).to(bf),
         "gate": torch.from_numpy(inp["gate"]).to(bf), "pkv": torch.from_numpy(inp["pkv"]).to(bf),
         "pgate": torch.from_numpy(inp["pgate"]).to(bf), "ikv": torch.from_numpy(inp["ikv"]).to(bf),
         "igate": torch.from_numpy(inp["igate"]).to(bf), "ipkv": torch.from_numpy(inp["ipkv"]).to(bf),
         "ipgate": torch.from_numpy(inp["ipgate"]).to(bf),
         "ecs": torch.from_numpy(cskv.rope_table(((n_b - 1) * r)[:, None])),
-        "qcs": torch.from_numpy(cskv.rope_table(wl.ctx_len - 1)),
-        "ctx": torch.from_numpy(wl.ctx_len.astype(np.int32)),
-        "first": torch.from_numpy((n_b - 1).astype(np.int32)),
-        "q": torch.from_numpy(inp["q"]).to(bf),   # last: the end-to-end leg copies the rest
     }
     # the step's inputs live in one pinned host buffer and one device buffer (views at
-    # 256-byte offsets), so that the end-to-end leg moves them with a single copy; the
-    # attention queries, last in the buffer, it leaves in place (read by the attention
-    # from pinned memory, before each tile waits for its selection)
+    # 256-byte offsets), so that the end-to-end leg moves them with a single copy of a
+    # prefix; what follows the prefix it leaves in place: the compressor's inputs (read
+    # by the compressor, which runs beside the score kernel) and, when the batch's
+    # attention tiles all fit on the GPU, the attention queries (read before each tile
+    # waits for its selection)
     offs, tot = {}, 0
     for kk, v in host.items():
         offs[kk] = tot
@@ -350,11 +353,16 @@ def run_gpu(args, rank, world, workload=WORKLOAD):
     # queries are copied in with the rest.
     tiles = 1 + (k + 127) // 128
     q_in_place = B * tiles * ((wl.H + 31) // 32) <= torch.cuda.get_device_properties(dev).multi_processor_count
-    h_in = host_buf[:offs["q"]] if q_in_place else host_buf
+    h_in = host_buf[:offs["q"]] if q_in_place else host_buf[:offs["kv"]]
     q_arg = view(host_buf, "q", host["q"]) if q_in_place else d["q"]
+    hv = {kk: view(host_buf, kk, host[kk]) for kk in ("kv", "gate", "pkv", "pgate", "ikv", "igate", "ipkv", "ipgate",
+                                                      "ecs")}
+    jobs_e2e = [dict(jobs[0], kv=hv["kv"], gate=hv["gate"], prev_kv=hv["pkv"], prev_gate=hv["pgate"], rope_cs=hv["ecs"]),
+                dict(jobs[1], kv=hv["ikv"], gate=hv["igate"], prev_kv=hv["ipkv"], prev_gate=hv["ipgate"],
+                     rope_cs=hv["ecs"])]
 
     def layer_call():
-        cskv.decode_layer(jobs, d["q_idx"], d["w"], keys, q_arg, main, swa, wl.swa_fmt, d["ctx"], k, r, L, sink,
+        cskv.decode_layer(jobs_e2e, d["q_idx"], d["w"], keys, q_arg, main, swa, wl.swa_fmt, d["ctx"], k, r, L, sink,
                           cskv.DEFAULT_SCALE, d["qcs"], topk_idx=topk, out=out, index_workspace=ws_i,
                           attn_workspace=ws_a, h_in=h_in, d_in=dev_buf, h_out=out_host)
 
@@ -431,8 +439,8 @@ def run_gpu(args, rank, world, workload=WORKLOAD):
         "kv_read_gbs": path_bytes / (mean_ms * 1e-3) / 1e9,
         "step_frac_of_hbm_roofline": (path_bytes / (peak * 1e9)) / (mean_ms * 1e-3),
         "e2e": {"value": job_throughput(world, B, e2e_mean), "unit": "queries/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "call": "cskv_decode_layer (pinned host buffers in and out%s)" % (
-                    "; the attention queries read in place from pinned memory" if q_in_place else ""),
+                "d2h_bytes_per_step": d2h, "call": "cskv_decode_layer (pinned host buffers in and out; the compressor's "
+                "inputs%s read in place from pinned memory)" % (" and the attention queries" if q_in_place else ""),
                 "ms_per_step": e2e_mean},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,

@@ -187,15 +187,24 @@ def compress_many(jobs, stream=None):
     _check(st, "cskv_compress_many")
 
 
-def _compress_jobs(jobs):
-    """ctypes array of struct cskv_compress_job for compress()-style job dicts."""
+def _compress_jobs(jobs, host_inputs=False):
+    """ctypes array of struct cskv_compress_job for compress()-style job dicts.  With
+    host_inputs (decode_layer), kv, gate, prev_kv, prev_gate and rope_cs may be pinned
+    host tensors (read in place by the compressor)."""
     import torch
+
+    def need_in(t, dtype, name):
+        _need(t, dtype, name, device=not host_inputs)
+        if t is not None and not t.is_cuda and not t.is_pinned():
+            raise ValueError("%s must be a CUDA tensor or a pinned host tensor" % name)
+
     arr = (_lib.CompressJob * max(1, len(jobs)))()
     for i, j in enumerate(jobs):
         kv, gate = j["kv"], j["gate"]
         for t, n in ((kv, "kv"), (gate, "gate"), (j.get("prev_kv"), "prev_kv"), (j.get("prev_gate"), "prev_gate")):
-            _need(t, torch.bfloat16, n)
-        for t, n in ((j.get("ape"), "ape"), (j.get("norm_w"), "norm_w"), (j.get("rope_cs"), "rope_cs")):
+            need_in(t, torch.bfloat16, n)
+        need_in(j.get("rope_cs"), torch.float32, "rope_cs")
+        for t, n in ((j.get("ape"), "ape"), (j.get("norm_w"), "norm_w")):
             _need(t, torch.float32, n)
         _need(j["req"], torch.int32, "req")
         _need(j["first_entry"], torch.int32, "first_entry")
@@ -338,8 +347,9 @@ def decode_layer(jobs, q_idx, w, keys, q, main_kv, swa, swa_fmt, ctx_len, k, rat
     copied into d_in (device uint8, which the other tensors may view), then compress_many(jobs)
     (jobs may be empty), index_topk (skipped when q_idx is None: HCA) and sparse_decode_attn
     run, and out is copied into h_out (host, out's dtype and size or less) last.  Host
-    buffers should be pinned; q may be a pinned host tensor (read in place by the
-    attention).  Returns (out, topk_idx); h_out holds the output once the stream has
+    buffers should be pinned; q, and the jobs' kv, gate, prev_kv, prev_gate and
+    rope_cs, may be pinned host tensors (read in place by the attention and the
+    compressor).  Returns (out, topk_idx); h_out holds the output once the stream has
     synchronised."""
     import torch
     for t, dt, n in ((q_idx, torch.bfloat16, "q_idx"), (w, torch.float32, "w"),
@@ -371,7 +381,7 @@ def decode_layer(jobs, q_idx, w, keys, q, main_kv, swa, swa_fmt, ctx_len, k, rat
     if attn_workspace is None:
         attn_workspace = torch.empty(sparse_decode_attn_workspace_size(B, H, max_ctx_len, ratio, kk),
                                      dtype=torch.uint8, device=dev)
-    arr = _compress_jobs(jobs)
+    arr = _compress_jobs(jobs, host_inputs=True)
     empty = _lib.Paged(None, None, 0, 0, 0, 0, 128)
     a = _lib.DecodeLayerArgs(
         ctypes.cast(arr, ctypes.POINTER(_lib.CompressJob)) if jobs else None, len(jobs), _ptr(q_idx), _ptr(w), keys.desc() if csa else empty, Hi, kk,

@@ -475,6 +475,22 @@ int32_t cskv_decode_layer(const cskv_decode_layer_args* args, void* stream) {
   if (a.in_bytes > 0 && (a.h_in == nullptr || a.d_in == nullptr)) return CSKV_ERR_INVALID;
   if (a.out_bytes > 0 && (a.h_out == nullptr || a.out_bytes > size_t(a.B) * a.H * 512 * 2)) return CSKV_ERR_INVALID;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // a job's per-step inputs (kv, gate, prev_*, rope_cs) in page-locked host memory are
+  // read in place by the compressor through their device alias: it runs beside the
+  // score kernel, whose tiles wait for it only at the step's newest entries
+  cskv_compress_job jobs[4];
+  for (int32_t j = 0; j < a.njobs; ++j) {
+    jobs[j] = a.jobs[j];
+    auto in_place = [](const void* p) -> const void* {
+      const void* al = p != nullptr ? host_alias(p) : nullptr;
+      return al != nullptr ? al : p;
+    };
+    jobs[j].kv = in_place(jobs[j].kv);
+    jobs[j].gate = in_place(jobs[j].gate);
+    jobs[j].prev_kv = in_place(jobs[j].prev_kv);
+    jobs[j].prev_gate = in_place(jobs[j].prev_gate);
+    jobs[j].rope_cs = static_cast<const float*>(in_place(jobs[j].rope_cs));
+  }
   if (a.in_bytes > 0 && stage_copy(a.d_in, a.h_in, a.in_bytes, true, st) != cudaSuccess) return CSKV_ERR_CUDA;
   // CSA: the indexer's prep, the compressor and the score kernel overlap (the score kernel
   // waits for the compressor only before the tiles holding the index keys it writes),
@@ -482,9 +498,9 @@ int32_t cskv_decode_layer(const cskv_decode_layer_args* args, void* stream) {
   const uint32_t* ready = nullptr;
   if (csa) {
     if (launch_index_topk_fused(a.q_idx, a.w, a.keys, a.ctx_len, a.B, a.Hi, a.ratio, a.k, a.max_ctx_len,
-                                a.topk_idx, nullptr, a.index_workspace, a.jobs, a.njobs, st, &ready) != cudaSuccess)
+                                a.topk_idx, nullptr, a.index_workspace, jobs, a.njobs, st, &ready) != cudaSuccess)
       return CSKV_ERR_CUDA;
-  } else if (a.njobs > 0 && launch_compress_many(a.jobs, a.njobs, st) != cudaSuccess) {
+  } else if (a.njobs > 0 && launch_compress_many(jobs, a.njobs, st) != cudaSuccess) {
     return CSKV_ERR_CUDA;
   }
   const int32_t kk = csa ? a.k : 0;

@@ -445,9 +445,13 @@ CSKV_API int32_t cskv_sparse_prefill_attn(const void* q, cskv_paged main_kv, csk
  * device alias, and a page-locked h_out of the whole output's size is written
  * by the attention's last kernel itself, beside `out`; any other host memory
  * goes through cudaMemcpyAsync (synchronous for pageable memory, and not
- * capturable into a CUDA graph).  `q` alone may also be page-locked host memory
- * outside h_in: the attention reads it in place through its device alias, before
- * it waits for its selection (so the transfer is off the step's critical path).
+ * capturable into a CUDA graph).  Two kinds of input may also be page-locked
+ * host memory outside h_in, read in place through their device alias, so that
+ * their transfer is off the step's critical path: `q`, which the attention reads
+ * before it waits for its selection, and a job's kv, gate, prev_kv, prev_gate and
+ * rope_cs, which the compressor reads while the score kernel streams the older
+ * keys (its other arrays, and every other pointer of steps 2-4, are device
+ * memory).
  * Ownership: every buffer is the caller's; h_in must hold in_bytes bytes, d_in at
  * least as many, h_out out_bytes.  The call returns once everything is enqueued;
  * h_out holds the output after the stream has synchronised.

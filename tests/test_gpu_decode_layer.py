@@ -108,18 +108,25 @@ def test_csa_layer_step_host_to_host(main_fmt, key_fmt):
                  req=v["req"], first_entry=v["first"], prev_kv=v["ipkv"], prev_gate=v["ipgate"],
                  norm_w=cuda(blk_i["nw"]), rope_cs=v["ecs"])]
     h_out = torch.empty((B, H, 512), dtype=torch.bfloat16, pin_memory=True)
+    pools0 = dev_main.pool.clone(), dev_idx.pool.clone()   # before the step writes its entries
     out, topk = cskv.decode_layer(jobs, v["q_idx"], v["w"], dev_idx, v["q"], dev_main, cuda(swa_b), codecs.FMT_FP8,
                                   v["ctx"], k, ratio, max_ctx, cuda(sink), SCALE, v["qcs"],
                                   h_in=h_in, d_in=d_in, h_out=h_out)
     torch.cuda.synchronize()
     assert cskv.device_status() == 0
     assert torch.equal(h_out, out.cpu())
-    # the same step with the attention queries left in pinned host memory (read in place
-    # by the attention): the same selection and the same output bits (the step's
-    # compressor writes the same entries again)
+    # the same step with the attention queries and the compressor's per-step inputs left
+    # in pinned host memory (read in place): the same selection and the same output bits
+    # (the step's compressor writes the same entries again; the caches are checked below)
     q_pin = q_t.clone().pin_memory()
+    pin = {kk: v[kk].cpu().pin_memory() for kk in ("kv", "gate", "pkv", "pgate", "ikv", "igate", "ipkv", "ipgate",
+                                                    "ecs")}
+    jobs_pin = [dict(j, kv=pin[a], gate=pin[g], prev_kv=pin[pa], prev_gate=pin[pg], rope_cs=pin["ecs"])
+                for j, (a, g, pa, pg) in zip(jobs, (("kv", "gate", "pkv", "pgate"), ("ikv", "igate", "ipkv", "ipgate")))]
     h_out2 = torch.empty((B, H, 512), dtype=torch.bfloat16, pin_memory=True)
-    _, topk2 = cskv.decode_layer(jobs, v["q_idx"], v["w"], dev_idx, q_pin, dev_main, cuda(swa_b), codecs.FMT_FP8,
+    dev_main.pool.copy_(pools0[0])   # the step's entries must be written again
+    dev_idx.pool.copy_(pools0[1])
+    _, topk2 = cskv.decode_layer(jobs_pin, v["q_idx"], v["w"], dev_idx, q_pin, dev_main, cuda(swa_b), codecs.FMT_FP8,
                                  v["ctx"], k, ratio, max_ctx, cuda(sink), SCALE, v["qcs"],
                                  h_in=h_in, d_in=d_in, h_out=h_out2)
     torch.cuda.synchronize()
