@@ -454,7 +454,9 @@ CSKV_API int32_t cskv_sparse_prefill_attn(const void* q, cskv_paged main_kv, csk
  * memory).
  * Ownership: every buffer is the caller's; h_in must hold in_bytes bytes, d_in at
  * least as many, h_out out_bytes.  The call returns once everything is enqueued;
- * h_out holds the output after the stream has synchronised.
+ * h_out holds the output after the stream has synchronised.  Host memory that the
+ * kernels read in place (q, the jobs' per-step inputs) and h_in must stay unchanged
+ * until then: a CUDA graph that captured the call reads them again at every replay.
  * Errors: the arguments of every stage are checked before anything is
  * enqueued (CSKV_ERR_INVALID / CSKV_ERR_UNSUPPORTED as the stage's own entry
  * point would return, and CSKV_ERR_INVALID for a NULL h_in / d_in / h_out with
